@@ -1,0 +1,466 @@
+/*
+ * dflash_oracle.c -- plain, slow CPU oracle for one DFlash draft-and-verify cycle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file; only the test suite, the smoke check and the bench's CPU-baseline
+ * leg use it.  It shares no code, header, table or constant with the CUDA
+ * library: every formula below is written out again from the method's
+ * description.
+ *
+ * Sources (web pages on DFlash; cited by page title and section):
+ *  [G]  "DFlash: block-diffusion accelerated LLM speculative decoding" guide
+ *       (txtmix.com), section 3.1 "one forward pass yields the whole block",
+ *       section 3.2 "draft conditioned on target features", section 3.3
+ *       "verification is still done by the target", section 4 "how one task
+ *       flows through the system", section 7 "DFlash 2" (path selector),
+ *       FAQ Q2 (where the context features come from).
+ *  [N]  "DFlash 2 release: parallel drafts keep lowering LLM inference
+ *       latency" (openai-hub.com news), sections "the core of DFlash 2: write
+ *       one block at a time" (prefix-acceptance example) and "KV injection".
+ *  [T]  "DFlash: diffusion draft models push speculative decoding ..."
+ *       (llmapis.com), "data and technical details" (draft sliding window).
+ *
+ * Arithmetic model.  Accumulation and activations are held in double.  In
+ * bf16 mode every value is rounded to bfloat16 (round-to-nearest-even, via
+ * float) at the tensor boundaries where the GPU path stores bf16: the inputs
+ * of every projection (post-RMSNorm activations, attention output, SiLU*up
+ * product, fused context feature c_t, tap features), the query, and the K/V
+ * cache entries.  The residual stream, softmax and logits are not rounded,
+ * except that the argmax is taken over logits rounded to float, the
+ * precision in which the GPU takes that decision.  In fp32 mode nothing is
+ * rounded.  Weights are read as bf16 (uint16 bit patterns) or float.
+ *
+ * Compile with -ffp-contract=off so that x86 and Arm builds agree.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_CAUSAL 0
+#define OR_BIDIR 1
+
+typedef struct {
+  int H;        /* hidden size */
+  int nq;       /* query heads */
+  int nkv;      /* key/value heads (GQA groups) */
+  int d;        /* head dim */
+  int I;        /* SwiGLU intermediate size */
+  int bf16;     /* 1: bf16 weights + bf16 rounding points; 0: fp32 weights, no rounding */
+  double theta; /* RoPE base */
+  double eps;   /* RMSNorm epsilon */
+} or_cfg;
+
+typedef struct {
+  const void *wq, *wk, *wv, *wo; /* [out][in] row-major */
+  const void *wg, *wu, *wd;      /* gate [I][H], up [I][H], down [H][I] */
+  const void *g1, *g2;           /* RMSNorm gains [H] before attention / before MLP */
+} or_layer;
+
+/* ---------------------------------------------------------------- scalars */
+
+/* float -> bfloat16 -> float, round to nearest even; NaN stays NaN. */
+double or_bf16_round(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) {
+    u |= 0x00400000u; /* quiet NaN */
+  } else {
+    u += 0x7fffu + ((u >> 16) & 1u);
+  }
+  u &= 0xffff0000u;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static double rnd(const or_cfg* c, double x) { return c->bf16 ? or_bf16_round(x) : x; }
+
+/* Element i of a weight tensor stored as bf16 bits or float. */
+static double wget(const or_cfg* c, const void* w, size_t i) {
+  if (c->bf16) {
+    uint32_t u = (uint32_t)((const uint16_t*)w)[i] << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+  }
+  return (double)((const float*)w)[i];
+}
+
+/* ------------------------------------------------------------- primitives */
+
+/* RMSNorm: y = x / sqrt(mean(x^2) + eps) * g  ([G] 3.2 names RMSNorm for the
+ * fused feature; the decoder layers use the same pre-norm). */
+void or_rmsnorm(const or_cfg* c, int n, const double* x, const void* g, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+  double inv = 1.0 / sqrt(ss / (double)n + c->eps);
+  for (int i = 0; i < n; ++i) y[i] = x[i] * inv * wget(c, g, (size_t)i);
+}
+
+/* Rotary position embedding, rotate-half pairing (i, i + d/2), angle
+ * pos * theta^(-2i/d), applied to one head vector in place. */
+void or_rope(double* v, int d, long pos, double theta) {
+  int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
+    double ang = (double)pos * inv_freq;
+    double cs = cos(ang), sn = sin(ang);
+    double a = v[i], b = v[i + half];
+    v[i] = a * cs - b * sn;
+    v[i + half] = b * cs + a * sn;
+  }
+}
+
+/* Y[m][n] = sum_k W[n][k] * X[m][k], serial k order (same arithmetic for a
+ * row whatever M is). */
+void or_linear(const or_cfg* c, const void* W, int N, int K, int M, const double* X,
+               double* Y) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    for (int m = 0; m < M; ++m) {
+      double s = 0.0;
+      for (int k = 0; k < K; ++k) s += wget(c, W, (size_t)n * K + k) * X[(size_t)m * K + k];
+      Y[(size_t)m * N + n] = s;
+    }
+  }
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Softmax attention of one query head over nk keys (pointers to head rows). */
+static void attend(int d, const double* q, int nk, const double* const* K, const double* const* V,
+                   double* out, double* scratch) {
+  double scale = 1.0 / sqrt((double)d);
+  double mx = -INFINITY;
+  for (int j = 0; j < nk; ++j) {
+    double s = 0.0;
+    for (int e = 0; e < d; ++e) s += q[e] * K[j][e];
+    s *= scale;
+    scratch[j] = s;
+    if (s > mx) mx = s;
+  }
+  double den = 0.0;
+  for (int j = 0; j < nk; ++j) {
+    scratch[j] = exp(scratch[j] - mx);
+    den += scratch[j];
+  }
+  for (int e = 0; e < d; ++e) out[e] = 0.0;
+  for (int j = 0; j < nk; ++j) {
+    double p = scratch[j] / den;
+    for (int e = 0; e < d; ++e) out[e] += p * V[j][e];
+  }
+}
+
+/* Slot of absolute position t in a context cache: plain index, or a ring of
+ * `window` slots when the draft sliding window is on ([T]). */
+static long slot_of(long t, long window) { return window > 0 ? t % window : t; }
+
+/* --------------------------------------------------------- decoder layer */
+
+/*
+ * One pre-norm decoder layer (RMSNorm -> QKV -> RoPE -> GQA attention -> O +
+ * residual -> RMSNorm -> SwiGLU MLP + residual) over M rows of ONE sequence
+ * at consecutive positions p0 .. p0+M-1.  h [M][H] is the residual stream,
+ * updated in place.  Caches are [nkv][cap][d].
+ *
+ * mode OR_CAUSAL (target verification, [G] 3.3): the rows' K/V are written
+ * into the cache at their positions first, and row i attends cache positions
+ * 0 .. p0+i.
+ *
+ * mode OR_BIDIR (draft block, [G] 3.1/3.2): the cache holds the injected
+ * context K/V of positions lo .. p0-1 (lo = max(0, p0-window) with a window,
+ * else 0); row i attends all of those and all M rows of the block, with no
+ * mask inside the block.  The block K/V are not stored.
+ */
+int or_decoder_layer(const or_cfg* c, const or_layer* L, int M, long p0, int mode,
+                     double* kc, double* vc, long cap, long window, double* h) {
+  const int H = c->H, d = c->d, nq = c->nq, nkv = c->nkv, I = c->I;
+  const int QD = nq * d, KD = nkv * d, grp = nq / nkv;
+  if (M <= 0) return 0;
+  if (mode == OR_CAUSAL && p0 + M > cap) return -1;
+  if (mode == OR_BIDIR && window <= 0 && p0 > cap) return -1;
+  if (mode == OR_BIDIR && window > 0 && window > cap) return -1;
+
+  double* x = malloc(sizeof(double) * (size_t)M * H);
+  double* q = malloc(sizeof(double) * (size_t)M * QD);
+  double* k = malloc(sizeof(double) * (size_t)M * KD);
+  double* v = malloc(sizeof(double) * (size_t)M * KD);
+  double* o = malloc(sizeof(double) * (size_t)M * QD);
+  double* y = malloc(sizeof(double) * (size_t)M * (H > I ? H : I));
+  double* gt = malloc(sizeof(double) * (size_t)M * I);
+  double* up = malloc(sizeof(double) * (size_t)M * I);
+  if (!x || !q || !k || !v || !o || !y || !gt || !up) return -2;
+
+  for (int m = 0; m < M; ++m) {
+    or_rmsnorm(c, H, h + (size_t)m * H, L->g1, x + (size_t)m * H);
+    for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
+  }
+  or_linear(c, L->wq, QD, H, M, x, q);
+  or_linear(c, L->wk, KD, H, M, x, k);
+  or_linear(c, L->wv, KD, H, M, x, v);
+  for (int m = 0; m < M; ++m) {
+    long pos = p0 + m;
+    for (int hh = 0; hh < nq; ++hh) or_rope(q + (size_t)m * QD + (size_t)hh * d, d, pos, c->theta);
+    for (int hh = 0; hh < nkv; ++hh) or_rope(k + (size_t)m * KD + (size_t)hh * d, d, pos, c->theta);
+    for (int i = 0; i < QD; ++i) q[(size_t)m * QD + i] = rnd(c, q[(size_t)m * QD + i]);
+    for (int i = 0; i < KD; ++i) {
+      k[(size_t)m * KD + i] = rnd(c, k[(size_t)m * KD + i]);
+      v[(size_t)m * KD + i] = rnd(c, v[(size_t)m * KD + i]);
+    }
+  }
+  if (mode == OR_CAUSAL) {
+    for (int m = 0; m < M; ++m)
+      for (int g = 0; g < nkv; ++g) {
+        memcpy(kc + ((size_t)g * cap + (size_t)(p0 + m)) * d, k + (size_t)m * KD + (size_t)g * d,
+               sizeof(double) * d);
+        memcpy(vc + ((size_t)g * cap + (size_t)(p0 + m)) * d, v + (size_t)m * KD + (size_t)g * d,
+               sizeof(double) * d);
+      }
+  }
+
+  long lo = (mode == OR_BIDIR && window > 0) ? (p0 > window ? p0 - window : 0) : 0;
+  long maxk = (mode == OR_CAUSAL) ? (p0 + M) : (p0 - lo + M);
+#pragma omp parallel
+  {
+    const double** Kp = malloc(sizeof(double*) * (size_t)maxk);
+    const double** Vp = malloc(sizeof(double*) * (size_t)maxk);
+    double* sc = malloc(sizeof(double) * (size_t)maxk);
+#pragma omp for schedule(static)
+    for (int mh = 0; mh < M * nq; ++mh) {
+      int m = mh / nq, hq = mh % nq, g = hq / grp;
+      int nk = 0;
+      if (mode == OR_CAUSAL) {
+        for (long t = 0; t <= p0 + m; ++t) {
+          Kp[nk] = kc + ((size_t)g * cap + (size_t)t) * d;
+          Vp[nk] = vc + ((size_t)g * cap + (size_t)t) * d;
+          ++nk;
+        }
+      } else {
+        for (long t = lo; t < p0; ++t) {
+          Kp[nk] = kc + ((size_t)g * cap + (size_t)slot_of(t, window)) * d;
+          Vp[nk] = vc + ((size_t)g * cap + (size_t)slot_of(t, window)) * d;
+          ++nk;
+        }
+        for (int j = 0; j < M; ++j) {
+          Kp[nk] = k + (size_t)j * KD + (size_t)g * d;
+          Vp[nk] = v + (size_t)j * KD + (size_t)g * d;
+          ++nk;
+        }
+      }
+      attend(d, q + (size_t)m * QD + (size_t)hq * d, nk, Kp, Vp, o + (size_t)m * QD + (size_t)hq * d,
+             sc);
+    }
+    free(Kp);
+    free(Vp);
+    free(sc);
+  }
+  for (size_t i = 0; i < (size_t)M * QD; ++i) o[i] = rnd(c, o[i]);
+
+  or_linear(c, L->wo, H, QD, M, o, y);
+  for (size_t i = 0; i < (size_t)M * H; ++i) h[i] += y[i];
+
+  for (int m = 0; m < M; ++m) {
+    or_rmsnorm(c, H, h + (size_t)m * H, L->g2, x + (size_t)m * H);
+    for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
+  }
+  or_linear(c, L->wg, I, H, M, x, gt);
+  or_linear(c, L->wu, I, H, M, x, up);
+  for (size_t i = 0; i < (size_t)M * I; ++i) gt[i] = rnd(c, silu(gt[i]) * up[i]);
+  or_linear(c, L->wd, H, I, M, gt, y);
+  for (size_t i = 0; i < (size_t)M * H; ++i) h[i] += y[i];
+
+  free(x); free(q); free(k); free(v); free(o); free(y); free(gt); free(up);
+  return 0;
+}
+
+/* ------------------------------------------------------------ output head */
+
+/* x_out[m] = round(RMSNorm(h[m]; g)) -- the final norm before the LM head. */
+void or_final_norm(const or_cfg* c, int M, const double* h, const void* g, double* x_out) {
+  for (int m = 0; m < M; ++m) {
+    or_rmsnorm(c, c->H, h + (size_t)m * c->H, g, x_out + (size_t)m * c->H);
+    for (int i = 0; i < c->H; ++i) x_out[(size_t)m * c->H + i] = rnd(c, x_out[(size_t)m * c->H + i]);
+  }
+}
+
+/*
+ * LM head + greedy argmax: logit[m][v] = W_lm[v] . x[m]; argmax over the
+ * float-rounded logits, lowest vocab index on ties; margin = top1 - top2
+ * (0 for an exact tie).  logits (optional, [M][V]) receives the float logits.
+ */
+void or_lm_head_argmax(const or_cfg* c, const void* Wlm, int V, int M, const double* x,
+                       int* argmax, double* margin, float* logits) {
+  const int H = c->H;
+  for (int m = 0; m < M; ++m) {
+    float* row = malloc(sizeof(float) * (size_t)V);
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < V; ++t) {
+      double s = 0.0;
+      for (int k = 0; k < H; ++k) s += wget(c, Wlm, (size_t)t * H + k) * x[(size_t)m * H + k];
+      row[t] = (float)s;
+    }
+    int best = 0;
+    for (int t = 1; t < V; ++t)
+      if (row[t] > row[best]) best = t;
+    double second = -INFINITY;
+    for (int t = 0; t < V; ++t)
+      if (t != best && (double)row[t] > second) second = (double)row[t];
+    argmax[m] = best;
+    margin[m] = (double)row[best] - second;
+    if (logits) memcpy(logits + (size_t)m * V, row, sizeof(float) * (size_t)V);
+    free(row);
+  }
+}
+
+/* -------------------------------------------------------------- acceptance */
+
+/*
+ * Greedy longest-prefix acceptance ([N] prefix example: 8 drafted, 6 agree,
+ * decoding resumes at the 7th from the target; [G] section 4 step 4).
+ * drafts[j-1] is the draft for block row j (j = 1..B-1); g[i] is the target's
+ * greedy token after block row i (i = 0..B-1).  Draft j is accepted while it
+ * equals g[j-1]; the bonus token is g[k] after k accepted drafts.
+ * out_tokens[0..k-1] = accepted drafts, out_tokens[k] = bonus.  Returns k.
+ */
+int or_accept(int B, const int* drafts, const int* g, int* out_tokens) {
+  int k = 0;
+  while (k < B - 1 && drafts[k] == g[k]) {
+    out_tokens[k] = drafts[k];
+    ++k;
+  }
+  out_tokens[k] = g[k];
+  return k;
+}
+
+/* ---------------------------------------------- context fusion + injection */
+
+/*
+ * Context-feature fusion and KV injection ([G] 3.2 and FAQ Q2; [N] "KV
+ * injection"): for each position t with tap features f_t = [h_t^{l_1}, ...,
+ * h_t^{l_F}] (already rounded, [T][F*H]),
+ *     c_t = round(RMSNorm(W_fc f_t; g_fc)),
+ * and for every draft layer j
+ *     K_ctx^j[t] = round(RoPE(W_k^j c_t, t)),  V_ctx^j[t] = round(W_v^j c_t),
+ * written to slot slot_of(t, window) of the layer's context cache [nkv][cap][d].
+ * c_out (optional, [T][H]) receives c_t.
+ */
+int or_fuse_context(const or_cfg* c, int F, const void* Wfc, const void* gfc, int T,
+                    const double* feats, const long* pos, int n_layers, const void* const* wk,
+                    const void* const* wv, double* const* kc, double* const* vc, long cap,
+                    long window, double* c_out) {
+  const int H = c->H, d = c->d, nkv = c->nkv, KD = nkv * d;
+  double* z = malloc(sizeof(double) * (size_t)T * H);
+  double* cc = malloc(sizeof(double) * (size_t)T * H);
+  double* kk = malloc(sizeof(double) * (size_t)T * KD);
+  double* vv = malloc(sizeof(double) * (size_t)T * KD);
+  if (!z || !cc || !kk || !vv) return -2;
+  for (int t = 0; t < T; ++t) {
+    long s = slot_of(pos[t], window);
+    if (pos[t] < 0 || s >= cap) return -1;
+  }
+  or_linear(c, Wfc, H, F * H, T, feats, z);
+  for (int t = 0; t < T; ++t) {
+    or_rmsnorm(c, H, z + (size_t)t * H, gfc, cc + (size_t)t * H);
+    for (int i = 0; i < H; ++i) cc[(size_t)t * H + i] = rnd(c, cc[(size_t)t * H + i]);
+  }
+  if (c_out) memcpy(c_out, cc, sizeof(double) * (size_t)T * H);
+  for (int j = 0; j < n_layers; ++j) {
+    or_linear(c, wk[j], KD, H, T, cc, kk);
+    or_linear(c, wv[j], KD, H, T, cc, vv);
+    for (int t = 0; t < T; ++t) {
+      long s = slot_of(pos[t], window);
+      for (int g = 0; g < nkv; ++g) {
+        double* kr = kk + (size_t)t * KD + (size_t)g * d;
+        or_rope(kr, d, pos[t], c->theta);
+        for (int e = 0; e < d; ++e) {
+          kc[j][((size_t)g * cap + (size_t)s) * d + e] = rnd(c, kr[e]);
+          vc[j][((size_t)g * cap + (size_t)s) * d + e] = rnd(c, vv[(size_t)t * KD + (size_t)g * d + e]);
+        }
+      }
+    }
+  }
+  free(z); free(cc); free(kk); free(vv);
+  return 0;
+}
+
+/* ----------------------------------------------------------- path selector */
+
+/*
+ * DFlash 2 path selector ([G] section 7), greedy form.  For each block row
+ * j = 1..B-1 keep the top-`topk` draft candidates of that row's logits
+ * (ordered by logit descending, index ascending).  The score of a transition
+ * a -> b is the low-rank bilinear form (U e_a) . (V e_b) with e the shared
+ * embedding rows and U, Vm in R^{R x H}.  Walk greedily: p_0 = anchor,
+ * p_j = the candidate of row j with the highest score from p_{j-1}, the
+ * lower rank on ties.  logits: [B-1][Vocab] float (row j-1 for block row j).
+ * path[j-1] = p_j; cand [B-1][topk] receives the candidate lists; margin[j-1]
+ * = best minus second-best score at step j.
+ */
+void or_path_select(const or_cfg* c, int B, int Vocab, int topk, int R, const float* logits,
+                    const void* E, const void* U, const void* Vm, int anchor, int* cand,
+                    int* path, double* margin) {
+  const int H = c->H;
+  double* ue = malloc(sizeof(double) * (size_t)R);
+  double* ve = malloc(sizeof(double) * (size_t)R);
+  for (int j = 0; j < B - 1; ++j) {
+    const float* row = logits + (size_t)j * Vocab;
+    int* cj = cand + (size_t)j * topk;
+    for (int r = 0; r < topk; ++r) {
+      int best = -1;
+      for (int t = 0; t < Vocab; ++t) {
+        int used = 0;
+        for (int q = 0; q < r; ++q)
+          if (cj[q] == t) used = 1;
+        if (used) continue;
+        if (best < 0 || row[t] > row[best]) best = t;
+      }
+      cj[r] = best;
+    }
+  }
+  int prev = anchor;
+  for (int j = 0; j < B - 1; ++j) {
+    for (int r = 0; r < R; ++r) {
+      double s = 0.0;
+      for (int k = 0; k < H; ++k) s += wget(c, U, (size_t)r * H + k) * wget(c, E, (size_t)prev * H + k);
+      ue[r] = s;
+    }
+    double best = -INFINITY, second = -INFINITY;
+    int bi = 0;
+    for (int q = 0; q < topk; ++q) {
+      int b = cand[(size_t)j * topk + q];
+      double sc = 0.0;
+      for (int r = 0; r < R; ++r) {
+        double s = 0.0;
+        for (int k = 0; k < H; ++k) s += wget(c, Vm, (size_t)r * H + k) * wget(c, E, (size_t)b * H + k);
+        ve[r] = s;
+        sc += ue[r] * ve[r];
+      }
+      sc = (double)(float)sc; /* decided in float, the precision of the GPU path */
+      if (sc > best) {
+        second = best;
+        best = sc;
+        bi = q;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+    path[j] = cand[(size_t)j * topk + bi];
+    margin[j] = best - second;
+    prev = path[j];
+  }
+  free(ue);
+  free(ve);
+}
+
+int or_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,450 @@
+"""CPU oracle for one DFlash draft-and-verify cycle (numpy + the plain C in
+dflash_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import this module.  It shares no
+code with the CUDA library and never imports it; inputs arrive as numpy arrays
+(weights as float32 or as bf16 bit patterns in uint16 arrays).
+
+Sources, cited by page title and section:
+  [G] "DFlash: block-diffusion accelerated LLM speculative decoding" guide
+      (txtmix.com): 3.1 one forward yields the whole block; 3.2 the draft is
+      conditioned on target features (taps, concat, projection, RMSNorm, K/V
+      injection into every draft layer); 3.3 verification by the target;
+      section 4 the cycle (draft 16 -> verify -> accept prefix -> redraft);
+      section 7 the DFlash 2 path selector; FAQ Q2 the taps.
+  [N] "DFlash 2 release: parallel drafts keep lowering LLM inference latency"
+      (openai-hub.com): the prefix-acceptance example; lossless greedy output;
+      the per-token cost example in "what it means for deployment".
+  [T] llmapis.com note on DFlash, "data and technical details": the draft
+      sliding window bounding draft KV growth.
+
+Every function is the plain definition: a row's result never depends on how
+many rows are processed together, so the speculative loop reproduces the plain
+greedy loop exactly (the lossless property of [N] and [G] 3.3).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dflash_oracle.c")
+_SO = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CAUSAL = 0
+BIDIR = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile dflash_oracle.c with gcc (no fused multiply-add contraction, so
+    x86 and Arm builds compute the same values)."""
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class _Cfg(C.Structure):
+    _fields_ = [("H", C.c_int), ("nq", C.c_int), ("nkv", C.c_int), ("d", C.c_int), ("I", C.c_int),
+                ("bf16", C.c_int), ("theta", C.c_double), ("eps", C.c_double)]
+
+
+class _Layer(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g1", "g2")]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            dp = C.POINTER(C.c_double)
+            L.or_bf16_round.restype = C.c_double
+            L.or_bf16_round.argtypes = [C.c_double]
+            L.or_rope.argtypes = [dp, C.c_int, C.c_long, C.c_double]
+            L.or_rmsnorm.argtypes = [C.POINTER(_Cfg), C.c_int, dp, C.c_void_p, dp]
+            L.or_linear.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_int, C.c_int, C.c_int, dp, dp]
+            L.or_decoder_layer.argtypes = [C.POINTER(_Cfg), C.POINTER(_Layer), C.c_int, C.c_long,
+                                           C.c_int, dp, dp, C.c_long, C.c_long, dp]
+            L.or_final_norm.argtypes = [C.POINTER(_Cfg), C.c_int, dp, C.c_void_p, dp]
+            L.or_lm_head_argmax.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_int, C.c_int, dp,
+                                            C.POINTER(C.c_int), dp, C.POINTER(C.c_float)]
+            L.or_accept.argtypes = [C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int),
+                                    C.POINTER(C.c_int)]
+            L.or_fuse_context.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_void_p, C.c_void_p,
+                                          C.c_int, dp, C.POINTER(C.c_long), C.c_int,
+                                          C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                          C.POINTER(dp), C.POINTER(dp), C.c_long, C.c_long, dp]
+            L.or_path_select.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, C.c_int, C.c_int,
+                                         C.POINTER(C.c_float), C.c_void_p, C.c_void_p, C.c_void_p,
+                                         C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), dp]
+            L.or_num_threads.restype = C.c_int
+            _lib = L
+    return _lib
+
+
+def _dp(a: np.ndarray):
+    assert a.dtype == np.float64 and a.flags.c_contiguous
+    return a.ctypes.data_as(C.POINTER(C.c_double))
+
+
+def _vp(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return C.c_void_p(a.ctypes.data)
+
+
+# ------------------------------------------------------------------ model data
+
+
+@dataclass
+class Cfg:
+    """Shape and arithmetic mode of one decoder stack."""
+    H: int
+    nq: int
+    nkv: int
+    d: int
+    I: int
+    bf16: bool
+    theta: float
+    eps: float
+
+    def c(self) -> _Cfg:
+        return _Cfg(self.H, self.nq, self.nkv, self.d, self.I, int(self.bf16), self.theta, self.eps)
+
+    def wdtype(self):
+        return np.uint16 if self.bf16 else np.float32
+
+
+@dataclass
+class Layer:
+    """One decoder layer's weights, [out][in] row-major (views are fine)."""
+    wq: np.ndarray
+    wk: np.ndarray
+    wv: np.ndarray
+    wo: np.ndarray
+    wg: np.ndarray
+    wu: np.ndarray
+    wd: np.ndarray
+    g1: np.ndarray
+    g2: np.ndarray
+
+    def c(self) -> _Layer:
+        arrs = [self.wq, self.wk, self.wv, self.wo, self.wg, self.wu, self.wd, self.g1, self.g2]
+        return _Layer(*[a.ctypes.data for a in arrs])
+
+    @staticmethod
+    def from_stacked(cfg: Cfg, w_qkv, w_o, w_gu, w_down, ln1, ln2) -> "Layer":
+        """Split a stacked [Wq; Wk; Wv] and [W_gate; W_up] into the per-matrix
+        views the definitions use."""
+        QD, KD = cfg.nq * cfg.d, cfg.nkv * cfg.d
+        c = np.ascontiguousarray
+        return Layer(c(w_qkv[:QD]), c(w_qkv[QD:QD + KD]), c(w_qkv[QD + KD:QD + 2 * KD]), c(w_o),
+                     c(w_gu[:cfg.I]), c(w_gu[cfg.I:]), c(w_down), c(ln1), c(ln2))
+
+
+def wfloat(cfg: Cfg, w: np.ndarray) -> np.ndarray:
+    """Weights as float64 (bf16 bit patterns are widened exactly)."""
+    if cfg.bf16:
+        return (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return w.astype(np.float64)
+
+
+def rnd(cfg: Cfg, x: np.ndarray) -> np.ndarray:
+    """Round to bf16 (RNE) in bf16 mode; identity in fp32 mode."""
+    if not cfg.bf16:
+        return x
+    return bf16_round_array(x)
+
+
+def bf16_round_array(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bfloat16 (via float32, round-to-nearest-even)
+    and widen back; NaN stays NaN, overflow goes to +-inf."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    r = u.astype(np.uint32).view(np.float32).astype(np.float64)
+    r[np.isnan(f)] = np.nan
+    return r
+
+
+# ------------------------------------------------------------------ primitives
+
+
+def rmsnorm(cfg: Cfg, x: np.ndarray, g: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    c = cfg.c()
+    for r in range(x.shape[0]):
+        lib().or_rmsnorm(C.byref(c), x.shape[1], _dp(x[r]), _vp(g), _dp(y[r]))
+    return y
+
+
+def rope(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
+    """Rotate-half RoPE of one head vector at absolute position pos."""
+    v = np.array(v, dtype=np.float64)
+    lib().or_rope(_dp(v), v.shape[0], int(pos), float(theta))
+    return v
+
+
+def linear(cfg: Cfg, W: np.ndarray, X: np.ndarray) -> np.ndarray:
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    N, K = W.shape
+    Y = np.empty((X.shape[0], N))
+    lib().or_linear(C.byref(cfg.c()), _vp(W), N, K, X.shape[0], _dp(X), _dp(Y))
+    return Y
+
+
+def decoder_layer(cfg: Cfg, L: Layer, h: np.ndarray, p0: int, mode: int, kc: np.ndarray,
+                  vc: np.ndarray, window: int = 0) -> None:
+    """One decoder layer over the rows h[M][H] of one sequence at positions
+    p0..p0+M-1, in place.  kc/vc: [nkv][cap][d] float64 caches."""
+    assert h.dtype == np.float64 and h.flags.c_contiguous
+    cap = kc.shape[1]
+    rc = lib().or_decoder_layer(C.byref(cfg.c()), C.byref(L.c()), h.shape[0], int(p0), int(mode),
+                                _dp(kc), _dp(vc), cap, int(window), _dp(h))
+    if rc != 0:
+        raise ValueError(f"or_decoder_layer failed ({rc})")
+
+
+def final_norm(cfg: Cfg, h: np.ndarray, g: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.float64)
+    x = np.empty_like(h)
+    lib().or_final_norm(C.byref(cfg.c()), h.shape[0], _dp(h), _vp(g), _dp(x))
+    return x
+
+
+def lm_head_argmax(cfg: Cfg, Wlm: np.ndarray, x: np.ndarray, want_logits: bool = False):
+    """Greedy argmax (lowest index on ties) and top1-top2 margin per row."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    M, V = x.shape[0], Wlm.shape[0]
+    am = np.empty(M, dtype=np.int32)
+    mg = np.empty(M, dtype=np.float64)
+    lg = np.empty((M, V), dtype=np.float32) if want_logits else None
+    lib().or_lm_head_argmax(C.byref(cfg.c()), _vp(Wlm), V, M, _dp(x),
+                            am.ctypes.data_as(C.POINTER(C.c_int)), _dp(mg),
+                            lg.ctypes.data_as(C.POINTER(C.c_float)) if lg is not None else None)
+    return am, mg, lg
+
+
+def accept(drafts, g) -> tuple[int, np.ndarray]:
+    """Greedy longest-prefix acceptance; returns (k, out_tokens[:k+1])."""
+    g = np.ascontiguousarray(g, dtype=np.int32)
+    B = g.shape[0]
+    d = np.ascontiguousarray(drafts, dtype=np.int32)
+    assert d.shape[0] == B - 1
+    out = np.zeros(B, dtype=np.int32)
+    k = lib().or_accept(B, d.ctypes.data_as(C.POINTER(C.c_int)),
+                        g.ctypes.data_as(C.POINTER(C.c_int)), out.ctypes.data_as(C.POINTER(C.c_int)))
+    return int(k), out[:k + 1].copy()
+
+
+def fuse_context(dcfg: Cfg, F: int, Wfc, gfc, feats: np.ndarray, pos, wk_list, wv_list,
+                 kc_list, vc_list, window: int = 0) -> np.ndarray:
+    """Fusion + K/V injection of T positions into every draft layer's context
+    cache; returns c_t [T][H]."""
+    feats = np.ascontiguousarray(feats, dtype=np.float64).reshape(len(pos), F * dcfg.H)
+    T = feats.shape[0]
+    pos_a = np.ascontiguousarray(pos, dtype=np.int64)
+    n = len(wk_list)
+    wk = (C.c_void_p * n)(*[w.ctypes.data for w in wk_list])
+    wv = (C.c_void_p * n)(*[w.ctypes.data for w in wv_list])
+    kc = (C.POINTER(C.c_double) * n)(*[_dp(a) for a in kc_list])
+    vc = (C.POINTER(C.c_double) * n)(*[_dp(a) for a in vc_list])
+    cout = np.empty((T, dcfg.H))
+    rc = lib().or_fuse_context(C.byref(dcfg.c()), F, _vp(Wfc), _vp(gfc), T, _dp(feats),
+                               pos_a.ctypes.data_as(C.POINTER(C.c_long)), n, wk, wv, kc, vc,
+                               kc_list[0].shape[1], int(window), _dp(cout))
+    if rc != 0:
+        raise ValueError(f"or_fuse_context failed ({rc})")
+    return cout
+
+
+def path_select(cfg: Cfg, logits: np.ndarray, E, U, Vm, anchor: int, topk: int = 16):
+    """DFlash 2 greedy path walk over the top-k candidates of each draft row."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    Bm1, Vocab = lg.shape
+    R = U.shape[0]
+    cand = np.zeros((Bm1, topk), dtype=np.int32)
+    path = np.zeros(Bm1, dtype=np.int32)
+    mg = np.zeros(Bm1)
+    lib().or_path_select(C.byref(cfg.c()), Bm1 + 1, Vocab, topk, R,
+                         lg.ctypes.data_as(C.POINTER(C.c_float)), _vp(E), _vp(U), _vp(Vm),
+                         int(anchor), cand.ctypes.data_as(C.POINTER(C.c_int)),
+                         path.ctypes.data_as(C.POINTER(C.c_int)), _dp(mg))
+    return path, cand, mg
+
+
+def tap_layers(n_layers: int, n_taps: int = 5, first: int = 2) -> list[int]:
+    """Tap layer ids spread uniformly from layer `first` to the third-from-last
+    ([G] 3.2, FAQ Q2), 0-indexed decoder-layer outputs, rounded down."""
+    last = n_layers - 3
+    if n_taps == 1:
+        return [first]
+    return [first + (i * (last - first)) // (n_taps - 1) for i in range(n_taps)]
+
+
+def per_token_cost_ms(t_draft_ms: float, t_verify_ms: float, accepted: float) -> float:
+    """Per-token cost of one cycle spread over the tokens it yields ([N],
+    'what it means for deployment': 3 ms + 20 ms over 6 tokens ~ 3.8 ms)."""
+    return (t_draft_ms + t_verify_ms) / accepted
+
+
+# ------------------------------------------------------------------- the cycle
+
+
+@dataclass
+class Stack:
+    """A decoder stack: config, layers, final norm gain."""
+    cfg: Cfg
+    layers: list
+    g_final: np.ndarray
+
+
+@dataclass
+class Model:
+    """Target + draft sharing the embedding E and LM head W_lm ([G] 3.1)."""
+    target: Stack
+    draft: Stack
+    E: np.ndarray
+    Wlm: np.ndarray
+    Wfc: np.ndarray
+    gfc: np.ndarray
+    taps: list
+    mask_id: int
+    block: int
+    window: int = 0
+
+
+@dataclass
+class SeqState:
+    """Per-sequence caches: target KV (D1) and injected draft context KV (D2)."""
+    tk: list = field(default_factory=list)
+    tv: list = field(default_factory=list)
+    dk: list = field(default_factory=list)
+    dv: list = field(default_factory=list)
+
+
+def new_state(m: Model, cap: int) -> SeqState:
+    t, d = m.target.cfg, m.draft.cfg
+    dcap = m.window if m.window > 0 else cap
+    s = SeqState()
+    s.tk = [np.zeros((t.nkv, cap, t.d)) for _ in m.target.layers]
+    s.tv = [np.zeros((t.nkv, cap, t.d)) for _ in m.target.layers]
+    s.dk = [np.zeros((d.nkv, dcap, d.d)) for _ in m.draft.layers]
+    s.dv = [np.zeros((d.nkv, dcap, d.d)) for _ in m.draft.layers]
+    return s
+
+
+def embed(cfg: Cfg, E: np.ndarray, tokens) -> np.ndarray:
+    return np.ascontiguousarray(wfloat(cfg, E[np.asarray(tokens, dtype=np.int64)]))
+
+
+def target_forward(m: Model, st: SeqState, tokens, p0: int, want_logits: bool = False):
+    """Causal target forward over tokens at positions p0.. ([G] 3.3): writes
+    their K/V into the target cache, returns greedy argmax per row, margins,
+    tap features [M][F*H] (rounded residual after each tap layer, in
+    increasing layer order) and optionally logits."""
+    cfg = m.target.cfg
+    h = embed(cfg, m.E, tokens)
+    taps = {}
+    for li, L in enumerate(m.target.layers):
+        decoder_layer(cfg, L, h, p0, CAUSAL, st.tk[li], st.tv[li])
+        if li in m.taps:
+            taps[li] = rnd(cfg, h.copy())
+    feats = np.concatenate([taps[l] for l in m.taps], axis=1)
+    x = final_norm(cfg, h, m.target.g_final)
+    am, mg, lg = lm_head_argmax(cfg, m.Wlm, x, want_logits)
+    return am, mg, feats, lg
+
+
+def fuse(m: Model, st: SeqState, feats: np.ndarray, pos) -> np.ndarray:
+    """Inject positions `pos` (tap features feats [T][F*H]) into D2."""
+    d = m.draft
+    wk = [L.wk for L in d.layers]
+    wv = [L.wv for L in d.layers]
+    return fuse_context(d.cfg, len(m.taps), m.Wfc, m.gfc, feats, pos, wk, wv, st.dk, st.dv,
+                        m.window)
+
+
+def draft_forward(m: Model, st: SeqState, anchor: int, P: int, want_logits: bool = False):
+    """Single-step block-diffusion draft ([G] 3.1): block [anchor, mask...]
+    at positions P..P+B-1, bidirectional over the injected context and the
+    block; row j (j >= 1) predicts the token at position P+j.  Returns
+    drafts [B-1], margins, and optionally logits [B-1][V]."""
+    cfg = m.draft.cfg
+    B = m.block
+    tokens = [anchor] + [m.mask_id] * (B - 1)
+    h = embed(cfg, m.E, tokens)
+    for li, L in enumerate(m.draft.layers):
+        decoder_layer(cfg, L, h, P, BIDIR, st.dk[li], st.dv[li], m.window)
+    x = final_norm(cfg, h, m.draft.g_final)
+    am, mg, lg = lm_head_argmax(cfg, m.Wlm, x[1:], want_logits)
+    return am, mg, lg
+
+
+def prefill(m: Model, st: SeqState, prompt):
+    """Target forward over the prompt, inject every prompt position into the
+    draft context; returns the first generated token (the first anchor)."""
+    am, mg, feats, _ = target_forward(m, st, prompt, 0)
+    fuse(m, st, feats, list(range(len(prompt))))
+    return int(am[-1])
+
+
+def greedy_generate(m: Model, prompt, n_new: int, cap: int):
+    """Plain autoregressive greedy decoding with the target alone: one target
+    forward per token.  Returns the generated tokens and the per-token argmax
+    margins."""
+    st = new_state(m, cap)
+    am, mg, _, _ = target_forward(m, st, prompt, 0)
+    out = [int(am[-1])]
+    margins = [float(mg[-1])]
+    P = len(prompt)
+    while len(out) < n_new:
+        am, mg, _, _ = target_forward(m, st, [out[-1]], P)
+        out.append(int(am[0]))
+        margins.append(float(mg[0]))
+        P += 1
+    return np.array(out, dtype=np.int32), np.array(margins)
+
+
+def speculative_generate(m: Model, prompt, n_new: int, cap: int, drafter=None):
+    """The DFlash loop ([G] section 4): prefill, then repeat {draft a block
+    from the anchor, verify it causally with the target, accept the longest
+    agreeing prefix plus the bonus token, inject the committed positions'
+    features}.  `drafter(m, st, anchor, P)` may replace the draft model
+    (tests plant perfect or wrong drafts).  Returns tokens, per-cycle accept
+    lengths."""
+    st = new_state(m, cap)
+    anchor = prefill(m, st, prompt)
+    out = [anchor]
+    P = len(prompt)
+    accepts = []
+    while len(out) < n_new:
+        if drafter is None:
+            drafts, _, _ = draft_forward(m, st, anchor, P)
+        else:
+            drafts = np.asarray(drafter(m, st, anchor, P), dtype=np.int32)
+        block = [anchor] + [int(t) for t in drafts]
+        g, _, feats, _ = target_forward(m, st, block, P)
+        k, emitted = accept(drafts, g)
+        accepts.append(k)
+        fuse(m, st, feats[:k + 1], list(range(P, P + k + 1)))
+        out.extend(int(t) for t in emitted)
+        P += k + 1
+        anchor = int(emitted[-1])
+    return np.array(out[:n_new], dtype=np.int32), accepts
+
+
+def threads() -> int:
+    return int(lib().or_num_threads())
