@@ -1,0 +1,738 @@
+// abi.cu -- the C ABI (include/dflash.h): host-side argument checks,
+// workspace carving and the launch sequence of each entry point.  Every
+// check runs before the first launch of a call; no exception crosses the ABI.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dfl;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define DF_CHECK(cond, ...)                                 \
+  do {                                                      \
+    if (!(cond)) return fail(DFLASH_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+#define DF_CUDA(call)                                                                       \
+  do {                                                                                      \
+    cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) return fail(DFLASH_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t elem_size(int dtype) { return dtype == DFLASH_BF16 ? 2 : 4; }
+
+// Carves a workspace into 256-byte aligned pieces; with base == nullptr it
+// only measures.
+struct Bump {
+  char* base;
+  size_t off = 0;
+  explicit Bump(void* b) : base(static_cast<char*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+int check_dims(const dflash_dims& d, const char* who) {
+  DF_CHECK(d.dtype == DFLASH_F32 || d.dtype == DFLASH_BF16, "%s: dtype %d not F32/BF16", who, d.dtype);
+  DF_CHECK(d.hidden > 0 && d.hidden % 8 == 0, "%s: hidden %d must be a positive multiple of 8", who, d.hidden);
+  DF_CHECK(d.head_dim == 64 || d.head_dim == 128, "%s: head_dim %d must be 64 or 128", who, d.head_dim);
+  DF_CHECK(d.n_q_heads > 0 && d.n_kv_heads > 0 && d.n_q_heads % d.n_kv_heads == 0,
+           "%s: n_q_heads %d must be a positive multiple of n_kv_heads %d", who, d.n_q_heads, d.n_kv_heads);
+  DF_CHECK(d.intermediate > 0 && d.intermediate % 8 == 0, "%s: intermediate %d must be a multiple of 8", who,
+           d.intermediate);
+  DF_CHECK((d.n_q_heads * d.head_dim) % 8 == 0, "%s: n_q_heads*head_dim must be a multiple of 8", who);
+  DF_CHECK(d.vocab > 0, "%s: vocab must be positive", who);
+  DF_CHECK(d.rms_eps >= 0.f && d.rope_theta > 0.f, "%s: rms_eps >= 0 and rope_theta > 0 required", who);
+  return DFLASH_OK;
+}
+
+struct Ctx {
+  uint32_t* status;
+  uint32_t* counters;
+};
+
+Ctx header(void* ws) {
+  Ctx c;
+  c.status = static_cast<uint32_t*>(ws);
+  c.counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kHeaderBytes);
+  return c;
+}
+
+// ------------------------------------------------------------------ GEMMs
+
+size_t gemm_scratch_bytes(const GemmDesc& g, int sms) {
+  return g.dtype == DFLASH_BF16 && gemm_tc_supported(g) ? gemm_tc_workspace(g, sms) : 0;
+}
+
+cudaError_t run_gemm(const GemmDesc& g, void* gpart, size_t gpart_bytes, const Ctx& c, int sms,
+                     cudaStream_t st) {
+  if (g.dtype == DFLASH_BF16 && gemm_tc_supported(g))
+    return launch_gemm_tc(g, gpart, gpart_bytes, c.counters, c.status, sms, st);
+  return launch_gemm_simt(g, st);
+}
+
+GemmDesc gemm_base(int dtype, int M, int K, const void* X, const int32_t* base_pos, const int32_t* valid,
+                   int rows) {
+  GemmDesc g;
+  memset(&g, 0, sizeof(g));
+  g.dtype = dtype;
+  g.M = M;
+  g.K = K;
+  g.X = X;
+  g.nseg = 1;
+  g.base_pos = base_pos;
+  g.valid = valid;
+  g.rows = rows;
+  return g;
+}
+
+// ----------------------------------------------------------- decoder layer
+
+struct LayerScratch {
+  void *x, *q, *kb, *vb, *attn, *act;
+  float* apart;
+  void* gpart;
+  size_t gpart_bytes;
+};
+
+struct LayerShape {
+  dflash_dims d;
+  int S, rows, mode, max_pos, cap, window;
+};
+
+void layer_gemms(const LayerShape& L, const dflash_layer_weights* w, GemmDesc* g4) {
+  const dflash_dims& d = L.d;
+  const int M = L.S * L.rows, H = d.hidden, QD = d.n_q_heads * d.head_dim, KD = d.n_kv_heads * d.head_dim;
+  GemmDesc qkv = gemm_base(d.dtype, M, H, nullptr, nullptr, nullptr, L.rows);
+  qkv.seg_w[0] = w ? w->w_qkv : nullptr;
+  qkv.seg_rows = QD + 2 * KD;
+  qkv.kind = EPI_QKV;
+  qkv.nq = d.n_q_heads;
+  qkv.nkv = d.n_kv_heads;
+  qkv.d = d.head_dim;
+  GemmDesc o = gemm_base(d.dtype, M, QD, nullptr, nullptr, nullptr, L.rows);
+  o.seg_w[0] = w ? w->w_o : nullptr;
+  o.seg_rows = H;
+  o.kind = EPI_RESID;
+  o.ldo = H;
+  GemmDesc gu = gemm_base(d.dtype, M, H, nullptr, nullptr, nullptr, L.rows);
+  gu.seg_w[0] = w ? w->w_gu : nullptr;
+  gu.seg_rows = 2 * d.intermediate;
+  gu.kind = EPI_SWIGLU;
+  gu.inter = d.intermediate;
+  GemmDesc dn = gemm_base(d.dtype, M, d.intermediate, nullptr, nullptr, nullptr, L.rows);
+  dn.seg_w[0] = w ? w->w_down : nullptr;
+  dn.seg_rows = H;
+  dn.kind = EPI_RESID;
+  dn.ldo = H;
+  g4[0] = qkv;
+  g4[1] = o;
+  g4[2] = gu;
+  g4[3] = dn;
+}
+
+AttnDesc attn_shape(const LayerShape& L) {
+  AttnDesc a;
+  memset(&a, 0, sizeof(a));
+  a.dtype = L.d.dtype;
+  a.mode = L.mode;
+  a.n_seqs = L.S;
+  a.rows = L.rows;
+  a.nq = L.d.n_q_heads;
+  a.nkv = L.d.n_kv_heads;
+  a.d = L.d.head_dim;
+  a.cap = L.cap;
+  a.window = L.window;
+  a.max_pos = L.max_pos;
+  return a;
+}
+
+void carve_layer(Bump& b, const LayerShape& L, int sms, LayerScratch& s) {
+  const dflash_dims& d = L.d;
+  const size_t es = elem_size(d.dtype);
+  const size_t M = (size_t)L.S * L.rows;
+  const size_t QD = (size_t)d.n_q_heads * d.head_dim;
+  s.x = b.take(M * d.hidden * es);
+  s.q = b.take(M * QD * es);
+  s.kb = b.take((size_t)L.S * d.n_kv_heads * L.rows * d.head_dim * es);
+  s.vb = b.take((size_t)L.S * d.n_kv_heads * L.rows * d.head_dim * es);
+  s.attn = b.take(M * QD * es);
+  s.act = b.take(M * d.intermediate * es);
+  s.apart = static_cast<float*>(b.take(attn_workspace(attn_shape(L))));
+  GemmDesc g4[4];
+  layer_gemms(L, nullptr, g4);
+  size_t gp = 0;
+  for (auto& g : g4) gp = std::max(gp, gemm_scratch_bytes(g, sms));
+  s.gpart_bytes = gp;
+  s.gpart = b.take(gp);
+}
+
+int check_layer_shape(const LayerShape& L, const char* who) {
+  DF_CHECK(L.S > 0 && L.rows > 0, "%s: n_seqs and rows must be positive", who);
+  DF_CHECK(L.mode == DFLASH_ATTN_CAUSAL || L.mode == DFLASH_ATTN_BLOCK_BIDIR, "%s: bad attn_mode", who);
+  DF_CHECK(L.cap > 0, "%s: kv capacity must be positive", who);
+  DF_CHECK(L.max_pos >= L.rows, "%s: max_pos must cover base_pos + rows", who);
+  if (L.mode == DFLASH_ATTN_CAUSAL) {
+    DF_CHECK(L.window == 0, "%s: causal layers take no window", who);
+    DF_CHECK(L.max_pos <= L.cap, "%s: max_pos %d exceeds cache capacity %d", who, L.max_pos, L.cap);
+  } else {
+    DF_CHECK(L.window == 0 ? L.max_pos - L.rows <= L.cap : L.window == L.cap,
+             "%s: context cache too small (window ring needs capacity == window)", who);
+  }
+  if (L.mode == DFLASH_ATTN_BLOCK_BIDIR)
+    DF_CHECK(L.rows <= 64, "%s: a bidirectional block holds at most 64 rows", who);
+  AttnDesc a = attn_shape(L);
+  const int grp = L.d.n_q_heads / L.d.n_kv_heads;
+  const int n_qt = (L.rows * grp + 63) / 64;
+  DF_CHECK((long)L.S * L.d.n_kv_heads * n_qt <= 16384, "%s: too many attention groups (n_seqs*n_kv*tiles > 16384)",
+           who);
+  (void)a;
+  return DFLASH_OK;
+}
+
+int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_kv& kv, float* h,
+              const int32_t* base_pos, const float* rope_cs, int rope_max_pos, void* tap, int tap_stride, int tap_offset,
+              const LayerScratch& s, const Ctx& c, int sms, cudaStream_t st) {
+  const dflash_dims& d = L.d;
+  const int M = L.S * L.rows, H = d.hidden;
+  GemmDesc g4[4];
+  layer_gemms(L, &w, g4);
+  for (auto& g : g4) g.base_pos = base_pos;
+  const bool causal = L.mode == DFLASH_ATTN_CAUSAL;
+
+  DF_CUDA(launch_rmsnorm(d.dtype, h, w.ln1, M, H, d.rms_eps, s.x, st));
+  GemmDesc& qkv = g4[0];
+  qkv.X = s.x;
+  qkv.q_out = s.q;
+  qkv.k_dst[0] = causal ? kv.k : s.kb;
+  qkv.v_dst[0] = causal ? kv.v : s.vb;
+  qkv.kv_cap = causal ? kv.capacity : L.rows;
+  qkv.kv_window = 0;
+  qkv.kv_slot_mode = causal ? 1 : 0;
+  qkv.rope_cs = rope_cs;
+  qkv.rope_max_pos = rope_max_pos;
+  DF_CUDA(run_gemm(qkv, s.gpart, s.gpart_bytes, c, sms, st));
+
+  AttnDesc a = attn_shape(L);
+  a.base_pos = base_pos;
+  a.q = s.q;
+  a.kc = kv.k;
+  a.vc = kv.v;
+  a.kb = s.kb;
+  a.vb = s.vb;
+  a.out = s.attn;
+  a.partials = s.apart;
+  a.counters = c.counters;
+  a.status = c.status;
+  DF_CUDA(launch_attention(a, st));
+
+  GemmDesc& o = g4[1];
+  o.X = s.attn;
+  o.out_f32 = h;
+  DF_CUDA(run_gemm(o, s.gpart, s.gpart_bytes, c, sms, st));
+
+  DF_CUDA(launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x, st));
+  GemmDesc& gu = g4[2];
+  gu.X = s.x;
+  gu.act_out = s.act;
+  DF_CUDA(run_gemm(gu, s.gpart, s.gpart_bytes, c, sms, st));
+
+  GemmDesc& dn = g4[3];
+  dn.X = s.act;
+  dn.out_f32 = h;
+  DF_CUDA(run_gemm(dn, s.gpart, s.gpart_bytes, c, sms, st));
+
+  if (tap) DF_CUDA(launch_store_tap(d.dtype, h, M, H, tap, tap_stride, tap_offset, st));
+  return DFLASH_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need, const char* who) {
+  if (!ws) return fail(DFLASH_ERR_INVALID_ARG, "%s: workspace is NULL", who);
+  if (ws_bytes < need)
+    return fail(DFLASH_ERR_WORKSPACE, "%s: workspace %zu bytes, %zu required", who, ws_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  return DFLASH_OK;
+}
+
+int check_weights(const dflash_layer_weights& w, const char* who) {
+  DF_CHECK(w.w_qkv && w.w_o && w.w_gu && w.w_down && w.ln1 && w.ln2, "%s: null layer weight", who);
+  return DFLASH_OK;
+}
+
+// --------------------------------------------------------------- LM head
+
+HeadDesc head_shape(const dflash_dims& d, int S, int block, int mode) {
+  HeadDesc h;
+  memset(&h, 0, sizeof(h));
+  h.dtype = d.dtype;
+  h.M = S * block;
+  h.H = d.hidden;
+  h.V = d.vocab;
+  h.n_seqs = S;
+  h.block = block;
+  h.mode = mode;
+  return h;
+}
+
+// Measure or carve the whole draft call.
+struct DraftScratch {
+  float* h;
+  LayerScratch ls;
+  void* xf;
+  void* hpart;
+  int32_t* cand;
+};
+
+LayerShape draft_layer_shape(const dflash_draft_args* a, int j) {
+  LayerShape L;
+  L.d = a->dims;
+  L.S = a->n_seqs;
+  L.rows = a->block;
+  L.mode = DFLASH_ATTN_BLOCK_BIDIR;
+  L.max_pos = a->max_pos;
+  L.cap = a->kv_layers[j].capacity;
+  L.window = a->kv_layers[j].window;
+  return L;
+}
+
+size_t carve_draft(Bump& b, const dflash_draft_args* a, int sms, DraftScratch& s) {
+  const dflash_dims& d = a->dims;
+  const size_t M = (size_t)a->n_seqs * a->block;
+  b.take(kReservedBytes);
+  s.h = static_cast<float*>(b.take(M * d.hidden * sizeof(float)));
+  // layer scratch carved for the layer geometry that needs the most
+  int jbest = 0;
+  size_t bb = 0;
+  for (int j = 0; j < a->n_layers; ++j) {
+    Bump t(nullptr);
+    LayerScratch tmp;
+    carve_layer(t, draft_layer_shape(a, j), sms, tmp);
+    if (t.off > bb) {
+      bb = t.off;
+      jbest = j;
+    }
+  }
+  carve_layer(b, draft_layer_shape(a, jbest), sms, s.ls);
+  s.xf = b.take(M * d.hidden * elem_size(d.dtype));
+  HeadDesc hd = head_shape(d, a->n_seqs, a->block, a->path_topk > 0 ? 2 : 0);
+  hd.topk = a->path_topk;
+  s.hpart = b.take(head_workspace(hd, sms));
+  s.cand = static_cast<int32_t*>(b.take((size_t)a->n_seqs * a->block * 16 * sizeof(int32_t)));
+  return b.off;
+}
+
+}  // namespace
+
+// =================================================================== ABI
+
+extern "C" {
+
+int32_t dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
+
+const char* dflash_last_error(void) { return g_err; }
+
+int dflash_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin, dflash_stream_t stream) {
+  DF_CHECK(cos_sin != nullptr, "dflash_rope_table: cos_sin is NULL");
+  DF_CHECK(head_dim > 0 && head_dim % 2 == 0 && max_pos > 0 && theta > 0.f,
+           "dflash_rope_table: need theta > 0, even head_dim > 0, max_pos > 0");
+  DF_CUDA(launch_rope_table(theta, head_dim, max_pos, cos_sin, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  DF_CHECK(ws != nullptr && ws_bytes >= kReservedBytes, "dflash_workspace_init: workspace below %zu bytes",
+           kReservedBytes);
+  DF_CUDA(cudaMemsetAsync(ws, 0, kReservedBytes, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status) {
+  DF_CHECK(ws != nullptr && host_status != nullptr, "dflash_read_status: NULL argument");
+  uint32_t v = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  DF_CUDA(cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st));
+  DF_CUDA(cudaStreamSynchronize(st));
+  DF_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st));
+  DF_CUDA(cudaStreamSynchronize(st));
+  *host_status = (v & ST_NUMERIC) ? DFLASH_ERR_NUMERIC : (v & ST_TIMEOUT) ? DFLASH_ERR_TIMEOUT : DFLASH_OK;
+  if (*host_status != DFLASH_OK) fail(*host_status, "device status word 0x%x", v);
+  return DFLASH_OK;
+}
+
+// ----------------------------------------------------------------- embed
+
+int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  DF_CHECK(a != nullptr, "dflash_embed: NULL args");
+  int rc = check_dims(a->dims, "dflash_embed");
+  if (rc) return rc;
+  DF_CHECK(a->embed && a->first && a->h, "dflash_embed: NULL embed/first/h");
+  DF_CHECK(a->n_seqs >= 0 && a->rows > 0, "dflash_embed: bad n_seqs/rows");
+  DF_CHECK(a->rest != nullptr || (a->fill_token >= 0 && a->fill_token < a->dims.vocab),
+           "dflash_embed: fill_token out of range");
+  rc = check_ws(ws, ws_bytes, kReservedBytes, "dflash_embed");
+  if (rc) return rc;
+  DF_CUDA(launch_embed(a->dims.dtype, a->embed, a->dims.hidden, a->n_seqs, a->rows, a->first, a->rest,
+                       a->fill_token, a->h, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// --------------------------------------------------------- decoder layer
+
+static LayerShape layer_shape_of(const dflash_layer_args* a) {
+  LayerShape L;
+  L.d = a->dims;
+  L.S = a->n_seqs;
+  L.rows = a->rows;
+  L.mode = a->attn_mode;
+  L.max_pos = a->max_pos;
+  L.cap = a->kv.capacity;
+  L.window = a->kv.window;
+  return L;
+}
+
+static size_t layer_ws(const dflash_layer_args* a, int sms) {
+  Bump b(nullptr);
+  b.take(kReservedBytes);
+  LayerScratch s;
+  carve_layer(b, layer_shape_of(a), sms, s);
+  return b.off;
+}
+
+int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws_bytes,
+                                 dflash_stream_t stream) {
+  const char* who = "dflash_decoder_layer_forward";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  rc = check_weights(a->w, who);
+  if (rc) return rc;
+  DF_CHECK(a->base_pos && a->h && a->kv.k && a->kv.v && a->rope_cs, "%s: NULL pointer", who);
+  LayerShape L = layer_shape_of(a);
+  rc = check_layer_shape(L, who);
+  if (rc) return rc;
+  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos %d beyond the RoPE table (%d)", who, a->max_pos,
+           a->rope_max_pos);
+  DF_CHECK(!a->tap || (a->tap_stride >= a->dims.hidden && a->tap_offset >= 0 &&
+                        a->tap_offset + a->dims.hidden <= a->tap_stride),
+           "%s: bad tap stride/offset", who);
+  const int sms = num_sms();
+  rc = check_ws(ws, ws_bytes, layer_ws(a, sms), who);
+  if (rc) return rc;
+  Bump b(ws);
+  b.take(kReservedBytes);
+  LayerScratch s;
+  carve_layer(b, L, sms, s);
+  return run_layer(L, a->w, a->kv, a->h, a->base_pos, a->rope_cs, a->rope_max_pos, a->tap, a->tap_stride, a->tap_offset, s,
+                   header(ws), sms, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------- fusion
+
+static size_t fuse_ws(const dflash_fuse_args* a, int sms, float** z, void** cbuf, void** gpart, size_t* gp,
+                      char* base) {
+  const dflash_dims& d = a->dims;
+  const size_t M = (size_t)a->n_seqs * a->rows;
+  Bump b(base);
+  b.take(kReservedBytes);
+  *z = static_cast<float*>(b.take(M * d.hidden * sizeof(float)));
+  *cbuf = b.take(M * d.hidden * elem_size(d.dtype));
+  GemmDesc fc = gemm_base(d.dtype, (int)M, a->n_taps * d.hidden, nullptr, nullptr, nullptr, a->rows);
+  fc.seg_rows = d.hidden;
+  fc.kind = EPI_STORE;
+  GemmDesc kv = gemm_base(d.dtype, (int)M, d.hidden, nullptr, nullptr, nullptr, a->rows);
+  kv.nseg = a->n_layers;
+  kv.seg_row0 = d.n_q_heads * d.head_dim;
+  kv.seg_rows = 2 * d.n_kv_heads * d.head_dim;
+  kv.kind = EPI_QKV;
+  kv.nq = d.n_q_heads;
+  kv.nkv = d.n_kv_heads;
+  kv.d = d.head_dim;
+  *gp = std::max(gemm_scratch_bytes(fc, sms), gemm_scratch_bytes(kv, sms));
+  *gpart = b.take(*gp);
+  return b.off;
+}
+
+int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_fuse_context";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  const dflash_dims& d = a->dims;
+  DF_CHECK(a->n_taps > 0 && a->n_taps <= 16, "%s: n_taps must be in [1, 16]", who);
+  DF_CHECK(a->n_layers > 0 && a->n_layers <= DFLASH_MAX_LAYERS, "%s: n_layers must be in [1, %d]", who,
+           DFLASH_MAX_LAYERS);
+  DF_CHECK(a->w_fc && a->fc_norm && a->feats && a->base_pos && a->rope_cs, "%s: NULL pointer", who);
+  DF_CHECK(a->n_seqs > 0 && a->rows > 0, "%s: n_seqs and rows must be positive", who);
+  const int cap = a->kv_layers[0].capacity, win = a->kv_layers[0].window;
+  for (int j = 0; j < a->n_layers; ++j) {
+    DF_CHECK(a->w_qkv_layers[j] && a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL layer %d pointer", who, j);
+    DF_CHECK(a->kv_layers[j].capacity == cap && a->kv_layers[j].window == win,
+             "%s: every layer's context cache must share capacity and window", who);
+  }
+  DF_CHECK(cap > 0 && (win == 0 || win == cap), "%s: window ring needs capacity == window", who);
+  const int sms = num_sms();
+  float* z;
+  void *cbuf, *gpart;
+  size_t gp;
+  rc = check_ws(ws, ws_bytes, fuse_ws(a, sms, &z, &cbuf, &gpart, &gp, nullptr), who);
+  if (rc) return rc;
+  fuse_ws(a, sms, &z, &cbuf, &gpart, &gp, static_cast<char*>(ws));
+  Ctx c = header(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = a->n_seqs * a->rows;
+
+  GemmDesc fc = gemm_base(d.dtype, M, a->n_taps * d.hidden, a->feats, a->base_pos, a->valid, a->rows);
+  fc.seg_w[0] = a->w_fc;
+  fc.seg_rows = d.hidden;
+  fc.kind = EPI_STORE;
+  fc.out_f32 = z;
+  fc.ldo = d.hidden;
+  DF_CUDA(run_gemm(fc, gpart, gp, c, sms, st));
+  DF_CUDA(launch_rmsnorm(d.dtype, z, a->fc_norm, M, d.hidden, d.rms_eps, cbuf, st));
+  if (a->c_out) DF_CUDA(launch_to_f32(d.dtype, cbuf, (size_t)M * d.hidden, a->c_out, st));
+
+  GemmDesc kv = gemm_base(d.dtype, M, d.hidden, cbuf, a->base_pos, a->valid, a->rows);
+  kv.nseg = a->n_layers;
+  for (int j = 0; j < a->n_layers; ++j) {
+    kv.seg_w[j] = a->w_qkv_layers[j];
+    kv.k_dst[j] = a->kv_layers[j].k;
+    kv.v_dst[j] = a->kv_layers[j].v;
+  }
+  kv.seg_row0 = d.n_q_heads * d.head_dim;
+  kv.seg_rows = 2 * d.n_kv_heads * d.head_dim;
+  kv.kind = EPI_QKV;
+  kv.nq = d.n_q_heads;
+  kv.nkv = d.n_kv_heads;
+  kv.d = d.head_dim;
+  kv.kv_cap = cap;
+  kv.kv_window = win;
+  kv.kv_slot_mode = 1;
+  kv.rope_cs = a->rope_cs;
+  kv.rope_max_pos = a->rope_max_pos;
+  DF_CUDA(run_gemm(kv, gpart, gp, c, sms, st));
+  return DFLASH_OK;
+}
+
+// ----------------------------------------------------------------- draft
+
+int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_draft_block";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  const dflash_dims& d = a->dims;
+  DF_CHECK(a->n_layers > 0 && a->n_layers <= DFLASH_MAX_LAYERS, "%s: n_layers must be in [1, %d]", who,
+           DFLASH_MAX_LAYERS);
+  DF_CHECK(a->block >= 2 && a->n_seqs > 0, "%s: block >= 2 and n_seqs > 0 required", who);
+  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
+  DF_CHECK(a->final_norm && a->embed && a->lm_head && a->anchor && a->base_pos && a->drafts && a->rope_cs,
+           "%s: NULL pointer", who);
+  DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
+  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
+  DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
+  if (a->path_topk > 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "%s: the path selector inside the draft is not available yet", who);
+  if (a->path_topk > 0)
+    DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
+             "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);
+  for (int j = 0; j < a->n_layers; ++j) {
+    rc = check_weights(a->layers[j], who);
+    if (rc) return rc;
+    DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
+    rc = check_layer_shape(draft_layer_shape(a, j), who);
+    if (rc) return rc;
+  }
+  const int sms = num_sms();
+  DraftScratch s;
+  Bump m(nullptr);
+  size_t need = carve_draft(m, a, sms, s);
+  rc = check_ws(ws, ws_bytes, need, who);
+  if (rc) return rc;
+  Bump b(ws);
+  carve_draft(b, a, sms, s);
+  Ctx c = header(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = a->n_seqs * a->block;
+
+  DF_CUDA(launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, nullptr, a->mask_token,
+                       s.h, st));
+  for (int j = 0; j < a->n_layers; ++j) {
+    rc = run_layer(draft_layer_shape(a, j), a->layers[j], a->kv_layers[j], s.h, a->base_pos, a->rope_cs,
+                   a->rope_max_pos, nullptr,
+                   0, 0, s.ls, c, sms, st);
+    if (rc) return rc;
+  }
+  DF_CUDA(launch_rmsnorm(d.dtype, s.h, a->final_norm, M, d.hidden, d.rms_eps, s.xf, st));
+  HeadDesc h = head_shape(d, a->n_seqs, a->block, a->path_topk > 0 ? 2 : 0);
+  h.topk = a->path_topk;
+  h.x = s.xf;
+  h.w = a->lm_head;
+  h.drafts_out = a->drafts;
+  h.cand_out = s.cand;
+  h.logits = a->logits;
+  h.partials = static_cast<float*>(s.hpart);
+  h.counters = c.counters;
+  h.status = c.status;
+  DF_CUDA(launch_head(h, sms, st));
+  if (a->path_topk > 0) {
+    PathDesc p;
+    memset(&p, 0, sizeof(p));
+    p.dtype = d.dtype;
+    p.n_seqs = a->n_seqs;
+    p.block = a->block;
+    p.topk = a->path_topk;
+    p.rank = a->path_rank;
+    p.H = d.hidden;
+    p.embed = a->embed;
+    p.u = a->path_u;
+    p.v = a->path_v;
+    p.anchor = a->anchor;
+    p.cand = s.cand;
+    p.path = a->drafts;
+    DF_CUDA(launch_path_select(p, st));
+  }
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- verify
+
+static size_t verify_ws(const dflash_verify_args* a, int sms, void** xf, void** hpart, char* base) {
+  Bump b(base);
+  b.take(kReservedBytes);
+  const size_t M = (size_t)a->n_seqs * a->block;
+  *xf = b.take(M * a->dims.hidden * elem_size(a->dims.dtype));
+  *hpart = b.take(head_workspace(head_shape(a->dims, a->n_seqs, a->block, 1), sms));
+  return b.off;
+}
+
+int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_verify_accept";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  DF_CHECK(a->n_seqs > 0 && a->block >= 1, "%s: n_seqs > 0 and block >= 1 required", who);
+  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
+  DF_CHECK(a->h && a->final_norm && a->lm_head && a->argmax && a->accept_len && a->out_tokens,
+           "%s: NULL pointer", who);
+  DF_CHECK(a->drafts || a->block == 1, "%s: drafts required when block > 1", who);
+  DF_CHECK(!a->commit_base || a->base_pos, "%s: commit_base needs base_pos", who);
+  const int sms = num_sms();
+  void *xf, *hpart;
+  rc = check_ws(ws, ws_bytes, verify_ws(a, sms, &xf, &hpart, nullptr), who);
+  if (rc) return rc;
+  verify_ws(a, sms, &xf, &hpart, static_cast<char*>(ws));
+  Ctx c = header(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  const dflash_dims& d = a->dims;
+  const int M = a->n_seqs * a->block;
+  DF_CUDA(launch_rmsnorm(d.dtype, a->h, a->final_norm, M, d.hidden, d.rms_eps, xf, st));
+  HeadDesc h = head_shape(d, a->n_seqs, a->block, 1);
+  h.x = xf;
+  h.w = a->lm_head;
+  h.drafts = a->drafts;
+  h.argmax = a->argmax;
+  h.margin = a->margin;
+  h.accept_len = a->accept_len;
+  h.out_tokens = a->out_tokens;
+  h.next_anchor = a->next_anchor;
+  h.base_pos = a->base_pos;
+  h.commit_base = a->commit_base;
+  h.commit_count = a->commit_count;
+  h.logits = a->logits;
+  h.partials = static_cast<float*>(hpart);
+  h.counters = c.counters;
+  h.status = c.status;
+  DF_CUDA(launch_head(h, sms, st));
+  return DFLASH_OK;
+}
+
+// ----------------------------------------------------------- path select
+
+int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_path_select";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  DF_CHECK(a->embed && a->path_u && a->path_v && a->anchor && a->cand && a->path, "%s: NULL pointer", who);
+  DF_CHECK(a->n_seqs > 0 && a->block >= 2 && a->topk > 0 && a->topk <= 16 && a->rank > 0 && a->rank <= 256,
+           "%s: need n_seqs > 0, block >= 2, 0 < topk <= 16, 0 < rank <= 256", who);
+  rc = check_ws(ws, ws_bytes, kReservedBytes, who);
+  if (rc) return rc;
+  PathDesc p;
+  memset(&p, 0, sizeof(p));
+  p.dtype = a->dims.dtype;
+  p.n_seqs = a->n_seqs;
+  p.block = a->block;
+  p.topk = a->topk;
+  p.rank = a->rank;
+  p.H = a->dims.hidden;
+  p.embed = a->embed;
+  p.u = a->path_u;
+  p.v = a->path_v;
+  p.anchor = a->anchor;
+  p.cand = a->cand;
+  p.path = a->path;
+  p.margin = a->margin;
+  DF_CUDA(launch_path_select(p, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------- workspace
+
+size_t dflash_workspace_bytes(int32_t op, const void* args) {
+  if (!args) return 0;
+  const int sms = num_sms();
+  switch (op) {
+    case DFLASH_OP_EMBED:
+    case DFLASH_OP_PATH:
+      return kReservedBytes;
+    case DFLASH_OP_LAYER:
+      return layer_ws(static_cast<const dflash_layer_args*>(args), sms);
+    case DFLASH_OP_FUSE: {
+      float* z;
+      void *cb, *gp;
+      size_t g;
+      return fuse_ws(static_cast<const dflash_fuse_args*>(args), sms, &z, &cb, &gp, &g, nullptr);
+    }
+    case DFLASH_OP_DRAFT: {
+      DraftScratch s;
+      Bump m(nullptr);
+      return carve_draft(m, static_cast<const dflash_draft_args*>(args), sms, s);
+    }
+    case DFLASH_OP_VERIFY: {
+      void *xf, *hp;
+      return verify_ws(static_cast<const dflash_verify_args*>(args), sms, &xf, &hp, nullptr);
+    }
+    default:
+      return 0;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// common.cuh -- device helpers shared by the DFlash kernels (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace dfl {
+
+// Device status word bits (first word of every workspace).
+enum : uint32_t {
+  ST_NUMERIC = 1u,  // NaN reached an argmax
+  ST_TIMEOUT = 2u,  // a bounded wait gave up
+};
+
+// Workspace header: status word + arrival counters of the last-CTA reductions.
+constexpr size_t kHeaderBytes = 256;
+constexpr int kNumCounters = 32768;
+constexpr size_t kCounterBytes = kNumCounters * sizeof(uint32_t);
+constexpr size_t kReservedBytes = kHeaderBytes + kCounterBytes;
+
+// Counter regions (indices into the counter array) per kernel family.
+constexpr int kCtrGemm = 0;        // 8192 tiles
+constexpr int kCtrAttn = 8192;     // 16384 (seq, head, query-tile) groups
+constexpr int kCtrHead = 24576;    // LM-head reduction (1)
+constexpr int kCtrHeadEnd = 24577;
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Round a float to the storage type and back (the value a consumer reads).
+template <typename T>
+__device__ __forceinline__ float round_to(float v) { return to_f<T>(from_f<T>(v)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Load 8 consecutive elements as floats (16-byte aligned for bf16, 2x16 for f32).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&o)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&o)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(b[i]);
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&o)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+// Token row m -> sequence, in-block index and absolute position.
+struct RowMap {
+  const int32_t* base_pos;  // [n_seqs]
+  const int32_t* valid;     // [n_seqs] or null
+  int32_t rows;             // rows per sequence
+  __device__ __forceinline__ int seq(int m) const { return m / rows; }
+  __device__ __forceinline__ int idx(int m) const { return m % rows; }
+  __device__ __forceinline__ int pos(int m) const { return base_pos[m / rows] + m % rows; }
+  __device__ __forceinline__ bool live(int m) const {
+    return valid == nullptr || (m % rows) < valid[m / rows];
+  }
+};
+
+// Programmatic dependent launch: wait for the previous grid's results /
+// allow the next grid to start its independent prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded waits give up after this long and raise ST_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+}  // namespace dfl

@@ -1,0 +1,141 @@
+// internal.h -- launch interface between the C-ABI layer (abi.cu) and the
+// kernel translation units.  Host-side declarations only.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dfl {
+
+enum EpiKind : int32_t {
+  EPI_STORE = 0,   // out_f32[m][n] = acc
+  EPI_RESID = 1,   // out_f32[m][n] += acc
+  EPI_QKV = 2,     // rows = [Q heads | K heads | V heads]: RoPE, then q_out / KV destinations
+  EPI_SWIGLU = 3,  // rows = [gate | up]: act[m][j] = SiLU(gate_j) * up_j
+};
+
+constexpr int kMaxSeg = 16;
+
+// One GEMM problem Y[m][n] = sum_k X[m][k] W[n][k] with a fused epilogue.
+// Several weight segments may share one launch (K/V injection into every
+// draft layer); segment s covers output rows [0, seg_rows) of weight
+// seg_w[s] starting at row seg_row0.
+struct GemmDesc {
+  int dtype;                  // DFLASH_F32 / DFLASH_BF16 (X, W, outputs)
+  int M, K;                   // token rows, reduction length
+  const void* X;              // [M][K]
+  int nseg;
+  const void* seg_w[kMaxSeg]; // weight base pointers ([rows][K])
+  int seg_row0;               // first weight row used in every segment
+  int seg_rows;               // output rows per segment
+  int kind;                   // EpiKind
+  // row map
+  const int32_t* base_pos;
+  const int32_t* valid;
+  int rows;                   // rows per sequence
+  // EPI_STORE / EPI_RESID
+  float* out_f32;
+  int ldo;
+  // EPI_QKV
+  void* q_out;                // [M][nq*d] or null when seg_row0 skips Q
+  int nq, nkv, d;
+  void* k_dst[kMaxSeg];
+  void* v_dst[kMaxSeg];
+  int kv_cap, kv_window;
+  int kv_slot_mode;           // 0: slot = in-block row index (block scratch); 1: slot = position (cache)
+  const float* rope_cs;
+  int rope_max_pos;
+  // EPI_SWIGLU
+  void* act_out;              // [M][inter]
+  int inter;
+};
+
+// Attention problem (see dflash_decoder_layer_forward).
+struct AttnDesc {
+  int dtype;
+  int mode;                   // dflash_attn_mode
+  int n_seqs, rows, nq, nkv, d;
+  const int32_t* base_pos;
+  const void* q;              // [M][nq*d]
+  const void* kc;             // cache [S][nkv][cap][d]
+  const void* vc;
+  int cap, window;
+  const void* kb;             // block scratch [S][nkv][rows][d] (bidir)
+  const void* vb;
+  void* out;                  // [M][nq*d]
+  int max_pos;                // bound on base_pos + rows
+  float* partials;            // workspace
+  uint32_t* counters;
+  uint32_t* status;
+};
+
+struct HeadDesc {
+  int dtype;
+  int M, H, V;
+  const void* x;              // [M][H] normalised, rounded
+  const void* w;              // [V][H]
+  int n_seqs, block;
+  int mode;                   // 0: draft (argmax rows 1..block-1 -> drafts), 1: verify, 2: draft top-k
+  int topk;
+  const int32_t* drafts;      // verify
+  int32_t* drafts_out;        // draft
+  int32_t* argmax;            // verify
+  float* margin;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  int32_t* next_anchor;
+  int32_t* base_pos;
+  int32_t* commit_base;
+  int32_t* commit_count;
+  int32_t* cand_out;          // top-k mode [S][block-1][topk]
+  float* logits;              // optional [M][V] (draft: rows 1.. only written)
+  float* partials;            // workspace
+  uint32_t* counters;
+  uint32_t* status;
+};
+
+struct PathDesc {
+  int dtype;
+  int n_seqs, block, topk, rank, H;
+  const void* embed;
+  const void* u;
+  const void* v;
+  const int32_t* anchor;
+  const int32_t* cand;
+  int32_t* path;
+  float* margin;
+};
+
+// elementwise
+cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaStream_t st);
+cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, const int32_t* first,
+                         const int32_t* rest, int fill, float* h, cudaStream_t st);
+cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int H, float eps,
+                           void* x_out, cudaStream_t st);
+cudaError_t launch_to_f32(int dtype, const void* src, size_t n, float* dst, cudaStream_t st);
+cudaError_t launch_store_tap(int dtype, const float* h, int M, int H, void* tap, int stride,
+                             int offset, cudaStream_t st);
+
+// GEMM (SIMT path; fp32 and bf16)
+cudaError_t launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
+int gemm_out_rows(const GemmDesc& g);
+
+// GEMM (tcgen05 path; bf16).  ws/ws_bytes: split-K partials; counters.
+size_t gemm_tc_workspace(const GemmDesc& g, int num_sms);
+cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
+                           uint32_t* status, int num_sms, cudaStream_t st);
+bool gemm_tc_supported(const GemmDesc& g);
+
+// attention
+size_t attn_workspace(const AttnDesc& a);
+cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st);
+
+// LM head + argmax / accept / top-k
+size_t head_workspace(const HeadDesc& h, int num_sms);
+cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st);
+cudaError_t launch_head_simt(const HeadDesc& h, int num_sms, cudaStream_t st);
+
+// path selector
+cudaError_t launch_path_select(const PathDesc& p, cudaStream_t st);
+
+}  // namespace dfl

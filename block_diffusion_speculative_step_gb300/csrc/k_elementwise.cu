@@ -1,0 +1,125 @@
+// k_elementwise.cu -- RoPE table, embedding gather, RMSNorm, tap store.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfl {
+
+// cos_sin[p][i] = (cos(p w_i), sin(p w_i)), w_i = theta^(-2i/d), evaluated in
+// double so large positions keep full float accuracy.
+__global__ void rope_table_kernel(double theta, int d, int max_pos, float* cs) {
+  int half = d / 2;
+  long n = (long)max_pos * half;
+  for (long t = blockIdx.x * (long)blockDim.x + threadIdx.x; t < n; t += (long)gridDim.x * blockDim.x) {
+    int p = (int)(t / half), i = (int)(t % half);
+    double w = pow(theta, -2.0 * (double)i / (double)d);
+    double a = (double)p * w;
+    cs[2 * t] = (float)cos(a);
+    cs[2 * t + 1] = (float)sin(a);
+  }
+}
+
+cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaStream_t st) {
+  long n = (long)max_pos * (d / 2);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  rope_table_kernel<<<blocks, 256, 0, st>>>((double)theta, d, max_pos, cs);
+  return cudaGetLastError();
+}
+
+// h[m][:] = E[token(m)][:] as fp32.
+template <typename T>
+__global__ void embed_kernel(const T* __restrict__ E, int H, int rows, const int32_t* __restrict__ first,
+                             const int32_t* __restrict__ rest, int fill, float* __restrict__ h) {
+  int m = blockIdx.x;
+  int s = m / rows, i = m % rows;
+  int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
+  const T* e = E + (size_t)tok * H;
+  float* o = h + (size_t)m * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = to_f<T>(e[k]);
+}
+
+cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, const int32_t* first,
+                         const int32_t* rest, int fill, float* h, cudaStream_t st) {
+  int M = n_seqs * rows;
+  if (M == 0) return cudaSuccess;
+  if (dtype == DFLASH_BF16)
+    embed_kernel<__nv_bfloat16><<<M, 256, 0, st>>>((const __nv_bfloat16*)E, H, rows, first, rest, fill, h);
+  else
+    embed_kernel<float><<<M, 256, 0, st>>>((const float*)E, H, rows, first, rest, fill, h);
+  return cudaGetLastError();
+}
+
+// x[m] = round(h[m] * rsqrt(mean(h[m]^2) + eps) * g), one block per row.  The
+// sum of squares runs in a fixed order (per-thread strided partials, then a
+// fixed reduction tree), so a row's result does not depend on M.
+template <typename T>
+__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, int H, float eps,
+                               T* __restrict__ x) {
+  __shared__ float red[32];
+  const float* r = h + (size_t)blockIdx.x * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) ss += r[k] * r[k];
+  ss = warp_sum(ss);
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = ss;
+  __syncthreads();
+  if (w == 0) {
+    float v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+    v = warp_sum(v);
+    if (l == 0) red[0] = v;
+  }
+  __syncthreads();
+  float inv = rsqrtf(red[0] / (float)H + eps);
+  T* o = x + (size_t)blockIdx.x * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f<T>(r[k] * inv * to_f<T>(g[k]));
+}
+
+cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int H, float eps, void* x,
+                           cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  if (dtype == DFLASH_BF16)
+    rmsnorm_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(h, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)x);
+  else
+    rmsnorm_kernel<float><<<M, 256, 0, st>>>(h, (const float*)g, H, eps, (float*)x);
+  return cudaGetLastError();
+}
+
+// tap[m*stride + offset + k] = round(h[m][k]).
+template <typename T>
+__global__ void store_tap_kernel(const float* __restrict__ h, int H, T* __restrict__ tap, int stride,
+                                 int offset) {
+  const float* r = h + (size_t)blockIdx.x * H;
+  T* o = tap + (size_t)blockIdx.x * stride + offset;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f<T>(r[k]);
+}
+
+cudaError_t launch_store_tap(int dtype, const float* h, int M, int H, void* tap, int stride, int offset,
+                             cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  if (dtype == DFLASH_BF16)
+    store_tap_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(h, H, (__nv_bfloat16*)tap, stride, offset);
+  else
+    store_tap_kernel<float><<<M, 256, 0, st>>>(h, H, (float*)tap, stride, offset);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void to_f32_kernel(const T* __restrict__ src, size_t n, float* __restrict__ dst) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = to_f<T>(src[i]);
+}
+
+cudaError_t launch_to_f32(int dtype, const void* src, size_t n, float* dst, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  if (dtype == DFLASH_BF16)
+    to_f32_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)src, n, dst);
+  else
+    to_f32_kernel<float><<<blocks, 256, 0, st>>>((const float*)src, n, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -1,0 +1,319 @@
+/*
+ * dflash.h -- C ABI of the GB300 (sm_103a) DFlash draft-and-verify library.
+ *
+ * One DFlash cycle ("DFlash: block-diffusion accelerated LLM speculative
+ * decoding" guide, section 4 "how one task flows through the system"):
+ *   1. context-feature fusion + KV injection      -> dflash_fuse_context
+ *   2. single-step block-diffusion draft forward   -> dflash_draft_block
+ *   3. causal target forward over the block        -> dflash_embed +
+ *                                                     dflash_decoder_layer_forward (per layer)
+ *   4. greedy verification + prefix acceptance     -> dflash_verify_accept
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers unless a field says "host".
+ *    The caller owns every buffer (weights, caches, activations, outputs and
+ *    the workspace); the library allocates nothing and keeps no state beyond
+ *    a thread-local error string.
+ *  - Every call is asynchronous on the caller's `stream` and does no host
+ *    synchronisation, except dflash_read_status.  Argument checks happen on
+ *    the host before any launch; a failed check launches nothing.
+ *  - Return value: DFLASH_OK (0) or a negative dflash_status.  On failure
+ *    dflash_last_error() describes the cause.
+ *  - Element type: dims.dtype selects bf16 or fp32 for weights, KV caches,
+ *    tap features and the projection inputs; the residual stream `h` and
+ *    logits are always fp32.
+ *  - Weights are row-major [out][in].  A decoder layer's weights are
+ *      w_qkv  [(n_q + 2 n_kv) * head_dim][hidden]   rows W_q, then W_k, then W_v
+ *      w_o    [hidden][n_q * head_dim]
+ *      w_gu   [2 * intermediate][hidden]            rows W_gate, then W_up
+ *      w_down [hidden][intermediate]
+ *      ln1, ln2 [hidden]                            RMSNorm gains
+ *  - A KV cache of one layer is [n_seqs][n_kv][capacity][head_dim]; key
+ *    vectors are stored already rotated (RoPE at their absolute position).
+ *    Slots never written must hold finite values: zero-initialise caches.
+ *  - A batch is n_seqs sequences of `rows` consecutive positions each: row i
+ *    of sequence s sits at absolute position base_pos[s] + i and is row
+ *    s*rows + i of every [M][...] activation (M = n_seqs * rows).
+ *  - Workspace: every call takes (ws, ws_bytes).  Size it with
+ *    dflash_workspace_bytes and zero it once with dflash_workspace_init; the
+ *    library keeps it consistent afterwards.  Calls that share a workspace
+ *    must be ordered on one stream.  Its first bytes hold the device status
+ *    word that kernels raise on a numeric fault or an expired bounded wait.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_ABI_VERSION 1
+#define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
+
+typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = -1, /* null pointer, bad size, inconsistent shapes */
+  DFLASH_ERR_UNSUPPORTED = -2, /* shape/dtype/device the kernels do not cover */
+  DFLASH_ERR_WORKSPACE = -3,   /* ws_bytes below dflash_workspace_bytes */
+  DFLASH_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+  DFLASH_ERR_TIMEOUT = -5,     /* a bounded device wait gave up (status word) */
+  DFLASH_ERR_NUMERIC = -6      /* NaN reached an argmax (status word) */
+} dflash_status;
+
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+
+typedef enum {
+  DFLASH_ATTN_CAUSAL = 0,     /* target verification: row i sees cache slots 0..pos_i */
+  DFLASH_ATTN_BLOCK_BIDIR = 1 /* draft block: every row sees the context and the whole block */
+} dflash_attn_mode;
+
+typedef enum {
+  DFLASH_OP_EMBED = 0,
+  DFLASH_OP_LAYER = 1,
+  DFLASH_OP_FUSE = 2,
+  DFLASH_OP_DRAFT = 3,
+  DFLASH_OP_VERIFY = 4,
+  DFLASH_OP_PATH = 5
+} dflash_op;
+
+/* Shapes and arithmetic of one decoder stack. */
+typedef struct {
+  int32_t hidden;       /* H */
+  int32_t n_q_heads;    /* query heads */
+  int32_t n_kv_heads;   /* key/value heads; n_q_heads % n_kv_heads == 0 */
+  int32_t head_dim;     /* 64 or 128 */
+  int32_t intermediate; /* SwiGLU width I */
+  int32_t vocab;        /* V (shared embedding / LM head rows) */
+  float rope_theta;     /* RoPE base (rotate-half pairing) */
+  float rms_eps;        /* RMSNorm epsilon */
+  int32_t dtype;        /* dflash_dtype */
+} dflash_dims;
+
+/* One layer's KV cache: k, v each [n_seqs][n_kv][capacity][head_dim]. */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t capacity; /* slots per (sequence, kv head) */
+  int32_t window;   /* 0: slot = position.  >0: ring of `window` slots
+                       (capacity == window), slot = position % window; the
+                       draft then sees the last `window` positions only. */
+} dflash_kv;
+
+typedef struct {
+  const void* w_qkv;
+  const void* w_o;
+  const void* w_gu;
+  const void* w_down;
+  const void* ln1;
+  const void* ln2;
+} dflash_layer_weights;
+
+/*
+ * RoPE table: cos_sin[p][i] = (cos(p * w_i), sin(p * w_i)), w_i =
+ * theta^(-2i/head_dim), i < head_dim/2, p < max_pos, computed on the device
+ * in double and stored as float pairs ([max_pos][head_dim/2][2] floats).
+ * Every call that applies RoPE reads it.
+ */
+int dflash_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin,
+                      dflash_stream_t stream);
+
+/*
+ * Token embedding (shared embedding, "DFlash ..." guide section 3.1: the
+ * draft reuses the target's embedding and LM head).  Row i of sequence s
+ * takes token first[s] for i == 0 and rest[s*(rows-1) + i-1] for i >= 1,
+ * or fill_token when rest == NULL (the draft's mask tokens).
+ * h[M][H] (fp32) receives the embedding rows.
+ */
+typedef struct {
+  dflash_dims dims;
+  const void* embed;     /* [V][H] */
+  int32_t n_seqs, rows;
+  const int32_t* first;  /* [n_seqs] */
+  const int32_t* rest;   /* [n_seqs][rows-1] or NULL */
+  int32_t fill_token;
+  float* h;              /* out [M][H] */
+} dflash_embed_args;
+int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * One pre-norm decoder layer, shared by the draft and the target:
+ *   x = RMSNorm(h; ln1); q,k,v = x W_qkv^T; RoPE(q, k) at each row's position;
+ *   o = GQA softmax attention; h += o W_o^T;
+ *   x = RMSNorm(h; ln2); h += (SiLU(x W_gate^T) * (x W_up^T)) W_down^T.
+ * DFLASH_ATTN_CAUSAL ("DFlash ..." guide 3.3, target verification): the
+ *   rows' K/V are first written to kv at slot = position, then row i attends
+ *   slots 0 .. base_pos[s] + i.  kv.window must be 0.
+ * DFLASH_ATTN_BLOCK_BIDIR (guide 3.1/3.2, draft block): kv holds the
+ *   injected context of positions < base_pos[s] (the last kv.window of them
+ *   with a window); every row attends all of those plus every row of its own
+ *   block, no mask.  The block's K/V are not stored in kv.
+ * tap (optional): writes the layer's output residual, rounded to dims.dtype,
+ *   to tap[row * tap_stride + tap_offset + j] (feature taps for fusion).
+ * max_pos: host-side bound with base_pos[s] + rows <= max_pos for every s
+ *   (sizes the attention grid; also must not exceed the RoPE table).
+ */
+typedef struct {
+  dflash_dims dims;
+  dflash_layer_weights w;
+  int32_t n_seqs, rows;
+  const int32_t* base_pos; /* [n_seqs] */
+  float* h;                /* in/out [M][H] fp32 residual stream */
+  dflash_kv kv;
+  int32_t attn_mode;       /* dflash_attn_mode */
+  int32_t max_pos;
+  const float* rope_cs;    /* dflash_rope_table output */
+  int32_t rope_max_pos;
+  void* tap;               /* optional */
+  int32_t tap_stride, tap_offset;
+} dflash_layer_args;
+int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws_bytes,
+                                 dflash_stream_t stream);
+
+/*
+ * Context-feature fusion + KV injection ("DFlash ..." guide 3.2 and FAQ Q2;
+ * "DFlash 2 release" news, "KV injection"): for row i < valid[s] of
+ * sequence s, at position t = base_pos[s] + i, with tap features
+ * f = feats[row] ([F][H], taps in increasing layer order):
+ *     c_t = RMSNorm(W_fc f; fc_norm)                  (rounded to dims.dtype)
+ *     for every draft layer j: K_j[t] = RoPE(W_k^j c_t, t), V_j[t] = W_v^j c_t
+ * written into kv_layers[j] at slot(t).  W_k^j, W_v^j are the K and V row
+ * blocks of w_qkv_layers[j].  Rows with i >= valid[s] are skipped (valid ==
+ * NULL: all rows).  c_out (optional, [M][H] fp32) receives c_t.
+ */
+typedef struct {
+  dflash_dims dims;                         /* draft dims */
+  int32_t n_taps;                           /* F */
+  const void* w_fc;                         /* [H][F*H] */
+  const void* fc_norm;                      /* [H] */
+  int32_t n_layers;                         /* <= DFLASH_MAX_LAYERS */
+  const void* w_qkv_layers[DFLASH_MAX_LAYERS];
+  dflash_kv kv_layers[DFLASH_MAX_LAYERS];
+  const void* feats;                        /* [M][F][H] */
+  int32_t n_seqs, rows;
+  const int32_t* base_pos;                  /* [n_seqs] */
+  const int32_t* valid;                     /* [n_seqs] or NULL */
+  const float* rope_cs;
+  int32_t rope_max_pos;
+  float* c_out;                             /* optional */
+} dflash_fuse_args;
+int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes,
+                        dflash_stream_t stream);
+
+/*
+ * Single-step block-diffusion draft ("DFlash ..." guide 3.1): the block is
+ * [anchor[s], mask, ..., mask] at positions base_pos[s] .. base_pos[s]+block-1;
+ * embed -> every draft layer in DFLASH_ATTN_BLOCK_BIDIR mode over its
+ * injected context -> RMSNorm(final_norm) -> shared LM head -> greedy argmax.
+ * Row j >= 1 predicts the token at position base_pos[s] + j:
+ * drafts[s*(block-1) + j-1] = argmax of row j (lowest index on ties).
+ * With path_topk > 0 the DFlash 2 path selector (dflash_path_select) replaces
+ * the drafts by its greedy path over each row's top-path_topk candidates.
+ * logits (optional, [n_seqs][block-1][V] fp32) receives rows 1..block-1.
+ */
+typedef struct {
+  dflash_dims dims;
+  int32_t n_layers;
+  dflash_layer_weights layers[DFLASH_MAX_LAYERS];
+  dflash_kv kv_layers[DFLASH_MAX_LAYERS];
+  const void* final_norm;                 /* [H] */
+  const void* embed;                      /* [V][H] */
+  const void* lm_head;                    /* [V][H] */
+  int32_t n_seqs, block;
+  const int32_t* anchor;                  /* [n_seqs] */
+  const int32_t* base_pos;                /* [n_seqs] */
+  int32_t mask_token;
+  int32_t max_pos;
+  const float* rope_cs;
+  int32_t rope_max_pos;
+  int32_t* drafts;                        /* out [n_seqs][block-1] */
+  float* logits;                          /* optional */
+  int32_t path_topk;                      /* 0 = off, else <= 16 */
+  int32_t path_rank;                      /* R of path_u / path_v */
+  const void* path_u;                     /* [R][H] */
+  const void* path_v;                     /* [R][H] */
+} dflash_draft_args;
+int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/*
+ * Verification + greedy acceptance ("DFlash ..." guide 3.3 and section 4
+ * step 4; "DFlash 2 release" news, prefix example): from the target's last
+ * residual h ([n_seqs*block][H]):
+ *   g[s][i]      = argmax_v (RMSNorm(h[s,i]; final_norm) . lm_head[v])
+ *   accept_len[s]= largest k <= block-1 with drafts[s][j-1] == g[s][j-1] for all j <= k
+ *   out_tokens[s]= drafts[s][0..k-1], then the bonus g[s][k]
+ * Ties go to the lowest vocab index; margin = top1 - top2 logit.  A NaN
+ * logit raises DFLASH_ERR_NUMERIC in the status word.  drafts may be NULL
+ * only when block == 1 (plain greedy decoding).
+ * State update (each optional): next_anchor[s] = g[s][k];
+ * commit_base[s] = base_pos[s]; commit_count[s] = k + 1;
+ * base_pos[s] += k + 1.
+ */
+typedef struct {
+  dflash_dims dims;
+  const float* h;            /* [n_seqs*block][H] */
+  const void* final_norm;    /* [H] */
+  const void* lm_head;       /* [V][H] */
+  int32_t n_seqs, block;
+  const int32_t* drafts;     /* [n_seqs][block-1] */
+  int32_t* argmax;           /* out [n_seqs][block] */
+  float* margin;             /* out [n_seqs][block], optional */
+  int32_t* accept_len;       /* out [n_seqs] */
+  int32_t* out_tokens;       /* out [n_seqs][block] */
+  int32_t* next_anchor;      /* optional */
+  int32_t* base_pos;         /* optional in/out */
+  int32_t* commit_base;      /* optional */
+  int32_t* commit_count;     /* optional */
+  float* logits;             /* optional [n_seqs][block][V] */
+} dflash_verify_args;
+int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
+                         dflash_stream_t stream);
+
+/*
+ * DFlash 2 path selector, greedy walk ("DFlash ..." guide section 7): for
+ * block rows j = 1..block-1 with candidate lists cand[s][j-1][0..topk-1]
+ * (ranked by draft logit, best first), score(a -> b) = (U e_a) . (V e_b)
+ * over the shared embedding rows e; p_0 = anchor[s]; p_j = the candidate of
+ * row j with the highest score from p_{j-1} (lower rank on ties).
+ * path[s][j-1] = p_j; margin (optional) = best - second-best score.
+ */
+typedef struct {
+  dflash_dims dims;
+  int32_t n_seqs, block, topk, rank;
+  const void* embed;       /* [V][H] */
+  const void* path_u;      /* [R][H] */
+  const void* path_v;      /* [R][H] */
+  const int32_t* anchor;   /* [n_seqs] */
+  const int32_t* cand;     /* [n_seqs][block-1][topk] */
+  int32_t* path;           /* out [n_seqs][block-1] */
+  float* margin;           /* optional out [n_seqs][block-1] */
+} dflash_path_args;
+int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/* Bytes of workspace `op` needs for these arguments (args points to the
+ * op's argument struct); 0 on invalid arguments. */
+size_t dflash_workspace_bytes(int32_t op, const void* args);
+
+/* Zero a workspace (status word and the library's arrival counters). */
+int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace's device status word.
+ * *host_status receives DFLASH_OK or the first error raised on the device. */
+int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
+
+/* Thread-local description of the last failure. */
+const char* dflash_last_error(void);
+
+int32_t dflash_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */

@@ -1,0 +1,102 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/dflash.h declares, its ctypes mirrors match the C struct layouts, and
+host-side argument checks fail cleanly before any launch."""
+import ctypes as C
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def D():
+    from block_diffusion_speculative_step_gb300 import build
+    build.build()
+    import torch  # noqa: F401  (loads the shared CUDA runtime first, as in use)
+    from block_diffusion_speculative_step_gb300 import dflash
+    return dflash
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(dflash_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_match_header(D):
+    declared = header_functions()
+    assert set(declared) == set(D.EXPORTS), (declared, D.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", D._build.LIB], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for name in declared:
+        assert name in exported, name
+        getattr(D.lib(), name)
+
+
+def test_abi_version(D):
+    v = int(re.search(r"#define DFLASH_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert D.dflash_abi_version() == v
+
+
+def test_struct_layouts_match_c(D):
+    structs = ["dflash_dims", "dflash_kv", "dflash_layer_weights", "dflash_embed_args", "dflash_layer_args",
+               "dflash_fuse_args", "dflash_draft_args", "dflash_verify_args", "dflash_path_args"]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void) {"]
+    for s in structs:
+        lines.append(f'  printf("{s} %zu\\n", sizeof({s}));')
+        for fname, _ in getattr(D, s)._fields_:
+            lines.append(f'  printf("{s}.{fname} %zu\\n", offsetof({s}, {fname}));')
+    lines.append("  return 0; }")
+    with tempfile.TemporaryDirectory() as td:
+        src = os.path.join(td, "l.c")
+        exe = os.path.join(td, "l")
+        open(src, "w").write("\n".join(lines))
+        subprocess.check_call(["gcc", "-o", exe, src])
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    ref = dict(l.rsplit(" ", 1) for l in out.splitlines())
+    for s in structs:
+        cls = getattr(D, s)
+        assert C.sizeof(cls) == int(ref[s]), s
+        for fname, _ in cls._fields_:
+            assert getattr(cls, fname).offset == int(ref[f"{s}.{fname}"]), f"{s}.{fname}"
+
+
+def test_invalid_arguments_fail_before_launch(D):
+    L = D.lib()
+    # NULL argument structs
+    for name in ("dflash_embed", "dflash_decoder_layer_forward", "dflash_fuse_context", "dflash_draft_block",
+                 "dflash_verify_accept", "dflash_path_select"):
+        assert getattr(L, name)(None, None, 0, None) == D.DFLASH_ERR_INVALID_ARG
+        assert "NULL args" in D.dflash_last_error()
+    # bad dims
+    a = D.dflash_embed_args()
+    a.dims = D.dflash_dims(256, 4, 3, 64, 512, 1000, 1e4, 1e-6, D.DFLASH_BF16)  # 4 % 3 != 0
+    assert L.dflash_embed(C.byref(a), None, 0, None) == D.DFLASH_ERR_INVALID_ARG
+    assert "n_kv_heads" in D.dflash_last_error()
+    a.dims = D.dflash_dims(256, 4, 2, 96, 512, 1000, 1e4, 1e-6, D.DFLASH_BF16)
+    assert L.dflash_embed(C.byref(a), None, 0, None) == D.DFLASH_ERR_INVALID_ARG
+    assert "head_dim" in D.dflash_last_error()
+    # workspace too small
+    a.dims = D.dflash_dims(256, 4, 2, 64, 512, 1000, 1e4, 1e-6, D.DFLASH_BF16)
+    a.embed, a.first, a.h = 16, 16, 16
+    a.n_seqs, a.rows, a.fill_token = 1, 4, 3
+    assert L.dflash_embed(C.byref(a), C.c_void_p(256), 16, None) == D.DFLASH_ERR_WORKSPACE
+    # verify needs drafts when block > 1
+    v = D.dflash_verify_args()
+    v.dims = a.dims
+    v.h = v.final_norm = v.lm_head = v.argmax = v.accept_len = v.out_tokens = 16
+    v.n_seqs, v.block = 1, 4
+    assert L.dflash_verify_accept(C.byref(v), C.c_void_p(256), 1 << 30, None) == D.DFLASH_ERR_INVALID_ARG
+    assert "drafts" in D.dflash_last_error()
+    # workspace sizing is positive for a valid request
+    assert D.dflash_workspace_bytes(D.DFLASH_OP_EMBED, a) > 0
+
+
+def test_binding_raises(D):
+    with pytest.raises(D.DFlashError) as e:
+        D.dflash_embed(D.dflash_embed_args(), 0, 0, stream=0)
+    assert e.value.code == D.DFLASH_ERR_INVALID_ARG

@@ -1,0 +1,251 @@
+"""GPU parity: every step of the cycle through the C ABI against the CPU
+oracle on the same seeded inputs (element by element; integers bit-exact,
+near-ties reported), plus the lossless invariants end to end."""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_step_gb300 import dflash as D
+from block_diffusion_speculative_step_gb300 import synth
+from oracle import oracle as O
+from tests import gpu_common as G
+from tests import helpers as Hh
+
+pytestmark = pytest.mark.gpu
+
+
+def small(dtype, d=64, **kw):
+    base = dict(dtype=dtype, H=256, nq=4, nkv=2, d=d, I=384, V=1000, t_layers=3, d_layers=2, taps=(0, 1),
+                block=8)
+    base.update(kw)
+    return Hh.small_workload(**base)
+
+
+def rand_cache(eng, layer_k, layer_v, S, upto, seed, cfg):
+    """Fill cache slots [0, upto) with rounded N(0,1) values; returns float64 copies."""
+    g = torch.Generator().manual_seed(seed)
+    shp = layer_k.shape
+    k = torch.randn(shp[0], shp[1], upto, shp[3], generator=g)
+    v = torch.randn(shp[0], shp[1], upto, shp[3], generator=g)
+    layer_k[:, :, :upto] = k.to(layer_k.dtype).cuda()
+    layer_v[:, :, :upto] = v.to(layer_v.dtype).cuda()
+    return G.f64(layer_k), G.f64(layer_v)
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128)])
+def test_causal_layer(dtype, d):
+    w = small(dtype, d=d)
+    S, rows = 2, 8
+    eng, om, _ = G.setup(w, S=S, cap=128)
+    c, L = om.target.cfg, om.target.layers[1]
+    base = [5, 37]
+    eng.base_pos.copy_(torch.tensor(base, dtype=torch.int32))
+    kc, vc = rand_cache(eng, eng.caches.tk[1], eng.caches.tv[1], S, 37, 1, c)
+    h0 = torch.randn(S * rows, w.target.hidden, generator=torch.Generator().manual_seed(2))
+    h = h0.cuda().contiguous()
+    eng.h[:S * rows].copy_(h)
+    D.dflash_decoder_layer_forward(eng.target_layer_args(1, rows, eng.h), eng.ws_ptr, eng.ws_bytes)
+    got = G.f64(eng.h[:S * rows])
+    tol = 1e-4 if dtype == "f32" else 2e-2
+    for s in range(S):
+        hs = h0[s * rows:(s + 1) * rows].double().numpy().copy()
+        kcs, vcs = kc[s].copy(), vc[s].copy()
+        O.decoder_layer(c, L, hs, base[s], O.CAUSAL, kcs, vcs)
+        np.testing.assert_allclose(got[s * rows:(s + 1) * rows], hs, rtol=0, atol=tol)
+        gk = G.f64(eng.caches.tk[1][s, :, base[s]:base[s] + rows])
+        np.testing.assert_allclose(gk, kcs[:, base[s]:base[s] + rows], rtol=1e-2 if dtype == "bf16" else 1e-5,
+                                   atol=1e-2 if dtype == "bf16" else 1e-5)
+
+
+@pytest.mark.parametrize("dtype,window", [("f32", 0), ("bf16", 0), ("bf16", 48)])
+def test_bidir_layer(dtype, window):
+    w = small(dtype, window=window)
+    S, rows = 2, w.block
+    eng, om, _ = G.setup(w, S=S, cap=160)
+    c, L = om.draft.cfg, om.draft.layers[0]
+    base = [3, 100]
+    eng.base_pos.copy_(torch.tensor(base, dtype=torch.int32))
+    dcap = eng.dcap
+    kc, vc = rand_cache(eng, eng.caches.dk[0], eng.caches.dv[0], S, dcap, 3, c)
+    h0 = torch.randn(S * rows, w.draft.hidden, generator=torch.Generator().manual_seed(4))
+    eng.h[:S * rows].copy_(h0.cuda())
+    a = D.dflash_layer_args()
+    a.dims = eng.ddims
+    a.w = __import__("block_diffusion_speculative_step_gb300.engine", fromlist=["x"]).layer_weights(
+        eng.m["draft"]["layers"][0])
+    a.n_seqs, a.rows = S, rows
+    a.base_pos = eng.base_pos.data_ptr()
+    a.h = eng.h.data_ptr()
+    a.kv = D.dflash_kv(eng.caches.dk[0].data_ptr(), eng.caches.dv[0].data_ptr(), dcap, window)
+    a.attn_mode = D.DFLASH_ATTN_BLOCK_BIDIR
+    a.max_pos = eng.cap
+    a.rope_cs = eng.rope_d.data_ptr()
+    a.rope_max_pos = eng.rope_max
+    ws = torch.zeros(D.dflash_workspace_bytes(D.DFLASH_OP_LAYER, a) + 256, dtype=torch.uint8, device="cuda")
+    D.dflash_decoder_layer_forward(a, ws.data_ptr(), ws.numel())
+    got = G.f64(eng.h[:S * rows])
+    tol = 1e-4 if dtype == "f32" else 2e-2
+    for s in range(S):
+        hs = h0[s * rows:(s + 1) * rows].double().numpy().copy()
+        O.decoder_layer(c, L, hs, base[s], O.BIDIR, kc[s].copy(), vc[s].copy(), window)
+        np.testing.assert_allclose(got[s * rows:(s + 1) * rows], hs, rtol=0, atol=tol)
+
+
+@pytest.mark.parametrize("dtype,window", [("f32", 0), ("bf16", 0), ("bf16", 16)])
+def test_fuse_context(dtype, window):
+    w = small(dtype, window=window)
+    S, rows = 2, 6
+    eng, om, m = G.setup(w, S=S, cap=64)
+    base = [0, 20]
+    valid = [6, 3]
+    eng.base_pos.copy_(torch.tensor(base, dtype=torch.int32))
+    vld = torch.tensor(valid, dtype=torch.int32, device="cuda")
+    F, H = len(w.taps), w.draft.hidden
+    feats = synth.make_features(5, S * rows, F, H, synth.torch_dtype(w))
+    eng.feats[:S * rows].copy_(feats.cuda())
+    cout = torch.zeros(S * rows, H, device="cuda")
+    a = eng.fuse_args(rows, eng.feats, eng.base_pos, vld)
+    a.c_out = cout.data_ptr()
+    D.dflash_fuse_context(a, eng.ws_ptr, eng.ws_bytes)
+    torch.cuda.synchronize()
+    d = om.draft
+    for s in range(S):
+        st = O.new_state(om, 64)
+        f = G.f64(feats[s * rows:s * rows + valid[s]].reshape(valid[s], F * H))
+        pos = list(range(base[s], base[s] + valid[s]))
+        cref = O.fuse(om, st, f, pos)
+        np.testing.assert_allclose(G.f64(cout[s * rows:s * rows + valid[s]]), cref, rtol=0,
+                                   atol=1e-4 if dtype == "f32" else 3e-2)
+        for j in range(w.draft.layers):
+            for t in pos:
+                slot = t % window if window else t
+                gk = G.f64(eng.caches.dk[j][s, :, slot])
+                gv = G.f64(eng.caches.dv[j][s, :, slot])
+                tol = 1e-4 if dtype == "f32" else 3e-2
+                np.testing.assert_allclose(gk, st.dk[j][:, slot], rtol=0, atol=tol)
+                np.testing.assert_allclose(gv, st.dv[j][:, slot], rtol=0, atol=tol)
+        # rows beyond valid[s] were not injected
+        if valid[s] < rows:
+            t = base[s] + valid[s]
+            slot = t % window if window else t
+            assert float(eng.caches.dk[0][s, :, slot].abs().sum()) == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_verify_accept(dtype):
+    w = small(dtype, V=1000)
+    S, B = 3, w.block
+    eng, om, _ = G.setup(w, S=S, cap=64)
+    H = w.target.hidden
+    h0 = torch.randn(S * B, H, generator=torch.Generator().manual_seed(6))
+    eng.h[:S * B].copy_(h0.cuda())
+    x = O.final_norm(om.target.cfg, h0.double().numpy(), om.target.g_final)
+    am, mg, lg = O.lm_head_argmax(om.target.cfg, om.Wlm, x, True)
+    am = am.reshape(S, B)
+    # plant drafts: seq 0 all agree, seq 1 agrees for 3, seq 2 none
+    drafts = np.zeros((S, B - 1), dtype=np.int32)
+    drafts[0] = am[0, :B - 1]
+    drafts[1, :3] = am[1, :3]
+    drafts[1, 3:] = (am[1, 3:B - 1] + 1) % w.vocab
+    drafts[2] = (am[2, :B - 1] + 7) % w.vocab
+    eng.drafts.copy_(torch.from_numpy(drafts))
+    eng.base_pos.copy_(torch.tensor([10, 20, 30], dtype=torch.int32))
+    logits = torch.zeros(S * B, w.vocab, device="cuda")
+    eng.verify(B, eng.drafts, logits)
+    assert eng.status() == D.DFLASH_OK
+    np.testing.assert_allclose(logits.cpu().numpy(), lg, rtol=0, atol=G.LOGIT_TOL[dtype] / 10)
+    gam = eng.argmax.cpu().numpy()
+    G.check_argmax(gam, am, mg)
+    for s in range(S):
+        k, out = O.accept(drafts[s], gam[s])
+        assert int(eng.accept_len[s]) == k
+        np.testing.assert_array_equal(eng.out_tokens[s, :k + 1].cpu().numpy(), out)
+        assert int(eng.anchor[s]) == out[-1]
+        assert int(eng.commit_count[s]) == k + 1
+    assert eng.accept_len.cpu().tolist()[0] == B - 1 and eng.accept_len.cpu().tolist()[2] == 0
+    assert eng.base_pos.cpu().tolist() == [10 + B, 20 + 4, 31]
+    np.testing.assert_allclose(eng.margin.cpu().numpy().ravel(), mg, rtol=0, atol=1e-3)
+
+
+@pytest.mark.parametrize("dtype,window", [("f32", 0), ("bf16", 0), ("bf16", 24)])
+def test_draft_block(dtype, window):
+    w = small(dtype, window=window)
+    S = 2
+    eng, om, _ = G.setup(w, S=S, cap=96)
+    base = [9, 40]
+    eng.base_pos.copy_(torch.tensor(base, dtype=torch.int32))
+    eng.anchor.copy_(torch.tensor([17, 400], dtype=torch.int32))
+    dk, dv = [], []
+    for j in range(w.draft.layers):
+        k, v = rand_cache(eng, eng.caches.dk[j], eng.caches.dv[j], S, eng.dcap, 10 + j, om.draft.cfg)
+        dk.append(k)
+        dv.append(v)
+    logits = torch.zeros(S * (w.block - 1), w.vocab, device="cuda")
+    eng.draft(logits)
+    torch.cuda.synchronize()
+    gd = eng.drafts.cpu().numpy()
+    gl = logits.cpu().numpy().reshape(S, w.block - 1, w.vocab)
+    for s in range(S):
+        st = O.new_state(om, 96)
+        st.dk = [k[s].copy() for k in dk]
+        st.dv = [v[s].copy() for v in dv]
+        am, mg, lg = O.draft_forward(om, st, int(eng.anchor[s]), base[s], want_logits=True)
+        err = np.abs(gl[s] - lg).max()
+        assert err <= G.LOGIT_TOL[dtype], f"draft logits differ by {err}"
+        G.check_argmax(gd[s], am, mg, tol=max(G.NEAR_TIE, 2 * err))
+        np.testing.assert_array_equal(gd[s], gl[s].argmax(-1))  # fused argmax == argmax of its logits
+
+
+def test_tiny_lossless_workload_gpu():
+    """The fp32 tiny workload end to end on the GPU: speculative output ==
+    GPU plain greedy == oracle plain greedy, 64 tokens after a 64-token prompt."""
+    w = synth.WORKLOADS["tiny-lossless"]
+    m_cpu = synth.make_model(w, seed=0)
+    prompt = synth.make_tokens(0, w.prompt, w.vocab)
+    cap = w.prompt + w.generate + 2 * w.block
+    from block_diffusion_speculative_step_gb300.engine import Engine
+    eng = Engine(w, G.to_dev(m_cpu), 1, cap)
+    greedy = eng.greedy_generate(prompt[None].cuda(), w.generate)[0].numpy()
+    eng2 = Engine(w, G.to_dev(m_cpu), 1, cap)
+    spec, acc = eng2.speculative_generate(prompt[None].cuda(), w.generate)
+    assert eng2.status() == D.DFLASH_OK
+    np.testing.assert_array_equal(spec[0].numpy(), greedy)
+    om = Hh.omodel(w, m_cpu)
+    ref, margins = O.greedy_generate(om, prompt.numpy(), w.generate, cap)
+    bad = np.nonzero(ref != greedy)[0]
+    if len(bad):
+        assert margins[bad[0]] < G.NEAR_TIE, f"first divergence at {bad[0]} with margin {margins[bad[0]]}"
+    assert int(acc.max()) <= w.block - 1
+
+
+@pytest.mark.parametrize("dtype,S", [("bf16", 1), ("bf16", 3), ("f32", 2)])
+def test_lossless_gpu(dtype, S):
+    """Speculative == plain greedy on the GPU itself (batch-invariant rows)."""
+    w = small(dtype, V=512, block=6)
+    m_cpu = synth.make_model(w, seed=3, jitter=0.1, with_target=True)
+    prompts = torch.stack([synth.make_tokens(10 + s, 20, w.vocab) for s in range(S)]).cuda()
+    from block_diffusion_speculative_step_gb300.engine import Engine
+    n = 40
+    greedy = Engine(w, G.to_dev(m_cpu), S, 96).greedy_generate(prompts, n)
+    spec, acc = Engine(w, G.to_dev(m_cpu), S, 96).speculative_generate(prompts, n)
+    np.testing.assert_array_equal(spec.numpy(), greedy.numpy())
+
+
+def test_perfect_drafter_gpu():
+    """Planted drafts equal to the greedy continuation are all accepted."""
+    w = small("bf16", V=512, block=6)
+    m_cpu = synth.make_model(w, seed=4, jitter=0.1, with_target=True)
+    prompts = synth.make_tokens(20, 16, w.vocab)[None].cuda()
+    from block_diffusion_speculative_step_gb300.engine import Engine
+    greedy = Engine(w, G.to_dev(m_cpu), 1, 96).greedy_generate(prompts, 40)[0]
+    eng = Engine(w, G.to_dev(m_cpu), 1, 96)
+    eng.prefill(prompts)
+    got = [int(eng.anchor[0])]
+    for _ in range(5):
+        i = len(got) - 1
+        planted = greedy[i + 1:i + w.block].to(torch.int32)[None].cuda()
+        eng.cycle(planted_drafts=planted)
+        k = int(eng.accept_len[0])
+        assert k == w.block - 1
+        got.extend(eng.out_tokens[0, :k + 1].cpu().tolist())
+    np.testing.assert_array_equal(np.array(got), greedy[:len(got)].numpy())
