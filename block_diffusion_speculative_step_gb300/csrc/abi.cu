@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "trace.h"
 
 using namespace dfl;
 
@@ -32,6 +33,15 @@ int fail(int code, const char* fmt, ...) {
 #define DF_CUDA(call)                                                                       \
   do {                                                                                      \
     cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) return fail(DFLASH_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+// Launch with optional tracing (family, algorithmic bytes).
+#define DF_LAUNCH(st, fam, bytes, call)                                                     \
+  do {                                                                                      \
+    trace_pre((st), (fam));                                                                 \
+    cudaError_t e_ = (call);                                                                \
+    trace_post((st), (double)(bytes));                                                      \
     if (e_ != cudaSuccess) return fail(DFLASH_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
   } while (0)
 
@@ -90,11 +100,27 @@ size_t gemm_scratch_bytes(const GemmDesc& g, int sms) {
   return g.dtype == DFLASH_BF16 && gemm_tc_supported(g) ? gemm_tc_workspace(g, sms) : 0;
 }
 
+// Algorithmic bytes of a GEMM launch: every weight row once, the token rows
+// once, the outputs once (residual outputs read and written).
+double gemm_bytes(const GemmDesc& g) {
+  const double es = g.dtype == DFLASH_BF16 ? 2.0 : 4.0;
+  const double rows = (double)g.nseg * g.seg_rows;
+  double b = rows * g.K * es + (double)g.M * g.K * es;
+  if (g.kind == EPI_RESID) b += 2.0 * g.M * rows * 4.0;
+  else if (g.kind == EPI_STORE) b += (double)g.M * rows * 4.0;
+  else if (g.kind == EPI_SWIGLU) b += (double)g.M * g.inter * es;
+  else b += (double)g.M * rows * es;
+  return b;
+}
+
 cudaError_t run_gemm(const GemmDesc& g, void* gpart, size_t gpart_bytes, const Ctx& c, int sms,
                      cudaStream_t st) {
-  if (g.dtype == DFLASH_BF16 && gemm_tc_supported(g))
-    return launch_gemm_tc(g, gpart, gpart_bytes, c.counters, c.status, sms, st);
-  return launch_gemm_simt(g, st);
+  const bool tc = g.dtype == DFLASH_BF16 && gemm_tc_supported(g);
+  trace_pre(st, tc ? TF_GEMM_TC : TF_GEMM_SIMT);
+  cudaError_t e = tc ? launch_gemm_tc(g, gpart, gpart_bytes, c.counters, c.status, sms, st)
+                     : launch_gemm_simt(g, st);
+  trace_post(st, gemm_bytes(g));
+  return e;
 }
 
 GemmDesc gemm_base(int dtype, int M, int K, const void* X, const int32_t* base_pos, const int32_t* valid,
@@ -226,7 +252,7 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   for (auto& g : g4) g.base_pos = base_pos;
   const bool causal = L.mode == DFLASH_ATTN_CAUSAL;
 
-  DF_CUDA(launch_rmsnorm(d.dtype, h, w.ln1, M, H, d.rms_eps, s.x, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln1, M, H, d.rms_eps, s.x, st));
   GemmDesc& qkv = g4[0];
   qkv.X = s.x;
   qkv.q_out = s.q;
@@ -250,14 +276,14 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   a.partials = s.apart;
   a.counters = c.counters;
   a.status = c.status;
-  DF_CUDA(launch_attention(a, st));
+  DF_LAUNCH(st, TF_ATTN, 0, launch_attention(a, st));
 
   GemmDesc& o = g4[1];
   o.X = s.attn;
   o.out_f32 = h;
   DF_CUDA(run_gemm(o, s.gpart, s.gpart_bytes, c, sms, st));
 
-  DF_CUDA(launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x, st));
   GemmDesc& gu = g4[2];
   gu.X = s.x;
   gu.act_out = s.act;
@@ -268,7 +294,7 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   dn.out_f32 = h;
   DF_CUDA(run_gemm(dn, s.gpart, s.gpart_bytes, c, sms, st));
 
-  if (tap) DF_CUDA(launch_store_tap(d.dtype, h, M, H, tap, tap_stride, tap_offset, st));
+  if (tap) DF_LAUNCH(st, TF_TAP, 0, launch_store_tap(d.dtype, h, M, H, tap, tap_stride, tap_offset, st));
   return DFLASH_OK;
 }
 
@@ -287,6 +313,12 @@ int check_weights(const dflash_layer_weights& w, const char* who) {
 }
 
 // --------------------------------------------------------------- LM head
+
+// Algorithmic bytes of the LM head: every vocabulary row once + the token rows.
+double head_bytes(const HeadDesc& h) {
+  const double es = h.dtype == DFLASH_BF16 ? 2.0 : 4.0;
+  return (double)h.V * h.H * es + (double)h.M * h.H * es;
+}
 
 HeadDesc head_shape(const dflash_dims& d, int S, int block, int mode) {
   HeadDesc h;
@@ -362,7 +394,8 @@ int dflash_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos
   DF_CHECK(cos_sin != nullptr, "dflash_rope_table: cos_sin is NULL");
   DF_CHECK(head_dim > 0 && head_dim % 2 == 0 && max_pos > 0 && theta > 0.f,
            "dflash_rope_table: need theta > 0, even head_dim > 0, max_pos > 0");
-  DF_CUDA(launch_rope_table(theta, head_dim, max_pos, cos_sin, (cudaStream_t)stream));
+  DF_LAUNCH((cudaStream_t)stream, TF_ROPE, 0,
+            launch_rope_table(theta, head_dim, max_pos, cos_sin, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
@@ -398,8 +431,9 @@ int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_s
            "dflash_embed: fill_token out of range");
   rc = check_ws(ws, ws_bytes, kReservedBytes, "dflash_embed");
   if (rc) return rc;
-  DF_CUDA(launch_embed(a->dims.dtype, a->embed, a->dims.hidden, a->n_seqs, a->rows, a->first, a->rest,
-                       a->fill_token, a->h, (cudaStream_t)stream));
+  DF_LAUNCH((cudaStream_t)stream, TF_EMBED, 0,
+            launch_embed(a->dims.dtype, a->embed, a->dims.hidden, a->n_seqs, a->rows, a->first, a->rest,
+                         a->fill_token, a->h, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
@@ -515,8 +549,8 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
   fc.out_f32 = z;
   fc.ldo = d.hidden;
   DF_CUDA(run_gemm(fc, gpart, gp, c, sms, st));
-  DF_CUDA(launch_rmsnorm(d.dtype, z, a->fc_norm, M, d.hidden, d.rms_eps, cbuf, st));
-  if (a->c_out) DF_CUDA(launch_to_f32(d.dtype, cbuf, (size_t)M * d.hidden, a->c_out, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, z, a->fc_norm, M, d.hidden, d.rms_eps, cbuf, st));
+  if (a->c_out) DF_LAUNCH(st, TF_CONVERT, 0, launch_to_f32(d.dtype, cbuf, (size_t)M * d.hidden, a->c_out, st));
 
   GemmDesc kv = gemm_base(d.dtype, M, d.hidden, cbuf, a->base_pos, a->valid, a->rows);
   kv.nseg = a->n_layers;
@@ -581,15 +615,16 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   cudaStream_t st = (cudaStream_t)stream;
   const int M = a->n_seqs * a->block;
 
-  DF_CUDA(launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, nullptr, a->mask_token,
-                       s.h, st));
+  DF_LAUNCH(st, TF_EMBED, 0,
+            launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, nullptr, a->mask_token,
+                         s.h, st));
   for (int j = 0; j < a->n_layers; ++j) {
     rc = run_layer(draft_layer_shape(a, j), a->layers[j], a->kv_layers[j], s.h, a->base_pos, a->rope_cs,
                    a->rope_max_pos, nullptr,
                    0, 0, s.ls, c, sms, st);
     if (rc) return rc;
   }
-  DF_CUDA(launch_rmsnorm(d.dtype, s.h, a->final_norm, M, d.hidden, d.rms_eps, s.xf, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, s.h, a->final_norm, M, d.hidden, d.rms_eps, s.xf, st));
   HeadDesc h = head_shape(d, a->n_seqs, a->block, a->path_topk > 0 ? 2 : 0);
   h.topk = a->path_topk;
   h.x = s.xf;
@@ -600,7 +635,7 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   h.partials = static_cast<float*>(s.hpart);
   h.counters = c.counters;
   h.status = c.status;
-  DF_CUDA(launch_head(h, sms, st));
+  DF_LAUNCH(st, TF_HEAD, head_bytes(h), launch_head(h, sms, st));
   if (a->path_topk > 0) {
     PathDesc p;
     memset(&p, 0, sizeof(p));
@@ -616,7 +651,7 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
     p.anchor = a->anchor;
     p.cand = s.cand;
     p.path = a->drafts;
-    DF_CUDA(launch_path_select(p, st));
+    DF_LAUNCH(st, TF_PATH, 0, launch_path_select(p, st));
   }
   return DFLASH_OK;
 }
@@ -652,7 +687,7 @@ int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
   cudaStream_t st = (cudaStream_t)stream;
   const dflash_dims& d = a->dims;
   const int M = a->n_seqs * a->block;
-  DF_CUDA(launch_rmsnorm(d.dtype, a->h, a->final_norm, M, d.hidden, d.rms_eps, xf, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, a->h, a->final_norm, M, d.hidden, d.rms_eps, xf, st));
   HeadDesc h = head_shape(d, a->n_seqs, a->block, 1);
   h.x = xf;
   h.w = a->lm_head;
@@ -669,7 +704,7 @@ int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
   h.partials = static_cast<float*>(hpart);
   h.counters = c.counters;
   h.status = c.status;
-  DF_CUDA(launch_head(h, sms, st));
+  DF_LAUNCH(st, TF_HEAD, head_bytes(h), launch_head(h, sms, st));
   return DFLASH_OK;
 }
 
@@ -700,7 +735,7 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   p.cand = a->cand;
   p.path = a->path;
   p.margin = a->margin;
-  DF_CUDA(launch_path_select(p, (cudaStream_t)stream));
+  DF_LAUNCH((cudaStream_t)stream, TF_PATH, 0, launch_path_select(p, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 

@@ -1,0 +1,24 @@
+// trace.h -- kernel-launch tracing hooks used by the ABI layer.
+#pragma once
+#include <cuda_runtime.h>
+
+namespace dfl {
+
+enum TraceFamily : int {
+  TF_EMBED = 0,
+  TF_RMSNORM = 1,
+  TF_GEMM_SIMT = 2,
+  TF_GEMM_TC = 3,
+  TF_ATTN = 4,
+  TF_HEAD = 5,
+  TF_PATH = 6,
+  TF_ROPE = 7,
+  TF_TAP = 8,
+  TF_CONVERT = 9,
+  kTraceFamilies = 10
+};
+
+void trace_pre(cudaStream_t st, int family);
+void trace_post(cudaStream_t st, double bytes);
+
+}  // namespace dfl

@@ -27,7 +27,9 @@ DFLASH_MAX_LAYERS = 16
 # Every symbol the header exports (checked by the CPU test suite).
 EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", "dflash_fuse_context",
            "dflash_draft_block", "dflash_verify_accept", "dflash_path_select", "dflash_workspace_bytes",
-           "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version")
+           "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
+           "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end")
+DFLASH_TRACE_FAMILIES = 10
 
 
 class DFlashError(RuntimeError):
@@ -97,6 +99,10 @@ class dflash_path_args(C.Structure):
                 ("margin", vp)]
 
 
+class dflash_trace_stat(C.Structure):
+    _fields_ = [("name", C.c_char * 24), ("launches", i32), ("total_ms", C.c_double), ("bytes", C.c_double)]
+
+
 _lib = None
 
 
@@ -122,6 +128,8 @@ def lib(path: str | None = None):
         L.dflash_read_status.restype = C.c_int
         L.dflash_last_error.restype = C.c_char_p
         L.dflash_abi_version.restype = i32
+        L.dflash_trace_begin.argtypes = [i32]
+        L.dflash_trace_read.argtypes = [C.POINTER(dflash_trace_stat), i32]
         _lib = L
     return _lib
 
@@ -191,3 +199,24 @@ def dflash_verify_accept(args: dflash_verify_args, ws_ptr: int, ws_bytes: int, s
 
 def dflash_path_select(args: dflash_path_args, ws_ptr: int, ws_bytes: int, stream=None):
     _call("dflash_path_select", args, ws_ptr, ws_bytes, stream)
+
+
+def dflash_trace_begin(max_launches: int = 4096):
+    _check(lib().dflash_trace_begin(max_launches))
+
+
+def dflash_trace_pause():
+    _check(lib().dflash_trace_pause())
+
+
+def dflash_trace_read() -> dict:
+    """Per kernel family: {name: (launches, total_ms, bytes)} of the last traced work."""
+    arr = (dflash_trace_stat * DFLASH_TRACE_FAMILIES)()
+    n = lib().dflash_trace_read(arr, DFLASH_TRACE_FAMILIES)
+    if n < 0:
+        _check(n)
+    return {a.name.decode(): (int(a.launches), float(a.total_ms), float(a.bytes)) for a in arr[:n]}
+
+
+def dflash_trace_end():
+    _check(lib().dflash_trace_end())

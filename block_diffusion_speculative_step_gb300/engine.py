@@ -49,7 +49,7 @@ class Engine:
     """One target + draft pair resident on the GPU, n_seqs sequences."""
 
     def __init__(self, w: synth.Workload, model: dict, n_seqs: int, cap: int, device="cuda",
-                 prefill_chunk: int = 256, ws_extra_rows: int = 0):
+                 prefill_chunk: int = 256, fuse_rows: int = 0):
         self.w = w
         self.m = model
         self.S = n_seqs
@@ -94,7 +94,7 @@ class Engine:
         self.ones = torch.ones(S, dtype=torch.int32, device=self.dev)
         self.ws = None
         self.ws_bytes = 0
-        self._size_workspace(ws_extra_rows)
+        self._size_workspace(fuse_rows)
         st = torch.cuda.current_stream()
         if self.has_target:
             D.dflash_rope_table(w.rope_theta, tdims.head_dim, self.rope_max, self.rope_t.data_ptr(), st)
@@ -196,11 +196,12 @@ class Engine:
         a.h = _ptr(h)
         return a
 
-    def _size_workspace(self, extra_rows: int):
+    def _size_workspace(self, fuse_rows: int):
         need = D.dflash_workspace_bytes(D.DFLASH_OP_DRAFT, self.draft_args())
         rows_list = [self.B, 1, min(self.chunk, self.cap)]
-        if extra_rows:
-            rows_list.append(extra_rows)
+        if fuse_rows:
+            need = max(need, D.dflash_workspace_bytes(D.DFLASH_OP_FUSE, self.fuse_args(fuse_rows, self.feats,
+                                                                                      self.base_pos, None)))
         for rows in rows_list:
             need = max(need, D.dflash_workspace_bytes(D.DFLASH_OP_FUSE, self.fuse_args(rows, self.feats,
                                                                                       self.base_pos, None)))
@@ -239,6 +240,10 @@ class Engine:
 
     def fuse(self, rows: int, base_pos, valid):
         D.dflash_fuse_context(self.fuse_args(rows, self.feats, base_pos, valid), self.ws_ptr, self.ws_bytes)
+
+    def fuse_with(self, feats, rows: int, base_pos, valid):
+        """Inject caller-provided tap features feats [S*rows][F][H]."""
+        D.dflash_fuse_context(self.fuse_args(rows, feats, base_pos, valid), self.ws_ptr, self.ws_bytes)
 
     def prefill(self, prompts: torch.Tensor):
         """prompts [S][L] int32 on the device.  Runs the target over the

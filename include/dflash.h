@@ -13,8 +13,9 @@
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers unless a field says "host".
  *    The caller owns every buffer (weights, caches, activations, outputs and
- *    the workspace); the library allocates nothing and keeps no state beyond
- *    a thread-local error string.
+ *    the workspace); the library allocates no device memory and keeps no
+ *    state beyond a thread-local error string and the opt-in, thread-local
+ *    tracing state (dflash_trace_*).
  *  - Every call is asynchronous on the caller's `stream` and does no host
  *    synchronisation, except dflash_read_status.  Argument checks happen on
  *    the host before any launch; a failed check launches nothing.
@@ -307,6 +308,29 @@ int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
 /* Synchronise `stream`, read and clear the workspace's device status word.
  * *host_status receives DFLASH_OK or the first error raised on the device. */
 int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
+
+/*
+ * Kernel tracing (off by default; state is per host thread).  Between
+ * dflash_trace_begin and dflash_trace_pause every kernel the library
+ * launches is bracketed by two CUDA events recorded on its stream (event
+ * records are captured into CUDA graphs as well).  dflash_trace_read, called
+ * after the traced work (or graph replay) has completed, sums the event
+ * durations per kernel family into stats[0 .. DFLASH_TRACE_FAMILIES-1] and
+ * returns the number of families.  `bytes` is the algorithmic DRAM traffic
+ * the library attributes to the launches (weights + activations read and
+ * written, each once), where it is known on the host; 0 otherwise.
+ */
+#define DFLASH_TRACE_FAMILIES 10
+typedef struct {
+  char name[24];
+  int32_t launches;
+  double total_ms;
+  double bytes;
+} dflash_trace_stat;
+int dflash_trace_begin(int32_t max_launches);
+int dflash_trace_pause(void);
+int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats);
+int dflash_trace_end(void);
 
 /* Thread-local description of the last failure. */
 const char* dflash_last_error(void);

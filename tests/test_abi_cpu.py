@@ -44,7 +44,8 @@ def test_abi_version(D):
 
 def test_struct_layouts_match_c(D):
     structs = ["dflash_dims", "dflash_kv", "dflash_layer_weights", "dflash_embed_args", "dflash_layer_args",
-               "dflash_fuse_args", "dflash_draft_args", "dflash_verify_args", "dflash_path_args"]
+               "dflash_fuse_args", "dflash_draft_args", "dflash_verify_args", "dflash_path_args",
+               "dflash_trace_stat"]
     lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void) {"]
     for s in structs:
         lines.append(f'  printf("{s} %zu\\n", sizeof({s}));')
