@@ -36,7 +36,8 @@ void trace_pre(cudaStream_t st, int family) {
   TraceState& t = g_trace;
   if (!t.on || (int)t.recs.size() >= t.cap) return;
   cudaEvent_t a = t.pool[2 * t.recs.size()];
-  if (cudaEventRecord(a, st) == cudaSuccess) {
+  // External records become event nodes when the stream is being captured.
+  if (cudaEventRecordWithFlags(a, st, cudaEventRecordExternal) == cudaSuccess) {
     t.open_family = family;
     t.open_a = a;
   }
@@ -46,7 +47,8 @@ void trace_post(cudaStream_t st, double bytes) {
   TraceState& t = g_trace;
   if (!t.on || t.open_a == nullptr) return;
   cudaEvent_t b = t.pool[2 * t.recs.size() + 1];
-  if (cudaEventRecord(b, st) == cudaSuccess) t.recs.push_back(Rec{t.open_family, bytes, t.open_a, b});
+  if (cudaEventRecordWithFlags(b, st, cudaEventRecordExternal) == cudaSuccess)
+    t.recs.push_back(Rec{t.open_family, bytes, t.open_a, b});
   t.open_a = nullptr;
 }
 
@@ -84,7 +86,10 @@ int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats) {
   }
   for (const Rec& r : t.recs) {
     float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return DFLASH_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      cudaGetLastError();
+      return DFLASH_ERR_CUDA;
+    }
     dflash_trace_stat& s = stats[r.family];
     s.launches += 1;
     s.total_ms += ms;
