@@ -65,9 +65,11 @@ __device__ __forceinline__ Top2 ldcg_top2(const Top2* p) {
   return t;
 }
 
-// Called by every CTA after it stored its per-token triples at
-// part[blockIdx.x * M + m].  The last CTA to arrive merges them in CTA order
-// and writes the mode's outputs.
+// Called by every CTA (all its threads) after it stored its per-token triples
+// at part[blockIdx.x * M + m].  The last CTA to arrive merges them and writes
+// the mode's outputs.  The merge (greater value wins, lower index on equal
+// values; second = the largest other value) is associative and commutative,
+// so the warp-parallel reduction below gives the same result in any order.
 __device__ __forceinline__ void head_finish(const HeadDesc& h, int nblocks, const Top2* part, int* s_last) {
   __shared__ int s_arg[kHeadMaxM];
   __threadfence();
@@ -82,10 +84,20 @@ __device__ __forceinline__ void head_finish(const HeadDesc& h, int nblocks, cons
   if (!*s_last) return;
   __threadfence();
   const int M = h.M, B = h.block;
-  for (int m = threadIdx.x; m < M; m += blockDim.x) {
+  const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int m = threadIdx.x >> 5; m < M; m += nwarps) {
     if (!head_row_used(h, m)) continue;
-    Top2 t = ldcg_top2(part + m);
-    for (int b = 1; b < nblocks; ++b) t = top2_merge(t, ldcg_top2(part + (size_t)b * M + m));
+    Top2 t = top2_empty();
+    for (int b = lane; b < nblocks; b += 32) t = top2_merge(t, ldcg_top2(part + (size_t)b * M + m));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Top2 u;
+      u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
+      u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+      u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
+      t = top2_merge(t, u);
+    }
+    if (lane != 0) continue;
     int idx = (t.i1 == INT_MAX) ? 0 : t.i1;
     s_arg[m] = idx;
     if (h.mode == 1) {

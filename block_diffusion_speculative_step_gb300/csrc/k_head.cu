@@ -74,7 +74,9 @@ __global__ void __launch_bounds__(kHeadWarps * 32) head_simt_kernel(const __grid
 }
 
 size_t head_workspace(const HeadDesc& h, int num_sms) {
-  return (size_t)(2 * num_sms) * h.M * sizeof(Top2) + 256;
+  size_t simt = (size_t)(2 * num_sms) * h.M * sizeof(Top2) + 256;
+  size_t tc = head_tc_workspace(h);
+  return simt > tc ? simt : tc;
 }
 
 cudaError_t launch_head_simt(const HeadDesc& h, int num_sms, cudaStream_t st) {
@@ -93,6 +95,7 @@ cudaError_t launch_head_simt(const HeadDesc& h, int num_sms, cudaStream_t st) {
 }
 
 cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st) {
+  if (head_tc_supported(h)) return launch_head_tc(h, st);
   return launch_head_simt(h, num_sms, st);
 }
 
