@@ -4,72 +4,137 @@
 //
 // Grid: x = key chunk (chunk c covers slots [c*CH, (c+1)*CH)), y = (kv head,
 // query tile), z = sequence.  Each CTA writes, for each query vector of its
-// tile, the chunk's softmax partial (running max m, denominator l, unnormalised
-// output o) in log2 units; the last CTA to arrive for a (sequence, kv head,
-// query tile) merges the chunks in chunk order.  Chunk boundaries sit at fixed
-// slot offsets and chunks past a row's last visible key contribute exact
-// zeros, so a row's output does not depend on how many rows share the launch.
+// tile, the chunk's softmax partial (max m, denominator l, unnormalised output
+// o, in log2 units); the last CTA to arrive for a (sequence, kv head, query
+// tile) merges the chunks in chunk order.  Chunk boundaries sit at fixed slot
+// offsets and chunks past a row's last visible key contribute exact zeros, so
+// a row's output does not depend on how many rows share the launch.
+//
+// bf16 path: mma.sync m16n8k16 tensor-core tiles (S = Q K^T and O = P V with
+// P rounded to bf16), K/V/Q staged by cp.async into XOR-swizzled shared
+// memory and read with ldmatrix.  fp32 path: CUDA-core dot products.
 #include "common.cuh"
 #include "internal.h"
 
 namespace dfl {
 
-constexpr int kAttnCH = 64;     // keys per chunk
-constexpr int kAttnQT = 64;     // query vectors per CTA
+constexpr int kAttnQT = 64;      // query vectors per CTA
 constexpr int kAttnWarps = 4;
+constexpr int kSimtCH = 64;      // keys per chunk, fp32 path
+constexpr int kMmaCH = 128;      // keys per chunk, bf16 tensor-core path
 constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ __forceinline__ int attn_ch(const AttnDesc& a) {
+  return a.dtype == DFLASH_BF16 ? kMmaCH : kSimtCH;
+}
 
 struct AttnGeom {
   int grp, nqv, n_qt, nch;
 };
 
 __host__ __device__ __forceinline__ AttnGeom attn_geom(const AttnDesc& a) {
+  const int CH = attn_ch(a);
   AttnGeom g;
   g.grp = a.nq / a.nkv;
   g.nqv = a.rows * g.grp;
   g.n_qt = (g.nqv + kAttnQT - 1) / kAttnQT;
   if (a.mode == DFLASH_ATTN_CAUSAL) {
-    g.nch = (a.max_pos + kAttnCH - 1) / kAttnCH;
+    g.nch = (a.max_pos + CH - 1) / CH;
   } else {
     int ctx = a.window > 0 ? (a.window < a.max_pos ? a.window : a.max_pos) : a.max_pos;
-    g.nch = (ctx + kAttnCH - 1) / kAttnCH + 1;  // + the block chunk
+    g.nch = (ctx + CH - 1) / CH + 1;  // + the block chunk
   }
   return g;
 }
 
-// Per-sequence chunk structure.
 struct SeqKeys {
-  int n_ctx;      // context slots visible (bidir) or cache slots in use (causal)
-  int n_ctx_ch;   // chunks over those slots
-  int n_ch;       // chunks this sequence uses (bidir: + block chunk)
+  int n_ctx;     // context slots visible (bidir) or cache slots in use (causal)
+  int n_ctx_ch;  // chunks over those slots
+  int n_ch;      // chunks this sequence uses (bidir: + block chunk)
 };
 
 // Slots beyond the cache or beyond the chunks the grid covers are never read
 // (positions past max_pos are a caller error; they are clamped, not read).
-__device__ __forceinline__ SeqKeys seq_keys(const AttnDesc& a, int P, int grid_ch) {
+__device__ __forceinline__ SeqKeys seq_keys(const AttnDesc& a, int P, int grid_ch, int CH) {
   SeqKeys k;
   if (a.mode == DFLASH_ATTN_CAUSAL) {
-    k.n_ctx = min(max(P + a.rows, 0), min(a.cap, grid_ch * kAttnCH));
-    k.n_ctx_ch = (k.n_ctx + kAttnCH - 1) / kAttnCH;
+    k.n_ctx = min(max(P + a.rows, 0), min(a.cap, grid_ch * CH));
+    k.n_ctx_ch = (k.n_ctx + CH - 1) / CH;
     k.n_ch = k.n_ctx_ch;
   } else {
     k.n_ctx = a.window > 0 ? min(P, a.window) : P;
-    k.n_ctx = min(max(k.n_ctx, 0), min(a.cap, (grid_ch - 1) * kAttnCH));
-    k.n_ctx_ch = (k.n_ctx + kAttnCH - 1) / kAttnCH;
+    k.n_ctx = min(max(k.n_ctx, 0), min(a.cap, (grid_ch - 1) * CH));
+    k.n_ctx_ch = (k.n_ctx + CH - 1) / CH;
     k.n_ch = k.n_ctx_ch + 1;
   }
   return k;
 }
 
+// Keys of chunk c: base pointers, count, first slot.
 template <typename T>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid_constant__ AttnDesc a,
-                                                                     int n_qt) {
-  extern __shared__ float sm[];
+__device__ __forceinline__ void chunk_keys(const AttnDesc& a, const SeqKeys& sk, int s, int g, int c, int CH,
+                                           const T*& kp, const T*& vp, int& nk, int& slot0) {
   const int d = a.d;
-  float* Ks = sm;                       // [CH][d]
-  float* Vs = Ks + kAttnCH * d;         // [CH][d]
-  float* qs = Vs + kAttnCH * d;         // [warps][d]
-  float* ps = qs + kAttnWarps * d;      // [warps][CH]
+  if (a.mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch) {
+    kp = reinterpret_cast<const T*>(a.kb) + ((size_t)s * a.nkv + g) * a.rows * d;
+    vp = reinterpret_cast<const T*>(a.vb) + ((size_t)s * a.nkv + g) * a.rows * d;
+    nk = min(a.rows, CH);
+    slot0 = -1;  // block chunk: every key visible
+  } else {
+    slot0 = c * CH;
+    kp = reinterpret_cast<const T*>(a.kc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
+    vp = reinterpret_cast<const T*>(a.vc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
+    nk = min(CH, sk.n_ctx - slot0);
+  }
+}
+
+// Arrival + merge of the chunk partials by the last CTA of the group.
+template <typename T>
+__device__ __forceinline__ void attn_finish(const AttnDesc& a, const float* part, size_t grp_id, int stride_c,
+                                            int nq_tile, int qv0, int g, int s, int n_ch, int* s_last) {
+  const int d = a.d, grp = a.nq / a.nkv, QD = a.nq * d;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t* ctr = a.counters + kCtrAttn + grp_id;
+    const uint32_t old = atomicAdd(ctr, 1u);
+    *s_last = (old == gridDim.x - 1);
+    if (*s_last) *ctr = 0u;
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  T* outp = reinterpret_cast<T*>(a.out);
+  for (int t = threadIdx.x; t < nq_tile * d; t += blockDim.x) {
+    const int qi = t / d, e = t % d;
+    const int qv = qv0 + qi;
+    const int row = qv / grp, head = g * grp + qv % grp;
+    float M = -INFINITY;
+    for (int cc = 0; cc < n_ch; ++cc) M = fmaxf(M, __ldcg(part + (size_t)cc * stride_c + (size_t)qi * (d + 2)));
+    float L = 0.f, O = 0.f;
+    for (int cc = 0; cc < n_ch; ++cc) {
+      const float* pp = part + (size_t)cc * stride_c + (size_t)qi * (d + 2);
+      const float mc = __ldcg(pp);
+      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+      L = fmaf(__ldcg(pp + 1), w, L);
+      O = fmaf(__ldcg(pp + 2 + e), w, O);
+    }
+    const float v = (L > 0.f) ? O / L : 0.f;
+    outp[((size_t)s * a.rows + row) * QD + (size_t)head * d + e] = from_f<T>(v);
+  }
+}
+
+// ------------------------------------------------------------- fp32 path
+
+template <typename T>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid_constant__ AttnDesc a, int n_qt) {
+  extern __shared__ float sm[];
+  constexpr int CH = kSimtCH;
+  const int d = a.d, ld = d + 1;  // padded rows: lanes reading different keys hit different banks
+  float* Ks = sm;                  // [CH][d+1]
+  float* Vs = Ks + CH * ld;        // [CH][d+1]
+  float* qs = Vs + CH * ld;        // [warps][d]
+  float* ps = qs + kAttnWarps * d; // [warps][CH]
   __shared__ int s_last;
 
   const int c = blockIdx.x;
@@ -79,7 +144,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid
   const int nqv = a.rows * grp;
   const int QD = a.nq * d;
   const int P = a.base_pos[s];
-  const SeqKeys sk = seq_keys(a, P, gridDim.x);
+  const SeqKeys sk = seq_keys(a, P, gridDim.x, CH);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qv0 = qt * kAttnQT;
   const int nq_tile = min(kAttnQT, nqv - qv0);
@@ -88,26 +153,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid
   float* part = a.partials + grp_id * (size_t)gridDim.x * stride_c;
 
   if (c < sk.n_ch) {
-    // ---- which keys this chunk holds
     const T* kp;
     const T* vp;
     int nk, slot0;
-    bool block_chunk = (a.mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
-    if (block_chunk) {
-      kp = reinterpret_cast<const T*>(a.kb) + ((size_t)s * a.nkv + g) * a.rows * d;
-      vp = reinterpret_cast<const T*>(a.vb) + ((size_t)s * a.nkv + g) * a.rows * d;
-      nk = a.rows;
-      slot0 = 0;
-    } else {
-      slot0 = c * kAttnCH;
-      kp = reinterpret_cast<const T*>(a.kc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
-      vp = reinterpret_cast<const T*>(a.vc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
-      nk = min(kAttnCH, sk.n_ctx - slot0);
-    }
-    for (int t = threadIdx.x; t < kAttnCH * d; t += blockDim.x) {
-      int j = t / d;
-      Ks[t] = j < nk ? to_f<T>(kp[t]) : 0.f;
-      Vs[t] = j < nk ? to_f<T>(vp[t]) : 0.f;
+    chunk_keys<T>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
+    for (int t = threadIdx.x; t < CH * d; t += blockDim.x) {
+      const int j = t / d, e = t % d;
+      Ks[j * ld + e] = j < nk ? to_f<T>(kp[t]) : 0.f;
+      Vs[j * ld + e] = j < nk ? to_f<T>(vp[t]) : 0.f;
     }
     __syncthreads();
     const float scale = rsqrtf((float)d) * kLog2e;
@@ -118,24 +171,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid
       const T* q = reinterpret_cast<const T*>(a.q) + (size_t)m * QD + (size_t)head * d;
       for (int e = lane; e < d; e += 32) qs[warp * d + e] = to_f<T>(q[e]);
       __syncwarp();
-      const int limit = (a.mode == DFLASH_ATTN_CAUSAL) ? (P + row - slot0) : nk - 1;  // last visible key
+      // last visible key of this chunk for this row
+      const int limit = (a.mode == DFLASH_ATTN_CAUSAL) ? (P + row - slot0) : nk - 1;
       float mx = -INFINITY;
-      for (int j = lane; j < kAttnCH; j += 32) {
+      for (int j = lane; j < CH; j += 32) {
         float sc = -INFINITY;
         if (j < nk && j <= limit) {
           float acc = 0.f;
-          for (int e = 0; e < d; ++e) acc = fmaf(qs[warp * d + e], Ks[j * d + e], acc);
+          for (int e = 0; e < d; ++e) acc = fmaf(qs[warp * d + e], Ks[j * ld + e], acc);
           sc = acc * scale;
         }
-        ps[warp * kAttnCH + j] = sc;
+        ps[warp * CH + j] = sc;
         mx = fmaxf(mx, sc);
       }
       mx = warp_max(mx);
       float l = 0.f;
-      for (int j = lane; j < kAttnCH; j += 32) {
-        float sc = ps[warp * kAttnCH + j];
-        float p = (mx == -INFINITY || sc == -INFINITY) ? 0.f : exp2f(sc - mx);
-        ps[warp * kAttnCH + j] = p;
+      for (int j = lane; j < CH; j += 32) {
+        const float sc = ps[warp * CH + j];
+        const float p = (mx == -INFINITY || sc == -INFINITY) ? 0.f : exp2f(sc - mx);
+        ps[warp * CH + j] = p;
         l += p;
       }
       l = warp_sum(l);
@@ -143,7 +197,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid
       float* out = part + (size_t)c * stride_c + (size_t)qi * (d + 2);
       for (int e = lane; e < d; e += 32) {
         float o = 0.f;
-        for (int j = 0; j < kAttnCH; ++j) o = fmaf(ps[warp * kAttnCH + j], Vs[j * d + e], o);
+        for (int j = 0; j < CH; ++j) o = fmaf(ps[warp * CH + j], Vs[j * ld + e], o);
         out[2 + e] = o;
       }
       if (lane == 0) {
@@ -153,37 +207,215 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid
       __syncwarp();
     }
   }
-  // ---- arrival; the last CTA of this (seq, head, tile) merges the chunks
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t* ctr = a.counters + kCtrAttn + grp_id;
-    uint32_t old = atomicAdd(ctr, 1u);
-    s_last = (old == gridDim.x - 1);
-    if (s_last) *ctr = 0u;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  T* outp = reinterpret_cast<T*>(a.out);
-  for (int t = threadIdx.x; t < nq_tile * d; t += blockDim.x) {
-    const int qi = t / d, e = t % d;
-    const int qv = qv0 + qi;
-    const int row = qv / grp, head = g * grp + qv % grp;
-    float M = -INFINITY;
-    for (int cc = 0; cc < sk.n_ch; ++cc) M = fmaxf(M, __ldcg(part + (size_t)cc * stride_c + (size_t)qi * (d + 2)));
-    float L = 0.f, O = 0.f;
-    for (int cc = 0; cc < sk.n_ch; ++cc) {
-      const float* pp = part + (size_t)cc * stride_c + (size_t)qi * (d + 2);
-      float mc = __ldcg(pp);
-      float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-      L = fmaf(__ldcg(pp + 1), w, L);
-      O = fmaf(__ldcg(pp + 2 + e), w, O);
-    }
-    float v = (L > 0.f) ? O / L : 0.f;
-    outp[((size_t)s * a.rows + row) * QD + (size_t)head * d + e] = from_f<T>(v);
-  }
+  attn_finish<T>(a, part, grp_id, stride_c, nq_tile, qv0, g, s, sk.n_ch, &s_last);
 }
+
+// ------------------------------------------------- bf16 tensor-core path
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of (row, 16-byte chunk) in a [rows][D] bf16 tile whose chunk
+// index is XOR-swizzled by the row, so ldmatrix row sets are bank-conflict free.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_mma_kernel(const __grid_constant__ AttnDesc a, int n_qt) {
+  constexpr int CH = kMmaCH;
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  extern __shared__ __align__(128) uint8_t asm_raw[];
+  uint8_t* Qs = asm_raw;                 // [64][D]
+  uint8_t* Ks = Qs + kAttnQT * D * 2;    // [CH][D]
+  uint8_t* Vs = Ks + CH * D * 2;         // [CH][D]
+  __shared__ int s_last;
+
+  const int c = blockIdx.x;
+  const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
+  const int s = blockIdx.z;
+  const int grp = a.nq / a.nkv;
+  const int nqv = a.rows * grp;
+  const int QD = a.nq * D;
+  const int P = a.base_pos[s];
+  const SeqKeys sk = seq_keys(a, P, gridDim.x, CH);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int qv0 = qt * kAttnQT;
+  const int nq_tile = min(kAttnQT, nqv - qv0);
+  const size_t grp_id = ((size_t)s * a.nkv + g) * n_qt + qt;
+  const int stride_c = kAttnQT * (D + 2);
+  float* part = a.partials + grp_id * (size_t)gridDim.x * stride_c;
+
+  if (c < sk.n_ch) {
+    const __nv_bfloat16* kp;
+    const __nv_bfloat16* vp;
+    int nk, slot0;
+    chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
+    const uint32_t qb = __cvta_generic_to_shared(Qs), kb = __cvta_generic_to_shared(Ks),
+                   vb = __cvta_generic_to_shared(Vs);
+    // ---- stage K, V (rows >= nk zero) and Q (rows >= nq_tile zero)
+    for (int t = threadIdx.x; t < CH * CPR; t += blockDim.x) {
+      const int j = t / CPR, ch = t % CPR;
+      if (j < nk) {
+        cp_async16(kb + swz<D>(j, ch), kp + (size_t)j * D + ch * 8);
+        cp_async16(vb + swz<D>(j, ch), vp + (size_t)j * D + ch * 8);
+      } else {
+        *reinterpret_cast<uint4*>(Ks + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Vs + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    for (int t = threadIdx.x; t < kAttnQT * CPR; t += blockDim.x) {
+      const int qi = t / CPR, ch = t % CPR;
+      if (qi < nq_tile) {
+        const int qv = qv0 + qi;
+        const int row = qv / grp, head = g * grp + qv % grp;
+        const __nv_bfloat16* q =
+            reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * a.rows + row) * QD + (size_t)head * D;
+        cp_async16(qb + swz<D>(qi, ch), q + ch * 8);
+      } else {
+        *reinterpret_cast<uint4*>(Qs + swz<D>(qi, ch)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    const int r0 = 16 * warp;  // this warp's 16 query vectors
+    if (r0 < nq_tile) {
+      // ---- S = Q K^T over the CH keys: 16 rows x (CH/8) n8 tiles
+      float S[CH / 8][4];
+#pragma unroll
+      for (int t = 0; t < CH / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(qb + swz<D>(r0 + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < CH / 16; ++nt) {
+          uint32_t b0, b1, b2, b3;
+          const int key = 16 * nt + (lane & 7) + ((lane >> 4) << 3);
+          ldsm_x4(kb + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
+          mma_16816(S[2 * nt], a0, a1, a2, a3, b0, b1);
+          mma_16816(S[2 * nt + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      // ---- mask, scale (log2 units), row max / sum over the quad
+      const float scale = rsqrtf((float)D) * kLog2e;
+      const int qa = r0 + (lane >> 2), qb2 = qa + 8;  // the two rows this thread holds
+      const int lim_a = (a.mode == DFLASH_ATTN_CAUSAL) ? P + (qv0 + qa) / grp - slot0 : CH;
+      const int lim_b = (a.mode == DFLASH_ATTN_CAUSAL) ? P + (qv0 + qb2) / grp - slot0 : CH;
+      float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < CH / 8; ++t) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = 8 * t + 2 * (lane & 3) + e;
+          const bool ok_a = j < nk && j <= lim_a;
+          const bool ok_b = j < nk && j <= lim_b;
+          S[t][e] = ok_a ? S[t][e] * scale : -INFINITY;
+          S[t][2 + e] = ok_b ? S[t][2 + e] * scale : -INFINITY;
+          mx_a = fmaxf(mx_a, S[t][e]);
+          mx_b = fmaxf(mx_b, S[t][2 + e]);
+        }
+      }
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+      float l_a = 0.f, l_b = 0.f;
+#pragma unroll
+      for (int t = 0; t < CH / 8; ++t) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pa = (S[t][e] == -INFINITY) ? 0.f : exp2f(S[t][e] - mx_a);
+          const float pb = (S[t][2 + e] == -INFINITY) ? 0.f : exp2f(S[t][2 + e] - mx_b);
+          S[t][e] = pa;
+          S[t][2 + e] = pb;
+          l_a += pa;
+          l_b += pb;
+        }
+      }
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      // ---- O = P V over the chunk: 16 rows x (D/8) n8 tiles
+      float O[D / 8][4];
+#pragma unroll
+      for (int t = 0; t < D / 8; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < CH / 16; ++kk) {
+        const uint32_t a0 = pack_bf16(S[2 * kk][0], S[2 * kk][1]);
+        const uint32_t a1 = pack_bf16(S[2 * kk][2], S[2 * kk][3]);
+        const uint32_t a2 = pack_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1]);
+        const uint32_t a3 = pack_bf16(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          uint32_t b0, b1, b2, b3;
+          const int key = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+          ldsm_x4_t(vb + swz<D>(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
+          mma_16816(O[2 * dt], a0, a1, a2, a3, b0, b1);
+          mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      // ---- chunk partials
+      float* pa = part + (size_t)c * stride_c + (size_t)qa * (D + 2);
+      float* pb = part + (size_t)c * stride_c + (size_t)qb2 * (D + 2);
+      const bool wa = qa < nq_tile, wb = qb2 < nq_tile;
+#pragma unroll
+      for (int t = 0; t < D / 8; ++t) {
+        const int col = 8 * t + 2 * (lane & 3);
+        if (wa) {
+          pa[2 + col] = O[t][0];
+          pa[3 + col] = O[t][1];
+        }
+        if (wb) {
+          pb[2 + col] = O[t][2];
+          pb[3 + col] = O[t][3];
+        }
+      }
+      if ((lane & 3) == 0) {
+        if (wa) {
+          pa[0] = mx_a;
+          pa[1] = l_a;
+        }
+        if (wb) {
+          pb[0] = mx_b;
+          pb[1] = l_b;
+        }
+      }
+    }
+  }
+  attn_finish<__nv_bfloat16>(a, part, grp_id, stride_c, nq_tile, qv0, g, s, sk.n_ch, &s_last);
+}
+
+// ------------------------------------------------------------------- host
 
 size_t attn_workspace(const AttnDesc& a) {
   AttnGeom g = attn_geom(a);
@@ -194,12 +426,19 @@ cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   AttnGeom g = attn_geom(a);
   if (a.n_seqs == 0 || a.rows == 0) return cudaSuccess;
   dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);
-  size_t smem = (size_t)(2 * kAttnCH * a.d + kAttnWarps * a.d + kAttnWarps * kAttnCH) * sizeof(float);
   if (a.dtype == DFLASH_BF16) {
-    auto k = attn_simt_kernel<__nv_bfloat16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
+    const size_t smem = (size_t)(kAttnQT + 2 * kMmaCH) * a.d * 2;
+    if (a.d == 128) {
+      auto k = attn_mma_kernel<128>;
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
+    } else {
+      auto k = attn_mma_kernel<64>;
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
+    }
   } else {
+    const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);
     auto k = attn_simt_kernel<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
