@@ -10,9 +10,19 @@
 // offsets and chunks past a row's last visible key contribute exact zeros, so
 // a row's output does not depend on how many rows share the launch.
 //
-// bf16 path: mma.sync m16n8k16 tensor-core tiles (S = Q K^T and O = P V with
-// P rounded to bf16), K/V/Q staged by cp.async into XOR-swizzled shared
-// memory and read with ldmatrix.  fp32 path: CUDA-core dot products.
+// fp32 path: CUDA-core dot products, chunk partials in the workspace, merged
+// by the last CTA of the group.
+//
+// bf16 path: a thread-block cluster of NC CTAs per (sequence, kv head, query
+// tile).  CTA rank r owns chunks r, r + NC, r + 2 NC, ... (CH = 128 key slots
+// each, at fixed absolute offsets), streams them through double-buffered
+// cp.async into XOR-swizzled shared memory, and runs mma.sync m16n8k16 tiles
+// (S = Q K^T, O = P V with P rounded to bf16) with an online softmax over its
+// chunks in order.  The NC partials are then merged in rank order through
+// distributed shared memory; cluster barriers are hardware barriers over
+// co-scheduled CTAs, so nothing spins and nothing round-trips through HBM.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -248,67 +258,109 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_mma_kernel(const __grid_constant__ AttnDesc a, int n_qt) {
-  constexpr int CH = kMmaCH;
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-  extern __shared__ __align__(128) uint8_t asm_raw[];
-  uint8_t* Qs = asm_raw;                 // [64][D]
-  uint8_t* Ks = Qs + kAttnQT * D * 2;    // [CH][D]
-  uint8_t* Vs = Ks + CH * D * 2;         // [CH][D]
-  __shared__ int s_last;
+namespace cg = cooperative_groups;
 
-  const int c = blockIdx.x;
+template <int D, int NC>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __grid_constant__ AttnDesc a,
+                                                                        int n_qt) {
+  constexpr int CH = kMmaCH;
+  constexpr int CPR = D / 8;         // 16-byte chunks per row
+  constexpr int TILE = CH * D * 2;   // one K or V chunk tile, bytes
+  constexpr int PST = D + 4;         // floats per row of the partial (16-byte aligned rows)
+  extern __shared__ __align__(128) uint8_t smem_att[];
+  uint8_t* Qs = smem_att;            // [64][D]
+  uint8_t* KV = Qs + kAttnQT * D * 2;  // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
+  float* psm = reinterpret_cast<float*>(KV);  // [64][PST] partial, written after the chunk loop
+
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
   const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
   const int s = blockIdx.z;
   const int grp = a.nq / a.nkv;
   const int nqv = a.rows * grp;
   const int QD = a.nq * D;
   const int P = a.base_pos[s];
-  const SeqKeys sk = seq_keys(a, P, gridDim.x, CH);
+  SeqKeys sk;
+  if (a.mode == DFLASH_ATTN_CAUSAL) {
+    sk.n_ctx = min(max(P + a.rows, 0), a.cap);
+    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
+    sk.n_ch = sk.n_ctx_ch;
+  } else {
+    sk.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), a.cap);
+    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
+    sk.n_ch = sk.n_ctx_ch + 1;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qv0 = qt * kAttnQT;
   const int nq_tile = min(kAttnQT, nqv - qv0);
-  const size_t grp_id = ((size_t)s * a.nkv + g) * n_qt + qt;
-  const int stride_c = kAttnQT * (D + 2);
-  float* part = a.partials + grp_id * (size_t)gridDim.x * stride_c;
+  const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
+  const uint32_t qb = __cvta_generic_to_shared(Qs);
+  const uint32_t kvb = __cvta_generic_to_shared(KV);
 
-  if (c < sk.n_ch) {
+  auto stage_chunk = [&](int c, int buf) {
     const __nv_bfloat16* kp;
     const __nv_bfloat16* vp;
     int nk, slot0;
     chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
-    const uint32_t qb = __cvta_generic_to_shared(Qs), kb = __cvta_generic_to_shared(Ks),
-                   vb = __cvta_generic_to_shared(Vs);
-    // ---- stage K, V (rows >= nk zero) and Q (rows >= nq_tile zero)
+    uint8_t* Kt = KV + 2 * buf * TILE;
+    uint8_t* Vt = Kt + TILE;
+    const uint32_t kb = kvb + 2 * buf * TILE, vb = kb + TILE;
     for (int t = threadIdx.x; t < CH * CPR; t += blockDim.x) {
       const int j = t / CPR, ch = t % CPR;
       if (j < nk) {
         cp_async16(kb + swz<D>(j, ch), kp + (size_t)j * D + ch * 8);
         cp_async16(vb + swz<D>(j, ch), vp + (size_t)j * D + ch * 8);
       } else {
-        *reinterpret_cast<uint4*>(Ks + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Vs + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Kt + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Vt + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
       }
     }
-    for (int t = threadIdx.x; t < kAttnQT * CPR; t += blockDim.x) {
-      const int qi = t / CPR, ch = t % CPR;
-      if (qi < nq_tile) {
-        const int qv = qv0 + qi;
-        const int row = qv / grp, head = g * grp + qv % grp;
-        const __nv_bfloat16* q =
-            reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * a.rows + row) * QD + (size_t)head * D;
-        cp_async16(qb + swz<D>(qi, ch), q + ch * 8);
-      } else {
-        *reinterpret_cast<uint4*>(Qs + swz<D>(qi, ch)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
+  };
 
-    const int r0 = 16 * warp;  // this warp's 16 query vectors
-    if (r0 < nq_tile) {
-      // ---- S = Q K^T over the CH keys: 16 rows x (CH/8) n8 tiles
+  // ---- stage Q (rows >= nq_tile zero) with the first chunk, then the second
+  for (int t = threadIdx.x; t < kAttnQT * CPR; t += blockDim.x) {
+    const int qi = t / CPR, ch = t % CPR;
+    if (qi < nq_tile) {
+      const int qv = qv0 + qi;
+      const int row = qv / grp, head = g * grp + qv % grp;
+      const __nv_bfloat16* q =
+          reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * a.rows + row) * QD + (size_t)head * D;
+      cp_async16(qb + swz<D>(qi, ch), q + ch * 8);
+    } else {
+      *reinterpret_cast<uint4*>(Qs + swz<D>(qi, ch)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (nmine > 0) stage_chunk(rank, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  if (nmine > 1) stage_chunk(rank + NC, 1);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  const int r0 = 16 * warp;  // this warp's 16 query vectors
+  const bool warp_on = r0 < nq_tile;
+  const int qa = r0 + (lane >> 2), qb2 = qa + 8;  // the two rows this thread holds
+  const int row_a = (qv0 + qa) / grp, row_b = (qv0 + qb2) / grp;
+  const float scale = rsqrtf((float)D) * kLog2e;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float O[D / 8][4];
+#pragma unroll
+  for (int t = 0; t < D / 8; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
+
+  for (int i = 0; i < nmine; ++i) {
+    if (i + 1 < nmine)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int c = rank + i * NC, buf = i & 1;
+    const uint32_t kb = kvb + 2 * buf * TILE, vb = kb + TILE;
+    int nk, slot0;
+    {
+      const __nv_bfloat16* kp;
+      const __nv_bfloat16* vp;
+      chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
+    }
+    if (warp_on) {
+      // S = Q K^T over the chunk's CH keys
       float S[CH / 8][4];
 #pragma unroll
       for (int t = 0; t < CH / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
@@ -325,50 +377,59 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_mma_kernel(const __grid_
           mma_16816(S[2 * nt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-      // ---- mask, scale (log2 units), row max / sum over the quad
-      const float scale = rsqrtf((float)D) * kLog2e;
-      const int qa = r0 + (lane >> 2), qb2 = qa + 8;  // the two rows this thread holds
-      const int lim_a = (a.mode == DFLASH_ATTN_CAUSAL) ? P + (qv0 + qa) / grp - slot0 : CH;
-      const int lim_b = (a.mode == DFLASH_ATTN_CAUSAL) ? P + (qv0 + qb2) / grp - slot0 : CH;
-      float mx_a = -INFINITY, mx_b = -INFINITY;
+      // mask, scale to log2 units, chunk maxima
+      const bool causal = a.mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
+      const int lim_a = causal ? P + row_a - slot0 : CH;
+      const int lim_b = causal ? P + row_b - slot0 : CH;
+      float cm_a = -INFINITY, cm_b = -INFINITY;
 #pragma unroll
       for (int t = 0; t < CH / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int j = 8 * t + 2 * (lane & 3) + e;
-          const bool ok_a = j < nk && j <= lim_a;
-          const bool ok_b = j < nk && j <= lim_b;
-          S[t][e] = ok_a ? S[t][e] * scale : -INFINITY;
-          S[t][2 + e] = ok_b ? S[t][2 + e] * scale : -INFINITY;
-          mx_a = fmaxf(mx_a, S[t][e]);
-          mx_b = fmaxf(mx_b, S[t][2 + e]);
+          S[t][e] = (j < nk && j <= lim_a) ? S[t][e] * scale : -INFINITY;
+          S[t][2 + e] = (j < nk && j <= lim_b) ? S[t][2 + e] * scale : -INFINITY;
+          cm_a = fmaxf(cm_a, S[t][e]);
+          cm_b = fmaxf(cm_b, S[t][2 + e]);
         }
       }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      float l_a = 0.f, l_b = 0.f;
+      cm_a = fmaxf(cm_a, __shfl_xor_sync(0xffffffffu, cm_a, 1));
+      cm_a = fmaxf(cm_a, __shfl_xor_sync(0xffffffffu, cm_a, 2));
+      cm_b = fmaxf(cm_b, __shfl_xor_sync(0xffffffffu, cm_b, 1));
+      cm_b = fmaxf(cm_b, __shfl_xor_sync(0xffffffffu, cm_b, 2));
+      // online softmax: rescale the running state to the new maximum
+      const float mn_a = fmaxf(m_a, cm_a), mn_b = fmaxf(m_b, cm_b);
+      const float al_a = (m_a == -INFINITY) ? 0.f : exp2f(m_a - mn_a);
+      const float al_b = (m_b == -INFINITY) ? 0.f : exp2f(m_b - mn_b);
+      float sl_a = 0.f, sl_b = 0.f;
 #pragma unroll
       for (int t = 0; t < CH / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float pa = (S[t][e] == -INFINITY) ? 0.f : exp2f(S[t][e] - mx_a);
-          const float pb = (S[t][2 + e] == -INFINITY) ? 0.f : exp2f(S[t][2 + e] - mx_b);
+          const float pa = (S[t][e] == -INFINITY) ? 0.f : exp2f(S[t][e] - mn_a);
+          const float pb = (S[t][2 + e] == -INFINITY) ? 0.f : exp2f(S[t][2 + e] - mn_b);
           S[t][e] = pa;
           S[t][2 + e] = pb;
-          l_a += pa;
-          l_b += pb;
+          sl_a += pa;
+          sl_b += pb;
         }
       }
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-      // ---- O = P V over the chunk: 16 rows x (D/8) n8 tiles
-      float O[D / 8][4];
+      sl_a += __shfl_xor_sync(0xffffffffu, sl_a, 1);
+      sl_a += __shfl_xor_sync(0xffffffffu, sl_a, 2);
+      sl_b += __shfl_xor_sync(0xffffffffu, sl_b, 1);
+      sl_b += __shfl_xor_sync(0xffffffffu, sl_b, 2);
+      l_a = fmaf(l_a, al_a, sl_a);
+      l_b = fmaf(l_b, al_b, sl_b);
+      m_a = mn_a;
+      m_b = mn_b;
 #pragma unroll
-      for (int t = 0; t < D / 8; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
+      for (int t = 0; t < D / 8; ++t) {
+        O[t][0] *= al_a;
+        O[t][1] *= al_a;
+        O[t][2] *= al_b;
+        O[t][3] *= al_b;
+      }
+      // O += P V
 #pragma unroll
       for (int kk = 0; kk < CH / 16; ++kk) {
         const uint32_t a0 = pack_bf16(S[2 * kk][0], S[2 * kk][1]);
@@ -384,40 +445,129 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_mma_kernel(const __grid_
           mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-      // ---- chunk partials
-      float* pa = part + (size_t)c * stride_c + (size_t)qa * (D + 2);
-      float* pb = part + (size_t)c * stride_c + (size_t)qb2 * (D + 2);
-      const bool wa = qa < nq_tile, wb = qb2 < nq_tile;
+    }
+    __syncthreads();  // every warp is done with this buffer
+    if (i + 2 < nmine) stage_chunk(rank + (i + 2) * NC, buf);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+
+  // ---- this CTA's partial (m, l, O) per query vector into its shared memory
+  if (warp_on) {
+    float* pa = psm + (size_t)qa * PST;
+    float* pb = psm + (size_t)qb2 * PST;
 #pragma unroll
-      for (int t = 0; t < D / 8; ++t) {
-        const int col = 8 * t + 2 * (lane & 3);
-        if (wa) {
-          pa[2 + col] = O[t][0];
-          pa[3 + col] = O[t][1];
-        }
-        if (wb) {
-          pb[2 + col] = O[t][2];
-          pb[3 + col] = O[t][3];
-        }
-      }
-      if ((lane & 3) == 0) {
-        if (wa) {
-          pa[0] = mx_a;
-          pa[1] = l_a;
-        }
-        if (wb) {
-          pb[0] = mx_b;
-          pb[1] = l_b;
-        }
-      }
+    for (int t = 0; t < D / 8; ++t) {
+      const int col = 8 * t + 2 * (lane & 3);
+      pa[col] = O[t][0];
+      pa[col + 1] = O[t][1];
+      pb[col] = O[t][2];
+      pb[col + 1] = O[t][3];
+    }
+    if ((lane & 3) == 0) {
+      pa[D] = m_a;
+      pa[D + 1] = l_a;
+      pb[D] = m_b;
+      pb[D + 1] = l_b;
     }
   }
-  attn_finish<__nv_bfloat16>(a, part, grp_id, stride_c, nq_tile, qv0, g, s, sk.n_ch, &s_last);
+  cl.sync();
+
+  // ---- merge the NC partials in rank order; rank r owns rows [r*RP, (r+1)*RP)
+  const int RP = (nq_tile + NC - 1) / NC;
+  const int q_lo = rank * RP, q_hi = min(nq_tile, q_lo + RP);
+  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out);
+  for (int t = threadIdx.x; t < (q_hi > q_lo ? (q_hi - q_lo) * D : 0); t += blockDim.x) {
+    const int qi = q_lo + t / D, e = t % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < NC; ++r) M = fmaxf(M, cl.map_shared_rank(psm, r)[(size_t)qi * PST + D]);
+    float L = 0.f, Ov = 0.f;
+#pragma unroll
+    for (int r = 0; r < NC; ++r) {
+      const float* pr = cl.map_shared_rank(psm, r) + (size_t)qi * PST;
+      const float mr = pr[D];
+      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+      L = fmaf(pr[D + 1], w, L);
+      Ov = fmaf(pr[e], w, Ov);
+    }
+    const int qv = qv0 + qi;
+    const int row = qv / grp, head = g * grp + qv % grp;
+    outp[((size_t)s * a.rows + row) * QD + (size_t)head * D + e] = __float2bfloat16_rn(L > 0.f ? Ov / L : 0.f);
+  }
+  cl.sync();  // peers keep their shared memory until every rank has read it
 }
 
 // ------------------------------------------------------------------- host
 
+namespace {
+
+// Cluster width: 16 CTAs when few (sequence, head, tile) groups must fill
+// the GPU, else 8.  Depends on the batch shape, never on the row count alone,
+// so decode (1 row) and verification (a block) of one batch use the same.
+int attn_nc(const AttnDesc& a, int n_qt) { return (long)a.n_seqs * a.nkv * n_qt <= 16 ? 16 : 8; }
+
+// Can this device co-schedule a 16-CTA cluster of this kernel?
+template <int D>
+bool wide_clusters_fit(size_t smem);
+
+template <int D, int NC>
+cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
+  auto k = attn_cluster_kernel<D, NC>;
+  const size_t smem = (size_t)kAttnQT * D * 2 + 4 * (size_t)kMmaCH * D * 2;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (NC > 8) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(NC, a.nkv * n_qt, a.n_seqs);
+  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = NC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, n_qt);
+}
+
+template <int D>
+bool wide_clusters_fit(size_t smem) {
+  auto k = attn_cluster_kernel<D, 16>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 16;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
+}  // namespace
+
 size_t attn_workspace(const AttnDesc& a) {
+  if (a.dtype == DFLASH_BF16) return 0;  // merged on chip
   AttnGeom g = attn_geom(a);
   return (size_t)a.n_seqs * a.nkv * g.n_qt * g.nch * kAttnQT * (a.d + 2) * sizeof(float);
 }
@@ -425,24 +575,18 @@ size_t attn_workspace(const AttnDesc& a) {
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   AttnGeom g = attn_geom(a);
   if (a.n_seqs == 0 || a.rows == 0) return cudaSuccess;
-  dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);
   if (a.dtype == DFLASH_BF16) {
-    const size_t smem = (size_t)(kAttnQT + 2 * kMmaCH) * a.d * 2;
-    if (a.d == 128) {
-      auto k = attn_mma_kernel<128>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
-    } else {
-      auto k = attn_mma_kernel<64>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
-    }
-  } else {
-    const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);
-    auto k = attn_simt_kernel<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
+    const size_t smem = (size_t)kAttnQT * a.d * 2 + 4 * (size_t)kMmaCH * a.d * 2;
+    const bool w16 = attn_nc(a, g.n_qt) == 16 &&
+                     (a.d == 128 ? wide_clusters_fit<128>(smem) : wide_clusters_fit<64>(smem));
+    if (a.d == 128) return w16 ? launch_cluster<128, 16>(a, g.n_qt, st) : launch_cluster<128, 8>(a, g.n_qt, st);
+    return w16 ? launch_cluster<64, 16>(a, g.n_qt, st) : launch_cluster<64, 8>(a, g.n_qt, st);
   }
+  dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);
+  const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);
+  auto k = attn_simt_kernel<float>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
   return cudaGetLastError();
 }
 
