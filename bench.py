@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--trace-replays", type=int, default=5)
+    p.add_argument("--layers", default="", help="T,D: shrink to T target / D draft layers (profiling captures "
+                   "only; the line then names the reduced config)")
     return p.parse_args()
 
 
@@ -326,6 +328,11 @@ def run_ours(args):
         dist.barrier()
     b.build()
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        t_l, d_l = (int(x) for x in args.layers.split(","))
+        w = dataclasses.replace(w, name=f"{w.name}-layers{t_l},{d_l}", target=dataclasses.replace(w.target, layers=t_l),
+                                draft=dataclasses.replace(w.draft, layers=d_l))
     eng, lens, planted = setup_workload(w, seed=0)
     planted_t, ks = (planted if planted else (None, None))
     base0, anchor0 = eng.base_pos.clone(), eng.anchor.clone()
