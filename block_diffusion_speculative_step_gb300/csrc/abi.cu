@@ -382,6 +382,11 @@ size_t carve_draft(Bump& b, const dflash_draft_args* a, int sms, DraftScratch& s
 
 }  // namespace
 
+namespace dfl {
+// Sets the thread-local error text from another translation unit.
+int abi_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace dfl
+
 // =================================================================== ABI
 
 extern "C" {

@@ -28,7 +28,8 @@ DFLASH_MAX_LAYERS = 16
 EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", "dflash_fuse_context",
            "dflash_draft_block", "dflash_verify_accept", "dflash_path_select", "dflash_workspace_bytes",
            "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
-           "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end")
+           "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
+           "dflash_verify_accept_noalloc")
 DFLASH_TRACE_FAMILIES = 10
 
 
@@ -129,6 +130,8 @@ def lib(path: str | None = None):
         L.dflash_last_error.restype = C.c_char_p
         L.dflash_abi_version.restype = i32
         L.dflash_trace_begin.argtypes = [i32]
+        L.dflash_verify_accept_noalloc.argtypes = [vp, vp, vp]
+        L.dflash_verify_accept_noalloc.restype = C.c_int
         L.dflash_trace_read.argtypes = [C.POINTER(dflash_trace_stat), i32]
         _lib = L
     return _lib
@@ -195,6 +198,12 @@ def dflash_draft_block(args: dflash_draft_args, ws_ptr: int, ws_bytes: int, stre
 
 def dflash_verify_accept(args: dflash_verify_args, ws_ptr: int, ws_bytes: int, stream=None):
     _call("dflash_verify_accept", args, ws_ptr, ws_bytes, stream)
+
+
+def dflash_verify_accept_noalloc(args: dflash_verify_args, status_ptr: int = 0, stream=None):
+    """dflash_verify_accept with the library's fixed 8 MiB device scratch
+    instead of a workspace (for callers that cannot allocate)."""
+    _check(lib().dflash_verify_accept_noalloc(C.byref(args), status_ptr, _stream(stream)))
 
 
 def dflash_path_select(args: dflash_path_args, ws_ptr: int, ws_bytes: int, stream=None):

@@ -332,6 +332,32 @@ int dflash_trace_pause(void);
 int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats);
 int dflash_trace_end(void);
 
+/*
+ * Allocation-free verification + acceptance.  (No counterpart in the paper:
+ * this is a deployment convenience of this library.)
+ *
+ * Same arguments, computation and outputs as dflash_verify_accept, but the
+ * scratch memory lives in a fixed 8 MiB array inside the library's device
+ * image instead of a caller-provided workspace.  It serves callers that
+ * cannot allocate device memory at the point of the call: a runtime whose
+ * memory is owned by a pre-sized arena or pool, a plugin that is handed
+ * only input and output buffers, or code that must not allocate on its hot
+ * path.  Every GPU that loads the library holds the 8 MiB array until the
+ * process exits.
+ *  - Rejects, with DFLASH_ERR_WORKSPACE and a message, any call whose scratch
+ *    (dflash_workspace_bytes(DFLASH_OP_VERIFY, a)) exceeds 8 MiB.
+ *  - Calls no cudaMalloc/cudaFree.  The first call on a device looks up the
+ *    array's device address once for that device (with it current); make
+ *    that first call before any stream capture.
+ *  - All calls share the one array: each call clears its status word and
+ *    arrival counters first, and calls whose work overlaps on the GPU (for
+ *    example on two streams at once) race.
+ *  - status_out (optional, device int32) receives this call's device status
+ *    bits: 0 = OK, bit 0 = a NaN reached the argmax, bit 1 = a bounded wait
+ *    expired.
+ */
+int dflash_verify_accept_noalloc(const dflash_verify_args* a, int32_t* status_out, dflash_stream_t stream);
+
 /* Thread-local description of the last failure. */
 const char* dflash_last_error(void);
 
