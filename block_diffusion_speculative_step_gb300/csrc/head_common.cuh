@@ -65,19 +65,20 @@ __device__ __forceinline__ Top2 ldcg_top2(const Top2* p) {
   return t;
 }
 
-// Called by every CTA (all its threads) after it stored its per-token triples
-// at part[blockIdx.x * M + m].  The last CTA to arrive merges them and writes
+// Called by every CTA (all its threads) once its per-token triples are stored
+// in part[0 .. n_parts)[M].  The last of n_arrivals CTAs to arrive merges them and writes
 // the mode's outputs.  The merge (greater value wins, lower index on equal
 // values; second = the largest other value) is associative and commutative,
 // so the warp-parallel reduction below gives the same result in any order.
-__device__ __forceinline__ void head_finish(const HeadDesc& h, int nblocks, const Top2* part, int* s_last) {
+__device__ __forceinline__ void head_finish(const HeadDesc& h, int n_arrivals, int n_parts, const Top2* part,
+                                            int* s_last) {
   __shared__ int s_arg[kHeadMaxM];
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t* ctr = h.counters + kCtrHead;
     uint32_t old = atomicAdd(ctr, 1u);
-    *s_last = (old == (uint32_t)nblocks - 1);
+    *s_last = (old == (uint32_t)n_arrivals - 1);
     if (*s_last) *ctr = 0u;
   }
   __syncthreads();
@@ -88,7 +89,7 @@ __device__ __forceinline__ void head_finish(const HeadDesc& h, int nblocks, cons
   for (int m = threadIdx.x >> 5; m < M; m += nwarps) {
     if (!head_row_used(h, m)) continue;
     Top2 t = top2_empty();
-    for (int b = lane; b < nblocks; b += 32) t = top2_merge(t, ldcg_top2(part + (size_t)b * M + m));
+    for (int b = lane; b < n_parts; b += 32) t = top2_merge(t, ldcg_top2(part + (size_t)b * M + m));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Top2 u;

@@ -135,8 +135,8 @@ size_t head_workspace(const HeadDesc& h, int num_sms);
 cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st);
 cudaError_t launch_head_simt(const HeadDesc& h, int num_sms, cudaStream_t st);
 bool head_tc_supported(const HeadDesc& h);
-size_t head_tc_workspace(const HeadDesc& h);
-cudaError_t launch_head_tc(const HeadDesc& h, cudaStream_t st);
+size_t head_tc_workspace(const HeadDesc& h, int num_sms);
+cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st);
 
 // path selector
 cudaError_t launch_path_select(const PathDesc& p, cudaStream_t st);

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace dfl {
 
@@ -138,6 +139,8 @@ __device__ __forceinline__ void attn_finish(const AttnDesc& a, const float* part
 
 template <typename T>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_simt_kernel(const __grid_constant__ AttnDesc a, int n_qt) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ float sm[];
   constexpr int CH = kSimtCH;
   const int d = a.d, ld = d + 1;  // padded rows: lanes reading different keys hit different banks
@@ -263,6 +266,8 @@ namespace cg = cooperative_groups;
 template <int D, int NC>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __grid_constant__ AttnDesc a,
                                                                         int n_qt) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int CH = kMmaCH;
   constexpr int CPR = D / 8;         // 16-byte chunks per row
   constexpr int TILE = CH * D * 2;   // one K or V chunk tile, bytes
@@ -527,13 +532,15 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = NC;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k, a, n_qt);
 }
 
@@ -586,8 +593,7 @@ cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);
   auto k = attn_simt_kernel<float>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k<<<grid, kAttnWarps * 32, smem, st>>>(a, g.n_qt);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(kAttnWarps * 32), smem, st, a, g.n_qt);
 }
 
 }  // namespace dfl

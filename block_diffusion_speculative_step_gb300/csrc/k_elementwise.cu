@@ -3,12 +3,15 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace dfl {
 
 // cos_sin[p][i] = (cos(p w_i), sin(p w_i)), w_i = theta^(-2i/d), evaluated in
 // double so large positions keep full float accuracy.
 __global__ void rope_table_kernel(double theta, int d, int max_pos, float* cs) {
+  pdl_wait();
+  pdl_launch_dependents();
   int half = d / 2;
   long n = (long)max_pos * half;
   for (long t = blockIdx.x * (long)blockDim.x + threadIdx.x; t < n; t += (long)gridDim.x * blockDim.x) {
@@ -25,7 +28,7 @@ cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaSt
   int blocks = (int)((n + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  rope_table_kernel<<<blocks, 256, 0, st>>>((double)theta, d, max_pos, cs);
+  return launch_pdl(rope_table_kernel, dim3(blocks), dim3(256), 0, st, (double)theta, d, max_pos, cs);
   return cudaGetLastError();
 }
 
@@ -33,6 +36,8 @@ cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaSt
 template <typename T>
 __global__ void embed_kernel(const T* __restrict__ E, int H, int rows, const int32_t* __restrict__ first,
                              const int32_t* __restrict__ rest, int fill, float* __restrict__ h) {
+  pdl_wait();
+  pdl_launch_dependents();
   int m = blockIdx.x;
   int s = m / rows, i = m % rows;
   int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
@@ -46,9 +51,9 @@ cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, 
   int M = n_seqs * rows;
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    embed_kernel<__nv_bfloat16><<<M, 256, 0, st>>>((const __nv_bfloat16*)E, H, rows, first, rest, fill, h);
+    return launch_pdl(embed_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, (const __nv_bfloat16*)E, H, rows, first, rest, fill, h);
   else
-    embed_kernel<float><<<M, 256, 0, st>>>((const float*)E, H, rows, first, rest, fill, h);
+    return launch_pdl(embed_kernel<float>, dim3(M), dim3(256), 0, st, (const float*)E, H, rows, first, rest, fill, h);
   return cudaGetLastError();
 }
 
@@ -58,6 +63,8 @@ cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, 
 template <typename T>
 __global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, int H, float eps,
                                T* __restrict__ x) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[32];
   const float* r = h + (size_t)blockIdx.x * H;
   float ss = 0.f;
@@ -81,9 +88,9 @@ cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int 
                            cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    rmsnorm_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(h, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)x);
+    return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, h, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)x);
   else
-    rmsnorm_kernel<float><<<M, 256, 0, st>>>(h, (const float*)g, H, eps, (float*)x);
+    return launch_pdl(rmsnorm_kernel<float>, dim3(M), dim3(256), 0, st, h, (const float*)g, H, eps, (float*)x);
   return cudaGetLastError();
 }
 
@@ -91,6 +98,8 @@ cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int 
 template <typename T>
 __global__ void store_tap_kernel(const float* __restrict__ h, int H, T* __restrict__ tap, int stride,
                                  int offset) {
+  pdl_wait();
+  pdl_launch_dependents();
   const float* r = h + (size_t)blockIdx.x * H;
   T* o = tap + (size_t)blockIdx.x * stride + offset;
   for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f<T>(r[k]);
@@ -100,14 +109,16 @@ cudaError_t launch_store_tap(int dtype, const float* h, int M, int H, void* tap,
                              cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    store_tap_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(h, H, (__nv_bfloat16*)tap, stride, offset);
+    return launch_pdl(store_tap_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, h, H, (__nv_bfloat16*)tap, stride, offset);
   else
-    store_tap_kernel<float><<<M, 256, 0, st>>>(h, H, (float*)tap, stride, offset);
+    return launch_pdl(store_tap_kernel<float>, dim3(M), dim3(256), 0, st, h, H, (float*)tap, stride, offset);
   return cudaGetLastError();
 }
 
 template <typename T>
 __global__ void to_f32_kernel(const T* __restrict__ src, size_t n, float* __restrict__ dst) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     dst[i] = to_f<T>(src[i]);
 }
@@ -116,9 +127,9 @@ cudaError_t launch_to_f32(int dtype, const void* src, size_t n, float* dst, cuda
   if (n == 0) return cudaSuccess;
   int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
   if (dtype == DFLASH_BF16)
-    to_f32_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)src, n, dst);
+    return launch_pdl(to_f32_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, st, (const __nv_bfloat16*)src, n, dst);
   else
-    to_f32_kernel<float><<<blocks, 256, 0, st>>>((const float*)src, n, dst);
+    return launch_pdl(to_f32_kernel<float>, dim3(blocks), dim3(256), 0, st, (const float*)src, n, dst);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace dfl {
 
@@ -14,6 +15,8 @@ constexpr int kSimtTok = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kSimtWarps * 32) gemm_simt_kernel(const __grid_constant__ GemmDesc g) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int U = epi_units(g);
@@ -77,9 +80,9 @@ cudaError_t launch_gemm_simt(const GemmDesc& g, cudaStream_t st) {
   long blocks = (units + kSimtWarps - 1) / kSimtWarps;
   if (blocks > 65535) blocks = 65535;
   if (g.dtype == DFLASH_BF16)
-    gemm_simt_kernel<__nv_bfloat16><<<(int)blocks, kSimtWarps * 32, 0, st>>>(g);
+    return launch_pdl(gemm_simt_kernel<__nv_bfloat16>, dim3((int)blocks), dim3(kSimtWarps * 32), 0, st, g);
   else
-    gemm_simt_kernel<float><<<(int)blocks, kSimtWarps * 32, 0, st>>>(g);
+    return launch_pdl(gemm_simt_kernel<float>, dim3((int)blocks), dim3(kSimtWarps * 32), 0, st, g);
   return cudaGetLastError();
 }
 

@@ -1,90 +1,184 @@
-// k_gemm_tc.cu -- tcgen05 GEMM Y[m][n] = sum_k X[m][k] W[n][k] for small
-// token counts (M <= 256), with the same fused epilogues as the SIMT GEMM.
+// k_gemm_tc.cu -- persistent stream-K tcgen05 kernel for every weight-
+// streaming product of the cycle: the layer GEMMs Y[m][n] = sum_k X[m][k]
+// W[n][k] (fused epilogues: RoPE + Q/KV scatter, SwiGLU, residual add, store)
+// and the LM head with the greedy argmax fused into its epilogue.
 //
-// Swap-AB: the weight tile (128 output rows x 64 k) is the MMA's A operand
-// (M = 128) and the token rows are the B operand (N = BN in 16..256), so the
-// one bf16 weight stream -- the dominant HBM traffic at small batch -- fills
-// the 128-row tensor-core side.  Per CTA: warp 0 issues TMA loads (128-byte
-// swizzle) into a STAGES-deep mbarrier ring, warp 1 allocates TMEM and one
-// lane issues tcgen05.mma into an fp32 TMEM accumulator, warps 2-5 drain TMEM
-// with tcgen05.ld and run the epilogue.  K is split over `splits` CTAs per
-// tile; the split count depends only on (tiles, K, SM count), never on M, and
-// the last CTA of a tile sums the fp32 partials in split order, so a token
-// row's result is the same whatever other rows share the launch.  No CTA waits
-// on another.  Every mbarrier wait is bounded (ST_TIMEOUT).
+// Swap-AB: a 128-row weight tile is the MMA's A operand (M = 128) and the
+// token rows are the B operand (N = BN in 16..256); at small batch the one
+// bf16 weight stream is the whole HBM traffic.  One CTA per SM.  The
+// (tile, 64-wide k-block) space is cut into G equal contiguous runs, one per
+// CTA (balanced to one k-block); a run's piece inside one tile accumulates in
+// TMEM.  Roles per CTA: warp 0 streams W and X boxes with TMA (128-byte
+// swizzle) through a STAGES-deep mbarrier ring, warp 1 allocates TMEM and one
+// lane issues tcgen05.mma into one of two TMEM accumulators, warps 2-5 drain
+// the other accumulator with tcgen05.ld, so a piece's epilogue overlaps the
+// next piece's loads.  A tile split over several CTAs is finished by the
+// piece that completes its k range, summing the fp32 partials in k order:
+// the run boundaries depend only on (tiles, K, SM count), never on M, so a
+// token row's result does not depend on the other rows in the launch.
+// Weight loads for the first stages are issued before griddepcontrol.wait,
+// overlapping the predecessor kernel's tail.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include "epilogue.cuh"
+#include "head_common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace dfl {
 
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kTcA = 128 * 128;  // one 128 x 64 bf16 weight tile, bytes
+constexpr int kTcA = 128 * 128;  // one 128 x 64 bf16 weight box, bytes
 
-struct TcParams {  // CUtensorMap members keep it 64-byte aligned
+enum TcMode : int { TC_GEMM = 0, TC_HEAD = 1 };
+
+struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   CUtensorMap wmap[kMaxSeg];
   CUtensorMap xmap;
   GemmDesc g;
+  HeadDesc h;
+  int mode;
   int tiles_per_seg;
-  int splits;
-  int nkb;  // K / 64
-  float* part;
+  int n_tiles;
+  int nkb;        // k-blocks per tile (K / 64)
+  long long T;    // n_tiles * nkb
+  int G;          // CTAs (runs)
+  int M;          // token rows
+  float* part;    // partial slots [n_tiles + G][BN][128]
+  Top2* tops;     // LM head: per-tile triples [n_tiles][M]
   uint32_t* counters;
   uint32_t* status;
 };
 
 template <int BN>
 struct TcCfg {
-  static constexpr int B = BN * 128;
-  static constexpr int STAGE = kTcA + B;
+  static constexpr int STAGE = kTcA + BN * 128;
+  // <= 100 KB below BN = 128 so the next kernel's CTA can share the SM (PDL)
   static constexpr int BUDGET = BN <= 64 ? 100 * 1024 : 200 * 1024;
-  static constexpr int STAGES = (BUDGET / STAGE) > 8 ? 8 : (BUDGET / STAGE);
-  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
-  static constexpr int XCH = 16 * 128 * 4;  // epilogue exchange tile
+  static constexpr int STAGES = (BUDGET / STAGE) > 10 ? 10 : (BUDGET / STAGE);
+  static constexpr int ACC = BN < 32 ? 32 : BN;  // columns of one accumulator
+  static constexpr int TMEM_COLS = 2 * ACC;       // double-buffered
+  static constexpr int XCH = 16 * 128 * 4;        // epilogue exchange tile
   static constexpr int SMEM = STAGES * STAGE + XCH + 256 + 1024;
 };
+
+__host__ __device__ __forceinline__ long long run_start(long long T, int G, int c) { return (T * c) / G; }
+
+__device__ __forceinline__ int run_of(long long p, long long T, int G) {
+  int c = (int)((p * G) / T);
+  while (c + 1 <= G && run_start(T, G, c + 1) <= p) ++c;
+  while (c > 0 && run_start(T, G, c) > p) --c;
+  return c;
+}
 
 __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort) {
   raise_status(status, ST_TIMEOUT);
   *abort = 1;
 }
 
+// Final epilogue of 16 accumulator columns [c0, c0+16) of tile t for the
+// weight row r of this thread (128 epilogue threads, uniform control flow).
+__device__ __forceinline__ void final_chunk(const TcParams& p, int t, int c0, int r, int et, float (&v)[16],
+                                            float* xch) {
+  const int M = p.M;
+  if (p.mode == TC_HEAD) {
+    const HeadDesc& h = p.h;
+    const int vrow = t * 128 + r;
+    if (h.logits && vrow < h.V) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < M && head_row_used(h, c0 + j)) head_store_logit(h, c0 + j, vrow, v[j]);
+    }
+    tc::named_bar(1, 128);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
+    tc::named_bar(1, 128);
+    const int jc = et >> 3, g8 = et & 7;  // column jc, rows 16*g8 .. 16*g8+15
+    const int m = c0 + jc;
+    Top2 tp = top2_empty();
+    if (m < M && head_row_used(h, m)) {
+      for (int rr = 16 * g8; rr < 16 * g8 + 16; ++rr) {
+        const int vi = t * 128 + rr;
+        if (vi < h.V) top2_push(tp, xch[jc * 128 + rr], vi, p.status);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      Top2 u;
+      u.v1 = __shfl_xor_sync(0xffffffffu, tp.v1, o);
+      u.i1 = __shfl_xor_sync(0xffffffffu, tp.i1, o);
+      u.v2 = __shfl_xor_sync(0xffffffffu, tp.v2, o);
+      tp = top2_merge(tp, u);
+    }
+    if (g8 == 0 && m < M) p.tops[(size_t)t * M + m] = tp;
+    return;
+  }
+  const GemmDesc& g = p.g;
+  const int seg = t / p.tiles_per_seg, tile = t % p.tiles_per_seg;
+  if (g.kind == EPI_STORE || g.kind == EPI_RESID) {
+    const int n = tile * 128 + r;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < M) epi_single<__nv_bfloat16>(g, n, c0 + j, v[j]);
+    return;
+  }
+  // pair epilogues: partner row r + half lives in another warp
+  const int half = (g.kind == EPI_SWIGLU) ? 64 : g.d / 2;
+  const int blk = (g.kind == EPI_SWIGLU) ? 128 : g.d;
+  tc::named_bar(1, 128);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
+  tc::named_bar(1, 128);
+  if ((r % blk) < half) {
+    int u;
+    if (g.kind == EPI_SWIGLU) {
+      u = tile * 64 + r;
+    } else {
+      const int rr = tile * 128 + r;
+      u = (rr / g.d) * half + rr % g.d;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < M) epi_pair<__nv_bfloat16>(g, seg, u, c0 + j, v[j], xch[j * 128 + r + half]);
+  }
+}
+
 template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<BN>;
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_last_head;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xch = reinterpret_cast<float*>(smem + ST * Cfg::STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * Cfg::STAGE + Cfg::XCH);
   uint64_t* empty = full + ST;
-  uint64_t* done = empty + ST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* accf = empty + ST;  // [2] accumulator full  (MMA -> epilogue)
+  uint64_t* acce = accf + 2;    // [2] accumulator empty (epilogue -> MMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
-  const GemmDesc& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_g = blockIdx.x / p.splits;
-  const int split = blockIdx.x % p.splits;
-  const int seg = tile_g / p.tiles_per_seg;
-  const int tile = tile_g % p.tiles_per_seg;
-  const int kb0 = split * p.nkb / p.splits;
-  const int nk = (split + 1) * p.nkb / p.splits - kb0;
+  const int nkb = p.nkb;
+  const long long p0 = run_start(p.T, p.G, blockIdx.x), p1 = run_start(p.T, p.G, blockIdx.x + 1);
+  const int n_my = (int)(p1 - p0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 1);
+    }
     *abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch_desc(&p.wmap[seg]);
+    for (int s = 0; s < (p.mode == TC_GEMM ? p.g.nseg : 1); ++s) tc::tma_prefetch_desc(&p.wmap[s]);
     tc::tma_prefetch_desc(&p.xmap);
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -92,30 +186,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       const uint64_t pol_w = tc::policy_evict_first();
       const uint64_t pol_x = tc::policy_evict_last();
-      int issued = 0;
-      for (int i = 0; i < nk; ++i) {
+      auto load_w = [&](int i) {
+        const long long pos = p0 + i;
+        const int t = (int)(pos / nkb), kx = (int)(pos - (long long)t * nkb) * 64;
+        uint8_t* a = smem + (i % ST) * Cfg::STAGE;
+        if (p.mode == TC_HEAD) {
+          tc::tma_load_2d(a, &p.wmap[0], kx, t * 128, &full[i % ST], pol_w);
+        } else {
+          const GemmDesc& g = p.g;
+          const int seg = t / p.tiles_per_seg, tile = t % p.tiles_per_seg;
+          if (g.kind == EPI_SWIGLU) {
+            tc::tma_load_2d(a, &p.wmap[seg], kx, tile * 64, &full[i % ST], pol_w);
+            tc::tma_load_2d(a + kTcA / 2, &p.wmap[seg], kx, g.inter + tile * 64, &full[i % ST], pol_w);
+          } else {
+            tc::tma_load_2d(a, &p.wmap[seg], kx, g.seg_row0 + tile * 128, &full[i % ST], pol_w);
+          }
+        }
+      };
+      auto load_x = [&](int i) {
+        const long long pos = p0 + i;
+        const int t = (int)(pos / nkb), kx = (int)(pos - (long long)t * nkb) * 64;
+        tc::tma_load_2d(smem + (i % ST) * Cfg::STAGE + kTcA, &p.xmap, kx, 0, &full[i % ST], pol_x);
+      };
+      // weights depend on nothing upstream: fill the ring before the wait
+      const int pre = n_my < ST ? n_my : ST;
+      for (int i = 0; i < pre; ++i) {
+        tc::mbar_arrive_expect_tx(&full[i], Cfg::STAGE);
+        load_w(i);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      int issued = pre;
+      for (int i = pre; i < n_my; ++i) {
         const int s = i % ST;
-        const uint32_t ph = (uint32_t)(i / ST) & 1u;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) {
+        if (!tc::mbar_wait(&empty[s], ((uint32_t)(i / ST) & 1u) ^ 1u, abort)) {
           tc_timeout(p.status, abort);
           break;
         }
-        uint8_t* a = smem + s * Cfg::STAGE;
         tc::mbar_arrive_expect_tx(&full[s], Cfg::STAGE);
-        const int kx = (kb0 + i) * 64;
-        if (g.kind == EPI_SWIGLU) {
-          tc::tma_load_2d(a, &p.wmap[seg], kx, tile * 64, &full[s], pol_w);
-          tc::tma_load_2d(a + kTcA / 2, &p.wmap[seg], kx, g.inter + tile * 64, &full[s], pol_w);
-        } else {
-          tc::tma_load_2d(a, &p.wmap[seg], kx, g.seg_row0 + tile * 128, &full[s], pol_w);
-        }
-        tc::tma_load_2d(a + kTcA, &p.xmap, kx, 0, &full[s], pol_x);
+        load_w(i);
+        load_x(i);
         ++issued;
       }
       // every issued copy has landed before this CTA's shared memory goes away
@@ -124,103 +241,115 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer, one accumulator per piece, alternating
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % ST;
-        const uint32_t ph = (uint32_t)(i / ST) & 1u;
-        if (!tc::mbar_wait(&full[s], ph, abort)) {
+      long long pos = p0;
+      int i = 0, k = 0;
+      bool stop = false;
+      while (pos < p1 && !stop) {
+        const int t = (int)(pos / nkb);
+        const long long end = p1 < (long long)(t + 1) * nkb ? p1 : (long long)(t + 1) * nkb;
+        const int b = k & 1;
+        if (!tc::mbar_wait(&acce[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort)) {
           tc_timeout(p.status, abort);
           break;
         }
         tc::tc_fence_after();
-        const uint32_t a = tc::smem_u32(smem + s * Cfg::STAGE);
-        const uint32_t b = a + kTcA;
+        const uint32_t d = tmem + (uint32_t)(b * Cfg::ACC);
+        for (long long q = pos; q < end; ++q, ++i) {
+          const int s = i % ST;
+          if (!tc::mbar_wait(&full[s], (uint32_t)(i / ST) & 1u, abort)) {
+            tc_timeout(p.status, abort);
+            stop = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t a = tc::smem_u32(smem + s * Cfg::STAGE);
+          const uint32_t bb = a + kTcA;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc::mma_bf16(tmem, tc::sdesc_sw128(a + 32 * j), tc::sdesc_sw128(b + 32 * j), idesc,
-                       (i > 0 || j > 0) ? 1u : 0u);
-        tc::mma_commit(&empty[s]);
+          for (int j = 0; j < 4; ++j)
+            tc::mma_bf16(d, tc::sdesc_sw128(a + 32 * j), tc::sdesc_sw128(bb + 32 * j), idesc,
+                         (q > pos || j > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(&accf[b]);  // arrives when this piece's MMAs completed
+        pos = end;
+        ++k;
       }
-      tc::mma_commit(done);  // arrives once every issued MMA has completed
     }
   } else {
-    // ---------------- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
-    const int q = warp & 3;
-    const int r = q * 32 + lane;  // accumulator row = weight row within the tile
+    // ---------------- epilogue: warps 2..5 (TMEM lanes 32*(warp%4) ..)
+    pdl_wait();
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // accumulator row = weight row within the tile
     const int et = threadIdx.x - 64;
-    if (!tc::mbar_wait(done, 0, nullptr)) tc_timeout(p.status, abort);
-    tc::named_bar(1, 128);
-    const bool ok = (*abort == 0);  // same value in every epilogue thread
-    tc::tc_fence_after();
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-    const int M = g.M;
+    const int M = p.M;
     const int ncol = min(BN, ((M + 15) / 16) * 16);
-    float* part_tile = p.part + (size_t)tile_g * p.splits * BN * 128;
-    bool active = ok;
-    if (active && p.splits > 1) {
-      for (int c0 = 0; c0 < ncol; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(trow + c0, v);
-        float* dst = part_tile + ((size_t)split * BN + c0) * 128 + r;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) dst[(size_t)j * 128] = v[j];
-      }
-      __threadfence();
+    long long pos = p0;
+    int k = 0;
+    while (pos < p1) {
+      const int t = (int)(pos / nkb);
+      const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
+      const long long end = p1 < tend ? p1 : tend;
+      const bool whole = (pos == tbeg && end == tend);
+      const int b = k & 1;
+      if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort)) tc_timeout(p.status, abort);
       tc::named_bar(1, 128);
-      if (et == 0) {
-        uint32_t* ctr = p.counters + kCtrGemm + tile_g;
-        const uint32_t old = atomicAdd(ctr, 1u);
-        *s_last = (old == (uint32_t)p.splits - 1);
-        if (*s_last) *ctr = 0u;
-      }
-      tc::named_bar(1, 128);
-      active = *s_last != 0;
-      if (active) __threadfence();
-    }
-    if (active) {
-      const bool pair = (g.kind == EPI_QKV || g.kind == EPI_SWIGLU);
-      const int half = (g.kind == EPI_SWIGLU) ? 64 : g.d / 2;
-      const int blk = (g.kind == EPI_SWIGLU) ? 128 : g.d;
-      for (int c0 = 0; c0 < ncol; c0 += 16) {
-        float v[16];
-        if (p.splits > 1) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          for (int s = 0; s < p.splits; ++s) {
-            const float* src = part_tile + ((size_t)s * BN + c0) * 128 + r;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * 128);
-          }
-        } else {
+      if (*abort) break;  // uniform: read after the barrier
+      tc::tc_fence_after();
+      const uint32_t trow = tmem + (uint32_t)(b * Cfg::ACC) + ((uint32_t)(q4 * 32) << 16);
+      if (whole) {
+        for (int c0 = 0; c0 < ncol; c0 += 16) {
+          float v[16];
           tc::tmem_ld16(trow + c0, v);
+          final_chunk(p, t, c0, r, et, v, xch);
         }
-        if (!pair) {
-          const int n = tile * 128 + r;
+        tc::tc_fence_before();
+        tc::named_bar(1, 128);
+        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&acce[b])) : "memory");
+      } else {
+        const long long slot = blockIdx.x + (long long)t;  // global piece index
+        float* dst0 = p.part + (size_t)slot * BN * 128 + r;
+        for (int c0 = 0; c0 < ncol; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(trow + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < M) epi_single<__nv_bfloat16>(g, n, c0 + j, v[j]);
-        } else {
-          tc::named_bar(1, 128);
+          for (int j = 0; j < 16; ++j) dst0[(size_t)(c0 + j) * 128] = v[j];
+        }
+        tc::tc_fence_before();
+        tc::named_bar(1, 128);
+        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&acce[b])) : "memory");
+        __threadfence();
+        tc::named_bar(1, 128);
+        if (et == 0) {
+          uint32_t* ctr = p.counters + kCtrGemm + t;
+          const uint32_t add = (uint32_t)(end - pos);
+          const uint32_t old = atomicAdd(ctr, add);
+          *s_flag = (old + add == (uint32_t)nkb);
+          if (*s_flag) *ctr = 0u;
+        }
+        tc::named_bar(1, 128);
+        if (*s_flag) {
+          __threadfence();
+          const int first = run_of(tbeg, p.T, p.G) + t;
+          const int last = run_of(tend - 1, p.T, p.G) + t;
+          for (int c0 = 0; c0 < ncol; c0 += 16) {
+            float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
-          tc::named_bar(1, 128);
-          if ((r % blk) < half) {
-            int u;
-            if (g.kind == EPI_SWIGLU) {
-              u = tile * 64 + r;
-            } else {
-              const int rr = tile * 128 + r;
-              u = (rr / g.d) * half + rr % g.d;
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int sl = first; sl <= last; ++sl) {
+              const float* src = p.part + (size_t)sl * BN * 128 + (size_t)c0 * 128 + r;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * 128);
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < M) epi_pair<__nv_bfloat16>(g, seg, u, c0 + j, v[j], xch[j * 128 + r + half]);
+            final_chunk(p, t, c0, r, et, v, xch);
           }
         }
+        tc::named_bar(1, 128);  // s_flag is rewritten by the next piece
       }
+      pos = end;
+      ++k;
     }
-    (void)et;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -228,6 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
+  if (p.mode == TC_HEAD) head_finish(p.h, gridDim.x, p.n_tiles, p.tops, &s_last_head);
 }
 
 // ------------------------------------------------------------------- host
@@ -237,12 +367,12 @@ namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   }
   return fn;
 }
@@ -255,10 +385,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int pick_bn(int M) {
@@ -269,34 +398,28 @@ int pick_bn(int M) {
   return 256;
 }
 
-int tiles_per_seg(const GemmDesc& g) { return g.kind == EPI_SWIGLU ? g.inter / 64 : g.seg_rows / 128; }
+int gemm_tiles_per_seg(const GemmDesc& g) { return g.kind == EPI_SWIGLU ? g.inter / 64 : g.seg_rows / 128; }
 
-// Split count from the tile count, K and the SM count only (never M): the
-// most even fill of two resident CTAs per SM, at least two k-blocks each.
-int pick_splits(int n_tiles, int nkb, int sms) {
-  const long slots = 2L * sms;
-  int best = 1;
-  double best_eff = 0.0;
-  const int max_s = nkb / 2 < 32 ? nkb / 2 : 32;
-  for (int s = 1; s <= (max_s > 0 ? max_s : 1); ++s) {
-    const long units = (long)n_tiles * s;
-    const long waves = (units + slots - 1) / slots;
-    const double eff = (double)units / (double)(waves * slots);
-    if (eff > best_eff + 0.01) {
-      best_eff = eff;
-      best = s;
-    }
-  }
-  return best;
-}
+int runs_for(long long T, int num_sms) { return (int)(T < num_sms ? T : num_sms); }
+
+size_t part_bytes(int n_tiles, int G, int bn) { return (size_t)(n_tiles + G) * bn * 128 * sizeof(float); }
 
 template <int BN>
-cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t st) {
-  auto k = gemm_tc_kernel<BN>;
+cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
+  auto k = tc_stream_kernel<BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
-  k<<<grid, kTcThreads, TcCfg<BN>::SMEM, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(p.G), dim3(kTcThreads), TcCfg<BN>::SMEM, st, p);
+}
+
+cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
+  switch (pick_bn(p.M)) {
+    case 16: return launch_bn<16>(p, st);
+    case 32: return launch_bn<32>(p, st);
+    case 64: return launch_bn<64>(p, st);
+    case 128: return launch_bn<128>(p, st);
+    default: return launch_bn<256>(p, st);
+  }
 }
 
 }  // namespace
@@ -318,10 +441,9 @@ bool gemm_tc_supported(const GemmDesc& g) {
 }
 
 size_t gemm_tc_workspace(const GemmDesc& g, int num_sms) {
-  const int n_tiles = g.nseg * tiles_per_seg(g);
-  const int splits = pick_splits(n_tiles, g.K / 64, num_sms);
-  if (splits <= 1) return 0;
-  return (size_t)n_tiles * splits * pick_bn(g.M) * 128 * sizeof(float);
+  const int n_tiles = g.nseg * gemm_tiles_per_seg(g);
+  const long long T = (long long)n_tiles * (g.K / 64);
+  return part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(g.M));
 }
 
 cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters, uint32_t* status,
@@ -329,14 +451,16 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_
   if (g.M == 0) return cudaSuccess;
   TcParams p;
   memset(&p, 0, sizeof(p));
+  p.mode = TC_GEMM;
   p.g = g;
-  p.tiles_per_seg = tiles_per_seg(g);
+  p.M = g.M;
+  p.tiles_per_seg = gemm_tiles_per_seg(g);
+  p.n_tiles = g.nseg * p.tiles_per_seg;
   p.nkb = g.K / 64;
-  const int n_tiles = g.nseg * p.tiles_per_seg;
-  if (n_tiles > 8192) return cudaErrorInvalidValue;
-  p.splits = pick_splits(n_tiles, p.nkb, num_sms);
-  const int bn = pick_bn(g.M);
-  if (p.splits > 1 && ws_bytes < (size_t)n_tiles * p.splits * bn * 128 * sizeof(float)) return cudaErrorInvalidValue;
+  p.T = (long long)p.n_tiles * p.nkb;
+  p.G = runs_for(p.T, num_sms);
+  if (p.n_tiles > 8192) return cudaErrorInvalidValue;
+  if (ws_bytes < part_bytes(p.n_tiles, p.G, pick_bn(g.M))) return cudaErrorInvalidValue;
   p.part = static_cast<float*>(ws);
   p.counters = counters;
   p.status = status;
@@ -344,15 +468,42 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_
   const uint32_t box_rows = g.kind == EPI_SWIGLU ? 64 : 128;
   for (int s = 0; s < g.nseg; ++s)
     if (!make_map(&p.wmap[s], g.seg_w[s], g.K, wrows, box_rows)) return cudaErrorInvalidValue;
-  if (!make_map(&p.xmap, g.X, g.K, g.M, bn)) return cudaErrorInvalidValue;
-  const int grid = n_tiles * p.splits;
-  switch (bn) {
-    case 16: return launch_bn<16>(p, grid, st);
-    case 32: return launch_bn<32>(p, grid, st);
-    case 64: return launch_bn<64>(p, grid, st);
-    case 128: return launch_bn<128>(p, grid, st);
-    default: return launch_bn<256>(p, grid, st);
-  }
+  if (!make_map(&p.xmap, g.X, g.K, g.M, pick_bn(g.M))) return cudaErrorInvalidValue;
+  return launch_params(p, st);
+}
+
+// ------------------------------------------------------------- LM head
+
+bool head_tc_supported(const HeadDesc& h) {
+  return h.dtype == DFLASH_BF16 && h.M >= 1 && h.M <= 256 && h.H % 64 == 0 && h.mode != 2 &&
+         (reinterpret_cast<uintptr_t>(h.x) & 15) == 0 && (h.V + 127) / 128 <= 8192;
+}
+
+size_t head_tc_workspace(const HeadDesc& h, int num_sms) {
+  const int n_tiles = (h.V + 127) / 128;
+  const long long T = (long long)n_tiles * (h.H / 64);
+  return part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(h.M)) + (size_t)n_tiles * h.M * sizeof(Top2) + 256;
+}
+
+cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = TC_HEAD;
+  p.h = h;
+  p.M = h.M;
+  p.tiles_per_seg = (h.V + 127) / 128;
+  p.n_tiles = p.tiles_per_seg;
+  p.nkb = h.H / 64;
+  p.T = (long long)p.n_tiles * p.nkb;
+  p.G = runs_for(p.T, num_sms);
+  const size_t pb = part_bytes(p.n_tiles, p.G, pick_bn(h.M));
+  p.part = h.partials;
+  p.tops = reinterpret_cast<Top2*>(reinterpret_cast<char*>(h.partials) + ((pb + 255) & ~size_t(255)));
+  p.counters = h.counters;
+  p.status = h.status;
+  if (!make_map(&p.wmap[0], h.w, h.H, h.V, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&p.xmap, h.x, h.H, h.M, pick_bn(h.M))) return cudaErrorInvalidValue;
+  return launch_params(p, st);
 }
 
 }  // namespace dfl

@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "head_common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace dfl {
 
@@ -18,6 +19,8 @@ constexpr int kHeadTok = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kHeadWarps * 32) head_simt_kernel(const __grid_constant__ HeadDesc h) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ Top2 tsm[];  // [warps][M]
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -70,12 +73,12 @@ __global__ void __launch_bounds__(kHeadWarps * 32) head_simt_kernel(const __grid
     for (int w = 1; w < kHeadWarps; ++w) t = top2_merge(t, tsm[(size_t)w * M + m]);
     part[(size_t)blockIdx.x * M + m] = t;
   }
-  head_finish(h, gridDim.x, part, &s_last);
+  head_finish(h, gridDim.x, gridDim.x, part, &s_last);
 }
 
 size_t head_workspace(const HeadDesc& h, int num_sms) {
   size_t simt = (size_t)(2 * num_sms) * h.M * sizeof(Top2) + 256;
-  size_t tc = head_tc_workspace(h);
+  size_t tc = head_tc_workspace(h, num_sms);
   return simt > tc ? simt : tc;
 }
 
@@ -85,17 +88,17 @@ cudaError_t launch_head_simt(const HeadDesc& h, int num_sms, cudaStream_t st) {
   if (h.dtype == DFLASH_BF16) {
     auto k = head_simt_kernel<__nv_bfloat16>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kHeadWarps * 32, smem, st>>>(h);
+    return launch_pdl(k, dim3(grid), dim3(kHeadWarps * 32), smem, st, h);
   } else {
     auto k = head_simt_kernel<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kHeadWarps * 32, smem, st>>>(h);
+    return launch_pdl(k, dim3(grid), dim3(kHeadWarps * 32), smem, st, h);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st) {
-  if (head_tc_supported(h)) return launch_head_tc(h, st);
+  if (head_tc_supported(h)) return launch_head_tc(h, num_sms, st);
   return launch_head_simt(h, num_sms, st);
 }
 
@@ -105,6 +108,8 @@ cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st) {
 // score = ue . (V e_b); walk greedily.  Scores are fp32 with fixed-order sums.
 template <typename T>
 __global__ void path_select_kernel(const __grid_constant__ PathDesc p) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ float psm[];
   float* ue = psm;                            // [rank]
   int* park = reinterpret_cast<int*>(psm + p.rank);  // chosen token of the step
@@ -163,9 +168,9 @@ cudaError_t launch_path_select(const PathDesc& p, cudaStream_t st) {
   if (p.n_seqs == 0 || p.block < 2) return cudaSuccess;
   size_t smem = (size_t)(p.rank + 1 + p.topk) * sizeof(float);
   if (p.dtype == DFLASH_BF16)
-    path_select_kernel<__nv_bfloat16><<<p.n_seqs, 256, smem, st>>>(p);
+    return launch_pdl(path_select_kernel<__nv_bfloat16>, dim3(p.n_seqs), dim3(256), smem, st, p);
   else
-    path_select_kernel<float><<<p.n_seqs, 256, smem, st>>>(p);
+    return launch_pdl(path_select_kernel<float>, dim3(p.n_seqs), dim3(256), smem, st, p);
   return cudaGetLastError();
 }
 
