@@ -23,6 +23,8 @@
 // co-scheduled CTAs, so nothing spins and nothing round-trips through HBM.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
@@ -263,21 +265,27 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 namespace cg = cooperative_groups;
 
-template <int D, int NC>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __grid_constant__ AttnDesc a,
-                                                                        int n_qt) {
+constexpr int kClusterWarps = 8;   // warps 0-3 take the low 64 keys of a chunk, warps 4-7 the high 64
+constexpr int kMaxNC = 16;
+
+template <int D>
+__global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const __grid_constant__ AttnDesc a,
+                                                                           int n_qt) {
   pdl_wait();
   pdl_launch_dependents();
   constexpr int CH = kMmaCH;
+  constexpr int HK = CH / 2;         // keys per warp group and chunk
   constexpr int CPR = D / 8;         // 16-byte chunks per row
   constexpr int TILE = CH * D * 2;   // one K or V chunk tile, bytes
-  constexpr int PST = D + 4;         // floats per row of the partial (16-byte aligned rows)
+  constexpr int PST = D + 4;         // floats per row of a partial (16-byte aligned rows)
   extern __shared__ __align__(128) uint8_t smem_att[];
-  uint8_t* Qs = smem_att;            // [64][D]
+  uint8_t* Qs = smem_att;              // [64][D]
   uint8_t* KV = Qs + kAttnQT * D * 2;  // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
-  float* psm = reinterpret_cast<float*>(KV);  // [64][PST] partial, written after the chunk loop
+  float* psm = reinterpret_cast<float*>(KV);  // [64][PST] CTA partial (after the chunk loop)
+  float* hsm = psm + kAttnQT * PST;           // [64][PST] high-key-half partial
 
   cg::cluster_group cl = cg::this_cluster();
+  const int NC = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
   const int s = blockIdx.z;
@@ -296,6 +304,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
     sk.n_ch = sk.n_ctx_ch + 1;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wq = warp & 3, kh = warp >> 2;
   const int qv0 = qt * kAttnQT;
   const int nq_tile = min(kAttnQT, nqv - qv0);
   const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
   if (nmine > 1) stage_chunk(rank + NC, 1);
   asm volatile("cp.async.commit_group;" ::: "memory");
 
-  const int r0 = 16 * warp;  // this warp's 16 query vectors
+  const int r0 = 16 * wq;  // this warp's 16 query vectors
   const bool warp_on = r0 < nq_tile;
   const int qa = r0 + (lane >> 2), qb2 = qa + 8;  // the two rows this thread holds
   const int row_a = (qv0 + qa) / grp, row_b = (qv0 + qb2) / grp;
@@ -364,34 +373,34 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
       const __nv_bfloat16* vp;
       chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
     }
-    if (warp_on) {
-      // S = Q K^T over the chunk's CH keys
-      float S[CH / 8][4];
+    if (warp_on && HK * kh < nk) {
+      // S = Q K^T over this warp's half of the chunk (keys HK*kh .. HK*kh + HK)
+      float S[HK / 8][4];
 #pragma unroll
-      for (int t = 0; t < CH / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
+      for (int t = 0; t < HK / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(qb + swz<D>(r0 + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < CH / 16; ++nt) {
+        for (int nt = 0; nt < HK / 16; ++nt) {
           uint32_t b0, b1, b2, b3;
-          const int key = 16 * nt + (lane & 7) + ((lane >> 4) << 3);
+          const int key = HK * kh + 16 * nt + (lane & 7) + ((lane >> 4) << 3);
           ldsm_x4(kb + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
           mma_16816(S[2 * nt], a0, a1, a2, a3, b0, b1);
           mma_16816(S[2 * nt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-      // mask, scale to log2 units, chunk maxima
+      // mask, scale to log2 units, maxima over this half
       const bool causal = a.mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
       const int lim_a = causal ? P + row_a - slot0 : CH;
       const int lim_b = causal ? P + row_b - slot0 : CH;
       float cm_a = -INFINITY, cm_b = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < CH / 8; ++t) {
+      for (int t = 0; t < HK / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int j = 8 * t + 2 * (lane & 3) + e;
+          const int j = HK * kh + 8 * t + 2 * (lane & 3) + e;  // key index within the chunk
           S[t][e] = (j < nk && j <= lim_a) ? S[t][e] * scale : -INFINITY;
           S[t][2 + e] = (j < nk && j <= lim_b) ? S[t][2 + e] * scale : -INFINITY;
           cm_a = fmaxf(cm_a, S[t][e]);
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
       const float al_b = (m_b == -INFINITY) ? 0.f : exp2f(m_b - mn_b);
       float sl_a = 0.f, sl_b = 0.f;
 #pragma unroll
-      for (int t = 0; t < CH / 8; ++t) {
+      for (int t = 0; t < HK / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float pa = (S[t][e] == -INFINITY) ? 0.f : exp2f(S[t][e] - mn_a);
@@ -434,9 +443,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
         O[t][2] *= al_b;
         O[t][3] *= al_b;
       }
-      // O += P V
+      // O += P V over the half
 #pragma unroll
-      for (int kk = 0; kk < CH / 16; ++kk) {
+      for (int kk = 0; kk < HK / 16; ++kk) {
         const uint32_t a0 = pack_bf16(S[2 * kk][0], S[2 * kk][1]);
         const uint32_t a1 = pack_bf16(S[2 * kk][2], S[2 * kk][3]);
         const uint32_t a2 = pack_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1]);
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
           uint32_t b0, b1, b2, b3;
-          const int key = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int key = HK * kh + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
           ldsm_x4_t(vb + swz<D>(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
           mma_16816(O[2 * dt], a0, a1, a2, a3, b0, b1);
           mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
@@ -458,10 +467,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
-  // ---- this CTA's partial (m, l, O) per query vector into its shared memory
-  if (warp_on) {
-    float* pa = psm + (size_t)qa * PST;
-    float* pb = psm + (size_t)qb2 * PST;
+  // ---- merge the two key halves (low half first), then this CTA's partial
+  if (warp_on && kh == 1) {
+    float* pa = hsm + (size_t)qa * PST;
+    float* pb = hsm + (size_t)qb2 * PST;
 #pragma unroll
     for (int t = 0; t < D / 8; ++t) {
       const int col = 8 * t + 2 * (lane & 3);
@@ -470,11 +479,32 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
       pb[col] = O[t][2];
       pb[col + 1] = O[t][3];
     }
+    pa[D + (lane & 3)] = (lane & 3) == 0 ? m_a : l_a;  // lanes 0/1 of the quad hold m / l
+    pb[D + (lane & 3)] = (lane & 3) == 0 ? m_b : l_b;
+  }
+  __syncthreads();
+  if (warp_on && kh == 0) {
+    float* pa = psm + (size_t)qa * PST;
+    float* pb = psm + (size_t)qb2 * PST;
+    const float* ha = hsm + (size_t)qa * PST;
+    const float* hb = hsm + (size_t)qb2 * PST;
+    const float m1a = ha[D], l1a = ha[D + 1], m1b = hb[D], l1b = hb[D + 1];
+    const float Ma = fmaxf(m_a, m1a), Mb = fmaxf(m_b, m1b);
+    const float w0a = (m_a == -INFINITY) ? 0.f : exp2f(m_a - Ma), w1a = (m1a == -INFINITY) ? 0.f : exp2f(m1a - Ma);
+    const float w0b = (m_b == -INFINITY) ? 0.f : exp2f(m_b - Mb), w1b = (m1b == -INFINITY) ? 0.f : exp2f(m1b - Mb);
+#pragma unroll
+    for (int t = 0; t < D / 8; ++t) {
+      const int col = 8 * t + 2 * (lane & 3);
+      pa[col] = fmaf(O[t][0], w0a, ha[col] * w1a);
+      pa[col + 1] = fmaf(O[t][1], w0a, ha[col + 1] * w1a);
+      pb[col] = fmaf(O[t][2], w0b, hb[col] * w1b);
+      pb[col + 1] = fmaf(O[t][3], w0b, hb[col + 1] * w1b);
+    }
     if ((lane & 3) == 0) {
-      pa[D] = m_a;
-      pa[D + 1] = l_a;
-      pb[D] = m_b;
-      pb[D + 1] = l_b;
+      pa[D] = Ma;
+      pa[D + 1] = fmaf(l_a, w0a, l1a * w1a);
+      pb[D] = Mb;
+      pb[D + 1] = fmaf(l_b, w0b, l1b * w1b);
     }
   }
   cl.sync();
@@ -486,10 +516,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
   for (int t = threadIdx.x; t < (q_hi > q_lo ? (q_hi - q_lo) * D : 0); t += blockDim.x) {
     const int qi = q_lo + t / D, e = t % D;
     float M = -INFINITY;
-#pragma unroll
     for (int r = 0; r < NC; ++r) M = fmaxf(M, cl.map_shared_rank(psm, r)[(size_t)qi * PST + D]);
     float L = 0.f, Ov = 0.f;
-#pragma unroll
     for (int r = 0; r < NC; ++r) {
       const float* pr = cl.map_shared_rank(psm, r) + (size_t)qi * PST;
       const float mr = pr[D];
@@ -508,67 +536,74 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const __g
 
 namespace {
 
-// Cluster width: 16 CTAs when few (sequence, head, tile) groups must fill
-// the GPU, else 8.  Depends on the batch shape, never on the row count alone,
-// so decode (1 row) and verification (a block) of one batch use the same.
-int attn_nc(const AttnDesc& a, int n_qt) { return (long)a.n_seqs * a.nkv * n_qt <= 16 ? 16 : 8; }
+size_t cluster_smem(int d) { return (size_t)kAttnQT * d * 2 + 4 * (size_t)kMmaCH * d * 2; }
 
-// Can this device co-schedule a 16-CTA cluster of this kernel?
 template <int D>
-bool wide_clusters_fit(size_t smem);
-
-template <int D, int NC>
-cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
-  auto k = attn_cluster_kernel<D, NC>;
-  const size_t smem = (size_t)kAttnQT * D * 2 + 4 * (size_t)kMmaCH * D * 2;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (NC > 8) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
+cudaLaunchConfig_t cluster_cfg(int nc, dim3 grid, cudaStream_t st, cudaLaunchAttribute* at) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(NC, a.nkv * n_qt, a.n_seqs);
-  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kClusterWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = cluster_smem(D);
   cfg.stream = st;
-  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = NC;
+  at[0].val.clusterDim.x = nc;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k, a, n_qt);
+  return cfg;
+}
+
+// How many clusters of width nc this device runs at once (cached per device).
+template <int D>
+int clusters_resident(int nc) {
+  static std::mutex mu;
+  static int cache[64][kMaxNC + 1];
+  static bool init[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init[dev]) {
+    auto k = attn_cluster_kernel<D>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cluster_smem(D));
+    cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int w = 1; w <= kMaxNC; ++w) {
+      cudaLaunchAttribute at[2];
+      cudaLaunchConfig_t cfg = cluster_cfg<D>(w, dim3(w, 1, 1), nullptr, at);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+      cache[dev][w] = n;
+    }
+    cudaGetLastError();
+    init[dev] = true;
+  }
+  return cache[dev][nc];
+}
+
+// Cluster width: the widest (<= 16) whose clusters for this batch shape all
+// run at once, at least 8.  Depends on the batch shape and the device, never
+// on the row count alone, so decode (1 row) and verification (a block) of one
+// batch use the same width.
+template <int D>
+int pick_nc(long groups) {
+  for (int nc = kMaxNC; nc > 8; --nc)
+    if (clusters_resident<D>(nc) >= groups) return nc;
+  return 8;
 }
 
 template <int D>
-bool wide_clusters_fit(size_t smem) {
-  auto k = attn_cluster_kernel<D, 16>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(16, 1, 1);
-  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 16;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return n > 0;
+cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
+  auto k = attn_cluster_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cluster_smem(D));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv * n_qt);
+  cudaLaunchAttribute at[2];
+  cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
+  return cudaLaunchKernelEx(&cfg, k, a, n_qt);
 }
 
 }  // namespace
@@ -583,11 +618,7 @@ cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   AttnGeom g = attn_geom(a);
   if (a.n_seqs == 0 || a.rows == 0) return cudaSuccess;
   if (a.dtype == DFLASH_BF16) {
-    const size_t smem = (size_t)kAttnQT * a.d * 2 + 4 * (size_t)kMmaCH * a.d * 2;
-    const bool w16 = attn_nc(a, g.n_qt) == 16 &&
-                     (a.d == 128 ? wide_clusters_fit<128>(smem) : wide_clusters_fit<64>(smem));
-    if (a.d == 128) return w16 ? launch_cluster<128, 16>(a, g.n_qt, st) : launch_cluster<128, 8>(a, g.n_qt, st);
-    return w16 ? launch_cluster<64, 16>(a, g.n_qt, st) : launch_cluster<64, 8>(a, g.n_qt, st);
+    return a.d == 128 ? launch_cluster<128>(a, g.n_qt, st) : launch_cluster<64>(a, g.n_qt, st);
   }
   dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);
   const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);

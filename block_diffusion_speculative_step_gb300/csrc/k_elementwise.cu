@@ -32,18 +32,40 @@ cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaSt
   return cudaGetLastError();
 }
 
-// h[m][:] = E[token(m)][:] as fp32.
+// 4 consecutive elements as floats / from floats (16-byte fp32, 8-byte bf16).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+constexpr int kRowThreads = 256;
+constexpr int kRowVec = 8;  // 4-element groups per thread: rows up to 8192 elements stay in registers
+
+// h[m][:] = E[token(m)][:] as fp32 (4 elements per access).
 template <typename T>
-__global__ void embed_kernel(const T* __restrict__ E, int H, int rows, const int32_t* __restrict__ first,
-                             const int32_t* __restrict__ rest, int fill, float* __restrict__ h) {
+__global__ void __launch_bounds__(kRowThreads) embed_kernel(const T* __restrict__ E, int H, int rows,
+                                                            const int32_t* __restrict__ first,
+                                                            const int32_t* __restrict__ rest, int fill,
+                                                            float* __restrict__ h) {
   pdl_wait();
   pdl_launch_dependents();
-  int m = blockIdx.x;
-  int s = m / rows, i = m % rows;
-  int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
+  const int m = blockIdx.x;
+  const int s = m / rows, i = m % rows;
+  const int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
   const T* e = E + (size_t)tok * H;
   float* o = h + (size_t)m * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = to_f<T>(e[k]);
+  for (int k = 4 * threadIdx.x; k < H; k += 4 * kRowThreads) st4(o + k, ld4(e + k));
 }
 
 cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, const int32_t* first,
@@ -51,68 +73,91 @@ cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, 
   int M = n_seqs * rows;
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    return launch_pdl(embed_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, (const __nv_bfloat16*)E, H, rows, first, rest, fill, h);
-  else
-    return launch_pdl(embed_kernel<float>, dim3(M), dim3(256), 0, st, (const float*)E, H, rows, first, rest, fill, h);
-  return cudaGetLastError();
+    return launch_pdl(embed_kernel<__nv_bfloat16>, dim3(M), dim3(kRowThreads), 0, st, (const __nv_bfloat16*)E,
+                      H, rows, first, rest, fill, h);
+  return launch_pdl(embed_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, (const float*)E, H, rows, first, rest,
+                    fill, h);
 }
 
-// x[m] = round(h[m] * rsqrt(mean(h[m]^2) + eps) * g), one block per row.  The
-// sum of squares runs in a fixed order (per-thread strided partials, then a
-// fixed reduction tree), so a row's result does not depend on M.
+// x[m] = round(h[m] * rsqrt(mean(h[m]^2) + eps) * g), one block per row, the
+// row held in registers between the two passes.  The sum of squares runs in
+// a fixed order (per-thread groups in index order, then a fixed tree), so a
+// row's result does not depend on M.  Rows longer than 4*256*8 elements use
+// the strided loop.
 template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g, int H, float eps,
-                               T* __restrict__ x) {
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g,
+                                                              int H, float eps, T* __restrict__ x) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[32];
   const float* r = h + (size_t)blockIdx.x * H;
+  T* o = x + (size_t)blockIdx.x * H;
+  const bool fits = H <= 4 * kRowThreads * kRowVec;
+  float4 v[kRowVec];
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) ss += r[k] * r[k];
+  if (fits) {
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+      const int k = 4 * (threadIdx.x + i * kRowThreads);
+      v[i] = k < H ? ld4(r + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  } else {
+    for (int k = threadIdx.x; k < H; k += kRowThreads) ss += r[k] * r[k];
+  }
   ss = warp_sum(ss);
-  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) red[w] = ss;
   __syncthreads();
   if (w == 0) {
-    float v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
-    v = warp_sum(v);
-    if (l == 0) red[0] = v;
+    float t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+    t = warp_sum(t);
+    if (l == 0) red[0] = t;
   }
   __syncthreads();
-  float inv = rsqrtf(red[0] / (float)H + eps);
-  T* o = x + (size_t)blockIdx.x * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f<T>(r[k] * inv * to_f<T>(g[k]));
+  const float inv = rsqrtf(red[0] / (float)H + eps);
+  if (fits) {
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+      const int k = 4 * (threadIdx.x + i * kRowThreads);
+      if (k < H) {
+        const float4 gg = ld4(g + k);
+        st4(o + k, make_float4(v[i].x * inv * gg.x, v[i].y * inv * gg.y, v[i].z * inv * gg.z, v[i].w * inv * gg.w));
+      }
+    }
+  } else {
+    for (int k = threadIdx.x; k < H; k += kRowThreads) o[k] = from_f<T>(r[k] * inv * to_f<T>(g[k]));
+  }
 }
 
 cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int H, float eps, void* x,
                            cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, h, (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)x);
-  else
-    return launch_pdl(rmsnorm_kernel<float>, dim3(M), dim3(256), 0, st, h, (const float*)g, H, eps, (float*)x);
-  return cudaGetLastError();
+    return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(M), dim3(kRowThreads), 0, st, h,
+                      (const __nv_bfloat16*)g, H, eps, (__nv_bfloat16*)x);
+  return launch_pdl(rmsnorm_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, h, (const float*)g, H, eps, (float*)x);
 }
 
 // tap[m*stride + offset + k] = round(h[m][k]).
 template <typename T>
-__global__ void store_tap_kernel(const float* __restrict__ h, int H, T* __restrict__ tap, int stride,
-                                 int offset) {
+__global__ void __launch_bounds__(kRowThreads) store_tap_kernel(const float* __restrict__ h, int H,
+                                                                T* __restrict__ tap, int stride, int offset) {
   pdl_wait();
   pdl_launch_dependents();
   const float* r = h + (size_t)blockIdx.x * H;
   T* o = tap + (size_t)blockIdx.x * stride + offset;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f<T>(r[k]);
+  for (int k = 4 * threadIdx.x; k < H; k += 4 * kRowThreads) st4(o + k, ld4(r + k));
 }
 
 cudaError_t launch_store_tap(int dtype, const float* h, int M, int H, void* tap, int stride, int offset,
                              cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
-    return launch_pdl(store_tap_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, h, H, (__nv_bfloat16*)tap, stride, offset);
-  else
-    return launch_pdl(store_tap_kernel<float>, dim3(M), dim3(256), 0, st, h, H, (float*)tap, stride, offset);
-  return cudaGetLastError();
+    return launch_pdl(store_tap_kernel<__nv_bfloat16>, dim3(M), dim3(kRowThreads), 0, st, h, H,
+                      (__nv_bfloat16*)tap, stride, offset);
+  return launch_pdl(store_tap_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, h, H, (float*)tap, stride, offset);
 }
 
 template <typename T>
