@@ -5,7 +5,8 @@
 //
 // Swap-AB: a 128-row weight tile is the MMA's A operand (M = 128) and the
 // token rows are the B operand (N = BN in 16..256); at small batch the one
-// bf16 weight stream is the whole HBM traffic.  One CTA per SM.  The
+// bf16 weight stream is the whole HBM traffic.  One CTA per SM (its shared
+// memory ring is sized so no second CTA fits).  The
 // (tile, 64-wide k-block) space is cut into G equal contiguous runs, one per
 // CTA (balanced to one k-block); a run's piece inside one tile accumulates in
 // TMEM.  Roles per CTA: warp 0 streams W and X boxes with TMA (128-byte
@@ -54,13 +55,15 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
 template <int BN>
 struct TcCfg {
   static constexpr int STAGE = kTcA + BN * 128;
-  // <= 100 KB below BN = 128 so the next kernel's CTA can share the SM (PDL)
-  static constexpr int BUDGET = BN <= 64 ? 100 * 1024 : 200 * 1024;
+  // Deep enough that one CTA needs more than half of an SM's shared memory:
+  // the block scheduler then places exactly one CTA (one run) on every SM.
+  static constexpr int BUDGET = BN <= 64 ? 128 * 1024 : 200 * 1024;
   static constexpr int STAGES = (BUDGET / STAGE) > 10 ? 10 : (BUDGET / STAGE);
   static constexpr int ACC = BN < 32 ? 32 : BN;  // columns of one accumulator
   static constexpr int TMEM_COLS = 2 * ACC;       // double-buffered
   static constexpr int XCH = 16 * 128 * 4;        // epilogue exchange tile
   static constexpr int SMEM = STAGES * STAGE + XCH + 256 + 1024;
+  static_assert(SMEM > 117 * 1024, "a second CTA must not fit on the SM");
 };
 
 __host__ __device__ __forceinline__ long long run_start(long long T, int G, int c) { return (T * c) / G; }
