@@ -7,14 +7,6 @@
 
 namespace dfl {
 
-__device__ __forceinline__ RowMap rowmap_of(const GemmDesc& g) {
-  RowMap r;
-  r.base_pos = g.base_pos;
-  r.valid = g.valid;
-  r.rows = g.rows;
-  return r;
-}
-
 // Output units per segment: row pairs for QKV (RoPE partners i, i + d/2) and
 // SwiGLU (gate j, up j); single rows otherwise.
 __host__ __device__ __forceinline__ int epi_units(const GemmDesc& g) {
@@ -38,12 +30,56 @@ __host__ __device__ __forceinline__ void epi_unit_rows(const GemmDesc& g, int u,
   }
 }
 
+// The epilogue's operands as plain scalars and pointers, built once per tile
+// so the per-element code never re-reads the (large) launch descriptor.
+struct Epi {
+  int kind, seg_row0, d, half, QD, KD, nkv, kv_cap, kv_window, kv_slot_mode, rope_max_pos, inter, ldo, rows;
+  const int32_t* base_pos;
+  const int32_t* valid;
+  float* out_f32;
+  void* q_out;
+  void* k_dst;
+  void* v_dst;
+  const float* rope_cs;
+  void* act_out;
+};
+
+__device__ __forceinline__ Epi make_epi(const GemmDesc& g, int seg) {
+  Epi e;
+  e.kind = g.kind;
+  e.seg_row0 = g.seg_row0;
+  e.d = g.d;
+  e.half = g.d / 2;
+  e.QD = g.nq * g.d;
+  e.KD = g.nkv * g.d;
+  e.nkv = g.nkv;
+  e.kv_cap = g.kv_cap;
+  e.kv_window = g.kv_window;
+  e.kv_slot_mode = g.kv_slot_mode;
+  e.rope_max_pos = g.rope_max_pos;
+  e.inter = g.inter;
+  e.ldo = g.ldo;
+  e.rows = g.rows;
+  e.base_pos = g.base_pos;
+  e.valid = g.valid;
+  e.out_f32 = g.out_f32;
+  e.q_out = g.q_out;
+  e.k_dst = g.k_dst[seg];
+  e.v_dst = g.v_dst[seg];
+  e.rope_cs = g.rope_cs;
+  e.act_out = g.act_out;
+  return e;
+}
+
+__device__ __forceinline__ bool epi_live(const Epi& e, int m) {
+  return e.valid == nullptr || (m % e.rows) < e.valid[m / e.rows];
+}
+
 template <typename T>
-__device__ __forceinline__ void epi_single(const GemmDesc& g, int n, int m, float v) {
-  RowMap rm = rowmap_of(g);
-  if (!rm.live(m)) return;
-  float* o = g.out_f32 + (size_t)m * g.ldo + n;
-  if (g.kind == EPI_RESID)
+__device__ __forceinline__ void epi_single(const Epi& e, int n, int m, float v) {
+  if (!epi_live(e, m)) return;
+  float* o = e.out_f32 + (size_t)m * e.ldo + n;
+  if (e.kind == EPI_RESID)
     *o += v;
   else
     *o = v;
@@ -51,50 +87,44 @@ __device__ __forceinline__ void epi_single(const GemmDesc& g, int n, int m, floa
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
-// Pair epilogue for unit u of segment seg, token row m, accumulators (va, vb).
+// Pair epilogue for unit u, token row m, accumulators (va, vb): SwiGLU, or
+// RoPE of the pair (e, e + d/2) followed by the Q / K / V scatter.
 template <typename T>
-__device__ __forceinline__ void epi_pair(const GemmDesc& g, int seg, int u, int m, float va, float vb) {
-  RowMap rm = rowmap_of(g);
-  if (!rm.live(m)) return;
-  if (g.kind == EPI_SWIGLU) {
-    T* act = reinterpret_cast<T*>(g.act_out);
-    act[(size_t)m * g.inter + u] = from_f<T>(silu_f(va) * vb);
+__device__ __forceinline__ void epi_pair(const Epi& e, int u, int m, float va, float vb) {
+  if (!epi_live(e, m)) return;
+  if (e.kind == EPI_SWIGLU) {
+    reinterpret_cast<T*>(e.act_out)[(size_t)m * e.inter + u] = from_f<T>(silu_f(va) * vb);
     return;
   }
-  // EPI_QKV
-  const int d = g.d, half = d / 2;
-  const int QD = g.nq * d, KD = g.nkv * d;
-  int ra, rb;
-  epi_unit_rows(g, u, ra, rb);
-  const int e = ra % d;  // < half
-  const int pos = rm.pos(m);
-  if (pos < 0 || pos >= g.rope_max_pos) return;  // outside the RoPE table: nothing is written
-  if (ra < QD + KD) {  // Q or K: rotate the pair (e, e + d/2) by pos * w_e
-    const float* cs = g.rope_cs + ((size_t)pos * half + e) * 2;
-    float c = cs[0], s = cs[1];
-    float lo = va * c - vb * s;
-    float hi = vb * c + va * s;
+  const int d = e.d, half = e.half;
+  const int ra = e.seg_row0 + (u / half) * d + (u % half);
+  const int col = ra % d;  // < half
+  const int s_idx = m / e.rows, idx = m % e.rows;
+  const int pos = e.base_pos[s_idx] + idx;
+  if (pos < 0 || pos >= e.rope_max_pos) return;  // outside the RoPE table: nothing is written
+  if (ra < e.QD + e.KD) {  // Q or K: rotate the pair by pos * w_col
+    const float2 cs = *reinterpret_cast<const float2*>(e.rope_cs + ((size_t)pos * half + col) * 2);
+    const float lo = va * cs.x - vb * cs.y;
+    const float hi = vb * cs.x + va * cs.y;
     va = lo;
     vb = hi;
   }
-  if (ra < QD) {
-    T* q = reinterpret_cast<T*>(g.q_out) + (size_t)m * QD + ra;
+  if (ra < e.QD) {
+    T* q = reinterpret_cast<T*>(e.q_out) + (size_t)m * e.QD + ra;
     q[0] = from_f<T>(va);
     q[half] = from_f<T>(vb);
     return;
   }
-  const bool is_k = ra < QD + KD;
-  const int r = is_k ? ra - QD : ra - QD - KD;
+  const bool is_k = ra < e.QD + e.KD;
+  const int r = is_k ? ra - e.QD : ra - e.QD - e.KD;
   const int head = r / d;
-  const int s_idx = rm.seq(m);
   int slot;
-  if (g.kv_slot_mode == 1)
-    slot = g.kv_window > 0 ? pos % g.kv_window : pos;
+  if (e.kv_slot_mode == 1)
+    slot = e.kv_window > 0 ? pos % e.kv_window : pos;
   else
-    slot = rm.idx(m);
-  if (slot >= g.kv_cap) return;
-  T* dst = reinterpret_cast<T*>(is_k ? g.k_dst[seg] : g.v_dst[seg]) +
-           (((size_t)s_idx * g.nkv + head) * g.kv_cap + slot) * d + e;
+    slot = idx;
+  if (slot >= e.kv_cap) return;
+  T* dst = reinterpret_cast<T*>(is_k ? e.k_dst : e.v_dst) + (((size_t)s_idx * e.nkv + head) * e.kv_cap + slot) * d + col;
   dst[0] = from_f<T>(va);
   dst[half] = from_f<T>(vb);
 }

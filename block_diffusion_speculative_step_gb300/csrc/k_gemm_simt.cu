@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) gemm_simt_kernel(const __grid
     int ra, rb;
     epi_unit_rows(g, u, ra, rb);
     const T* W = reinterpret_cast<const T*>(g.seg_w[seg]);
+    const Epi ep = make_epi(g, seg);
     const T* wa = W + (size_t)ra * g.K;
     const T* wb = pair ? W + (size_t)rb * g.K : wa;
     for (int m0 = 0; m0 < g.M; m0 += kSimtTok) {
@@ -63,9 +64,9 @@ __global__ void __launch_bounds__(kSimtWarps * 32) gemm_simt_kernel(const __grid
       for (int t = 0; t < kSimtTok; ++t) {
         if (lane == t && m0 + t < g.M) {
           if (pair)
-            epi_pair<T>(g, seg, u, m0 + t, acc_a[t], acc_b[t]);
+            epi_pair<T>(ep, u, m0 + t, acc_a[t], acc_b[t]);
           else
-            epi_single<T>(g, ra - g.seg_row0, m0 + t, acc_a[t]);
+            epi_single<T>(ep, ra - g.seg_row0, m0 + t, acc_a[t]);
         }
       }
     }

@@ -80,18 +80,66 @@ __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort
   *abort = 1;
 }
 
+// Launch scalars held in registers: the inline-asm memory clobbers of the
+// pipeline would otherwise force every use to re-read the parameter block.
+struct TcLocal {
+  int mode, M, tps, nkb, G, n_tiles, kind, d, inter, row0;
+  long long T;
+  int V, hmode, hblock;
+  float* logits;
+  Top2* tops;
+  float* part;
+  uint32_t* counters;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ TcLocal tc_local(const TcParams& p) {
+  TcLocal L;
+  L.mode = p.mode;
+  L.M = p.M;
+  L.tps = p.tiles_per_seg;
+  L.nkb = p.nkb;
+  L.G = p.G;
+  L.n_tiles = p.n_tiles;
+  L.T = p.T;
+  L.kind = p.g.kind;
+  L.d = p.g.d;
+  L.inter = p.g.inter;
+  L.row0 = p.g.seg_row0;
+  L.V = p.h.V;
+  L.hmode = p.h.mode;
+  L.hblock = p.h.block;
+  L.logits = p.h.logits;
+  L.tops = p.tops;
+  L.part = p.part;
+  L.counters = p.counters;
+  L.status = p.status;
+  return L;
+}
+
+__device__ __forceinline__ bool row_used(const TcLocal& L, int m) { return L.hmode == 1 || (m % L.hblock) != 0; }
+
 // Final epilogue of 16 accumulator columns [c0, c0+16) of tile t for the
 // weight row r of this thread (128 epilogue threads, uniform control flow).
-__device__ __forceinline__ void final_chunk(const TcParams& p, int t, int c0, int r, int et, float (&v)[16],
-                                            float* xch) {
-  const int M = p.M;
-  if (p.mode == TC_HEAD) {
-    const HeadDesc& h = p.h;
+__device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int t, int c0, int r, int et,
+                                            float (&v)[16], float* xch) {
+  const int M = L.M;
+  if (L.mode == TC_HEAD) {
     const int vrow = t * 128 + r;
-    if (h.logits && vrow < h.V) {
+    if (L.logits && vrow < L.V) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c0 + j < M && head_row_used(h, c0 + j)) head_store_logit(h, c0 + j, vrow, v[j]);
+      for (int j = 0; j < 16; ++j) {
+        const int m = c0 + j;
+        if (m < M && row_used(L, m)) {
+          size_t row;
+          if (L.hmode == 1) {
+            row = (size_t)m;
+          } else {
+            row = (size_t)(m / L.hblock) * (L.hblock - 1) + (m % L.hblock) - 1;
+          }
+          L.logits[row * L.V + vrow] = v[j];
+        }
+      }
     }
     tc::named_bar(1, 128);
 #pragma unroll
@@ -100,10 +148,10 @@ __device__ __forceinline__ void final_chunk(const TcParams& p, int t, int c0, in
     const int jc = et >> 3, g8 = et & 7;  // column jc, rows 16*g8 .. 16*g8+15
     const int m = c0 + jc;
     Top2 tp = top2_empty();
-    if (m < M && head_row_used(h, m)) {
+    if (m < M && row_used(L, m)) {
       for (int rr = 16 * g8; rr < 16 * g8 + 16; ++rr) {
         const int vi = t * 128 + rr;
-        if (vi < h.V) top2_push(tp, xch[jc * 128 + rr], vi, p.status);
+        if (vi < L.V) top2_push(tp, xch[jc * 128 + rr], vi, L.status);
       }
     }
 #pragma unroll
@@ -114,36 +162,38 @@ __device__ __forceinline__ void final_chunk(const TcParams& p, int t, int c0, in
       u.v2 = __shfl_xor_sync(0xffffffffu, tp.v2, o);
       tp = top2_merge(tp, u);
     }
-    if (g8 == 0 && m < M) p.tops[(size_t)t * M + m] = tp;
+    if (g8 == 0 && m < M) L.tops[(size_t)t * M + m] = tp;
     return;
   }
-  const GemmDesc& g = p.g;
-  const int seg = t / p.tiles_per_seg, tile = t % p.tiles_per_seg;
-  if (g.kind == EPI_STORE || g.kind == EPI_RESID) {
+  const int tile = t % L.tps;
+  if (L.kind == EPI_STORE || L.kind == EPI_RESID) {
     const int n = tile * 128 + r;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < M) epi_single<__nv_bfloat16>(g, n, c0 + j, v[j]);
+      if (c0 + j < M) epi_single<__nv_bfloat16>(e, n, c0 + j, v[j]);
     return;
   }
   // pair epilogues: partner row r + half lives in another warp
-  const int half = (g.kind == EPI_SWIGLU) ? 64 : g.d / 2;
-  const int blk = (g.kind == EPI_SWIGLU) ? 128 : g.d;
+  const int half = (L.kind == EPI_SWIGLU) ? 64 : L.d / 2;
+  const int blk = (L.kind == EPI_SWIGLU) ? 128 : L.d;
   tc::named_bar(1, 128);
 #pragma unroll
   for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
   tc::named_bar(1, 128);
   if ((r % blk) < half) {
     int u;
-    if (g.kind == EPI_SWIGLU) {
+    if (L.kind == EPI_SWIGLU) {
       u = tile * 64 + r;
     } else {
       const int rr = tile * 128 + r;
-      u = (rr / g.d) * half + rr % g.d;
+      u = (rr / L.d) * half + rr % L.d;
     }
+    float w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = xch[j * 128 + r + half];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < M) epi_pair<__nv_bfloat16>(g, seg, u, c0 + j, v[j], xch[j * 128 + r + half]);
+      if (c0 + j < M) epi_pair<__nv_bfloat16>(e, u, c0 + j, v[j], w[j]);
   }
 }
 
@@ -163,9 +213,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
+  const TcLocal L = tc_local(p);
+  const CUtensorMap* wmaps = p.wmap;
+  const CUtensorMap* xmap = &p.xmap;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = p.nkb;
-  const long long p0 = run_start(p.T, p.G, blockIdx.x), p1 = run_start(p.T, p.G, blockIdx.x + 1);
+  const int nkb = L.nkb;
+  const long long p0 = run_start(L.T, L.G, blockIdx.x), p1 = run_start(L.T, L.G, blockIdx.x + 1);
   const int n_my = (int)(p1 - p0);
 
   if (threadIdx.x == 0) {
@@ -181,8 +234,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     tc::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < (p.mode == TC_GEMM ? p.g.nseg : 1); ++s) tc::tma_prefetch_desc(&p.wmap[s]);
-    tc::tma_prefetch_desc(&p.xmap);
+    const int nmaps = L.mode == TC_GEMM ? p.g.nseg : 1;
+    for (int s = 0; s < nmaps; ++s) tc::tma_prefetch_desc(wmaps + s);
+    tc::tma_prefetch_desc(xmap);
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
   tc::tc_fence_before();
@@ -196,27 +250,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       // ---------------- TMA producer
       const uint64_t pol_w = tc::policy_evict_first();
       const uint64_t pol_x = tc::policy_evict_last();
+      const bool head = L.mode == TC_HEAD, swiglu = L.kind == EPI_SWIGLU;
+      const int tps = L.tps, inter = L.inter, row0 = L.row0;
+      int t = (int)(p0 / nkb), kb = (int)(p0 - (long long)t * nkb);  // position of load i
+      int t_x = t, kb_x = kb;                                          // position of the next X load
       auto load_w = [&](int i) {
-        const long long pos = p0 + i;
-        const int t = (int)(pos / nkb), kx = (int)(pos - (long long)t * nkb) * 64;
         uint8_t* a = smem + (i % ST) * Cfg::STAGE;
-        if (p.mode == TC_HEAD) {
-          tc::tma_load_2d(a, &p.wmap[0], kx, t * 128, &full[i % ST], pol_w);
+        const int kx = kb * 64;
+        if (head) {
+          tc::tma_load_2d(a, wmaps, kx, t * 128, &full[i % ST], pol_w);
         } else {
-          const GemmDesc& g = p.g;
-          const int seg = t / p.tiles_per_seg, tile = t % p.tiles_per_seg;
-          if (g.kind == EPI_SWIGLU) {
-            tc::tma_load_2d(a, &p.wmap[seg], kx, tile * 64, &full[i % ST], pol_w);
-            tc::tma_load_2d(a + kTcA / 2, &p.wmap[seg], kx, g.inter + tile * 64, &full[i % ST], pol_w);
+          const int seg = t / tps, tile = t - seg * tps;
+          if (swiglu) {
+            tc::tma_load_2d(a, wmaps + seg, kx, tile * 64, &full[i % ST], pol_w);
+            tc::tma_load_2d(a + kTcA / 2, wmaps + seg, kx, inter + tile * 64, &full[i % ST], pol_w);
           } else {
-            tc::tma_load_2d(a, &p.wmap[seg], kx, g.seg_row0 + tile * 128, &full[i % ST], pol_w);
+            tc::tma_load_2d(a, wmaps + seg, kx, row0 + tile * 128, &full[i % ST], pol_w);
           }
+        }
+        if (++kb == nkb) {
+          kb = 0;
+          ++t;
         }
       };
       auto load_x = [&](int i) {
-        const long long pos = p0 + i;
-        const int t = (int)(pos / nkb), kx = (int)(pos - (long long)t * nkb) * 64;
-        tc::tma_load_2d(smem + (i % ST) * Cfg::STAGE + kTcA, &p.xmap, kx, 0, &full[i % ST], pol_x);
+        tc::tma_load_2d(smem + (i % ST) * Cfg::STAGE + kTcA, xmap, kb_x * 64, 0, &full[i % ST], pol_x);
+        if (++kb_x == nkb) {
+          kb_x = 0;
+          ++t_x;
+        }
       };
       // weights depend on nothing upstream: fill the ring before the wait
       const int pre = n_my < ST ? n_my : ST;
@@ -230,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       for (int i = pre; i < n_my; ++i) {
         const int s = i % ST;
         if (!tc::mbar_wait(&empty[s], ((uint32_t)(i / ST) & 1u) ^ 1u, abort)) {
-          tc_timeout(p.status, abort);
+          tc_timeout(L.status, abort);
           break;
         }
         tc::mbar_arrive_expect_tx(&full[s], Cfg::STAGE);
@@ -246,6 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     if (lane == 0) {
       // ---------------- MMA issuer, one accumulator per piece, alternating
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, BN);
+      const uint32_t sbase = tc::smem_u32(smem);
       long long pos = p0;
       int i = 0, k = 0;
       bool stop = false;
@@ -254,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         const long long end = p1 < (long long)(t + 1) * nkb ? p1 : (long long)(t + 1) * nkb;
         const int b = k & 1;
         if (!tc::mbar_wait(&acce[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort)) {
-          tc_timeout(p.status, abort);
+          tc_timeout(L.status, abort);
           break;
         }
         tc::tc_fence_after();
@@ -262,12 +325,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         for (long long q = pos; q < end; ++q, ++i) {
           const int s = i % ST;
           if (!tc::mbar_wait(&full[s], (uint32_t)(i / ST) & 1u, abort)) {
-            tc_timeout(p.status, abort);
+            tc_timeout(L.status, abort);
             stop = true;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a = tc::smem_u32(smem + s * Cfg::STAGE);
+          const uint32_t a = sbase + (uint32_t)(s * Cfg::STAGE);
           const uint32_t bb = a + kTcA;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -286,17 +349,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // accumulator row = weight row within the tile
     const int et = threadIdx.x - 64;
-    const int M = p.M;
-    const int ncol = min(BN, ((M + 15) / 16) * 16);
+    const int ncol = min(BN, ((L.M + 15) / 16) * 16);
+    const uint32_t acce0 = tc::smem_u32(&acce[0]);
     long long pos = p0;
     int k = 0;
+    int seg_built = -1;
+    Epi e;
     while (pos < p1) {
       const int t = (int)(pos / nkb);
       const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
       const long long end = p1 < tend ? p1 : tend;
       const bool whole = (pos == tbeg && end == tend);
       const int b = k & 1;
-      if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort)) tc_timeout(p.status, abort);
+      if (L.mode == TC_GEMM && t / L.tps != seg_built) {
+        seg_built = t / L.tps;
+        e = make_epi(p.g, seg_built);
+      }
+      if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort)) tc_timeout(L.status, abort);
       tc::named_bar(1, 128);
       if (*abort) break;  // uniform: read after the barrier
       tc::tc_fence_after();
@@ -305,14 +374,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
-          final_chunk(p, t, c0, r, et, v, xch);
+          final_chunk(L, e, t, c0, r, et, v, xch);
         }
         tc::tc_fence_before();
         tc::named_bar(1, 128);
-        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&acce[b])) : "memory");
+        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
       } else {
         const long long slot = blockIdx.x + (long long)t;  // global piece index
-        float* dst0 = p.part + (size_t)slot * BN * 128 + r;
+        float* dst0 = L.part + (size_t)slot * BN * 128 + r;
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
@@ -321,11 +390,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         }
         tc::tc_fence_before();
         tc::named_bar(1, 128);
-        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&acce[b])) : "memory");
+        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
         __threadfence();
         tc::named_bar(1, 128);
         if (et == 0) {
-          uint32_t* ctr = p.counters + kCtrGemm + t;
+          uint32_t* ctr = L.counters + kCtrGemm + t;
           const uint32_t add = (uint32_t)(end - pos);
           const uint32_t old = atomicAdd(ctr, add);
           *s_flag = (old + add == (uint32_t)nkb);
@@ -334,18 +403,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         tc::named_bar(1, 128);
         if (*s_flag) {
           __threadfence();
-          const int first = run_of(tbeg, p.T, p.G) + t;
-          const int last = run_of(tend - 1, p.T, p.G) + t;
+          const int first = run_of(tbeg, L.T, L.G) + t;
+          const int last = run_of(tend - 1, L.T, L.G) + t;
           for (int c0 = 0; c0 < ncol; c0 += 16) {
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
             for (int sl = first; sl <= last; ++sl) {
-              const float* src = p.part + (size_t)sl * BN * 128 + (size_t)c0 * 128 + r;
+              const float* src = L.part + (size_t)sl * BN * 128 + (size_t)c0 * 128 + r;
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * 128);
             }
-            final_chunk(p, t, c0, r, et, v, xch);
+            final_chunk(L, e, t, c0, r, et, v, xch);
           }
         }
         tc::named_bar(1, 128);  // s_flag is rewritten by the next piece
@@ -360,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
-  if (p.mode == TC_HEAD) head_finish(p.h, gridDim.x, p.n_tiles, p.tops, &s_last_head);
+  if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, L.n_tiles, L.tops, &s_last_head);
 }
 
 // ------------------------------------------------------------------- host
