@@ -32,12 +32,20 @@ const char* kFamilyNames[kTraceFamilies] = {"embed",      "rmsnorm", "gemm_simt"
                                             "tap_store",  "convert"};
 }  // namespace
 
+// Inside stream capture an external record becomes an event node of the
+// graph; outside capture a plain record is used.
+cudaError_t record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, st, cudaEventRecordExternal)
+                                             : cudaEventRecord(e, st);
+}
+
 void trace_pre(cudaStream_t st, int family) {
   TraceState& t = g_trace;
   if (!t.on || (int)t.recs.size() >= t.cap) return;
   cudaEvent_t a = t.pool[2 * t.recs.size()];
-  // External records become event nodes when the stream is being captured.
-  if (cudaEventRecordWithFlags(a, st, cudaEventRecordExternal) == cudaSuccess) {
+  if (record(a, st) == cudaSuccess) {
     t.open_family = family;
     t.open_a = a;
   }
@@ -47,8 +55,7 @@ void trace_post(cudaStream_t st, double bytes) {
   TraceState& t = g_trace;
   if (!t.on || t.open_a == nullptr) return;
   cudaEvent_t b = t.pool[2 * t.recs.size() + 1];
-  if (cudaEventRecordWithFlags(b, st, cudaEventRecordExternal) == cudaSuccess)
-    t.recs.push_back(Rec{t.open_family, bytes, t.open_a, b});
+  if (record(b, st) == cudaSuccess) t.recs.push_back(Rec{t.open_family, bytes, t.open_a, b});
   t.open_a = nullptr;
 }
 
@@ -96,6 +103,22 @@ int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats) {
     s.bytes += r.bytes;
   }
   return kTraceFamilies;
+}
+
+int dflash_trace_launches(float* ms, int32_t* family, int32_t n) {
+  TraceState& t = g_trace;
+  if (n < 0 || (n > 0 && (!ms || !family))) return DFLASH_ERR_INVALID_ARG;
+  const int count = (int)t.recs.size();
+  for (int i = 0; i < count && i < n; ++i) {
+    float v = 0.f;
+    if (cudaEventElapsedTime(&v, t.recs[i].a, t.recs[i].b) != cudaSuccess) {
+      cudaGetLastError();
+      return DFLASH_ERR_CUDA;
+    }
+    ms[i] = v;
+    family[i] = t.recs[i].family;
+  }
+  return count;
 }
 
 int dflash_trace_end(void) {

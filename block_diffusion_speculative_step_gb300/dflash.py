@@ -29,7 +29,7 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_draft_block", "dflash_verify_accept", "dflash_path_select", "dflash_workspace_bytes",
            "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
-           "dflash_verify_accept_noalloc")
+           "dflash_verify_accept_noalloc", "dflash_trace_launches")
 DFLASH_TRACE_FAMILIES = 10
 
 
@@ -133,6 +133,7 @@ def lib(path: str | None = None):
         L.dflash_verify_accept_noalloc.argtypes = [vp, vp, vp]
         L.dflash_verify_accept_noalloc.restype = C.c_int
         L.dflash_trace_read.argtypes = [C.POINTER(dflash_trace_stat), i32]
+        L.dflash_trace_launches.argtypes = [vp, vp, i32]
         _lib = L
     return _lib
 
@@ -225,6 +226,17 @@ def dflash_trace_read() -> dict:
     if n < 0:
         _check(n)
     return {a.name.decode(): (int(a.launches), float(a.total_ms), float(a.bytes)) for a in arr[:n]}
+
+
+def dflash_trace_launches() -> list:
+    """[(family index, ms)] for every traced launch, in launch order."""
+    n = lib().dflash_trace_launches(None, None, 0)
+    if n < 0:
+        _check(n)
+    ms = (C.c_float * max(n, 1))()
+    fam = (C.c_int32 * max(n, 1))()
+    _check(0 if lib().dflash_trace_launches(ms, fam, n) >= 0 else DFLASH_ERR_CUDA)
+    return [(int(fam[i]), float(ms[i])) for i in range(n)]
 
 
 def dflash_trace_end():

@@ -330,6 +330,9 @@ typedef struct {
 int dflash_trace_begin(int32_t max_launches);
 int dflash_trace_pause(void);
 int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats);
+/* Per-launch durations of the traced work in launch order: ms[i], family[i]
+ * for i < min(n, count); returns count (the number of traced launches). */
+int dflash_trace_launches(float* ms, int32_t* family, int32_t n);
 int dflash_trace_end(void);
 
 /*
