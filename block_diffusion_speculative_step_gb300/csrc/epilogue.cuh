@@ -129,4 +129,96 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int u, int m, float va, f
   dst[half] = from_f<T>(vb);
 }
 
+// ---- 16-column forms used by the tensor-core kernel: every load of the 16
+// columns is issued before any store, so the columns do not serialise on
+// load latency (the compiler cannot prove the stores leave them untouched).
+
+__device__ __forceinline__ void epi_live16(const Epi& e, int c0, int M, bool (&live)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int m = c0 + j;
+    live[j] = m < M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+  }
+}
+
+// Residual add / store of output column n for token rows c0 .. c0+15.
+__device__ __forceinline__ void epi_single16(const Epi& e, int n, int c0, int M, const float (&v)[16]) {
+  bool live[16];
+  epi_live16(e, c0, M, live);
+  float old[16];
+  if (e.kind == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = live[j] ? e.out_f32[(size_t)(c0 + j) * e.ldo + n] : 0.f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (live[j]) e.out_f32[(size_t)(c0 + j) * e.ldo + n] = old[j] + v[j];
+}
+
+// Pair epilogue (SwiGLU, or RoPE + Q/K/V scatter) of unit u for token rows
+// c0 .. c0+15.
+template <typename T>
+__device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, int M, const float (&va)[16],
+                                           const float (&vb)[16]) {
+  bool live[16];
+  epi_live16(e, c0, M, live);
+  if (e.kind == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (live[j])
+        reinterpret_cast<T*>(e.act_out)[(size_t)(c0 + j) * e.inter + u] = from_f<T>(silu_f(va[j]) * vb[j]);
+    return;
+  }
+  const int d = e.d, half = e.half;
+  const int ra = e.seg_row0 + (u / half) * d + (u % half);
+  const int col = ra % d;  // < half
+  const bool rotate = ra < e.QD + e.KD;
+  int pos[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int m = c0 + j;
+    pos[j] = live[j] ? __ldg(e.base_pos + m / e.rows) + m % e.rows : -1;
+    if (pos[j] < 0 || pos[j] >= e.rope_max_pos) live[j] = false;  // outside the RoPE table: nothing is written
+  }
+  float2 cs[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    cs[j] = (live[j] && rotate) ? __ldg(reinterpret_cast<const float2*>(e.rope_cs) + (size_t)pos[j] * half + col)
+                                : make_float2(1.f, 0.f);
+  float lo[16], hi[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    lo[j] = va[j] * cs[j].x - vb[j] * cs[j].y;
+    hi[j] = vb[j] * cs[j].x + va[j] * cs[j].y;
+  }
+  if (ra < e.QD) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (live[j]) {
+        T* q = reinterpret_cast<T*>(e.q_out) + (size_t)(c0 + j) * e.QD + ra;
+        q[0] = from_f<T>(lo[j]);
+        q[half] = from_f<T>(hi[j]);
+      }
+    return;
+  }
+  const bool is_k = ra < e.QD + e.KD;
+  const int r = is_k ? ra - e.QD : ra - e.QD - e.KD;
+  const int head = r / d;
+  T* base = reinterpret_cast<T*>(is_k ? e.k_dst : e.v_dst);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (!live[j]) continue;
+    const int m = c0 + j;
+    const int s_idx = m / e.rows, idx = m % e.rows;
+    const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? pos[j] % e.kv_window : pos[j]) : idx;
+    if (slot >= e.kv_cap) continue;
+    T* dst = base + (((size_t)s_idx * e.nkv + head) * e.kv_cap + slot) * d + col;
+    dst[0] = from_f<T>(lo[j]);
+    dst[half] = from_f<T>(hi[j]);
+  }
+}
+
 }  // namespace dfl

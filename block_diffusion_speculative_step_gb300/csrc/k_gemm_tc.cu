@@ -167,10 +167,7 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
   }
   const int tile = t % L.tps;
   if (L.kind == EPI_STORE || L.kind == EPI_RESID) {
-    const int n = tile * 128 + r;
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (c0 + j < M) epi_single<__nv_bfloat16>(e, n, c0 + j, v[j]);
+    epi_single16(e, tile * 128 + r, c0, M, v);
     return;
   }
   // pair epilogues: partner row r + half lives in another warp
@@ -191,9 +188,7 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
     float w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = xch[j * 128 + r + half];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (c0 + j < M) epi_pair<__nv_bfloat16>(e, u, c0 + j, v[j], w[j]);
+    epi_pair16<__nv_bfloat16>(e, u, c0, M, v, w);
   }
 }
 
