@@ -265,7 +265,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 namespace cg = cooperative_groups;
 
-constexpr int kClusterWarps = 8;   // warps 0-3 take the low 64 keys of a chunk, warps 4-7 the high 64
+constexpr int kClusterWarps = 8;   // 2 row tiles x 4 key quarters of every chunk
+constexpr int kClQT = 32;          // query vectors per cluster CTA
 constexpr int kMaxNC = 16;
 
 template <int D>
@@ -274,39 +275,40 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
   pdl_wait();
   pdl_launch_dependents();
   constexpr int CH = kMmaCH;
-  constexpr int HK = CH / 2;         // keys per warp group and chunk
+  constexpr int QK = CH / 4;         // keys per warp and chunk
   constexpr int CPR = D / 8;         // 16-byte chunks per row
   constexpr int TILE = CH * D * 2;   // one K or V chunk tile, bytes
   constexpr int PST = D + 4;         // floats per row of a partial (16-byte aligned rows)
   extern __shared__ __align__(128) uint8_t smem_att[];
-  uint8_t* Qs = smem_att;              // [64][D]
-  uint8_t* KV = Qs + kAttnQT * D * 2;  // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
-  float* psm = reinterpret_cast<float*>(KV);  // [64][PST] CTA partial (after the chunk loop)
-  float* hsm = psm + kAttnQT * PST;           // [64][PST] high-key-half partial
+  uint8_t* Qs = smem_att;              // [32][D]
+  uint8_t* KV = Qs + kClQT * D * 2;    // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
+  float* psm = reinterpret_cast<float*>(KV);  // [32][PST] CTA partial (after the chunk loop)
+  float* qsm = psm + kClQT * PST;             // [3][32][PST] key-quarter partials 1..3
 
   cg::cluster_group cl = cg::this_cluster();
   const int NC = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
   const int s = blockIdx.z;
+  const int mode = a.mode, rows = a.rows, cap = a.cap;
   const int grp = a.nq / a.nkv;
-  const int nqv = a.rows * grp;
+  const int nqv = rows * grp;
   const int QD = a.nq * D;
   const int P = a.base_pos[s];
   SeqKeys sk;
-  if (a.mode == DFLASH_ATTN_CAUSAL) {
-    sk.n_ctx = min(max(P + a.rows, 0), a.cap);
+  if (mode == DFLASH_ATTN_CAUSAL) {
+    sk.n_ctx = min(max(P + rows, 0), cap);
     sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
     sk.n_ch = sk.n_ctx_ch;
   } else {
-    sk.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), a.cap);
+    sk.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), cap);
     sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
     sk.n_ch = sk.n_ctx_ch + 1;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int wq = warp & 3, kh = warp >> 2;
-  const int qv0 = qt * kAttnQT;
-  const int nq_tile = min(kAttnQT, nqv - qv0);
+  const int wq = warp & 1, kq = warp >> 1;
+  const int qv0 = qt * kClQT;
+  const int nq_tile = min(kClQT, nqv - qv0);
   const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
   const uint32_t qb = __cvta_generic_to_shared(Qs);
   const uint32_t kvb = __cvta_generic_to_shared(KV);
@@ -332,13 +334,13 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
   };
 
   // ---- stage Q (rows >= nq_tile zero) with the first chunk, then the second
-  for (int t = threadIdx.x; t < kAttnQT * CPR; t += blockDim.x) {
+  for (int t = threadIdx.x; t < kClQT * CPR; t += blockDim.x) {
     const int qi = t / CPR, ch = t % CPR;
     if (qi < nq_tile) {
       const int qv = qv0 + qi;
       const int row = qv / grp, head = g * grp + qv % grp;
       const __nv_bfloat16* q =
-          reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * a.rows + row) * QD + (size_t)head * D;
+          reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * rows + row) * QD + (size_t)head * D;
       cp_async16(qb + swz<D>(qi, ch), q + ch * 8);
     } else {
       *reinterpret_cast<uint4*>(Qs + swz<D>(qi, ch)) = make_uint4(0, 0, 0, 0);
@@ -373,34 +375,34 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
       const __nv_bfloat16* vp;
       chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
     }
-    if (warp_on && HK * kh < nk) {
-      // S = Q K^T over this warp's half of the chunk (keys HK*kh .. HK*kh + HK)
-      float S[HK / 8][4];
+    if (warp_on && QK * kq < nk) {
+      // S = Q K^T over this warp's quarter of the chunk (keys QK*kq .. QK*kq + QK)
+      float S[QK / 8][4];
 #pragma unroll
-      for (int t = 0; t < HK / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
+      for (int t = 0; t < QK / 8; ++t) S[t][0] = S[t][1] = S[t][2] = S[t][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(qb + swz<D>(r0 + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < HK / 16; ++nt) {
+        for (int nt = 0; nt < QK / 16; ++nt) {
           uint32_t b0, b1, b2, b3;
-          const int key = HK * kh + 16 * nt + (lane & 7) + ((lane >> 4) << 3);
+          const int key = QK * kq + 16 * nt + (lane & 7) + ((lane >> 4) << 3);
           ldsm_x4(kb + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
           mma_16816(S[2 * nt], a0, a1, a2, a3, b0, b1);
           mma_16816(S[2 * nt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-      // mask, scale to log2 units, maxima over this half
-      const bool causal = a.mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
+      // mask, scale to log2 units, maxima over this quarter
+      const bool causal = mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
       const int lim_a = causal ? P + row_a - slot0 : CH;
       const int lim_b = causal ? P + row_b - slot0 : CH;
       float cm_a = -INFINITY, cm_b = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < HK / 8; ++t) {
+      for (int t = 0; t < QK / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int j = HK * kh + 8 * t + 2 * (lane & 3) + e;  // key index within the chunk
+          const int j = QK * kq + 8 * t + 2 * (lane & 3) + e;  // key index within the chunk
           S[t][e] = (j < nk && j <= lim_a) ? S[t][e] * scale : -INFINITY;
           S[t][2 + e] = (j < nk && j <= lim_b) ? S[t][2 + e] * scale : -INFINITY;
           cm_a = fmaxf(cm_a, S[t][e]);
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
       const float al_b = (m_b == -INFINITY) ? 0.f : exp2f(m_b - mn_b);
       float sl_a = 0.f, sl_b = 0.f;
 #pragma unroll
-      for (int t = 0; t < HK / 8; ++t) {
+      for (int t = 0; t < QK / 8; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float pa = (S[t][e] == -INFINITY) ? 0.f : exp2f(S[t][e] - mn_a);
@@ -443,9 +445,9 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
         O[t][2] *= al_b;
         O[t][3] *= al_b;
       }
-      // O += P V over the half
+      // O += P V over the quarter
 #pragma unroll
-      for (int kk = 0; kk < HK / 16; ++kk) {
+      for (int kk = 0; kk < QK / 16; ++kk) {
         const uint32_t a0 = pack_bf16(S[2 * kk][0], S[2 * kk][1]);
         const uint32_t a1 = pack_bf16(S[2 * kk][2], S[2 * kk][3]);
         const uint32_t a2 = pack_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1]);
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
           uint32_t b0, b1, b2, b3;
-          const int key = HK * kh + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int key = QK * kq + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
           ldsm_x4_t(vb + swz<D>(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
           mma_16816(O[2 * dt], a0, a1, a2, a3, b0, b1);
           mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
@@ -467,10 +469,10 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
-  // ---- merge the two key halves (low half first), then this CTA's partial
-  if (warp_on && kh == 1) {
-    float* pa = hsm + (size_t)qa * PST;
-    float* pb = hsm + (size_t)qb2 * PST;
+  // ---- merge the four key quarters in order, then this CTA's partial
+  if (warp_on && kq > 0) {
+    float* pa = qsm + ((size_t)(kq - 1) * kClQT + qa) * PST;
+    float* pb = qsm + ((size_t)(kq - 1) * kClQT + qb2) * PST;
 #pragma unroll
     for (int t = 0; t < D / 8; ++t) {
       const int col = 8 * t + 2 * (lane & 3);
@@ -483,28 +485,51 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
     pb[D + (lane & 3)] = (lane & 3) == 0 ? m_b : l_b;
   }
   __syncthreads();
-  if (warp_on && kh == 0) {
+  if (warp_on && kq == 0) {
+    float Ma = m_a, Mb = m_b;
+#pragma unroll
+    for (int qq = 0; qq < 3; ++qq) {
+      Ma = fmaxf(Ma, qsm[((size_t)qq * kClQT + qa) * PST + D]);
+      Mb = fmaxf(Mb, qsm[((size_t)qq * kClQT + qb2) * PST + D]);
+    }
+    float wa[4], wb[4];
+    wa[0] = (m_a == -INFINITY) ? 0.f : exp2f(m_a - Ma);
+    wb[0] = (m_b == -INFINITY) ? 0.f : exp2f(m_b - Mb);
+    float La = l_a * wa[0], Lb = l_b * wb[0];
+#pragma unroll
+    for (int qq = 0; qq < 3; ++qq) {
+      const float* ha = qsm + ((size_t)qq * kClQT + qa) * PST;
+      const float* hb = qsm + ((size_t)qq * kClQT + qb2) * PST;
+      wa[qq + 1] = (ha[D] == -INFINITY) ? 0.f : exp2f(ha[D] - Ma);
+      wb[qq + 1] = (hb[D] == -INFINITY) ? 0.f : exp2f(hb[D] - Mb);
+      La = fmaf(ha[D + 1], wa[qq + 1], La);
+      Lb = fmaf(hb[D + 1], wb[qq + 1], Lb);
+    }
     float* pa = psm + (size_t)qa * PST;
     float* pb = psm + (size_t)qb2 * PST;
-    const float* ha = hsm + (size_t)qa * PST;
-    const float* hb = hsm + (size_t)qb2 * PST;
-    const float m1a = ha[D], l1a = ha[D + 1], m1b = hb[D], l1b = hb[D + 1];
-    const float Ma = fmaxf(m_a, m1a), Mb = fmaxf(m_b, m1b);
-    const float w0a = (m_a == -INFINITY) ? 0.f : exp2f(m_a - Ma), w1a = (m1a == -INFINITY) ? 0.f : exp2f(m1a - Ma);
-    const float w0b = (m_b == -INFINITY) ? 0.f : exp2f(m_b - Mb), w1b = (m1b == -INFINITY) ? 0.f : exp2f(m1b - Mb);
 #pragma unroll
     for (int t = 0; t < D / 8; ++t) {
       const int col = 8 * t + 2 * (lane & 3);
-      pa[col] = fmaf(O[t][0], w0a, ha[col] * w1a);
-      pa[col + 1] = fmaf(O[t][1], w0a, ha[col + 1] * w1a);
-      pb[col] = fmaf(O[t][2], w0b, hb[col] * w1b);
-      pb[col + 1] = fmaf(O[t][3], w0b, hb[col + 1] * w1b);
+      float oa0 = O[t][0] * wa[0], oa1 = O[t][1] * wa[0], ob0 = O[t][2] * wb[0], ob1 = O[t][3] * wb[0];
+#pragma unroll
+      for (int qq = 0; qq < 3; ++qq) {
+        const float* ha = qsm + ((size_t)qq * kClQT + qa) * PST;
+        const float* hb = qsm + ((size_t)qq * kClQT + qb2) * PST;
+        oa0 = fmaf(ha[col], wa[qq + 1], oa0);
+        oa1 = fmaf(ha[col + 1], wa[qq + 1], oa1);
+        ob0 = fmaf(hb[col], wb[qq + 1], ob0);
+        ob1 = fmaf(hb[col + 1], wb[qq + 1], ob1);
+      }
+      pa[col] = oa0;
+      pa[col + 1] = oa1;
+      pb[col] = ob0;
+      pb[col + 1] = ob1;
     }
     if ((lane & 3) == 0) {
       pa[D] = Ma;
-      pa[D + 1] = fmaf(l_a, w0a, l1a * w1a);
+      pa[D + 1] = La;
       pb[D] = Mb;
-      pb[D + 1] = fmaf(l_b, w0b, l1b * w1b);
+      pb[D + 1] = Lb;
     }
   }
   cl.sync();
@@ -527,7 +552,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
     }
     const int qv = qv0 + qi;
     const int row = qv / grp, head = g * grp + qv % grp;
-    outp[((size_t)s * a.rows + row) * QD + (size_t)head * D + e] = __float2bfloat16_rn(L > 0.f ? Ov / L : 0.f);
+    outp[((size_t)s * rows + row) * QD + (size_t)head * D + e] = __float2bfloat16_rn(L > 0.f ? Ov / L : 0.f);
   }
   cl.sync();  // peers keep their shared memory until every rank has read it
 }
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
 
 namespace {
 
-size_t cluster_smem(int d) { return (size_t)kAttnQT * d * 2 + 4 * (size_t)kMmaCH * d * 2; }
+size_t cluster_smem(int d) { return (size_t)kClQT * d * 2 + 4 * (size_t)kMmaCH * d * 2; }
 
 template <int D>
 cudaLaunchConfig_t cluster_cfg(int nc, dim3 grid, cudaStream_t st, cudaLaunchAttribute* at) {
@@ -582,10 +607,10 @@ int clusters_resident(int nc) {
   return cache[dev][nc];
 }
 
-// Cluster width: the widest (<= 16) whose clusters for this batch shape all
-// run at once, at least 8.  Depends on the batch shape and the device, never
-// on the row count alone, so decode (1 row) and verification (a block) of one
-// batch use the same width.
+// Cluster width: the widest (<= 16) for which two clusters per (sequence,
+// kv head) all run at once, at least 8.  Depends on the sequence and head
+// counts and the device, never on the row count, so decode (1 row) and
+// verification (a block) of one batch use the same width and per-row order.
 template <int D>
 int pick_nc(long groups) {
   for (int nc = kMaxNC; nc > 8; --nc)
@@ -600,7 +625,7 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv * n_qt);
+  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv * 2);
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
   return cudaLaunchKernelEx(&cfg, k, a, n_qt);
@@ -618,7 +643,8 @@ cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   AttnGeom g = attn_geom(a);
   if (a.n_seqs == 0 || a.rows == 0) return cudaSuccess;
   if (a.dtype == DFLASH_BF16) {
-    return a.d == 128 ? launch_cluster<128>(a, g.n_qt, st) : launch_cluster<64>(a, g.n_qt, st);
+    const int n_qt = (g.nqv + kClQT - 1) / kClQT;
+    return a.d == 128 ? launch_cluster<128>(a, n_qt, st) : launch_cluster<64>(a, n_qt, st);
   }
   dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);
   const size_t smem = (size_t)(2 * kSimtCH * (a.d + 1) + kAttnWarps * a.d + kAttnWarps * kSimtCH) * sizeof(float);

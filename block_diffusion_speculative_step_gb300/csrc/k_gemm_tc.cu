@@ -404,10 +404,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            for (int sl = first; sl <= last; ++sl) {
-              const float* src = L.part + (size_t)sl * BN * 128 + (size_t)c0 * 128 + r;
+            // partial slots in k order; each batch of up to 4 slots is loaded at once
+            for (int sb = first; sb <= last; sb += 4) {
+              float pv[4][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * 128);
+              for (int q = 0; q < 4; ++q) {
+                const float* src = L.part + (size_t)(sb + q) * BN * 128 + (size_t)c0 * 128 + r;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (sb + q <= last) v[j] += pv[q][j];
             }
             final_chunk(L, e, t, c0, r, et, v, xch);
           }

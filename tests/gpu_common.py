@@ -47,3 +47,30 @@ def check_argmax(gpu_idx, ora_idx, ora_margin, gpu_logits=None, ora_logits=None,
             assert mg < tol, f"row {i}: gpu argmax {g} != oracle {o} with oracle margin {mg:.3g} >= {tol}"
             excl += 1
     return excl
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """One unit in the last place of bfloat16 at |x| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def assert_bf16_close(got, ref, ulps: float = 1.0):
+    """Values the GPU stores in bf16 (K/V cache, fused features): the GPU
+    rounds an fp32 sum, the oracle an fp64 one, so a value sitting on a
+    rounding boundary may land one bf16 step away."""
+    got, ref = np.asarray(got, dtype=np.float64), np.asarray(ref, dtype=np.float64)
+    tol = ulps * bf16_ulp(ref) + 1e-6
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} beyond {ulps} bf16 ulp; max err {np.abs(got - ref).max():.4g}"
+
+
+def assert_hidden_close(got, ref):
+    """fp32 residual stream after one bf16 layer: bf16 rounding of the
+    projection inputs (one-step differences at rounding boundaries) and of
+    the attention probabilities move individual outputs by up to ~1e-2 of
+    their size; bound |err| <= 0.02 * max(1, |ref|)."""
+    got, ref = np.asarray(got, dtype=np.float64), np.asarray(ref, dtype=np.float64)
+    tol = 2e-2 * np.maximum(1.0, np.abs(ref))
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} beyond tolerance; max err {np.abs(got - ref).max():.4g}"

@@ -60,9 +60,9 @@ def test_fullsize_causal_layer(big):
     assert eng.status() == D.DFLASH_OK
     h = h0.double().numpy().copy()
     O.decoder_layer(ocfg(w, w.target), olayer(w, w.target, m["target"]["layers"][0]), h, CTX, O.CAUSAL, kc, vc)
-    np.testing.assert_allclose(got, h, rtol=0, atol=2e-2)
+    G.assert_hidden_close(got, h)
     # the block's K/V went into the cache at positions CTX .. CTX+B-1
-    np.testing.assert_allclose(G.f64(eng.caches.tk[0][0, :, CTX:CTX + B]), kc[:, CTX:CTX + B], rtol=0, atol=3e-2)
+    G.assert_bf16_close(G.f64(eng.caches.tk[0][0, :, CTX:CTX + B]), kc[:, CTX:CTX + B])
 
 
 def test_fullsize_draft_layer(big):
@@ -87,7 +87,7 @@ def test_fullsize_draft_layer(big):
     h = h0.double().numpy().copy()
     O.decoder_layer(ocfg(w, w.draft), olayer(w, w.draft, m["draft"]["layers"][2]), h, CTX, O.BIDIR,
                     G.f64(eng.caches.dk[2][0]), G.f64(eng.caches.dv[2][0]))
-    np.testing.assert_allclose(got, h, rtol=0, atol=2e-2)
+    G.assert_hidden_close(got, h)
 
 
 def test_fullsize_fusion(big):
@@ -111,12 +111,10 @@ def test_fullsize_fusion(big):
     pos = list(range(CTX, CTX + 11))
     cref = O.fuse_context(dc, F, n(m["fc"]), n(m["fc_norm"]), G.f64(feats[:11].reshape(11, F * H)), pos, wk, wv,
                           kcs, vcs)
-    np.testing.assert_allclose(G.f64(cout[:11]), cref, rtol=0, atol=3e-2)
+    G.assert_bf16_close(G.f64(cout[:11]), cref)
     for j in range(w.draft.layers):
-        np.testing.assert_allclose(G.f64(eng.caches.dk[j][0, :, CTX:CTX + 11]), kcs[j][:, CTX:CTX + 11], rtol=0,
-                                   atol=3e-2)
-        np.testing.assert_allclose(G.f64(eng.caches.dv[j][0, :, CTX:CTX + 11]), vcs[j][:, CTX:CTX + 11], rtol=0,
-                                   atol=3e-2)
+        G.assert_bf16_close(G.f64(eng.caches.dk[j][0, :, CTX:CTX + 11]), kcs[j][:, CTX:CTX + 11])
+        G.assert_bf16_close(G.f64(eng.caches.dv[j][0, :, CTX:CTX + 11]), vcs[j][:, CTX:CTX + 11])
 
 
 def test_fullsize_verify_accept(big):
