@@ -129,93 +129,137 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int u, int m, float va, f
   dst[half] = from_f<T>(vb);
 }
 
-// ---- 16-column forms used by the tensor-core kernel: every load of the 16
-// columns is issued before any store, so the columns do not serialise on
-// load latency (the compiler cannot prove the stores leave them untouched).
+// ---- 16-column forms used by the tensor-core kernel.  Every load the
+// epilogue of one output row needs is issued early, while the accumulator is
+// still being computed, so the tail after the last MMA holds only arithmetic
+// and stores:
+//   epi_preload_rows -- liveness, token positions, RoPE (cos, sin) for the
+//     row's rotation column.  With tiles aligned to heads these depend only on
+//     the row within the head, never on the tile, so one load serves every
+//     tile of the run.
+//   epi_preload_tile -- per output column: the residual being added to, or
+//     an L2 prefetch of the store destination.
 
-__device__ __forceinline__ void epi_live16(const Epi& e, int c0, int M, bool (&live)[16]) {
+struct EpiRows {
+  uint32_t live;    // bit j: token row c0 + j is written
+  uint32_t inpos;   // QKV, bit j: the row's position lies inside the RoPE table
+  uint32_t kvr[16]; // QKV: K/V destination row (sequence, head 0, slot) of token row c0 + j; ~0u: none
+  float2 cs[16];    // QKV: rotation (cos, sin) of the row's column
+};
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Rotation column of QKV unit u (the pair (col, col + d/2) of one head).
+__device__ __forceinline__ int epi_rope_col(const Epi& e, int u) {
+  return (e.seg_row0 + (u / e.half) * e.d + (u % e.half)) % e.d;
+}
+
+__device__ __forceinline__ void epi_preload_rows(const Epi& e, int u, int c0, int M, EpiRows& p) {
+  p.live = 0u;
+  p.inpos = 0u;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int m = c0 + j;
-    live[j] = m < M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+    const bool lv = m < M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+    p.live |= lv ? (1u << j) : 0u;
+    p.kvr[j] = ~0u;
+    p.cs[j] = make_float2(1.f, 0.f);
+  }
+  if (e.kind != EPI_QKV) return;
+  const int col = epi_rope_col(e, u);
+  int pos[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int m = c0 + j;
+    pos[j] = (p.live >> j) & 1u ? __ldg(e.base_pos + m / e.rows) + m % e.rows : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (pos[j] < 0 || pos[j] >= e.rope_max_pos) continue;  // outside the RoPE table: nothing is written
+    p.inpos |= 1u << j;
+    p.cs[j] = __ldg(reinterpret_cast<const float2*>(e.rope_cs) + (size_t)pos[j] * e.half + col);
+    const int m = c0 + j;
+    const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? pos[j] % e.kv_window : pos[j]) : m % e.rows;
+    if (slot < e.kv_cap) p.kvr[j] = (uint32_t)((m / e.rows) * e.nkv) * (uint32_t)e.kv_cap + (uint32_t)slot;
+  }
+}
+
+// n: output column (single kinds) or unit (pair kinds).
+__device__ __forceinline__ void epi_preload_tile(const Epi& e, int n, int c0, const EpiRows& rw, float (&old)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) old[j] = 0.f;
+  if (!(rw.live & 1u)) return;
+  if (e.kind == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if ((rw.live >> j) & 1u) old[j] = e.out_f32[(size_t)(c0 + j) * e.ldo + n];
+  } else if (e.kind == EPI_STORE) {
+    prefetch_l2(e.out_f32 + (size_t)c0 * e.ldo + n);
+  } else if (e.kind == EPI_SWIGLU) {
+    if (e.act_out) prefetch_l2(static_cast<const char*>(e.act_out) + ((size_t)c0 * e.inter + n) * 2);
+  } else if (rw.inpos & 1u) {
+    const int ra = e.seg_row0 + (n / e.half) * e.d + (n % e.half);
+    if (ra < e.QD) {
+      prefetch_l2(static_cast<const char*>(e.q_out) + ((size_t)c0 * e.QD + ra) * 2);
+    } else if (rw.kvr[0] != ~0u) {
+      const bool is_k = ra < e.QD + e.KD;
+      const int r = is_k ? ra - e.QD : ra - e.QD - e.KD;
+      prefetch_l2(static_cast<const char*>(is_k ? e.k_dst : e.v_dst) +
+                  (((size_t)rw.kvr[0] + (size_t)(r / e.d) * e.kv_cap) * e.d + ra % e.d) * 2);
+    }
   }
 }
 
 // Residual add / store of output column n for token rows c0 .. c0+15.
-__device__ __forceinline__ void epi_single16(const Epi& e, int n, int c0, int M, const float (&v)[16]) {
-  bool live[16];
-  epi_live16(e, c0, M, live);
-  float old[16];
-  if (e.kind == EPI_RESID) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) old[j] = live[j] ? e.out_f32[(size_t)(c0 + j) * e.ldo + n] : 0.f;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) old[j] = 0.f;
-  }
+__device__ __forceinline__ void epi_single16(const Epi& e, int n, int c0, const float (&v)[16], const EpiRows& rw,
+                                             const float (&old)[16]) {
 #pragma unroll
   for (int j = 0; j < 16; ++j)
-    if (live[j]) e.out_f32[(size_t)(c0 + j) * e.ldo + n] = old[j] + v[j];
+    if ((rw.live >> j) & 1u) e.out_f32[(size_t)(c0 + j) * e.ldo + n] = old[j] + v[j];
 }
 
 // Pair epilogue (SwiGLU, or RoPE + Q/K/V scatter) of unit u for token rows
 // c0 .. c0+15.
 template <typename T>
-__device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, int M, const float (&va)[16],
-                                           const float (&vb)[16]) {
-  bool live[16];
-  epi_live16(e, c0, M, live);
+__device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, const float (&va)[16], const float (&vb)[16],
+                                           const EpiRows& rw) {
   if (e.kind == EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (live[j])
+      if ((rw.live >> j) & 1u)
         reinterpret_cast<T*>(e.act_out)[(size_t)(c0 + j) * e.inter + u] = from_f<T>(silu_f(va[j]) * vb[j]);
     return;
   }
   const int d = e.d, half = e.half;
   const int ra = e.seg_row0 + (u / half) * d + (u % half);
   const int col = ra % d;  // < half
-  const bool rotate = ra < e.QD + e.KD;
-  int pos[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int m = c0 + j;
-    pos[j] = live[j] ? __ldg(e.base_pos + m / e.rows) + m % e.rows : -1;
-    if (pos[j] < 0 || pos[j] >= e.rope_max_pos) live[j] = false;  // outside the RoPE table: nothing is written
-  }
-  float2 cs[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    cs[j] = (live[j] && rotate) ? __ldg(reinterpret_cast<const float2*>(e.rope_cs) + (size_t)pos[j] * half + col)
-                                : make_float2(1.f, 0.f);
+  const bool rotate = ra < e.QD + e.KD;  // Q and K rows turn by pos * w_col; V rows do not
   float lo[16], hi[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    lo[j] = va[j] * cs[j].x - vb[j] * cs[j].y;
-    hi[j] = vb[j] * cs[j].x + va[j] * cs[j].y;
+    const float2 cs = rotate ? rw.cs[j] : make_float2(1.f, 0.f);
+    lo[j] = va[j] * cs.x - vb[j] * cs.y;
+    hi[j] = vb[j] * cs.x + va[j] * cs.y;
   }
   if (ra < e.QD) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (live[j]) {
+      if ((rw.inpos >> j) & 1u) {
         T* q = reinterpret_cast<T*>(e.q_out) + (size_t)(c0 + j) * e.QD + ra;
         q[0] = from_f<T>(lo[j]);
         q[half] = from_f<T>(hi[j]);
       }
     return;
   }
-  const bool is_k = ra < e.QD + e.KD;
+  const bool is_k = rotate;
   const int r = is_k ? ra - e.QD : ra - e.QD - e.KD;
-  const int head = r / d;
-  T* base = reinterpret_cast<T*>(is_k ? e.k_dst : e.v_dst);
+  T* base = reinterpret_cast<T*>(is_k ? e.k_dst : e.v_dst) + (size_t)(r / d) * e.kv_cap * d + col;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    if (!live[j]) continue;
-    const int m = c0 + j;
-    const int s_idx = m / e.rows, idx = m % e.rows;
-    const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? pos[j] % e.kv_window : pos[j]) : idx;
-    if (slot >= e.kv_cap) continue;
-    T* dst = base + (((size_t)s_idx * e.nkv + head) * e.kv_cap + slot) * d + col;
+    if (rw.kvr[j] == ~0u) continue;
+    T* dst = base + (size_t)rw.kvr[j] * d;
     dst[0] = from_f<T>(lo[j]);
     dst[half] = from_f<T>(hi[j]);
   }

@@ -28,6 +28,8 @@
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace dfl {
 
@@ -265,35 +267,51 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 namespace cg = cooperative_groups;
 
-constexpr int kClusterWarps = 8;   // 2 row tiles x 4 key quarters of every chunk
-constexpr int kClQT = 32;          // query vectors per cluster CTA
+constexpr int kClusterWarps = 16;  // 4 row tiles x 4 key quarters of every chunk
+constexpr int kClQT = 64;          // query vectors per cluster CTA
 constexpr int kMaxNC = 16;
 
+struct AttnTma {
+  CUtensorMap kc, vc;  // cache [S*nkv*cap][D], box 64 dims x 128 keys, 128-byte swizzle
+  CUtensorMap kb, vb;  // block scratch [S*nkv*rows][D] (bidirectional mode)
+  AttnDesc a;
+};
+
+// Byte offset of (key row j, 16-byte chunk ch) in a 128-key tile written by
+// two (D = 128) or one (D = 64) TMA boxes of 64 dims with 128-byte swizzle.
+__device__ __forceinline__ uint32_t kv_off(int j, int ch) {
+  return (uint32_t)((ch >> 3) * (kMmaCH * 128) + j * 128 + (((ch & 7) ^ (j & 7)) << 4));
+}
+
 template <int D>
-__global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const __grid_constant__ AttnDesc a,
-                                                                           int n_qt) {
-  pdl_wait();
-  pdl_launch_dependents();
+__global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(const __grid_constant__ AttnTma p,
+                                                                              int n_qt) {
   constexpr int CH = kMmaCH;
   constexpr int QK = CH / 4;         // keys per warp and chunk
   constexpr int CPR = D / 8;         // 16-byte chunks per row
   constexpr int TILE = CH * D * 2;   // one K or V chunk tile, bytes
   constexpr int PST = D + 4;         // floats per row of a partial (16-byte aligned rows)
-  extern __shared__ __align__(128) uint8_t smem_att[];
-  uint8_t* Qs = smem_att;              // [32][D]
-  uint8_t* KV = Qs + kClQT * D * 2;    // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
-  float* psm = reinterpret_cast<float*>(KV);  // [32][PST] CTA partial (after the chunk loop)
-  float* qsm = psm + kClQT * PST;             // [3][32][PST] key-quarter partials 1..3
+  extern __shared__ __align__(1024) uint8_t smem_att[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_att) + 1023) & ~uintptr_t(1023));
+  uint8_t* KV = sm;                        // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
+  uint8_t* Qs = KV + 4 * TILE;             // [64][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(Qs + kClQT * D * 2);  // [2]
+  float* psm = reinterpret_cast<float*>(sm);         // [64][PST] CTA partial (after the chunk loop)
+  float* qsm = psm + kClQT * PST;                    // [3][64][PST] key-quarter partials 1..3
 
+  const AttnDesc& a = p.a;
   cg::cluster_group cl = cg::this_cluster();
   const int NC = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
   const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
   const int s = blockIdx.z;
-  const int mode = a.mode, rows = a.rows, cap = a.cap;
+  const int mode = a.mode, rows = a.rows, cap = a.cap, nkv = a.nkv;
   const int grp = a.nq / a.nkv;
   const int nqv = rows * grp;
   const int QD = a.nq * D;
+  uint32_t* status = a.status;
+  // base_pos is written only by the acceptance step, never by the kernel that
+  // precedes attention inside a call, so it may be read before the PDL wait.
   const int P = a.base_pos[s];
   SeqKeys sk;
   if (mode == DFLASH_ATTN_CAUSAL) {
@@ -306,34 +324,55 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
     sk.n_ch = sk.n_ctx_ch + 1;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int wq = warp & 1, kq = warp >> 1;
+  const int wq = warp & 3, kq = warp >> 2;
   const int qv0 = qt * kClQT;
   const int nq_tile = min(kClQT, nqv - qv0);
   const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
   const uint32_t qb = __cvta_generic_to_shared(Qs);
   const uint32_t kvb = __cvta_generic_to_shared(KV);
 
-  auto stage_chunk = [&](int c, int buf) {
-    const __nv_bfloat16* kp;
-    const __nv_bfloat16* vp;
-    int nk, slot0;
-    chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
+  // chunk c -> (is block chunk, first tensor row)
+  auto chunk_row = [&](int c, bool& blk) -> int {
+    blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
+    return blk ? (s * nkv + g) * rows : (s * nkv + g) * cap + c * CH;
+  };
+  auto issue = [&](int c, int buf) {  // one thread
+    bool blk;
+    const int row = chunk_row(c, blk);
+    const CUtensorMap* km = blk ? &p.kb : &p.kc;
+    const CUtensorMap* vm = blk ? &p.vb : &p.vc;
     uint8_t* Kt = KV + 2 * buf * TILE;
-    uint8_t* Vt = Kt + TILE;
-    const uint32_t kb = kvb + 2 * buf * TILE, vb = kb + TILE;
-    for (int t = threadIdx.x; t < CH * CPR; t += blockDim.x) {
-      const int j = t / CPR, ch = t % CPR;
-      if (j < nk) {
-        cp_async16(kb + swz<D>(j, ch), kp + (size_t)j * D + ch * 8);
-        cp_async16(vb + swz<D>(j, ch), vp + (size_t)j * D + ch * 8);
-      } else {
-        *reinterpret_cast<uint4*>(Kt + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Vt + swz<D>(j, ch)) = make_uint4(0, 0, 0, 0);
-      }
+    tc::mbar_arrive_expect_tx(&full[buf], 2 * TILE);
+    const uint64_t pol = tc::policy_evict_first();
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tc::tma_load_2d(Kt + h * (CH * 128), km, 64 * h, row, &full[buf], pol);
+      tc::tma_load_2d(Kt + TILE + h * (CH * 128), vm, 64 * h, row, &full[buf], pol);
     }
   };
+  // a chunk the preceding kernel cannot have written (context below P)
+  auto early_ok = [&](int c) { return c < sk.n_ctx_ch && (mode == DFLASH_ATTN_BLOCK_BIDIR || (c + 1) * CH <= P); };
 
-  // ---- stage Q (rows >= nq_tile zero) with the first chunk, then the second
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&full[0], 1);
+    tc::mbar_init(&full[1], 1);
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&p.kc);
+    tc::tma_prefetch_desc(&p.vc);
+  }
+  __syncthreads();
+  bool pre0 = false, pre1 = false;
+  if (threadIdx.x == 0) {
+    if (nmine > 0 && early_ok(rank)) { issue(rank, 0); pre0 = true; }
+    if (nmine > 1 && early_ok(rank + NC)) { issue(rank + NC, 1); pre1 = true; }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    if (nmine > 0 && !pre0) issue(rank, 0);
+    if (nmine > 1 && !pre1) issue(rank + NC, 1);
+  }
+  // ---- Q (rows >= nq_tile zero)
   for (int t = threadIdx.x; t < kClQT * CPR; t += blockDim.x) {
     const int qi = t / CPR, ch = t % CPR;
     if (qi < nq_tile) {
@@ -346,10 +385,8 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
       *reinterpret_cast<uint4*>(Qs + swz<D>(qi, ch)) = make_uint4(0, 0, 0, 0);
     }
   }
-  if (nmine > 0) stage_chunk(rank, 0);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  if (nmine > 1) stage_chunk(rank + NC, 1);
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  cp_async_wait_all();
+  __syncthreads();
 
   const int r0 = 16 * wq;  // this warp's 16 query vectors
   const bool warp_on = r0 < nq_tile;
@@ -360,22 +397,31 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
   float O[D / 8][4];
 #pragma unroll
   for (int t = 0; t < D / 8; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
+  bool failed = false;
 
   for (int i = 0; i < nmine; ++i) {
-    if (i + 1 < nmine)
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
     const int c = rank + i * NC, buf = i & 1;
-    const uint32_t kb = kvb + 2 * buf * TILE, vb = kb + TILE;
-    int nk, slot0;
-    {
-      const __nv_bfloat16* kp;
-      const __nv_bfloat16* vp;
-      chunk_keys<__nv_bfloat16>(a, sk, s, g, c, CH, kp, vp, nk, slot0);
+    if (!tc::mbar_wait(&full[buf], (uint32_t)(i >> 1) & 1u, nullptr)) {
+      raise_status(status, ST_TIMEOUT);
+      failed = true;
     }
-    if (warp_on && QK * kq < nk) {
+    const uint32_t kb = kvb + 2 * buf * TILE, vb = kb + TILE;
+    bool blk;
+    chunk_row(c, blk);
+    const int slot0 = blk ? -1 : c * CH;
+    const int nk = blk ? min(rows, CH) : min(CH, sk.n_ctx - c * CH);
+    if (nk < CH) {
+      // Rows past the last key hold whatever follows in memory (unwritten
+      // cache slots may be NaN); zero V there so that P = 0 contributes 0.
+      uint8_t* Vt = KV + (2 * buf + 1) * TILE;
+      for (int t = threadIdx.x; t < (CH - nk) * (D / 8); t += blockDim.x) {
+        const int j = nk + t / (D / 8), ch = t % (D / 8);
+        *reinterpret_cast<uint4*>(Vt + kv_off(j, ch)) = make_uint4(0, 0, 0, 0);
+      }
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+    }
+    if (!failed && warp_on && QK * kq < nk) {
       // S = Q K^T over this warp's quarter of the chunk (keys QK*kq .. QK*kq + QK)
       float S[QK / 8][4];
 #pragma unroll
@@ -388,7 +434,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
         for (int nt = 0; nt < QK / 16; ++nt) {
           uint32_t b0, b1, b2, b3;
           const int key = QK * kq + 16 * nt + (lane & 7) + ((lane >> 4) << 3);
-          ldsm_x4(kb + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
+          ldsm_x4(kb + kv_off(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
           mma_16816(S[2 * nt], a0, a1, a2, a3, b0, b1);
           mma_16816(S[2 * nt + 1], a0, a1, a2, a3, b2, b3);
         }
@@ -456,17 +502,15 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
         for (int dt = 0; dt < D / 16; ++dt) {
           uint32_t b0, b1, b2, b3;
           const int key = QK * kq + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-          ldsm_x4_t(vb + swz<D>(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
+          ldsm_x4_t(vb + kv_off(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
           mma_16816(O[2 * dt], a0, a1, a2, a3, b0, b1);
           mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
     __syncthreads();  // every warp is done with this buffer
-    if (i + 2 < nmine) stage_chunk(rank + (i + 2) * NC, buf);
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (threadIdx.x == 0 && i + 2 < nmine && !failed) issue(rank + (i + 2) * NC, buf);
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   // ---- merge the four key quarters in order, then this CTA's partial
@@ -534,25 +578,58 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
   }
   cl.sync();
 
-  // ---- merge the NC partials in rank order; rank r owns rows [r*RP, (r+1)*RP)
+  // ---- merge the NC partials in rank order; rank r owns rows [r*RP, (r+1)*RP).
+  // The per-(row, rank) weights are formed once; then every output element
+  // reads its NC partial values with independent loads.
   const int RP = (nq_tile + NC - 1) / NC;
-  const int q_lo = rank * RP, q_hi = min(nq_tile, q_lo + RP);
-  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out);
-  for (int t = threadIdx.x; t < (q_hi > q_lo ? (q_hi - q_lo) * D : 0); t += blockDim.x) {
-    const int qi = q_lo + t / D, e = t % D;
+  const int q_lo = rank * RP;
+  const int nrow = max(0, min(nq_tile, q_lo + RP) - q_lo);
+  float* mw = qsm;                   // [RP][kMaxNC] partial maxima, then weights
+  float* lw = mw + RP * kMaxNC;      // [RP][kMaxNC] partial sums
+  float* Ls = lw + RP * kMaxNC;      // [RP] merged sums
+  for (int t = threadIdx.x; t < nrow * NC; t += blockDim.x) {
+    const int i = t / NC, r = t % NC;
+    const float* pr = cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST;
+    mw[i * kMaxNC + r] = pr[D];
+    lw[i * kMaxNC + r] = pr[D + 1];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nrow; i += blockDim.x) {
     float M = -INFINITY;
-    for (int r = 0; r < NC; ++r) M = fmaxf(M, cl.map_shared_rank(psm, r)[(size_t)qi * PST + D]);
-    float L = 0.f, Ov = 0.f;
+    for (int r = 0; r < NC; ++r) M = fmaxf(M, mw[i * kMaxNC + r]);
+    float L = 0.f;
     for (int r = 0; r < NC; ++r) {
-      const float* pr = cl.map_shared_rank(psm, r) + (size_t)qi * PST;
-      const float mr = pr[D];
+      const float mr = mw[i * kMaxNC + r];
       const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
-      L = fmaf(pr[D + 1], w, L);
-      Ov = fmaf(pr[e], w, Ov);
+      mw[i * kMaxNC + r] = w;
+      L = fmaf(lw[i * kMaxNC + r], w, L);
     }
-    const int qv = qv0 + qi;
+    Ls[i] = L;
+  }
+  __syncthreads();
+  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out);
+  for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
+    const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
+    float4 v[kMaxNC];
+#pragma unroll
+    for (int r = 0; r < kMaxNC; ++r)
+      if (r < NC) v[r] = *reinterpret_cast<const float4*>(cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST + e4);
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxNC; ++r)
+      if (r < NC) {
+        const float w = mw[i * kMaxNC + r];
+        o0 = fmaf(v[r].x, w, o0);
+        o1 = fmaf(v[r].y, w, o1);
+        o2 = fmaf(v[r].z, w, o2);
+        o3 = fmaf(v[r].w, w, o3);
+      }
+    const float L = Ls[i];
+    const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
-    outp[((size_t)s * rows + row) * QD + (size_t)head * D + e] = __float2bfloat16_rn(L > 0.f ? Ov / L : 0.f);
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
+    dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
+    dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
   }
   cl.sync();  // peers keep their shared memory until every rank has read it
 }
@@ -561,7 +638,11 @@ __global__ void __launch_bounds__(kClusterWarps * 32) attn_cluster_kernel(const 
 
 namespace {
 
-size_t cluster_smem(int d) { return (size_t)kClQT * d * 2 + 4 * (size_t)kMmaCH * d * 2; }
+size_t cluster_smem(int d) {
+  const size_t kv = 4 * (size_t)kMmaCH * d * 2, q = (size_t)kClQT * d * 2;
+  const size_t parts = 4 * (size_t)kClQT * (d + 4) * sizeof(float);
+  return (kv + q > parts ? kv + q : parts) + 64 + 1024;
+}
 
 template <int D>
 cudaLaunchConfig_t cluster_cfg(int nc, dim3 grid, cudaStream_t st, cudaLaunchAttribute* at) {
@@ -607,7 +688,7 @@ int clusters_resident(int nc) {
   return cache[dev][nc];
 }
 
-// Cluster width: the widest (<= 16) for which two clusters per (sequence,
+// Cluster width: the widest (<= 16) for which one cluster per (sequence,
 // kv head) all run at once, at least 8.  Depends on the sequence and head
 // counts and the device, never on the row count, so decode (1 row) and
 // verification (a block) of one batch use the same width and per-row order.
@@ -625,10 +706,24 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv * 2);
+  AttnTma p;
+  memset(&p, 0, sizeof(p));
+  p.a = a;
+  const uint64_t crow = (uint64_t)a.n_seqs * a.nkv * a.cap;
+  if (!make_tmap_bf16(&p.kc, a.kc, D, crow, kMmaCH) || !make_tmap_bf16(&p.vc, a.vc, D, crow, kMmaCH))
+    return cudaErrorInvalidValue;
+  if (a.mode == DFLASH_ATTN_BLOCK_BIDIR) {
+    const uint64_t brow = (uint64_t)a.n_seqs * a.nkv * a.rows;
+    if (!make_tmap_bf16(&p.kb, a.kb, D, brow, kMmaCH) || !make_tmap_bf16(&p.vb, a.vb, D, brow, kMmaCH))
+      return cudaErrorInvalidValue;
+  } else {
+    p.kb = p.kc;
+    p.vb = p.vc;
+  }
+  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv);
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
-  return cudaLaunchKernelEx(&cfg, k, a, n_qt);
+  return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 
 }  // namespace

@@ -7,9 +7,8 @@
 // token rows are the B operand (N = BN in 16..256); at small batch the one
 // bf16 weight stream is the whole HBM traffic.  One CTA per SM (its shared
 // memory ring is sized so no second CTA fits).  The
-// (tile, 64-wide k-block) space is cut into G equal contiguous runs, one per
-// CTA (balanced to one k-block); a run's piece inside one tile accumulates in
-// TMEM.  Roles per CTA: warp 0 streams W and X boxes with TMA (128-byte
+// (tile, 64-wide k-block) space is cut into contiguous runs, one per CTA; a
+// run's piece inside one tile accumulates in TMEM.  Roles per CTA: warp 0 streams W and X boxes with TMA (128-byte
 // swizzle) through a STAGES-deep mbarrier ring, warp 1 allocates TMEM and one
 // lane issues tcgen05.mma into one of two TMEM accumulators, warps 2-5 drain
 // the other accumulator with tcgen05.ld, so a piece's epilogue overlaps the
@@ -26,6 +25,7 @@
 #include "internal.h"
 #include "launch.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace dfl {
 
@@ -66,6 +66,7 @@ struct TcCfg {
   static_assert(SMEM > 117 * 1024, "a second CTA must not fit on the SM");
 };
 
+// Run c of the G equal contiguous runs of the (tile, k-block) line [0, T).
 __host__ __device__ __forceinline__ long long run_start(long long T, int G, int c) { return (T * c) / G; }
 
 __device__ __forceinline__ int run_of(long long p, long long T, int G) {
@@ -119,10 +120,33 @@ __device__ __forceinline__ TcLocal tc_local(const TcParams& p) {
 
 __device__ __forceinline__ bool row_used(const TcLocal& L, int m) { return L.hmode == 1 || (m % L.hblock) != 0; }
 
+// Output unit of this thread's accumulator row r in tile t: the output
+// column (store / residual kinds) or the RoPE / SwiGLU pair unit, whose
+// partner row lives in another warp.  False for pair partners (r % blk >= half).
+__device__ __forceinline__ bool tc_unit(const TcLocal& L, int t, int r, int& unit) {
+  const int tile = t % L.tps;
+  if (L.kind == EPI_STORE || L.kind == EPI_RESID) {
+    unit = tile * 128 + r;
+    return true;
+  }
+  const int half = (L.kind == EPI_SWIGLU) ? 64 : L.d / 2;
+  const int blk = (L.kind == EPI_SWIGLU) ? 128 : L.d;
+  if ((r % blk) >= half) return false;
+  if (L.kind == EPI_SWIGLU) {
+    unit = tile * 64 + r;
+  } else {
+    const int rr = tile * 128 + r;
+    unit = (rr / L.d) * half + rr % L.d;
+  }
+  return true;
+}
+
 // Final epilogue of 16 accumulator columns [c0, c0+16) of tile t for the
 // weight row r of this thread (128 epilogue threads, uniform control flow).
+// rw / old hold the epilogue's loads for columns 0..15, issued while the
+// accumulator was being computed; later column groups load here.
 __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int t, int c0, int r, int et,
-                                            float (&v)[16], float* xch) {
+                                            float (&v)[16], float* xch, const EpiRows& rw, const float (&old)[16]) {
   const int M = L.M;
   if (L.mode == TC_HEAD) {
     const int vrow = t * 128 + r;
@@ -165,30 +189,37 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
     if (g8 == 0 && m < M) L.tops[(size_t)t * M + m] = tp;
     return;
   }
-  const int tile = t % L.tps;
+  int unit = 0;
+  const bool works = tc_unit(L, t, r, unit);
   if (L.kind == EPI_STORE || L.kind == EPI_RESID) {
-    epi_single16(e, tile * 128 + r, c0, M, v);
+    if (c0 == 0) {
+      epi_single16(e, unit, c0, v, rw, old);
+    } else {
+      EpiRows rw2;
+      float old2[16];
+      epi_preload_rows(e, unit, c0, M, rw2);
+      epi_preload_tile(e, unit, c0, rw2, old2);
+      epi_single16(e, unit, c0, v, rw2, old2);
+    }
     return;
   }
   // pair epilogues: partner row r + half lives in another warp
   const int half = (L.kind == EPI_SWIGLU) ? 64 : L.d / 2;
-  const int blk = (L.kind == EPI_SWIGLU) ? 128 : L.d;
   tc::named_bar(1, 128);
 #pragma unroll
   for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
   tc::named_bar(1, 128);
-  if ((r % blk) < half) {
-    int u;
-    if (L.kind == EPI_SWIGLU) {
-      u = tile * 64 + r;
-    } else {
-      const int rr = tile * 128 + r;
-      u = (rr / L.d) * half + rr % L.d;
-    }
+  if (works) {
     float w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = xch[j * 128 + r + half];
-    epi_pair16<__nv_bfloat16>(e, u, c0, M, v, w);
+    if (c0 == 0) {
+      epi_pair16<__nv_bfloat16>(e, unit, c0, v, w, rw);
+    } else {
+      EpiRows rw2;
+      epi_preload_rows(e, unit, c0, M, rw2);
+      epi_pair16<__nv_bfloat16>(e, unit, c0, v, w, rw2);
+    }
   }
 }
 
@@ -350,6 +381,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     int k = 0;
     int seg_built = -1;
     Epi e;
+    EpiRows rows;  // columns 0..15: the same for every tile of the run
+    float old[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = 0.f;
+    rows.live = 0u;
+    if (L.mode == TC_GEMM && p0 < p1) {
+      // Nothing loaded here is written before this run's pieces are added:
+      // a tile's outputs are written once, by the piece completing its k range.
+      const int t = (int)(p0 / nkb);
+      seg_built = t / L.tps;
+      e = make_epi(p.g, seg_built);
+      int unit = 0;
+      if (tc_unit(L, t, r, unit)) {
+        epi_preload_rows(e, unit, 0, L.M, rows);
+        epi_preload_tile(e, unit, 0, rows, old);
+      }
+    }
     while (pos < p1) {
       const int t = (int)(pos / nkb);
       const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
@@ -364,12 +412,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       tc::named_bar(1, 128);
       if (*abort) break;  // uniform: read after the barrier
       tc::tc_fence_after();
+      // the next piece's per-tile loads go out before this piece's stores
+      float old_next[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) old_next[j] = 0.f;
+      if (L.mode == TC_GEMM && end < p1) {
+        const int t2 = (int)(end / nkb);
+        const Epi e2 = (t2 / L.tps != seg_built) ? make_epi(p.g, t2 / L.tps) : e;
+        int unit2 = 0;
+        if (tc_unit(L, t2, r, unit2)) epi_preload_tile(e2, unit2, 0, rows, old_next);
+      }
       const uint32_t trow = tmem + (uint32_t)(b * Cfg::ACC) + ((uint32_t)(q4 * 32) << 16);
       if (whole) {
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
-          final_chunk(L, e, t, c0, r, et, v, xch);
+          final_chunk(L, e, t, c0, r, et, v, xch, rows, old);
         }
         tc::tc_fence_before();
         tc::named_bar(1, 128);
@@ -384,20 +442,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
           for (int j = 0; j < 16; ++j) dst0[(size_t)(c0 + j) * 128] = v[j];
         }
         tc::tc_fence_before();
-        tc::named_bar(1, 128);
-        if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
-        __threadfence();
+        // bar.sync orders every epilogue thread's partial stores before the
+        // release of the one thread that publishes the piece; its acquire
+        // (and the barrier after it) orders the fixup's loads after the
+        // other pieces' stores.
         tc::named_bar(1, 128);
         if (et == 0) {
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
           uint32_t* ctr = L.counters + kCtrGemm + t;
           const uint32_t add = (uint32_t)(end - pos);
-          const uint32_t old = atomicAdd(ctr, add);
-          *s_flag = (old + add == (uint32_t)nkb);
+          uint32_t old_ctr;
+          asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old_ctr) : "l"(ctr), "r"(add) : "memory");
+          *s_flag = (old_ctr + add == (uint32_t)nkb);
           if (*s_flag) *ctr = 0u;
         }
         tc::named_bar(1, 128);
         if (*s_flag) {
-          __threadfence();
           const int first = run_of(tbeg, L.T, L.G) + t;
           const int last = run_of(tend - 1, L.T, L.G) + t;
           for (int c0 = 0; c0 < ncol; c0 += 16) {
@@ -419,11 +479,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
                 for (int j = 0; j < 16; ++j)
                   if (sb + q <= last) v[j] += pv[q][j];
             }
-            final_chunk(L, e, t, c0, r, et, v, xch);
+            final_chunk(L, e, t, c0, r, et, v, xch, rows, old);
           }
         }
         tc::named_bar(1, 128);  // s_flag is rewritten by the next piece
       }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) old[j] = old_next[j];
       pos = end;
       ++k;
     }
@@ -441,30 +503,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// Row-major bf16 [rows][inner] tensor, box = 64 (inner) x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_bf16(m, base, inner, rows, box_rows);
 }
 
 int pick_bn(int M) {

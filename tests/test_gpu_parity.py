@@ -249,3 +249,35 @@ def test_perfect_drafter_gpu():
         assert k == w.block - 1
         got.extend(eng.out_tokens[0, :k + 1].cpu().tolist())
     np.testing.assert_array_equal(np.array(got), greedy[:len(got)].numpy())
+
+
+@pytest.mark.parametrize("kind", ["causal", "bidir"])
+def test_rows_independent_of_batch(kind):
+    """A token row's layer output does not depend on the other rows of the
+    launch: sequence 0 alone (16 rows: partial tiles reduced through
+    distributed shared memory) and next to four more sequences (80 rows:
+    the same pieces reduced through global memory) give bit-identical hidden
+    states and K/V, the invariant that lets verification reproduce greedy
+    decoding exactly."""
+    w = small("bf16", d=64, block=16)
+    outs = []
+    for S in (1, 5):
+        eng, om, _ = G.setup(w, S=S, cap=128)
+        rows = 16
+        g = torch.Generator().manual_seed(3)
+        h0 = torch.randn(5 * rows, w.target.hidden, generator=g)
+        kc = torch.randn(5, *eng.caches.tk[1].shape[1:], generator=g).to(eng.caches.tk[1].dtype)
+        vc = torch.randn(5, *eng.caches.tv[1].shape[1:], generator=g).to(eng.caches.tv[1].dtype)
+        eng.caches.tk[1].copy_(kc[:S].cuda())
+        eng.caches.tv[1].copy_(vc[:S].cuda())
+        eng.base_pos.copy_(torch.tensor([40, 7, 90, 3, 64][:S], dtype=torch.int32))
+        eng.h[:S * rows].copy_(h0[:S * rows].cuda())
+        a = eng.target_layer_args(1, rows, eng.h)
+        if kind == "bidir":
+            a.attn_mode = D.DFLASH_ATTN_BLOCK_BIDIR
+        D.dflash_decoder_layer_forward(a, eng.ws_ptr, eng.ws_bytes)
+        torch.cuda.synchronize()
+        assert eng.status() == D.DFLASH_OK
+        outs.append((eng.h[:rows].clone().cpu(), eng.caches.tk[1][0].clone().cpu(), eng.caches.tv[1][0].clone().cpu()))
+    for a_, b_ in zip(outs[0], outs[1]):
+        assert torch.equal(a_, b_)
