@@ -340,6 +340,8 @@ struct DraftScratch {
   void* xf;
   void* hpart;
   int32_t* cand;
+  float* proj;     // path selector projections (path_topk > 0)
+  float* logits;   // draft logit rows when the CUDA-core head feeds the top-k merge
 };
 
 LayerShape draft_layer_shape(const dflash_draft_args* a, int j) {
@@ -375,8 +377,17 @@ size_t carve_draft(Bump& b, const dflash_draft_args* a, int sms, DraftScratch& s
   s.xf = b.take(M * d.hidden * elem_size(d.dtype));
   HeadDesc hd = head_shape(d, a->n_seqs, a->block, a->path_topk > 0 ? 2 : 0);
   hd.topk = a->path_topk;
+  hd.x = s.xf;
   s.hpart = b.take(head_workspace(hd, sms));
   s.cand = static_cast<int32_t*>(b.take((size_t)a->n_seqs * a->block * 16 * sizeof(int32_t)));
+  s.proj = nullptr;
+  s.logits = nullptr;
+  if (a->path_topk > 0) {
+    s.proj = static_cast<float*>(
+        b.take(path_proj_floats(a->n_seqs, a->block, a->path_topk, a->path_rank) * sizeof(float)));
+    if (!head_tc_supported(hd) && a->logits == nullptr)
+      s.logits = static_cast<float*>(b.take((size_t)a->n_seqs * (a->block - 1) * d.vocab * sizeof(float)));
+  }
   return b.off;
 }
 
@@ -419,7 +430,10 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status) {
   DF_CUDA(cudaStreamSynchronize(st));
   DF_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st));
   DF_CUDA(cudaStreamSynchronize(st));
-  *host_status = (v & ST_NUMERIC) ? DFLASH_ERR_NUMERIC : (v & ST_TIMEOUT) ? DFLASH_ERR_TIMEOUT : DFLASH_OK;
+  *host_status = (v & ST_NUMERIC)   ? DFLASH_ERR_NUMERIC
+                 : (v & ST_TIMEOUT) ? DFLASH_ERR_TIMEOUT
+                 : (v & ST_RANGE)   ? DFLASH_ERR_INVALID_ARG
+                                    : DFLASH_OK;
   if (*host_status != DFLASH_OK) fail(*host_status, "device status word 0x%x", v);
   return DFLASH_OK;
 }
@@ -596,11 +610,11 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
   DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
   DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
-  if (a->path_topk > 0)
-    return fail(DFLASH_ERR_UNSUPPORTED, "%s: the path selector inside the draft is not available yet", who);
-  if (a->path_topk > 0)
+  if (a->path_topk > 0) {
     DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
              "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);
+    DF_CHECK(d.hidden % 8 == 0, "%s: the path selector needs hidden %% 8 == 0", who);
+  }
   for (int j = 0; j < a->n_layers; ++j) {
     rc = check_weights(a->layers[j], who);
     if (rc) return rc;
@@ -636,12 +650,16 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   h.w = a->lm_head;
   h.drafts_out = a->drafts;
   h.cand_out = s.cand;
-  h.logits = a->logits;
+  h.logits = a->logits ? a->logits : s.logits;
   h.partials = static_cast<float*>(s.hpart);
   h.counters = c.counters;
   h.status = c.status;
   DF_LAUNCH(st, TF_HEAD, head_bytes(h), launch_head(h, sms, st));
   if (a->path_topk > 0) {
+    // the rows' top-k candidates (ranked by draft logit), then the walk
+    int n_tiles = 0;
+    const void* tl = head_tc_supported(h) ? head_tc_tlist(h, sms, &n_tiles) : nullptr;
+    DF_LAUNCH(st, TF_PATH, 0, launch_topk_merge(h, tl, n_tiles, st));
     PathDesc p;
     memset(&p, 0, sizeof(p));
     p.dtype = d.dtype;
@@ -650,12 +668,15 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
     p.topk = a->path_topk;
     p.rank = a->path_rank;
     p.H = d.hidden;
+    p.V = d.vocab;
     p.embed = a->embed;
     p.u = a->path_u;
     p.v = a->path_v;
     p.anchor = a->anchor;
     p.cand = s.cand;
     p.path = a->drafts;
+    p.proj = s.proj;
+    p.status = c.status;
     DF_LAUNCH(st, TF_PATH, 0, launch_path_select(p, st));
   }
   return DFLASH_OK;
@@ -715,6 +736,10 @@ int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
 
 // ----------------------------------------------------------- path select
 
+static size_t path_ws(const dflash_path_args* a) {
+  return kReservedBytes + path_proj_floats(a->n_seqs, a->block, a->topk, a->rank) * sizeof(float);
+}
+
 int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
   const char* who = "dflash_path_select";
   DF_CHECK(a != nullptr, "%s: NULL args", who);
@@ -723,8 +748,10 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   DF_CHECK(a->embed && a->path_u && a->path_v && a->anchor && a->cand && a->path, "%s: NULL pointer", who);
   DF_CHECK(a->n_seqs > 0 && a->block >= 2 && a->topk > 0 && a->topk <= 16 && a->rank > 0 && a->rank <= 256,
            "%s: need n_seqs > 0, block >= 2, 0 < topk <= 16, 0 < rank <= 256", who);
-  rc = check_ws(ws, ws_bytes, kReservedBytes, who);
+  DF_CHECK(a->dims.hidden % 8 == 0, "%s: hidden %% 8 == 0 required", who);
+  rc = check_ws(ws, ws_bytes, path_ws(a), who);
   if (rc) return rc;
+  Ctx c = header(ws);
   PathDesc p;
   memset(&p, 0, sizeof(p));
   p.dtype = a->dims.dtype;
@@ -737,9 +764,12 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   p.u = a->path_u;
   p.v = a->path_v;
   p.anchor = a->anchor;
+  p.V = a->dims.vocab;
   p.cand = a->cand;
   p.path = a->path;
   p.margin = a->margin;
+  p.proj = reinterpret_cast<float*>(static_cast<char*>(ws) + kReservedBytes);
+  p.status = c.status;
   DF_LAUNCH((cudaStream_t)stream, TF_PATH, 0, launch_path_select(p, (cudaStream_t)stream));
   return DFLASH_OK;
 }
@@ -751,8 +781,9 @@ size_t dflash_workspace_bytes(int32_t op, const void* args) {
   const int sms = num_sms();
   switch (op) {
     case DFLASH_OP_EMBED:
-    case DFLASH_OP_PATH:
       return kReservedBytes;
+    case DFLASH_OP_PATH:
+      return path_ws(static_cast<const dflash_path_args*>(args));
     case DFLASH_OP_LAYER:
       return layer_ws(static_cast<const dflash_layer_args*>(args), sms);
     case DFLASH_OP_FUSE: {

@@ -12,6 +12,7 @@ namespace dfl {
 enum : uint32_t {
   ST_NUMERIC = 1u,  // NaN reached an argmax
   ST_TIMEOUT = 2u,  // a bounded wait gave up
+  ST_RANGE = 4u,    // a token id read on the device lay outside the vocabulary
 };
 
 // Workspace header: status word + arrival counters of the last-CTA reductions.

@@ -22,6 +22,15 @@ __device__ __forceinline__ bool beats(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// Top-k mode (path selector candidates): per (tile, token row) the k best
+// (logit, index) pairs of the tile, best first (greater logit, then lower
+// index); index INT_MAX marks an empty entry.
+constexpr int kMaxTopK = 16;
+struct Cand {
+  float v;
+  int i;
+};
+
 __device__ __forceinline__ void top2_push(Top2& t, float v, int i, uint32_t* status) {
   if (v != v) {  // NaN never wins; flag it
     raise_status(status, ST_NUMERIC);
@@ -73,6 +82,7 @@ __device__ __forceinline__ Top2 ldcg_top2(const Top2* p) {
 __device__ __forceinline__ void head_finish(const HeadDesc& h, int n_arrivals, int n_parts, const Top2* part,
                                             int* s_last) {
   __shared__ int s_arg[kHeadMaxM];
+  if (h.mode == 2) return;  // top-k mode: candidates are merged by their own kernel
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {

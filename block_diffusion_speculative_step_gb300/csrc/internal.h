@@ -96,15 +96,22 @@ struct HeadDesc {
 
 struct PathDesc {
   int dtype;
-  int n_seqs, block, topk, rank, H;
+  int n_seqs, block, topk, rank, H, V;
   const void* embed;
   const void* u;
   const void* v;
   const int32_t* anchor;
-  const int32_t* cand;
+  const int32_t* cand;        // [S][block-1][topk]
   int32_t* path;
   float* margin;
+  float* proj;                // workspace [S][1 + (block-1)*topk][2*rank]: U e, V e per token slot
+  uint32_t* status;
 };
+
+// Path-selector projection scratch (floats) for S sequences.
+inline size_t path_proj_floats(int S, int block, int topk, int rank) {
+  return (size_t)S * (1 + (size_t)(block - 1) * topk) * 2 * rank;
+}
 
 // elementwise
 cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaStream_t st);
@@ -140,5 +147,11 @@ cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st);
 
 // path selector
 cudaError_t launch_path_select(const PathDesc& p, cudaStream_t st);
+// Top-k mode of the draft head: the per-tile lists of the tensor-core head
+// (tlist, n_tiles), or the logit rows h.logits of the CUDA-core head (tlist
+// NULL), merged into h.cand_out [S][block-1][topk].
+cudaError_t launch_topk_merge(const HeadDesc& h, const void* tlist, int n_tiles, cudaStream_t st);
+// The tensor-core head's per-tile top-k lists inside h.partials.
+const void* head_tc_tlist(const HeadDesc& h, int num_sms, int* n_tiles);
 
 }  // namespace dfl

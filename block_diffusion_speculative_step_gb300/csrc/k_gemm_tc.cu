@@ -48,6 +48,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int M;          // token rows
   float* part;    // partial slots [n_tiles + G][BN][128]
   Top2* tops;     // LM head: per-tile triples [n_tiles][M]
+  Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
   uint32_t* counters;
   uint32_t* status;
 };
@@ -86,9 +87,10 @@ __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort
 struct TcLocal {
   int mode, M, tps, nkb, G, n_tiles, kind, d, inter, row0;
   long long T;
-  int V, hmode, hblock;
+  int V, hmode, hblock, topk;
   float* logits;
   Top2* tops;
+  Cand* tlist;
   float* part;
   uint32_t* counters;
   uint32_t* status;
@@ -110,8 +112,10 @@ __device__ __forceinline__ TcLocal tc_local(const TcParams& p) {
   L.V = p.h.V;
   L.hmode = p.h.mode;
   L.hblock = p.h.block;
+  L.topk = p.h.topk;
   L.logits = p.h.logits;
   L.tops = p.tops;
+  L.tlist = p.tlist;
   L.part = p.part;
   L.counters = p.counters;
   L.status = p.status;
@@ -171,6 +175,48 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
     tc::named_bar(1, 128);
     const int jc = et >> 3, g8 = et & 7;  // column jc, rows 16*g8 .. 16*g8+15
     const int m = c0 + jc;
+    if (L.topk > 0) {
+      // k rounds: each of the column's 8 threads offers its best unselected
+      // row; the winner over the 8 (greater logit, then lower index) is taken.
+      const bool used = m < M && row_used(L, m);
+      uint32_t taken = 0u;
+      Cand* out = L.tlist + ((size_t)t * M + m) * L.topk;
+      for (int q = 0; q < L.topk; ++q) {
+        float bv = -INFINITY;
+        int bi = INT_MAX, brr = -1;
+        if (used) {
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const int vi = t * 128 + 16 * g8 + rr;
+            const float x = xch[jc * 128 + 16 * g8 + rr];
+            if (vi >= L.V || ((taken >> rr) & 1u)) continue;
+            if (x != x) {  // NaN never wins; flag it
+              if (q == 0) raise_status(L.status, ST_NUMERIC);
+              continue;
+            }
+            if (beats(x, vi, bv, bi)) {
+              bv = x;
+              bi = vi;
+              brr = rr;
+            }
+          }
+        }
+        float rv = bv;
+        int ri = bi;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, rv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, ri, o);
+          if (beats(ov, oi, rv, ri)) {
+            rv = ov;
+            ri = oi;
+          }
+        }
+        if (brr >= 0 && bi == ri) taken |= 1u << brr;
+        if (g8 == 0 && used) out[q] = Cand{rv, ri};
+      }
+      return;
+    }
     Top2 tp = top2_empty();
     if (m < M && row_used(L, m)) {
       for (int rr = 16 * g8; rr < 16 * g8 + 16; ++rr) {
@@ -596,10 +642,26 @@ bool head_tc_supported(const HeadDesc& h) {
          (reinterpret_cast<uintptr_t>(h.x) & 15) == 0 && (h.V + 127) / 128 <= 8192;
 }
 
+// Per-tile selections of the LM head: triples, or top-k lists.
+size_t head_sel_bytes(const HeadDesc& h, int n_tiles) {
+  const size_t t2 = (size_t)n_tiles * h.M * sizeof(Top2);
+  const size_t tk = (size_t)n_tiles * h.M * (h.topk > 0 ? h.topk : 0) * sizeof(Cand);
+  return t2 > tk ? t2 : tk;
+}
+
 size_t head_tc_workspace(const HeadDesc& h, int num_sms) {
   const int n_tiles = (h.V + 127) / 128;
   const long long T = (long long)n_tiles * (h.H / 64);
-  return part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(h.M)) + (size_t)n_tiles * h.M * sizeof(Top2) + 256;
+  return ((part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(h.M)) + 255) & ~size_t(255)) +
+         head_sel_bytes(h, n_tiles) + 256;
+}
+
+const void* head_tc_tlist(const HeadDesc& h, int num_sms, int* n_tiles) {
+  const int nt = (h.V + 127) / 128;
+  const long long T = (long long)nt * (h.H / 64);
+  const size_t pb = part_bytes(nt, runs_for(T, num_sms), pick_bn(h.M));
+  *n_tiles = nt;
+  return reinterpret_cast<const char*>(h.partials) + ((pb + 255) & ~size_t(255));
 }
 
 cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st) {
@@ -616,6 +678,7 @@ cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st) {
   const size_t pb = part_bytes(p.n_tiles, p.G, pick_bn(h.M));
   p.part = h.partials;
   p.tops = reinterpret_cast<Top2*>(reinterpret_cast<char*>(h.partials) + ((pb + 255) & ~size_t(255)));
+  p.tlist = reinterpret_cast<Cand*>(p.tops);
   p.counters = h.counters;
   p.status = h.status;
   if (!make_map(&p.wmap[0], h.w, h.H, h.V, 128)) return cudaErrorInvalidValue;

@@ -102,76 +102,202 @@ cudaError_t launch_head(const HeadDesc& h, int num_sms, cudaStream_t st) {
   return launch_head_simt(h, num_sms, st);
 }
 
-// ------------------------------------------------------------ path selector
+// ------------------------------------------------- top-k candidate merge
 
-// One CTA per sequence.  ue = U e_prev, then for each candidate b of row j,
-// score = ue . (V e_b); walk greedily.  Scores are fp32 with fixed-order sums.
-template <typename T>
-__global__ void path_select_kernel(const __grid_constant__ PathDesc p) {
+// Insert (v, i) into a register list of the 16 best pairs, best first.
+__device__ __forceinline__ void cand_insert(float (&lv)[kMaxTopK], int (&li)[kMaxTopK], float v, int i) {
+  if (!beats(v, i, lv[kMaxTopK - 1], li[kMaxTopK - 1])) return;
+  bool done = false;
+#pragma unroll
+  for (int q = kMaxTopK - 1; q > 0; --q) {
+    if (!done) {
+      if (beats(v, i, lv[q - 1], li[q - 1])) {
+        lv[q] = lv[q - 1];
+        li[q] = li[q - 1];
+      } else {
+        lv[q] = v;
+        li[q] = i;
+        done = true;
+      }
+    }
+  }
+  if (!done) {
+    lv[0] = v;
+    li[0] = i;
+  }
+}
+
+// One warp per draft row: every lane keeps the 16 best pairs of its share
+// (tiles lane, lane+32, .. or vocabulary entries), then k rounds take the
+// best list head of the warp.  The order (greater logit, then lower index)
+// is total, so the result does not depend on how the pairs were split.
+__global__ void topk_merge_kernel(const __grid_constant__ HeadDesc h, const Cand* tlist, int n_tiles) {
   pdl_wait();
   pdl_launch_dependents();
-  extern __shared__ float psm[];
-  float* ue = psm;                            // [rank]
-  int* park = reinterpret_cast<int*>(psm + p.rank);  // chosen token of the step
-  float* sc = psm + p.rank + 1;               // [topk]
-  const int s = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int B = h.block;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // s * (B-1) + j - 1
+  if (row >= h.n_seqs * (B - 1)) return;  // whole warp
+  const int m = (row / (B - 1)) * B + row % (B - 1) + 1;
+  float lv[kMaxTopK];
+  int li[kMaxTopK];
+#pragma unroll
+  for (int q = 0; q < kMaxTopK; ++q) {
+    lv[q] = -INFINITY;
+    li[q] = INT_MAX;
+  }
+  if (tlist) {
+    for (int t = lane; t < n_tiles; t += 32) {
+      const Cand* c = tlist + ((size_t)t * h.M + m) * h.topk;
+      for (int q = 0; q < h.topk; ++q) {
+        const float v = __ldcg(&c[q].v);
+        const int i = __ldcg(&c[q].i);
+        if (i == INT_MAX) break;
+        cand_insert(lv, li, v, i);
+      }
+    }
+  } else {
+    const float* lr = h.logits + (size_t)row * h.V;
+    for (int v = lane; v < h.V; v += 32) {
+      const float x = lr[v];
+      if (x != x) {
+        raise_status(h.status, ST_NUMERIC);
+        continue;
+      }
+      cand_insert(lv, li, x, v);
+    }
+  }
+  int32_t* out = h.cand_out + (size_t)row * h.topk;
+  for (int q = 0; q < h.topk; ++q) {
+    float rv = lv[0];
+    int ri = li[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, rv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, ri, o);
+      if (beats(ov, oi, rv, ri)) {
+        rv = ov;
+        ri = oi;
+      }
+    }
+    if (ri != INT_MAX && li[0] == ri) {  // this lane's head was taken
+#pragma unroll
+      for (int z = 0; z < kMaxTopK - 1; ++z) {
+        lv[z] = lv[z + 1];
+        li[z] = li[z + 1];
+      }
+      lv[kMaxTopK - 1] = -INFINITY;
+      li[kMaxTopK - 1] = INT_MAX;
+    }
+    if (lane == 0) out[q] = (ri == INT_MAX) ? 0 : ri;
+  }
+}
+
+cudaError_t launch_topk_merge(const HeadDesc& h, const void* tlist, int n_tiles, cudaStream_t st) {
+  const int rows = h.n_seqs * (h.block - 1);
+  if (rows <= 0) return cudaSuccess;
+  constexpr int kWarps = 4;
+  return launch_pdl(topk_merge_kernel, dim3((rows + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, st, h,
+                    static_cast<const Cand*>(tlist), n_tiles);
+}
+
+// ------------------------------------------------------------ path selector
+//
+// score(a -> b) = (U e_a) . (V e_b).  The projections of the anchor and of
+// every candidate do not depend on the walk, so they are formed first, one
+// CTA per token slot; the walk then needs rank-long dot products only.
+
+constexpr int kPathThreads = 256;
+
+// proj[s][slot][0..R) = U e_tok, [R..2R) = V e_tok; slot 0 is the anchor,
+// slot 1 + j*topk + q is candidate q of draft row j.  Fixed-order sums.
+template <typename T>
+__global__ void __launch_bounds__(kPathThreads) path_proj_kernel(const __grid_constant__ PathDesc p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = blockIdx.y, slot = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const T* E = reinterpret_cast<const T*>(p.embed);
-  const T* U = reinterpret_cast<const T*>(p.u);
-  const T* Vm = reinterpret_cast<const T*>(p.v);
-  int prev = p.anchor[s];
-  for (int j = 0; j < p.block - 1; ++j) {
-    for (int r = warp; r < p.rank; r += nw) {
+  const int nslot = 1 + (p.block - 1) * p.topk, R = p.rank, H = p.H;
+  int tok = slot == 0 ? p.anchor[s] : p.cand[(size_t)s * (p.block - 1) * p.topk + (slot - 1)];
+  float* dst = p.proj + ((size_t)s * nslot + slot) * 2 * R;
+  if (tok < 0 || tok >= p.V) {  // never read outside the embedding table
+    if (threadIdx.x == 0) raise_status(p.status, ST_RANGE);
+    for (int o = threadIdx.x; o < 2 * R; o += blockDim.x) dst[o] = 0.f;
+    return;
+  }
+  const T* e = reinterpret_cast<const T*>(p.embed) + (size_t)tok * H;
+  for (int o = warp; o < 2 * R; o += nw) {
+    const T* w = reinterpret_cast<const T*>(o < R ? p.u : p.v) + (size_t)(o < R ? o : o - R) * H;
+    float acc = 0.f;
+    for (int k = lane * 8; k < H; k += 256) {
+      float fw[8], fe[8];
+      load8<T>(w + k, fw);
+      load8<T>(e + k, fe);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(fw[i], fe[i], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) dst[o] = acc;
+  }
+}
+
+// One warp per sequence: lane q scores candidate q of row j from p_{j-1};
+// the greatest score wins, the lower rank on ties (the candidates are ranked
+// by draft logit).
+__global__ void path_walk_kernel(const __grid_constant__ PathDesc p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = blockIdx.x, lane = threadIdx.x & 31;
+  const int K = p.topk, R = p.rank, B = p.block, nslot = 1 + (B - 1) * K;
+  const float* base = p.proj + (size_t)s * nslot * 2 * R;
+  int prev = 0;  // slot of p_{j-1}
+  for (int j = 0; j < B - 1; ++j) {
+    const float* ue = base + (size_t)prev * 2 * R;
+    float sc = -INFINITY;
+    if (lane < K) {
+      const float* ve = base + (size_t)(1 + j * K + lane) * 2 * R + R;
       float acc = 0.f;
-      for (int k = lane; k < p.H; k += 32) acc = fmaf(to_f<T>(U[(size_t)r * p.H + k]), to_f<T>(E[(size_t)prev * p.H + k]), acc);
-      acc = warp_sum(acc);
-      if (lane == 0) ue[r] = acc;
-    }
-    __syncthreads();
-    const int32_t* cj = p.cand + ((size_t)s * (p.block - 1) + j) * p.topk;
-    for (int q = warp; q < p.topk; q += nw) {
-      const int b = cj[q];
-      float tot = 0.f;
-      for (int r = 0; r < p.rank; ++r) {
-        float acc = 0.f;
-        for (int k = lane; k < p.H; k += 32)
-          acc = fmaf(to_f<T>(Vm[(size_t)r * p.H + k]), to_f<T>(E[(size_t)b * p.H + k]), acc);
-        acc = warp_sum(acc);
-        tot = fmaf(ue[r], acc, tot);
+      for (int r = 0; r < R; ++r) acc = fmaf(ue[r], ve[r], acc);
+      if (acc != acc) {
+        raise_status(p.status, ST_NUMERIC);
+        acc = -INFINITY;
       }
-      if (lane == 0) sc[q] = tot;
+      sc = acc;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int bi = 0;
-      float best = sc[0], second = -INFINITY;
-      for (int q = 1; q < p.topk; ++q) {
-        if (sc[q] > best) {
-          second = best;
-          best = sc[q];
-          bi = q;
-        } else if (sc[q] > second) {
-          second = sc[q];
-        }
+    float bv = sc;
+    int bq = lane < K ? lane : 64;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oq = __shfl_xor_sync(0xffffffffu, bq, o);
+      if (ov > bv || (ov == bv && oq < bq)) {
+        bv = ov;
+        bq = oq;
       }
-      p.path[(size_t)s * (p.block - 1) + j] = cj[bi];
-      if (p.margin) p.margin[(size_t)s * (p.block - 1) + j] = best - second;
-      *park = cj[bi];
     }
-    __syncthreads();
-    prev = *park;
-    __syncthreads();
+    bq = __shfl_sync(0xffffffffu, bq, 0);
+    bq = bq < K ? bq : 0;
+    float sv = (lane < K && lane != bq) ? sc : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, o));
+    if (lane == 0) {
+      p.path[(size_t)s * (B - 1) + j] = p.cand[((size_t)s * (B - 1) + j) * K + bq];
+      if (p.margin) p.margin[(size_t)s * (B - 1) + j] = bv - sv;
+    }
+    prev = 1 + j * K + bq;
   }
 }
 
 cudaError_t launch_path_select(const PathDesc& p, cudaStream_t st) {
   if (p.n_seqs == 0 || p.block < 2) return cudaSuccess;
-  size_t smem = (size_t)(p.rank + 1 + p.topk) * sizeof(float);
+  const dim3 grid(1 + (p.block - 1) * p.topk, p.n_seqs);
+  cudaError_t e;
   if (p.dtype == DFLASH_BF16)
-    return launch_pdl(path_select_kernel<__nv_bfloat16>, dim3(p.n_seqs), dim3(256), smem, st, p);
+    e = launch_pdl(path_proj_kernel<__nv_bfloat16>, grid, dim3(kPathThreads), 0, st, p);
   else
-    return launch_pdl(path_select_kernel<float>, dim3(p.n_seqs), dim3(256), smem, st, p);
-  return cudaGetLastError();
+    e = launch_pdl(path_proj_kernel<float>, grid, dim3(kPathThreads), 0, st, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(path_walk_kernel, dim3(p.n_seqs), dim3(32), 0, st, p);
 }
 
 }  // namespace dfl

@@ -281,3 +281,94 @@ def test_rows_independent_of_batch(kind):
         outs.append((eng.h[:rows].clone().cpu(), eng.caches.tk[1][0].clone().cpu(), eng.caches.tv[1][0].clone().cpu()))
     for a_, b_ in zip(outs[0], outs[1]):
         assert torch.equal(a_, b_)
+
+
+def _path_factors(eng, w, seed, dtype):
+    """O(1)-scale selector factors, so scores are O(1) and a fixed near-tie
+    threshold is meaningful; installed on the device, returned for the oracle."""
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    U = torch.randn(w.path_rank, w.draft.hidden, generator=g).to(dt)
+    Vm = torch.randn(w.path_rank, w.draft.hidden, generator=g).to(dt)
+    eng.m["path_u"].copy_(U.cuda())
+    eng.m["path_v"].copy_(Vm.cuda())
+    return synth.to_numpy(U), synth.to_numpy(Vm)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_draft_path_selector(dtype):
+    """The draft with the DFlash 2 path selector: top-16 candidates per draft
+    row from the fused LM head (tensor-core head in bf16, CUDA-core head in
+    fp32), then the greedy rank-64 walk.  The oracle walks the GPU's own draft
+    logits, so its candidate lists are the exact top-16 of the same values;
+    paths must agree step by step up to the first reported score near-tie."""
+    w = small(dtype, V=1000, block=10, topk=16, rank=64)
+    S, B = 2, w.block
+    eng, om, _ = G.setup(w, S=S, cap=96)
+    Un, Vn = _path_factors(eng, w, 7, dtype)
+    eng.base_pos.copy_(torch.tensor([9, 40], dtype=torch.int32))
+    eng.anchor.copy_(torch.tensor([17, 400], dtype=torch.int32))
+    for j in range(w.draft.layers):
+        rand_cache(eng, eng.caches.dk[j], eng.caches.dv[j], S, eng.dcap, 10 + j, om.draft.cfg)
+    logits = torch.zeros(S * (B - 1), w.vocab, device="cuda")
+    eng.draft(logits)
+    torch.cuda.synchronize()
+    assert eng.status() == D.DFLASH_OK
+    gp = eng.drafts.cpu().numpy()
+    gl = logits.cpu().numpy().reshape(S, B - 1, w.vocab)
+    compared = 0
+    for s in range(S):
+        path, cand, mg = O.path_select(om.draft.cfg, gl[s], om.E, Un, Vn, int(eng.anchor[s]), topk=16)
+        for j in range(B - 1):
+            if mg[j] < 1e-4:  # near-tie: the walk may branch, later steps differ legitimately
+                break
+            assert gp[s, j] == path[j], f"seq {s} step {j}: gpu {gp[s, j]} oracle {path[j]} (margin {mg[j]:.3g})"
+            compared += 1
+    assert compared >= S * (B - 1) // 2
+
+
+def test_path_select_entry_point():
+    """dflash_path_select on caller-given candidate lists: zero factors make
+    every score tie, so the path is each row's rank-0 candidate; random
+    factors match the oracle walk over the same lists."""
+    w = small("bf16", V=600, block=6, topk=8, rank=32)
+    S, B, K, R = 3, w.block, 8, 32
+    eng, om, _ = G.setup(w, S=S, cap=64)
+    rng = np.random.default_rng(12)
+    cand = np.stack([np.stack([rng.choice(w.vocab, K, replace=False) for _ in range(B - 1)]) for _ in range(S)])
+    cand_d = torch.from_numpy(cand.astype(np.int32)).cuda()
+    anchor = torch.tensor([5, 77, 599], dtype=torch.int32, device="cuda")
+    path = torch.full((S, B - 1), -1, dtype=torch.int32, device="cuda")
+    margin = torch.zeros(S, B - 1, device="cuda")
+    for zero in (True, False):
+        if zero:
+            eng.m["path_u"].zero_()
+            eng.m["path_v"].zero_()
+            Un = Vn = np.zeros((R, w.draft.hidden), dtype=np.uint16)
+        else:
+            Un, Vn = _path_factors(eng, w, 8, "bf16")
+        a = D.dflash_path_args()
+        a.dims = eng.ddims
+        a.n_seqs, a.block, a.topk, a.rank = S, B, K, R
+        a.embed, a.path_u, a.path_v = eng.m["embed"].data_ptr(), eng.m["path_u"].data_ptr(), eng.m["path_v"].data_ptr()
+        a.anchor, a.cand, a.path, a.margin = anchor.data_ptr(), cand_d.data_ptr(), path.data_ptr(), margin.data_ptr()
+        need = D.dflash_workspace_bytes(D.DFLASH_OP_PATH, a)
+        assert need <= eng.ws_bytes
+        D.dflash_path_select(a, eng.ws_ptr, eng.ws_bytes)
+        torch.cuda.synchronize()
+        assert eng.status() == D.DFLASH_OK
+        gp = path.cpu().numpy()
+        if zero:
+            np.testing.assert_array_equal(gp, cand[:, :, 0])
+            continue
+        for s in range(S):
+            # logits whose top-K in rank order are exactly the given lists
+            lg = np.full((B - 1, w.vocab), -100.0, dtype=np.float32)
+            for j in range(B - 1):
+                lg[j, cand[s, j]] = np.arange(K, 0, -1, dtype=np.float32)
+            op, oc, mg = O.path_select(om.draft.cfg, lg, om.E, Un, Vn, int(anchor[s]), topk=K)
+            np.testing.assert_array_equal(oc, cand[s])
+            for j in range(B - 1):
+                if mg[j] < 1e-4:
+                    break
+                assert gp[s, j] == op[j]
