@@ -320,6 +320,9 @@ double head_bytes(const HeadDesc& h) {
   return (double)h.V * h.H * es + (double)h.M * h.H * es;
 }
 
+// Sequences per LM-head launch: whole sequences, at most 256 token rows.
+int head_seqs_per_launch(int block) { return block >= 256 ? 1 : 256 / block; }
+
 HeadDesc head_shape(const dflash_dims& d, int S, int block, int mode) {
   HeadDesc h;
   memset(&h, 0, sizeof(h));
@@ -385,10 +388,52 @@ size_t carve_draft(Bump& b, const dflash_draft_args* a, int sms, DraftScratch& s
   if (a->path_topk > 0) {
     s.proj = static_cast<float*>(
         b.take(path_proj_floats(a->n_seqs, a->block, a->path_topk, a->path_rank) * sizeof(float)));
-    if (!head_tc_supported(hd) && a->logits == nullptr)
+    HeadDesc one = hd;  // the shape of one head launch
+    one.n_seqs = std::min(a->n_seqs, head_seqs_per_launch(a->block));
+    one.M = one.n_seqs * a->block;
+    if (!head_tc_supported(one) && a->logits == nullptr)
       s.logits = static_cast<float*>(b.take((size_t)a->n_seqs * (a->block - 1) * d.vocab * sizeof(float)));
   }
   return b.off;
+}
+
+// Sequences [s0, s0 + n) of an LM-head problem.
+HeadDesc head_slice(const HeadDesc& h, int s0, int n) {
+  HeadDesc c = h;
+  const int B = h.block, Bd = B - 1;
+  const bool verify = h.mode == 1;
+  c.n_seqs = n;
+  c.M = n * B;
+  c.x = static_cast<const char*>(h.x) + (size_t)s0 * B * h.H * elem_size(h.dtype);
+  if (h.drafts) c.drafts = h.drafts + (size_t)s0 * Bd;
+  if (h.drafts_out) c.drafts_out = h.drafts_out + (size_t)s0 * Bd;
+  if (h.argmax) c.argmax = h.argmax + (size_t)s0 * B;
+  if (h.margin) c.margin = h.margin + (size_t)s0 * (verify ? B : Bd);
+  if (h.accept_len) c.accept_len = h.accept_len + s0;
+  if (h.out_tokens) c.out_tokens = h.out_tokens + (size_t)s0 * B;
+  if (h.next_anchor) c.next_anchor = h.next_anchor + s0;
+  if (h.base_pos) c.base_pos = h.base_pos + s0;
+  if (h.commit_base) c.commit_base = h.commit_base + s0;
+  if (h.commit_count) c.commit_count = h.commit_count + s0;
+  if (h.cand_out) c.cand_out = h.cand_out + (size_t)s0 * Bd * h.topk;
+  if (h.logits) c.logits = h.logits + (size_t)s0 * (verify ? B : Bd) * h.V;
+  return c;
+}
+
+// The LM head in launches of whole sequences (at most 256 token rows each);
+// in top-k mode each launch's candidates are merged after it.
+int run_head(const HeadDesc& h, int sms, cudaStream_t st) {
+  const int per = head_seqs_per_launch(h.block);
+  for (int s0 = 0; s0 < h.n_seqs; s0 += per) {
+    const HeadDesc c = head_slice(h, s0, std::min(per, h.n_seqs - s0));
+    DF_LAUNCH(st, TF_HEAD, head_bytes(c), launch_head(c, sms, st));
+    if (c.topk > 0) {
+      int n_tiles = 0;
+      const void* tl = head_tc_supported(c) ? head_tc_tlist(c, sms, &n_tiles) : nullptr;
+      DF_LAUNCH(st, TF_PATH, 0, launch_topk_merge(c, tl, n_tiles, st));
+    }
+  }
+  return DFLASH_OK;
 }
 
 }  // namespace
@@ -654,12 +699,9 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   h.partials = static_cast<float*>(s.hpart);
   h.counters = c.counters;
   h.status = c.status;
-  DF_LAUNCH(st, TF_HEAD, head_bytes(h), launch_head(h, sms, st));
+  rc = run_head(h, sms, st);  // top-k mode: also each row's candidates, ranked by draft logit
+  if (rc) return rc;
   if (a->path_topk > 0) {
-    // the rows' top-k candidates (ranked by draft logit), then the walk
-    int n_tiles = 0;
-    const void* tl = head_tc_supported(h) ? head_tc_tlist(h, sms, &n_tiles) : nullptr;
-    DF_LAUNCH(st, TF_PATH, 0, launch_topk_merge(h, tl, n_tiles, st));
     PathDesc p;
     memset(&p, 0, sizeof(p));
     p.dtype = d.dtype;
@@ -730,7 +772,8 @@ int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
   h.partials = static_cast<float*>(hpart);
   h.counters = c.counters;
   h.status = c.status;
-  DF_LAUNCH(st, TF_HEAD, head_bytes(h), launch_head(h, sms, st));
+  rc = run_head(h, sms, st);
+  if (rc) return rc;
   return DFLASH_OK;
 }
 

@@ -688,10 +688,11 @@ int clusters_resident(int nc) {
   return cache[dev][nc];
 }
 
-// Cluster width: the widest (<= 16) for which one cluster per (sequence,
-// kv head) all run at once, at least 8.  Depends on the sequence and head
-// counts and the device, never on the row count, so decode (1 row) and
-// verification (a block) of one batch use the same width and per-row order.
+// Cluster width: the widest (<= 16) for which the clusters of one sequence
+// (one per KV head) all run at once, at least 8.  It depends on the KV-head
+// count and the device only -- never on the row or sequence count -- so a
+// token row's attention is computed the same way whatever else is in the
+// launch (decode and verification, one sequence or a batch).
 template <int D>
 int pick_nc(long groups) {
   for (int nc = kMaxNC; nc > 8; --nc)
@@ -720,7 +721,7 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
     p.kb = p.kc;
     p.vb = p.vc;
   }
-  const int nc = pick_nc<D>((long)a.n_seqs * a.nkv);
+  const int nc = pick_nc<D>((long)a.nkv);
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);

@@ -588,8 +588,8 @@ cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
 }  // namespace
 
 bool gemm_tc_supported(const GemmDesc& g) {
-  if (g.dtype != DFLASH_BF16 || g.M < 1 || g.M > 256 || g.K % 64 != 0 || g.nseg < 1 || g.nseg > kMaxSeg)
-    return false;
+  if (g.dtype != DFLASH_BF16 || g.M < 1 || g.K % 64 != 0 || g.nseg < 1 || g.nseg > kMaxSeg) return false;
+  if (g.M > 256 && g.rows > 256) return false;  // launches of <= 256 rows split at sequence boundaries
   if ((reinterpret_cast<uintptr_t>(g.X) & 15) != 0) return false;
   switch (g.kind) {
     case EPI_STORE:
@@ -609,8 +609,40 @@ size_t gemm_tc_workspace(const GemmDesc& g, int num_sms) {
   return part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(g.M));
 }
 
+cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
+                                uint32_t* status, int num_sms, cudaStream_t st);
+
+// More than 256 token rows run as launches of whole sequences (<= 256 rows
+// each).  A row's result does not depend on the launch it is in: the
+// k-partition is a function of the tiles and K only.
 cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters, uint32_t* status,
                            int num_sms, cudaStream_t st) {
+  if (g.M <= 256) return launch_gemm_tc_rows(g, ws, ws_bytes, counters, status, num_sms, st);
+  const int per = g.rows > 0 ? g.rows : 1;
+  const int mc = (256 / per) * per;
+  for (int m0 = 0; m0 < g.M; m0 += mc) {
+    GemmDesc c = g;
+    const int sq = m0 / per;  // first sequence of the launch
+    c.M = g.M - m0 < mc ? g.M - m0 : mc;
+    c.X = static_cast<const char*>(g.X) + (size_t)m0 * g.K * 2;
+    if (g.base_pos) c.base_pos = g.base_pos + sq;
+    if (g.valid) c.valid = g.valid + sq;
+    if (g.out_f32) c.out_f32 = g.out_f32 + (size_t)m0 * g.ldo;
+    if (g.q_out) c.q_out = static_cast<char*>(g.q_out) + (size_t)m0 * g.nq * g.d * 2;
+    if (g.act_out) c.act_out = static_cast<char*>(g.act_out) + (size_t)m0 * g.inter * 2;
+    for (int q = 0; q < g.nseg; ++q) {
+      const size_t kv = (size_t)sq * g.nkv * g.kv_cap * g.d * 2;
+      if (g.k_dst[q]) c.k_dst[q] = static_cast<char*>(g.k_dst[q]) + kv;
+      if (g.v_dst[q]) c.v_dst[q] = static_cast<char*>(g.v_dst[q]) + kv;
+    }
+    const cudaError_t e = launch_gemm_tc_rows(c, ws, ws_bytes, counters, status, num_sms, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
+                                uint32_t* status, int num_sms, cudaStream_t st) {
   if (g.M == 0) return cudaSuccess;
   TcParams p;
   memset(&p, 0, sizeof(p));
