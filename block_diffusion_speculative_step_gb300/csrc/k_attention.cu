@@ -258,6 +258,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (x, y) as a bf16 pair hi plus the bf16 pair of the remainders lo: hi + lo
+// carries the fp32 values to about 2^-17 relative, so a product with
+// bf16 operands keeps the probabilities at fp32-like precision.
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16(x - hf.x, y - hf.y);
+}
+
 // Byte offset of (row, 16-byte chunk) in a [rows][D] bf16 tile whose chunk
 // index is XOR-swizzled by the row, so ldmatrix row sets are bank-conflict free.
 template <int D>
@@ -491,13 +501,15 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
         O[t][2] *= al_b;
         O[t][3] *= al_b;
       }
-      // O += P V over the quarter
+      // O += P V over the quarter.  The probabilities stay fp32 (softmax is
+      // not a rounding point): P = P_hi + P_lo as two bf16 operands.
 #pragma unroll
       for (int kk = 0; kk < QK / 16; ++kk) {
-        const uint32_t a0 = pack_bf16(S[2 * kk][0], S[2 * kk][1]);
-        const uint32_t a1 = pack_bf16(S[2 * kk][2], S[2 * kk][3]);
-        const uint32_t a2 = pack_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1]);
-        const uint32_t a3 = pack_bf16(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+        uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+        split_bf16(S[2 * kk][0], S[2 * kk][1], a0, l0);
+        split_bf16(S[2 * kk][2], S[2 * kk][3], a1, l1);
+        split_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1], a2, l2);
+        split_bf16(S[2 * kk + 1][2], S[2 * kk + 1][3], a3, l3);
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
           uint32_t b0, b1, b2, b3;
@@ -505,6 +517,8 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
           ldsm_x4_t(vb + kv_off(key, 2 * dt + (lane >> 4)), b0, b1, b2, b3);
           mma_16816(O[2 * dt], a0, a1, a2, a3, b0, b1);
           mma_16816(O[2 * dt + 1], a0, a1, a2, a3, b2, b3);
+          mma_16816(O[2 * dt], l0, l1, l2, l3, b0, b1);
+          mma_16816(O[2 * dt + 1], l0, l1, l2, l3, b2, b3);
         }
       }
     }

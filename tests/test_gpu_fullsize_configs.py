@@ -1,0 +1,140 @@
+"""Parity at the full shapes of the other two workloads, one draft layer
+each (the per-layer work is what the full stack repeats):
+
+- the Coder-shaped long-context draft: H 2048, 32/4 heads, vocabulary
+  151936, position 32768 with a 4096-slot context window (ring slots
+  pos mod window), one and eight sequences;
+- the Llama-3.1-8B-shaped draft with block 10 and the DFlash 2 path
+  selector (top-16 candidates, rank 64), vocabulary 128256, context 2048,
+  one and sixteen sequences.
+
+Draft logits are compared with the oracle on a sampled sequence, argmax /
+paths bit-exact up to reported near-ties, and every sampled sequence re-run
+alone reproduces its rows of the batched launch bit for bit."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_step_gb300 import dflash as D
+from block_diffusion_speculative_step_gb300 import synth
+from block_diffusion_speculative_step_gb300.engine import Engine
+from oracle import oracle as O
+from tests import gpu_common as G
+from tests import helpers as Hh
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(name, S, ctx, cap):
+    w = synth.WORKLOADS[name]
+    w = dataclasses.replace(w, target=dataclasses.replace(w.target, layers=1),
+                            draft=dataclasses.replace(w.draft, layers=1), taps=(0, 0, 0, 0, 0), batch=S)
+    m = synth.make_model(w, seed=8, device="cuda", jitter=0.1)
+    eng = Engine(w, m, S, cap, prefill_chunk=16)
+    g = torch.Generator(device="cuda").manual_seed(13)
+    for t in eng.caches.dk + eng.caches.dv:
+        t.copy_(torch.randn(t.shape, generator=g, device="cuda").to(t.dtype))
+    eng.base_pos.fill_(ctx)
+    eng.anchor.copy_(torch.randint(0, w.vocab, (S,), generator=torch.Generator().manual_seed(3), dtype=torch.int32))
+    torch.cuda.synchronize()
+    return w, m, eng
+
+
+def _oracle_model(w, m):
+    n = synth.to_numpy
+    c = Hh.ocfg(w, w.draft)
+    L = m["draft"]["layers"][0]
+    layers = [O.Layer.from_stacked(c, n(L["w_qkv"]), n(L["w_o"]), n(L["w_gu"]), n(L["w_down"]), n(L["ln1"]),
+                                   n(L["ln2"]))]
+    st = O.Stack(c, layers, n(m["draft"]["final_norm"]))
+    # the draft forward reads no target state; the draft stack stands in for it
+    return O.Model(target=st, draft=st, E=n(m["embed"]), Wlm=n(m["lm_head"]), Wfc=n(m["fc"]),
+                   gfc=n(m["fc_norm"]), taps=list(w.taps), mask_id=w.mask_id, block=w.block, window=w.window)
+
+
+def _alone(eng, w, s, logits_row):
+    """dflash_draft_block for sequence s alone (pointers into the batch's buffers)."""
+    a = eng.draft_args(logits_row)
+    a.n_seqs = 1
+    a.anchor = eng.anchor.data_ptr() + 4 * s
+    a.base_pos = eng.base_pos.data_ptr() + 4 * s
+    drafts = torch.zeros(1, w.block - 1, dtype=torch.int32, device="cuda")
+    a.drafts = drafts.data_ptr()
+    for j in range(w.draft.layers):
+        k, v = eng.caches.dk[j], eng.caches.dv[j]
+        a.kv_layers[j] = D.dflash_kv(k.data_ptr() + s * k.stride(0) * k.element_size(),
+                                     v.data_ptr() + s * v.stride(0) * v.element_size(), eng.dcap, w.window)
+    D.dflash_draft_block(a, eng.ws_ptr, eng.ws_bytes)
+    torch.cuda.synchronize()
+    return drafts[0]
+
+
+def _check_logits_vs_oracle(w, m, eng, s, gl, gd):
+    om = _oracle_model(w, m)
+    st = O.new_state(om, eng.cap)
+    st.dk = [G.f64(eng.caches.dk[0][s])]
+    st.dv = [G.f64(eng.caches.dv[0][s])]
+    am, mg, lg = O.draft_forward(om, st, int(eng.anchor[s]), int(eng.base_pos[s]), want_logits=True)
+    err = np.abs(gl - lg).max()
+    # bf16 error is relative: the 2e-2 logit bound is applied per unit of the
+    # logits' RMS (1.28 at H = 4096 with these weights).  Through a whole
+    # layer the GPU (fp32 sums) and the oracle (fp64 sums) cross the bf16
+    # rounding points on either side of a tie at a small rate, and those
+    # one-ulp differences compound over the layer's rounding points.
+    tol = G.LOGIT_TOL["bf16"] * max(1.0, float(np.sqrt((lg.astype(np.float64) ** 2).mean())))
+    assert err <= tol, f"draft logits differ by {err} (bound {tol:.4g})"
+    if gd is not None:
+        G.check_argmax(gd, am, mg, tol=max(G.NEAR_TIE, 2 * err))
+    return om
+
+
+@pytest.mark.parametrize("S", [1, 8])
+def test_coder_long_window_draft(S):
+    w, m, eng = _setup("coder-long", S, 32768, 32768 + 64)
+    assert eng.dcap == w.window == 4096
+    B = w.block
+    logits = torch.zeros(S * (B - 1), w.vocab, device="cuda")
+    eng.draft(logits)
+    torch.cuda.synchronize()
+    assert eng.status() == D.DFLASH_OK
+    gd = eng.drafts.cpu().numpy()
+    gl = logits.view(S, B - 1, w.vocab)
+    s = S - 1
+    _check_logits_vs_oracle(w, m, eng, s, gl[s].cpu().numpy(), gd[s])
+    one = torch.zeros(B - 1, w.vocab, device="cuda")
+    d1 = _alone(eng, w, s, one)
+    assert torch.equal(one, gl[s]) and torch.equal(d1, eng.drafts[s])
+
+
+@pytest.mark.parametrize("S", [1, 16])
+def test_llama_path_selector_draft(S):
+    w, m, eng = _setup("llama31-8b", S, 2048, 2048 + 64)
+    B, K = w.block, w.path_topk
+    g = torch.Generator().manual_seed(21)
+    U = torch.randn(w.path_rank, w.draft.hidden, generator=g).to(torch.bfloat16)
+    Vm = torch.randn(w.path_rank, w.draft.hidden, generator=g).to(torch.bfloat16)
+    eng.m["path_u"].copy_(U.cuda())
+    eng.m["path_v"].copy_(Vm.cuda())
+    logits = torch.zeros(S * (B - 1), w.vocab, device="cuda")
+    eng.draft(logits)
+    torch.cuda.synchronize()
+    assert eng.status() == D.DFLASH_OK
+    gp = eng.drafts.cpu().numpy()
+    gl = logits.view(S, B - 1, w.vocab)
+    s = S // 2
+    om = _check_logits_vs_oracle(w, m, eng, s, gl[s].cpu().numpy(), None)
+    compared = 0
+    for q in sorted({0, s, S - 1}):
+        path, cand, mg = O.path_select(om.draft.cfg, gl[q].cpu().numpy(), om.E, synth.to_numpy(U),
+                                       synth.to_numpy(Vm), int(eng.anchor[q]), topk=K)
+        for j in range(B - 1):
+            if mg[j] < 1e-4:
+                break
+            assert gp[q, j] == path[j], f"seq {q} step {j}: gpu {gp[q, j]} oracle {path[j]} (margin {mg[j]:.3g})"
+            compared += 1
+    assert compared >= B - 1
+    one = torch.zeros(B - 1, w.vocab, device="cuda")
+    d1 = _alone(eng, w, s, one)
+    assert torch.equal(one, gl[s]) and torch.equal(d1, eng.drafts[s])
