@@ -285,6 +285,27 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def reduce_max(x: float, world: int, device: str = "cpu") -> float:
+    """The largest x over the ranks (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rates(world: int, S: int, steps: int, ms: float, tokens_per_step: float):
+    """Whole-job draft-block steps/s and verified tokens/s: every rank runs its
+    own replica of S sequences, so the job does world * S draft blocks and
+    world * tokens_per_step verified tokens per step in ms per `steps` steps."""
+    value = world * S * steps / (ms / 1000.0)
+    verified = world * tokens_per_step * steps / (ms / 1000.0)
+    return value, verified
+
+
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_speculative_step_gb300", "csrc")
@@ -390,17 +411,13 @@ def run_ours(args):
     e1.record()
     torch.cuda.synchronize()
     clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
+    ms = reduce_max(e0.elapsed_time(e1), world, "cuda")
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     ms_per_step = ms / args.steps
     S = w.batch
-    value = world * S * args.steps / (ms / 1000.0)
     mean_accept = float(accept.float().mean())
-    verified = world * float((accept + 1).sum()) * args.steps / (ms / 1000.0)
+    value, verified = job_rates(world, S, args.steps, ms, float((accept + 1).sum()))
 
     # end to end through the public API with host buffers
     e2e = None
@@ -425,11 +442,7 @@ def run_ours(args):
             h_out[:S].copy_(eng.accept_len, non_blocking=True)
             h_out[S:].copy_(eng.out_tokens.view(-1), non_blocking=True)
             torch.cuda.synchronize()
-        el = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([el], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
+        el = reduce_max(time.perf_counter() - t0, world, "cuda")
         e2e = {"value": world * S * e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": int(h_in.numel() * 4),
                "d2h_bytes_per_step": int(h_out.numel() * 4), "steps": e2e_steps,
                "path": "eager C-ABI calls per step (no graph), pinned host inputs/outputs"}

@@ -1,0 +1,68 @@
+"""The replica path of bench.py on CPU with two gloo ranks: the timed region
+is the maximum over ranks, the whole-job rate counts every replica's work,
+and the reference arm runs on rank 0 only."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    local_ms = 100.0 + 50.0 * rank  # rank 1 is the slower replica
+    ms = bench.reduce_max(local_ms, world)
+    value, verified = bench.job_rates(world, 1, 10, ms, 3.0)
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, ms, value, verified))
+
+
+def test_two_ranks_take_the_slowest_replica():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    out = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, ms, value, verified in out:
+        assert ms == 150.0                          # max over ranks
+        assert value == pytest.approx(2 * 1 * 10 / 0.150)   # both replicas' draft blocks
+        assert verified == pytest.approx(2 * 3.0 * 10 / 0.150)
+
+
+def test_single_rank_is_unchanged():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.reduce_max(12.5, 1) == 12.5
+    value, verified = bench.job_rates(1, 32, 4, 200.0, 64.0)
+    assert value == pytest.approx(32 * 4 / 0.2) and verified == pytest.approx(64 * 4 / 0.2)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("RANK", "1")
+    args = type("A", (), {"workload": "qwen3-8b-b1", "steps": 1, "warmup": 0, "gpus": 2})()
+    assert bench.run_reference(args) is None
+    assert capsys.readouterr().out == ""
