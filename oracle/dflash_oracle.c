@@ -457,6 +457,165 @@ void or_path_select(const or_cfg* c, int B, int Vocab, int topk, int R, const fl
   free(ve);
 }
 
+/* ------------------------------------------------------------- sampling
+ *
+ * Sampling-mode verification, the lossless-in-distribution variant of the
+ * greedy rule ([G] section 7: the path is walked "greedily or by sampling"
+ * and rejection sampling keeps the output distribution exactly the
+ * target's).  This follows speculative sampling as published (Leviathan,
+ * Kalman, Matias, "Fast Inference from Transformers via Speculative
+ * Decoding", ICML 2023; Chen et al., "Accelerating Large Language Model
+ * Decoding with Speculative Sampling", 2023) at temperature T:
+ *   p_j = softmax(target logits of block row j / T), q_j = softmax(draft
+ *   logits of block row j+1 / T) -- both the distribution of the token at
+ *   position P+j+1;
+ *   the draft token d of block row j+1 is sampled from q_j;
+ *   it is accepted with probability min(1, p_j(d) / q_j(d)), i.e. iff
+ *   log u < log p_j(d) - log q_j(d);
+ *   at the first rejection the emitted token is sampled from
+ *   max(0, p_j - q_j) normalised; if every draft is accepted a bonus token
+ *   is sampled from the last target row.
+ * A categorical draw from weights w is the argmax over v of log w_v + g_v
+ * (Gumbel-max; exponential race for unnormalised weights), g_v Gumbel(0,1).
+ *
+ * Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC'11), key (seed low, seed high),
+ * counter (vocabulary entry, position, sequence << 8 | purpose, cycle);
+ * u = ((x0 >> 8) + 1/2) 2^-24 in (0, 1), g = -log(-log u).
+ */
+enum { OR_RNG_DRAFT = 1, OR_RNG_ACCEPT = 2, OR_RNG_RESID = 3, OR_RNG_BONUS = 4 };
+
+void or_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u; /* Weyl key schedule */
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+    c0 = n0;
+    c1 = n1;
+    c2 = n2;
+    c3 = n3;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+double or_uniform(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose, uint32_t cycle) {
+  const uint32_t ctr[4] = {v, pos, (seq << 8) | (purpose & 0xFFu), cycle};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t x[4];
+  or_philox4x32_10(ctr, key, x);
+  return ((double)(x[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+static double gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose, uint32_t cycle) {
+  return -log(-log(or_uniform(seed, v, pos, seq, purpose, cycle)));
+}
+
+/* log sum_v exp(l_v / T) */
+static double row_lse(const float* l, int V, double T) {
+  double mx = -INFINITY;
+  for (int v = 0; v < V; ++v) mx = fmax(mx, (double)l[v] / T);
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += exp((double)l[v] / T - mx);
+  return mx + log(s);
+}
+
+/* A draw from softmax(l / T): argmax_v l_v / T + g_v (lowest index on ties).
+ * Returns the token; *lse = log sum exp(l / T); *margin = best - second. */
+int or_sample_row(const float* l, int V, double T, uint64_t seed, int pos, int seq, int purpose, int cycle,
+                  double* lse, double* margin) {
+  int bi = -1;
+  double best = -INFINITY, second = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    const double sc = (double)l[v] / T + gumbel(seed, (uint32_t)v, (uint32_t)pos, (uint32_t)seq, (uint32_t)purpose,
+                                                (uint32_t)cycle);
+    if (bi < 0 || sc > best) {
+      second = best;
+      best = sc;
+      bi = v;
+    } else if (sc > second) {
+      second = sc;
+    }
+  }
+  if (lse) *lse = row_lse(l, V, T);
+  if (margin) *margin = best - second;
+  return bi;
+}
+
+/* One sequence's block: target logits tl [B][V] (row j: position P+j+1),
+ * draft logits dl [B-1][V] (row i: block row i+1, position P+i+1), drafts
+ * [B-1].  Writes out_tokens[0..k] and returns the accept length k.
+ * *margin = the smallest decision margin met (acceptance tests and the final
+ * draw), for near-tie reporting. */
+int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const int* drafts, double T,
+                          uint64_t seed, int seq, int P, int cycle, int* out_tokens, double* margin) {
+  double mg = INFINITY;
+  int k = 0;
+  for (int j = 1; j <= B - 1; ++j) {
+    const int d = drafts[j - 1];
+    const float* trow = tl + (size_t)(j - 1) * V;
+    const float* drow = dl + (size_t)(j - 1) * V;
+    const double lp = (double)trow[d] / T - row_lse(trow, V, T);
+    const double lq = (double)drow[d] / T - row_lse(drow, V, T);
+    const double lu = log(or_uniform(seed, 0u, (uint32_t)(P + j), (uint32_t)seq, OR_RNG_ACCEPT, (uint32_t)cycle));
+    mg = fmin(mg, fabs(lu - (lp - lq)));
+    if (!(lu < lp - lq)) break;
+    out_tokens[k++] = d;
+  }
+  int x = -1;
+  double best = -INFINITY, second = -INFINITY;
+  if (k < B - 1) {
+    /* residual max(0, p - q) at the rejected row, by exponential race */
+    const float* trow = tl + (size_t)k * V;
+    const float* drow = dl + (size_t)k * V;
+    const double lt = row_lse(trow, V, T), ld = row_lse(drow, V, T);
+    for (int v = 0; v < V; ++v) {
+      const double a = (double)trow[v] / T - lt, b = (double)drow[v] / T - ld;
+      if (!(a > b)) continue; /* weight 0 */
+      const double sc = a + log1p(-exp(b - a)) +
+                        gumbel(seed, (uint32_t)v, (uint32_t)(P + k + 1), (uint32_t)seq, OR_RNG_RESID, (uint32_t)cycle);
+      if (x < 0 || sc > best) {
+        second = best;
+        best = sc;
+        x = v;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+  }
+  if (x < 0) {
+    /* all drafts accepted (or p == q at the rejected row): a draw from p */
+    const int row = k < B - 1 ? k : B - 1;
+    const int purpose = k < B - 1 ? OR_RNG_RESID : OR_RNG_BONUS;
+    const float* trow = tl + (size_t)row * V;
+    for (int v = 0; v < V; ++v) {
+      const double sc = (double)trow[v] / T +
+                        gumbel(seed, (uint32_t)v, (uint32_t)(P + row + 1), (uint32_t)seq, (uint32_t)purpose, (uint32_t)cycle);
+      if (x < 0 || sc > best) {
+        second = best;
+        best = sc;
+        x = v;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+  }
+  out_tokens[k] = x;
+  mg = fmin(mg, best - second);
+  if (margin) *margin = mg;
+  return k;
+}
+
 int or_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -90,6 +90,17 @@ def lib():
                                          C.POINTER(C.c_float), C.c_void_p, C.c_void_p, C.c_void_p,
                                          C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), dp]
             L.or_num_threads.restype = C.c_int
+            u32p = C.POINTER(C.c_uint32)
+            L.or_philox4x32_10.argtypes = [u32p, u32p, u32p]
+            L.or_uniform.restype = C.c_double
+            L.or_uniform.argtypes = [C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint32]
+            L.or_sample_row.restype = C.c_int
+            L.or_sample_row.argtypes = [C.POINTER(C.c_float), C.c_int, C.c_double, C.c_uint64, C.c_int, C.c_int,
+                                        C.c_int, C.c_int, dp, dp]
+            L.or_spec_sample_accept.restype = C.c_int
+            L.or_spec_sample_accept.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float),
+                                                C.POINTER(C.c_int), C.c_double, C.c_uint64, C.c_int, C.c_int,
+                                                C.c_int, C.POINTER(C.c_int), dp]
             _lib = L
     return _lib
 
@@ -448,3 +459,47 @@ def speculative_generate(m: Model, prompt, n_new: int, cap: int, drafter=None):
 
 def threads() -> int:
     return int(lib().or_num_threads())
+
+
+# ---------------------------------------------------------------- sampling
+# Random-number purposes (the counter's low byte next to the sequence id).
+RNG_DRAFT, RNG_ACCEPT, RNG_RESID, RNG_BONUS = 1, 2, 3, 4
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 (Salmon et al., SC'11): 4 x uint32 counter, 2 x uint32 key."""
+    c = (C.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in ctr])
+    k = (C.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    o = (C.c_uint32 * 4)()
+    lib().or_philox4x32_10(c, k, o)
+    return [int(x) for x in o]
+
+
+def uniform(seed: int, v: int, pos: int, seq: int, purpose: int, cycle: int) -> float:
+    return lib().or_uniform(seed, v, pos, seq, purpose, cycle)
+
+
+def sample_row(logits: np.ndarray, T: float, seed: int, pos: int, seq: int, purpose: int, cycle: int):
+    """A draw from softmax(logits / T) by Gumbel-max: (token, log-sum-exp, margin)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    lse, mg = C.c_double(), C.c_double()
+    tok = lib().or_sample_row(lg.ctypes.data_as(C.POINTER(C.c_float)), lg.shape[0], float(T), seed, pos, seq,
+                              purpose, cycle, C.byref(lse), C.byref(mg))
+    return tok, lse.value, mg.value
+
+
+def spec_sample_accept(tl: np.ndarray, dl: np.ndarray, drafts, T: float, seed: int, seq: int, P: int, cycle: int):
+    """Speculative sampling over one sequence's block: target logits [B][V],
+    draft logits [B-1][V], drafts [B-1] -> (accept length k, emitted tokens
+    [k+1], smallest decision margin)."""
+    tl = np.ascontiguousarray(tl, dtype=np.float32)
+    dl = np.ascontiguousarray(dl, dtype=np.float32)
+    B, V = tl.shape
+    dr = np.ascontiguousarray(drafts, dtype=np.int32)
+    out = np.zeros(B, dtype=np.int32)
+    mg = C.c_double()
+    k = lib().or_spec_sample_accept(B, V, tl.ctypes.data_as(C.POINTER(C.c_float)),
+                                    dl.ctypes.data_as(C.POINTER(C.c_float)), dr.ctypes.data_as(C.POINTER(C.c_int)),
+                                    float(T), seed, seq, P, cycle, out.ctypes.data_as(C.POINTER(C.c_int)), C.byref(mg))
+    return k, out[:k + 1].copy(), mg.value
+
