@@ -817,6 +817,96 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   return DFLASH_OK;
 }
 
+// ------------------------------------------------------------- sampling
+
+static size_t sample_ws(int S, int B, size_t* lse_off, size_t* k_off, size_t* part_off) {
+  size_t off = kReservedBytes;
+  *lse_off = off;
+  off += ((size_t)S * B * sizeof(float) + 255) & ~size_t(255);
+  *k_off = off;
+  off += ((size_t)S * sizeof(int32_t) + 255) & ~size_t(255);
+  *part_off = off;
+  off += sample_part_bytes(S * B);
+  return off;
+}
+
+static int check_sample_shape(const dflash_dims& d, int S, int B, float T, const char* who) {
+  DF_CHECK(d.vocab > 0, "%s: vocab must be > 0", who);
+  DF_CHECK(S > 0 && B >= 2 && (long)S * B <= 1024, "%s: n_seqs > 0, block >= 2, n_seqs*block <= 1024", who);
+  DF_CHECK(T > 0.f && T == T, "%s: temperature must be > 0", who);
+  return DFLASH_OK;
+}
+
+int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_sample_drafts";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, who);
+  if (rc) return rc;
+  DF_CHECK(a->base_pos && a->draft_logits && a->drafts && a->draft_lse, "%s: NULL pointer", who);
+  size_t lo, ko, po;
+  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po), who);
+  if (rc) return rc;
+  Ctx c = header(ws);
+  SampleDesc d;
+  memset(&d, 0, sizeof(d));
+  d.n_seqs = a->n_seqs;
+  d.block = a->block;
+  d.V = a->dims.vocab;
+  d.cycle = a->cycle;
+  d.T = a->temperature;
+  d.seed = a->seed;
+  d.base_pos = const_cast<int32_t*>(a->base_pos);
+  d.draft_logits = a->draft_logits;
+  d.draft_lse_out = a->draft_lse;
+  d.drafts_out = a->drafts;
+  d.part = static_cast<char*>(ws) + po;
+  d.counters = c.counters + kCtrSample;
+  d.status = c.status;
+  DF_LAUNCH((cudaStream_t)stream, TF_SAMPLE, 0, launch_sample_drafts(d, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_sample_accept";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, who);
+  if (rc) return rc;
+  DF_CHECK(a->target_logits && a->draft_logits && a->draft_lse && a->drafts && a->base_pos && a->accept_len &&
+               a->out_tokens,
+           "%s: NULL pointer", who);
+  DF_CHECK(!a->commit_base || a->update_base_pos, "%s: commit_base needs update_base_pos", who);
+  size_t lo, ko, po;
+  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po), who);
+  if (rc) return rc;
+  Ctx c = header(ws);
+  SampleDesc d;
+  memset(&d, 0, sizeof(d));
+  d.n_seqs = a->n_seqs;
+  d.block = a->block;
+  d.V = a->dims.vocab;
+  d.cycle = a->cycle;
+  d.T = a->temperature;
+  d.seed = a->seed;
+  d.base_pos = a->base_pos;
+  d.target_logits = a->target_logits;
+  d.draft_logits = a->draft_logits;
+  d.draft_lse = a->draft_lse;
+  d.drafts = a->drafts;
+  d.out_tokens = a->out_tokens;
+  d.accept_len = a->accept_len;
+  d.next_anchor = a->next_anchor;
+  d.commit_base = a->commit_base;
+  d.commit_count = a->commit_count;
+  d.update_base = a->update_base_pos;
+  d.seq_k = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + ko);
+  d.part = static_cast<char*>(ws) + po;
+  d.counters = c.counters + kCtrSample;
+  d.status = c.status;
+  float* lse_t = reinterpret_cast<float*>(static_cast<char*>(ws) + lo);
+  DF_LAUNCH((cudaStream_t)stream, TF_SAMPLE, 0, launch_sample_accept(d, lse_t, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
 // ------------------------------------------------------------- workspace
 
 size_t dflash_workspace_bytes(int32_t op, const void* args) {
@@ -827,6 +917,16 @@ size_t dflash_workspace_bytes(int32_t op, const void* args) {
       return kReservedBytes;
     case DFLASH_OP_PATH:
       return path_ws(static_cast<const dflash_path_args*>(args));
+    case DFLASH_OP_SAMPLE_DRAFTS: {
+      const dflash_sample_drafts_args* a = static_cast<const dflash_sample_drafts_args*>(args);
+      size_t lo, ko, po;
+      return sample_ws(a->n_seqs, a->block, &lo, &ko, &po);
+    }
+    case DFLASH_OP_SAMPLE_ACCEPT: {
+      const dflash_sample_accept_args* a = static_cast<const dflash_sample_accept_args*>(args);
+      size_t lo, ko, po;
+      return sample_ws(a->n_seqs, a->block, &lo, &ko, &po);
+    }
     case DFLASH_OP_LAYER:
       return layer_ws(static_cast<const dflash_layer_args*>(args), sms);
     case DFLASH_OP_FUSE: {

@@ -108,6 +108,33 @@ struct PathDesc {
   uint32_t* status;
 };
 
+// Sampling-mode verification (k_sample.cu).
+struct SampleDesc {
+  int n_seqs, block, V, cycle;
+  float T;
+  uint64_t seed;
+  int32_t* base_pos;          // [S] position of block row 0 (advanced when update_base)
+  const float* draft_logits;  // [S][block-1][V]
+  const float* target_logits; // [S][block][V]
+  const float* draft_lse;     // [S][block-1] (acceptance)
+  float* draft_lse_out;       // [S][block-1] (draft draws)
+  int32_t* drafts_out;        // [S][block-1] (draft draws)
+  const int32_t* drafts;      // [S][block-1] (acceptance)
+  int32_t* out_tokens;
+  int32_t* accept_len;
+  int32_t* next_anchor;
+  int32_t* commit_base;
+  int32_t* commit_count;
+  int update_base;
+  int32_t* seq_k;             // workspace [S]
+  void* part;                 // workspace, sample_part_bytes(rows)
+  uint32_t* counters;
+  uint32_t* status;
+};
+size_t sample_part_bytes(int rows);
+cudaError_t launch_sample_drafts(const SampleDesc& d, cudaStream_t st);
+cudaError_t launch_sample_accept(const SampleDesc& d, float* lse_t, cudaStream_t st);
+
 // Path-selector projection scratch (floats) for S sequences.
 inline size_t path_proj_floats(int S, int block, int topk, int rank) {
   return (size_t)S * (1 + (size_t)(block - 1) * topk) * 2 * rank;

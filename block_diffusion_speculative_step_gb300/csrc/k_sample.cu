@@ -1,0 +1,308 @@
+// k_sample.cu -- sampling-mode verification: the lossless-in-distribution
+// variant of the greedy acceptance ("DFlash：块扩散加速的 LLM 推测解码技术",
+// section 7: the path is walked greedily or by sampling, and rejection
+// sampling keeps the output distribution exactly the target's).  It is
+// speculative sampling at temperature T: drafts are draws from
+// q = softmax(draft logits / T); draft d is accepted iff log u < log p(d) -
+// log q(d) with p = softmax(target logits / T); the first rejection emits a
+// draw from max(0, p - q), and if every draft is accepted a bonus draw from
+// the last target row is emitted.
+//
+// A categorical draw from weights w is the argmax over v of log w_v + g_v
+// with g_v Gumbel(0, 1) (Gumbel-max; the exponential race for unnormalised
+// weights).  Random numbers: Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11), key (seed low, seed
+// high), counter (vocabulary entry, position, sequence << 8 | purpose,
+// cycle); u = ((x0 >> 8) + 1/2) 2^-24.  Every reduction runs in a fixed
+// order: the row is cut into kSplit contiguous slices, one CTA each, and the
+// last CTA of a row merges the slices in slice order.
+#include <limits.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "launch.cuh"
+
+namespace dfl {
+
+constexpr int kSampleThreads = 256;
+constexpr int kSplit = 16;  // CTAs per vocabulary row
+
+enum : uint32_t { RNG_DRAFT = 1, RNG_ACCEPT = 2, RNG_RESID = 3, RNG_BONUS = 4 };
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ float rng_uniform(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose,
+                                             uint32_t cycle) {
+  const uint4 x = philox4x32_10(make_uint4(v, pos, (seq << 8) | (purpose & 0xFFu), cycle), (uint32_t)seed,
+                                (uint32_t)(seed >> 32));
+  return ((float)(x.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
+}
+
+__device__ __forceinline__ float rng_gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose,
+                                            uint32_t cycle) {
+  return -logf(-logf(rng_uniform(seed, v, pos, seq, purpose, cycle)));
+}
+
+// Running state of one slice: log-sum-exp pieces (m, s: sum exp(x - m)) and
+// the best draw (score, index; lower index on equal scores).
+struct RowAcc {
+  float m, s, best;
+  int idx;
+};
+
+__device__ __forceinline__ RowAcc acc_empty() { return RowAcc{-INFINITY, 0.f, -INFINITY, INT_MAX}; }
+
+__device__ __forceinline__ void acc_lse(RowAcc& a, float x) {
+  if (x == -INFINITY) return;  // exp(-inf) adds nothing
+  if (x > a.m) {
+    a.s = a.s * expf(a.m - x) + 1.f;
+    a.m = x;
+  } else {
+    a.s += expf(x - a.m);
+  }
+}
+
+__device__ __forceinline__ void acc_draw(RowAcc& a, float sc, int v) {
+  if (sc > a.best || (sc == a.best && v < a.idx)) {
+    a.best = sc;
+    a.idx = v;
+  }
+}
+
+// Associative merge (the order of merges is fixed by the callers).
+__device__ __forceinline__ RowAcc acc_merge(const RowAcc& a, const RowAcc& b) {
+  RowAcc r;
+  if (b.m == -INFINITY) {
+    r.m = a.m;
+    r.s = a.s;
+  } else if (a.m == -INFINITY) {
+    r.m = b.m;
+    r.s = b.s;
+  } else if (a.m >= b.m) {
+    r.m = a.m;
+    r.s = a.s + b.s * expf(b.m - a.m);
+  } else {
+    r.m = b.m;
+    r.s = b.s + a.s * expf(a.m - b.m);
+  }
+  const bool tb = b.best > a.best || (b.best == a.best && b.idx < a.idx);
+  r.best = tb ? b.best : a.best;
+  r.idx = tb ? b.idx : a.idx;
+  return r;
+}
+
+// Block-wide merge in a fixed order: lanes by a butterfly, then warps in order.
+__device__ __forceinline__ RowAcc block_merge(RowAcc a, RowAcc* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    RowAcc b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    b.best = __shfl_xor_sync(0xffffffffu, a.best, o);
+    b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    a = acc_merge(a, b);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = a;
+  __syncthreads();
+  RowAcc t = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) t = acc_merge(t, red[i]);
+  __syncthreads();
+  return t;
+}
+
+// Last of kSplit slice CTAs of `row` to arrive (its slice partial stored).
+__device__ __forceinline__ bool slice_last(uint32_t* ctr, int* s_last) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(ctr, 1u);
+    *s_last = (old == (uint32_t)kSplit - 1);
+    if (*s_last) *ctr = 0u;
+  }
+  __syncthreads();
+  if (*s_last) __threadfence();
+  return *s_last != 0;
+}
+
+// One vocabulary row per blockIdx.x (row = s * rows_per_seq + i), slice
+// blockIdx.y.  lse_out[row] = log sum exp(l / T); with draw != 0 also
+// tok_out[row] = a Gumbel-max draw from softmax(l / T) at position
+// base_pos[s] + first_pos + i.
+__global__ void __launch_bounds__(kSampleThreads) row_sample_kernel(const __grid_constant__ SampleDesc d,
+                                                                    const float* logits, int rows_per_seq,
+                                                                    int first_pos, int draw, float* lse_out,
+                                                                    int32_t* tok_out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ RowAcc red[kSampleThreads / 32];
+  __shared__ int s_last;
+  const int row = blockIdx.x, sl = blockIdx.y;
+  const int s = row / rows_per_seq, i = row % rows_per_seq;
+  const int V = d.V;
+  const float invT = 1.f / d.T;
+  const float* l = logits + (size_t)row * V;
+  const int per = (V + kSplit - 1) / kSplit;
+  const int v0 = sl * per, v1 = min(V, v0 + per);
+  const uint32_t pos = (uint32_t)(d.base_pos[s] + first_pos + i);
+  RowAcc a = acc_empty();
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const float x = l[v] * invT;
+    if (x != x) {
+      raise_status(d.status, ST_NUMERIC);
+      continue;
+    }
+    acc_lse(a, x);
+    if (draw) acc_draw(a, x + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_DRAFT, (uint32_t)d.cycle), v);
+  }
+  a = block_merge(a, red);
+  RowAcc* part = static_cast<RowAcc*>(d.part) + (size_t)row * kSplit;
+  if (threadIdx.x == 0) part[sl] = a;
+  if (!slice_last(d.counters + row, &s_last)) return;
+  if (threadIdx.x == 0) {
+    RowAcc t = part[0];
+    for (int k = 1; k < kSplit; ++k) {
+      RowAcc p;
+      p.m = __ldcg(&part[k].m);
+      p.s = __ldcg(&part[k].s);
+      p.best = __ldcg(&part[k].best);
+      p.idx = __ldcg(&part[k].idx);
+      t = acc_merge(t, p);
+    }
+    lse_out[row] = t.m + logf(t.s);
+    if (draw) tok_out[row] = t.idx == INT_MAX ? 0 : t.idx;
+  }
+}
+
+// One warp per sequence: the acceptance tests of the block, then the row of
+// the final draw (its index into the target rows, or -1 for none).
+__global__ void spec_accept_kernel(const __grid_constant__ SampleDesc d, const float* lse_t) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = blockIdx.x;
+  if (threadIdx.x != 0) return;
+  const int B = d.block, V = d.V;
+  const float invT = 1.f / d.T;
+  const int P = d.base_pos[s];
+  int k = 0;
+  for (int j = 1; j <= B - 1; ++j) {
+    const int dj = d.drafts[(size_t)s * (B - 1) + j - 1];
+    if (dj < 0 || dj >= V) {
+      raise_status(d.status, ST_RANGE);
+      break;
+    }
+    const float lp = d.target_logits[((size_t)s * B + j - 1) * V + dj] * invT - lse_t[(size_t)s * B + j - 1];
+    const float lq = d.draft_logits[((size_t)s * (B - 1) + j - 1) * V + dj] * invT - d.draft_lse[(size_t)s * (B - 1) + j - 1];
+    const float lu = logf(rng_uniform(d.seed, 0u, (uint32_t)(P + j), (uint32_t)s, RNG_ACCEPT, (uint32_t)d.cycle));
+    if (!(lu < lp - lq)) break;
+    d.out_tokens[(size_t)s * B + k] = dj;
+    ++k;
+  }
+  d.seq_k[s] = k;
+}
+
+// Final draw of each sequence (blockIdx.x), slice blockIdx.y: from
+// max(0, p - q) at the rejected row, or from p (every draft accepted, or
+// p == q there); the last slice CTA writes the token and the cycle state.
+__global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_constant__ SampleDesc d,
+                                                                  const float* lse_t) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ RowAcc red[kSampleThreads / 32];
+  __shared__ int s_last;
+  const int s = blockIdx.x, sl = blockIdx.y;
+  const int B = d.block, V = d.V;
+  const float invT = 1.f / d.T;
+  const int k = d.seq_k[s];
+  const int P = d.base_pos[s];
+  const bool resid = k < B - 1;
+  const int trow = resid ? k : B - 1;
+  const float* tl = d.target_logits + ((size_t)s * B + trow) * V;
+  const float* dl = resid ? d.draft_logits + ((size_t)s * (B - 1) + k) * V : nullptr;
+  const float lt = lse_t[(size_t)s * B + trow];
+  const float ld = resid ? d.draft_lse[(size_t)s * (B - 1) + k] : 0.f;
+  const uint32_t pos = (uint32_t)(P + trow + 1);
+  const int per = (V + kSplit - 1) / kSplit;
+  const int v0 = sl * per, v1 = min(V, v0 + per);
+  RowAcc ar = acc_empty();  // the residual draw
+  RowAcc ap = acc_empty();  // the draw from p (used when no residual weight is positive)
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const float a = tl[v] * invT - lt;
+    if (resid) {
+      const float b = dl[v] * invT - ld;
+      if (a > b)
+        acc_draw(ar, a + log1pf(-expf(b - a)) + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID,
+                                                             (uint32_t)d.cycle), v);
+      acc_draw(ap, tl[v] * invT + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID, (uint32_t)d.cycle), v);
+    } else {
+      acc_draw(ap, tl[v] * invT + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_BONUS, (uint32_t)d.cycle), v);
+    }
+  }
+  ar = block_merge(ar, red);
+  ap = block_merge(ap, red);
+  RowAcc* part = static_cast<RowAcc*>(d.part) + (size_t)s * 2 * kSplit;
+  if (threadIdx.x == 0) {
+    part[sl] = ar;
+    part[kSplit + sl] = ap;
+  }
+  if (!slice_last(d.counters + s, &s_last)) return;
+  if (threadIdx.x == 0) {
+    RowAcc r = part[0], q = part[kSplit];
+    for (int i = 1; i < kSplit; ++i) {
+      RowAcc x, y;
+      x.m = -INFINITY;
+      x.s = 0.f;
+      x.best = __ldcg(&part[i].best);
+      x.idx = __ldcg(&part[i].idx);
+      y.m = -INFINITY;
+      y.s = 0.f;
+      y.best = __ldcg(&part[kSplit + i].best);
+      y.idx = __ldcg(&part[kSplit + i].idx);
+      r = acc_merge(r, x);
+      q = acc_merge(q, y);
+    }
+    const int x = (resid && r.idx != INT_MAX) ? r.idx : (q.idx == INT_MAX ? 0 : q.idx);
+    d.out_tokens[(size_t)s * B + k] = x;
+    for (int j = k + 1; j < B; ++j) d.out_tokens[(size_t)s * B + j] = -1;
+    d.accept_len[s] = k;
+    if (d.next_anchor) d.next_anchor[s] = x;
+    if (d.update_base) {
+      if (d.commit_base) d.commit_base[s] = P;
+      d.base_pos[s] = P + k + 1;
+    }
+    if (d.commit_count) d.commit_count[s] = k + 1;
+  }
+}
+
+cudaError_t launch_sample_drafts(const SampleDesc& d, cudaStream_t st) {
+  const int rows = d.n_seqs * (d.block - 1);
+  if (rows == 0) return cudaSuccess;
+  return launch_pdl(row_sample_kernel, dim3(rows, kSplit), dim3(kSampleThreads), 0, st, d, d.draft_logits,
+                    d.block - 1, 1, 1, d.draft_lse_out, d.drafts_out);
+}
+
+cudaError_t launch_sample_accept(const SampleDesc& d, float* lse_t, cudaStream_t st) {
+  if (d.n_seqs == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(row_sample_kernel, dim3(d.n_seqs * d.block, kSplit), dim3(kSampleThreads), 0, st, d,
+                             d.target_logits, d.block, 0, 0, lse_t, (int32_t*)nullptr);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(spec_accept_kernel, dim3(d.n_seqs), dim3(32), 0, st, d, (const float*)lse_t);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(resample_kernel, dim3(d.n_seqs, kSplit), dim3(kSampleThreads), 0, st, d, (const float*)lse_t);
+}
+
+size_t sample_part_bytes(int rows) { return (size_t)rows * 2 * kSplit * sizeof(RowAcc); }
+
+}  // namespace dfl

@@ -15,7 +15,8 @@ enum TraceFamily : int {
   TF_ROPE = 7,
   TF_TAP = 8,
   TF_CONVERT = 9,
-  kTraceFamilies = 10
+  TF_SAMPLE = 10,
+  kTraceFamilies = 11
 };
 
 void trace_pre(cudaStream_t st, int family);

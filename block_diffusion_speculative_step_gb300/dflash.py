@@ -21,7 +21,8 @@ DFLASH_F32 = 0
 DFLASH_BF16 = 1
 DFLASH_ATTN_CAUSAL = 0
 DFLASH_ATTN_BLOCK_BIDIR = 1
-DFLASH_OP_EMBED, DFLASH_OP_LAYER, DFLASH_OP_FUSE, DFLASH_OP_DRAFT, DFLASH_OP_VERIFY, DFLASH_OP_PATH = range(6)
+(DFLASH_OP_EMBED, DFLASH_OP_LAYER, DFLASH_OP_FUSE, DFLASH_OP_DRAFT, DFLASH_OP_VERIFY, DFLASH_OP_PATH,
+ DFLASH_OP_SAMPLE_DRAFTS, DFLASH_OP_SAMPLE_ACCEPT) = range(8)
 DFLASH_MAX_LAYERS = 16
 
 # Every symbol the header exports (checked by the CPU test suite).
@@ -29,8 +30,9 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_draft_block", "dflash_verify_accept", "dflash_path_select", "dflash_workspace_bytes",
            "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
-           "dflash_verify_accept_noalloc", "dflash_trace_launches")
-DFLASH_TRACE_FAMILIES = 10
+           "dflash_verify_accept_noalloc", "dflash_trace_launches", "dflash_sample_drafts",
+           "dflash_sample_accept")
+DFLASH_TRACE_FAMILIES = 11
 
 
 class DFlashError(RuntimeError):
@@ -100,6 +102,20 @@ class dflash_path_args(C.Structure):
                 ("margin", vp)]
 
 
+class dflash_sample_drafts_args(C.Structure):
+    _fields_ = [("dims", dflash_dims), ("n_seqs", i32), ("block", i32), ("temperature", C.c_float),
+                ("cycle", i32), ("seed", C.c_uint64), ("base_pos", vp), ("draft_logits", vp), ("drafts", vp),
+                ("draft_lse", vp)]
+
+
+class dflash_sample_accept_args(C.Structure):
+    _fields_ = [("dims", dflash_dims), ("n_seqs", i32), ("block", i32), ("temperature", C.c_float),
+                ("cycle", i32), ("seed", C.c_uint64), ("target_logits", vp), ("draft_logits", vp),
+                ("draft_lse", vp), ("drafts", vp), ("base_pos", vp), ("update_base_pos", i32),
+                ("accept_len", vp), ("out_tokens", vp), ("next_anchor", vp), ("commit_base", vp),
+                ("commit_count", vp)]
+
+
 class dflash_trace_stat(C.Structure):
     _fields_ = [("name", C.c_char * 24), ("launches", i32), ("total_ms", C.c_double), ("bytes", C.c_double)]
 
@@ -116,7 +132,7 @@ def lib(path: str | None = None):
             raise RuntimeError(f"{path} is missing: build the CUDA library first (__graft_entry__.build())")
         L = C.CDLL(path)
         for name in ("dflash_embed", "dflash_decoder_layer_forward", "dflash_fuse_context", "dflash_draft_block",
-                     "dflash_verify_accept", "dflash_path_select"):
+                     "dflash_verify_accept", "dflash_path_select", "dflash_sample_drafts", "dflash_sample_accept"):
             getattr(L, name).argtypes = [vp, vp, C.c_size_t, vp]
             getattr(L, name).restype = C.c_int
         L.dflash_rope_table.argtypes = [f32, i32, i32, vp, vp]
@@ -209,6 +225,14 @@ def dflash_verify_accept_noalloc(args: dflash_verify_args, status_ptr: int = 0, 
 
 def dflash_path_select(args: dflash_path_args, ws_ptr: int, ws_bytes: int, stream=None):
     _call("dflash_path_select", args, ws_ptr, ws_bytes, stream)
+
+
+def dflash_sample_drafts(args: dflash_sample_drafts_args, ws_ptr: int, ws_bytes: int, stream=None):
+    _call("dflash_sample_drafts", args, ws_ptr, ws_bytes, stream)
+
+
+def dflash_sample_accept(args: dflash_sample_accept_args, ws_ptr: int, ws_bytes: int, stream=None):
+    _call("dflash_sample_accept", args, ws_ptr, ws_bytes, stream)
 
 
 def dflash_trace_begin(max_launches: int = 4096):

@@ -274,6 +274,36 @@ class Engine:
         self.verify(self.B, self.drafts)
         self.fuse(self.B, self.commit_base, self.commit_count)
 
+    def cycle_sampled(self, T: float, seed: int, cycle: int):
+        """One cycle in sampling mode (speculative sampling at temperature T):
+        the draft's logits give drafts drawn from its distribution, the
+        target's logits the acceptance tests and the final draw.  `cycle`
+        numbers the random draws; give every cycle its own."""
+        S, B, V = self.S, self.B, self.w.vocab
+        if getattr(self, "dlogits", None) is None:
+            self.dlogits = torch.zeros(S * (B - 1), V, dtype=torch.float32, device=self.dev)
+            self.tlogits = torch.zeros(S * B, V, dtype=torch.float32, device=self.dev)
+            self.dlse = torch.zeros(S, B - 1, dtype=torch.float32, device=self.dev)
+        self.draft(self.dlogits)
+        a = D.dflash_sample_drafts_args()
+        a.dims = self.ddims
+        a.n_seqs, a.block, a.temperature, a.cycle, a.seed = S, B, T, cycle, seed
+        a.base_pos, a.draft_logits = _ptr(self.base_pos), _ptr(self.dlogits)
+        a.drafts, a.draft_lse = _ptr(self.drafts), _ptr(self.dlse)
+        D.dflash_sample_drafts(a, self.ws_ptr, self.ws_bytes)
+        self.target_forward(B, self.anchor, self.drafts)
+        D.dflash_verify_accept(self.verify_args(B, self.h, self.drafts, self.tlogits, update=False), self.ws_ptr,
+                               self.ws_bytes)
+        b = D.dflash_sample_accept_args()
+        b.dims = self.tdims
+        b.n_seqs, b.block, b.temperature, b.cycle, b.seed = S, B, T, cycle, seed
+        b.target_logits, b.draft_logits, b.draft_lse = _ptr(self.tlogits), _ptr(self.dlogits), _ptr(self.dlse)
+        b.drafts, b.base_pos, b.update_base_pos = _ptr(self.drafts), _ptr(self.base_pos), 1
+        b.accept_len, b.out_tokens, b.next_anchor = _ptr(self.accept_len), _ptr(self.out_tokens), _ptr(self.anchor)
+        b.commit_base, b.commit_count = _ptr(self.commit_base), _ptr(self.commit_count)
+        D.dflash_sample_accept(b, self.ws_ptr, self.ws_bytes)
+        self.fuse(B, self.commit_base, self.commit_count)
+
     def greedy_step(self):
         """Plain autoregressive step: one target forward of the anchor."""
         self.target_forward(1, self.anchor, taps=False)

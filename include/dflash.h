@@ -80,7 +80,9 @@ typedef enum {
   DFLASH_OP_FUSE = 2,
   DFLASH_OP_DRAFT = 3,
   DFLASH_OP_VERIFY = 4,
-  DFLASH_OP_PATH = 5
+  DFLASH_OP_PATH = 5,
+  DFLASH_OP_SAMPLE_DRAFTS = 6,
+  DFLASH_OP_SAMPLE_ACCEPT = 7
 } dflash_op;
 
 /* Shapes and arithmetic of one decoder stack. */
@@ -298,6 +300,64 @@ typedef struct {
 int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);
 
+/*
+ * Sampling-mode verification: the lossless-in-distribution variant of the
+ * greedy acceptance ("DFlash：块扩散加速的 LLM 推测解码技术", section 7: the
+ * path is walked greedily or by sampling and rejection sampling keeps the
+ * output distribution exactly the target's), i.e. speculative sampling at
+ * temperature T > 0:
+ *   q_j = softmax(draft logits of block row j / T), p_j = softmax(target
+ *   logits of block row j-1 / T): both the distribution of the token at
+ *   position P + j;
+ *   dflash_sample_drafts draws the draft d_j of every block row j >= 1 from
+ *   q_j (use the logits dflash_draft_block writes);
+ *   dflash_sample_accept accepts d_j iff log u_j < log p_j(d_j) -
+ *   log q_j(d_j), in order, stopping at the first rejection; it then emits a
+ *   draw from max(0, p_j - q_j) normalised at that row, or -- every draft
+ *   accepted -- a draw from the last target row (use the logits
+ *   dflash_verify_accept writes).
+ * Draws are Gumbel-max over the vocabulary.  Random numbers are Philox4x32-10
+ * (Salmon et al., SC'11) with key (seed low, seed high) and counter
+ * (vocabulary entry, position, sequence << 8 | purpose, cycle): give every
+ * cycle its own `cycle` value.  Reductions run in a fixed order, so a call
+ * is deterministic.  Token ids out of range raise DFLASH_ERR_INVALID_ARG in
+ * the status word.  n_seqs * block <= 1024.
+ */
+typedef struct {
+  dflash_dims dims;             /* vocab is used */
+  int32_t n_seqs, block;
+  float temperature;            /* > 0 */
+  int32_t cycle;
+  uint64_t seed;
+  const int32_t* base_pos;      /* [n_seqs] position P of block row 0 */
+  const float* draft_logits;    /* [n_seqs][block-1][V] */
+  int32_t* drafts;              /* out [n_seqs][block-1] */
+  float* draft_lse;             /* out [n_seqs][block-1]: log sum exp(logits / T) */
+} dflash_sample_drafts_args;
+int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws_bytes,
+                         dflash_stream_t stream);
+
+typedef struct {
+  dflash_dims dims;             /* vocab is used */
+  int32_t n_seqs, block;
+  float temperature;            /* > 0, as for the drafts */
+  int32_t cycle;                /* as for the drafts */
+  uint64_t seed;
+  const float* target_logits;   /* [n_seqs][block][V] */
+  const float* draft_logits;    /* [n_seqs][block-1][V] */
+  const float* draft_lse;       /* [n_seqs][block-1], from dflash_sample_drafts */
+  const int32_t* drafts;        /* [n_seqs][block-1] */
+  int32_t* base_pos;            /* in: P; out: P + accept_len + 1 when update_base_pos */
+  int32_t update_base_pos;
+  int32_t* accept_len;          /* out [n_seqs] */
+  int32_t* out_tokens;          /* out [n_seqs][block]: accepted drafts, the final draw, then -1 */
+  int32_t* next_anchor;         /* optional out [n_seqs]: the final draw */
+  int32_t* commit_base;         /* optional out [n_seqs]: P (with update_base_pos) */
+  int32_t* commit_count;        /* optional out [n_seqs]: accept_len + 1 */
+} dflash_sample_accept_args;
+int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws_bytes,
+                         dflash_stream_t stream);
+
 /* Bytes of workspace `op` needs for these arguments (args points to the
  * op's argument struct); 0 on invalid arguments. */
 size_t dflash_workspace_bytes(int32_t op, const void* args);
@@ -320,7 +380,7 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
  * the library attributes to the launches (weights + activations read and
  * written, each once), where it is known on the host; 0 otherwise.
  */
-#define DFLASH_TRACE_FAMILIES 10
+#define DFLASH_TRACE_FAMILIES 11
 typedef struct {
   char name[24];
   int32_t launches;

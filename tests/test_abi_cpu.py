@@ -45,7 +45,7 @@ def test_abi_version(D):
 def test_struct_layouts_match_c(D):
     structs = ["dflash_dims", "dflash_kv", "dflash_layer_weights", "dflash_embed_args", "dflash_layer_args",
                "dflash_fuse_args", "dflash_draft_args", "dflash_verify_args", "dflash_path_args",
-               "dflash_trace_stat"]
+               "dflash_sample_drafts_args", "dflash_sample_accept_args", "dflash_trace_stat"]
     lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void) {"]
     for s in structs:
         lines.append(f'  printf("{s} %zu\\n", sizeof({s}));')
@@ -70,7 +70,7 @@ def test_invalid_arguments_fail_before_launch(D):
     L = D.lib()
     # NULL argument structs
     for name in ("dflash_embed", "dflash_decoder_layer_forward", "dflash_fuse_context", "dflash_draft_block",
-                 "dflash_verify_accept", "dflash_path_select"):
+                 "dflash_verify_accept", "dflash_path_select", "dflash_sample_drafts", "dflash_sample_accept"):
         assert getattr(L, name)(None, None, 0, None) == D.DFLASH_ERR_INVALID_ARG
         assert "NULL args" in D.dflash_last_error()
     # bad dims
