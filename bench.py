@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--trace-replays", type=int, default=5)
+    p.add_argument("--no-sampling", action="store_true", help="skip the sampling-mode cycle timing")
     p.add_argument("--layers", default="", help="T,D: shrink to T target / D draft layers (profiling captures "
                    "only; the line then names the reduced config)")
     return p.parse_args()
@@ -419,6 +420,37 @@ def run_ours(args):
     mean_accept = float(accept.float().mean())
     value, verified = job_rates(world, S, args.steps, ms, float((accept + 1).sum()))
 
+    # the same cycle in sampling mode (speculative sampling at T = 1), graph replay
+    sampling = None
+    if eng.has_target and not args.no_sampling:
+        def step_sampled():
+            eng.base_pos.copy_(base0)
+            eng.anchor.copy_(anchor0)
+            eng.cycle_sampled(1.0, 0x5EED, 0)
+
+        step_sampled()
+        torch.cuda.synchronize()
+        assert eng.status() == D.DFLASH_OK
+        sgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sgraph):
+            step_sampled()
+        for _ in range(args.warmup):
+            sgraph.replay()
+        n_s = max(3, min(args.steps, 50))
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_s):
+            sgraph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_s = reduce_max(e0.elapsed_time(e1), world, "cuda") / n_s
+        sampling = {"mode": "speculative sampling, temperature 1.0 (Philox4x32-10 draws)",
+                    "ms_per_step": ms_s, "value": world * S * 1000.0 / ms_s, "unit": UNIT, "steps": n_s,
+                    "overhead_vs_greedy": ms_s / ms_per_step - 1.0}
+        del sgraph
+        eng.base_pos.copy_(base0)
+        eng.anchor.copy_(anchor0)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -481,7 +513,7 @@ def run_ours(args):
             "verified_tok_s": verified, "mean_accept": mean_accept,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-            "clocks": clocks, "kernels": per_fam}
+            "clocks": clocks, "kernels": per_fam, "sampling": sampling}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
