@@ -15,13 +15,22 @@
 //
 // bf16 path: a thread-block cluster of NC CTAs per (sequence, kv head, query
 // tile).  CTA rank r owns chunks r, r + NC, r + 2 NC, ... (CH = 128 key slots
-// each, at fixed absolute offsets), streams them through double-buffered
-// cp.async into XOR-swizzled shared memory, and runs mma.sync m16n8k16 tiles
-// (S = Q K^T, O = P V with P rounded to bf16) with an online softmax over its
-// chunks in order.  The NC partials are then merged in rank order through
-// distributed shared memory; cluster barriers are hardware barriers over
-// co-scheduled CTAs, so nothing spins and nothing round-trips through HBM.
+// each, at fixed absolute offsets), streams them through double-buffered TMA
+// loads (128-byte swizzled boxes) and runs mma.sync m16n8k16 tiles with an
+// online softmax over its chunks in order: S = Q K^T, then O += P V with P
+// carried as a bf16 pair (hi + lo) so the product keeps about 16 bits of P.
+// The NC partials are then merged in rank order through distributed shared
+// memory; cluster barriers are hardware barriers over co-scheduled CTAs, so
+// nothing spins and nothing round-trips through HBM.
+//
+// A second bf16 kernel for head dimension 128 (attn_tc_kernel, chosen with
+// DFLASH_ATTN_TCGEN05=1) computes the same function on the tcgen05 tensor
+// cores: S and O are TMEM accumulators, the 64 query rows are duplicated into
+// MMA rows 64..127 so that four softmax warps each take one query row and one
+// half of the chunk's keys, and the partials merge through the same cluster
+// path.
 #include <cooperative_groups.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -291,6 +300,69 @@ struct AttnTma {
 // two (D = 128) or one (D = 64) TMA boxes of 64 dims with 128-byte swizzle.
 __device__ __forceinline__ uint32_t kv_off(int j, int ch) {
   return (uint32_t)((ch >> 3) * (kMmaCH * 128) + j * 128 + (((ch & 7) ^ (j & 7)) << 4));
+}
+
+// Merge of the NC rank partials of one 64-query tile, in rank order; rank r
+// writes rows [r*RP, (r+1)*RP) of the tile.  psm: this CTA's partial
+// [64][D+4] (O, then m and l, log2 units), read by every rank through
+// distributed shared memory; scratch: local shared memory.  The per-(row,
+// rank) weights are formed once; then every output element reads its NC
+// partial values with independent loads.
+template <int D>
+__device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, float* scratch, int NC, int rank,
+                                           int nq_tile, int qv0, int grp, int g, int s, int rows, int QD,
+                                           void* out) {
+  constexpr int PST = D + 4;
+  const int RP = (nq_tile + NC - 1) / NC;
+  const int q_lo = rank * RP;
+  const int nrow = max(0, min(nq_tile, q_lo + RP) - q_lo);
+  float* mw = scratch;               // [RP][kMaxNC] partial maxima, then weights
+  float* lw = mw + RP * kMaxNC;      // [RP][kMaxNC] partial sums
+  float* Ls = lw + RP * kMaxNC;      // [RP] merged sums
+  for (int t = threadIdx.x; t < nrow * NC; t += blockDim.x) {
+    const int i = t / NC, r = t % NC;
+    const float* pr = cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST;
+    mw[i * kMaxNC + r] = pr[D];
+    lw[i * kMaxNC + r] = pr[D + 1];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nrow; i += blockDim.x) {
+    float M = -INFINITY;
+    for (int r = 0; r < NC; ++r) M = fmaxf(M, mw[i * kMaxNC + r]);
+    float L = 0.f;
+    for (int r = 0; r < NC; ++r) {
+      const float mr = mw[i * kMaxNC + r];
+      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+      mw[i * kMaxNC + r] = w;
+      L = fmaf(lw[i * kMaxNC + r], w, L);
+    }
+    Ls[i] = L;
+  }
+  __syncthreads();
+  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(out);
+  for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
+    const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
+    float4 v[kMaxNC];
+#pragma unroll
+    for (int r = 0; r < kMaxNC; ++r)
+      if (r < NC) v[r] = *reinterpret_cast<const float4*>(cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST + e4);
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxNC; ++r)
+      if (r < NC) {
+        const float w = mw[i * kMaxNC + r];
+        o0 = fmaf(v[r].x, w, o0);
+        o1 = fmaf(v[r].y, w, o1);
+        o2 = fmaf(v[r].z, w, o2);
+        o3 = fmaf(v[r].w, w, o3);
+      }
+    const float L = Ls[i];
+    const int qv = qv0 + q_lo + i;
+    const int row = qv / grp, head = g * grp + qv % grp;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
+    dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
+    dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
+  }
 }
 
 template <int D>
@@ -592,59 +664,375 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
   }
   cl.sync();
 
-  // ---- merge the NC partials in rank order; rank r owns rows [r*RP, (r+1)*RP).
-  // The per-(row, rank) weights are formed once; then every output element
-  // reads its NC partial values with independent loads.
-  const int RP = (nq_tile + NC - 1) / NC;
-  const int q_lo = rank * RP;
-  const int nrow = max(0, min(nq_tile, q_lo + RP) - q_lo);
-  float* mw = qsm;                   // [RP][kMaxNC] partial maxima, then weights
-  float* lw = mw + RP * kMaxNC;      // [RP][kMaxNC] partial sums
-  float* Ls = lw + RP * kMaxNC;      // [RP] merged sums
-  for (int t = threadIdx.x; t < nrow * NC; t += blockDim.x) {
-    const int i = t / NC, r = t % NC;
-    const float* pr = cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST;
-    mw[i * kMaxNC + r] = pr[D];
-    lw[i * kMaxNC + r] = pr[D + 1];
+  rank_merge<D>(cl, psm, qsm, NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
+  cl.sync();  // peers keep their shared memory until every rank has read it
+}
+
+// ---------------------------------------------------------- tcgen05 variant
+//
+// Same work split as attn_cluster_kernel (one cluster of NC CTAs per
+// (sequence, KV head, 64-query tile), rank r owns chunks r, r+NC, ...), with
+// both products on the 5th-generation tensor cores: per 128-key chunk
+// S = Q K^T (M = 128 query rows, the 64 of the tile padded with zeros; N =
+// 128 keys; K = 128 dims) into one of two TMEM accumulators, the softmax in
+// the two warps that own TMEM lanes 0..63 (one query row per thread), P
+// written to shared memory as a bf16 pair (P_hi, P_lo), the running output
+// O rescaled in TMEM, then O += P_hi V + P_lo V (V as an MN-major operand).
+// Roles: warp 0 issues the K/V TMA copies, one lane of warp 1 the MMAs,
+// warps 4-5 the softmax; S of chunk i+1 is computed while the softmax of
+// chunk i runs.  Every wait is bounded.
+constexpr int kTcAttnThreads = 192;
+constexpr int kTcAttnRows = 128;  // MMA rows (the 64-query tile, padded)
+
+__host__ __device__ constexpr size_t tc_attn_smem(int d) {
+  return 4 * (size_t)kMmaCH * d * 2           // two K/V chunk buffers
+         + (size_t)kTcAttnRows * d * 2          // Q
+         + 2 * (size_t)kTcAttnRows * kMmaCH * 2 // P_hi, P_lo
+         + 128 + 4 * 64 * 4 + 1024;             // barriers, row max / sum exchange, alignment
+}
+
+// Byte offset of (row, 16-byte chunk) in a [128 rows][64 x nbox] bf16 operand
+// stored as nbox 128-byte swizzled boxes of 128 rows (the TMA layout).
+__device__ __forceinline__ uint32_t op_off(int row, int ch) {
+  return (uint32_t)((ch >> 3) * (kTcAttnRows * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTma p, int n_qt) {
+  static_assert(D == 128, "two 64-dim boxes per row");
+  constexpr int CH = kMmaCH;
+  constexpr int TILE = CH * D * 2;
+  constexpr int QB = kTcAttnRows * D * 2;
+  constexpr int PB = kTcAttnRows * CH * 2;
+  constexpr int PST = D + 4;
+  extern __shared__ __align__(1024) uint8_t smem_att[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_att) + 1023) & ~uintptr_t(1023));
+  uint8_t* KV = sm;  // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
+  uint8_t* Qs = KV + 4 * TILE;
+  uint8_t* Ph = Qs + QB;
+  uint8_t* Pl = Ph + PB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(Pl + PB);  // [2] K/V chunk landed
+  uint64_t* empty = full + 2;                             // [2] K/V chunk consumed
+  uint64_t* sfull = empty + 2;                            // [2] S in TMEM
+  uint64_t* pdone = sfull + 2;                            // [2] P written, O rescaled
+  uint64_t* ofull = pdone + 2;                            // P V done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(ofull + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+  float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ofull) + 64);  // [2 halves][64 rows]
+  float* xsum = xmax + 2 * 64;                                                      // [2 halves][64 rows]
+  float* psm = reinterpret_cast<float*>(sm);   // [64][PST] CTA partial (after the chunk loop)
+  float* scr = psm + kClQT * PST;              // merge scratch
+
+  const AttnDesc& a = p.a;
+  cg::cluster_group cl = cg::this_cluster();
+  const int NC = (int)cl.num_blocks();
+  const int rank = (int)cl.block_rank();
+  const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
+  const int s = blockIdx.z;
+  const int mode = a.mode, rows = a.rows, cap = a.cap, nkv = a.nkv;
+  const int grp = a.nq / a.nkv;
+  const int nqv = rows * grp;
+  const int QD = a.nq * D;
+  uint32_t* status = a.status;
+  // base_pos is written only by the acceptance step, never by the kernel that
+  // precedes attention inside a call, so it may be read before the PDL wait.
+  const int P = a.base_pos[s];
+  SeqKeys sk;
+  if (mode == DFLASH_ATTN_CAUSAL) {
+    sk.n_ctx = min(max(P + rows, 0), cap);
+    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
+    sk.n_ch = sk.n_ctx_ch;
+  } else {
+    sk.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), cap);
+    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
+    sk.n_ch = sk.n_ctx_ch + 1;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < nrow; i += blockDim.x) {
-    float M = -INFINITY;
-    for (int r = 0; r < NC; ++r) M = fmaxf(M, mw[i * kMaxNC + r]);
-    float L = 0.f;
-    for (int r = 0; r < NC; ++r) {
-      const float mr = mw[i * kMaxNC + r];
-      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
-      mw[i * kMaxNC + r] = w;
-      L = fmaf(lw[i * kMaxNC + r], w, L);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int qv0 = qt * kClQT;
+  const int nq_tile = min(kClQT, nqv - qv0);
+  const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
+
+  auto chunk_row = [&](int c, bool& blk) -> int {
+    blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
+    return blk ? (s * nkv + g) * rows : (s * nkv + g) * cap + c * CH;
+  };
+  auto issue = [&](int c, int buf) {  // one thread
+    bool blk;
+    const int row = chunk_row(c, blk);
+    const CUtensorMap* km = blk ? &p.kb : &p.kc;
+    const CUtensorMap* vm = blk ? &p.vb : &p.vc;
+    uint8_t* Kt = KV + 2 * buf * TILE;
+    tc::mbar_arrive_expect_tx(&full[buf], 2 * TILE);
+    const uint64_t pol = tc::policy_evict_first();
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tc::tma_load_2d(Kt + h * (CH * 128), km, 64 * h, row, &full[buf], pol);
+      tc::tma_load_2d(Kt + TILE + h * (CH * 128), vm, 64 * h, row, &full[buf], pol);
     }
-    Ls[i] = L;
+  };
+  auto early_ok = [&](int c) { return c < sk.n_ctx_ch && (mode == DFLASH_ATTN_BLOCK_BIDIR || (c + 1) * CH <= P); };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&full[b], 1);
+      tc::mbar_init(&empty[b], 1);
+      tc::mbar_init(&sfull[b], 1);
+      tc::mbar_init(&pdone[b], 1);
+    }
+    tc::mbar_init(ofull, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&p.kc);
+    tc::tma_prefetch_desc(&p.vc);
   }
+  if (warp == 1) tc::tmem_alloc(tslot, 512);
+  tc::tc_fence_before();
   __syncthreads();
-  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out);
-  for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
-    const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
-    float4 v[kMaxNC];
-#pragma unroll
-    for (int r = 0; r < kMaxNC; ++r)
-      if (r < NC) v[r] = *reinterpret_cast<const float4*>(cl.map_shared_rank(psm, r) + (size_t)(q_lo + i) * PST + e4);
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxNC; ++r)
-      if (r < NC) {
-        const float w = mw[i * kMaxNC + r];
-        o0 = fmaf(v[r].x, w, o0);
-        o1 = fmaf(v[r].y, w, o1);
-        o2 = fmaf(v[r].z, w, o2);
-        o3 = fmaf(v[r].w, w, o3);
-      }
-    const float L = Ls[i];
-    const int qv = qv0 + q_lo + i;
-    const int row = qv / grp, head = g * grp + qv % grp;
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
-    dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
-    dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  bool pre0 = false, pre1 = false;
+  if (threadIdx.x == 0) {
+    if (nmine > 0 && early_ok(rank)) { issue(rank, 0); pre0 = true; }
+    if (nmine > 1 && early_ok(rank + NC)) { issue(rank + NC, 1); pre1 = true; }
   }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    if (nmine > 0 && !pre0) issue(rank, 0);
+    if (nmine > 1 && !pre1) issue(rank + NC, 1);
+  }
+  // ---- Q: the tile's query vectors in rows 0..nq_tile-1 and again in rows
+  // 64.., zero elsewhere (TMEM lanes 64..127 then hold a copy of every score
+  // row, so four warps share the softmax: one key half each)
+  const uint32_t qb = __cvta_generic_to_shared(Qs);
+  for (int t = threadIdx.x; t < kTcAttnRows * (D / 8); t += blockDim.x) {
+    const int qrow = t / (D / 8), ch = t % (D / 8);
+    const int qi = qrow & (kClQT - 1);
+    if (qi < nq_tile) {
+      const int qv = qv0 + qi;
+      const int row = qv / grp, head = g * grp + qv % grp;
+      const __nv_bfloat16* q =
+          reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * rows + row) * QD + (size_t)head * D;
+      cp_async16(qb + op_off(qrow, ch), q + ch * 8);
+    } else {
+      *reinterpret_cast<uint4*>(Qs + op_off(qrow, ch)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  cp_async_wait_all();
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+
+  const uint32_t kvb = __cvta_generic_to_shared(KV);
+  const uint32_t phb = __cvta_generic_to_shared(Ph), plb = __cvta_generic_to_shared(Pl);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- K/V producer: chunk i into buffer i & 1 once P V of chunk i-2 is done
+      for (int i = 2; i < nmine; ++i) {
+        if (!tc::mbar_wait(&empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          break;
+        }
+        issue(rank + i * NC, i & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idS = tc::idesc_bf16_f32(kTcAttnRows, CH);
+      constexpr uint32_t idV = tc::idesc_bf16_f32_bmn(kTcAttnRows, D);
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (ok && !tc::mbar_wait(bar, par, abort)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          ok = false;
+        }
+        return ok;
+      };
+      auto issue_s = [&](int i) {
+        const int b = i & 1;
+        if (!wait(&full[b], (uint32_t)(i >> 1) & 1u)) return;
+        tc::tc_fence_after();
+        const uint32_t kb = kvb + 2 * b * TILE;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t off = (uint32_t)((j >> 2) * (kTcAttnRows * 128) + (j & 3) * 32);
+          const uint32_t koff = (uint32_t)((j >> 2) * (CH * 128) + (j & 3) * 32);
+          tc::mma_bf16(tmem + (uint32_t)(b * CH), tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + koff), idS,
+                       j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull[b]);
+      };
+      // S of the first two chunks up front; then P V of chunk i as soon as its
+      // P is written, and S of chunk i+2 after it (its K/V buffer and S
+      // accumulator are the ones chunk i used), so that a chunk's load
+      // latency hides behind the softmax of the chunk before it.
+      if (nmine > 0) issue_s(0);
+      if (nmine > 1) issue_s(1);
+      for (int i = 0; i < nmine && ok; ++i) {
+        if (!wait(&pdone[i & 1], (uint32_t)(i >> 1) & 1u)) break;
+        tc::tc_fence_after();
+        const uint32_t vb = kvb + (2 * (i & 1) + 1) * TILE;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t pb = half ? plb : phb;
+#pragma unroll
+          for (int j = 0; j < CH / 16; ++j) {
+            const uint32_t poff = (uint32_t)((j >> 2) * (kTcAttnRows * 128) + (j & 3) * 32);
+            tc::mma_bf16(tmem + 2u * CH, tc::sdesc_sw128(pb + poff),
+                         tc::sdesc_sw128_mn(vb + (uint32_t)j * 2048u, CH * 128, 1024), idV,
+                         (i > 0 || half > 0 || j > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&empty[i & 1]);
+        tc::mma_commit(ofull);
+        if (i + 2 < nmine) issue_s(i + 2);
+      }
+    }
+  } else {
+    // ---------------- softmax, warps 2..5: TMEM lane L holds score row L;
+    // rows 0..63 and their copies 64..127 are the same query row q = L & 63.
+    // The thread of lane L takes key half h = L >> 6 of row q; the two halves
+    // exchange their row maximum and sum in shared memory (fixed order).
+    const int L = (warp & 3) * 32 + lane;
+    const int qr = L & (kClQT - 1), h = L >> 6;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const bool o_owner = h == 0;  // lanes 0..63 also own the output row in TMEM
+    const int row_tok = (qv0 + qr) / grp;
+    const float scale = rsqrtf((float)D) * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int i = 0; i < nmine; ++i) {
+      const int c = rank + i * NC, b = i & 1;
+      bool blk;
+      chunk_row(c, blk);
+      const int slot0 = blk ? -1 : c * CH;
+      const int nk = blk ? min(rows, CH) : min(CH, sk.n_ctx - c * CH);
+      const bool causal = mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
+      const int lim = causal ? P + row_tok - slot0 : CH;
+      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
+      }
+      __syncwarp();  // the TMEM loads below are warp-collective
+      tc::tc_fence_after();
+      float sc[CH / 2];
+#pragma unroll
+      for (int q = 0; q < CH / 32; ++q) {
+        float t16[16];
+        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + h * (CH / 2) + q * 16), t16);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const int j = h * (CH / 2) + q * 16 + t;  // key index in the chunk
+          sc[q * 16 + t] = (j < nk && j <= lim) ? t16[t] * scale : -INFINITY;
+        }
+      }
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < CH / 2; ++j) cmax = fmaxf(cmax, sc[j]);
+      xmax[h * 64 + qr] = cmax;
+      tc::named_bar(2, 128);
+      const float m_new = fmaxf(m_run, fmaxf(xmax[qr], xmax[64 + qr]));
+      const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < CH / 2; ++j) {
+        const float pj = (sc[j] == -INFINITY) ? 0.f : exp2f(sc[j] - m_new);
+        sc[j] = pj;
+        sum += pj;
+      }
+      xsum[h * 64 + qr] = sum;
+      // P = P_hi + P_lo: this thread's 64 keys of row q, 8 per 16-byte chunk
+#pragma unroll
+      for (int cc = 0; cc < CH / 16; ++cc) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16(sc[8 * cc + 2 * e], sc[8 * cc + 2 * e + 1], hi[e], lo[e]);
+        const int ch = h * (CH / 16) + cc;
+        *reinterpret_cast<uint4*>(Ph + op_off(qr, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(Pl + op_off(qr, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      if (nk < CH) {
+        // Rows past the last key hold whatever follows in memory (unwritten
+        // cache slots may be NaN); zero V there so that P = 0 contributes 0.
+        uint8_t* Vt = KV + (2 * b + 1) * TILE;
+        for (int t = L; t < (CH - nk) * (D / 8); t += 128) {
+          const int j = nk + t / (D / 8), ch = t % (D / 8);
+          *reinterpret_cast<uint4*>(Vt + kv_off(j, ch)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc::named_bar(2, 128);
+      l_run = fmaf(l_run, alpha, xsum[qr] + xsum[64 + qr]);
+      // O (lanes 0..63) holds the chunks before this one: rescale it to the
+      // new maximum.  TMEM accesses are warp-collective: the whole warp takes
+      // the branch when any of its rows needs it (alpha = 1 keeps a row).
+      if (o_owner && i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          ok = false;
+        }
+        __syncwarp();
+        tc::tc_fence_after();
+#pragma unroll 1
+        for (int q = 0; q < D / 16; ++q) {
+          float o16[16];
+          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) o16[t] *= alpha;
+          tc::tmem_st16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+        }
+      }
+      m_run = m_new;
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::named_bar(2, 128);  // also: xmax / xsum are rewritten by the next chunk
+      if (L == 0) tc::mbar_arrive(&pdone[b]);
+    }
+    // ---- this CTA's partial of its 64 rows (lanes 0..63)
+    if (o_owner) {
+      float* pr = psm + (size_t)qr * PST;
+      if (nmine > 0) {
+        if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          ok = false;
+        }
+        __syncwarp();
+        tc::tc_fence_after();
+      }
+    }
+    // psm overlays the K/V buffers: every MMA (the last P V) has completed here
+    tc::named_bar(2, 128);
+    if (o_owner) {
+      float* pr = psm + (size_t)qr * PST;
+#pragma unroll 1
+      for (int q = 0; q < D / 16; ++q) {
+        float o16[16];
+        if (nmine > 0) {
+          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) o16[t] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; t += 4)
+          *reinterpret_cast<float4*>(pr + q * 16 + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
+      }
+      pr[D] = m_run;
+      pr[D + 1] = l_run;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+  cl.sync();
+  rank_merge<D>(cl, psm, scr, NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
   cl.sync();  // peers keep their shared memory until every rank has read it
 }
 
@@ -714,6 +1102,24 @@ int pick_nc(long groups) {
   return 8;
 }
 
+// Tensor maps of the context cache and (bidirectional mode) the block K/V:
+// [rows][D] bf16, boxes of 64 dims x 128 keys, 128-byte swizzle.
+template <int D>
+bool attn_maps(const AttnDesc& a, AttnTma& p) {
+  memset(&p, 0, sizeof(p));
+  p.a = a;
+  const uint64_t crow = (uint64_t)a.n_seqs * a.nkv * a.cap;
+  if (!make_tmap_bf16(&p.kc, a.kc, D, crow, kMmaCH) || !make_tmap_bf16(&p.vc, a.vc, D, crow, kMmaCH)) return false;
+  if (a.mode == DFLASH_ATTN_BLOCK_BIDIR) {
+    const uint64_t brow = (uint64_t)a.n_seqs * a.nkv * a.rows;
+    if (!make_tmap_bf16(&p.kb, a.kb, D, brow, kMmaCH) || !make_tmap_bf16(&p.vb, a.vb, D, brow, kMmaCH)) return false;
+  } else {
+    p.kb = p.kc;
+    p.vb = p.vc;
+  }
+  return true;
+}
+
 template <int D>
 cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   auto k = attn_cluster_kernel<D>;
@@ -722,22 +1128,30 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   AttnTma p;
-  memset(&p, 0, sizeof(p));
-  p.a = a;
-  const uint64_t crow = (uint64_t)a.n_seqs * a.nkv * a.cap;
-  if (!make_tmap_bf16(&p.kc, a.kc, D, crow, kMmaCH) || !make_tmap_bf16(&p.vc, a.vc, D, crow, kMmaCH))
-    return cudaErrorInvalidValue;
-  if (a.mode == DFLASH_ATTN_BLOCK_BIDIR) {
-    const uint64_t brow = (uint64_t)a.n_seqs * a.nkv * a.rows;
-    if (!make_tmap_bf16(&p.kb, a.kb, D, brow, kMmaCH) || !make_tmap_bf16(&p.vb, a.vb, D, brow, kMmaCH))
-      return cudaErrorInvalidValue;
-  } else {
-    p.kb = p.kc;
-    p.vb = p.vc;
-  }
+  if (!attn_maps<D>(a, p)) return cudaErrorInvalidValue;
   const int nc = pick_nc<D>((long)a.nkv);
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
+  return cudaLaunchKernelEx(&cfg, k, p, n_qt);
+}
+
+// The tcgen05 variant: the cluster width comes from the same residency
+// query (both kernels hold one CTA per SM), so it too depends on the KV-head
+// count and the device only.
+template <int D>
+cudaError_t launch_tc(const AttnDesc& a, int n_qt, cudaStream_t st) {
+  auto k = attn_tc_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_attn_smem(D));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  AttnTma p;
+  if (!attn_maps<D>(a, p)) return cudaErrorInvalidValue;
+  const int nc = pick_nc<D>((long)a.nkv);
+  cudaLaunchAttribute at[2];
+  cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
+  cfg.blockDim = dim3(kTcAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc_attn_smem(D);
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 
@@ -749,11 +1163,24 @@ size_t attn_workspace(const AttnDesc& a) {
   return (size_t)a.n_seqs * a.nkv * g.n_qt * g.nch * kAttnQT * (a.d + 2) * sizeof(float);
 }
 
+// The tcgen05 attention kernel is chosen with DFLASH_ATTN_TCGEN05=1 in the
+// environment (read once per process).  It computes the same function; in
+// the whole cycle at 16 block rows the mma.sync kernel measured faster, so
+// it is the default.
+static bool use_tc_attention() {
+  static const bool on = [] {
+    const char* v = getenv("DFLASH_ATTN_TCGEN05");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   AttnGeom g = attn_geom(a);
   if (a.n_seqs == 0 || a.rows == 0) return cudaSuccess;
   if (a.dtype == DFLASH_BF16) {
     const int n_qt = (g.nqv + kClQT - 1) / kClQT;
+    if (a.d == 128 && use_tc_attention()) return launch_tc<128>(a, n_qt, st);
     return a.d == 128 ? launch_cluster<128>(a, n_qt, st) : launch_cluster<64>(a, n_qt, st);
   }
   dim3 grid(g.nch, a.nkv * g.n_qt, a.n_seqs);

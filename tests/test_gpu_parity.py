@@ -372,3 +372,32 @@ def test_path_select_entry_point():
                 if mg[j] < 1e-4:
                     break
                 assert gp[s, j] == op[j]
+
+
+@pytest.mark.parametrize("mode", ["causal", "bidir"])
+def test_long_context_layer(mode):
+    """A 4k-position context at small hidden sizes with d = 128: every rank
+    of the attention cluster owns two or more key chunks, so the running
+    maximum, the rescale of the accumulated output and the chunk-buffer reuse
+    all take part."""
+    w = small("bf16", d=128)
+    S, rows = 2, 8
+    cap = 4224
+    eng, om, _ = G.setup(w, S=S, cap=cap)
+    c, L = om.target.cfg, om.target.layers[1]
+    base = [4100, 2600]
+    eng.base_pos.copy_(torch.tensor(base, dtype=torch.int32))
+    kc, vc = rand_cache(eng, eng.caches.tk[1], eng.caches.tv[1], S, 4100, 5, c)
+    h0 = torch.randn(S * rows, w.target.hidden, generator=torch.Generator().manual_seed(6))
+    eng.h[:S * rows].copy_(h0.cuda())
+    a = eng.target_layer_args(1, rows, eng.h)
+    if mode == "bidir":
+        a.attn_mode = D.DFLASH_ATTN_BLOCK_BIDIR
+    D.dflash_decoder_layer_forward(a, eng.ws_ptr, eng.ws_bytes)
+    torch.cuda.synchronize()
+    assert eng.status() == D.DFLASH_OK
+    got = G.f64(eng.h[:S * rows])
+    for s in range(S):
+        hs = h0[s * rows:(s + 1) * rows].double().numpy().copy()
+        O.decoder_layer(c, L, hs, base[s], O.CAUSAL if mode == "causal" else O.BIDIR, kc[s].copy(), vc[s].copy())
+        np.testing.assert_allclose(got[s * rows:(s + 1) * rows], hs, rtol=0, atol=2e-2)
