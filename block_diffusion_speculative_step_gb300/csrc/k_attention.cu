@@ -673,16 +673,17 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
 // Same work split as attn_cluster_kernel (one cluster of NC CTAs per
 // (sequence, KV head, 64-query tile), rank r owns chunks r, r+NC, ...), with
 // both products on the 5th-generation tensor cores: per 128-key chunk
-// S = Q K^T (M = 128 query rows, the 64 of the tile padded with zeros; N =
-// 128 keys; K = 128 dims) into one of two TMEM accumulators, the softmax in
-// the two warps that own TMEM lanes 0..63 (one query row per thread), P
-// written to shared memory as a bf16 pair (P_hi, P_lo), the running output
-// O rescaled in TMEM, then O += P_hi V + P_lo V (V as an MN-major operand).
-// Roles: warp 0 issues the K/V TMA copies, one lane of warp 1 the MMAs,
-// warps 4-5 the softmax; S of chunk i+1 is computed while the softmax of
+// S = Q K^T (M = 128 MMA rows: the 64 query rows of the tile, then the same
+// 64 again; N = 128 keys; K = 128 dims) into one of two TMEM accumulators.
+// Four softmax warps (2..5) read S: the thread on TMEM lane l takes query row
+// l mod 64 and key half l / 64, and the two halves exchange their maxima and
+// sums through shared memory.  P goes to shared memory as a bf16 pair (P_hi,
+// P_lo), the running output O is rescaled in TMEM, then O += P_hi V + P_lo V
+// (V as an MN-major operand).  Roles: warp 0 issues the K/V TMA copies, one
+// lane of warp 1 the MMAs; S of chunk i+1 is computed while the softmax of
 // chunk i runs.  Every wait is bounded.
 constexpr int kTcAttnThreads = 192;
-constexpr int kTcAttnRows = 128;  // MMA rows (the 64-query tile, padded)
+constexpr int kTcAttnRows = 128;  // MMA rows (the 64-query tile, twice)
 
 __host__ __device__ constexpr size_t tc_attn_smem(int d) {
   return 4 * (size_t)kMmaCH * d * 2           // two K/V chunk buffers
@@ -944,6 +945,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         sum += pj;
       }
       xsum[h * 64 + qr] = sum;
+      // P has one buffer: the P V products of the chunk before must have
+      // finished reading it (S of this chunk was issued ahead of them).
+      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
+      }
       // P = P_hi + P_lo: this thread's 64 keys of row q, 8 per 16-byte chunk
 #pragma unroll
       for (int cc = 0; cc < CH / 16; ++cc) {
@@ -968,12 +976,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // O (lanes 0..63) holds the chunks before this one: rescale it to the
       // new maximum.  TMEM accesses are warp-collective: the whole warp takes
       // the branch when any of its rows needs it (alpha = 1 keeps a row).
+      // (The P V products of the chunk before have completed: waited above.)
       if (o_owner && i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort)) {
-          raise_status(status, ST_TIMEOUT);
-          *abort = 1;
-          ok = false;
-        }
         __syncwarp();
         tc::tc_fence_after();
 #pragma unroll 1
@@ -993,7 +997,6 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     }
     // ---- this CTA's partial of its 64 rows (lanes 0..63)
     if (o_owner) {
-      float* pr = psm + (size_t)qr * PST;
       if (nmine > 0) {
         if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort)) {
           raise_status(status, ST_TIMEOUT);
