@@ -23,12 +23,12 @@
 // memory; cluster barriers are hardware barriers over co-scheduled CTAs, so
 // nothing spins and nothing round-trips through HBM.
 //
-// A second bf16 kernel for head dimension 128 (attn_tc_kernel, chosen with
-// DFLASH_ATTN_TCGEN05=1) computes the same function on the tcgen05 tensor
-// cores: S and O are TMEM accumulators, the 64 query rows are duplicated into
-// MMA rows 64..127 so that four softmax warps each take one query row and one
-// half of the chunk's keys, and the partials merge through the same cluster
-// path.
+// For head dimension 128 the bf16 path runs attn_tc_kernel instead, which
+// computes the same function on the tcgen05 tensor cores: S and O are TMEM
+// accumulators, the 64 query rows are duplicated into MMA rows 64..127 so
+// that the softmax warps on all four TMEM lane quadrants share the rows, and
+// the partials merge through the same cluster path.  DFLASH_ATTN_MMASYNC=1 in
+// the environment selects the mma.sync kernel for head dimension 128 too.
 #include <cooperative_groups.h>
 #include <stdlib.h>
 
@@ -675,21 +675,44 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
 // both products on the 5th-generation tensor cores: per 128-key chunk
 // S = Q K^T (M = 128 MMA rows: the 64 query rows of the tile, then the same
 // 64 again; N = 128 keys; K = 128 dims) into one of two TMEM accumulators.
-// Four softmax warps (2..5) read S: the thread on TMEM lane l takes query row
-// l mod 64 and key half l / 64, and the two halves exchange their maxima and
-// sums through shared memory.  P goes to shared memory as a bf16 pair (P_hi,
-// P_lo), the running output O is rescaled in TMEM, then O += P_hi V + P_lo V
-// (V as an MN-major operand).  Roles: warp 0 issues the K/V TMA copies, one
-// lane of warp 1 the MMAs; S of chunk i+1 is computed while the softmax of
-// chunk i runs.  Every wait is bounded.
-constexpr int kTcAttnThreads = 192;
-constexpr int kTcAttnRows = 128;  // MMA rows (the 64-query tile, twice)
+// The softmax warps (eight: 2..9), four per key group and one of each group
+// on every TMEM lane quadrant, read S: the thread on TMEM lane l of key group
+// k takes query row l mod 64 and the KP = 32 keys of piece 2k + l / 64, so
+// every row is shared by 4 threads, which exchange their maxima and sums
+// through shared memory in piece order.  P
+// goes to shared memory as a bf16 pair (P_hi, P_lo), the running output O is
+// rescaled in TMEM, then O += P_hi V + P_lo V (V as an MN-major operand).
+// Roles: warp 0 issues the K/V TMA copies, one lane of warp 1 the MMAs; S of
+// chunk i+1 is computed while the softmax of chunk i runs.  Every wait is
+// bounded.
+// Eight softmax warps (KP = 32 keys per thread) measured faster than sixteen
+// (which need more than a quarter of the register file per sub-partition and
+// spill) and than four (latency-bound).
+#ifndef DFLASH_TC_ATTN_SOFT_WARPS
+#define DFLASH_TC_ATTN_SOFT_WARPS 8
+#endif
+constexpr int kTcAttnSoftWarps = DFLASH_TC_ATTN_SOFT_WARPS;  // 4 per TMEM lane quadrant x key groups
+constexpr int kTcAttnSoft = kTcAttnSoftWarps * 32;
+constexpr int kTcAttnThreads = 64 + kTcAttnSoft;
+constexpr int kTcAttnRows = 128;                          // MMA rows (the 64-query tile, twice)
+constexpr int kTcAttnGroups = kTcAttnSoftWarps / 4;       // key groups
+constexpr int kTcAttnPieces = 2 * kTcAttnGroups;          // key pieces of a chunk (x 2 row copies)
+constexpr int kTcAttnKP = kMmaCH / kTcAttnPieces;         // keys per softmax thread
+static_assert(kTcAttnSoftWarps % 4 == 0 && kTcAttnKP % 16 == 0, "whole 16-column TMEM loads");
+// P_hi and P_lo are [128 rows][128 keys] operands (two 64-key boxes of 128
+// rows), but only rows 0..63 are ever written: P_lo starts 64 rows after P_hi,
+// so the rows 64..127 the PV MMA reads (and whose output is discarded) fall on
+// the other operand's live rows, and the pair takes 40 KB instead of 64.
+constexpr int kTcAttnPloOff = 64 * 128;
+constexpr int kTcAttnPBytes = kTcAttnPloOff + 2 * kTcAttnRows * 128;
 
 __host__ __device__ constexpr size_t tc_attn_smem(int d) {
-  return 4 * (size_t)kMmaCH * d * 2           // two K/V chunk buffers
+  return 4 * (size_t)kMmaCH * d * 2             // two K/V chunk buffers
          + (size_t)kTcAttnRows * d * 2          // Q
-         + 2 * (size_t)kTcAttnRows * kMmaCH * 2 // P_hi, P_lo
-         + 128 + 4 * 64 * 4 + 1024;             // barriers, row max / sum exchange, alignment
+         + (size_t)kTcAttnPBytes                // P_hi, P_lo
+         + 128                                  // barriers
+         + 2 * 2 * kTcAttnPieces * 64 * 4       // row max / sum exchange, double-buffered
+         + 1024;                                // alignment
 }
 
 // Byte offset of (row, 16-byte chunk) in a [128 rows][64 x nbox] bf16 operand
@@ -704,23 +727,26 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   constexpr int CH = kMmaCH;
   constexpr int TILE = CH * D * 2;
   constexpr int QB = kTcAttnRows * D * 2;
-  constexpr int PB = kTcAttnRows * CH * 2;
   constexpr int PST = D + 4;
+  constexpr int KP = kTcAttnKP;
+  constexpr int OC = D / kTcAttnGroups;  // output columns per owner thread
+  static_assert(CH == 128 && OC % 16 == 0, "whole 16-column TMEM loads");
   extern __shared__ __align__(1024) uint8_t smem_att[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_att) + 1023) & ~uintptr_t(1023));
   uint8_t* KV = sm;  // buffer b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
   uint8_t* Qs = KV + 4 * TILE;
   uint8_t* Ph = Qs + QB;
-  uint8_t* Pl = Ph + PB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(Pl + PB);  // [2] K/V chunk landed
+  uint8_t* Pl = Ph + kTcAttnPloOff;
+  uint64_t* full = reinterpret_cast<uint64_t*>(Ph + kTcAttnPBytes);  // [2] K/V chunk landed
   uint64_t* empty = full + 2;                             // [2] K/V chunk consumed
   uint64_t* sfull = empty + 2;                            // [2] S in TMEM
   uint64_t* pdone = sfull + 2;                            // [2] P written, O rescaled
   uint64_t* ofull = pdone + 2;                            // P V done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(ofull + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
-  float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ofull) + 64);  // [2 halves][64 rows]
-  float* xsum = xmax + 2 * 64;                                                      // [2 halves][64 rows]
+  // [2 chunk parities][8 pieces][64 rows] each
+  float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 128);
+  float* xsum = xmax + 2 * kTcAttnPieces * 64;
   float* psm = reinterpret_cast<float*>(sm);   // [64][PST] CTA partial (after the chunk loop)
   float* scr = psm + kClQT * PST;              // merge scratch
 
@@ -778,7 +804,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       tc::mbar_init(&full[b], 1);
       tc::mbar_init(&empty[b], 1);
       tc::mbar_init(&sfull[b], 1);
-      tc::mbar_init(&pdone[b], 1);
+      tc::mbar_init(&pdone[b], kTcAttnSoft);
     }
     tc::mbar_init(ofull, 1);
     *abort = 0;
@@ -892,20 +918,24 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       }
     }
   } else {
-    // ---------------- softmax, warps 2..5: TMEM lane L holds score row L;
+    // ---------------- softmax, warps 2..17: TMEM lane L holds score row L;
     // rows 0..63 and their copies 64..127 are the same query row q = L & 63.
-    // The thread of lane L takes key half h = L >> 6 of row q; the two halves
-    // exchange their row maximum and sum in shared memory (fixed order).
+    // Warp w reads the lanes of quadrant w & 3; its key group kg = (w - 2) / 4
+    // and the row copy h = L >> 6 pick the KP keys of piece 2 kg + h.
+    const int sw = warp - 2;
     const int L = (warp & 3) * 32 + lane;
     const int qr = L & (kClQT - 1), h = L >> 6;
+    const int kg = sw >> 2, piece = 2 * kg + h;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const bool o_owner = h == 0;  // lanes 0..63 also own the output row in TMEM
+    const bool o_owner = h == 0;  // lanes 0..63 hold the output rows; this thread takes columns OC kg ..
     const int row_tok = (qv0 + qr) / grp;
     const float scale = rsqrtf((float)D) * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int i = 0; i < nmine; ++i) {
       const int c = rank + i * NC, b = i & 1;
+      float* xm = xmax + b * (kTcAttnPieces * 64);
+      float* xs = xsum + b * (kTcAttnPieces * 64);
       bool blk;
       chunk_row(c, blk);
       const int slot0 = blk ? -1 : c * CH;
@@ -917,34 +947,37 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         *abort = 1;
         ok = false;
       }
-      __syncwarp();  // the TMEM loads below are warp-collective
+      __syncwarp();  // the TMEM load below is warp-collective
       tc::tc_fence_after();
-      float sc[CH / 2];
+      float sc[KP];
 #pragma unroll
-      for (int q = 0; q < CH / 32; ++q) {
+      for (int q = 0; q < KP / 16; ++q) {
         float t16[16];
-        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + h * (CH / 2) + q * 16), t16);
+        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + KP * piece + 16 * q), t16);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int j = h * (CH / 2) + q * 16 + t;  // key index in the chunk
-          sc[q * 16 + t] = (j < nk && j <= lim) ? t16[t] * scale : -INFINITY;
-        }
+        for (int t = 0; t < 16; ++t) sc[16 * q + t] = t16[t];
       }
       float cmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < CH / 2; ++j) cmax = fmaxf(cmax, sc[j]);
-      xmax[h * 64 + qr] = cmax;
-      tc::named_bar(2, 128);
-      const float m_new = fmaxf(m_run, fmaxf(xmax[qr], xmax[64 + qr]));
+      for (int t = 0; t < KP; ++t) {
+        const int j = KP * piece + t;  // key index in the chunk
+        sc[t] = (j < nk && j <= lim) ? sc[t] * scale : -INFINITY;
+        cmax = fmaxf(cmax, sc[t]);
+      }
+      xm[piece * 64 + qr] = cmax;
+      tc::named_bar(2, kTcAttnSoft);
+      float m_new = m_run;
+#pragma unroll
+      for (int pc = 0; pc < kTcAttnPieces; ++pc) m_new = fmaxf(m_new, xm[pc * 64 + qr]);
       const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
       float sum = 0.f;
 #pragma unroll
-      for (int j = 0; j < CH / 2; ++j) {
-        const float pj = (sc[j] == -INFINITY) ? 0.f : exp2f(sc[j] - m_new);
-        sc[j] = pj;
+      for (int t = 0; t < KP; ++t) {
+        const float pj = (sc[t] == -INFINITY) ? 0.f : exp2f(sc[t] - m_new);
+        sc[t] = pj;
         sum += pj;
       }
-      xsum[h * 64 + qr] = sum;
+      xs[piece * 64 + qr] = sum;
       // P has one buffer: the P V products of the chunk before must have
       // finished reading it (S of this chunk was issued ahead of them).
       if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort)) {
@@ -952,13 +985,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         *abort = 1;
         ok = false;
       }
-      // P = P_hi + P_lo: this thread's 64 keys of row q, 8 per 16-byte chunk
+      // P = P_hi + P_lo: this thread's KP keys of row q, 8 per 16-byte chunk
 #pragma unroll
-      for (int cc = 0; cc < CH / 16; ++cc) {
+      for (int cc = 0; cc < KP / 8; ++cc) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) split_bf16(sc[8 * cc + 2 * e], sc[8 * cc + 2 * e + 1], hi[e], lo[e]);
-        const int ch = h * (CH / 16) + cc;
+        const int ch = (KP / 8) * piece + cc;
         *reinterpret_cast<uint4*>(Ph + op_off(qr, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(Pl + op_off(qr, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -966,66 +999,71 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         // Rows past the last key hold whatever follows in memory (unwritten
         // cache slots may be NaN); zero V there so that P = 0 contributes 0.
         uint8_t* Vt = KV + (2 * b + 1) * TILE;
-        for (int t = L; t < (CH - nk) * (D / 8); t += 128) {
+        for (int t = sw * 32 + lane; t < (CH - nk) * (D / 8); t += kTcAttnSoft) {
           const int j = nk + t / (D / 8), ch = t % (D / 8);
           *reinterpret_cast<uint4*>(Vt + kv_off(j, ch)) = make_uint4(0, 0, 0, 0);
         }
       }
-      tc::named_bar(2, 128);
-      l_run = fmaf(l_run, alpha, xsum[qr] + xsum[64 + qr]);
-      // O (lanes 0..63) holds the chunks before this one: rescale it to the
+      tc::named_bar(2, kTcAttnSoft);
+      float lsum = 0.f;
+#pragma unroll
+      for (int pc = 0; pc < kTcAttnPieces; ++pc) lsum += xs[pc * 64 + qr];
+      l_run = fmaf(l_run, alpha, lsum);
+      // O (lanes 0..63) holds the chunks before this one (their P V products
+      // have completed: waited above): rescale this thread's OC columns to the
       // new maximum.  TMEM accesses are warp-collective: the whole warp takes
       // the branch when any of its rows needs it (alpha = 1 keeps a row).
-      // (The P V products of the chunk before have completed: waited above.)
       if (o_owner && i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         __syncwarp();
         tc::tc_fence_after();
-#pragma unroll 1
-        for (int q = 0; q < D / 16; ++q) {
+#pragma unroll
+        for (int q = 0; q < OC / 16; ++q) {
           float o16[16];
-          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+          const uint32_t col = (uint32_t)(2 * CH + OC * kg + 16 * q);
+          tc::tmem_ld16(lane_base + col, o16);
 #pragma unroll
           for (int t = 0; t < 16; ++t) o16[t] *= alpha;
-          tc::tmem_st16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+          tc::tmem_st16(lane_base + col, o16);
         }
       }
       m_run = m_new;
+      // This thread's P (and V zero) stores and TMEM stores are done: release
+      // them to the MMA issuer (pdone counts every softmax thread).
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::named_bar(2, 128);  // also: xmax / xsum are rewritten by the next chunk
-      if (L == 0) tc::mbar_arrive(&pdone[b]);
+      tc::mbar_arrive(&pdone[b]);
     }
-    // ---- this CTA's partial of its 64 rows (lanes 0..63)
-    if (o_owner) {
-      if (nmine > 0) {
-        if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort)) {
-          raise_status(status, ST_TIMEOUT);
-          *abort = 1;
-          ok = false;
-        }
-        __syncwarp();
-        tc::tc_fence_after();
+    // ---- this CTA's partial of its 64 rows (lanes 0..63, OC columns per thread)
+    if (o_owner && nmine > 0) {
+      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
       }
     }
     // psm overlays the K/V buffers: every MMA (the last P V) has completed here
-    tc::named_bar(2, 128);
+    tc::named_bar(2, kTcAttnSoft);
     if (o_owner) {
+      __syncwarp();
+      tc::tc_fence_after();
       float* pr = psm + (size_t)qr * PST;
-#pragma unroll 1
-      for (int q = 0; q < D / 16; ++q) {
+#pragma unroll
+      for (int q = 0; q < OC / 16; ++q) {
         float o16[16];
         if (nmine > 0) {
-          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + q * 16), o16);
+          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + OC * kg + 16 * q), o16);
         } else {
 #pragma unroll
           for (int t = 0; t < 16; ++t) o16[t] = 0.f;
         }
 #pragma unroll
         for (int t = 0; t < 16; t += 4)
-          *reinterpret_cast<float4*>(pr + q * 16 + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
+          *reinterpret_cast<float4*>(pr + OC * kg + 16 * q + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
       }
-      pr[D] = m_run;
-      pr[D + 1] = l_run;
+      if (kg == 0) {
+        pr[D] = m_run;
+        pr[D + 1] = l_run;
+      }
     }
   }
   tc::tc_fence_before();
@@ -1166,14 +1204,13 @@ size_t attn_workspace(const AttnDesc& a) {
   return (size_t)a.n_seqs * a.nkv * g.n_qt * g.nch * kAttnQT * (a.d + 2) * sizeof(float);
 }
 
-// The tcgen05 attention kernel is chosen with DFLASH_ATTN_TCGEN05=1 in the
-// environment (read once per process).  It computes the same function; in
-// the whole cycle at 16 block rows the mma.sync kernel measured faster, so
-// it is the default.
+// Head dimension 128 runs the tcgen05 kernel unless DFLASH_ATTN_MMASYNC=1 is
+// set in the environment (read once per process); both compute the same
+// function, and the tcgen05 one measured faster in the whole cycle.
 static bool use_tc_attention() {
   static const bool on = [] {
-    const char* v = getenv("DFLASH_ATTN_TCGEN05");
-    return v != nullptr && v[0] == '1';
+    const char* v = getenv("DFLASH_ATTN_MMASYNC");
+    return !(v != nullptr && v[0] == '1');
   }();
   return on;
 }
