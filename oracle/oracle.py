@@ -404,6 +404,34 @@ def draft_forward(m: Model, st: SeqState, anchor: int, P: int, want_logits: bool
     return am, mg, lg
 
 
+def draft_denoise(m: Model, st: SeqState, anchor: int, P: int, rounds: int, want_logits: bool = False,
+                  selector=None):
+    """Multi-round block denoising ([N] "the core of DFlash 2": a block
+    diffusion model settles a block in several rounds of parallel denoising
+    or correction, predicting and revising every block position at once).
+    Round 1 is the single-step draft on [anchor, mask...]; round r >= 2 runs
+    the same forward on [anchor, drafts of round r-1] at the same positions
+    P..P+B-1, every row j >= 1 predicting the token at P+j again.  With
+    selector = (U, Vm, topk) every round's drafts are the DFlash 2 greedy
+    path over that round's top-k candidates ([G] section 7).  Returns the
+    last round's drafts, their margins (argmax or walk) and, if asked, the
+    last round's logits [B-1][V]."""
+    cfg = m.draft.cfg
+    B = m.block
+    rest = [m.mask_id] * (B - 1)
+    for _ in range(max(1, int(rounds))):
+        h = embed(cfg, m.E, [anchor] + [int(t) for t in rest])
+        for li, L in enumerate(m.draft.layers):
+            decoder_layer(cfg, L, h, P, BIDIR, st.dk[li], st.dv[li], m.window)
+        x = final_norm(cfg, h, m.draft.g_final)
+        am, mg, lg = lm_head_argmax(cfg, m.Wlm, x[1:], want_logits or selector is not None)
+        if selector is not None:
+            U, Vm, topk = selector
+            am, _, mg = path_select(cfg, lg, m.E, U, Vm, anchor, topk)
+        rest = am
+    return am, mg, (lg if want_logits else None)
+
+
 def prefill(m: Model, st: SeqState, prompt):
     """Target forward over the prompt, inject every prompt position into the
     draft context; returns the first generated token (the first anchor)."""
