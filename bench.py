@@ -43,6 +43,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--trace-replays", type=int, default=5)
     p.add_argument("--no-sampling", action="store_true", help="skip the sampling-mode cycle timing")
+    p.add_argument("--no-denoise", action="store_true", help="skip the multi-round denoising draft timing")
     p.add_argument("--layers", default="", help="T,D: shrink to T target / D draft layers (profiling captures "
                    "only; the line then names the reduced config)")
     return p.parse_args()
@@ -451,6 +452,34 @@ def run_ours(args):
         eng.base_pos.copy_(base0)
         eng.anchor.copy_(anchor0)
 
+    # multi-round block denoising: the draft-block step alone at 1 and 2
+    # rounds (graph replay; the state is untouched by a draft)
+    denoise = None
+    if not args.no_denoise:
+        dms = {}
+        for R in (1, 2):
+            eng.draft(rounds=R)
+            torch.cuda.synchronize()
+            assert eng.status() == D.DFLASH_OK
+            dgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(dgraph):
+                eng.draft(rounds=R)
+            for _ in range(args.warmup):
+                dgraph.replay()
+            n_d = max(3, min(args.steps, 50))
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(n_d):
+                dgraph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            dms[str(R)] = reduce_max(e0.elapsed_time(e1), world, "cuda") / n_d
+            del dgraph
+        denoise = {"mode": "draft-block step alone, graph replay", "rounds_ms": dms,
+                   "unit": "ms per draft-block step", "steps": n_d}
+        eng.base_pos.copy_(base0)
+        eng.anchor.copy_(anchor0)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -513,7 +542,7 @@ def run_ours(args):
             "verified_tok_s": verified, "mean_accept": mean_accept,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-            "clocks": clocks, "kernels": per_fam, "sampling": sampling}
+            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -640,48 +640,12 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
 
 // ----------------------------------------------------------------- draft
 
-int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  const char* who = "dflash_draft_block";
-  DF_CHECK(a != nullptr, "%s: NULL args", who);
-  int rc = check_dims(a->dims, who);
-  if (rc) return rc;
+// One draft forward over the embedded block in s.h: every draft layer, the
+// final norm, the fused LM head (argmax, or top-k candidates + path walk).
+static int draft_round(const dflash_draft_args* a, const DraftScratch& s, const Ctx& c, int sms, cudaStream_t st) {
   const dflash_dims& d = a->dims;
-  DF_CHECK(a->n_layers > 0 && a->n_layers <= DFLASH_MAX_LAYERS, "%s: n_layers must be in [1, %d]", who,
-           DFLASH_MAX_LAYERS);
-  DF_CHECK(a->block >= 2 && a->n_seqs > 0, "%s: block >= 2 and n_seqs > 0 required", who);
-  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
-  DF_CHECK(a->final_norm && a->embed && a->lm_head && a->anchor && a->base_pos && a->drafts && a->rope_cs,
-           "%s: NULL pointer", who);
-  DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
-  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
-  DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
-  if (a->path_topk > 0) {
-    DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
-             "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);
-    DF_CHECK(d.hidden % 8 == 0, "%s: the path selector needs hidden %% 8 == 0", who);
-  }
-  for (int j = 0; j < a->n_layers; ++j) {
-    rc = check_weights(a->layers[j], who);
-    if (rc) return rc;
-    DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
-    rc = check_layer_shape(draft_layer_shape(a, j), who);
-    if (rc) return rc;
-  }
-  const int sms = num_sms();
-  DraftScratch s;
-  Bump m(nullptr);
-  size_t need = carve_draft(m, a, sms, s);
-  rc = check_ws(ws, ws_bytes, need, who);
-  if (rc) return rc;
-  Bump b(ws);
-  carve_draft(b, a, sms, s);
-  Ctx c = header(ws);
-  cudaStream_t st = (cudaStream_t)stream;
   const int M = a->n_seqs * a->block;
-
-  DF_LAUNCH(st, TF_EMBED, 0,
-            launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, nullptr, a->mask_token,
-                         s.h, st));
+  int rc;
   for (int j = 0; j < a->n_layers; ++j) {
     rc = run_layer(draft_layer_shape(a, j), a->layers[j], a->kv_layers[j], s.h, a->base_pos, a->rope_cs,
                    a->rope_max_pos, nullptr,
@@ -720,6 +684,60 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
     p.proj = s.proj;
     p.status = c.status;
     DF_LAUNCH(st, TF_PATH, 0, launch_path_select(p, st));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_draft_block";
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  const dflash_dims& d = a->dims;
+  DF_CHECK(a->n_layers > 0 && a->n_layers <= DFLASH_MAX_LAYERS, "%s: n_layers must be in [1, %d]", who,
+           DFLASH_MAX_LAYERS);
+  DF_CHECK(a->block >= 2 && a->n_seqs > 0, "%s: block >= 2 and n_seqs > 0 required", who);
+  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
+  DF_CHECK(a->final_norm && a->embed && a->lm_head && a->anchor && a->base_pos && a->drafts && a->rope_cs,
+           "%s: NULL pointer", who);
+  DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
+  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
+  DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
+  DF_CHECK(a->denoise_rounds >= 0 && a->denoise_rounds <= DFLASH_MAX_DENOISE_ROUNDS,
+           "%s: denoise_rounds must be in [0, %d]", who, DFLASH_MAX_DENOISE_ROUNDS);
+  if (a->path_topk > 0) {
+    DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
+             "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);
+    DF_CHECK(d.hidden % 8 == 0, "%s: the path selector needs hidden %% 8 == 0", who);
+  }
+  for (int j = 0; j < a->n_layers; ++j) {
+    rc = check_weights(a->layers[j], who);
+    if (rc) return rc;
+    DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
+    rc = check_layer_shape(draft_layer_shape(a, j), who);
+    if (rc) return rc;
+  }
+  const int sms = num_sms();
+  DraftScratch s;
+  Bump m(nullptr);
+  size_t need = carve_draft(m, a, sms, s);
+  rc = check_ws(ws, ws_bytes, need, who);
+  if (rc) return rc;
+  Bump b(ws);
+  carve_draft(b, a, sms, s);
+  Ctx c = header(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+
+  // Round 1 embeds [anchor, mask, ...]; a later round embeds [anchor, the
+  // drafts of the round before] (written to a->drafts by that round's head
+  // or path walk, read here in stream order).
+  const int rounds = a->denoise_rounds > 1 ? a->denoise_rounds : 1;
+  for (int r = 0; r < rounds; ++r) {
+    DF_LAUNCH(st, TF_EMBED, 0,
+              launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, r == 0 ? nullptr : a->drafts,
+                           a->mask_token, s.h, st));
+    rc = draft_round(a, s, c, sms, st);
+    if (rc) return rc;
   }
   return DFLASH_OK;
 }

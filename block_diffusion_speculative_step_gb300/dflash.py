@@ -86,7 +86,7 @@ class dflash_draft_args(C.Structure):
                 ("lm_head", vp), ("n_seqs", i32), ("block", i32), ("anchor", vp), ("base_pos", vp),
                 ("mask_token", i32), ("max_pos", i32), ("rope_cs", vp), ("rope_max_pos", i32),
                 ("drafts", vp), ("logits", vp), ("path_topk", i32), ("path_rank", i32), ("path_u", vp),
-                ("path_v", vp)]
+                ("path_v", vp), ("denoise_rounds", i32)]
 
 
 class dflash_verify_args(C.Structure):

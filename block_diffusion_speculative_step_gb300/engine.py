@@ -140,7 +140,7 @@ class Engine:
         a.rope_max_pos = self.rope_max
         return a
 
-    def draft_args(self, logits=None):
+    def draft_args(self, logits=None, rounds: int = 1):
         d = self.w.draft
         a = D.dflash_draft_args()
         a.dims = self.ddims
@@ -163,6 +163,7 @@ class Engine:
         if self.w.path_topk:
             a.path_topk, a.path_rank = self.w.path_topk, self.w.path_rank
             a.path_u, a.path_v = _ptr(self.m["path_u"]), _ptr(self.m["path_v"])
+        a.denoise_rounds = rounds
         return a
 
     def verify_args(self, block: int, h, drafts=None, logits=None, update=True):
@@ -232,8 +233,8 @@ class Engine:
             D.dflash_decoder_layer_forward(self.target_layer_args(li, rows, self.h, tap, off, base_pos), self.ws_ptr,
                                            self.ws_bytes)
 
-    def draft(self, logits=None):
-        D.dflash_draft_block(self.draft_args(logits), self.ws_ptr, self.ws_bytes)
+    def draft(self, logits=None, rounds: int = 1):
+        D.dflash_draft_block(self.draft_args(logits, rounds), self.ws_ptr, self.ws_bytes)
 
     def verify(self, block: int, drafts=None, logits=None):
         D.dflash_verify_accept(self.verify_args(block, self.h, drafts, logits), self.ws_ptr, self.ws_bytes)

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 1
+#define DFLASH_ABI_VERSION 2
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -218,7 +218,16 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes,
  * With path_topk > 0 the DFlash 2 path selector (dflash_path_select) replaces
  * the drafts by its greedy path over each row's top-path_topk candidates.
  * logits (optional, [n_seqs][block-1][V] fp32) receives rows 1..block-1.
+ *
+ * Multi-round block denoising ("DFlash 2 release" news, "the core of DFlash
+ * 2": a block diffusion model settles a block in rounds of parallel
+ * denoising or correction): with denoise_rounds = R >= 2 the forward above
+ * runs R times; round 1 on [anchor, mask, ...], round r >= 2 on [anchor,
+ * drafts of round r-1] at the same positions, each round ending with its
+ * argmax (or path walk).  drafts and logits hold the last round's.  0 and 1
+ * both mean the single step; R <= DFLASH_MAX_DENOISE_ROUNDS.
  */
+#define DFLASH_MAX_DENOISE_ROUNDS 16
 typedef struct {
   dflash_dims dims;
   int32_t n_layers;
@@ -240,6 +249,7 @@ typedef struct {
   int32_t path_rank;                      /* R of path_u / path_v */
   const void* path_u;                     /* [R][H] */
   const void* path_v;                     /* [R][H] */
+  int32_t denoise_rounds;                 /* 0 / 1 = single step, else R rounds */
 } dflash_draft_args;
 int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);

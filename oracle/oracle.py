@@ -405,7 +405,7 @@ def draft_forward(m: Model, st: SeqState, anchor: int, P: int, want_logits: bool
 
 
 def draft_denoise(m: Model, st: SeqState, anchor: int, P: int, rounds: int, want_logits: bool = False,
-                  selector=None):
+                  selector=None, init=None):
     """Multi-round block denoising ([N] "the core of DFlash 2": a block
     diffusion model settles a block in several rounds of parallel denoising
     or correction, predicting and revising every block position at once).
@@ -415,10 +415,12 @@ def draft_denoise(m: Model, st: SeqState, anchor: int, P: int, rounds: int, want
     selector = (U, Vm, topk) every round's drafts are the DFlash 2 greedy
     path over that round's top-k candidates ([G] section 7).  Returns the
     last round's drafts, their margins (argmax or walk) and, if asked, the
-    last round's logits [B-1][V]."""
+    last round's logits [B-1][V].  init (optional, B-1 tokens) replaces the
+    mask tokens of round 1: the rounds then continue from those drafts."""
     cfg = m.draft.cfg
     B = m.block
-    rest = [m.mask_id] * (B - 1)
+    rest = [m.mask_id] * (B - 1) if init is None else [int(t) for t in init]
+    assert len(rest) == B - 1
     for _ in range(max(1, int(rounds))):
         h = embed(cfg, m.E, [anchor] + [int(t) for t in rest])
         for li, L in enumerate(m.draft.layers):

@@ -70,3 +70,22 @@ def test_denoise_zero_selector_is_plain_rounds(orc):
         walked, mg, _ = orc.draft_denoise(om, st, 11, 16, R, selector=(z, z, 4))
         np.testing.assert_array_equal(walked, plain)
         assert np.all(mg == 0.0)
+
+
+def test_denoise_init_continues_rounds(orc):
+    """Rounds compose: R rounds from the masks == R - r rounds started from
+    the drafts of the first r rounds."""
+    w = Hh.small_workload(V=128, block=5)
+    m = synth.make_model(w, seed=6, jitter=0.1, with_target=True)
+    om = Hh.omodel(w, m)
+    st = orc.new_state(om, 48)
+    rng = np.random.default_rng(4)
+    for li in range(len(om.draft.layers)):
+        st.dk[li][:, :16] = rng.standard_normal(st.dk[li][:, :16].shape)
+        st.dv[li][:, :16] = rng.standard_normal(st.dv[li][:, :16].shape)
+    d3, m3, l3 = orc.draft_denoise(om, st, 2, 16, 3, want_logits=True)
+    d1, _, _ = orc.draft_denoise(om, st, 2, 16, 1)
+    e2, n2, k2 = orc.draft_denoise(om, st, 2, 16, 2, want_logits=True, init=d1)
+    np.testing.assert_array_equal(d3, e2)
+    np.testing.assert_array_equal(m3, n2)
+    np.testing.assert_array_equal(l3, k2)
