@@ -15,6 +15,8 @@ Layouts (row-major, [out][in] for every projection):
   final_norm [H]
   fc [H][F H], fc_norm [H]                context-feature fusion (draft side)
   path_u, path_v [R][H]                   path-selector low-rank factors
+  draft layer.conv_w1 [4][r][H],          DFlash 2 dynamic depthwise convolution tap
+  draft layer.conv_w2 [4][2H][r]          generators (attention in / out, MLP in / out)
 """
 from __future__ import annotations
 
@@ -53,6 +55,7 @@ class Workload:
     run_target: bool = True    # False: tap features are synthesised N(0,1)
     path_topk: int = 0         # DFlash 2 path selector (0 = off)
     path_rank: int = 0
+    conv_rank: int = 0         # DFlash 2 dynamic depthwise convolutions in the draft (0 = off)
     accept_mean: float = 0.0   # >0: plant drafts so accept lengths ~ Geom(mean)
     prompt: int = 0
     generate: int = 0
@@ -156,6 +159,10 @@ def make_model(w: Workload, seed: int = 0, device="cpu", std: float = 0.02, jitt
     if w.path_topk:
         m["path_u"] = dr.normal((w.path_rank, H), std, dt)
         m["path_v"] = dr.normal((w.path_rank, H), std, dt)
+    if w.conv_rank:  # drawn last, so the other weights do not depend on it
+        for L in m["draft"]["layers"]:
+            L["conv_w1"] = dr.normal((4, w.conv_rank, H), std, dt)
+            L["conv_w2"] = dr.normal((4, 2 * H, w.conv_rank), std, dt)
     return m
 
 

@@ -55,6 +55,20 @@ typedef struct {
   double eps;   /* RMSNorm epsilon */
 } or_cfg;
 
+/* DFlash 2 two-tap dynamic depthwise convolutions of one draft layer, at
+ * OR_CONV_PRE_ATTN (the attention input), OR_CONV_POST_ATTN (the attention
+ * block's output), OR_CONV_PRE_MLP, OR_CONV_POST_MLP.  w1[i] [r][H] and
+ * w2[i] [2H][r] generate the taps (see or_dyn_conv). */
+#define OR_CONV_PRE_ATTN 0
+#define OR_CONV_POST_ATTN 1
+#define OR_CONV_PRE_MLP 2
+#define OR_CONV_POST_MLP 3
+typedef struct {
+  const void* w1[4];
+  const void* w2[4];
+  int r;
+} or_conv;
+
 typedef struct {
   const void *wq, *wk, *wv, *wo; /* [out][in] row-major */
   const void *wg, *wu, *wd;      /* gate [I][H], up [I][H], down [H][I] */
@@ -132,6 +146,54 @@ void or_linear(const or_cfg* c, const void* W, int N, int K, int M, const double
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/*
+ * DFlash 2 two-tap dynamic depthwise convolution ([G] section 7: a two-tap
+ * convolution that looks at the current and the previous position only,
+ * inserted before and after attention and the MLP of every draft layer; the
+ * block head reads the last verified token).  The page gives neither the tap
+ * generator nor the residual form; as read here, over the M rows u[0..M-1]
+ * of one block at consecutive positions:
+ *   z_t       = SiLU(W1 u_t)                 W1 [r][H]
+ *   (a_t,b_t) = W2 z_t                       W2 [2H][r]: rows 0..H-1 -> a, H..2H-1 -> b
+ *   y_t       = u_t + a_t * u_t + b_t * u_{t-1}   per channel
+ * with u_{-1} = 0: block row 0 (the anchor) has no predecessor inside the
+ * block, and row 1, the first drafted position, reads the anchor, which is
+ * the last verified token.  The taps come from the row itself (dynamic), one
+ * pair per channel (depthwise).  Nothing is rounded here.
+ */
+void or_dyn_conv(const or_cfg* c, int M, int r, const void* W1, const void* W2, const double* u,
+                 double* y) {
+  const int H = c->H;
+  double* z = malloc(sizeof(double) * (size_t)r);
+  for (int t = 0; t < M; ++t) {
+    const double* ut = u + (size_t)t * H;
+    const double* up = t > 0 ? u + (size_t)(t - 1) * H : NULL;
+    for (int j = 0; j < r; ++j) {
+      double s = 0.0;
+      for (int k = 0; k < H; ++k) s += wget(c, W1, (size_t)j * H + k) * ut[k];
+      z[j] = silu(s);
+    }
+    for (int ch = 0; ch < H; ++ch) {
+      double a = 0.0, b = 0.0;
+      for (int j = 0; j < r; ++j) {
+        a += wget(c, W2, (size_t)ch * r + j) * z[j];
+        b += wget(c, W2, (size_t)(H + ch) * r + j) * z[j];
+      }
+      y[(size_t)t * H + ch] = ut[ch] + a * ut[ch] + (up ? b * up[ch] : 0.0);
+    }
+  }
+  free(z);
+}
+
+/* rows u[M][H] -> conv (in place through a scratch copy) */
+static void conv_rows(const or_cfg* c, const or_conv* cv, int at, int M, double* u, int round_out) {
+  const int H = c->H;
+  double* y = malloc(sizeof(double) * (size_t)M * H);
+  or_dyn_conv(c, M, cv->r, cv->w1[at], cv->w2[at], u, y);
+  for (size_t i = 0; i < (size_t)M * H; ++i) u[i] = round_out ? rnd(c, y[i]) : y[i];
+  free(y);
+}
+
 /* Softmax attention of one query head over nk keys (pointers to head rows). */
 static void attend(int d, const double* q, int nk, const double* const* K, const double* const* V,
                    double* out, double* scratch) {
@@ -177,8 +239,8 @@ static long slot_of(long t, long window) { return window > 0 ? t % window : t; }
  * else 0); row i attends all of those and all M rows of the block, with no
  * mask inside the block.  The block K/V are not stored.
  */
-int or_decoder_layer(const or_cfg* c, const or_layer* L, int M, long p0, int mode,
-                     double* kc, double* vc, long cap, long window, double* h) {
+int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv, int M, long p0,
+                          int mode, double* kc, double* vc, long cap, long window, double* h) {
   const int H = c->H, d = c->d, nq = c->nq, nkv = c->nkv, I = c->I;
   const int QD = nq * d, KD = nkv * d, grp = nq / nkv;
   if (M <= 0) return 0;
@@ -200,6 +262,7 @@ int or_decoder_layer(const or_cfg* c, const or_layer* L, int M, long p0, int mod
     or_rmsnorm(c, H, h + (size_t)m * H, L->g1, x + (size_t)m * H);
     for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
   }
+  if (cv) conv_rows(c, cv, OR_CONV_PRE_ATTN, M, x, 1); /* a projection input: rounded */
   or_linear(c, L->wq, QD, H, M, x, q);
   or_linear(c, L->wk, KD, H, M, x, k);
   or_linear(c, L->wv, KD, H, M, x, v);
@@ -262,20 +325,29 @@ int or_decoder_layer(const or_cfg* c, const or_layer* L, int M, long p0, int mod
   for (size_t i = 0; i < (size_t)M * QD; ++i) o[i] = rnd(c, o[i]);
 
   or_linear(c, L->wo, H, QD, M, o, y);
+  if (cv) conv_rows(c, cv, OR_CONV_POST_ATTN, M, y, 0); /* added to the residual: not rounded */
   for (size_t i = 0; i < (size_t)M * H; ++i) h[i] += y[i];
 
   for (int m = 0; m < M; ++m) {
     or_rmsnorm(c, H, h + (size_t)m * H, L->g2, x + (size_t)m * H);
     for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
   }
+  if (cv) conv_rows(c, cv, OR_CONV_PRE_MLP, M, x, 1);
   or_linear(c, L->wg, I, H, M, x, gt);
   or_linear(c, L->wu, I, H, M, x, up);
   for (size_t i = 0; i < (size_t)M * I; ++i) gt[i] = rnd(c, silu(gt[i]) * up[i]);
   or_linear(c, L->wd, H, I, M, gt, y);
+  if (cv) conv_rows(c, cv, OR_CONV_POST_MLP, M, y, 0);
   for (size_t i = 0; i < (size_t)M * H; ++i) h[i] += y[i];
 
   free(x); free(q); free(k); free(v); free(o); free(y); free(gt); free(up);
   return 0;
+}
+
+/* The layer without the DFlash 2 convolutions. */
+int or_decoder_layer(const or_cfg* c, const or_layer* L, int M, long p0, int mode,
+                     double* kc, double* vc, long cap, long window, double* h) {
+  return or_decoder_layer_conv(c, L, NULL, M, p0, mode, kc, vc, cap, window, h);
 }
 
 /* ------------------------------------------------------------ output head */

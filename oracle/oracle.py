@@ -64,6 +64,10 @@ class _Layer(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g1", "g2")]
 
 
+class _Conv(C.Structure):
+    _fields_ = [("w1", C.c_void_p * 4), ("w2", C.c_void_p * 4), ("r", C.c_int)]
+
+
 def lib():
     global _lib
     with _lock:
@@ -77,6 +81,9 @@ def lib():
             L.or_linear.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_int, C.c_int, C.c_int, dp, dp]
             L.or_decoder_layer.argtypes = [C.POINTER(_Cfg), C.POINTER(_Layer), C.c_int, C.c_long,
                                            C.c_int, dp, dp, C.c_long, C.c_long, dp]
+            L.or_decoder_layer_conv.argtypes = [C.POINTER(_Cfg), C.POINTER(_Layer), C.POINTER(_Conv), C.c_int,
+                                                C.c_long, C.c_int, dp, dp, C.c_long, C.c_long, dp]
+            L.or_dyn_conv.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, C.c_void_p, C.c_void_p, dp, dp]
             L.or_final_norm.argtypes = [C.POINTER(_Cfg), C.c_int, dp, C.c_void_p, dp]
             L.or_lm_head_argmax.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_int, C.c_int, dp,
                                             C.POINTER(C.c_int), dp, C.POINTER(C.c_float)]
@@ -138,8 +145,26 @@ class Cfg:
 
 
 @dataclass
+class Conv:
+    """The DFlash 2 dynamic depthwise convolutions of one draft layer: tap
+    generators w1[i] [r][H], w2[i] [2H][r] at i = 0 attention input, 1
+    attention output, 2 MLP input, 3 MLP output (see dyn_conv)."""
+    w1: list
+    w2: list
+
+    def c(self) -> _Conv:
+        cv = _Conv()
+        for i in range(4):
+            cv.w1[i] = self.w1[i].ctypes.data
+            cv.w2[i] = self.w2[i].ctypes.data
+        cv.r = int(self.w1[0].shape[0])
+        return cv
+
+
+@dataclass
 class Layer:
-    """One decoder layer's weights, [out][in] row-major (views are fine)."""
+    """One decoder layer's weights, [out][in] row-major (views are fine);
+    conv: the DFlash 2 convolutions of a draft layer, or None."""
     wq: np.ndarray
     wk: np.ndarray
     wv: np.ndarray
@@ -149,19 +174,24 @@ class Layer:
     wd: np.ndarray
     g1: np.ndarray
     g2: np.ndarray
+    conv: Conv | None = None
 
     def c(self) -> _Layer:
         arrs = [self.wq, self.wk, self.wv, self.wo, self.wg, self.wu, self.wd, self.g1, self.g2]
         return _Layer(*[a.ctypes.data for a in arrs])
 
     @staticmethod
-    def from_stacked(cfg: Cfg, w_qkv, w_o, w_gu, w_down, ln1, ln2) -> "Layer":
+    def from_stacked(cfg: Cfg, w_qkv, w_o, w_gu, w_down, ln1, ln2, conv_w1=None, conv_w2=None) -> "Layer":
         """Split a stacked [Wq; Wk; Wv] and [W_gate; W_up] into the per-matrix
-        views the definitions use."""
+        views the definitions use; conv_w1 [4][r][H] / conv_w2 [4][2H][r]
+        (optional) are the layer's convolution tap generators."""
         QD, KD = cfg.nq * cfg.d, cfg.nkv * cfg.d
         c = np.ascontiguousarray
+        conv = None
+        if conv_w1 is not None:
+            conv = Conv([c(conv_w1[i]) for i in range(4)], [c(conv_w2[i]) for i in range(4)])
         return Layer(c(w_qkv[:QD]), c(w_qkv[QD:QD + KD]), c(w_qkv[QD + KD:QD + 2 * KD]), c(w_o),
-                     c(w_gu[:cfg.I]), c(w_gu[cfg.I:]), c(w_down), c(ln1), c(ln2))
+                     c(w_gu[:cfg.I]), c(w_gu[cfg.I:]), c(w_down), c(ln1), c(ln2), conv)
 
 
 def wfloat(cfg: Cfg, w: np.ndarray) -> np.ndarray:
@@ -222,10 +252,25 @@ def decoder_layer(cfg: Cfg, L: Layer, h: np.ndarray, p0: int, mode: int, kc: np.
     p0..p0+M-1, in place.  kc/vc: [nkv][cap][d] float64 caches."""
     assert h.dtype == np.float64 and h.flags.c_contiguous
     cap = kc.shape[1]
-    rc = lib().or_decoder_layer(C.byref(cfg.c()), C.byref(L.c()), h.shape[0], int(p0), int(mode),
-                                _dp(kc), _dp(vc), cap, int(window), _dp(h))
+    if L.conv is not None:
+        rc = lib().or_decoder_layer_conv(C.byref(cfg.c()), C.byref(L.c()), C.byref(L.conv.c()), h.shape[0],
+                                         int(p0), int(mode), _dp(kc), _dp(vc), cap, int(window), _dp(h))
+    else:
+        rc = lib().or_decoder_layer(C.byref(cfg.c()), C.byref(L.c()), h.shape[0], int(p0), int(mode),
+                                    _dp(kc), _dp(vc), cap, int(window), _dp(h))
     if rc != 0:
         raise ValueError(f"or_decoder_layer failed ({rc})")
+
+
+def dyn_conv(cfg: Cfg, W1: np.ndarray, W2: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """DFlash 2 two-tap dynamic depthwise convolution ([G] section 7) over
+    the rows u [M][H] of one block: z_t = SiLU(W1 u_t), (a_t, b_t) = W2 z_t,
+    y_t = u_t + a_t * u_t + b_t * u_{t-1}, u_{-1} = 0 (the reading stated in
+    dflash_oracle.c, or_dyn_conv)."""
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    y = np.empty_like(u)
+    lib().or_dyn_conv(C.byref(cfg.c()), u.shape[0], W1.shape[0], _vp(W1), _vp(W2), _dp(u), _dp(y))
+    return y
 
 
 def final_norm(cfg: Cfg, h: np.ndarray, g: np.ndarray) -> np.ndarray:

@@ -13,11 +13,12 @@ from oracle import oracle as O
 
 
 def small_workload(dtype="f32", H=64, nq=4, nkv=2, d=16, I=96, V=128, t_layers=3, d_layers=2,
-                   taps=(0, 1), block=4, theta=1e4, eps=1e-6, window=0, topk=0, rank=0):
+                   taps=(0, 1), block=4, theta=1e4, eps=1e-6, window=0, topk=0, rank=0, conv_rank=0):
     return synth.Workload(
         name="test", target=synth.Shape(t_layers, H, nq, nkv, d, I),
         draft=synth.Shape(d_layers, H, nq, nkv, d, I), vocab=V, taps=tuple(taps), block=block,
-        rope_theta=theta, rms_eps=eps, dtype=dtype, window=window, path_topk=topk, path_rank=rank)
+        rope_theta=theta, rms_eps=eps, dtype=dtype, window=window, path_topk=topk, path_rank=rank,
+        conv_rank=conv_rank)
 
 
 def ocfg(w: synth.Workload, s: synth.Shape) -> O.Cfg:
@@ -29,7 +30,9 @@ def ostack(w, s, st) -> O.Stack:
     c = ocfg(w, s)
     n = synth.to_numpy
     layers = [O.Layer.from_stacked(c, n(L["w_qkv"]), n(L["w_o"]), n(L["w_gu"]), n(L["w_down"]),
-                                   n(L["ln1"]), n(L["ln2"])) for L in st["layers"]]
+                                   n(L["ln1"]), n(L["ln2"]),
+                                   n(L["conv_w1"]) if "conv_w1" in L else None,
+                                   n(L["conv_w2"]) if "conv_w2" in L else None) for L in st["layers"]]
     return O.Stack(c, layers, n(st["final_norm"]))
 
 
@@ -69,6 +72,15 @@ def trope(x: torch.Tensor, pos: torch.Tensor, theta: float) -> torch.Tensor:
     return torch.cat([z.real, z.imag], dim=-1)
 
 
+def tconv(c: O.Cfg, cv: O.Conv, i: int, u: torch.Tensor) -> torch.Tensor:
+    """The two-tap dynamic depthwise convolution with torch ops: taps from
+    F.silu / matmul, the previous row by F.pad (a zero row before row 0)."""
+    ab = F.silu(u @ t64(cv.w1[i]).T) @ t64(cv.w2[i]).T
+    a, b = ab[:, :c.H], ab[:, c.H:]
+    prev = F.pad(u, (0, 0, 1, 0))[:-1]
+    return u + a * u + b * prev
+
+
 def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=None, ctx_v=None,
                 causal=True, past_k=None, past_v=None):
     """One decoder layer with F.rms_norm / F.scaled_dot_product_attention /
@@ -76,7 +88,10 @@ def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=
     keys = ctx ++ the rows', no mask.  Returns (h_out, k_rows, v_rows)."""
     M = h.shape[0]
     bf = c.bf16
+    cv = L.conv
     x = tround(F.rms_norm(h, (c.H,), t64(L.g1), c.eps), bf)
+    if cv is not None:
+        x = tround(tconv(c, cv, 0, x), bf)
     q = (x @ t64(L.wq).T).view(M, c.nq, c.d)
     k = (x @ t64(L.wk).T).view(M, c.nkv, c.d)
     v = (x @ t64(L.wv).T).view(M, c.nkv, c.d)
@@ -99,8 +114,12 @@ def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=
     Vq = V.repeat_interleave(grp, dim=1).permute(1, 0, 2)
     o = F.scaled_dot_product_attention(q.permute(1, 0, 2), Kq, Vq, attn_mask=mask)
     o = tround(o.permute(1, 0, 2).reshape(M, c.nq * c.d), bf)
-    h = h + o @ t64(L.wo).T
+    y = o @ t64(L.wo).T
+    h = h + (y if cv is None else tconv(c, cv, 1, y))
     x = tround(F.rms_norm(h, (c.H,), t64(L.g2), c.eps), bf)
+    if cv is not None:
+        x = tround(tconv(c, cv, 2, x), bf)
     a = tround(F.silu(x @ t64(L.wg).T) * (x @ t64(L.wu).T), bf)
-    h = h + a @ t64(L.wd).T
+    y = a @ t64(L.wd).T
+    h = h + (y if cv is None else tconv(c, cv, 3, y))
     return h, k, v
