@@ -44,6 +44,7 @@ def parse():
     p.add_argument("--trace-replays", type=int, default=5)
     p.add_argument("--no-sampling", action="store_true", help="skip the sampling-mode cycle timing")
     p.add_argument("--no-denoise", action="store_true", help="skip the multi-round denoising draft timing")
+    p.add_argument("--no-conv", action="store_true", help="skip the draft-convolution timing")
     p.add_argument("--layers", default="", help="T,D: shrink to T target / D draft layers (profiling captures "
                    "only; the line then names the reduced config)")
     return p.parse_args()
@@ -480,6 +481,40 @@ def run_ours(args):
         eng.base_pos.copy_(base0)
         eng.anchor.copy_(anchor0)
 
+    # DFlash 2 draft convolutions (rank 64, four per draft layer): the
+    # draft-block step alone with and without them (graph replay)
+    conv = None
+    if not args.no_conv:
+        synth.add_conv_weights(eng.m, w, 64)
+        if D.dflash_workspace_bytes(D.DFLASH_OP_DRAFT, eng.draft_args(conv_rank=64)) <= eng.ws_bytes:
+            cms = {}
+            for tag, r in (("none", 0), ("rank64", 64)):
+                eng.draft(conv_rank=r)
+                torch.cuda.synchronize()
+                assert eng.status() == D.DFLASH_OK
+                cgraph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(cgraph):
+                    eng.draft(conv_rank=r)
+                for _ in range(args.warmup):
+                    cgraph.replay()
+                n_c = max(3, min(args.steps, 50))
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(n_c):
+                    cgraph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                cms[tag] = reduce_max(e0.elapsed_time(e1), world, "cuda") / n_c
+                del cgraph
+            conv = {"mode": "draft-block step alone, graph replay", "draft_ms": cms, "steps": n_c,
+                    "overhead": cms["rank64"] / cms["none"] - 1.0,
+                    "params": w.draft.layers * 4 * 3 * 64 * w.draft.hidden}
+        for L in eng.m["draft"]["layers"]:
+            L.pop("conv_w1", None)
+            L.pop("conv_w2", None)
+        eng.base_pos.copy_(base0)
+        eng.anchor.copy_(anchor0)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -542,7 +577,7 @@ def run_ours(args):
             "verified_tok_s": verified, "mean_accept": mean_accept,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise}
+            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise, "conv": conv}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

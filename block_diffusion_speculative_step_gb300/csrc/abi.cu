@@ -145,6 +145,17 @@ struct LayerScratch {
   float* apart;
   void* gpart;
   size_t gpart_bytes;
+  // DFlash 2 convolutions (draft layers with conv_rank > 0)
+  void* xc;    // [M][H] convolved projection input
+  float* yc;   // [M][H] sublayer output before its convolution
+  float* zc;   // [M][r] tap generator activations
+};
+
+// The four convolutions of one draft layer (w1 [4][r][H], w2 [4][2H][r]).
+struct LayerConv {
+  const void* w1;
+  const void* w2;
+  int r;
 };
 
 struct LayerShape {
@@ -199,7 +210,7 @@ AttnDesc attn_shape(const LayerShape& L) {
   return a;
 }
 
-void carve_layer(Bump& b, const LayerShape& L, int sms, LayerScratch& s) {
+void carve_layer(Bump& b, const LayerShape& L, int sms, LayerScratch& s, int conv_rank = 0) {
   const dflash_dims& d = L.d;
   const size_t es = elem_size(d.dtype);
   const size_t M = (size_t)L.S * L.rows;
@@ -217,6 +228,40 @@ void carve_layer(Bump& b, const LayerShape& L, int sms, LayerScratch& s) {
   for (auto& g : g4) gp = std::max(gp, gemm_scratch_bytes(g, sms));
   s.gpart_bytes = gp;
   s.gpart = b.take(gp);
+  s.xc = nullptr;
+  s.yc = nullptr;
+  s.zc = nullptr;
+  if (conv_rank > 0) {
+    s.xc = b.take(M * d.hidden * es);
+    s.yc = static_cast<float*>(b.take(M * d.hidden * sizeof(float)));
+    s.zc = static_cast<float*>(b.take(M * (size_t)conv_rank * sizeof(float)));
+  }
+}
+
+// Convolution `at` (0 attention input, 1 attention output, 2 MLP input, 3 MLP
+// output) of a draft layer over the M rows of u.
+static cudaError_t layer_conv(const LayerShape& L, const LayerConv& cv, int at, const void* u, void* out, int resid,
+                              const LayerScratch& s, cudaStream_t st) {
+  const dflash_dims& d = L.d;
+  const size_t es = elem_size(d.dtype);
+  ConvDesc c;
+  c.dtype = d.dtype;
+  c.M = L.S * L.rows;
+  c.H = d.hidden;
+  c.r = cv.r;
+  c.rows = L.rows;
+  c.w1 = static_cast<const char*>(cv.w1) + (size_t)at * cv.r * d.hidden * es;
+  c.w2 = static_cast<const char*>(cv.w2) + (size_t)at * 2 * d.hidden * cv.r * es;
+  c.u = u;
+  c.out = out;
+  c.resid = resid;
+  c.z = s.zc;
+  return launch_dyn_conv(c, st);
+}
+
+static double conv_bytes(const LayerShape& L, const LayerConv& cv) {
+  const double es = elem_size(L.d.dtype), M = (double)L.S * L.rows, H = L.d.hidden;
+  return 3.0 * cv.r * H * es + 2.0 * M * H * 4.0;
 }
 
 int check_layer_shape(const LayerShape& L, const char* who) {
@@ -244,7 +289,7 @@ int check_layer_shape(const LayerShape& L, const char* who) {
 
 int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_kv& kv, float* h,
               const int32_t* base_pos, const float* rope_cs, int rope_max_pos, void* tap, int tap_stride, int tap_offset,
-              const LayerScratch& s, const Ctx& c, int sms, cudaStream_t st) {
+              const LayerScratch& s, const Ctx& c, int sms, cudaStream_t st, const LayerConv* cv = nullptr) {
   const dflash_dims& d = L.d;
   const int M = L.S * L.rows, H = d.hidden;
   GemmDesc g4[4];
@@ -253,8 +298,9 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   const bool causal = L.mode == DFLASH_ATTN_CAUSAL;
 
   DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln1, M, H, d.rms_eps, s.x, st));
+  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 0, s.x, s.xc, 0, s, st));
   GemmDesc& qkv = g4[0];
-  qkv.X = s.x;
+  qkv.X = cv ? s.xc : s.x;
   qkv.q_out = s.q;
   qkv.k_dst[0] = causal ? kv.k : s.kb;
   qkv.v_dst[0] = causal ? kv.v : s.vb;
@@ -278,21 +324,28 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   a.status = c.status;
   DF_LAUNCH(st, TF_ATTN, 0, launch_attention(a, st));
 
+  // With convolutions the O and down projections store their output, which
+  // the convolution then adds to the residual.
   GemmDesc& o = g4[1];
   o.X = s.attn;
-  o.out_f32 = h;
+  o.out_f32 = cv ? s.yc : h;
+  if (cv) o.kind = EPI_STORE;
   DF_CUDA(run_gemm(o, s.gpart, s.gpart_bytes, c, sms, st));
+  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 1, s.yc, h, 1, s, st));
 
   DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x, st));
+  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 2, s.x, s.xc, 0, s, st));
   GemmDesc& gu = g4[2];
-  gu.X = s.x;
+  gu.X = cv ? s.xc : s.x;
   gu.act_out = s.act;
   DF_CUDA(run_gemm(gu, s.gpart, s.gpart_bytes, c, sms, st));
 
   GemmDesc& dn = g4[3];
   dn.X = s.act;
-  dn.out_f32 = h;
+  dn.out_f32 = cv ? s.yc : h;
+  if (cv) dn.kind = EPI_STORE;
   DF_CUDA(run_gemm(dn, s.gpart, s.gpart_bytes, c, sms, st));
+  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 3, s.yc, h, 1, s, st));
 
   if (tap) DF_LAUNCH(st, TF_TAP, 0, launch_store_tap(d.dtype, h, M, H, tap, tap_stride, tap_offset, st));
   return DFLASH_OK;
@@ -370,13 +423,13 @@ size_t carve_draft(Bump& b, const dflash_draft_args* a, int sms, DraftScratch& s
   for (int j = 0; j < a->n_layers; ++j) {
     Bump t(nullptr);
     LayerScratch tmp;
-    carve_layer(t, draft_layer_shape(a, j), sms, tmp);
+    carve_layer(t, draft_layer_shape(a, j), sms, tmp, a->conv_rank);
     if (t.off > bb) {
       bb = t.off;
       jbest = j;
     }
   }
-  carve_layer(b, draft_layer_shape(a, jbest), sms, s.ls);
+  carve_layer(b, draft_layer_shape(a, jbest), sms, s.ls, a->conv_rank);
   s.xf = b.take(M * d.hidden * elem_size(d.dtype));
   HeadDesc hd = head_shape(d, a->n_seqs, a->block, a->path_topk > 0 ? 2 : 0);
   hd.topk = a->path_topk;
@@ -647,9 +700,10 @@ static int draft_round(const dflash_draft_args* a, const DraftScratch& s, const 
   const int M = a->n_seqs * a->block;
   int rc;
   for (int j = 0; j < a->n_layers; ++j) {
+    const LayerConv cv = {a->conv_rank > 0 ? a->conv_w1[j] : nullptr, a->conv_rank > 0 ? a->conv_w2[j] : nullptr,
+                          a->conv_rank};
     rc = run_layer(draft_layer_shape(a, j), a->layers[j], a->kv_layers[j], s.h, a->base_pos, a->rope_cs,
-                   a->rope_max_pos, nullptr,
-                   0, 0, s.ls, c, sms, st);
+                   a->rope_max_pos, nullptr, 0, 0, s.ls, c, sms, st, a->conv_rank > 0 ? &cv : nullptr);
     if (rc) return rc;
   }
   DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, s.h, a->final_norm, M, d.hidden, d.rms_eps, s.xf, st));
@@ -705,6 +759,13 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
   DF_CHECK(a->denoise_rounds >= 0 && a->denoise_rounds <= DFLASH_MAX_DENOISE_ROUNDS,
            "%s: denoise_rounds must be in [0, %d]", who, DFLASH_MAX_DENOISE_ROUNDS);
+  DF_CHECK(a->conv_rank >= 0 && a->conv_rank <= DFLASH_MAX_CONV_RANK, "%s: conv_rank must be in [0, %d]", who,
+           DFLASH_MAX_CONV_RANK);
+  if (a->conv_rank > 0)
+    DF_CHECK(a->conv_rank % 8 == 0 && d.hidden % 8 == 0, "%s: convolutions need conv_rank %% 8 == 0 and hidden %% 8 == 0",
+             who);
+  for (int j = 0; a->conv_rank > 0 && j < a->n_layers; ++j)
+    DF_CHECK(a->conv_w1[j] && a->conv_w2[j], "%s: NULL convolution weights of layer %d", who, j);
   if (a->path_topk > 0) {
     DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
              "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);

@@ -50,6 +50,22 @@ struct GemmDesc {
   int inter;
 };
 
+// DFlash 2 dynamic depthwise convolution over M token rows (rows per
+// sequence = `rows`): z = SiLU(W1 u) into z [M][r], then y = u + a u + b u_prev
+// with (a, b) = W2 z; out = round(y) (resid = 0, out of the compute type) or
+// out += y (resid = 1, out and u fp32).
+struct ConvDesc {
+  int dtype;
+  int M, H, r, rows;
+  const void* w1;   // [r][H]
+  const void* w2;   // [2H][r]
+  const void* u;    // [M][H]: compute type (resid = 0) or fp32 (resid = 1)
+  void* out;        // [M][H]
+  int resid;
+  float* z;         // [M][r] scratch
+};
+cudaError_t launch_dyn_conv(const ConvDesc& c, cudaStream_t st);
+
 // Attention problem (see dflash_decoder_layer_forward).
 struct AttnDesc {
   int dtype;

@@ -16,7 +16,8 @@ enum TraceFamily : int {
   TF_TAP = 8,
   TF_CONVERT = 9,
   TF_SAMPLE = 10,
-  kTraceFamilies = 11
+  TF_CONV = 11,
+  kTraceFamilies = 12
 };
 
 void trace_pre(cudaStream_t st, int family);

@@ -32,7 +32,7 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
            "dflash_verify_accept_noalloc", "dflash_trace_launches", "dflash_sample_drafts",
            "dflash_sample_accept")
-DFLASH_TRACE_FAMILIES = 11
+DFLASH_TRACE_FAMILIES = 12
 
 
 class DFlashError(RuntimeError):
@@ -86,7 +86,8 @@ class dflash_draft_args(C.Structure):
                 ("lm_head", vp), ("n_seqs", i32), ("block", i32), ("anchor", vp), ("base_pos", vp),
                 ("mask_token", i32), ("max_pos", i32), ("rope_cs", vp), ("rope_max_pos", i32),
                 ("drafts", vp), ("logits", vp), ("path_topk", i32), ("path_rank", i32), ("path_u", vp),
-                ("path_v", vp), ("denoise_rounds", i32)]
+                ("path_v", vp), ("denoise_rounds", i32), ("conv_rank", i32),
+                ("conv_w1", vp * DFLASH_MAX_LAYERS), ("conv_w2", vp * DFLASH_MAX_LAYERS)]
 
 
 class dflash_verify_args(C.Structure):

@@ -93,6 +93,9 @@ class Engine:
         self.feats = z(S * max(B, prefill_chunk), self.F, H)
         self.ones = torch.ones(S, dtype=torch.int32, device=self.dev)
         self.ws = None
+        # DFlash 2 draft convolutions: on when the workload has them (the
+        # weights sit in the draft layers as conv_w1 / conv_w2)
+        self.conv_rank = w.conv_rank
         self.ws_bytes = 0
         self._size_workspace(fuse_rows)
         st = torch.cuda.current_stream()
@@ -140,7 +143,7 @@ class Engine:
         a.rope_max_pos = self.rope_max
         return a
 
-    def draft_args(self, logits=None, rounds: int = 1):
+    def draft_args(self, logits=None, rounds: int = 1, conv_rank: int | None = None):
         d = self.w.draft
         a = D.dflash_draft_args()
         a.dims = self.ddims
@@ -164,6 +167,12 @@ class Engine:
             a.path_topk, a.path_rank = self.w.path_topk, self.w.path_rank
             a.path_u, a.path_v = _ptr(self.m["path_u"]), _ptr(self.m["path_v"])
         a.denoise_rounds = rounds
+        r = self.conv_rank if conv_rank is None else conv_rank
+        if r:
+            a.conv_rank = r
+            for j in range(d.layers):
+                L = self.m["draft"]["layers"][j]
+                a.conv_w1[j], a.conv_w2[j] = _ptr(L["conv_w1"]), _ptr(L["conv_w2"])
         return a
 
     def verify_args(self, block: int, h, drafts=None, logits=None, update=True):
@@ -233,8 +242,8 @@ class Engine:
             D.dflash_decoder_layer_forward(self.target_layer_args(li, rows, self.h, tap, off, base_pos), self.ws_ptr,
                                            self.ws_bytes)
 
-    def draft(self, logits=None, rounds: int = 1):
-        D.dflash_draft_block(self.draft_args(logits, rounds), self.ws_ptr, self.ws_bytes)
+    def draft(self, logits=None, rounds: int = 1, conv_rank: int | None = None):
+        D.dflash_draft_block(self.draft_args(logits, rounds, conv_rank), self.ws_ptr, self.ws_bytes)
 
     def verify(self, block: int, drafts=None, logits=None):
         D.dflash_verify_accept(self.verify_args(block, self.h, drafts, logits), self.ws_ptr, self.ws_bytes)

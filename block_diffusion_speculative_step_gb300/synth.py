@@ -166,6 +166,18 @@ def make_model(w: Workload, seed: int = 0, device="cpu", std: float = 0.02, jitt
     return m
 
 
+def add_conv_weights(m: dict, w: Workload, rank: int, seed: int = 1, std: float = 0.02) -> None:
+    """Draw DFlash 2 convolution tap generators (conv_w1 [4][r][H], conv_w2
+    [4][2H][r]) into every draft layer of an existing model dict, from a
+    generator of their own on the model's device."""
+    L0 = m["draft"]["layers"][0]["w_o"]
+    dr = _Draw(seed, L0.device)
+    H = w.draft.hidden
+    for L in m["draft"]["layers"]:
+        L["conv_w1"] = dr.normal((4, rank, H), std, L0.dtype)
+        L["conv_w2"] = dr.normal((4, 2 * H, rank), std, L0.dtype)
+
+
 def make_tokens(seed: int, n: int, vocab: int, device="cpu") -> torch.Tensor:
     """n token ids uniform over [0, vocab-1) (the mask id vocab-1 excluded)."""
     g = torch.Generator(device=torch.device(device))

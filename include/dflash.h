@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 2
+#define DFLASH_ABI_VERSION 3
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -226,8 +226,21 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes,
  * drafts of round r-1] at the same positions, each round ending with its
  * argmax (or path walk).  drafts and logits hold the last round's.  0 and 1
  * both mean the single step; R <= DFLASH_MAX_DENOISE_ROUNDS.
+ *
+ * DFlash 2 two-tap dynamic depthwise convolutions (guide section 7): with
+ * conv_rank = r > 0 every draft layer j carries four convolutions, at the
+ * attention input (after its RMSNorm), the attention block's output (before
+ * the residual add), the MLP input and the MLP output, with tap generators
+ * conv_w1[j] ([4][r][H]) and conv_w2[j] ([4][2H][r]), in that order.  Over
+ * the block rows u_t of a sequence: z_t = SiLU(W1 u_t), (a_t, b_t) = W2 z_t
+ * (rows 0..H-1 of W2 give a, rows H..2H-1 give b), y_t = u_t + a_t u_t +
+ * b_t u_{t-1} per channel with u_{-1} = 0 (block row 1 reads the anchor,
+ * the last verified token).  Inputs of projections are rounded to the
+ * compute type after the convolution; outputs are added to the residual.
+ * r <= DFLASH_MAX_CONV_RANK.
  */
 #define DFLASH_MAX_DENOISE_ROUNDS 16
+#define DFLASH_MAX_CONV_RANK 128
 typedef struct {
   dflash_dims dims;
   int32_t n_layers;
@@ -250,6 +263,9 @@ typedef struct {
   const void* path_u;                     /* [R][H] */
   const void* path_v;                     /* [R][H] */
   int32_t denoise_rounds;                 /* 0 / 1 = single step, else R rounds */
+  int32_t conv_rank;                      /* 0 = no convolutions */
+  const void* conv_w1[DFLASH_MAX_LAYERS]; /* [4][r][H] per draft layer */
+  const void* conv_w2[DFLASH_MAX_LAYERS]; /* [4][2H][r] per draft layer */
 } dflash_draft_args;
 int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);
@@ -390,7 +406,7 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
  * the library attributes to the launches (weights + activations read and
  * written, each once), where it is known on the host; 0 otherwise.
  */
-#define DFLASH_TRACE_FAMILIES 11
+#define DFLASH_TRACE_FAMILIES 12
 typedef struct {
   char name[24];
   int32_t launches;
