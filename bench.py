@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--no-sampling", action="store_true", help="skip the sampling-mode cycle timing")
     p.add_argument("--no-denoise", action="store_true", help="skip the multi-round denoising draft timing")
     p.add_argument("--no-conv", action="store_true", help="skip the draft-convolution timing")
+    p.add_argument("--no-paged", action="store_true", help="skip the paged-KV cycle timing")
     p.add_argument("--layers", default="", help="T,D: shrink to T target / D draft layers (profiling captures "
                    "only; the line then names the reduced config)")
     return p.parse_args()
@@ -128,7 +129,7 @@ def setup_workload(w, seed: int = 0):
     S, B = w.batch, w.block
     lens = synth.make_ctx_lengths(seed + 7, w)
     ctx_max = max(lens)
-    cap = ((ctx_max + 2 * B + 63) // 64) * 64
+    cap = ((ctx_max + 2 * B + 127) // 128) * 128  # whole 128-slot pages (the paged-cache line)
     model = synth.make_model(w, seed=seed, device="cuda")
     fill_rows = 256
     eng = Engine(w, model, S, cap, prefill_chunk=B, fuse_rows=fill_rows)
@@ -566,6 +567,33 @@ def run_ours(args):
                          "workload's shapes; cycle extrapolated by layer counts; per-unit seconds " +
                          json.dumps({k: round(t, 3) for k, t in times.items()})}
 
+    # paged KV: the same cycle with the target and draft caches moved into
+    # 128-slot page pools handed out in a shuffled order (graph replay)
+    paged = None
+    if not args.no_paged and eng.has_target and eng.cap % 128 == 0 and eng.dcap % 128 == 0:
+        eng.page_caches(128, seed=0)
+        step()
+        torch.cuda.synchronize()
+        assert eng.status() == D.DFLASH_OK
+        same = bool(torch.equal(eng.accept_len.cpu(), accept))
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph):
+            step()
+        for _ in range(args.warmup):
+            pgraph.replay()
+        n_p = max(3, min(args.steps, 50))
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_p):
+            pgraph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_p = reduce_max(e0.elapsed_time(e1), world, "cuda") / n_p
+        paged = {"mode": "the same cycle on 128-slot KV pages (shuffled page order), graph replay",
+                 "ms_per_step": ms_p, "value": world * S * 1000.0 / ms_p, "unit": UNIT, "steps": n_p,
+                 "overhead_vs_contiguous": ms_p / ms_per_step - 1.0, "same_accept_lengths": same}
+        del pgraph
+
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded random-init weights, N(0,1) context)",
@@ -577,7 +605,8 @@ def run_ours(args):
             "verified_tok_s": verified, "mean_accept": mean_accept,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise, "conv": conv}
+            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise, "conv": conv,
+            "paged": paged}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

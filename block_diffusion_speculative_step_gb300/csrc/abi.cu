@@ -287,6 +287,29 @@ int check_layer_shape(const LayerShape& L, const char* who) {
   return DFLASH_OK;
 }
 
+// The shared fields of a page scatter (the per-layer pointers are the caller's).
+static KvScatter kv_scatter_base(const dflash_dims& d, int S, int rows, const int32_t* base_pos, const int32_t* valid,
+                                 int window, int cap, int rope_max_pos, const dflash_kv& kv, const Ctx& c) {
+  KvScatter k;
+  memset(&k, 0, sizeof(k));
+  k.dtype = d.dtype;
+  k.n_layers = 1;
+  k.S = S;
+  k.rows = rows;
+  k.nkv = d.n_kv_heads;
+  k.d = d.head_dim;
+  k.base_pos = base_pos;
+  k.valid = valid;
+  k.window = window;
+  k.cap = cap;
+  k.rope_max_pos = rope_max_pos;
+  k.ps = kv.page_size;
+  k.max_pages = kv.max_pages;
+  k.pool = kv.pool_pages;
+  k.status = c.status;
+  return k;
+}
+
 int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_kv& kv, float* h,
               const int32_t* base_pos, const float* rope_cs, int rope_max_pos, void* tap, int tap_stride, int tap_offset,
               const LayerScratch& s, const Ctx& c, int sms, cudaStream_t st, const LayerConv* cv = nullptr) {
@@ -302,20 +325,37 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   GemmDesc& qkv = g4[0];
   qkv.X = cv ? s.xc : s.x;
   qkv.q_out = s.q;
-  qkv.k_dst[0] = causal ? kv.k : s.kb;
-  qkv.v_dst[0] = causal ? kv.v : s.vb;
-  qkv.kv_cap = causal ? kv.capacity : L.rows;
+  // Causal rows go straight to their cache slots; bidirectional block rows
+  // and the rows of a paged cache go to the block scratch (a paged cache
+  // receives them from the page scatter below).
+  const bool direct = causal && kv.pages == nullptr;
+  qkv.k_dst[0] = direct ? kv.k : s.kb;
+  qkv.v_dst[0] = direct ? kv.v : s.vb;
+  qkv.kv_cap = direct ? kv.capacity : L.rows;
   qkv.kv_window = 0;
-  qkv.kv_slot_mode = causal ? 1 : 0;
+  qkv.kv_slot_mode = direct ? 1 : 0;
   qkv.rope_cs = rope_cs;
   qkv.rope_max_pos = rope_max_pos;
   DF_CUDA(run_gemm(qkv, s.gpart, s.gpart_bytes, c, sms, st));
+  if (causal && kv.pages) {
+    KvScatter ks = kv_scatter_base(L.d, L.S, L.rows, base_pos, nullptr, 0, kv.capacity, rope_max_pos, kv, c);
+    ks.kb[0] = s.kb;
+    ks.vb[0] = s.vb;
+    ks.kpool[0] = kv.k;
+    ks.vpool[0] = kv.v;
+    ks.pages[0] = kv.pages;
+    DF_LAUNCH(st, TF_PAGE, 0, launch_kv_page_scatter(ks, st));
+  }
 
   AttnDesc a = attn_shape(L);
   a.base_pos = base_pos;
   a.q = s.q;
   a.kc = kv.k;
   a.vc = kv.v;
+  a.pages = kv.pages;
+  a.ps = kv.page_size;
+  a.max_pages = kv.max_pages;
+  a.pool = kv.pool_pages;
   a.kb = s.kb;
   a.vb = s.vb;
   a.out = s.attn;
@@ -357,6 +397,17 @@ int check_ws(void* ws, size_t ws_bytes, size_t need, const char* who) {
     return fail(DFLASH_ERR_WORKSPACE, "%s: workspace %zu bytes, %zu required", who, ws_bytes, need);
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
     return fail(DFLASH_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  return DFLASH_OK;
+}
+
+// A paged cache: page size a multiple of the 128-key attention chunk,
+// capacity == max_pages * page_size.
+int check_kv_pages(const dflash_kv& kv, const char* who) {
+  if (!kv.pages) return DFLASH_OK;
+  DF_CHECK(kv.page_size > 0 && kv.page_size % 128 == 0, "%s: page_size must be a positive multiple of 128", who);
+  DF_CHECK(kv.max_pages > 0 && kv.pool_pages > 0, "%s: max_pages and pool_pages must be positive", who);
+  DF_CHECK((long)kv.max_pages * kv.page_size == kv.capacity, "%s: capacity must equal max_pages * page_size", who);
+  DF_CHECK((long)kv.pool_pages * kv.page_size <= (1L << 30), "%s: page pool too large", who);
   return DFLASH_OK;
 }
 
@@ -585,6 +636,8 @@ int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws
   rc = check_weights(a->w, who);
   if (rc) return rc;
   DF_CHECK(a->base_pos && a->h && a->kv.k && a->kv.v && a->rope_cs, "%s: NULL pointer", who);
+  rc = check_kv_pages(a->kv, who);
+  if (rc) return rc;
   LayerShape L = layer_shape_of(a);
   rc = check_layer_shape(L, who);
   if (rc) return rc;
@@ -607,7 +660,7 @@ int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws
 // ---------------------------------------------------------------- fusion
 
 static size_t fuse_ws(const dflash_fuse_args* a, int sms, float** z, void** cbuf, void** gpart, size_t* gp,
-                      char* base) {
+                      char* base, void** kscr = nullptr, void** vscr = nullptr) {
   const dflash_dims& d = a->dims;
   const size_t M = (size_t)a->n_seqs * a->rows;
   Bump b(base);
@@ -627,6 +680,15 @@ static size_t fuse_ws(const dflash_fuse_args* a, int sms, float** z, void** cbuf
   kv.d = d.head_dim;
   *gp = std::max(gemm_scratch_bytes(fc, sms), gemm_scratch_bytes(kv, sms));
   *gpart = b.take(*gp);
+  if (a->kv_layers[0].pages) {  // block scratch per layer for the page scatter
+    const size_t blk = M * d.n_kv_heads * d.head_dim * elem_size(d.dtype);
+    for (int j = 0; j < a->n_layers; ++j) {
+      void* k = b.take(blk);
+      void* v = b.take(blk);
+      if (kscr) kscr[j] = k;
+      if (vscr) vscr[j] = v;
+    }
+  }
   return b.off;
 }
 
@@ -643,6 +705,15 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
   DF_CHECK(a->n_seqs > 0 && a->rows > 0, "%s: n_seqs and rows must be positive", who);
   const int cap = a->kv_layers[0].capacity, win = a->kv_layers[0].window;
   for (int j = 0; j < a->n_layers; ++j) {
+    const int rc2 = check_kv_pages(a->kv_layers[j], who);
+    if (rc2) return rc2;
+    DF_CHECK((a->kv_layers[j].pages == nullptr) == (a->kv_layers[0].pages == nullptr) &&
+                 a->kv_layers[j].page_size == a->kv_layers[0].page_size &&
+                 a->kv_layers[j].max_pages == a->kv_layers[0].max_pages &&
+                 a->kv_layers[j].pool_pages == a->kv_layers[0].pool_pages,
+             "%s: every layer's context cache must share its paging geometry", who);
+  }
+  for (int j = 0; j < a->n_layers; ++j) {
     DF_CHECK(a->w_qkv_layers[j] && a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL layer %d pointer", who, j);
     DF_CHECK(a->kv_layers[j].capacity == cap && a->kv_layers[j].window == win,
              "%s: every layer's context cache must share capacity and window", who);
@@ -654,7 +725,9 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
   size_t gp;
   rc = check_ws(ws, ws_bytes, fuse_ws(a, sms, &z, &cbuf, &gpart, &gp, nullptr), who);
   if (rc) return rc;
-  fuse_ws(a, sms, &z, &cbuf, &gpart, &gp, static_cast<char*>(ws));
+  void* kscr[DFLASH_MAX_LAYERS] = {};
+  void* vscr[DFLASH_MAX_LAYERS] = {};
+  fuse_ws(a, sms, &z, &cbuf, &gpart, &gp, static_cast<char*>(ws), kscr, vscr);
   Ctx c = header(ws);
   cudaStream_t st = (cudaStream_t)stream;
   const int M = a->n_seqs * a->rows;
@@ -671,10 +744,12 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
 
   GemmDesc kv = gemm_base(d.dtype, M, d.hidden, cbuf, a->base_pos, a->valid, a->rows);
   kv.nseg = a->n_layers;
+  const bool paged = a->kv_layers[0].pages != nullptr;
   for (int j = 0; j < a->n_layers; ++j) {
     kv.seg_w[j] = a->w_qkv_layers[j];
-    kv.k_dst[j] = a->kv_layers[j].k;
-    kv.v_dst[j] = a->kv_layers[j].v;
+    // a paged cache receives its rows from the page scatter below
+    kv.k_dst[j] = paged ? kscr[j] : a->kv_layers[j].k;
+    kv.v_dst[j] = paged ? vscr[j] : a->kv_layers[j].v;
   }
   kv.seg_row0 = d.n_q_heads * d.head_dim;
   kv.seg_rows = 2 * d.n_kv_heads * d.head_dim;
@@ -682,12 +757,25 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
   kv.nq = d.n_q_heads;
   kv.nkv = d.n_kv_heads;
   kv.d = d.head_dim;
-  kv.kv_cap = cap;
-  kv.kv_window = win;
-  kv.kv_slot_mode = 1;
+  kv.kv_cap = paged ? a->rows : cap;
+  kv.kv_window = paged ? 0 : win;
+  kv.kv_slot_mode = paged ? 0 : 1;
   kv.rope_cs = a->rope_cs;
   kv.rope_max_pos = a->rope_max_pos;
   DF_CUDA(run_gemm(kv, gpart, gp, c, sms, st));
+  if (paged) {
+    KvScatter ks = kv_scatter_base(d, a->n_seqs, a->rows, a->base_pos, a->valid, win, cap, a->rope_max_pos,
+                                   a->kv_layers[0], c);
+    ks.n_layers = a->n_layers;
+    for (int j = 0; j < a->n_layers; ++j) {
+      ks.kb[j] = kscr[j];
+      ks.vb[j] = vscr[j];
+      ks.kpool[j] = a->kv_layers[j].k;
+      ks.vpool[j] = a->kv_layers[j].v;
+      ks.pages[j] = a->kv_layers[j].pages;
+    }
+    DF_LAUNCH(st, TF_PAGE, 0, launch_kv_page_scatter(ks, st));
+  }
   return DFLASH_OK;
 }
 
@@ -775,6 +863,8 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
     rc = check_weights(a->layers[j], who);
     if (rc) return rc;
     DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
+    rc = check_kv_pages(a->kv_layers[j], who);
+    if (rc) return rc;
     rc = check_layer_shape(draft_layer_shape(a, j), who);
     if (rc) return rc;
   }

@@ -12,7 +12,7 @@ namespace dfl {
 enum : uint32_t {
   ST_NUMERIC = 1u,  // NaN reached an argmax
   ST_TIMEOUT = 2u,  // a bounded wait gave up
-  ST_RANGE = 4u,    // a token id read on the device lay outside the vocabulary
+  ST_RANGE = 4u,    // a token id (vocabulary) or KV page id (pool) read on the device was out of range
 };
 
 // Workspace header: status word + arrival counters of the last-CTA reductions.
@@ -93,6 +93,27 @@ struct RowMap {
   __device__ __forceinline__ int pos(int m) const { return base_pos[m / rows] + m % rows; }
   __device__ __forceinline__ bool live(int m) const {
     return valid == nullptr || (m % rows) < valid[m / rows];
+  }
+};
+
+// Where cache slot `slot` of sequence s lives.  Contiguous caches
+// [S][nkv][cap][d] (pages == nullptr), or paged pools [pool][nkv][ps][d]
+// with the page table pages[s * max_pages + slot / ps].  row0() is the row
+// (in head_dim vectors) of KV head 0; KV head g adds g * head_rows().  An
+// unmapped page id (outside [0, pool)) sets *bad and maps to page 0, so no
+// access leaves the pool.
+struct KvMap {
+  const int32_t* pages;
+  int cap, ps, max_pages, pool, nkv;
+  __host__ __device__ __forceinline__ int head_rows() const { return pages ? ps : cap; }
+  __device__ __forceinline__ uint32_t row0(int s, int slot, bool* bad) const {
+    if (!pages) return (uint32_t)(s * nkv) * (uint32_t)cap + (uint32_t)slot;
+    int pg = __ldg(pages + (size_t)s * max_pages + slot / ps);
+    if (pg < 0 || pg >= pool) {
+      *bad = true;
+      pg = 0;
+    }
+    return (uint32_t)(pg * nkv) * (uint32_t)ps + (uint32_t)(slot % ps);
   }
 };
 

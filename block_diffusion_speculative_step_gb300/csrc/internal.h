@@ -66,6 +66,27 @@ struct ConvDesc {
 };
 cudaError_t launch_dyn_conv(const ConvDesc& c, cudaStream_t st);
 
+// Paged KV caches: copy the K/V rows that a projection wrote into the
+// contiguous block scratch [S][nkv][rows][d] (per layer) to their cache
+// slots in the page pools.  Row m of sequence s = m / rows is copied when it
+// is live (valid), its position base_pos[s] + m % rows lies in
+// [0, rope_max_pos) and its slot (position, or position % window) is below
+// the capacity -- the rows the projection's epilogue wrote.
+struct KvScatter {
+  int dtype, n_layers, S, rows, nkv, d;
+  const int32_t* base_pos;
+  const int32_t* valid;
+  int window, cap, rope_max_pos;
+  const void* kb[kMaxSeg];
+  const void* vb[kMaxSeg];
+  void* kpool[kMaxSeg];
+  void* vpool[kMaxSeg];
+  const int32_t* pages[kMaxSeg];
+  int ps, max_pages, pool;
+  uint32_t* status;
+};
+cudaError_t launch_kv_page_scatter(const KvScatter& k, cudaStream_t st);
+
 // Attention problem (see dflash_decoder_layer_forward).
 struct AttnDesc {
   int dtype;
@@ -73,9 +94,11 @@ struct AttnDesc {
   int n_seqs, rows, nq, nkv, d;
   const int32_t* base_pos;
   const void* q;              // [M][nq*d]
-  const void* kc;             // cache [S][nkv][cap][d]
+  const void* kc;             // cache [S][nkv][cap][d], or a page pool [pool][nkv][ps][d]
   const void* vc;
   int cap, window;
+  const int32_t* pages;       // page table [S][max_pages] (paged caches) or null
+  int ps, max_pages, pool;
   const void* kb;             // block scratch [S][nkv][rows][d] (bidir)
   const void* vb;
   void* out;                  // [M][nq*d]

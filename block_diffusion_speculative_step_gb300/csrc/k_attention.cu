@@ -106,8 +106,12 @@ __device__ __forceinline__ void chunk_keys(const AttnDesc& a, const SeqKeys& sk,
     slot0 = -1;  // block chunk: every key visible
   } else {
     slot0 = c * CH;
-    kp = reinterpret_cast<const T*>(a.kc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
-    vp = reinterpret_cast<const T*>(a.vc) + (((size_t)s * a.nkv + g) * a.cap + slot0) * d;
+    const KvMap km{a.pages, a.cap, a.ps, a.max_pages, a.pool, a.nkv};
+    bool bad = false;
+    const size_t row = (size_t)km.row0(s, slot0, &bad) + (size_t)g * km.head_rows();
+    if (bad) raise_status(a.status, ST_RANGE);  // read from page 0 instead
+    kp = reinterpret_cast<const T*>(a.kc) + row * d;
+    vp = reinterpret_cast<const T*>(a.vc) + row * d;
     nk = min(CH, sk.n_ctx - slot0);
   }
 }
@@ -414,9 +418,14 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
   const uint32_t kvb = __cvta_generic_to_shared(KV);
 
   // chunk c -> (is block chunk, first tensor row)
+  const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
   auto chunk_row = [&](int c, bool& blk) -> int {
     blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
-    return blk ? (s * nkv + g) * rows : (s * nkv + g) * cap + c * CH;
+    if (blk) return (s * nkv + g) * rows;
+    bool bad = false;
+    const int r = (int)(km.row0(s, c * CH, &bad) + (uint32_t)g * (uint32_t)km.head_rows());
+    if (bad) raise_status(status, ST_RANGE);  // read from page 0 instead
+    return r;
   };
   auto issue = [&](int c, int buf) {  // one thread
     bool blk;
@@ -779,9 +788,14 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   const int nq_tile = min(kClQT, nqv - qv0);
   const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
 
+  const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
   auto chunk_row = [&](int c, bool& blk) -> int {
     blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
-    return blk ? (s * nkv + g) * rows : (s * nkv + g) * cap + c * CH;
+    if (blk) return (s * nkv + g) * rows;
+    bool bad = false;
+    const int r = (int)(km.row0(s, c * CH, &bad) + (uint32_t)g * (uint32_t)km.head_rows());
+    if (bad) raise_status(status, ST_RANGE);  // read from page 0 instead
+    return r;
   };
   auto issue = [&](int c, int buf) {  // one thread
     bool blk;
@@ -1149,7 +1163,7 @@ template <int D>
 bool attn_maps(const AttnDesc& a, AttnTma& p) {
   memset(&p, 0, sizeof(p));
   p.a = a;
-  const uint64_t crow = (uint64_t)a.n_seqs * a.nkv * a.cap;
+  const uint64_t crow = a.pages ? (uint64_t)a.pool * a.nkv * a.ps : (uint64_t)a.n_seqs * a.nkv * a.cap;
   if (!make_tmap_bf16(&p.kc, a.kc, D, crow, kMmaCH) || !make_tmap_bf16(&p.vc, a.vc, D, crow, kMmaCH)) return false;
   if (a.mode == DFLASH_ATTN_BLOCK_BIDIR) {
     const uint64_t brow = (uint64_t)a.n_seqs * a.nkv * a.rows;

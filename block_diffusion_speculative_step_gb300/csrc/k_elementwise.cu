@@ -178,4 +178,44 @@ cudaError_t launch_to_f32(int dtype, const void* src, size_t n, float* dst, cuda
   return cudaGetLastError();
 }
 
+// Paged KV caches: row m of the block scratch (sequence s = m / rows, in-block
+// index i = m % rows) goes to its slot's page, KV head by KV head, in 16-byte
+// pieces.  Grid: (S * rows, n_layers); one CTA moves one row's K and V.
+template <typename T>
+__global__ void __launch_bounds__(128) kv_page_scatter_kernel(const __grid_constant__ KvScatter k) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x, layer = blockIdx.y;
+  const int s = m / k.rows, i = m % k.rows;
+  if (k.valid && i >= __ldg(k.valid + s)) return;
+  const int pos = __ldg(k.base_pos + s) + i;
+  if (pos < 0 || pos >= k.rope_max_pos) return;
+  const int slot = k.window > 0 ? pos % k.window : pos;
+  if (slot >= k.cap) return;
+  const KvMap km{k.pages[layer], k.cap, k.ps, k.max_pages, k.pool, k.nkv};
+  bool bad = false;
+  const size_t r0 = km.row0(s, slot, &bad);
+  if (bad) {
+    if (threadIdx.x == 0) raise_status(k.status, ST_RANGE);
+    return;
+  }
+  const int per_head = k.d * (int)sizeof(T) / 16;  // 16-byte pieces per head row
+  for (int t = threadIdx.x; t < 2 * k.nkv * per_head; t += blockDim.x) {
+    const int is_v = t / (k.nkv * per_head), rem = t % (k.nkv * per_head);
+    const int g = rem / per_head, piece = rem % per_head;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(is_v ? k.vb[layer] : k.kb[layer]) +
+                                                      (((size_t)s * k.nkv + g) * k.rows + i) * k.d) + piece;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(is_v ? k.vpool[layer] : k.kpool[layer]) +
+                                          (r0 + (size_t)g * k.ps) * k.d) + piece;
+    *dst = *src;
+  }
+}
+
+cudaError_t launch_kv_page_scatter(const KvScatter& k, cudaStream_t st) {
+  if (k.S == 0 || k.rows == 0) return cudaSuccess;
+  const dim3 grid(k.S * k.rows, k.n_layers);
+  if (k.dtype == DFLASH_BF16) return launch_pdl(kv_page_scatter_kernel<__nv_bfloat16>, grid, dim3(128), 0, st, k);
+  return launch_pdl(kv_page_scatter_kernel<float>, grid, dim3(128), 0, st, k);
+}
+
 }  // namespace dfl

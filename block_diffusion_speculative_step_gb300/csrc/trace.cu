@@ -29,7 +29,7 @@ thread_local TraceState g_trace;
 
 const char* kFamilyNames[kTraceFamilies] = {"embed",      "rmsnorm", "gemm_simt", "gemm_tc",
                                             "attention",  "lm_head", "path",      "rope_table",
-                                            "tap_store",  "convert", "sample",  "conv"};
+                                            "tap_store",  "convert", "sample",  "conv",   "kv_page"};
 }  // namespace
 
 // Inside stream capture an external record becomes an event node of the

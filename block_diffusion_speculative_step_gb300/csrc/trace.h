@@ -17,7 +17,8 @@ enum TraceFamily : int {
   TF_CONVERT = 9,
   TF_SAMPLE = 10,
   TF_CONV = 11,
-  kTraceFamilies = 12
+  TF_PAGE = 12,
+  kTraceFamilies = 13
 };
 
 void trace_pre(cudaStream_t st, int family);

@@ -32,7 +32,7 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
            "dflash_verify_accept_noalloc", "dflash_trace_launches", "dflash_sample_drafts",
            "dflash_sample_accept")
-DFLASH_TRACE_FAMILIES = 12
+DFLASH_TRACE_FAMILIES = 13
 
 
 class DFlashError(RuntimeError):
@@ -54,7 +54,8 @@ class dflash_dims(C.Structure):
 
 
 class dflash_kv(C.Structure):
-    _fields_ = [("k", vp), ("v", vp), ("capacity", i32), ("window", i32)]
+    _fields_ = [("k", vp), ("v", vp), ("capacity", i32), ("window", i32), ("pages", vp), ("page_size", i32),
+                ("max_pages", i32), ("pool_pages", i32)]
 
 
 class dflash_layer_weights(C.Structure):

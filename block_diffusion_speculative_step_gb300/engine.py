@@ -93,6 +93,7 @@ class Engine:
         self.feats = z(S * max(B, prefill_chunk), self.F, H)
         self.ones = torch.ones(S, dtype=torch.int32, device=self.dev)
         self.ws = None
+        self.paging = {}  # "t" / "d" -> (page table, page size, max pages, pool pages) once paged
         # DFlash 2 draft convolutions: on when the workload has them (the
         # weights sit in the draft layers as conv_w1 / conv_w2)
         self.conv_rank = w.conv_rank
@@ -113,7 +114,7 @@ class Engine:
         a.n_seqs, a.rows = self.S, rows
         a.base_pos = _ptr(self.base_pos if base_pos is None else base_pos)
         a.h = _ptr(h)
-        a.kv = D.dflash_kv(_ptr(self.caches.tk[li]), _ptr(self.caches.tv[li]), self.cap, 0)
+        a.kv = self._kv("t", li)
         a.attn_mode = D.DFLASH_ATTN_CAUSAL
         a.max_pos = self.cap
         a.rope_cs = _ptr(self.rope_t)
@@ -134,7 +135,7 @@ class Engine:
         a.n_layers = d.layers
         for j in range(d.layers):
             a.w_qkv_layers[j] = _ptr(self.m["draft"]["layers"][j]["w_qkv"])
-            a.kv_layers[j] = D.dflash_kv(_ptr(self.caches.dk[j]), _ptr(self.caches.dv[j]), self.dcap, self.w.window)
+            a.kv_layers[j] = self._kv("d", j)
         a.feats = _ptr(feats)
         a.n_seqs, a.rows = self.S, rows
         a.base_pos = _ptr(base_pos)
@@ -143,6 +144,61 @@ class Engine:
         a.rope_max_pos = self.rope_max
         return a
 
+    def _kv(self, kind: str, j: int):
+        """The dflash_kv of target ("t") or draft-context ("d") cache layer j."""
+        if kind == "t":
+            k, v, cap, win = self.caches.tk[j], self.caches.tv[j], self.cap, 0
+        else:
+            k, v, cap, win = self.caches.dk[j], self.caches.dv[j], self.dcap, self.w.window
+        kv = D.dflash_kv(_ptr(k), _ptr(v), cap, win)
+        if kind in self.paging:
+            table, ps, mp, pool = self.paging[kind]
+            kv.pages, kv.page_size, kv.max_pages, kv.pool_pages = _ptr(table), ps, mp, pool
+        return kv
+
+    def page_caches(self, page_size: int = 128, seed: int = 0, spare_pages: int = 0):
+        """Move the target and draft-context caches into page pools
+        [pool][n_kv][page_size][head_dim] whose pages are handed out in a
+        seeded random order (page table [S][max_pages], one table per cache
+        kind shared by its layers), copying the current contents; the calls
+        then address the caches through the page tables.  spare_pages adds
+        unmapped pages to each pool."""
+        g = torch.Generator().manual_seed(seed)
+        for kind, ks, vs, cap in (("t", self.caches.tk, self.caches.tv, self.cap),
+                                  ("d", self.caches.dk, self.caches.dv, self.dcap)):
+            if not ks:
+                continue
+            assert cap % page_size == 0, "capacity must be a multiple of the page size"
+            mp = cap // page_size
+            S, nkv, _, d = ks[0].shape
+            pool = S * mp + spare_pages
+            table = torch.randperm(pool, generator=g)[:S * mp].view(S, mp).to(torch.int32)
+            idx = table.view(-1).long().to(self.dev)
+            for lst in (ks, vs):
+                for j, c in enumerate(lst):
+                    pages = c.view(S, nkv, mp, page_size, d).permute(0, 2, 1, 3, 4).reshape(S * mp, nkv, page_size, d)
+                    p = torch.zeros(pool, nkv, page_size, d, dtype=c.dtype, device=self.dev)
+                    p[idx] = pages
+                    lst[j] = p
+            self.paging[kind] = (table.to(self.dev), page_size, mp, pool)
+
+    def unpaged_caches(self):
+        """The caches' contents in the contiguous layout [S][n_kv][cap][d]
+        (copies when paged)."""
+        out = {}
+        for kind, ks, vs, cap in (("t", self.caches.tk, self.caches.tv, self.cap),
+                                  ("d", self.caches.dk, self.caches.dv, self.dcap)):
+            if kind not in self.paging:
+                out[kind] = ([c.clone() for c in ks], [c.clone() for c in vs])
+                continue
+            table, ps, mp, pool = self.paging[kind]
+            idx = table.view(-1).long()
+            S = table.shape[0]
+            conv = lambda p: p[idx].view(S, mp, p.shape[1], ps, p.shape[3]).permute(0, 2, 1, 3, 4).reshape(
+                S, p.shape[1], mp * ps, p.shape[3])
+            out[kind] = ([conv(p) for p in ks], [conv(p) for p in vs])
+        return out
+
     def draft_args(self, logits=None, rounds: int = 1, conv_rank: int | None = None):
         d = self.w.draft
         a = D.dflash_draft_args()
@@ -150,7 +206,7 @@ class Engine:
         a.n_layers = d.layers
         for j in range(d.layers):
             a.layers[j] = layer_weights(self.m["draft"]["layers"][j])
-            a.kv_layers[j] = D.dflash_kv(_ptr(self.caches.dk[j]), _ptr(self.caches.dv[j]), self.dcap, self.w.window)
+            a.kv_layers[j] = self._kv("d", j)
         a.final_norm = _ptr(self.m["draft"]["final_norm"])
         a.embed = _ptr(self.m["embed"])
         a.lm_head = _ptr(self.m["lm_head"])

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 3
+#define DFLASH_ABI_VERSION 4
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -98,14 +98,33 @@ typedef struct {
   int32_t dtype;        /* dflash_dtype */
 } dflash_dims;
 
-/* One layer's KV cache: k, v each [n_seqs][n_kv][capacity][head_dim]. */
+/*
+ * One layer's KV cache.  Contiguous (pages == NULL): k, v each
+ * [n_seqs][n_kv][capacity][head_dim].
+ *
+ * Paged (pages != NULL; serving-style batches whose sequences hold very
+ * different lengths): k, v are page pools [pool_pages][n_kv][page_size]
+ * [head_dim], and sequence s's cache slots [i*page_size, (i+1)*page_size)
+ * live in pool page pages[s*max_pages + i].  capacity == max_pages *
+ * page_size, page_size a multiple of 128 (one attention chunk never spans
+ * two pages).  Only the pages a sequence reaches need to be mapped; a page
+ * id outside [0, pool_pages) that a kernel meets raises DFLASH_ERR_INVALID_ARG
+ * in the status word: its writes are skipped, its reads come from page 0.
+ * With a window the ring slots (position % window) are paged the same way.
+ * The arithmetic does not depend on the layout: a paged call returns what
+ * the contiguous call returns, bit for bit.
+ */
 typedef struct {
   void* k;
   void* v;
-  int32_t capacity; /* slots per (sequence, kv head) */
-  int32_t window;   /* 0: slot = position.  >0: ring of `window` slots
-                       (capacity == window), slot = position % window; the
-                       draft then sees the last `window` positions only. */
+  int32_t capacity;      /* slots per (sequence, kv head) */
+  int32_t window;        /* 0: slot = position.  >0: ring of `window` slots
+                            (capacity == window), slot = position % window; the
+                            draft then sees the last `window` positions only. */
+  const int32_t* pages;  /* NULL, or the page table [n_seqs][max_pages] */
+  int32_t page_size;
+  int32_t max_pages;
+  int32_t pool_pages;
 } dflash_kv;
 
 typedef struct {
@@ -406,7 +425,7 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
  * the library attributes to the launches (weights + activations read and
  * written, each once), where it is known on the host; 0 otherwise.
  */
-#define DFLASH_TRACE_FAMILIES 12
+#define DFLASH_TRACE_FAMILIES 13
 typedef struct {
   char name[24];
   int32_t launches;
