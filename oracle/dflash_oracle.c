@@ -593,22 +593,79 @@ static double gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint
   return -log(-log(or_uniform(seed, v, pos, seq, purpose, cycle)));
 }
 
-/* log sum_v exp(l_v / T) */
-static double row_lse(const float* l, int V, double T) {
+/* ------------------------------------------------- top-k / top-p filter
+ *
+ * The pages name sampling but no filter; the usual one is read here.  The
+ * entries of a row are ordered by logit (descending; lower index first on
+ * equal logits), which is the order of l / T for any T > 0.  top_k > 0
+ * keeps the first top_k; then top_p < 1 keeps the shortest prefix of those
+ * whose probability mass, softmax(l / T) renormalised over them, reaches
+ * top_p.  keep[v] = 1 for the kept entries; returns their number.  *pmargin
+ * (near-tie reporting) = the smallest |cumulative mass - top_p| on either
+ * side of the top-p boundary, +inf when top-p is off.
+ */
+static const float* g_sort_row;
+static int by_logit_desc(const void* x, const void* y) {
+  const int a = *(const int*)x, b = *(const int*)y;
+  const float la = g_sort_row[a], lb = g_sort_row[b];
+  if (la > lb) return -1;
+  if (la < lb) return 1;
+  return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+int or_filter_row(const float* l, int V, double T, int top_k, double top_p, unsigned char* keep,
+                  double* pmargin) {
+  if (V <= 0) return 0;
+  int* order = malloc(sizeof(int) * (size_t)V);
+  for (int v = 0; v < V; ++v) order[v] = v;
+  g_sort_row = l;
+  qsort(order, (size_t)V, sizeof(int), by_logit_desc);
+  int n = (top_k > 0 && top_k < V) ? top_k : V;
+  double mg = INFINITY;
+  if (top_p < 1.0) {
+    const double mx = (double)l[order[0]] / T;
+    double z = 0.0;
+    for (int i = 0; i < n; ++i) z += exp((double)l[order[i]] / T - mx);
+    double cum = 0.0;
+    int cut = n;
+    for (int i = 0; i < n; ++i) {
+      const double before = cum;
+      cum += exp((double)l[order[i]] / T - mx);
+      if (cum >= top_p * z) {
+        cut = i + 1;
+        mg = fmin(fabs(before / z - top_p), fabs(cum / z - top_p));
+        break;
+      }
+    }
+    n = cut;
+  }
+  memset(keep, 0, (size_t)V);
+  for (int i = 0; i < n; ++i) keep[order[i]] = 1;
+  free(order);
+  if (pmargin) *pmargin = mg;
+  return n;
+}
+
+/* log sum_v exp(l_v / T) over the kept entries (keep == NULL: all) */
+static double row_lse_k(const float* l, int V, double T, const unsigned char* keep) {
   double mx = -INFINITY;
-  for (int v = 0; v < V; ++v) mx = fmax(mx, (double)l[v] / T);
+  for (int v = 0; v < V; ++v)
+    if (!keep || keep[v]) mx = fmax(mx, (double)l[v] / T);
   double s = 0.0;
-  for (int v = 0; v < V; ++v) s += exp((double)l[v] / T - mx);
+  for (int v = 0; v < V; ++v)
+    if (!keep || keep[v]) s += exp((double)l[v] / T - mx);
   return mx + log(s);
 }
 
-/* A draw from softmax(l / T): argmax_v l_v / T + g_v (lowest index on ties).
- * Returns the token; *lse = log sum exp(l / T); *margin = best - second. */
-int or_sample_row(const float* l, int V, double T, uint64_t seed, int pos, int seq, int purpose, int cycle,
-                  double* lse, double* margin) {
+/* A draw from softmax(l / T) restricted to the kept entries (keep == NULL:
+ * all): argmax_v l_v / T + g_v (lowest index on ties).  Returns the token;
+ * *lse = log sum exp(l / T) over the kept entries; *margin = best - second. */
+int or_sample_row_f(const float* l, int V, double T, const unsigned char* keep, uint64_t seed, int pos, int seq,
+                    int purpose, int cycle, double* lse, double* margin) {
   int bi = -1;
   double best = -INFINITY, second = -INFINITY;
   for (int v = 0; v < V; ++v) {
+    if (keep && !keep[v]) continue;
     const double sc = (double)l[v] / T + gumbel(seed, (uint32_t)v, (uint32_t)pos, (uint32_t)seq, (uint32_t)purpose,
                                                 (uint32_t)cycle);
     if (bi < 0 || sc > best) {
@@ -619,28 +676,39 @@ int or_sample_row(const float* l, int V, double T, uint64_t seed, int pos, int s
       second = sc;
     }
   }
-  if (lse) *lse = row_lse(l, V, T);
+  if (lse) *lse = row_lse_k(l, V, T, keep);
   if (margin) *margin = best - second;
   return bi;
 }
 
+int or_sample_row(const float* l, int V, double T, uint64_t seed, int pos, int seq, int purpose, int cycle,
+                  double* lse, double* margin) {
+  return or_sample_row_f(l, V, T, NULL, seed, pos, seq, purpose, cycle, lse, margin);
+}
+
 /* One sequence's block: target logits tl [B][V] (row j: position P+j+1),
  * draft logits dl [B-1][V] (row i: block row i+1, position P+i+1), drafts
- * [B-1].  Writes out_tokens[0..k] and returns the accept length k.
- * *margin = the smallest decision margin met (acceptance tests and the final
- * draw), for near-tie reporting. */
-int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const int* drafts, double T,
-                          uint64_t seed, int seq, int P, int cycle, int* out_tokens, double* margin) {
+ * [B-1]; keep_t [B][V] / keep_d [B-1][V] the filtered entries of each row
+ * (NULL: all).  p and q are the filtered, renormalised softmax(l / T): an
+ * entry outside its row's kept set has probability 0.  Writes
+ * out_tokens[0..k] and returns the accept length k.  *margin = the smallest
+ * decision margin met (acceptance tests and the final draw), for near-tie
+ * reporting. */
+int or_spec_sample_accept_f(int B, int V, const float* tl, const float* dl, const unsigned char* keep_t,
+                            const unsigned char* keep_d, const int* drafts, double T, uint64_t seed, int seq, int P,
+                            int cycle, int* out_tokens, double* margin) {
   double mg = INFINITY;
   int k = 0;
   for (int j = 1; j <= B - 1; ++j) {
     const int d = drafts[j - 1];
     const float* trow = tl + (size_t)(j - 1) * V;
     const float* drow = dl + (size_t)(j - 1) * V;
-    const double lp = (double)trow[d] / T - row_lse(trow, V, T);
-    const double lq = (double)drow[d] / T - row_lse(drow, V, T);
+    const unsigned char* kt = keep_t ? keep_t + (size_t)(j - 1) * V : NULL;
+    const unsigned char* kd = keep_d ? keep_d + (size_t)(j - 1) * V : NULL;
+    const double lp = (kt && !kt[d]) ? -INFINITY : (double)trow[d] / T - row_lse_k(trow, V, T, kt);
+    const double lq = (double)drow[d] / T - row_lse_k(drow, V, T, kd);
     const double lu = log(or_uniform(seed, 0u, (uint32_t)(P + j), (uint32_t)seq, OR_RNG_ACCEPT, (uint32_t)cycle));
-    mg = fmin(mg, fabs(lu - (lp - lq)));
+    if (lp > -INFINITY) mg = fmin(mg, fabs(lu - (lp - lq)));
     if (!(lu < lp - lq)) break;
     out_tokens[k++] = d;
   }
@@ -650,11 +718,15 @@ int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const 
     /* residual max(0, p - q) at the rejected row, by exponential race */
     const float* trow = tl + (size_t)k * V;
     const float* drow = dl + (size_t)k * V;
-    const double lt = row_lse(trow, V, T), ld = row_lse(drow, V, T);
+    const unsigned char* kt = keep_t ? keep_t + (size_t)k * V : NULL;
+    const unsigned char* kd = keep_d ? keep_d + (size_t)k * V : NULL;
+    const double lt = row_lse_k(trow, V, T, kt), ld = row_lse_k(drow, V, T, kd);
     for (int v = 0; v < V; ++v) {
-      const double a = (double)trow[v] / T - lt, b = (double)drow[v] / T - ld;
+      if (kt && !kt[v]) continue; /* p = 0: weight 0 */
+      const double a = (double)trow[v] / T - lt;
+      const double b = (kd && !kd[v]) ? -INFINITY : (double)drow[v] / T - ld;
       if (!(a > b)) continue; /* weight 0 */
-      const double sc = a + log1p(-exp(b - a)) +
+      const double sc = (b == -INFINITY ? a : a + log1p(-exp(b - a))) +
                         gumbel(seed, (uint32_t)v, (uint32_t)(P + k + 1), (uint32_t)seq, OR_RNG_RESID, (uint32_t)cycle);
       if (x < 0 || sc > best) {
         second = best;
@@ -666,11 +738,13 @@ int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const 
     }
   }
   if (x < 0) {
-    /* all drafts accepted (or p == q at the rejected row): a draw from p */
+    /* all drafts accepted (or p <= q everywhere at the rejected row): a draw from p */
     const int row = k < B - 1 ? k : B - 1;
     const int purpose = k < B - 1 ? OR_RNG_RESID : OR_RNG_BONUS;
     const float* trow = tl + (size_t)row * V;
+    const unsigned char* kt = keep_t ? keep_t + (size_t)row * V : NULL;
     for (int v = 0; v < V; ++v) {
+      if (kt && !kt[v]) continue;
       const double sc = (double)trow[v] / T +
                         gumbel(seed, (uint32_t)v, (uint32_t)(P + row + 1), (uint32_t)seq, (uint32_t)purpose, (uint32_t)cycle);
       if (x < 0 || sc > best) {
@@ -686,6 +760,11 @@ int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const 
   mg = fmin(mg, best - second);
   if (margin) *margin = mg;
   return k;
+}
+
+int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const int* drafts, double T,
+                          uint64_t seed, int seq, int P, int cycle, int* out_tokens, double* margin) {
+  return or_spec_sample_accept_f(B, V, tl, dl, NULL, NULL, drafts, T, seed, seq, P, cycle, out_tokens, margin);
 }
 
 int or_num_threads(void) {

@@ -104,6 +104,16 @@ def lib():
             L.or_sample_row.restype = C.c_int
             L.or_sample_row.argtypes = [C.POINTER(C.c_float), C.c_int, C.c_double, C.c_uint64, C.c_int, C.c_int,
                                         C.c_int, C.c_int, dp, dp]
+            u8p = C.POINTER(C.c_ubyte)
+            L.or_filter_row.restype = C.c_int
+            L.or_filter_row.argtypes = [C.POINTER(C.c_float), C.c_int, C.c_double, C.c_int, C.c_double, u8p, dp]
+            L.or_sample_row_f.restype = C.c_int
+            L.or_sample_row_f.argtypes = [C.POINTER(C.c_float), C.c_int, C.c_double, u8p, C.c_uint64, C.c_int,
+                                          C.c_int, C.c_int, C.c_int, dp, dp]
+            L.or_spec_sample_accept_f.restype = C.c_int
+            L.or_spec_sample_accept_f.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float), u8p,
+                                                  u8p, C.POINTER(C.c_int), C.c_double, C.c_uint64, C.c_int, C.c_int,
+                                                  C.c_int, C.POINTER(C.c_int), dp]
             L.or_spec_sample_accept.restype = C.c_int
             L.or_spec_sample_accept.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float),
                                                 C.POINTER(C.c_int), C.c_double, C.c_uint64, C.c_int, C.c_int,
@@ -554,27 +564,50 @@ def uniform(seed: int, v: int, pos: int, seq: int, purpose: int, cycle: int) -> 
     return lib().or_uniform(seed, v, pos, seq, purpose, cycle)
 
 
-def sample_row(logits: np.ndarray, T: float, seed: int, pos: int, seq: int, purpose: int, cycle: int):
-    """A draw from softmax(logits / T) by Gumbel-max: (token, log-sum-exp, margin)."""
+def _u8(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.uint8).ctypes.data_as(C.POINTER(C.c_ubyte))
+
+
+def filter_row(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0):
+    """Top-k / top-p filter of one logit row (the reading stated in
+    dflash_oracle.c, or_filter_row): (keep mask [V] uint8, kept count,
+    top-p boundary margin)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    keep = np.zeros(lg.shape[0], dtype=np.uint8)
+    mg = C.c_double()
+    n = lib().or_filter_row(lg.ctypes.data_as(C.POINTER(C.c_float)), lg.shape[0], float(T), int(top_k), float(top_p),
+                            keep.ctypes.data_as(C.POINTER(C.c_ubyte)), C.byref(mg))
+    return keep, n, mg.value
+
+
+def sample_row(logits: np.ndarray, T: float, seed: int, pos: int, seq: int, purpose: int, cycle: int, keep=None):
+    """A draw from softmax(logits / T) (over the kept entries) by Gumbel-max:
+    (token, log-sum-exp over the kept entries, margin)."""
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     lse, mg = C.c_double(), C.c_double()
-    tok = lib().or_sample_row(lg.ctypes.data_as(C.POINTER(C.c_float)), lg.shape[0], float(T), seed, pos, seq,
-                              purpose, cycle, C.byref(lse), C.byref(mg))
+    kp = None if keep is None else np.ascontiguousarray(keep, dtype=np.uint8)
+    tok = lib().or_sample_row_f(lg.ctypes.data_as(C.POINTER(C.c_float)), lg.shape[0], float(T), _u8(kp), seed, pos,
+                                seq, purpose, cycle, C.byref(lse), C.byref(mg))
     return tok, lse.value, mg.value
 
 
-def spec_sample_accept(tl: np.ndarray, dl: np.ndarray, drafts, T: float, seed: int, seq: int, P: int, cycle: int):
+def spec_sample_accept(tl: np.ndarray, dl: np.ndarray, drafts, T: float, seed: int, seq: int, P: int, cycle: int,
+                       keep_t=None, keep_d=None):
     """Speculative sampling over one sequence's block: target logits [B][V],
-    draft logits [B-1][V], drafts [B-1] -> (accept length k, emitted tokens
-    [k+1], smallest decision margin)."""
+    draft logits [B-1][V], drafts [B-1], optional kept-entry masks of the
+    target [B][V] and draft [B-1][V] rows (top-k / top-p) -> (accept length
+    k, emitted tokens [k+1], smallest decision margin)."""
     tl = np.ascontiguousarray(tl, dtype=np.float32)
     dl = np.ascontiguousarray(dl, dtype=np.float32)
     B, V = tl.shape
     dr = np.ascontiguousarray(drafts, dtype=np.int32)
     out = np.zeros(B, dtype=np.int32)
     mg = C.c_double()
-    k = lib().or_spec_sample_accept(B, V, tl.ctypes.data_as(C.POINTER(C.c_float)),
-                                    dl.ctypes.data_as(C.POINTER(C.c_float)), dr.ctypes.data_as(C.POINTER(C.c_int)),
-                                    float(T), seed, seq, P, cycle, out.ctypes.data_as(C.POINTER(C.c_int)), C.byref(mg))
+    kt = None if keep_t is None else np.ascontiguousarray(keep_t, dtype=np.uint8)
+    kd = None if keep_d is None else np.ascontiguousarray(keep_d, dtype=np.uint8)
+    k = lib().or_spec_sample_accept_f(B, V, tl.ctypes.data_as(C.POINTER(C.c_float)),
+                                      dl.ctypes.data_as(C.POINTER(C.c_float)), _u8(kt), _u8(kd),
+                                      dr.ctypes.data_as(C.POINTER(C.c_int)), float(T), seed, seq, P, cycle,
+                                      out.ctypes.data_as(C.POINTER(C.c_int)), C.byref(mg))
     return k, out[:k + 1].copy(), mg.value
 
