@@ -451,6 +451,30 @@ def run_ours(args):
                     "ms_per_step": ms_s, "value": world * S * 1000.0 / ms_s, "unit": UNIT, "steps": n_s,
                     "overhead_vs_greedy": ms_s / ms_per_step - 1.0}
         del sgraph
+
+        # the same with top-k 50 / top-p 0.9 filtering of the draft and target rows
+        def step_filtered():
+            eng.base_pos.copy_(base0)
+            eng.anchor.copy_(anchor0)
+            eng.cycle_sampled(1.0, 0x5EED, 0, top_k=50, top_p=0.9)
+
+        step_filtered()
+        torch.cuda.synchronize()
+        assert eng.status() == D.DFLASH_OK
+        fgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fgraph):
+            step_filtered()
+        for _ in range(args.warmup):
+            fgraph.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_s):
+            fgraph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_f = reduce_max(e0.elapsed_time(e1), world, "cuda") / n_s
+        sampling["top_k50_top_p0.9_ms_per_step"] = ms_f
+        del fgraph
         eng.base_pos.copy_(base0)
         eng.anchor.copy_(anchor0)
 

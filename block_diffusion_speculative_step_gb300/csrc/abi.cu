@@ -988,7 +988,7 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
 
 // ------------------------------------------------------------- sampling
 
-static size_t sample_ws(int S, int B, size_t* lse_off, size_t* k_off, size_t* part_off) {
+static size_t sample_ws(int S, int B, size_t* lse_off, size_t* k_off, size_t* part_off, size_t* filt_off = nullptr) {
   size_t off = kReservedBytes;
   *lse_off = off;
   off += ((size_t)S * B * sizeof(float) + 255) & ~size_t(255);
@@ -996,11 +996,14 @@ static size_t sample_ws(int S, int B, size_t* lse_off, size_t* k_off, size_t* pa
   off += ((size_t)S * sizeof(int32_t) + 255) & ~size_t(255);
   *part_off = off;
   off += sample_part_bytes(S * B);
+  if (filt_off) *filt_off = off;  // target rows' then draft rows' kept sets
+  off += ((size_t)S * (2 * B - 1) * sizeof(RowFilter) + 255) & ~size_t(255);
   return off;
 }
 
-static int check_sample_shape(const dflash_dims& d, int S, int B, float T, const char* who) {
-  DF_CHECK(d.vocab > 0, "%s: vocab must be > 0", who);
+static int check_sample_shape(const dflash_dims& d, int S, int B, float T, int top_k, float top_p, const char* who) {
+  DF_CHECK(d.vocab > 0 && d.vocab < (1 << 24), "%s: vocab must be in [1, 2^24)", who);
+  DF_CHECK(top_k >= 0 && top_p >= 0.f && top_p <= 1.f, "%s: top_k >= 0 and 0 <= top_p <= 1 required", who);
   DF_CHECK(S > 0 && B >= 2 && (long)S * B <= 1024, "%s: n_seqs > 0, block >= 2, n_seqs*block <= 1024", who);
   DF_CHECK(T > 0.f && T == T, "%s: temperature must be > 0", who);
   return DFLASH_OK;
@@ -1009,11 +1012,11 @@ static int check_sample_shape(const dflash_dims& d, int S, int B, float T, const
 int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
   const char* who = "dflash_sample_drafts";
   DF_CHECK(a != nullptr, "%s: NULL args", who);
-  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, who);
+  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, a->top_k, a->top_p, who);
   if (rc) return rc;
   DF_CHECK(a->base_pos && a->draft_logits && a->drafts && a->draft_lse, "%s: NULL pointer", who);
-  size_t lo, ko, po;
-  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po), who);
+  size_t lo, ko, po, fo;
+  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po, &fo), who);
   if (rc) return rc;
   Ctx c = header(ws);
   SampleDesc d;
@@ -1028,6 +1031,9 @@ int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws
   d.draft_logits = a->draft_logits;
   d.draft_lse_out = a->draft_lse;
   d.drafts_out = a->drafts;
+  d.top_k = a->top_k;
+  d.top_p = a->top_p;
+  d.filt_d_out = reinterpret_cast<RowFilter*>(static_cast<char*>(ws) + fo) + (size_t)a->n_seqs * a->block;
   d.part = static_cast<char*>(ws) + po;
   d.counters = c.counters + kCtrSample;
   d.status = c.status;
@@ -1038,14 +1044,14 @@ int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws
 int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
   const char* who = "dflash_sample_accept";
   DF_CHECK(a != nullptr, "%s: NULL args", who);
-  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, who);
+  int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, a->top_k, a->top_p, who);
   if (rc) return rc;
   DF_CHECK(a->target_logits && a->draft_logits && a->draft_lse && a->drafts && a->base_pos && a->accept_len &&
                a->out_tokens,
            "%s: NULL pointer", who);
   DF_CHECK(!a->commit_base || a->update_base_pos, "%s: commit_base needs update_base_pos", who);
-  size_t lo, ko, po;
-  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po), who);
+  size_t lo, ko, po, fo;
+  rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po, &fo), who);
   if (rc) return rc;
   Ctx c = header(ws);
   SampleDesc d;
@@ -1067,6 +1073,13 @@ int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws
   d.commit_base = a->commit_base;
   d.commit_count = a->commit_count;
   d.update_base = a->update_base_pos;
+  d.top_k = a->top_k;
+  d.top_p = a->top_p;
+  if ((a->top_k > 0 && a->top_k < a->dims.vocab) || (a->top_p > 0.f && a->top_p < 1.f)) {
+    RowFilter* f = reinterpret_cast<RowFilter*>(static_cast<char*>(ws) + fo);
+    d.filt_t = f;
+    d.filt_d = f + (size_t)a->n_seqs * a->block;
+  }
   d.seq_k = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + ko);
   d.part = static_cast<char*>(ws) + po;
   d.counters = c.counters + kCtrSample;

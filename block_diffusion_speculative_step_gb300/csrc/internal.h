@@ -148,9 +148,21 @@ struct PathDesc {
 };
 
 // Sampling-mode verification (k_sample.cu).
+// Kept set of one logit row under top-k / top-p: the entries up to (key,
+// idx) in the order (logit descending, index ascending); see k_sample.cu.
+struct RowFilter {
+  uint32_t key;
+  int idx;
+};
+
 struct SampleDesc {
   int n_seqs, block, V, cycle;
   float T;
+  int top_k;                  // 0 = off
+  float top_p;                // 1 = off
+  const RowFilter* filt_t;    // [S][block] target rows' kept sets (filtering), else null
+  const RowFilter* filt_d;    // [S][block-1] draft rows' kept sets (acceptance, filtering), else null
+  RowFilter* filt_d_out;      // [S][block-1] (draft draws, filtering)
   uint64_t seed;
   int32_t* base_pos;          // [S] position of block row 0 (advanced when update_base)
   const float* draft_logits;  // [S][block-1][V]

@@ -137,6 +137,173 @@ __device__ __forceinline__ bool slice_last(uint32_t* ctr, int* s_last) {
   return *s_last != 0;
 }
 
+// ---------------------------------------------------- top-k / top-p filter
+//
+// The kept set of a row: entries ordered by logit (descending, lower index
+// first on equal logits), the first top_k of them, then the shortest prefix
+// of those whose renormalised softmax(l / T) mass reaches top_p.  It is a
+// prefix of that order, held as its last entry (key, idx): v is kept iff
+// key(l_v) > key, or key(l_v) == key and v <= idx.  One CTA per row finds it
+// by radix selection on the order-preserving key of the logits (four 8-bit
+// rounds over the entries that match the key bits chosen so far) and, among
+// equal logits, on the index.  Top-p counts masses as integers, w_v =
+// floor(exp((l_v - max) / T) 2^32), summed by 64-bit integer atomics, so the
+// selection is the same whatever the order of the additions.
+constexpr int kFiltThreads = 1024;
+
+__device__ __forceinline__ uint32_t okey(float x) {
+  const uint32_t b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ bool filt_kept(const RowFilter* f, float l, int v) {
+  if (l != l) return false;
+  if (f == nullptr) return true;
+  const uint32_t k = okey(l);
+  return k > f->key || (k == f->key && v <= f->idx);
+}
+
+__device__ __forceinline__ unsigned long long filt_mass(float l, float mx, float invT) {
+  return __float2ull_rd(expf((l - mx) * invT) * 4294967296.0f);
+}
+
+// Among the entries v passing `in(v)`, select by `weight(v)` (1 for counts,
+// the integer mass for top-p) the entry at which the running total in the
+// order (key descending, index ascending) first reaches `need` (>= 1): its
+// key and index.  Radix rounds on the key from the top byte, then on the
+// index (ascending) among the entries with that key.
+template <typename In, typename W>
+__device__ void filt_select(const float* l, int V, In in, W weight, unsigned long long need, uint32_t* key_out,
+                            int* idx_out) {
+  __shared__ unsigned long long hist[256];
+  __shared__ unsigned long long s_need;
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_bin;
+  if (threadIdx.x == 0) {
+    s_need = need;
+    s_prefix = 0u;
+  }
+  __syncthreads();
+  uint32_t mask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0ull;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = l[v];
+      if (!in(x, v)) continue;
+      const uint32_t k = okey(x);
+      if ((k & mask) != prefix) continue;
+      const unsigned long long w = weight(x);
+      if (w) atomicAdd(&hist[(k >> shift) & 255u], w);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long acc = 0ull, nd = s_need;
+      int b = 255;
+      for (; b > 0; --b) {
+        if (acc + hist[b] >= nd) break;
+        acc += hist[b];
+      }
+      s_need = nd - acc;
+      s_prefix = prefix | ((uint32_t)b << shift);
+    }
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  const uint32_t key = s_prefix;
+  // among the entries with this key (equal logits, equal weights), the
+  // lowest indices first: the one where the total reaches s_need
+  __shared__ int s_ip;
+  if (threadIdx.x == 0) s_ip = 0;
+  __syncthreads();
+  int imask = 0;
+  for (int shift = 16; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0ull;
+    __syncthreads();
+    const int ip = s_ip;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = l[v];
+      if (!in(x, v) || okey(x) != key || (v & imask) != ip) continue;
+      const unsigned long long w = weight(x);
+      if (w) atomicAdd(&hist[(v >> shift) & 255], w);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long acc = 0ull, nd = s_need;
+      int b = 0;
+      for (; b < 255; ++b) {
+        if (acc + hist[b] >= nd) break;
+        acc += hist[b];
+      }
+      s_need = nd - acc;
+      s_ip = ip | (b << shift);
+    }
+    imask |= 255 << shift;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    *key_out = key;
+    *idx_out = s_ip;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* logits, int V, float invT, int top_k,
+                                                                  float top_p, RowFilter* out, uint32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float red[kFiltThreads / 32];
+  __shared__ unsigned long long redu[kFiltThreads / 32];
+  __shared__ RowFilter s_f;
+  const float* l = logits + (size_t)blockIdx.x * V;
+  float mx = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = l[v];
+    if (x == x) mx = fmaxf(mx, x);
+  }
+  mx = warp_max(mx);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  if (threadIdx.x == 0) s_f = RowFilter{0u, INT_MAX};
+  __syncthreads();
+  if (top_k > 0 && top_k < V) {
+    uint32_t k;
+    int i;
+    filt_select(l, V, [](float x, int) { return x == x; }, [](float) { return 1ull; }, (unsigned long long)top_k, &k,
+                &i);
+    if (threadIdx.x == 0) s_f = RowFilter{k, i};
+    __syncthreads();
+  }
+  if (top_p > 0.f && top_p < 1.f) {
+    const RowFilter fk = s_f;
+    auto in = [fk](float x, int v) { return filt_kept(&fk, x, v); };
+    auto mass = [mx, invT](float x) { return filt_mass(x, mx, invT); };
+    unsigned long long z = 0ull;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = l[v];
+      if (in(x, v)) z += mass(x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if ((threadIdx.x & 31) == 0) redu[threadIdx.x >> 5] = z;
+    __syncthreads();
+    z = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) z += redu[w];
+    unsigned long long need = (unsigned long long)ceil((double)top_p * (double)z);
+    if (need < 1ull) need = 1ull;
+    uint32_t k;
+    int i;
+    filt_select(l, V, in, mass, need, &k, &i);
+    if (threadIdx.x == 0) s_f = RowFilter{k, i};
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[blockIdx.x] = s_f;
+  (void)status;
+}
+
 // One vocabulary row per blockIdx.x (row = s * rows_per_seq + i), slice
 // blockIdx.y.  lse_out[row] = log sum exp(l / T); with draw != 0 also
 // tok_out[row] = a Gumbel-max draw from softmax(l / T) at position
@@ -144,7 +311,7 @@ __device__ __forceinline__ bool slice_last(uint32_t* ctr, int* s_last) {
 __global__ void __launch_bounds__(kSampleThreads) row_sample_kernel(const __grid_constant__ SampleDesc d,
                                                                     const float* logits, int rows_per_seq,
                                                                     int first_pos, int draw, float* lse_out,
-                                                                    int32_t* tok_out) {
+                                                                    int32_t* tok_out, const RowFilter* filt) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ RowAcc red[kSampleThreads / 32];
@@ -157,6 +324,7 @@ __global__ void __launch_bounds__(kSampleThreads) row_sample_kernel(const __grid
   const int per = (V + kSplit - 1) / kSplit;
   const int v0 = sl * per, v1 = min(V, v0 + per);
   const uint32_t pos = (uint32_t)(d.base_pos[s] + first_pos + i);
+  const RowFilter* f = filt ? filt + row : nullptr;
   RowAcc a = acc_empty();
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     const float x = l[v] * invT;
@@ -164,6 +332,7 @@ __global__ void __launch_bounds__(kSampleThreads) row_sample_kernel(const __grid
       raise_status(d.status, ST_NUMERIC);
       continue;
     }
+    if (!filt_kept(f, l[v], v)) continue;
     acc_lse(a, x);
     if (draw) acc_draw(a, x + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_DRAFT, (uint32_t)d.cycle), v);
   }
@@ -203,7 +372,10 @@ __global__ void spec_accept_kernel(const __grid_constant__ SampleDesc d, const f
       raise_status(d.status, ST_RANGE);
       break;
     }
-    const float lp = d.target_logits[((size_t)s * B + j - 1) * V + dj] * invT - lse_t[(size_t)s * B + j - 1];
+    const float lt_dj = d.target_logits[((size_t)s * B + j - 1) * V + dj];
+    const float lp = filt_kept(d.filt_t ? d.filt_t + (size_t)s * B + j - 1 : nullptr, lt_dj, dj)
+                         ? lt_dj * invT - lse_t[(size_t)s * B + j - 1]
+                         : -INFINITY;
     const float lq = d.draft_logits[((size_t)s * (B - 1) + j - 1) * V + dj] * invT - d.draft_lse[(size_t)s * (B - 1) + j - 1];
     const float lu = logf(rng_uniform(d.seed, 0u, (uint32_t)(P + j), (uint32_t)s, RNG_ACCEPT, (uint32_t)d.cycle));
     if (!(lu < lp - lq)) break;
@@ -236,15 +408,18 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
   const uint32_t pos = (uint32_t)(P + trow + 1);
   const int per = (V + kSplit - 1) / kSplit;
   const int v0 = sl * per, v1 = min(V, v0 + per);
+  const RowFilter* ft = d.filt_t ? d.filt_t + (size_t)s * B + trow : nullptr;
+  const RowFilter* fd = (resid && d.filt_d) ? d.filt_d + (size_t)s * (B - 1) + k : nullptr;
   RowAcc ar = acc_empty();  // the residual draw
   RowAcc ap = acc_empty();  // the draw from p (used when no residual weight is positive)
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    if (!filt_kept(ft, tl[v], v)) continue;  // p = 0 here
     const float a = tl[v] * invT - lt;
     if (resid) {
-      const float b = dl[v] * invT - ld;
+      const float b = filt_kept(fd, dl[v], v) ? dl[v] * invT - ld : -INFINITY;
       if (a > b)
-        acc_draw(ar, a + log1pf(-expf(b - a)) + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID,
-                                                             (uint32_t)d.cycle), v);
+        acc_draw(ar, (b == -INFINITY ? a : a + log1pf(-expf(b - a))) +
+                         rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID, (uint32_t)d.cycle), v);
       acc_draw(ap, tl[v] * invT + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID, (uint32_t)d.cycle), v);
     } else {
       acc_draw(ap, tl[v] * invT + rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_BONUS, (uint32_t)d.cycle), v);
@@ -286,17 +461,37 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
   }
 }
 
+static bool filtering(const SampleDesc& d) {
+  return (d.top_k > 0 && d.top_k < d.V) || (d.top_p > 0.f && d.top_p < 1.f);
+}
+
 cudaError_t launch_sample_drafts(const SampleDesc& d, cudaStream_t st) {
   const int rows = d.n_seqs * (d.block - 1);
   if (rows == 0) return cudaSuccess;
+  const RowFilter* fd = nullptr;
+  if (filtering(d)) {
+    cudaError_t e = launch_pdl(row_filter_kernel, dim3(rows), dim3(kFiltThreads), 0, st, d.draft_logits, d.V,
+                               1.f / d.T, d.top_k, d.top_p, d.filt_d_out, d.status);
+    if (e != cudaSuccess) return e;
+    fd = d.filt_d_out;
+  }
   return launch_pdl(row_sample_kernel, dim3(rows, kSplit), dim3(kSampleThreads), 0, st, d, d.draft_logits,
-                    d.block - 1, 1, 1, d.draft_lse_out, d.drafts_out);
+                    d.block - 1, 1, 1, d.draft_lse_out, d.drafts_out, fd);
 }
 
 cudaError_t launch_sample_accept(const SampleDesc& d, float* lse_t, cudaStream_t st) {
   if (d.n_seqs == 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(row_sample_kernel, dim3(d.n_seqs * d.block, kSplit), dim3(kSampleThreads), 0, st, d,
-                             d.target_logits, d.block, 0, 0, lse_t, (int32_t*)nullptr);
+  cudaError_t e;
+  if (filtering(d)) {  // the target rows' and (again, identically) the draft rows' kept sets
+    e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * d.block), dim3(kFiltThreads), 0, st, d.target_logits, d.V,
+                   1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_t), d.status);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * (d.block - 1)), dim3(kFiltThreads), 0, st, d.draft_logits, d.V,
+                   1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_d), d.status);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_pdl(row_sample_kernel, dim3(d.n_seqs * d.block, kSplit), dim3(kSampleThreads), 0, st, d,
+                 d.target_logits, d.block, 0, 0, lse_t, (int32_t*)nullptr, d.filt_t);
   if (e != cudaSuccess) return e;
   e = launch_pdl(spec_accept_kernel, dim3(d.n_seqs), dim3(32), 0, st, d, (const float*)lse_t);
   if (e != cudaSuccess) return e;

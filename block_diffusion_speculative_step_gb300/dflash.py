@@ -107,7 +107,7 @@ class dflash_path_args(C.Structure):
 class dflash_sample_drafts_args(C.Structure):
     _fields_ = [("dims", dflash_dims), ("n_seqs", i32), ("block", i32), ("temperature", C.c_float),
                 ("cycle", i32), ("seed", C.c_uint64), ("base_pos", vp), ("draft_logits", vp), ("drafts", vp),
-                ("draft_lse", vp)]
+                ("draft_lse", vp), ("top_k", i32), ("top_p", C.c_float)]
 
 
 class dflash_sample_accept_args(C.Structure):
@@ -115,7 +115,7 @@ class dflash_sample_accept_args(C.Structure):
                 ("cycle", i32), ("seed", C.c_uint64), ("target_logits", vp), ("draft_logits", vp),
                 ("draft_lse", vp), ("drafts", vp), ("base_pos", vp), ("update_base_pos", i32),
                 ("accept_len", vp), ("out_tokens", vp), ("next_anchor", vp), ("commit_base", vp),
-                ("commit_count", vp)]
+                ("commit_count", vp), ("top_k", i32), ("top_p", C.c_float)]
 
 
 class dflash_trace_stat(C.Structure):

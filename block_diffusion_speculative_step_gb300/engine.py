@@ -340,11 +340,12 @@ class Engine:
         self.verify(self.B, self.drafts)
         self.fuse(self.B, self.commit_base, self.commit_count)
 
-    def cycle_sampled(self, T: float, seed: int, cycle: int):
-        """One cycle in sampling mode (speculative sampling at temperature T):
-        the draft's logits give drafts drawn from its distribution, the
-        target's logits the acceptance tests and the final draw.  `cycle`
-        numbers the random draws; give every cycle its own."""
+    def cycle_sampled(self, T: float, seed: int, cycle: int, top_k: int = 0, top_p: float = 1.0):
+        """One cycle in sampling mode (speculative sampling at temperature T,
+        optionally over the top_k / top_p filtered distributions): the
+        draft's logits give drafts drawn from its distribution, the target's
+        logits the acceptance tests and the final draw.  `cycle` numbers the
+        random draws; give every cycle its own."""
         S, B, V = self.S, self.B, self.w.vocab
         if getattr(self, "dlogits", None) is None:
             self.dlogits = torch.zeros(S * (B - 1), V, dtype=torch.float32, device=self.dev)
@@ -356,6 +357,7 @@ class Engine:
         a.n_seqs, a.block, a.temperature, a.cycle, a.seed = S, B, T, cycle, seed
         a.base_pos, a.draft_logits = _ptr(self.base_pos), _ptr(self.dlogits)
         a.drafts, a.draft_lse = _ptr(self.drafts), _ptr(self.dlse)
+        a.top_k, a.top_p = top_k, top_p
         D.dflash_sample_drafts(a, self.ws_ptr, self.ws_bytes)
         self.target_forward(B, self.anchor, self.drafts)
         D.dflash_verify_accept(self.verify_args(B, self.h, self.drafts, self.tlogits, update=False), self.ws_ptr,
@@ -367,6 +369,7 @@ class Engine:
         b.drafts, b.base_pos, b.update_base_pos = _ptr(self.drafts), _ptr(self.base_pos), 1
         b.accept_len, b.out_tokens, b.next_anchor = _ptr(self.accept_len), _ptr(self.out_tokens), _ptr(self.anchor)
         b.commit_base, b.commit_count = _ptr(self.commit_base), _ptr(self.commit_count)
+        b.top_k, b.top_p = top_k, top_p
         D.dflash_sample_accept(b, self.ws_ptr, self.ws_bytes)
         self.fuse(B, self.commit_base, self.commit_count)
 

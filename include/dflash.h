@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 4
+#define DFLASH_ABI_VERSION 5
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -367,6 +367,15 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes,
  * cycle its own `cycle` value.  Reductions run in a fixed order, so a call
  * is deterministic.  Token ids out of range raise DFLASH_ERR_INVALID_ARG in
  * the status word.  n_seqs * block <= 1024.
+ *
+ * Top-k / top-p (both calls must be given the same values): every row's
+ * entries are ordered by logit (descending, lower index first on equal
+ * logits); top_k > 0 keeps the first top_k, then top_p < 1 keeps the
+ * shortest prefix of those whose softmax(logits / T) mass, renormalised over
+ * them, reaches top_p (masses counted as floor(exp((l - max) / T) 2^32)).
+ * p_j and q_j are then the renormalised softmax over each row's kept
+ * entries (0 elsewhere): the output follows the filtered target
+ * distribution.  top_k = 0 and top_p = 0 or 1 turn filtering off.
  */
 typedef struct {
   dflash_dims dims;             /* vocab is used */
@@ -377,7 +386,9 @@ typedef struct {
   const int32_t* base_pos;      /* [n_seqs] position P of block row 0 */
   const float* draft_logits;    /* [n_seqs][block-1][V] */
   int32_t* drafts;              /* out [n_seqs][block-1] */
-  float* draft_lse;             /* out [n_seqs][block-1]: log sum exp(logits / T) */
+  float* draft_lse;             /* out [n_seqs][block-1]: log sum exp(logits / T) over the kept entries */
+  int32_t top_k;                /* 0 = off */
+  float top_p;                  /* 0 or 1 = off */
 } dflash_sample_drafts_args;
 int dflash_sample_drafts(const dflash_sample_drafts_args* a, void* ws, size_t ws_bytes,
                          dflash_stream_t stream);
@@ -399,6 +410,8 @@ typedef struct {
   int32_t* next_anchor;         /* optional out [n_seqs]: the final draw */
   int32_t* commit_base;         /* optional out [n_seqs]: P (with update_base_pos) */
   int32_t* commit_count;        /* optional out [n_seqs]: accept_len + 1 */
+  int32_t top_k;                /* as for the drafts */
+  float top_p;                  /* as for the drafts */
 } dflash_sample_accept_args;
 int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws_bytes,
                          dflash_stream_t stream);

@@ -29,7 +29,7 @@ def _dims(V):
     return D.dflash_dims(64, 4, 2, 16, 96, V, 1e4, 1e-6, D.DFLASH_BF16)
 
 
-def _run(tl, dl, P, T, cycle, ws):
+def _run(tl, dl, P, T, cycle, ws, top_k=0, top_p=1.0):
     """dflash_sample_drafts then dflash_sample_accept on [S][B][V] / [S][B-1][V]."""
     S, B, V = tl.shape
     tl_d, dl_d = tl.cuda().contiguous(), dl.cuda().contiguous()
@@ -39,6 +39,7 @@ def _run(tl, dl, P, T, cycle, ws):
     a = D.dflash_sample_drafts_args()
     a.dims, a.n_seqs, a.block, a.temperature, a.cycle, a.seed = _dims(V), S, B, T, cycle, SEED
     a.base_pos, a.draft_logits, a.drafts, a.draft_lse = base.data_ptr(), dl_d.data_ptr(), drafts.data_ptr(), dlse.data_ptr()
+    a.top_k, a.top_p = top_k, top_p
     assert D.dflash_workspace_bytes(D.DFLASH_OP_SAMPLE_DRAFTS, a) <= ws.numel()
     D.dflash_sample_drafts(a, ws.data_ptr(), ws.numel())
     k = torch.full((S,), -1, dtype=torch.int32, device="cuda")
@@ -48,6 +49,7 @@ def _run(tl, dl, P, T, cycle, ws):
     b.target_logits, b.draft_logits, b.draft_lse = tl_d.data_ptr(), dl_d.data_ptr(), dlse.data_ptr()
     b.drafts, b.base_pos, b.update_base_pos = drafts.data_ptr(), base.data_ptr(), 0
     b.accept_len, b.out_tokens = k.data_ptr(), out.data_ptr()
+    b.top_k, b.top_p = top_k, top_p
     D.dflash_sample_accept(b, ws.data_ptr(), ws.numel())
     torch.cuda.synchronize()
     st = D.dflash_read_status(ws.data_ptr())
@@ -133,3 +135,81 @@ def test_sampled_cycle_through_the_engine():
             assert int(eng.anchor[s]) == int(toks[-1])
         total += k.long() + 1
     assert torch.equal(eng.base_pos.cpu().long(), base0.cpu().long() + total)
+
+
+@pytest.mark.parametrize("V,T,top_k,top_p", [(1000, 0.8, 50, 1.0), (1000, 0.8, 0, 0.9), (1000, 1.2, 20, 0.7),
+                                             (151936, 1.0, 40, 1.0), (151936, 1.0, 0, 0.6)])
+def test_filtered_sampling_matches_oracle(V, T, top_k, top_p):
+    """Top-k / top-p: with the oracle's kept sets of the same rows, the drafts,
+    the draft rows' log-normalisers over their kept entries, the accept
+    lengths and the emitted tokens equal the oracle's (sequences meeting a
+    near-tie -- a draw, a test or the top-p boundary -- are reported and
+    skipped).  Flat logits (spread 0.5) give every kept entry a share of the
+    mass, so a wrong kept set moves the normalisers far beyond the tolerance.
+    At the full vocabulary the logits are peaked (spread 3) so that the kept
+    sets stay small and their boundary entries carry measurable mass."""
+    S, B = 3, 6
+    g = torch.Generator().manual_seed(V + top_k)
+    spread = 0.5 if V <= 1000 else 3.0
+    tl = torch.randn(S, B, V, generator=g) * spread
+    dl = tl[:, 1:] * 0.6 + torch.randn(S, B - 1, V, generator=g) * 0.8 * spread
+    P = [17, 400, 4095]
+    ws = _ws()
+    compared = 0
+    for cycle in range(3):
+        dr, dlse, k, out = _run(tl, dl, P, T, cycle, ws, top_k, top_p)
+        for s in range(S):
+            kt, kd, near = [], [], False
+            for j in range(B):
+                keep, n, mg = O.filter_row(tl[s, j].numpy(), T, top_k, top_p)
+                kt.append(keep)
+                near |= mg < 1e-6  # above the float-vs-double error of the cumulative mass
+            for j in range(B - 1):
+                keep, n, mg = O.filter_row(dl[s, j].numpy(), T, top_k, top_p)
+                kd.append(keep)
+                near |= mg < 1e-6
+            if near:
+                continue
+            for j in range(B - 1):
+                tok, lse, mg = O.sample_row(dl[s, j].numpy(), T, SEED, P[s] + j + 1, s, O.RNG_DRAFT, cycle, keep=kd[j])
+                assert abs(dlse[s, j] - lse) <= 1e-4 * max(1.0, abs(lse)), (s, j, dlse[s, j], lse)
+                assert kd[j][dr[s, j]] == 1
+                if mg < 1e-4:
+                    near = True
+                    break
+                assert dr[s, j] == tok, f"cycle {cycle} seq {s} row {j}: gpu {dr[s, j]} oracle {tok}"
+            if near:
+                continue
+            ok, oout, omg = O.spec_sample_accept(tl[s].numpy(), dl[s].numpy(), dr[s], T, SEED, s, P[s], cycle,
+                                                 keep_t=np.stack(kt), keep_d=np.stack(kd))
+            if omg < 1e-4:
+                continue
+            assert k[s] == ok and list(out[s, :ok + 1]) == list(oout)
+            compared += 1
+    assert compared >= 5
+
+
+def test_filtered_emitted_token_follows_the_filtered_target():
+    """Top-k 4 and top-p 0.85 on both sides, 300 sequences x 20 cycles: the
+    first emitted token follows the filtered, renormalised softmax of target
+    row 0 (entries outside its kept set never appear)."""
+    S, B, V, T, top_k, top_p = 300, 3, 6, 0.9, 4, 0.85
+    g = torch.Generator().manual_seed(6)
+    t1 = torch.randn(B, V, generator=g)
+    d1 = t1[1:] * 0.3 + torch.randn(B - 1, V, generator=g)
+    tl, dl = t1.expand(S, B, V).contiguous(), d1.expand(S, B - 1, V).contiguous()
+    ws = _ws()
+    first = np.zeros(V)
+    n = 0
+    for cycle in range(20):
+        _, _, k, out = _run(tl, dl, [9] * S, T, cycle, ws, top_k, top_p)
+        for s in range(S):
+            first[out[s, 0]] += 1
+            n += 1
+    keep, _, _ = O.filter_row(t1[0].numpy(), T, top_k, top_p)
+    z = np.where(keep > 0, t1[0].double().numpy() / T, -np.inf)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    assert np.all(first[keep == 0] == 0)
+    se = np.sqrt(p * (1 - p) / n) + 1e-12
+    assert np.all(np.abs(first / n - p) < 4.5 * se), (first / n, p)
