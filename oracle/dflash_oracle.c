@@ -555,7 +555,7 @@ void or_path_select(const or_cfg* c, int B, int Vocab, int topk, int R, const fl
  * counter (vocabulary entry, position, sequence << 8 | purpose, cycle);
  * u = ((x0 >> 8) + 1/2) 2^-24 in (0, 1), g = -log(-log u).
  */
-enum { OR_RNG_DRAFT = 1, OR_RNG_ACCEPT = 2, OR_RNG_RESID = 3, OR_RNG_BONUS = 4 };
+enum { OR_RNG_DRAFT = 1, OR_RNG_ACCEPT = 2, OR_RNG_RESID = 3, OR_RNG_BONUS = 4, OR_RNG_PATH = 5 };
 
 void or_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
   uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
@@ -765,6 +765,146 @@ int or_spec_sample_accept_f(int B, int V, const float* tl, const float* dl, cons
 int or_spec_sample_accept(int B, int V, const float* tl, const float* dl, const int* drafts, double T,
                           uint64_t seed, int seq, int P, int cycle, int* out_tokens, double* margin) {
   return or_spec_sample_accept_f(B, V, tl, dl, NULL, NULL, drafts, T, seed, seq, P, cycle, out_tokens, margin);
+}
+
+/* ------------------------------------------------- sampled path walk
+ *
+ * The DFlash 2 path walked by sampling ([G] section 7: the path is walked
+ * "greedily or by sampling" along the pair scores, and rejection sampling
+ * keeps the output distribution exactly the target's).  Read here: at step
+ * j (block row j+1) the proposal over row j's candidates is
+ *   q_j(c) = softmax over the topk candidates c of s(p_{j-1}, c) / T,
+ * s(a, b) = (U e_a) . (V e_b) the low-rank pair score of the greedy walk,
+ * p_0 = anchor; p_j is a Gumbel-max draw from q_j (Philox purpose
+ * OR_RNG_PATH, counter entry = the candidate's rank, position P + j + 1),
+ * lower rank on equal draw scores.  The tokens outside the candidates have
+ * proposal probability 0.  cand [B-1][topk] in; path [B-1], logq
+ * [B-1][topk] (log q_j per candidate) and margin [B-1] (best - second draw
+ * score) out.
+ */
+static double pair_score(const or_cfg* c, int R, const void* E, const void* U, const void* Vm, int a, int b) {
+  const int H = c->H;
+  double sc = 0.0;
+  for (int r = 0; r < R; ++r) {
+    double ua = 0.0, vb = 0.0;
+    for (int k = 0; k < H; ++k) {
+      ua += wget(c, U, (size_t)r * H + k) * wget(c, E, (size_t)a * H + k);
+      vb += wget(c, Vm, (size_t)r * H + k) * wget(c, E, (size_t)b * H + k);
+    }
+    sc += ua * vb;
+  }
+  return sc;
+}
+
+void or_path_walk_sample(const or_cfg* c, int B, int topk, int R, const int* cand, const void* E, const void* U,
+                         const void* Vm, int anchor, double T, uint64_t seed, int seq, int P, int cycle, int* path,
+                         double* logq, double* margin) {
+  double* z = malloc(sizeof(double) * (size_t)topk);
+  int prev = anchor;
+  for (int j = 0; j < B - 1; ++j) {
+    double mx = -INFINITY;
+    for (int q = 0; q < topk; ++q) {
+      z[q] = pair_score(c, R, E, U, Vm, prev, cand[(size_t)j * topk + q]) / T;
+      mx = fmax(mx, z[q]);
+    }
+    double sum = 0.0;
+    for (int q = 0; q < topk; ++q) sum += exp(z[q] - mx);
+    const double lse = mx + log(sum);
+    double best = -INFINITY, second = -INFINITY;
+    int bi = 0;
+    for (int q = 0; q < topk; ++q) {
+      logq[(size_t)j * topk + q] = z[q] - lse;
+      const double sc = z[q] + gumbel(seed, (uint32_t)q, (uint32_t)(P + j + 1), (uint32_t)seq, OR_RNG_PATH,
+                                      (uint32_t)cycle);
+      if (sc > best) {
+        second = best;
+        best = sc;
+        bi = q;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+    path[j] = cand[(size_t)j * topk + bi];
+    margin[j] = best - second;
+    prev = path[j];
+  }
+  free(z);
+}
+
+/* Speculative sampling against a sparse proposal: q_j is supported on the
+ * candidates qc [B-1][K] with log-probabilities lq [B-1][K] (the sampled
+ * walk's); everything else is as or_spec_sample_accept_f, whose target
+ * filtering keep_t (NULL: none) applies. */
+int or_spec_sample_accept_sparse(int B, int V, const float* tl, const unsigned char* keep_t, int K, const int* qc,
+                                 const double* lq, const int* drafts, double T, uint64_t seed, int seq, int P,
+                                 int cycle, int* out_tokens, double* margin) {
+  double mg = INFINITY;
+  int k = 0;
+  for (int j = 1; j <= B - 1; ++j) {
+    const int d = drafts[j - 1];
+    const float* trow = tl + (size_t)(j - 1) * V;
+    const unsigned char* kt = keep_t ? keep_t + (size_t)(j - 1) * V : NULL;
+    const double lp = (kt && !kt[d]) ? -INFINITY : (double)trow[d] / T - row_lse_k(trow, V, T, kt);
+    double lqd = -INFINITY;
+    for (int q = 0; q < K; ++q)
+      if (qc[(size_t)(j - 1) * K + q] == d) {
+        lqd = lq[(size_t)(j - 1) * K + q];
+        break;
+      }
+    const double lu = log(or_uniform(seed, 0u, (uint32_t)(P + j), (uint32_t)seq, OR_RNG_ACCEPT, (uint32_t)cycle));
+    if (lp > -INFINITY && lqd > -INFINITY) mg = fmin(mg, fabs(lu - (lp - lqd)));
+    if (!(lu < lp - lqd)) break;
+    out_tokens[k++] = d;
+  }
+  int x = -1;
+  double best = -INFINITY, second = -INFINITY;
+  if (k < B - 1) {
+    const float* trow = tl + (size_t)k * V;
+    const unsigned char* kt = keep_t ? keep_t + (size_t)k * V : NULL;
+    const double lt = row_lse_k(trow, V, T, kt);
+    for (int v = 0; v < V; ++v) {
+      if (kt && !kt[v]) continue;
+      const double a = (double)trow[v] / T - lt;
+      double b = -INFINITY;
+      for (int q = 0; q < K; ++q)
+        if (qc[(size_t)k * K + q] == v) {
+          b = lq[(size_t)k * K + q];
+          break;
+        }
+      if (!(a > b)) continue;
+      const double sc = (b == -INFINITY ? a : a + log1p(-exp(b - a))) +
+                        gumbel(seed, (uint32_t)v, (uint32_t)(P + k + 1), (uint32_t)seq, OR_RNG_RESID, (uint32_t)cycle);
+      if (x < 0 || sc > best) {
+        second = best;
+        best = sc;
+        x = v;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+  }
+  if (x < 0) {
+    const int row = k < B - 1 ? k : B - 1;
+    const int purpose = k < B - 1 ? OR_RNG_RESID : OR_RNG_BONUS;
+    const float* trow = tl + (size_t)row * V;
+    const unsigned char* kt = keep_t ? keep_t + (size_t)row * V : NULL;
+    for (int v = 0; v < V; ++v) {
+      if (kt && !kt[v]) continue;
+      const double sc = (double)trow[v] / T +
+                        gumbel(seed, (uint32_t)v, (uint32_t)(P + row + 1), (uint32_t)seq, (uint32_t)purpose, (uint32_t)cycle);
+      if (x < 0 || sc > best) {
+        second = best;
+        best = sc;
+        x = v;
+      } else if (sc > second) {
+        second = sc;
+      }
+    }
+  }
+  out_tokens[k] = x;
+  mg = fmin(mg, best - second);
+  if (margin) *margin = mg;
+  return k;
 }
 
 int or_num_threads(void) {

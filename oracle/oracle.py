@@ -114,6 +114,13 @@ def lib():
             L.or_spec_sample_accept_f.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float), u8p,
                                                   u8p, C.POINTER(C.c_int), C.c_double, C.c_uint64, C.c_int, C.c_int,
                                                   C.c_int, C.POINTER(C.c_int), dp]
+            L.or_path_walk_sample.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int), C.c_void_p,
+                                              C.c_void_p, C.c_void_p, C.c_int, C.c_double, C.c_uint64, C.c_int,
+                                              C.c_int, C.c_int, C.POINTER(C.c_int), dp, dp]
+            L.or_spec_sample_accept_sparse.restype = C.c_int
+            L.or_spec_sample_accept_sparse.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), u8p, C.c_int,
+                                                       C.POINTER(C.c_int), dp, C.POINTER(C.c_int), C.c_double,
+                                                       C.c_uint64, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int), dp]
             L.or_spec_sample_accept.restype = C.c_int
             L.or_spec_sample_accept.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float),
                                                 C.POINTER(C.c_int), C.c_double, C.c_uint64, C.c_int, C.c_int,
@@ -548,7 +555,7 @@ def threads() -> int:
 
 # ---------------------------------------------------------------- sampling
 # Random-number purposes (the counter's low byte next to the sequence id).
-RNG_DRAFT, RNG_ACCEPT, RNG_RESID, RNG_BONUS = 1, 2, 3, 4
+RNG_DRAFT, RNG_ACCEPT, RNG_RESID, RNG_BONUS, RNG_PATH = 1, 2, 3, 4, 5
 
 
 def philox4x32_10(ctr, key):
@@ -611,3 +618,38 @@ def spec_sample_accept(tl: np.ndarray, dl: np.ndarray, drafts, T: float, seed: i
                                       out.ctypes.data_as(C.POINTER(C.c_int)), C.byref(mg))
     return k, out[:k + 1].copy(), mg.value
 
+
+
+def path_walk_sample(cfg: Cfg, cand: np.ndarray, E, U, Vm, anchor: int, T: float, seed: int, seq: int, P: int,
+                     cycle: int):
+    """The DFlash 2 path walked by sampling ([G] section 7; the reading in
+    dflash_oracle.c, or_path_walk_sample) over the candidates cand
+    [B-1][topk]: (path [B-1], log q [B-1][topk], draw margins [B-1])."""
+    cd = np.ascontiguousarray(cand, dtype=np.int32)
+    Bm1, K = cd.shape
+    path = np.zeros(Bm1, dtype=np.int32)
+    lq = np.zeros((Bm1, K))
+    mg = np.zeros(Bm1)
+    lib().or_path_walk_sample(C.byref(cfg.c()), Bm1 + 1, K, U.shape[0], cd.ctypes.data_as(C.POINTER(C.c_int)),
+                              _vp(E), _vp(U), _vp(Vm), int(anchor), float(T), seed, seq, P, cycle,
+                              path.ctypes.data_as(C.POINTER(C.c_int)), _dp(lq), _dp(mg))
+    return path, lq, mg
+
+
+def spec_sample_accept_sparse(tl: np.ndarray, qcand: np.ndarray, qlogq: np.ndarray, drafts, T: float, seed: int,
+                              seq: int, P: int, cycle: int, keep_t=None):
+    """Speculative sampling with the sampled walk's sparse proposal (qcand,
+    qlogq [B-1][K]) in place of the draft softmax -> (k, emitted tokens, smallest margin)."""
+    tl = np.ascontiguousarray(tl, dtype=np.float32)
+    B, V = tl.shape
+    qc = np.ascontiguousarray(qcand, dtype=np.int32)
+    lq = np.ascontiguousarray(qlogq, dtype=np.float64)
+    dr = np.ascontiguousarray(drafts, dtype=np.int32)
+    out = np.zeros(B, dtype=np.int32)
+    mg = C.c_double()
+    kt = None if keep_t is None else np.ascontiguousarray(keep_t, dtype=np.uint8)
+    k = lib().or_spec_sample_accept_sparse(B, V, tl.ctypes.data_as(C.POINTER(C.c_float)), _u8(kt), qc.shape[1],
+                                           qc.ctypes.data_as(C.POINTER(C.c_int)), _dp(lq),
+                                           dr.ctypes.data_as(C.POINTER(C.c_int)), float(T), seed, seq, P, cycle,
+                                           out.ctypes.data_as(C.POINTER(C.c_int)), C.byref(mg))
+    return k, out[:k + 1].copy(), mg.value
