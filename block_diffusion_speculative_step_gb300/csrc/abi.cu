@@ -825,6 +825,12 @@ static int draft_round(const dflash_draft_args* a, const DraftScratch& s, const 
     p.path = a->drafts;
     p.proj = s.proj;
     p.status = c.status;
+    p.T = a->path_temperature;
+    p.seed = a->path_seed;
+    p.cycle = a->path_cycle;
+    p.base_pos = a->base_pos;
+    p.logq = a->path_logq;
+    p.cand_out = a->path_cand_out;
     DF_LAUNCH(st, TF_PATH, 0, launch_path_select(p, st));
   }
   return DFLASH_OK;
@@ -845,6 +851,8 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
   DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
   DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
+  DF_CHECK(a->path_temperature >= 0.f && a->path_temperature == a->path_temperature,
+           "%s: path_temperature must be >= 0", who);
   DF_CHECK(a->denoise_rounds >= 0 && a->denoise_rounds <= DFLASH_MAX_DENOISE_ROUNDS,
            "%s: denoise_rounds must be in [0, %d]", who, DFLASH_MAX_DENOISE_ROUNDS);
   DF_CHECK(a->conv_rank >= 0 && a->conv_rank <= DFLASH_MAX_CONV_RANK, "%s: conv_rank must be in [0, %d]", who,
@@ -961,6 +969,8 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   DF_CHECK(a->n_seqs > 0 && a->block >= 2 && a->topk > 0 && a->topk <= 16 && a->rank > 0 && a->rank <= 256,
            "%s: need n_seqs > 0, block >= 2, 0 < topk <= 16, 0 < rank <= 256", who);
   DF_CHECK(a->dims.hidden % 8 == 0, "%s: hidden %% 8 == 0 required", who);
+  DF_CHECK(a->temperature >= 0.f && a->temperature == a->temperature, "%s: temperature must be >= 0", who);
+  DF_CHECK(a->temperature == 0.f || a->base_pos, "%s: the sampled walk needs base_pos", who);
   rc = check_ws(ws, ws_bytes, path_ws(a), who);
   if (rc) return rc;
   Ctx c = header(ws);
@@ -982,6 +992,11 @@ int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dfl
   p.margin = a->margin;
   p.proj = reinterpret_cast<float*>(static_cast<char*>(ws) + kReservedBytes);
   p.status = c.status;
+  p.T = a->temperature;
+  p.seed = a->seed;
+  p.cycle = a->cycle;
+  p.base_pos = a->base_pos;
+  p.logq = a->logq;
   DF_LAUNCH((cudaStream_t)stream, TF_PATH, 0, launch_path_select(p, (cudaStream_t)stream));
   return DFLASH_OK;
 }
@@ -1046,10 +1061,13 @@ int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws
   DF_CHECK(a != nullptr, "%s: NULL args", who);
   int rc = check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, a->top_k, a->top_p, who);
   if (rc) return rc;
-  DF_CHECK(a->target_logits && a->draft_logits && a->draft_lse && a->drafts && a->base_pos && a->accept_len &&
+  DF_CHECK(a->target_logits && (a->draft_cand || (a->draft_logits && a->draft_lse)) && a->drafts && a->base_pos &&
+               a->accept_len &&
                a->out_tokens,
            "%s: NULL pointer", who);
   DF_CHECK(!a->commit_base || a->update_base_pos, "%s: commit_base needs update_base_pos", who);
+  DF_CHECK(!a->draft_cand || (a->draft_logq && a->draft_topk >= 1 && a->draft_topk <= 16),
+           "%s: draft_cand needs draft_logq and 1 <= draft_topk <= 16", who);
   size_t lo, ko, po, fo;
   rc = check_ws(ws, ws_bytes, sample_ws(a->n_seqs, a->block, &lo, &ko, &po, &fo), who);
   if (rc) return rc;
@@ -1073,6 +1091,11 @@ int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws
   d.commit_base = a->commit_base;
   d.commit_count = a->commit_count;
   d.update_base = a->update_base_pos;
+  if (a->draft_cand) {
+    d.qk = a->draft_topk;
+    d.qcand = a->draft_cand;
+    d.qlogq = a->draft_logq;
+  }
   d.top_k = a->top_k;
   d.top_p = a->top_p;
   if ((a->top_k > 0 && a->top_k < a->dims.vocab) || (a->top_p > 0.f && a->top_p < 1.f)) {

@@ -145,6 +145,13 @@ struct PathDesc {
   float* margin;
   float* proj;                // workspace [S][1 + (block-1)*topk][2*rank]: U e, V e per token slot
   uint32_t* status;
+  // sampled walk (T > 0): Philox draws, the proposal's log-probabilities
+  float T;                    // 0: greedy walk
+  uint64_t seed;
+  int cycle;
+  const int32_t* base_pos;    // [S] position of block row 0
+  float* logq;                // optional out [S][block-1][topk]
+  int32_t* cand_out;          // optional out [S][block-1][topk]: the candidate lists walked
 };
 
 // Sampling-mode verification (k_sample.cu).
@@ -163,6 +170,9 @@ struct SampleDesc {
   const RowFilter* filt_t;    // [S][block] target rows' kept sets (filtering), else null
   const RowFilter* filt_d;    // [S][block-1] draft rows' kept sets (acceptance, filtering), else null
   RowFilter* filt_d_out;      // [S][block-1] (draft draws, filtering)
+  int qk;                     // sparse proposal (the sampled path walk): candidates per row, else 0
+  const int32_t* qcand;       // [S][block-1][qk]
+  const float* qlogq;         // [S][block-1][qk] log q over the candidates
   uint64_t seed;
   int32_t* base_pos;          // [S] position of block row 0 (advanced when update_base)
   const float* draft_logits;  // [S][block-1][V]

@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "head_common.cuh"
 #include "internal.h"
+#include "rng.cuh"
 #include "launch.cuh"
 
 namespace dfl {
@@ -243,7 +244,10 @@ __global__ void __launch_bounds__(kPathThreads) path_proj_kernel(const __grid_co
 
 // One warp per sequence: lane q scores candidate q of row j from p_{j-1};
 // the greatest score wins, the lower rank on ties (the candidates are ranked
-// by draft logit).
+// by draft logit).  Sampled walk (T > 0): the proposal over the candidates
+// is softmax(score / T); p_j is a Gumbel-max draw from it (purpose
+// RNG_PATH, entry = candidate rank, position base_pos + j + 1), lower rank
+// on equal draw scores; logq receives log q_j per candidate.
 __global__ void path_walk_kernel(const __grid_constant__ PathDesc p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -264,6 +268,17 @@ __global__ void path_walk_kernel(const __grid_constant__ PathDesc p) {
       }
       sc = acc;
     }
+    if (p.T > 0.f) {
+      const float z = sc / p.T;
+      float mx = warp_max(lane < K ? z : -INFINITY);
+      const float lse = mx + logf(warp_sum(lane < K ? expf(z - mx) : 0.f));
+      const size_t o = ((size_t)s * (B - 1) + j) * K + lane;
+      if (lane < K && p.logq) p.logq[o] = z - lse;
+      sc = lane < K ? z + rng_gumbel(p.seed, (uint32_t)lane, (uint32_t)(p.base_pos[s] + j + 1), (uint32_t)s, RNG_PATH,
+                                     (uint32_t)p.cycle)
+                    : -INFINITY;
+    }
+    if (lane < K && p.cand_out) p.cand_out[((size_t)s * (B - 1) + j) * K + lane] = p.cand[((size_t)s * (B - 1) + j) * K + lane];
     float bv = sc;
     int bq = lane < K ? lane : 64;
 #pragma unroll

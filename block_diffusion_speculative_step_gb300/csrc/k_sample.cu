@@ -21,39 +21,12 @@
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
+#include "rng.cuh"
 
 namespace dfl {
 
 constexpr int kSampleThreads = 256;
 constexpr int kSplit = 16;  // CTAs per vocabulary row
-
-enum : uint32_t { RNG_DRAFT = 1, RNG_ACCEPT = 2, RNG_RESID = 3, RNG_BONUS = 4 };
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int round = 0; round < 10; ++round) {
-    if (round > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-  }
-  return c;
-}
-
-__device__ __forceinline__ float rng_uniform(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose,
-                                             uint32_t cycle) {
-  const uint4 x = philox4x32_10(make_uint4(v, pos, (seq << 8) | (purpose & 0xFFu), cycle), (uint32_t)seed,
-                                (uint32_t)(seed >> 32));
-  return ((float)(x.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
-}
-
-__device__ __forceinline__ float rng_gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t seq, uint32_t purpose,
-                                            uint32_t cycle) {
-  return -logf(-logf(rng_uniform(seed, v, pos, seq, purpose, cycle)));
-}
 
 // Running state of one slice: log-sum-exp pieces (m, s: sum exp(x - m)) and
 // the best draw (score, index; lower index on equal scores).
@@ -376,7 +349,18 @@ __global__ void spec_accept_kernel(const __grid_constant__ SampleDesc d, const f
     const float lp = filt_kept(d.filt_t ? d.filt_t + (size_t)s * B + j - 1 : nullptr, lt_dj, dj)
                          ? lt_dj * invT - lse_t[(size_t)s * B + j - 1]
                          : -INFINITY;
-    const float lq = d.draft_logits[((size_t)s * (B - 1) + j - 1) * V + dj] * invT - d.draft_lse[(size_t)s * (B - 1) + j - 1];
+    float lq;
+    if (d.qcand) {  // the sampled path walk's proposal: log q of d_j among the row's candidates
+      lq = -INFINITY;
+      const size_t o = ((size_t)s * (B - 1) + j - 1) * d.qk;
+      for (int q = 0; q < d.qk; ++q)
+        if (d.qcand[o + q] == dj) {
+          lq = d.qlogq[o + q];
+          break;
+        }
+    } else {
+      lq = d.draft_logits[((size_t)s * (B - 1) + j - 1) * V + dj] * invT - d.draft_lse[(size_t)s * (B - 1) + j - 1];
+    }
     const float lu = logf(rng_uniform(d.seed, 0u, (uint32_t)(P + j), (uint32_t)s, RNG_ACCEPT, (uint32_t)d.cycle));
     if (!(lu < lp - lq)) break;
     d.out_tokens[(size_t)s * B + k] = dj;
@@ -394,6 +378,8 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
   pdl_launch_dependents();
   __shared__ RowAcc red[kSampleThreads / 32];
   __shared__ int s_last;
+  __shared__ int s_qc[16];  // the sparse proposal of the rejected row (<= 16 candidates)
+  __shared__ float s_ql[16];
   const int s = blockIdx.x, sl = blockIdx.y;
   const int B = d.block, V = d.V;
   const float invT = 1.f / d.T;
@@ -402,9 +388,15 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
   const bool resid = k < B - 1;
   const int trow = resid ? k : B - 1;
   const float* tl = d.target_logits + ((size_t)s * B + trow) * V;
-  const float* dl = resid ? d.draft_logits + ((size_t)s * (B - 1) + k) * V : nullptr;
+  const bool sparse = d.qcand != nullptr;
+  const float* dl = (resid && !sparse) ? d.draft_logits + ((size_t)s * (B - 1) + k) * V : nullptr;
   const float lt = lse_t[(size_t)s * B + trow];
-  const float ld = resid ? d.draft_lse[(size_t)s * (B - 1) + k] : 0.f;
+  const float ld = (resid && !sparse) ? d.draft_lse[(size_t)s * (B - 1) + k] : 0.f;
+  if (sparse && resid && threadIdx.x < d.qk) {
+    s_qc[threadIdx.x] = d.qcand[((size_t)s * (B - 1) + k) * d.qk + threadIdx.x];
+    s_ql[threadIdx.x] = d.qlogq[((size_t)s * (B - 1) + k) * d.qk + threadIdx.x];
+  }
+  __syncthreads();
   const uint32_t pos = (uint32_t)(P + trow + 1);
   const int per = (V + kSplit - 1) / kSplit;
   const int v0 = sl * per, v1 = min(V, v0 + per);
@@ -416,7 +408,16 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
     if (!filt_kept(ft, tl[v], v)) continue;  // p = 0 here
     const float a = tl[v] * invT - lt;
     if (resid) {
-      const float b = filt_kept(fd, dl[v], v) ? dl[v] * invT - ld : -INFINITY;
+      float b = -INFINITY;
+      if (sparse) {
+        for (int q = 0; q < d.qk; ++q)
+          if (s_qc[q] == v) {
+            b = s_ql[q];
+            break;
+          }
+      } else if (filt_kept(fd, dl[v], v)) {
+        b = dl[v] * invT - ld;
+      }
       if (a > b)
         acc_draw(ar, (b == -INFINITY ? a : a + log1pf(-expf(b - a))) +
                          rng_gumbel(d.seed, (uint32_t)v, pos, (uint32_t)s, RNG_RESID, (uint32_t)d.cycle), v);
@@ -486,9 +487,11 @@ cudaError_t launch_sample_accept(const SampleDesc& d, float* lse_t, cudaStream_t
     e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * d.block), dim3(kFiltThreads), 0, st, d.target_logits, d.V,
                    1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_t), d.status);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * (d.block - 1)), dim3(kFiltThreads), 0, st, d.draft_logits, d.V,
-                   1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_d), d.status);
-    if (e != cudaSuccess) return e;
+    if (!d.qcand) {  // a sparse proposal (the sampled walk) is not filtered
+      e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * (d.block - 1)), dim3(kFiltThreads), 0, st, d.draft_logits,
+                     d.V, 1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_d), d.status);
+      if (e != cudaSuccess) return e;
+    }
   }
   e = launch_pdl(row_sample_kernel, dim3(d.n_seqs * d.block, kSplit), dim3(kSampleThreads), 0, st, d,
                  d.target_logits, d.block, 0, 0, lse_t, (int32_t*)nullptr, d.filt_t);

@@ -87,7 +87,8 @@ class dflash_draft_args(C.Structure):
                 ("lm_head", vp), ("n_seqs", i32), ("block", i32), ("anchor", vp), ("base_pos", vp),
                 ("mask_token", i32), ("max_pos", i32), ("rope_cs", vp), ("rope_max_pos", i32),
                 ("drafts", vp), ("logits", vp), ("path_topk", i32), ("path_rank", i32), ("path_u", vp),
-                ("path_v", vp), ("denoise_rounds", i32), ("conv_rank", i32),
+                ("path_v", vp), ("denoise_rounds", i32), ("path_temperature", C.c_float), ("path_seed", C.c_uint64),
+                ("path_cycle", i32), ("path_cand_out", vp), ("path_logq", vp), ("conv_rank", i32),
                 ("conv_w1", vp * DFLASH_MAX_LAYERS), ("conv_w2", vp * DFLASH_MAX_LAYERS)]
 
 
@@ -101,7 +102,8 @@ class dflash_verify_args(C.Structure):
 class dflash_path_args(C.Structure):
     _fields_ = [("dims", dflash_dims), ("n_seqs", i32), ("block", i32), ("topk", i32), ("rank", i32),
                 ("embed", vp), ("path_u", vp), ("path_v", vp), ("anchor", vp), ("cand", vp), ("path", vp),
-                ("margin", vp)]
+                ("margin", vp), ("temperature", C.c_float), ("seed", C.c_uint64), ("cycle", i32), ("base_pos", vp),
+                ("logq", vp)]
 
 
 class dflash_sample_drafts_args(C.Structure):
@@ -115,7 +117,8 @@ class dflash_sample_accept_args(C.Structure):
                 ("cycle", i32), ("seed", C.c_uint64), ("target_logits", vp), ("draft_logits", vp),
                 ("draft_lse", vp), ("drafts", vp), ("base_pos", vp), ("update_base_pos", i32),
                 ("accept_len", vp), ("out_tokens", vp), ("next_anchor", vp), ("commit_base", vp),
-                ("commit_count", vp), ("top_k", i32), ("top_p", C.c_float)]
+                ("commit_count", vp), ("top_k", i32), ("top_p", C.c_float), ("draft_topk", i32),
+                ("draft_cand", vp), ("draft_logq", vp)]
 
 
 class dflash_trace_stat(C.Structure):

@@ -351,6 +351,8 @@ class Engine:
             self.dlogits = torch.zeros(S * (B - 1), V, dtype=torch.float32, device=self.dev)
             self.tlogits = torch.zeros(S * B, V, dtype=torch.float32, device=self.dev)
             self.dlse = torch.zeros(S, B - 1, dtype=torch.float32, device=self.dev)
+        if self.w.path_topk:
+            return self._cycle_sampled_path(T, seed, cycle, top_k, top_p)
         self.draft(self.dlogits)
         a = D.dflash_sample_drafts_args()
         a.dims = self.ddims
@@ -366,6 +368,33 @@ class Engine:
         b.dims = self.tdims
         b.n_seqs, b.block, b.temperature, b.cycle, b.seed = S, B, T, cycle, seed
         b.target_logits, b.draft_logits, b.draft_lse = _ptr(self.tlogits), _ptr(self.dlogits), _ptr(self.dlse)
+        b.drafts, b.base_pos, b.update_base_pos = _ptr(self.drafts), _ptr(self.base_pos), 1
+        b.accept_len, b.out_tokens, b.next_anchor = _ptr(self.accept_len), _ptr(self.out_tokens), _ptr(self.anchor)
+        b.commit_base, b.commit_count = _ptr(self.commit_base), _ptr(self.commit_count)
+        b.top_k, b.top_p = top_k, top_p
+        D.dflash_sample_accept(b, self.ws_ptr, self.ws_bytes)
+        self.fuse(B, self.commit_base, self.commit_count)
+
+    def _cycle_sampled_path(self, T: float, seed: int, cycle: int, top_k: int, top_p: float):
+        """Sampling mode with the DFlash 2 path selector: the drafts are the
+        path walked by sampling over each row's candidates, and the
+        acceptance runs against that walk's sparse proposal."""
+        S, B, K = self.S, self.B, self.w.path_topk
+        if getattr(self, "pcand", None) is None:
+            self.pcand = torch.zeros(S, B - 1, K, dtype=torch.int32, device=self.dev)
+            self.plogq = torch.zeros(S, B - 1, K, dtype=torch.float32, device=self.dev)
+        a = self.draft_args()
+        a.path_temperature, a.path_seed, a.path_cycle = T, seed, cycle
+        a.path_cand_out, a.path_logq = _ptr(self.pcand), _ptr(self.plogq)
+        D.dflash_draft_block(a, self.ws_ptr, self.ws_bytes)
+        self.target_forward(B, self.anchor, self.drafts)
+        D.dflash_verify_accept(self.verify_args(B, self.h, self.drafts, self.tlogits, update=False), self.ws_ptr,
+                               self.ws_bytes)
+        b = D.dflash_sample_accept_args()
+        b.dims = self.tdims
+        b.n_seqs, b.block, b.temperature, b.cycle, b.seed = S, B, T, cycle, seed
+        b.target_logits = _ptr(self.tlogits)
+        b.draft_topk, b.draft_cand, b.draft_logq = K, _ptr(self.pcand), _ptr(self.plogq)
         b.drafts, b.base_pos, b.update_base_pos = _ptr(self.drafts), _ptr(self.base_pos), 1
         b.accept_len, b.out_tokens, b.next_anchor = _ptr(self.accept_len), _ptr(self.out_tokens), _ptr(self.anchor)
         b.commit_base, b.commit_count = _ptr(self.commit_base), _ptr(self.commit_count)

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 5
+#define DFLASH_ABI_VERSION 6
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -282,6 +282,12 @@ typedef struct {
   const void* path_u;                     /* [R][H] */
   const void* path_v;                     /* [R][H] */
   int32_t denoise_rounds;                 /* 0 / 1 = single step, else R rounds */
+  /* path selector walked by sampling (see dflash_path_select): */
+  float path_temperature;                 /* 0: greedy walk */
+  uint64_t path_seed;
+  int32_t path_cycle;
+  int32_t* path_cand_out;                 /* optional out [n_seqs][block-1][path_topk]: candidates */
+  float* path_logq;                       /* optional out [n_seqs][block-1][path_topk]: log q */
   int32_t conv_rank;                      /* 0 = no convolutions */
   const void* conv_w1[DFLASH_MAX_LAYERS]; /* [4][r][H] per draft layer */
   const void* conv_w2[DFLASH_MAX_LAYERS]; /* [4][2H][r] per draft layer */
@@ -330,6 +336,15 @@ int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes,
  * over the shared embedding rows e; p_0 = anchor[s]; p_j = the candidate of
  * row j with the highest score from p_{j-1} (lower rank on ties).
  * path[s][j-1] = p_j; margin (optional) = best - second-best score.
+ *
+ * Sampled walk (temperature > 0; the section's "greedily or by sampling"):
+ * the proposal over row j's candidates is q_j(c) = softmax(score(p_{j-1},
+ * c) / temperature); p_j is a Gumbel-max draw from it (Philox4x32-10 as in
+ * sampling mode, purpose 5, entry = candidate rank, position base_pos[s] +
+ * j); logq (optional [n_seqs][block-1][topk]) receives log q_j per
+ * candidate, margin the best - second draw score.  Hand cand and logq to
+ * dflash_sample_accept (draft_cand / draft_logq) for speculative sampling
+ * against this proposal.
  */
 typedef struct {
   dflash_dims dims;
@@ -341,6 +356,11 @@ typedef struct {
   const int32_t* cand;     /* [n_seqs][block-1][topk] */
   int32_t* path;           /* out [n_seqs][block-1] */
   float* margin;           /* optional out [n_seqs][block-1] */
+  float temperature;       /* 0: greedy walk; > 0: sampled walk */
+  uint64_t seed;           /* sampled walk */
+  int32_t cycle;           /* sampled walk */
+  const int32_t* base_pos; /* [n_seqs] position of block row 0 (sampled walk) */
+  float* logq;             /* optional out [n_seqs][block-1][topk] (sampled walk) */
 } dflash_path_args;
 int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);
@@ -412,6 +432,13 @@ typedef struct {
   int32_t* commit_count;        /* optional out [n_seqs]: accept_len + 1 */
   int32_t top_k;                /* as for the drafts */
   float top_p;                  /* as for the drafts */
+  /* Drafts from the sampled path walk: their proposal is sparse -- q_j over
+   * row j's candidates, log q_j from the walk, 0 elsewhere -- and replaces
+   * softmax(draft logits / T) (draft_logits / draft_lse are then unused).
+   * top_k / top_p filter the target rows only. */
+  int32_t draft_topk;           /* 0, or the candidates per row (<= 16) */
+  const int32_t* draft_cand;    /* [n_seqs][block-1][draft_topk] */
+  const float* draft_logq;      /* [n_seqs][block-1][draft_topk] */
 } dflash_sample_accept_args;
 int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws_bytes,
                          dflash_stream_t stream);
