@@ -297,6 +297,8 @@ constexpr int kMaxNC = 16;
 struct AttnTma {
   CUtensorMap kc, vc;  // cache [S*nkv*cap][D], box 64 dims x 128 keys, 128-byte swizzle
   CUtensorMap kb, vb;  // block scratch [S*nkv*rows][D] (bidirectional mode)
+  CUtensorMap q3;      // queries [M][nq][D], box 64 dims x grp heads x 64/grp tokens (q_tma)
+  int q_tma;           // the GQA group divides 64: a query tile is one 3-D box per 64 dims
   AttnDesc a;
 };
 
@@ -361,6 +363,52 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
         o3 = fmaf(v[r].w, w, o3);
       }
     const float L = Ls[i];
+    const int qv = qv0 + q_lo + i;
+    const int row = qv / grp, head = g * grp + qv % grp;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
+    dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
+    dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
+  }
+}
+
+// The same merge with the partials pushed instead of pulled: after a
+// cluster barrier (every rank's chunks done, its K/V buffers free), each
+// rank stores its partial rows into their owner's shared memory (recv:
+// [NC][RP][D+4], on the owner, away from psm); after a second barrier each
+// owner merges its rows from local shared memory, with the arithmetic and
+// order of rank_merge, and nothing reads a peer's memory any more.
+template <int D>
+__device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* psm, float* recv, int NC, int rank,
+                                           int nq_tile, int qv0, int grp, int g, int s, int rows, int QD, void* out) {
+  constexpr int PST = D + 4;
+  const int RP = (nq_tile + NC - 1) / NC;
+  for (int t = threadIdx.x; t < nq_tile * (PST / 4); t += blockDim.x) {
+    const int qr = t / (PST / 4), c4 = t % (PST / 4);
+    const int dst = qr / RP, i = qr - dst * RP;
+    const float4 v = *reinterpret_cast<const float4*>(psm + (size_t)qr * PST + 4 * c4);
+    float* r = cl.map_shared_rank(recv, dst) + ((size_t)rank * RP + i) * PST;
+    *reinterpret_cast<float4*>(r + 4 * c4) = v;
+  }
+  cl.sync();
+  const int q_lo = rank * RP;
+  const int nrow = max(0, min(nq_tile, q_lo + RP) - q_lo);
+  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(out);
+  for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
+    const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
+    float M = -INFINITY;
+    for (int r = 0; r < NC; ++r) M = fmaxf(M, recv[((size_t)r * RP + i) * PST + D]);
+    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    for (int r = 0; r < NC; ++r) {
+      const float* pr = recv + ((size_t)r * RP + i) * PST;
+      const float mr = pr[D];
+      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+      L = fmaf(pr[D + 1], w, L);
+      const float4 v = *reinterpret_cast<const float4*>(pr + e4);
+      o0 = fmaf(v.x, w, o0);
+      o1 = fmaf(v.y, w, o1);
+      o2 = fmaf(v.z, w, o2);
+      o3 = fmaf(v.w, w, o3);
+    }
     const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
@@ -751,13 +799,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   uint64_t* sfull = empty + 2;                            // [2] S in TMEM
   uint64_t* pdone = sfull + 2;                            // [2] P written, O rescaled
   uint64_t* ofull = pdone + 2;                            // P V done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(ofull + 1);
+  uint64_t* qfull = ofull + 1;                            // Q landed (TMA path)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(qfull + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
   // [2 chunk parities][8 pieces][64 rows] each
   float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 128);
   float* xsum = xmax + 2 * kTcAttnPieces * 64;
   float* psm = reinterpret_cast<float*>(sm);   // [64][PST] CTA partial (after the chunk loop)
-  float* scr = psm + kClQT * PST;              // merge scratch
 
   const AttnDesc& a = p.a;
   cg::cluster_group cl = cg::this_cluster();
@@ -821,10 +869,12 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       tc::mbar_init(&pdone[b], kTcAttnSoft);
     }
     tc::mbar_init(ofull, 1);
+    tc::mbar_init(qfull, 1);
     *abort = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&p.kc);
     tc::tma_prefetch_desc(&p.vc);
+    if (p.q_tma) tc::tma_prefetch_desc(&p.q3);
   }
   if (warp == 1) tc::tmem_alloc(tslot, 512);
   tc::tc_fence_before();
@@ -842,25 +892,40 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     if (nmine > 0 && !pre0) issue(rank, 0);
     if (nmine > 1 && !pre1) issue(rank + NC, 1);
   }
-  // ---- Q: the tile's query vectors in rows 0..nq_tile-1 and again in rows
-  // 64.., zero elsewhere (TMEM lanes 64..127 then hold a copy of every score
-  // row, so four warps share the softmax: one key half each)
+  // ---- Q: the tile's query vectors in rows 0..63 and again in rows 64..127
+  // (TMEM lanes 64..127 then hold a copy of every score row, so the softmax
+  // warps on all four lane quadrants share the rows).  When the GQA group
+  // divides 64 the tile (64 / grp tokens x grp heads) is one 3-D TMA box per
+  // 64 dims, loaded twice; rows past the tile's last query vector then hold
+  // other queries or zeros, whose rows of S, P and O are never used.
   const uint32_t qb = __cvta_generic_to_shared(Qs);
-  for (int t = threadIdx.x; t < kTcAttnRows * (D / 8); t += blockDim.x) {
-    const int qrow = t / (D / 8), ch = t % (D / 8);
-    const int qi = qrow & (kClQT - 1);
-    if (qi < nq_tile) {
-      const int qv = qv0 + qi;
-      const int row = qv / grp, head = g * grp + qv % grp;
-      const __nv_bfloat16* q =
-          reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * rows + row) * QD + (size_t)head * D;
-      cp_async16(qb + op_off(qrow, ch), q + ch * 8);
-    } else {
-      *reinterpret_cast<uint4*>(Qs + op_off(qrow, ch)) = make_uint4(0, 0, 0, 0);
+  if (p.q_tma) {
+    if (threadIdx.x == 0) {
+      tc::mbar_arrive_expect_tx(qfull, 4 * kClQT * 128);
+      const int z = s * rows + qv0 / grp, y = g * grp;
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+        for (int dup = 0; dup < 2; ++dup)
+          tc::tma_load_3d(Qs + h * (kTcAttnRows * 128) + dup * (kClQT * 128), &p.q3, 64 * h, y, z, qfull);
     }
+  } else {
+    for (int t = threadIdx.x; t < kTcAttnRows * (D / 8); t += blockDim.x) {
+      const int qrow = t / (D / 8), ch = t % (D / 8);
+      const int qi = qrow & (kClQT - 1);
+      if (qi < nq_tile) {
+        const int qv = qv0 + qi;
+        const int row = qv / grp, head = g * grp + qv % grp;
+        const __nv_bfloat16* q =
+            reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)s * rows + row) * QD + (size_t)head * D;
+        cp_async16(qb + op_off(qrow, ch), q + ch * 8);
+      } else {
+        *reinterpret_cast<uint4*>(Qs + op_off(qrow, ch)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_wait_all();
+    tc::fence_proxy_async_smem();
   }
-  cp_async_wait_all();
-  tc::fence_proxy_async_smem();
   __syncthreads();
 
   const uint32_t kvb = __cvta_generic_to_shared(KV);
@@ -905,6 +970,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         }
         tc::mma_commit(&sfull[b]);
       };
+      if (p.q_tma) wait(qfull, 0u);  // a timeout raises the abort flag: the loops below then stop
       // S of the first two chunks up front; then P V of chunk i as soon as its
       // P is written, and S of chunk i+2 after it (its K/V buffer and S
       // accumulator are the ones chunk i used), so that a chunk's load
@@ -1086,9 +1152,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 512);
   }
-  cl.sync();
-  rank_merge<D>(cl, psm, scr, NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
-  cl.sync();  // peers keep their shared memory until every rank has read it
+  cl.sync();  // every rank's chunks are done: its K/V buffers may receive
+  push_merge<D>(cl, psm, reinterpret_cast<float*>(sm + 2 * TILE), NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
 }
 
 // ------------------------------------------------------------------- host
@@ -1165,6 +1230,10 @@ bool attn_maps(const AttnDesc& a, AttnTma& p) {
   p.a = a;
   const uint64_t crow = a.pages ? (uint64_t)a.pool * a.nkv * a.ps : (uint64_t)a.n_seqs * a.nkv * a.cap;
   if (!make_tmap_bf16(&p.kc, a.kc, D, crow, kMmaCH) || !make_tmap_bf16(&p.vc, a.vc, D, crow, kMmaCH)) return false;
+  const int grp = a.nq / a.nkv;
+  p.q_tma = 0;
+  if (D == 128 && grp <= 64 && kClQT % grp == 0)
+    p.q_tma = make_tmap3_bf16(&p.q3, a.q, D, a.nq, (uint64_t)a.n_seqs * a.rows, grp, kClQT / grp) ? 1 : 0;
   if (a.mode == DFLASH_ATTN_BLOCK_BIDIR) {
     const uint64_t brow = (uint64_t)a.n_seqs * a.nkv * a.rows;
     if (!make_tmap_bf16(&p.kb, a.kb, D, brow, kMmaCH) || !make_tmap_bf16(&p.vb, a.vb, D, brow, kMmaCH)) return false;

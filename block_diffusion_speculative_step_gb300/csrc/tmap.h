@@ -33,4 +33,20 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 [outer][mid][inner] tensor (inner contiguous), box =
+// 64 (inner) x box_mid x box_outer, 128-byte swizzle: the box lands as
+// box_mid * box_outer rows of 128 bytes, outer-major.
+inline bool make_tmap3_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                            uint32_t box_mid, uint32_t box_outer) {
+  auto fn = tmap_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint32_t box[3] = {64, box_mid, box_outer};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace dfl
