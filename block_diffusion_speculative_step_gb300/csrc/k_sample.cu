@@ -140,96 +140,167 @@ __device__ __forceinline__ unsigned long long filt_mass(float l, float mx, float
   return __float2ull_rd(expf((l - mx) * invT) * 4294967296.0f);
 }
 
-// Among the entries v passing `in(v)`, select by `weight(v)` (1 for counts,
-// the integer mass for top-p) the entry at which the running total in the
-// order (key descending, index ascending) first reaches `need` (>= 1): its
-// key and index.  Radix rounds on the key from the top byte, then on the
-// index (ascending) among the entries with that key.
-template <typename In, typename W>
-__device__ void filt_select(const float* l, int V, In in, W weight, unsigned long long need, uint32_t* key_out,
-                            int* idx_out) {
-  __shared__ unsigned long long hist[256];
-  __shared__ unsigned long long s_need;
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_bin;
-  if (threadIdx.x == 0) {
-    s_need = need;
-    s_prefix = 0u;
+// Histogram of one radix round: one private 256-bin histogram per warp;
+// the lanes of a warp that hit the same bin are combined first (match +
+// add, the 64-bit weight added as two 16-bit halves, each sum < 2^21) and
+// one lane adds the group's total, so no bin is ever updated by two threads
+// at once and no atomics are needed (logits concentrate in a few key bytes,
+// which made shared atomics on one address the bottleneck).  Integer sums:
+// the result does not depend on the order of the additions.
+constexpr int kFiltWarps = kFiltThreads / 32;
+
+template <typename In, typename W, typename Bin>
+__device__ void filt_hist(const float* l, int V, In in, W weight, Bin bin_of, unsigned long long* hist,
+                          unsigned long long* whist) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long* mine = whist + warp * 256;
+  for (int i = threadIdx.x; i < kFiltWarps * 256; i += blockDim.x) whist[i] = 0ull;
+  __syncthreads();
+  // eight elements per thread loaded before any is processed: the warp
+  // intrinsics below keep the compiler from moving later loads ahead
+  constexpr int U = 8;
+  for (int base = warp * 32 * U; base < V; base += blockDim.x * U) {
+    float xs[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = base + u * 32 + lane;
+      xs[u] = v < V ? l[v] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = base + u * 32 + lane;
+      int bin = -1;
+      unsigned long long w = 0ull;
+      if (v < V && in(xs[u], v)) {
+        bin = bin_of(xs[u], v);
+        if (bin >= 0) w = weight(xs[u]);
+      }
+      if (w == 0ull) bin = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      const unsigned hi = __reduce_add_sync(peers, (unsigned)(w >> 16));
+      const unsigned lo = __reduce_add_sync(peers, (unsigned)(w & 0xFFFFull));
+      if (bin >= 0 && lane == __ffs(peers) - 1) mine[bin] += ((unsigned long long)hi << 16) + lo;
+      __syncwarp();
+    }
   }
   __syncthreads();
-  uint32_t mask = 0u;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0ull;
-    __syncthreads();
-    const uint32_t prefix = s_prefix;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) {
-      const float x = l[v];
-      if (!in(x, v)) continue;
-      const uint32_t k = okey(x);
-      if ((k & mask) != prefix) continue;
-      const unsigned long long w = weight(x);
-      if (w) atomicAdd(&hist[(k >> shift) & 255u], w);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long acc = 0ull, nd = s_need;
-      int b = 255;
-      for (; b > 0; --b) {
-        if (acc + hist[b] >= nd) break;
-        acc += hist[b];
-      }
-      s_need = nd - acc;
-      s_prefix = prefix | ((uint32_t)b << shift);
-    }
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  const uint32_t key = s_prefix;
-  // among the entries with this key (equal logits, equal weights), the
-  // lowest indices first: the one where the total reaches s_need
-  __shared__ int s_ip;
-  if (threadIdx.x == 0) s_ip = 0;
-  __syncthreads();
-  int imask = 0;
-  for (int shift = 16; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0ull;
-    __syncthreads();
-    const int ip = s_ip;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) {
-      const float x = l[v];
-      if (!in(x, v) || okey(x) != key || (v & imask) != ip) continue;
-      const unsigned long long w = weight(x);
-      if (w) atomicAdd(&hist[(v >> shift) & 255], w);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long acc = 0ull, nd = s_need;
-      int b = 0;
-      for (; b < 255; ++b) {
-        if (acc + hist[b] >= nd) break;
-        acc += hist[b];
-      }
-      s_need = nd - acc;
-      s_ip = ip | (b << shift);
-    }
-    imask |= 255 << shift;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    *key_out = key;
-    *idx_out = s_ip;
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    unsigned long long t = 0ull;
+    for (int g = 0; g < kFiltWarps; ++g) t += whist[g * 256 + b];
+    hist[b] = t;
   }
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* logits, int V, float invT, int top_k,
-                                                                  float top_p, RowFilter* out, uint32_t* status) {
+// One warp finds the bin at which the running total of hist -- from bin 255
+// down (desc) or from bin 0 up -- first reaches nd (>= 1): lane l sums its 8
+// bins, a shuffle scan locates the lane, that lane walks its bins and
+// writes the bin, the need left inside it and the bin's own total to shared
+// memory (the last bin takes whatever is left, as a serial walk would).
+__device__ __forceinline__ void filt_find_bin(const unsigned long long* hist, unsigned long long nd, bool desc,
+                                              int* s_bin, unsigned long long* s_need, unsigned long long* s_binv) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long t = 0ull;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) t += hist[desc ? 255 - (8 * lane + e) : 8 * lane + e];
+  unsigned long long inc = t;  // inclusive scan over lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, inc >= nd);
+  const int src = hit ? __ffs(hit) - 1 : 31;
+  if (lane == src) {
+    unsigned long long acc = inc - t;
+    int k = 0;
+    for (; k < 7; ++k) {
+      const unsigned long long h = hist[desc ? 255 - (8 * lane + k) : 8 * lane + k];
+      if (acc + h >= nd) break;
+      acc += h;
+    }
+    const int bn = desc ? 255 - (8 * lane + k) : 8 * lane + k;
+    *s_bin = bn;
+    *s_need = nd - acc;
+    *s_binv = hist[bn];
+  }
+}
+
+// Among the entries v passing `in(v)`, select by `weight(v)` (1 for counts,
+// the integer mass for top-p) the entry at which the running total in the
+// order (key descending, index ascending) first reaches `need` (>= 1): its
+// key and index.  Radix rounds on the key from the top byte; then, only when
+// the boundary falls inside a group of equal logits, on the index
+// (ascending) among that group (idx = INT_MAX: the whole group is kept).
+template <typename In, typename W>
+__device__ void filt_select(const float* l, int V, In in, W weight, unsigned long long need, uint32_t* key_out,
+                            int* idx_out, unsigned long long* whist) {
+  __shared__ unsigned long long hist[256];
+  __shared__ unsigned long long s_need, s_binv;
+  __shared__ int s_bin;
+  if (threadIdx.x == 0) s_need = need;
+  __syncthreads();
+  uint32_t prefix = 0u, mask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    filt_hist(l, V, in, weight,
+              [prefix, mask, shift](float x, int) {
+                const uint32_t k = okey(x);
+                return (k & mask) == prefix ? (int)((k >> shift) & 255u) : -1;
+              },
+              hist, whist);
+    if (threadIdx.x < 32) filt_find_bin(hist, s_need, true, &s_bin, &s_need, &s_binv);
+    __syncthreads();
+    prefix |= (uint32_t)s_bin << shift;
+    mask |= 255u << shift;
+  }
+  const uint32_t key = prefix;
+  // the group of entries with this key has equal weights e: it holds
+  // s_binv / e entries, of which ceil(s_need / e) are kept
+  const uint32_t kb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+  const unsigned long long e = weight(__uint_as_float(kb));
+  const unsigned long long n_grp = e ? s_binv / e : 0ull;
+  const unsigned long long n_need = e ? (s_need + e - 1) / e : 0ull;
+  int idx = INT_MAX;
+  if (n_need < n_grp) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_need = n_need;
+    __syncthreads();
+    int ip = 0, imask = 0;
+    for (int shift = 16; shift >= 0; shift -= 8) {
+      filt_hist(l, V, in, [](float) { return 1ull; },
+                [key, imask, ip, shift](float x, int v) {
+                  return (okey(x) == key && (v & imask) == ip) ? ((v >> shift) & 255) : -1;
+                },
+                hist, whist);
+      if (threadIdx.x < 32) filt_find_bin(hist, s_need, false, &s_bin, &s_need, &s_binv);
+      __syncthreads();
+      ip |= s_bin << shift;
+      imask |= 255 << shift;
+    }
+    idx = ip;
+  }
+  if (threadIdx.x == 0) {
+    *key_out = key;
+    *idx_out = idx;
+  }
+  __syncthreads();
+}
+
+// Rows [0, rows_a) of logits_a and then the rows of logits_b (two row sets
+// in one launch); one CTA per row.
+__global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* logits_a, int rows_a, RowFilter* out_a,
+                                                                  const float* logits_b, RowFilter* out_b, int V,
+                                                                  float invT, int top_k, float top_p, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[kFiltThreads / 32];
   __shared__ unsigned long long redu[kFiltThreads / 32];
   __shared__ RowFilter s_f;
-  const float* l = logits + (size_t)blockIdx.x * V;
+  extern __shared__ unsigned long long filt_sm[];  // [kFiltWarps][256] private histograms
+  const bool in_a = (int)blockIdx.x < rows_a;
+  const int row = in_a ? (int)blockIdx.x : (int)blockIdx.x - rows_a;
+  const float* l = (in_a ? logits_a : logits_b) + (size_t)row * V;
+  RowFilter* out = in_a ? out_a : out_b;
   float mx = -INFINITY;
   for (int v = threadIdx.x; v < V; v += blockDim.x) {
     const float x = l[v];
@@ -246,7 +317,7 @@ __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* l
     uint32_t k;
     int i;
     filt_select(l, V, [](float x, int) { return x == x; }, [](float) { return 1ull; }, (unsigned long long)top_k, &k,
-                &i);
+                &i, filt_sm);
     if (threadIdx.x == 0) s_f = RowFilter{k, i};
     __syncthreads();
   }
@@ -269,11 +340,11 @@ __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* l
     if (need < 1ull) need = 1ull;
     uint32_t k;
     int i;
-    filt_select(l, V, in, mass, need, &k, &i);
+    filt_select(l, V, in, mass, need, &k, &i, filt_sm);
     if (threadIdx.x == 0) s_f = RowFilter{k, i};
     __syncthreads();
   }
-  if (threadIdx.x == 0) out[blockIdx.x] = s_f;
+  if (threadIdx.x == 0) out[row] = s_f;
   (void)status;
 }
 
@@ -462,6 +533,12 @@ __global__ void __launch_bounds__(kSampleThreads) resample_kernel(const __grid_c
   }
 }
 
+constexpr size_t kFiltSmem = (size_t)kFiltWarps * 256 * sizeof(unsigned long long);
+
+static cudaError_t filter_smem_attr() {
+  return cudaFuncSetAttribute(row_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFiltSmem);
+}
+
 static bool filtering(const SampleDesc& d) {
   return (d.top_k > 0 && d.top_k < d.V) || (d.top_p > 0.f && d.top_p < 1.f);
 }
@@ -471,8 +548,11 @@ cudaError_t launch_sample_drafts(const SampleDesc& d, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const RowFilter* fd = nullptr;
   if (filtering(d)) {
-    cudaError_t e = launch_pdl(row_filter_kernel, dim3(rows), dim3(kFiltThreads), 0, st, d.draft_logits, d.V,
-                               1.f / d.T, d.top_k, d.top_p, d.filt_d_out, d.status);
+    cudaError_t e = filter_smem_attr();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(row_filter_kernel, dim3(rows), dim3(kFiltThreads), kFiltSmem, st, d.draft_logits, rows,
+                   d.filt_d_out, (const float*)nullptr, (RowFilter*)nullptr, d.V, 1.f / d.T, d.top_k, d.top_p,
+                   d.status);
     if (e != cudaSuccess) return e;
     fd = d.filt_d_out;
   }
@@ -483,15 +563,14 @@ cudaError_t launch_sample_drafts(const SampleDesc& d, cudaStream_t st) {
 cudaError_t launch_sample_accept(const SampleDesc& d, float* lse_t, cudaStream_t st) {
   if (d.n_seqs == 0) return cudaSuccess;
   cudaError_t e;
-  if (filtering(d)) {  // the target rows' and (again, identically) the draft rows' kept sets
-    e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * d.block), dim3(kFiltThreads), 0, st, d.target_logits, d.V,
-                   1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_t), d.status);
+  if (filtering(d)) {  // one launch: the target rows' and (again, identically) the draft rows' kept sets
+    e = filter_smem_attr();
     if (e != cudaSuccess) return e;
-    if (!d.qcand) {  // a sparse proposal (the sampled walk) is not filtered
-      e = launch_pdl(row_filter_kernel, dim3(d.n_seqs * (d.block - 1)), dim3(kFiltThreads), 0, st, d.draft_logits,
-                     d.V, 1.f / d.T, d.top_k, d.top_p, const_cast<RowFilter*>(d.filt_d), d.status);
-      if (e != cudaSuccess) return e;
-    }
+    const int rt = d.n_seqs * d.block, rd = d.qcand ? 0 : d.n_seqs * (d.block - 1);  // a sparse proposal is not filtered
+    e = launch_pdl(row_filter_kernel, dim3(rt + rd), dim3(kFiltThreads), kFiltSmem, st, d.target_logits, rt,
+                   const_cast<RowFilter*>(d.filt_t), d.draft_logits, const_cast<RowFilter*>(d.filt_d), d.V, 1.f / d.T,
+                   d.top_k, d.top_p, d.status);
+    if (e != cudaSuccess) return e;
   }
   e = launch_pdl(row_sample_kernel, dim3(d.n_seqs * d.block, kSplit), dim3(kSampleThreads), 0, st, d,
                  d.target_logits, d.block, 0, 0, lse_t, (int32_t*)nullptr, d.filt_t);
