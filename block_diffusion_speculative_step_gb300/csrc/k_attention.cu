@@ -1046,9 +1046,14 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       }
       xm[piece * 64 + qr] = cmax;
       tc::named_bar(2, kTcAttnSoft);
-      float m_new = m_run;
+      float m_cand = m_run;
 #pragma unroll
-      for (int pc = 0; pc < kTcAttnPieces; ++pc) m_new = fmaxf(m_new, xm[pc * 64 + qr]);
+      for (int pc = 0; pc < kTcAttnPieces; ++pc) m_cand = fmaxf(m_cand, xm[pc * 64 + qr]);
+      // The reference maximum moves only when the chunk's maximum exceeds it
+      // by more than 8 (log2 units, a factor 256): P then stays below 2^8, and
+      // most chunks skip rescaling O in TMEM (alpha = 1 exactly).  O and l
+      // are kept against the same reference, so the result is unchanged.
+      const float m_new = (m_run == -INFINITY || m_cand > m_run + 8.f) ? m_cand : m_run;
       const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
       float sum = 0.f;
 #pragma unroll
