@@ -423,6 +423,18 @@ def run_ours(args):
     mean_accept = float(accept.float().mean())
     value, verified = job_rates(world, S, args.steps, ms, float((accept + 1).sum()))
 
+    # per-step distribution: each replay between its own pair of events
+    n_pct = max(3, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pct)]
+    torch.cuda.synchronize()
+    for a_ev, b_ev in evs:
+        a_ev.record()
+        graph.replay()
+        b_ev.record()
+    torch.cuda.synchronize()
+    per = sorted(a_ev.elapsed_time(b_ev) for a_ev, b_ev in evs)
+    step_pct = {"steps": n_pct, "p50_ms": per[len(per) // 2], "p95_ms": per[min(len(per) - 1, int(0.95 * len(per)))]}
+
     # the same cycle in sampling mode (speculative sampling at T = 1), graph replay
     sampling = None
     if eng.has_target and not args.no_sampling:
@@ -629,8 +641,8 @@ def run_ours(args):
             "verified_tok_s": verified, "mean_accept": mean_accept,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-            "clocks": clocks, "kernels": per_fam, "sampling": sampling, "denoise": denoise, "conv": conv,
-            "paged": paged}
+            "clocks": clocks, "step_ms_distribution": step_pct, "kernels": per_fam, "sampling": sampling,
+            "denoise": denoise, "conv": conv, "paged": paged}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
