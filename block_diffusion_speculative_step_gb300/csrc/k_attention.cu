@@ -24,11 +24,13 @@
 // nothing spins and nothing round-trips through HBM.
 //
 // For head dimension 128 the bf16 path runs attn_tc_kernel instead, which
-// computes the same function on the tcgen05 tensor cores: S and O are TMEM
-// accumulators, the 64 query rows are duplicated into MMA rows 64..127 so
-// that the softmax warps on all four TMEM lane quadrants share the rows, and
-// the partials merge through the same cluster path.  DFLASH_ATTN_MMASYNC=1 in
-// the environment selects the mma.sync kernel for head dimension 128 too.
+// computes the same function on the tcgen05 tensor cores: the query tile
+// arrives as one 3-D TMA box per 64 dims, S and O are TMEM accumulators, the
+// 64 query rows are duplicated into MMA rows 64..127 so that the softmax
+// warps on all four TMEM lane quadrants share the rows, and each rank pushes
+// its partial rows into their owner's shared memory for a local merge (same
+// arithmetic and order as the pulled merge).  DFLASH_ATTN_MMASYNC=1 in the
+// environment selects the mma.sync kernel for head dimension 128 too.
 #include <cooperative_groups.h>
 #include <stdlib.h>
 
