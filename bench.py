@@ -310,6 +310,16 @@ def job_rates(world: int, S: int, steps: int, ms: float, tokens_per_step: float)
     return value, verified
 
 
+def cost_model(t_draft_ms: float, t_cycle_ms: float, tokens_per_cycle: float) -> dict:
+    """The per-token cost of a speculative cycle (DFlash 2 release news,
+    'beyond speed: what DFlash 2 means for deployment'): the draft and the
+    verification of one round spread over the tokens the round yields.  The
+    verification share is the rest of the measured cycle (target forward,
+    acceptance and context injection)."""
+    return {"draft_ms": t_draft_ms, "verify_and_fusion_ms": t_cycle_ms - t_draft_ms,
+            "tokens_per_cycle": tokens_per_cycle, "per_token_ms": t_cycle_ms / tokens_per_cycle}
+
+
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_speculative_step_gb300", "csrc")
@@ -552,6 +562,12 @@ def run_ours(args):
         eng.base_pos.copy_(base0)
         eng.anchor.copy_(anchor0)
 
+    # per-token cost: the draft-block step alone, the rest of the cycle, over
+    # the tokens a cycle emits (accepted drafts + the bonus token)
+    cost = None
+    if denoise is not None:
+        cost = cost_model(denoise["rounds_ms"]["1"], ms_per_step, mean_accept + 1.0)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -642,7 +658,7 @@ def run_ours(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "clocks": clocks, "step_ms_distribution": step_pct, "kernels": per_fam, "sampling": sampling,
-            "denoise": denoise, "conv": conv, "paged": paged}
+            "denoise": denoise, "conv": conv, "paged": paged, "cost_model": cost}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -1,7 +1,10 @@
 """The replica path of bench.py on CPU with two gloo ranks: the timed region
 is the maximum over ranks, the whole-job rate counts every replica's work,
-and the reference arm runs on rank 0 only."""
+the reference arm runs on rank 0 only, and the per-token cost model
+matches the pages' worked example."""
+import json
 import os
+import pathlib
 import socket
 import sys
 
@@ -66,3 +69,18 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = type("A", (), {"workload": "qwen3-8b-b1", "steps": 1, "warmup": 0, "gpus": 2})()
     assert bench.run_reference(args) is None
     assert capsys.readouterr().out == ""
+
+
+def test_cost_model_matches_the_worked_example():
+    """The bench's per-token cost against the pages' worked example: a 3 ms
+    draft and a 20 ms verification (a 23 ms cycle) cost about 3.8 ms a token
+    at 6 tokens per round and 11.5 ms at 2."""
+    import bench
+    g = json.loads((pathlib.Path(__file__).parent / "golden" / "cost_model_example.json").read_text())
+    cycle = g["t_draft_ms"] + g["t_verify_ms"]
+    for case in g["cases"]:
+        c = bench.cost_model(g["t_draft_ms"], cycle, case["accepted"])
+        assert abs(c["per_token_ms"] - case["ms_per_token"]) <= case["abs_tol"]
+        assert c["verify_and_fusion_ms"] == g["t_verify_ms"]
+    sp = g["baseline_ms_per_token"] / bench.cost_model(g["t_draft_ms"], cycle, 6)["per_token_ms"]
+    assert abs(sp - g["speedup_at_6"]) <= g["speedup_tol"]
