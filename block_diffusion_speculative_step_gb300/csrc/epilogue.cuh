@@ -87,6 +87,15 @@ __device__ __forceinline__ void epi_single(const Epi& e, int n, int m, float v) 
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Rotation of one RoPE pair by (c, s) = (cos, sin): every product and sum
+// rounded on its own (no fused multiply-add), so every epilogue that applies
+// it gets the same bits whatever code surrounds it: a token row's K/V and
+// queries do not depend on how many rows share the launch.
+__device__ __forceinline__ void rope_rot(float va, float vb, float c, float s, float& lo, float& hi) {
+  lo = __fsub_rn(__fmul_rn(va, c), __fmul_rn(vb, s));
+  hi = __fadd_rn(__fmul_rn(vb, c), __fmul_rn(va, s));
+}
+
 // Pair epilogue for unit u, token row m, accumulators (va, vb): SwiGLU, or
 // RoPE of the pair (e, e + d/2) followed by the Q / K / V scatter.
 template <typename T>
@@ -104,8 +113,8 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int u, int m, float va, f
   if (pos < 0 || pos >= e.rope_max_pos) return;  // outside the RoPE table: nothing is written
   if (ra < e.QD + e.KD) {  // Q or K: rotate the pair by pos * w_col
     const float2 cs = *reinterpret_cast<const float2*>(e.rope_cs + ((size_t)pos * half + col) * 2);
-    const float lo = va * cs.x - vb * cs.y;
-    const float hi = vb * cs.x + va * cs.y;
+    float lo, hi;
+    rope_rot(va, vb, cs.x, cs.y, lo, hi);
     va = lo;
     vb = hi;
   }
@@ -240,8 +249,7 @@ __device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, const fl
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 cs = rotate ? rw.cs[j] : make_float2(1.f, 0.f);
-    lo[j] = va[j] * cs.x - vb[j] * cs.y;
-    hi[j] = vb[j] * cs.x + va[j] * cs.y;
+    rope_rot(va[j], vb[j], cs.x, cs.y, lo[j], hi[j]);
   }
   if (ra < e.QD) {
 #pragma unroll

@@ -99,7 +99,16 @@ __device__ __forceinline__ void head_finish(const HeadDesc& h, int n_arrivals, i
   for (int m = threadIdx.x >> 5; m < M; m += nwarps) {
     if (!head_row_used(h, m)) continue;
     Top2 t = top2_empty();
-    for (int b = lane; b < n_parts; b += 32) t = top2_merge(t, ldcg_top2(part + (size_t)b * M + m));
+    for (int b0 = 0; b0 < n_parts; b0 += 32 * 8) {  // eight loads in flight per lane
+      Top2 x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int b = b0 + 32 * q + lane;
+        x[q] = b < n_parts ? ldcg_top2(part + (size_t)b * M + m) : top2_empty();
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t = top2_merge(t, x[q]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Top2 u;

@@ -18,6 +18,12 @@
 // token row's result does not depend on the other rows in the launch.
 // Weight loads for the first stages are issued before griddepcontrol.wait,
 // overlapping the predecessor kernel's tail.  Every wait is bounded.
+//
+// Tiles of more than 16 token rows finish in 16-column chunks; their
+// column-independent row operands are staged once per CTA in shared memory
+// (RowTab), so a chunk costs one global round trip.  The LM head keeps, per
+// CTA, each token row's best (logit, index) and runner-up over the tiles the
+// CTA finishes; the last CTA merges one triple per CTA.
 #include <cudaTypedefs.h>
 
 #include "epilogue.cuh"
@@ -47,7 +53,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int G;          // CTAs (runs)
   int M;          // token rows
   float* part;    // partial slots [n_tiles + G][BN][128]
-  Top2* tops;     // LM head: per-tile triples [n_tiles][M]
+  Top2* tops;     // LM head: per-CTA triples [G][M]
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
   uint32_t* counters;
   uint32_t* status;
@@ -63,7 +69,9 @@ struct TcCfg {
   static constexpr int ACC = BN < 32 ? 32 : BN;  // columns of one accumulator
   static constexpr int TMEM_COLS = 2 * ACC;       // double-buffered
   static constexpr int XCH = 16 * 128 * 4;        // epilogue exchange tile
-  static constexpr int SMEM = STAGES * STAGE + XCH + 256 + 1024;
+  static constexpr bool WIDE = BN > 16;           // several 16-column chunks per tile
+  static constexpr int TAB = WIDE ? 2304 : 0;     // RowTab, 256-byte multiple
+  static constexpr int SMEM = STAGES * STAGE + XCH + 256 + TAB + 1024;
   static_assert(SMEM > 117 * 1024, "a second CTA must not fit on the SM");
 };
 
@@ -150,7 +158,8 @@ __device__ __forceinline__ bool tc_unit(const TcLocal& L, int t, int r, int& uni
 // rw / old hold the epilogue's loads for columns 0..15, issued while the
 // accumulator was being computed; later column groups load here.
 __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int t, int c0, int r, int et,
-                                            float (&v)[16], float* xch, const EpiRows& rw, const float (&old)[16]) {
+                                            float (&v)[16], float* xch, const EpiRows& rw, const float (&old)[16],
+                                            Top2* s_top) {
   const int M = L.M;
   if (L.mode == TC_HEAD) {
     const int vrow = t * 128 + r;
@@ -232,7 +241,9 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
       u.v2 = __shfl_xor_sync(0xffffffffu, tp.v2, o);
       tp = top2_merge(tp, u);
     }
-    if (g8 == 0 && m < M) L.tops[(size_t)t * M + m] = tp;
+    // the CTA's running selection of token row m over the tiles it finished
+    // (one writer per row: thread 8 * (m % 16))
+    if (g8 == 0 && m < M) s_top[m] = top2_merge(s_top[m], tp);
     return;
   }
   int unit = 0;
@@ -269,12 +280,146 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
   }
 }
 
+// ---- wide tiles (more than 16 token rows).  The operands of a token row
+// that do not depend on the output column (liveness, position, K/V slot) are
+// resolved once per CTA into shared memory, and each 16-column chunk issues
+// its few global loads -- the residual being added to, or the rotation of the
+// unit's column -- all at once, before its accumulator values are read: one
+// round trip per chunk instead of a chain of dependent loads.  The arithmetic
+// and the set of writes are those of the 16-column forms.
+struct RowTab {
+  uint32_t live[8];  // bit m % 32 of word m / 32: token row m is written
+  int32_t pos[256];  // QKV: position of a live row inside the RoPE table, else -1
+  uint32_t kvr[256]; // QKV: K/V destination row (sequence, head 0, slot); ~0u: none
+};
+static_assert(sizeof(RowTab) <= 2304, "row table");
+
+// All 128 epilogue threads (et = 0..127) call this: it holds named barriers.
+__device__ __forceinline__ void row_tab_build(const Epi& e, int M, int et, RowTab* tb) {
+  const int lane = et & 31;
+#pragma unroll
+  for (int m0 = 0; m0 < 256; m0 += 128) {
+    const int m = m0 + et;
+    const bool lv = m < M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+    const uint32_t bits = __ballot_sync(0xffffffffu, lv);
+    if (lane == 0) tb->live[m >> 5] = bits;
+    int pos = -1;
+    uint32_t kvr = ~0u;
+    if (e.kind == EPI_QKV && lv) {
+      const int q = __ldg(e.base_pos + m / e.rows) + m % e.rows;
+      if (q >= 0 && q < e.rope_max_pos) {
+        pos = q;
+        const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? q % e.kv_window : q) : m % e.rows;
+        if (slot < e.kv_cap) kvr = (uint32_t)((m / e.rows) * e.nkv) * (uint32_t)e.kv_cap + (uint32_t)slot;
+      }
+    }
+    tb->pos[m] = pos;
+    tb->kvr[m] = kvr;
+  }
+  tc::named_bar(1, 128);
+}
+
+// The global loads of chunk [c0, c0+16) for output unit `unit`: residual
+// rows (EPI_RESID; rows < M are in the buffer whether live or not) or the
+// (cos, sin) pairs of the unit's column (EPI_QKV, Q and K rows).
+__device__ __forceinline__ void wide_loads(const Epi& e, const RowTab* tb, int unit, bool works, int c0, int M,
+                                           float (&pre)[32]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    pre[2 * j] = 0.f;
+    pre[2 * j + 1] = 0.f;
+  }
+  if (e.kind == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < M) pre[j] = e.out_f32[(size_t)(c0 + j) * e.ldo + unit];
+  } else if (e.kind == EPI_QKV) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pre[2 * j] = 1.f;  // (1, 0): V rows are not rotated
+    const int ra = e.seg_row0 + (unit / e.half) * e.d + (unit % e.half);
+    if (works && ra < e.QD + e.KD) {
+      const float2* cs = reinterpret_cast<const float2*>(e.rope_cs) + ra % e.d;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int q = tb->pos[c0 + j];
+        const float2 c = q >= 0 ? __ldg(cs + (size_t)q * e.half) : make_float2(1.f, 0.f);
+        pre[2 * j] = c.x;
+        pre[2 * j + 1] = c.y;
+      }
+    }
+  }
+}
+
+// Epilogue of chunk [c0, c0+16) of tile t for accumulator row r, with the
+// chunk's loads in `pre` (all 128 epilogue threads: pair kinds exchange rows).
+__device__ __forceinline__ void final_wide(const TcLocal& L, const Epi& e, const RowTab* tb, int t, int c0, int r,
+                                           const float (&v)[16], float* xch, const float (&pre)[32]) {
+  int unit = 0;
+  const bool works = tc_unit(L, t, r, unit);
+  const uint32_t live = (tb->live[c0 >> 5] >> (c0 & 31)) & 0xffffu;
+  if (L.kind == EPI_STORE || L.kind == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if ((live >> j) & 1u) e.out_f32[(size_t)(c0 + j) * e.ldo + unit] = pre[j] + v[j];
+    return;
+  }
+  const int half = (L.kind == EPI_SWIGLU) ? 64 : L.d / 2;
+  tc::named_bar(1, 128);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
+  tc::named_bar(1, 128);
+  if (!works) return;
+  float w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = xch[j * 128 + r + half];
+  if (L.kind == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if ((live >> j) & 1u)
+        reinterpret_cast<__nv_bfloat16*>(e.act_out)[(size_t)(c0 + j) * e.inter + unit] =
+            from_f<__nv_bfloat16>(silu_f(v[j]) * w[j]);
+    return;
+  }
+  const int d = e.d;
+  const int ra = e.seg_row0 + (unit / half) * d + (unit % half);
+  const int col = ra % d;
+  float lo[16], hi[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    // pre holds (1, 0) for V rows and rows outside the RoPE table
+    rope_rot(v[j], w[j], pre[2 * j], pre[2 * j + 1], lo[j], hi[j]);
+  }
+  if (ra < e.QD) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (tb->pos[c0 + j] >= 0) {
+        __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(e.q_out) + (size_t)(c0 + j) * e.QD + ra;
+        q[0] = from_f<__nv_bfloat16>(lo[j]);
+        q[half] = from_f<__nv_bfloat16>(hi[j]);
+      }
+    return;
+  }
+  const bool is_k = ra < e.QD + e.KD;
+  const int rr = is_k ? ra - e.QD : ra - e.QD - e.KD;
+  __nv_bfloat16* base =
+      reinterpret_cast<__nv_bfloat16*>(is_k ? e.k_dst : e.v_dst) + (size_t)(rr / d) * e.kv_cap * d + col;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t kv = tb->kvr[c0 + j];
+    if (kv == ~0u) continue;
+    __nv_bfloat16* dst = base + (size_t)kv * d;
+    dst[0] = from_f<__nv_bfloat16>(lo[j]);
+    dst[half] = from_f<__nv_bfloat16>(hi[j]);
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<BN>;
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_last_head;
+  __shared__ Top2 s_top[256];  // LM head: best (logit, index) and runner-up of each token row so far
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xch = reinterpret_cast<float*>(smem + ST * Cfg::STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * Cfg::STAGE + Cfg::XCH);
@@ -284,6 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_flag = reinterpret_cast<int*>(tmem_slot + 2);
+  RowTab* tab = reinterpret_cast<RowTab*>(smem + ST * Cfg::STAGE + Cfg::XCH + 256);
 
   const TcLocal L = tc_local(p);
   const CUtensorMap* wmaps = p.wmap;
@@ -432,16 +578,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 #pragma unroll
     for (int j = 0; j < 16; ++j) old[j] = 0.f;
     rows.live = 0u;
+    if (L.mode == TC_HEAD)
+      for (int m = et; m < 256; m += 128) s_top[m] = top2_empty();  // ordered by the barrier after accf
     if (L.mode == TC_GEMM && p0 < p1) {
       // Nothing loaded here is written before this run's pieces are added:
       // a tile's outputs are written once, by the piece completing its k range.
       const int t = (int)(p0 / nkb);
       seg_built = t / L.tps;
       e = make_epi(p.g, seg_built);
-      int unit = 0;
-      if (tc_unit(L, t, r, unit)) {
-        epi_preload_rows(e, unit, 0, L.M, rows);
-        epi_preload_tile(e, unit, 0, rows, old);
+      if constexpr (Cfg::WIDE) {
+        row_tab_build(e, L.M, et, tab);
+      } else {
+        int unit = 0;
+        if (tc_unit(L, t, r, unit)) {
+          epi_preload_rows(e, unit, 0, L.M, rows);
+          epi_preload_tile(e, unit, 0, rows, old);
+        }
       }
     }
     while (pos < p1) {
@@ -462,7 +614,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       float old_next[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) old_next[j] = 0.f;
-      if (L.mode == TC_GEMM && end < p1) {
+      if (!Cfg::WIDE && L.mode == TC_GEMM && end < p1) {
         const int t2 = (int)(end / nkb);
         const Epi e2 = (t2 / L.tps != seg_built) ? make_epi(p.g, t2 / L.tps) : e;
         int unit2 = 0;
@@ -472,8 +624,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       if (whole) {
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
+          if (Cfg::WIDE && L.mode == TC_GEMM) {
+            float pre[32];
+            int unit = 0;
+            const bool works = tc_unit(L, t, r, unit);
+            wide_loads(e, tab, unit, works, c0, L.M, pre);
+            tc::tmem_ld16(trow + c0, v);
+            final_wide(L, e, tab, t, c0, r, v, xch, pre);
+            continue;
+          }
           tc::tmem_ld16(trow + c0, v);
-          final_chunk(L, e, t, c0, r, et, v, xch, rows, old);
+          final_chunk(L, e, t, c0, r, et, v, xch, rows, old, s_top);
         }
         tc::tc_fence_before();
         tc::named_bar(1, 128);
@@ -508,6 +669,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
           const int last = run_of(tend - 1, L.T, L.G) + t;
           for (int c0 = 0; c0 < ncol; c0 += 16) {
             float v[16];
+            float pre[32];
+            if (Cfg::WIDE && L.mode == TC_GEMM) {  // in flight with the partial loads
+              int unit = 0;
+              const bool works = tc_unit(L, t, r, unit);
+              wide_loads(e, tab, unit, works, c0, L.M, pre);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
             // partial slots in k order; each batch of up to 4 slots is loaded at once
@@ -525,7 +692,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
                 for (int j = 0; j < 16; ++j)
                   if (sb + q <= last) v[j] += pv[q][j];
             }
-            final_chunk(L, e, t, c0, r, et, v, xch, rows, old);
+            if (Cfg::WIDE && L.mode == TC_GEMM)
+              final_wide(L, e, tab, t, c0, r, v, xch, pre);
+            else
+              final_chunk(L, e, t, c0, r, et, v, xch, rows, old, s_top);
           }
         }
         tc::named_bar(1, 128);  // s_flag is rewritten by the next piece
@@ -535,6 +705,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       pos = end;
       ++k;
     }
+    if (L.mode == TC_HEAD && L.topk == 0) {
+      tc::named_bar(1, 128);
+      for (int m = et; m < L.M; m += 128) L.tops[(size_t)blockIdx.x * L.M + m] = s_top[m];
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -542,7 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
-  if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, L.n_tiles, L.tops, &s_last_head);
+  if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, gridDim.x, L.tops, &s_last_head);
 }
 
 // ------------------------------------------------------------------- host
@@ -670,13 +844,15 @@ cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, ui
 // ------------------------------------------------------------- LM head
 
 bool head_tc_supported(const HeadDesc& h) {
-  return h.dtype == DFLASH_BF16 && h.M >= 1 && h.M <= 256 && h.H % 64 == 0 && h.mode != 2 &&
+  return h.dtype == DFLASH_BF16 && h.M >= 1 && h.M <= 256 && h.H % 64 == 0 &&
+         (h.mode != 2 || (h.topk >= 1 && h.topk <= kMaxTopK)) &&
          (reinterpret_cast<uintptr_t>(h.x) & 15) == 0 && (h.V + 127) / 128 <= 8192;
 }
 
-// Per-tile selections of the LM head: triples, or top-k lists.
-size_t head_sel_bytes(const HeadDesc& h, int n_tiles) {
-  const size_t t2 = (size_t)n_tiles * h.M * sizeof(Top2);
+// Selections of the LM head: one triple per (CTA, token row), or the top-k
+// lists of every (tile, token row).
+size_t head_sel_bytes(const HeadDesc& h, int n_tiles, int G) {
+  const size_t t2 = (size_t)G * h.M * sizeof(Top2);  // one selection per CTA
   const size_t tk = (size_t)n_tiles * h.M * (h.topk > 0 ? h.topk : 0) * sizeof(Cand);
   return t2 > tk ? t2 : tk;
 }
@@ -685,7 +861,7 @@ size_t head_tc_workspace(const HeadDesc& h, int num_sms) {
   const int n_tiles = (h.V + 127) / 128;
   const long long T = (long long)n_tiles * (h.H / 64);
   return ((part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(h.M)) + 255) & ~size_t(255)) +
-         head_sel_bytes(h, n_tiles) + 256;
+         head_sel_bytes(h, n_tiles, runs_for(T, num_sms)) + 256;
 }
 
 const void* head_tc_tlist(const HeadDesc& h, int num_sms, int* n_tiles) {
