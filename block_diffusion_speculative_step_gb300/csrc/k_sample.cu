@@ -286,6 +286,98 @@ __device__ void filt_select(const float* l, int V, In in, W weight, unsigned lon
   __syncthreads();
 }
 
+// Top-p inside a top-k set of at most kFiltCompact entries: the k kept
+// entries are gathered into shared memory (one pass over the row), sorted by
+// (key descending, index ascending) as 64-bit words, and the prefix whose
+// integer mass first reaches `need` is found by a block scan.  The row's
+// maximum is the first sorted entry.  The result names the last kept entry
+// exactly (its key and index), so entries that share its logit but fell
+// outside the top-k set stay out.
+constexpr int kFiltCompact = kFiltWarps * 256;  // u64 words of the histogram space
+
+__device__ void filt_top_p_compact(const float* l, int V, const RowFilter& fk, int top_k, float invT, float top_p,
+                                   unsigned long long* cand, RowFilter* s_f) {
+  __shared__ int s_cnt;
+  __shared__ unsigned long long s_part[kFiltThreads / 32];
+  __shared__ unsigned long long s_z;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = l[v];
+    if (filt_kept(&fk, x, v)) {
+      const int slot = atomicAdd(&s_cnt, 1);
+      if (slot < kFiltCompact) cand[slot] = ((unsigned long long)(~okey(x)) << 32) | (uint32_t)v;
+    }
+  }
+  __syncthreads();
+  const int cnt = min(s_cnt, kFiltCompact);  // == top_k
+  int n = 1;
+  while (n < cnt) n <<= 1;
+  for (int i = cnt + threadIdx.x; i < n; i += blockDim.x) cand[i] = ~0ull;
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= n; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long a = cand[i], b = cand[j];
+          const bool up = (i & size) == 0;
+          if ((a > b) == up) {
+            cand[i] = b;
+            cand[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  auto logit_of = [](unsigned long long c) {
+    const uint32_t k = ~(uint32_t)(c >> 32);
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  };
+  const float mx = logit_of(cand[0]);
+  // each thread a contiguous segment of the sorted entries
+  const int E = (cnt + blockDim.x - 1) / blockDim.x;
+  const int b0 = threadIdx.x * E, b1 = min(cnt, b0 + E);
+  unsigned long long mine = 0ull;
+  for (int i = b0; i < b1; ++i) mine += filt_mass(logit_of(cand[i]), mx, invT);
+  // exclusive scan of the segment sums over the block
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long inc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) s_part[warp] = inc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      const unsigned long long x = s_part[w];
+      s_part[w] = t;
+      t += x;
+    }
+    s_z = t;
+  }
+  __syncthreads();
+  const unsigned long long excl = s_part[warp] + inc - mine;
+  unsigned long long need = (unsigned long long)ceil((double)top_p * (double)s_z);
+  if (need < 1ull) need = 1ull;
+  if (excl < need && need <= excl + mine) {
+    unsigned long long acc = excl;
+    for (int i = b0; i < b1; ++i) {
+      acc += filt_mass(logit_of(cand[i]), mx, invT);
+      if (acc >= need) {
+        *s_f = RowFilter{~(uint32_t)(cand[i] >> 32), (int)(uint32_t)cand[i]};
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  (void)top_k;
+}
+
 // Rows [0, rows_a) of logits_a and then the rows of logits_b (two row sets
 // in one launch); one CTA per row.
 __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* logits_a, int rows_a, RowFilter* out_a,
@@ -301,19 +393,10 @@ __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* l
   const int row = in_a ? (int)blockIdx.x : (int)blockIdx.x - rows_a;
   const float* l = (in_a ? logits_a : logits_b) + (size_t)row * V;
   RowFilter* out = in_a ? out_a : out_b;
-  float mx = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    const float x = l[v];
-    if (x == x) mx = fmaxf(mx, x);
-  }
-  mx = warp_max(mx);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
   if (threadIdx.x == 0) s_f = RowFilter{0u, INT_MAX};
   __syncthreads();
-  if (top_k > 0 && top_k < V) {
+  const bool use_k = top_k > 0 && top_k < V, use_p = top_p > 0.f && top_p < 1.f;
+  if (use_k) {
     uint32_t k;
     int i;
     filt_select(l, V, [](float x, int) { return x == x; }, [](float) { return 1ull; }, (unsigned long long)top_k, &k,
@@ -321,7 +404,21 @@ __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* l
     if (threadIdx.x == 0) s_f = RowFilter{k, i};
     __syncthreads();
   }
-  if (top_p > 0.f && top_p < 1.f) {
+  if (use_p && use_k && top_k <= kFiltCompact) {
+    const RowFilter fk = s_f;
+    __syncthreads();
+    filt_top_p_compact(l, V, fk, top_k, invT, top_p, filt_sm, &s_f);
+  } else if (use_p) {
+    float mx = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = l[v];
+      if (x == x) mx = fmaxf(mx, x);
+    }
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
     const RowFilter fk = s_f;
     auto in = [fk](float x, int v) { return filt_kept(&fk, x, v); };
     auto mass = [mx, invT](float x) { return filt_mass(x, mx, invT); };
@@ -341,6 +438,9 @@ __global__ void __launch_bounds__(kFiltThreads) row_filter_kernel(const float* l
     uint32_t k;
     int i;
     filt_select(l, V, in, mass, need, &k, &i, filt_sm);
+    // a boundary group kept whole (i = INT_MAX) holds only its members inside
+    // the top-k set: on the top-k boundary key, cap at the top-k index
+    if (use_k && k == fk.key && i > fk.idx) i = fk.idx;
     if (threadIdx.x == 0) s_f = RowFilter{k, i};
     __syncthreads();
   }

@@ -137,9 +137,11 @@ def test_sampled_cycle_through_the_engine():
     assert torch.equal(eng.base_pos.cpu().long(), base0.cpu().long() + total)
 
 
-@pytest.mark.parametrize("V,T,top_k,top_p", [(1000, 0.8, 50, 1.0), (1000, 0.8, 0, 0.9), (1000, 1.2, 20, 0.7),
-                                             (151936, 1.0, 40, 1.0), (151936, 1.0, 0, 0.6)])
-def test_filtered_sampling_matches_oracle(V, T, top_k, top_p):
+@pytest.mark.parametrize("V,T,top_k,top_p,q", [(1000, 0.8, 50, 1.0, 0), (1000, 0.8, 0, 0.9, 0), (1000, 1.2, 20, 0.7, 0),
+                                               (1000, 1.0, 20, 0.7, 0.125), (1000, 1.0, 0, 0.8, 0.125),
+                                               (151936, 1.0, 40, 1.0, 0), (151936, 1.0, 0, 0.6, 0),
+                                               (151936, 1.0, 50, 0.9, 0)])
+def test_filtered_sampling_matches_oracle(V, T, top_k, top_p, q):
     """Top-k / top-p: with the oracle's kept sets of the same rows, the drafts,
     the draft rows' log-normalisers over their kept entries, the accept
     lengths and the emitted tokens equal the oracle's (sequences meeting a
@@ -147,12 +149,19 @@ def test_filtered_sampling_matches_oracle(V, T, top_k, top_p):
     skipped).  Flat logits (spread 0.5) give every kept entry a share of the
     mass, so a wrong kept set moves the normalisers far beyond the tolerance.
     At the full vocabulary the logits are peaked (spread 3) so that the kept
-    sets stay small and their boundary entries carry measurable mass."""
+    sets stay small and their boundary entries carry measurable mass.  With
+    q > 0 the logits are rounded to multiples of q: large groups of equal
+    logits, so the top-k and top-p boundaries fall inside them and the
+    index order decides (a group kept whole past the top-k index would move
+    the normalisers)."""
     S, B = 3, 6
     g = torch.Generator().manual_seed(V + top_k)
     spread = 0.5 if V <= 1000 else 3.0
     tl = torch.randn(S, B, V, generator=g) * spread
     dl = tl[:, 1:] * 0.6 + torch.randn(S, B - 1, V, generator=g) * 0.8 * spread
+    if q > 0:
+        tl = torch.round(tl / q) * q
+        dl = torch.round(dl / q) * q
     P = [17, 400, 4095]
     ws = _ws()
     compared = 0
