@@ -29,8 +29,12 @@
 // 64 query rows are duplicated into MMA rows 64..127 so that the softmax
 // warps on all four TMEM lane quadrants share the rows, and each rank pushes
 // its partial rows into their owner's shared memory for a local merge (same
-// arithmetic and order as the pulled merge).  DFLASH_ATTN_MMASYNC=1 in the
-// environment selects the mma.sync kernel for head dimension 128 too.
+// arithmetic and order as the pulled merge).  With more (sequence, KV head)
+// items than clusters fit at once, clusters of half the width run them, each
+// CTA taking two of the logical ranks into two TMEM output accumulators; the
+// chunk split and the merge order do not change, nor do the results.
+// DFLASH_ATTN_MMASYNC=1 in the environment selects the mma.sync kernel for
+// head dimension 128 too.
 #include <cooperative_groups.h>
 #include <stdlib.h>
 
@@ -375,33 +379,44 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
 
 // The same merge with the partials pushed instead of pulled: after a
 // cluster barrier (every rank's chunks done, its K/V buffers free), each
-// rank stores its partial rows into their owner's shared memory (recv:
-// [NC][RP][D+4], on the owner, away from psm); after a second barrier each
-// owner merges its rows from local shared memory, with the arithmetic and
-// order of rank_merge, and nothing reads a peer's memory any more.
+// rank stores its partial rows into their owner's shared memory (recv, on
+// the owner, away from psm); after a second barrier each owner merges its
+// rows from local shared memory, with the arithmetic and order of
+// rank_merge, and nothing reads a peer's memory any more.  With E = 2 each
+// CTA holds two logical ranks (rank and rank + NC; partials psm[0], psm[1])
+// and owns the rows of both: the merge runs over the NL = E NC logical ranks
+// in the same order as a cluster of NL CTAs.  recv: [E owned][NL][RP][D+4].
 template <int D>
-__device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* psm, float* recv, int NC, int rank,
-                                           int nq_tile, int qv0, int grp, int g, int s, int rows, int QD, void* out) {
+__device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* psm, float* recv, int NC, int E,
+                                           int rank, int nq_tile, int qv0, int grp, int g, int s, int rows, int QD,
+                                           void* out) {
   constexpr int PST = D + 4;
-  const int RP = (nq_tile + NC - 1) / NC;
-  for (int t = threadIdx.x; t < nq_tile * (PST / 4); t += blockDim.x) {
-    const int qr = t / (PST / 4), c4 = t % (PST / 4);
-    const int dst = qr / RP, i = qr - dst * RP;
-    const float4 v = *reinterpret_cast<const float4*>(psm + (size_t)qr * PST + 4 * c4);
-    float* r = cl.map_shared_rank(recv, dst) + ((size_t)rank * RP + i) * PST;
-    *reinterpret_cast<float4*>(r + 4 * c4) = v;
+  const int NL = NC * E;
+  const int RP = (nq_tile + NL - 1) / NL;
+  for (int e = 0; e < E; ++e) {
+    const float* pe = psm + (size_t)e * kClQT * PST;
+    const int lr = rank + e * NC;  // logical rank of this partial
+    for (int t = threadIdx.x; t < nq_tile * (PST / 4); t += blockDim.x) {
+      const int qr = t / (PST / 4), c4 = t % (PST / 4);
+      const int lo = qr / RP, i = qr - lo * RP;  // logical owner of the row
+      const float4 v = *reinterpret_cast<const float4*>(pe + (size_t)qr * PST + 4 * c4);
+      float* r = cl.map_shared_rank(recv, lo % NC) + (((size_t)(lo / NC) * NL + lr) * RP + i) * PST;
+      *reinterpret_cast<float4*>(r + 4 * c4) = v;
+    }
   }
   cl.sync();
-  const int q_lo = rank * RP;
+  for (int sl = 0; sl < E; ++sl) {
+  const float* rv = recv + (size_t)sl * NL * RP * PST;
+  const int q_lo = (rank + sl * NC) * RP;
   const int nrow = max(0, min(nq_tile, q_lo + RP) - q_lo);
   __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(out);
   for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
     const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
     float M = -INFINITY;
-    for (int r = 0; r < NC; ++r) M = fmaxf(M, recv[((size_t)r * RP + i) * PST + D]);
+    for (int r = 0; r < NL; ++r) M = fmaxf(M, rv[((size_t)r * RP + i) * PST + D]);
     float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int r = 0; r < NC; ++r) {
-      const float* pr = recv + ((size_t)r * RP + i) * PST;
+    for (int r = 0; r < NL; ++r) {
+      const float* pr = rv + ((size_t)r * RP + i) * PST;
       const float mr = pr[D];
       const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
       L = fmaf(pr[D + 1], w, L);
@@ -416,6 +431,7 @@ __device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* p
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
     dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
     dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
+  }
   }
 }
 
@@ -780,8 +796,10 @@ __device__ __forceinline__ uint32_t op_off(int row, int ch) {
   return (uint32_t)((ch >> 3) * (kTcAttnRows * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
-template <int D>
+// E: logical ranks per CTA (1, or 2 on clusters of half the logical width).
+template <int D, int E>
 __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid_constant__ AttnTma p, int n_qt) {
+  static_assert(E == 1 || E == 2, "one or two logical ranks per CTA");
   static_assert(D == 128, "two 64-dim boxes per row");
   constexpr int CH = kMmaCH;
   constexpr int TILE = CH * D * 2;
@@ -807,12 +825,16 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   // [2 chunk parities][8 pieces][64 rows] each
   float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 128);
   float* xsum = xmax + 2 * kTcAttnPieces * 64;
-  float* psm = reinterpret_cast<float*>(sm);   // [64][PST] CTA partial (after the chunk loop)
+  float* psm = reinterpret_cast<float*>(sm);   // [E][64][PST] CTA partials (after the chunk loop)
 
   const AttnDesc& a = p.a;
   cg::cluster_group cl = cg::this_cluster();
   const int NC = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
+  // Logical ranks: NL = E x the cluster width; this CTA runs logical ranks
+  // rank and (E = 2) rank + NC one after the other, each an online softmax
+  // over its own chunks with its own output accumulator.
+  const int NL = E * NC;
   const int g = blockIdx.y / n_qt, qt = blockIdx.y % n_qt;
   const int s = blockIdx.z;
   const int mode = a.mode, rows = a.rows, cap = a.cap, nkv = a.nkv;
@@ -836,7 +858,11 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qv0 = qt * kClQT;
   const int nq_tile = min(kClQT, nqv - qv0);
-  const int nmine = sk.n_ch > rank ? (sk.n_ch - rank + NC - 1) / NC : 0;
+  const int rB = rank + NC;  // second logical rank (E = 2)
+  const int nA = sk.n_ch > rank ? (sk.n_ch - rank + NL - 1) / NL : 0;
+  const int nB = (E > 1 && sk.n_ch > rB) ? (sk.n_ch - rB + NL - 1) / NL : 0;
+  const int nmine = nA + nB;
+  auto chunk_of = [&](int i) { return i < nA ? rank + i * NL : rB + (i - nA) * NL; };
 
   const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
   auto chunk_row = [&](int c, bool& blk) -> int {
@@ -885,14 +911,14 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   const uint32_t tmem = *tslot;
   bool pre0 = false, pre1 = false;
   if (threadIdx.x == 0) {
-    if (nmine > 0 && early_ok(rank)) { issue(rank, 0); pre0 = true; }
-    if (nmine > 1 && early_ok(rank + NC)) { issue(rank + NC, 1); pre1 = true; }
+    if (nmine > 0 && early_ok(chunk_of(0))) { issue(chunk_of(0), 0); pre0 = true; }
+    if (nmine > 1 && early_ok(chunk_of(1))) { issue(chunk_of(1), 1); pre1 = true; }
   }
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    if (nmine > 0 && !pre0) issue(rank, 0);
-    if (nmine > 1 && !pre1) issue(rank + NC, 1);
+    if (nmine > 0 && !pre0) issue(chunk_of(0), 0);
+    if (nmine > 1 && !pre1) issue(chunk_of(1), 1);
   }
   // ---- Q: the tile's query vectors in rows 0..63 and again in rows 64..127
   // (TMEM lanes 64..127 then hold a copy of every score row, so the softmax
@@ -941,7 +967,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
           *abort = 1;
           break;
         }
-        issue(rank + i * NC, i & 1);
+        issue(chunk_of(i), i & 1);
       }
     }
   } else if (warp == 1) {
@@ -983,15 +1009,17 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         if (!wait(&pdone[i & 1], (uint32_t)(i >> 1) & 1u)) break;
         tc::tc_fence_after();
         const uint32_t vb = kvb + (2 * (i & 1) + 1) * TILE;
+        const int li = i < nA ? i : i - nA;                          // chunk within its logical rank
+        const uint32_t od = tmem + (uint32_t)((i < nA ? 2 : 3) * CH);  // that rank's output accumulator
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const uint32_t pb = half ? plb : phb;
 #pragma unroll
           for (int j = 0; j < CH / 16; ++j) {
             const uint32_t poff = (uint32_t)((j >> 2) * (kTcAttnRows * 128) + (j & 3) * 32);
-            tc::mma_bf16(tmem + 2u * CH, tc::sdesc_sw128(pb + poff),
+            tc::mma_bf16(od, tc::sdesc_sw128(pb + poff),
                          tc::sdesc_sw128_mn(vb + (uint32_t)j * 2048u, CH * 128, 1024), idV,
-                         (i > 0 || half > 0 || j > 0) ? 1u : 0u);
+                         (li > 0 || half > 0 || j > 0) ? 1u : 0u);
           }
         }
         tc::mma_commit(&empty[i & 1]);
@@ -1013,9 +1041,17 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     const int row_tok = (qv0 + qr) / grp;
     const float scale = rsqrtf((float)D) * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
+    float mA = -INFINITY, lA = 0.f;  // the first logical rank's state once the second starts
     bool ok = true;
     for (int i = 0; i < nmine; ++i) {
-      const int c = rank + i * NC, b = i & 1;
+      const int c = chunk_of(i), b = i & 1;
+      const int li = i < nA ? i : i - nA;
+      if (i == nA) {  // the second logical rank starts from scratch
+        mA = m_run;
+        lA = l_run;
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
       float* xm = xmax + b * (kTcAttnPieces * 64);
       float* xs = xsum + b * (kTcAttnPieces * 64);
       bool blk;
@@ -1100,13 +1136,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // have completed: waited above): rescale this thread's OC columns to the
       // new maximum.  TMEM accesses are warp-collective: the whole warp takes
       // the branch when any of its rows needs it (alpha = 1 keeps a row).
-      if (o_owner && i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (o_owner && li > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         __syncwarp();
         tc::tc_fence_after();
 #pragma unroll
         for (int q = 0; q < OC / 16; ++q) {
           float o16[16];
-          const uint32_t col = (uint32_t)(2 * CH + OC * kg + 16 * q);
+          const uint32_t col = (uint32_t)((i < nA ? 2 : 3) * CH + OC * kg + 16 * q);
           tc::tmem_ld16(lane_base + col, o16);
 #pragma unroll
           for (int t = 0; t < 16; ++t) o16[t] *= alpha;
@@ -1128,28 +1164,39 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         ok = false;
       }
     }
+    float mB = -INFINITY, lB = 0.f;
+    if (nB > 0) {
+      mB = m_run;
+      lB = l_run;
+    } else {
+      mA = m_run;
+      lA = l_run;
+    }
     // psm overlays the K/V buffers: every MMA (the last P V) has completed here
     tc::named_bar(2, kTcAttnSoft);
     if (o_owner) {
       __syncwarp();
       tc::tc_fence_after();
-      float* pr = psm + (size_t)qr * PST;
+      for (int e = 0; e < E; ++e) {
+        float* pr = psm + ((size_t)e * kClQT + qr) * PST;
+        const bool any = (e == 0 ? nA : nB) > 0;  // uniform over the CTA
 #pragma unroll
-      for (int q = 0; q < OC / 16; ++q) {
-        float o16[16];
-        if (nmine > 0) {
-          tc::tmem_ld16(lane_base + (uint32_t)(2 * CH + OC * kg + 16 * q), o16);
-        } else {
+        for (int q = 0; q < OC / 16; ++q) {
+          float o16[16];
+          if (any) {
+            tc::tmem_ld16(lane_base + (uint32_t)((2 + e) * CH + OC * kg + 16 * q), o16);
+          } else {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) o16[t] = 0.f;
+            for (int t = 0; t < 16; ++t) o16[t] = 0.f;
+          }
+#pragma unroll
+          for (int t = 0; t < 16; t += 4)
+            *reinterpret_cast<float4*>(pr + OC * kg + 16 * q + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
         }
-#pragma unroll
-        for (int t = 0; t < 16; t += 4)
-          *reinterpret_cast<float4*>(pr + OC * kg + 16 * q + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
-      }
-      if (kg == 0) {
-        pr[D] = m_run;
-        pr[D + 1] = l_run;
+        if (kg == 0) {
+          pr[D] = e == 0 ? mA : mB;
+          pr[D + 1] = e == 0 ? lA : lB;
+        }
       }
     }
   }
@@ -1160,7 +1207,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     tc::tmem_dealloc(tmem, 512);
   }
   cl.sync();  // every rank's chunks are done: its K/V buffers may receive
-  push_merge<D>(cl, psm, reinterpret_cast<float*>(sm + 2 * TILE), NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
+  // recv follows the E partials (E = 2: 67.6 KB + 76 KB, inside the K/V, Q and P space)
+  push_merge<D>(cl, psm, psm + (size_t)E * kClQT * PST, NC, E, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
 }
 
 // ------------------------------------------------------------------- host
@@ -1266,24 +1314,38 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 
-// The tcgen05 variant: the cluster width comes from the same residency
-// query (both kernels hold one CTA per SM), so it too depends on the KV-head
-// count and the device only.
-template <int D>
-cudaError_t launch_tc(const AttnDesc& a, int n_qt, cudaStream_t st) {
-  auto k = attn_tc_kernel<D>;
+// The tcgen05 variant: the number of logical ranks comes from the same
+// residency query (both kernels hold one CTA per SM), so it too depends on
+// the KV-head count and the device only.  When there are more (sequence, KV
+// head, query tile) items than clusters of that width fit at once, the
+// items run on clusters of half the width, each CTA taking two logical
+// ranks: the chunk split and the merge order are those of the full width,
+// so every output is the same bit for bit, and the narrower clusters pack
+// the GPCs more fully.
+template <int D, int E>
+cudaError_t launch_tc_e(const AttnTma& p, int nc, int n_qt, cudaStream_t st) {
+  auto k = attn_tc_kernel<D, E>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_attn_smem(D));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  AttnTma p;
-  if (!attn_maps<D>(a, p)) return cudaErrorInvalidValue;
-  const int nc = pick_nc<D>((long)a.nkv);
+  const AttnDesc& a = p.a;
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
   cfg.blockDim = dim3(kTcAttnThreads, 1, 1);
   cfg.dynamicSmemBytes = tc_attn_smem(D);
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
+}
+
+template <int D>
+cudaError_t launch_tc(const AttnDesc& a, int n_qt, cudaStream_t st) {
+  AttnTma p;
+  if (!attn_maps<D>(a, p)) return cudaErrorInvalidValue;
+  const int nl = pick_nc<D>((long)a.nkv);
+  const long items = (long)a.nkv * n_qt * a.n_seqs;
+  if (nl % 2 == 0 && items > clusters_resident<D>(nl) && clusters_resident<D>(nl / 2) > clusters_resident<D>(nl))
+    return launch_tc_e<D, 2>(p, nl / 2, n_qt, st);
+  return launch_tc_e<D, 1>(p, nl, n_qt, st);
 }
 
 }  // namespace
