@@ -1311,6 +1311,7 @@ cudaError_t launch_cluster(const AttnDesc& a, int n_qt, cudaStream_t st) {
   const int nc = pick_nc<D>((long)a.nkv);
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
+  trace_kernel();
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 
@@ -1334,6 +1335,7 @@ cudaError_t launch_tc_e(const AttnTma& p, int nc, int n_qt, cudaStream_t st) {
   cudaLaunchConfig_t cfg = cluster_cfg<D>(nc, dim3(nc, a.nkv * n_qt, a.n_seqs), st, at);
   cfg.blockDim = dim3(kTcAttnThreads, 1, 1);
   cfg.dynamicSmemBytes = tc_attn_smem(D);
+  trace_kernel();
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 

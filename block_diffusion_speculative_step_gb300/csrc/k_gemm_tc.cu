@@ -52,6 +52,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   long long T;    // n_tiles * nkb
   int G;          // CTAs (runs)
   int M;          // token rows
+  int defer;      // GEMM, BN >= 128: split tiles are finished by tc_fixup_kernel, not by their last piece
   float* part;    // partial slots [n_tiles + G][BN][128]
   Top2* tops;     // LM head: per-CTA triples [G][M]
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
@@ -93,7 +94,7 @@ __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort
 // Launch scalars held in registers: the inline-asm memory clobbers of the
 // pipeline would otherwise force every use to re-read the parameter block.
 struct TcLocal {
-  int mode, M, tps, nkb, G, n_tiles, kind, d, inter, row0;
+  int mode, M, tps, nkb, G, n_tiles, kind, d, inter, row0, defer;
   long long T;
   int V, hmode, hblock, topk;
   float* logits;
@@ -108,6 +109,7 @@ __device__ __forceinline__ TcLocal tc_local(const TcParams& p) {
   TcLocal L;
   L.mode = p.mode;
   L.M = p.M;
+  L.defer = p.defer;
   L.tps = p.tiles_per_seg;
   L.nkb = p.nkb;
   L.G = p.G;
@@ -654,6 +656,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         // (and the barrier after it) orders the fixup's loads after the
         // other pieces' stores.
         tc::named_bar(1, 128);
+        if (Cfg::WIDE && L.defer) {  // finished by tc_fixup_kernel once the grid has completed
+          if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
+          pos = end;
+          ++k;
+          continue;
+        }
         if (et == 0) {
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
           uint32_t* ctr = L.counters + kCtrGemm + t;
@@ -719,6 +727,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, gridDim.x, L.tops, &s_last_head);
 }
 
+// Split tiles of a deferred launch (BN >= 128), once the GEMM grid has
+// completed: one CTA of 128 threads per (tile, 16-column chunk); thread r
+// sums accumulator row r's partial slots in k order and runs the chunk's
+// epilogue -- the arithmetic and order of a last piece finishing its tile
+// inline, spread over every SM instead of one CTA per tile.
+template <int BN>
+__global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ TcParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ RowTab s_tab;
+  __shared__ float s_xch[16 * 128];
+  const TcLocal L = tc_local(p);
+  const int nkb = L.nkb;
+  const int nch = min(BN, ((L.M + 15) / 16) * 16) / 16;
+  const int t = (int)(blockIdx.x / nch), c0 = (int)(blockIdx.x % nch) * 16;
+  const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
+  const int first = run_of(tbeg, L.T, L.G) + t, last = run_of(tend - 1, L.T, L.G) + t;
+  if (first == last) return;  // one run covers the tile: finished inline (uniform over the CTA)
+  const int r = threadIdx.x, lane = r & 31;
+  // the partial slots first: they depend on nothing below
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+  const Epi e = make_epi(p.g, t / L.tps);
+  // row operands of the 32-row word holding the chunk (warp 0)
+  if (r < 32) {
+    const int m = (c0 & ~31) + lane;
+    const bool lv = m < L.M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+    const uint32_t bits = __ballot_sync(0xffffffffu, lv);
+    if (lane == 0) s_tab.live[c0 >> 5] = bits;
+    int pos = -1;
+    uint32_t kvr = ~0u;
+    if (e.kind == EPI_QKV && lv) {
+      const int q = __ldg(e.base_pos + m / e.rows) + m % e.rows;
+      if (q >= 0 && q < e.rope_max_pos) {
+        pos = q;
+        const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? q % e.kv_window : q) : m % e.rows;
+        if (slot < e.kv_cap) kvr = (uint32_t)((m / e.rows) * e.nkv) * (uint32_t)e.kv_cap + (uint32_t)slot;
+      }
+    }
+    s_tab.pos[m] = pos;
+    s_tab.kvr[m] = kvr;
+  }
+  __syncthreads();
+  float pre[32];
+  int unit = 0;
+  const bool works = tc_unit(L, t, r, unit);
+  wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
+  for (int sb = first; sb <= last; sb += 4) {
+    float pv[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float* src = L.part + (size_t)(sb + q) * BN * 128 + (size_t)c0 * 128 + r;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (sb + q <= last) v[j] += pv[q][j];
+  }
+  final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
+}
+
 // ------------------------------------------------------------------- host
 
 namespace {
@@ -746,7 +819,13 @@ cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
   auto k = tc_stream_kernel<BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(p.G), dim3(kTcThreads), TcCfg<BN>::SMEM, st, p);
+  e = launch_pdl(k, dim3(p.G), dim3(kTcThreads), TcCfg<BN>::SMEM, st, p);
+  if (e != cudaSuccess || !p.defer) return e;
+  if constexpr (BN >= 128) {
+    const int nch = (p.M < BN ? (p.M + 15) / 16 * 16 : BN) / 16;
+    return launch_pdl(tc_fixup_kernel<BN>, dim3(p.n_tiles * nch), dim3(128), 0, st, p);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
@@ -833,6 +912,7 @@ cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, ui
   p.part = static_cast<float*>(ws);
   p.counters = counters;
   p.status = status;
+  p.defer = pick_bn(g.M) >= 128 ? 1 : 0;
   const uint64_t wrows = g.kind == EPI_SWIGLU ? (uint64_t)2 * g.inter : (uint64_t)(g.seg_row0 + g.seg_rows);
   const uint32_t box_rows = g.kind == EPI_SWIGLU ? 64 : 128;
   for (int s = 0; s < g.nseg; ++s)

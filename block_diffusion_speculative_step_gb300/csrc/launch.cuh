@@ -10,6 +10,8 @@
 
 #include <utility>
 
+#include "trace.h"
+
 namespace dfl {
 
 template <typename... KArgs, typename... Args>
@@ -25,6 +27,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  trace_kernel();
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

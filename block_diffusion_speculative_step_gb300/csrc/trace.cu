@@ -14,6 +14,7 @@ namespace dfl {
 namespace {
 struct Rec {
   int family;
+  int kernels;  // kernels the traced call launched
   double bytes;
   cudaEvent_t a, b;
 };
@@ -24,6 +25,8 @@ struct TraceState {
   std::vector<Rec> recs;
   int open_family = -1;
   cudaEvent_t open_a = nullptr;
+  long long kernels = 0;  // kernel launches on this host thread
+  long long open_k = 0;
 };
 thread_local TraceState g_trace;
 
@@ -48,14 +51,18 @@ void trace_pre(cudaStream_t st, int family) {
   if (record(a, st) == cudaSuccess) {
     t.open_family = family;
     t.open_a = a;
+    t.open_k = t.kernels;
   }
 }
+
+void trace_kernel() { ++g_trace.kernels; }
 
 void trace_post(cudaStream_t st, double bytes) {
   TraceState& t = g_trace;
   if (!t.on || t.open_a == nullptr) return;
   cudaEvent_t b = t.pool[2 * t.recs.size() + 1];
-  if (record(b, st) == cudaSuccess) t.recs.push_back(Rec{t.open_family, bytes, t.open_a, b});
+  if (record(b, st) == cudaSuccess)
+    t.recs.push_back(Rec{t.open_family, (int)(t.kernels - t.open_k), bytes, t.open_a, b});
   t.open_a = nullptr;
 }
 
@@ -98,7 +105,7 @@ int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats) {
       return DFLASH_ERR_CUDA;
     }
     dflash_trace_stat& s = stats[r.family];
-    s.launches += 1;
+    s.launches += r.kernels;
     s.total_ms += ms;
     s.bytes += r.bytes;
   }

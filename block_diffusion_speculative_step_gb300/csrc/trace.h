@@ -23,5 +23,7 @@ enum TraceFamily : int {
 
 void trace_pre(cudaStream_t st, int family);
 void trace_post(cudaStream_t st, double bytes);
+// Called at every kernel launch: a traced call counts the kernels it launched.
+void trace_kernel();
 
 }  // namespace dfl

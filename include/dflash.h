@@ -456,12 +456,14 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
 
 /*
  * Kernel tracing (off by default; state is per host thread).  Between
- * dflash_trace_begin and dflash_trace_pause every kernel the library
- * launches is bracketed by two CUDA events recorded on its stream (event
- * records are captured into CUDA graphs as well).  dflash_trace_read, called
- * after the traced work (or graph replay) has completed, sums the event
- * durations per kernel family into stats[0 .. DFLASH_TRACE_FAMILIES-1] and
- * returns the number of families.  `bytes` is the algorithmic DRAM traffic
+ * dflash_trace_begin and dflash_trace_pause every launch step of the library
+ * (one or a few kernels of one family: a projection over several token-row
+ * tiles, a GEMM and its split-K fixup) is bracketed by two CUDA events
+ * recorded on its stream (event records are captured into CUDA graphs as
+ * well).  dflash_trace_read, called after the traced work (or graph replay)
+ * has completed, sums the event durations per kernel family into
+ * stats[0 .. DFLASH_TRACE_FAMILIES-1] and returns the number of families;
+ * `launches` counts the kernels launched.  `bytes` is the algorithmic DRAM traffic
  * the library attributes to the launches (weights + activations read and
  * written, each once), where it is known on the host; 0 otherwise.
  */
@@ -475,8 +477,8 @@ typedef struct {
 int dflash_trace_begin(int32_t max_launches);
 int dflash_trace_pause(void);
 int dflash_trace_read(dflash_trace_stat* stats, int32_t n_stats);
-/* Per-launch durations of the traced work in launch order: ms[i], family[i]
- * for i < min(n, count); returns count (the number of traced launches). */
+/* Per-step durations of the traced work in launch order: ms[i], family[i]
+ * for i < min(n, count); returns count (the number of traced steps). */
 int dflash_trace_launches(float* ms, int32_t* family, int32_t n);
 int dflash_trace_end(void);
 
