@@ -21,7 +21,10 @@
 //
 // Tiles of more than 16 token rows finish in 16-column chunks; their
 // column-independent row operands are staged once per CTA in shared memory
-// (RowTab), so a chunk costs one global round trip.  The LM head keeps, per
+// (RowTab), so a chunk costs one global round trip.  From 128 token rows on,
+// the pieces of a split tile only store their partials and tc_fixup_kernel,
+// launched behind the GEMM, finishes every split tile with one CTA per
+// 16-column chunk (same k-order sum, same epilogue).  The LM head keeps, per
 // CTA, each token row's best (logit, index) and runner-up over the tiles the
 // CTA finishes; the last CTA merges one triple per CTA.
 #include <cudaTypedefs.h>
