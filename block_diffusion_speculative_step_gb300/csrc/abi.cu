@@ -141,7 +141,7 @@ GemmDesc gemm_base(int dtype, int M, int K, const void* X, const int32_t* base_p
 // ----------------------------------------------------------- decoder layer
 
 struct LayerScratch {
-  void *x, *q, *kb, *vb, *attn, *act;
+  void *x, *x2, *q, *kb, *vb, *attn, *act;  // x: attention input, x2: MLP input (the same buffer by default)
   float* apart;
   void* gpart;
   size_t gpart_bytes;
@@ -216,6 +216,7 @@ void carve_layer(Bump& b, const LayerShape& L, int sms, LayerScratch& s, int con
   const size_t M = (size_t)L.S * L.rows;
   const size_t QD = (size_t)d.n_q_heads * d.head_dim;
   s.x = b.take(M * d.hidden * es);
+  s.x2 = s.x;
   s.q = b.take(M * QD * es);
   s.kb = b.take((size_t)L.S * d.n_kv_heads * L.rows * d.head_dim * es);
   s.vb = b.take((size_t)L.S * d.n_kv_heads * L.rows * d.head_dim * es);
@@ -373,10 +374,10 @@ int run_layer(const LayerShape& L, const dflash_layer_weights& w, const dflash_k
   DF_CUDA(run_gemm(o, s.gpart, s.gpart_bytes, c, sms, st));
   if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 1, s.yc, h, 1, s, st));
 
-  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x, st));
-  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 2, s.x, s.xc, 0, s, st));
+  DF_LAUNCH(st, TF_RMSNORM, 0, launch_rmsnorm(d.dtype, h, w.ln2, M, H, d.rms_eps, s.x2, st));
+  if (cv) DF_LAUNCH(st, TF_CONV, conv_bytes(L, *cv), layer_conv(L, *cv, 2, s.x2, s.xc, 0, s, st));
   GemmDesc& gu = g4[2];
-  gu.X = cv ? s.xc : s.x;
+  gu.X = cv ? s.xc : s.x2;
   gu.act_out = s.act;
   DF_CUDA(run_gemm(gu, s.gpart, s.gpart_bytes, c, sms, st));
 
@@ -542,9 +543,30 @@ int run_head(const HeadDesc& h, int sms, cudaStream_t st) {
 
 }  // namespace
 
+static int check_verify_shape(const dflash_verify_args* a, const char* who) {
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  DF_CHECK(a->n_seqs > 0 && a->block >= 1, "%s: n_seqs > 0 and block >= 1 required", who);
+  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
+  return DFLASH_OK;
+}
+
+
 namespace dfl {
 // Sets the thread-local error text from another translation unit.
 int abi_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// Every host-side check of dflash_verify_accept (shapes, then pointers).
+int verify_check(const dflash_verify_args* a, const char* who) {
+  int rc = check_verify_shape(a, who);
+  if (rc) return rc;
+  DF_CHECK(a->h && a->final_norm && a->lm_head && a->argmax && a->accept_len && a->out_tokens,
+           "%s: NULL pointer", who);
+  DF_CHECK(a->drafts || a->block == 1, "%s: drafts required when block > 1", who);
+  DF_CHECK(!a->commit_base || a->base_pos, "%s: commit_base needs base_pos", who);
+  return DFLASH_OK;
+}
 }  // namespace dfl
 
 // =================================================================== ABI
@@ -571,6 +593,19 @@ int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream) {
   return DFLASH_OK;
 }
 
+int dflash_workspace_control(void* ws, size_t ws_bytes, uint64_t wait_limit_ns, int32_t stall_kv_loads,
+                             dflash_stream_t stream) {
+  DF_CHECK(ws != nullptr && ws_bytes >= kReservedBytes, "dflash_workspace_control: workspace below %zu bytes",
+           kReservedBytes);
+  DF_CHECK((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "dflash_workspace_control: workspace must be 256-byte aligned");
+  // bytes 8..15: the wait limit, 16..19: the stall switch (see wait_limit_ns)
+  uint32_t ctl[4] = {(uint32_t)(wait_limit_ns & 0xffffffffu), (uint32_t)(wait_limit_ns >> 32),
+                     stall_kv_loads ? 1u : 0u, 0u};
+  DF_CUDA(cudaMemcpyAsync(static_cast<char*>(ws) + 8, ctl, sizeof(ctl), cudaMemcpyHostToDevice,
+                          (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
 int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status) {
   DF_CHECK(ws != nullptr && host_status != nullptr, "dflash_read_status: NULL argument");
   uint32_t v = 0;
@@ -589,12 +624,18 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status) {
 
 // ----------------------------------------------------------------- embed
 
+static int check_embed_shape(const dflash_embed_args* a, const char* who) {
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  DF_CHECK(a->n_seqs >= 0 && a->rows > 0, "%s: bad n_seqs/rows", who);
+  return DFLASH_OK;
+}
+
 int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DF_CHECK(a != nullptr, "dflash_embed: NULL args");
-  int rc = check_dims(a->dims, "dflash_embed");
+  int rc = check_embed_shape(a, "dflash_embed");
   if (rc) return rc;
   DF_CHECK(a->embed && a->first && a->h, "dflash_embed: NULL embed/first/h");
-  DF_CHECK(a->n_seqs >= 0 && a->rows > 0, "dflash_embed: bad n_seqs/rows");
   DF_CHECK(a->rest != nullptr || (a->fill_token >= 0 && a->fill_token < a->dims.vocab),
            "dflash_embed: fill_token out of range");
   rc = check_ws(ws, ws_bytes, kReservedBytes, "dflash_embed");
@@ -627,22 +668,31 @@ static size_t layer_ws(const dflash_layer_args* a, int sms) {
   return b.off;
 }
 
+static int check_layer_args_shape(const dflash_layer_args* a, const char* who) {
+  DF_CHECK(a != nullptr, "%s: NULL args", who);
+  int rc = check_dims(a->dims, who);
+  if (rc) return rc;
+  rc = check_kv_pages(a->kv, who);
+  if (rc) return rc;
+  return check_layer_shape(layer_shape_of(a), who);
+}
+
 int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws_bytes,
                                  dflash_stream_t stream) {
   const char* who = "dflash_decoder_layer_forward";
-  DF_CHECK(a != nullptr, "%s: NULL args", who);
-  int rc = check_dims(a->dims, who);
+  int rc = check_layer_args_shape(a, who);
   if (rc) return rc;
   rc = check_weights(a->w, who);
   if (rc) return rc;
   DF_CHECK(a->base_pos && a->h && a->kv.k && a->kv.v && a->rope_cs, "%s: NULL pointer", who);
-  rc = check_kv_pages(a->kv, who);
-  if (rc) return rc;
   LayerShape L = layer_shape_of(a);
-  rc = check_layer_shape(L, who);
-  if (rc) return rc;
   DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos %d beyond the RoPE table (%d)", who, a->max_pos,
            a->rope_max_pos);
+  {
+    const void* st[] = {a->out_x_attn, a->out_q, a->out_kb, a->out_vb, a->out_attn, a->out_x_mlp, a->out_act};
+    for (const void* p : st)
+      DF_CHECK((reinterpret_cast<uintptr_t>(p) & 15) == 0, "%s: stage outputs must be 16-byte aligned", who);
+  }
   DF_CHECK(!a->tap || (a->tap_stride >= a->dims.hidden && a->tap_offset >= 0 &&
                         a->tap_offset + a->dims.hidden <= a->tap_stride),
            "%s: bad tap stride/offset", who);
@@ -653,6 +703,14 @@ int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws
   b.take(kReservedBytes);
   LayerScratch s;
   carve_layer(b, L, sms, s);
+  // stage outputs replace the scratch they would have occupied
+  if (a->out_x_attn) s.x = a->out_x_attn;
+  if (a->out_x_mlp) s.x2 = a->out_x_mlp;
+  if (a->out_q) s.q = a->out_q;
+  if (a->out_kb && L.mode == DFLASH_ATTN_BLOCK_BIDIR) s.kb = a->out_kb;
+  if (a->out_vb && L.mode == DFLASH_ATTN_BLOCK_BIDIR) s.vb = a->out_vb;
+  if (a->out_attn) s.attn = a->out_attn;
+  if (a->out_act) s.act = a->out_act;
   return run_layer(L, a->w, a->kv, a->h, a->base_pos, a->rope_cs, a->rope_max_pos, a->tap, a->tap_stride, a->tap_offset, s,
                    header(ws), sms, (cudaStream_t)stream);
 }
@@ -692,16 +750,13 @@ static size_t fuse_ws(const dflash_fuse_args* a, int sms, float** z, void** cbuf
   return b.off;
 }
 
-int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  const char* who = "dflash_fuse_context";
+static int check_fuse_shape(const dflash_fuse_args* a, const char* who) {
   DF_CHECK(a != nullptr, "%s: NULL args", who);
   int rc = check_dims(a->dims, who);
   if (rc) return rc;
-  const dflash_dims& d = a->dims;
   DF_CHECK(a->n_taps > 0 && a->n_taps <= 16, "%s: n_taps must be in [1, 16]", who);
   DF_CHECK(a->n_layers > 0 && a->n_layers <= DFLASH_MAX_LAYERS, "%s: n_layers must be in [1, %d]", who,
            DFLASH_MAX_LAYERS);
-  DF_CHECK(a->w_fc && a->fc_norm && a->feats && a->base_pos && a->rope_cs, "%s: NULL pointer", who);
   DF_CHECK(a->n_seqs > 0 && a->rows > 0, "%s: n_seqs and rows must be positive", who);
   const int cap = a->kv_layers[0].capacity, win = a->kv_layers[0].window;
   for (int j = 0; j < a->n_layers; ++j) {
@@ -712,13 +767,22 @@ int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, df
                  a->kv_layers[j].max_pages == a->kv_layers[0].max_pages &&
                  a->kv_layers[j].pool_pages == a->kv_layers[0].pool_pages,
              "%s: every layer's context cache must share its paging geometry", who);
-  }
-  for (int j = 0; j < a->n_layers; ++j) {
-    DF_CHECK(a->w_qkv_layers[j] && a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL layer %d pointer", who, j);
     DF_CHECK(a->kv_layers[j].capacity == cap && a->kv_layers[j].window == win,
              "%s: every layer's context cache must share capacity and window", who);
   }
   DF_CHECK(cap > 0 && (win == 0 || win == cap), "%s: window ring needs capacity == window", who);
+  return DFLASH_OK;
+}
+
+int dflash_fuse_context(const dflash_fuse_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_fuse_context";
+  int rc = check_fuse_shape(a, who);
+  if (rc) return rc;
+  const dflash_dims& d = a->dims;
+  DF_CHECK(a->w_fc && a->fc_norm && a->feats && a->base_pos && a->rope_cs, "%s: NULL pointer", who);
+  for (int j = 0; j < a->n_layers; ++j)
+    DF_CHECK(a->w_qkv_layers[j] && a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL layer %d pointer", who, j);
+  const int cap = a->kv_layers[0].capacity, win = a->kv_layers[0].window;
   const int sms = num_sms();
   float* z;
   void *cbuf, *gpart;
@@ -836,8 +900,7 @@ static int draft_round(const dflash_draft_args* a, const DraftScratch& s, const 
   return DFLASH_OK;
 }
 
-int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  const char* who = "dflash_draft_block";
+static int check_draft_shape(const dflash_draft_args* a, const char* who) {
   DF_CHECK(a != nullptr, "%s: NULL args", who);
   int rc = check_dims(a->dims, who);
   if (rc) return rc;
@@ -846,10 +909,7 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
            DFLASH_MAX_LAYERS);
   DF_CHECK(a->block >= 2 && a->n_seqs > 0, "%s: block >= 2 and n_seqs > 0 required", who);
   DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
-  DF_CHECK(a->final_norm && a->embed && a->lm_head && a->anchor && a->base_pos && a->drafts && a->rope_cs,
-           "%s: NULL pointer", who);
   DF_CHECK(a->mask_token >= 0 && a->mask_token < d.vocab, "%s: mask_token out of range", who);
-  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
   DF_CHECK(a->path_topk >= 0 && a->path_topk <= 16, "%s: path_topk must be in [0, 16]", who);
   DF_CHECK(a->path_temperature >= 0.f && a->path_temperature == a->path_temperature,
            "%s: path_temperature must be >= 0", who);
@@ -860,21 +920,33 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   if (a->conv_rank > 0)
     DF_CHECK(a->conv_rank % 8 == 0 && d.hidden % 8 == 0, "%s: convolutions need conv_rank %% 8 == 0 and hidden %% 8 == 0",
              who);
-  for (int j = 0; a->conv_rank > 0 && j < a->n_layers; ++j)
-    DF_CHECK(a->conv_w1[j] && a->conv_w2[j], "%s: NULL convolution weights of layer %d", who, j);
-  if (a->path_topk > 0) {
-    DF_CHECK(a->path_u && a->path_v && a->path_rank > 0 && a->path_rank <= 256,
-             "%s: path selector needs path_u, path_v and 0 < path_rank <= 256", who);
-    DF_CHECK(d.hidden % 8 == 0, "%s: the path selector needs hidden %% 8 == 0", who);
-  }
+  if (a->path_topk > 0)
+    DF_CHECK(a->path_rank > 0 && a->path_rank <= 256 && d.hidden % 8 == 0,
+             "%s: the path selector needs 0 < path_rank <= 256 and hidden %% 8 == 0", who);
   for (int j = 0; j < a->n_layers; ++j) {
-    rc = check_weights(a->layers[j], who);
-    if (rc) return rc;
-    DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
     rc = check_kv_pages(a->kv_layers[j], who);
     if (rc) return rc;
     rc = check_layer_shape(draft_layer_shape(a, j), who);
     if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_draft_block";
+  int rc = check_draft_shape(a, who);
+  if (rc) return rc;
+  const dflash_dims& d = a->dims;
+  DF_CHECK(a->final_norm && a->embed && a->lm_head && a->anchor && a->base_pos && a->drafts && a->rope_cs,
+           "%s: NULL pointer", who);
+  DF_CHECK(a->max_pos <= a->rope_max_pos, "%s: max_pos beyond the RoPE table", who);
+  for (int j = 0; a->conv_rank > 0 && j < a->n_layers; ++j)
+    DF_CHECK(a->conv_w1[j] && a->conv_w2[j], "%s: NULL convolution weights of layer %d", who, j);
+  if (a->path_topk > 0) DF_CHECK(a->path_u && a->path_v, "%s: path selector needs path_u and path_v", who);
+  for (int j = 0; j < a->n_layers; ++j) {
+    rc = check_weights(a->layers[j], who);
+    if (rc) return rc;
+    DF_CHECK(a->kv_layers[j].k && a->kv_layers[j].v, "%s: NULL context cache %d", who, j);
   }
   const int sms = num_sms();
   DraftScratch s;
@@ -914,15 +986,8 @@ static size_t verify_ws(const dflash_verify_args* a, int sms, void** xf, void** 
 
 int dflash_verify_accept(const dflash_verify_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
   const char* who = "dflash_verify_accept";
-  DF_CHECK(a != nullptr, "%s: NULL args", who);
-  int rc = check_dims(a->dims, who);
+  int rc = dfl::verify_check(a, who);
   if (rc) return rc;
-  DF_CHECK(a->n_seqs > 0 && a->block >= 1, "%s: n_seqs > 0 and block >= 1 required", who);
-  DF_CHECK((long)a->n_seqs * a->block <= 1024, "%s: n_seqs*block must be <= 1024", who);
-  DF_CHECK(a->h && a->final_norm && a->lm_head && a->argmax && a->accept_len && a->out_tokens,
-           "%s: NULL pointer", who);
-  DF_CHECK(a->drafts || a->block == 1, "%s: drafts required when block > 1", who);
-  DF_CHECK(!a->commit_base || a->base_pos, "%s: commit_base needs base_pos", who);
   const int sms = num_sms();
   void *xf, *hpart;
   rc = check_ws(ws, ws_bytes, verify_ws(a, sms, &xf, &hpart, nullptr), who);
@@ -960,15 +1025,21 @@ static size_t path_ws(const dflash_path_args* a) {
   return kReservedBytes + path_proj_floats(a->n_seqs, a->block, a->topk, a->rank) * sizeof(float);
 }
 
-int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  const char* who = "dflash_path_select";
+static int check_path_shape(const dflash_path_args* a, const char* who) {
   DF_CHECK(a != nullptr, "%s: NULL args", who);
   int rc = check_dims(a->dims, who);
   if (rc) return rc;
-  DF_CHECK(a->embed && a->path_u && a->path_v && a->anchor && a->cand && a->path, "%s: NULL pointer", who);
   DF_CHECK(a->n_seqs > 0 && a->block >= 2 && a->topk > 0 && a->topk <= 16 && a->rank > 0 && a->rank <= 256,
            "%s: need n_seqs > 0, block >= 2, 0 < topk <= 16, 0 < rank <= 256", who);
   DF_CHECK(a->dims.hidden % 8 == 0, "%s: hidden %% 8 == 0 required", who);
+  return DFLASH_OK;
+}
+
+int dflash_path_select(const dflash_path_args* a, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  const char* who = "dflash_path_select";
+  int rc = check_path_shape(a, who);
+  if (rc) return rc;
+  DF_CHECK(a->embed && a->path_u && a->path_v && a->anchor && a->cand && a->path, "%s: NULL pointer", who);
   DF_CHECK(a->temperature >= 0.f && a->temperature == a->temperature, "%s: temperature must be >= 0", who);
   DF_CHECK(a->temperature == 0.f || a->base_pos, "%s: the sampled walk needs base_pos", who);
   rc = check_ws(ws, ws_bytes, path_ws(a), who);
@@ -1114,42 +1185,62 @@ int dflash_sample_accept(const dflash_sample_accept_args* a, void* ws, size_t ws
 
 // ------------------------------------------------------------- workspace
 
+// The size of every op is computed only from arguments whose shape fields
+// pass the op's checks (pointers are not needed to size a workspace); on a
+// failed check the size is 0 and dflash_last_error() names the field.
 size_t dflash_workspace_bytes(int32_t op, const void* args) {
-  if (!args) return 0;
+  if (!args) {
+    fail(DFLASH_ERR_INVALID_ARG, "dflash_workspace_bytes: NULL args");
+    return 0;
+  }
   const int sms = num_sms();
+  const char* who = "dflash_workspace_bytes";
   switch (op) {
     case DFLASH_OP_EMBED:
-      return kReservedBytes;
-    case DFLASH_OP_PATH:
-      return path_ws(static_cast<const dflash_path_args*>(args));
+      return check_embed_shape(static_cast<const dflash_embed_args*>(args), who) ? 0 : kReservedBytes;
+    case DFLASH_OP_PATH: {
+      const dflash_path_args* a = static_cast<const dflash_path_args*>(args);
+      return check_path_shape(a, who) ? 0 : path_ws(a);
+    }
     case DFLASH_OP_SAMPLE_DRAFTS: {
       const dflash_sample_drafts_args* a = static_cast<const dflash_sample_drafts_args*>(args);
+      if (check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, a->top_k, a->top_p, who)) return 0;
       size_t lo, ko, po;
       return sample_ws(a->n_seqs, a->block, &lo, &ko, &po);
     }
     case DFLASH_OP_SAMPLE_ACCEPT: {
       const dflash_sample_accept_args* a = static_cast<const dflash_sample_accept_args*>(args);
+      if (check_sample_shape(a->dims, a->n_seqs, a->block, a->temperature, a->top_k, a->top_p, who)) return 0;
       size_t lo, ko, po;
       return sample_ws(a->n_seqs, a->block, &lo, &ko, &po);
     }
-    case DFLASH_OP_LAYER:
-      return layer_ws(static_cast<const dflash_layer_args*>(args), sms);
+    case DFLASH_OP_LAYER: {
+      const dflash_layer_args* a = static_cast<const dflash_layer_args*>(args);
+      return check_layer_args_shape(a, who) ? 0 : layer_ws(a, sms);
+    }
     case DFLASH_OP_FUSE: {
+      const dflash_fuse_args* a = static_cast<const dflash_fuse_args*>(args);
+      if (check_fuse_shape(a, who)) return 0;
       float* z;
       void *cb, *gp;
       size_t g;
-      return fuse_ws(static_cast<const dflash_fuse_args*>(args), sms, &z, &cb, &gp, &g, nullptr);
+      return fuse_ws(a, sms, &z, &cb, &gp, &g, nullptr);
     }
     case DFLASH_OP_DRAFT: {
+      const dflash_draft_args* a = static_cast<const dflash_draft_args*>(args);
+      if (check_draft_shape(a, who)) return 0;
       DraftScratch s;
       Bump m(nullptr);
-      return carve_draft(m, static_cast<const dflash_draft_args*>(args), sms, s);
+      return carve_draft(m, a, sms, s);
     }
     case DFLASH_OP_VERIFY: {
+      const dflash_verify_args* a = static_cast<const dflash_verify_args*>(args);
+      if (check_verify_shape(a, who)) return 0;
       void *xf, *hp;
-      return verify_ws(static_cast<const dflash_verify_args*>(args), sms, &xf, &hp, nullptr);
+      return verify_ws(a, sms, &xf, &hp, nullptr);
     }
     default:
+      fail(DFLASH_ERR_INVALID_ARG, "dflash_workspace_bytes: unknown op %d", op);
       return 0;
   }
 }

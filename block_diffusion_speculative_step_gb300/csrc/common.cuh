@@ -130,7 +130,21 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Bounded waits give up after this long and raise ST_TIMEOUT.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// Bounded waits give up after a limit and raise ST_TIMEOUT.  The limit and
+// a test switch live in the workspace header right after the status word
+// (dflash_workspace_control): bytes 8..15 the limit in ns (0: the default,
+// 1 s), bytes 16..19 a nonzero word that makes the attention kernels issue
+// no K/V copies, so that their waits expire with nothing in flight.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* status) {
+  if (status == nullptr) return kDefaultWaitNs;
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return v != 0 ? v : kDefaultWaitNs;
+}
+
+__device__ __forceinline__ bool stall_kv_loads(const uint32_t* status) {
+  return status != nullptr && *reinterpret_cast<const volatile uint32_t*>(status + 4) != 0u;
+}
 
 }  // namespace dfl

@@ -485,6 +485,8 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
 
   // chunk c -> (is block chunk, first tensor row)
   const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
+  const uint64_t lim = wait_limit_ns(status);
+  const bool stall = stall_kv_loads(status);  // test switch: issue no K/V copy
   auto chunk_row = [&](int c, bool& blk) -> int {
     blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
     if (blk) return (s * nkv + g) * rows;
@@ -494,6 +496,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
     return r;
   };
   auto issue = [&](int c, int buf) {  // one thread
+    if (stall) return;
     bool blk;
     const int row = chunk_row(c, blk);
     const CUtensorMap* km = blk ? &p.kb : &p.kc;
@@ -519,9 +522,11 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
   }
   __syncthreads();
   bool pre0 = false, pre1 = false;
+  int issued = 0;  // chunks thread 0 issued (stalled: none)
   if (threadIdx.x == 0) {
     if (nmine > 0 && early_ok(rank)) { issue(rank, 0); pre0 = true; }
     if (nmine > 1 && early_ok(rank + NC)) { issue(rank + NC, 1); pre1 = true; }
+    issued = stall ? 0 : (nmine < 2 ? nmine : 2);
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
 
   for (int i = 0; i < nmine; ++i) {
     const int c = rank + i * NC, buf = i & 1;
-    if (!tc::mbar_wait(&full[buf], (uint32_t)(i >> 1) & 1u, nullptr)) {
+    if (!failed && !tc::mbar_wait(&full[buf], (uint32_t)(i >> 1) & 1u, nullptr, lim)) {
       raise_status(status, ST_TIMEOUT);
       failed = true;
     }
@@ -670,8 +675,15 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
       }
     }
     __syncthreads();  // every warp is done with this buffer
-    if (threadIdx.x == 0 && i + 2 < nmine && !failed) issue(rank + (i + 2) * NC, buf);
+    if (threadIdx.x == 0 && i + 2 < nmine && !failed) {
+      issue(rank + (i + 2) * NC, buf);
+      if (!stall) ++issued;
+    }
   }
+  // every issued copy has landed before the partials overwrite the buffers
+  if (threadIdx.x == 0)
+    for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+      tc::mbar_wait(&full[i & 1], (uint32_t)(i >> 1) & 1u, nullptr, lim);
   __syncthreads();
 
   // ---- merge the four key quarters in order, then this CTA's partial
@@ -865,6 +877,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   auto chunk_of = [&](int i) { return i < nA ? rank + i * NL : rB + (i - nA) * NL; };
 
   const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
+  const uint64_t lim = wait_limit_ns(status);
+  const bool stall = stall_kv_loads(status);  // test switch: issue no K/V copy
   auto chunk_row = [&](int c, bool& blk) -> int {
     blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
     if (blk) return (s * nkv + g) * rows;
@@ -874,6 +888,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     return r;
   };
   auto issue = [&](int c, int buf) {  // one thread
+    if (stall) return;
     bool blk;
     const int row = chunk_row(c, blk);
     const CUtensorMap* km = blk ? &p.kb : &p.kc;
@@ -961,14 +976,21 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- K/V producer: chunk i into buffer i & 1 once P V of chunk i-2 is done
+      int issued = stall ? 0 : (nmine < 2 ? nmine : 2);  // this thread issued chunks 0 and 1 above
       for (int i = 2; i < nmine; ++i) {
-        if (!tc::mbar_wait(&empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort)) {
+        if (!tc::mbar_wait(&empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, lim)) {
           raise_status(status, ST_TIMEOUT);
           *abort = 1;
           break;
         }
         issue(chunk_of(i), i & 1);
+        if (!stall) ++issued;
       }
+      // Every copy this CTA issued has landed before its shared memory goes
+      // away, also when a wait gave up (the last copy into each buffer).
+      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+        tc::mbar_wait(&full[i & 1], (uint32_t)(i >> 1) & 1u, nullptr, lim);
+      if (p.q_tma) tc::mbar_wait(qfull, 0u, nullptr, lim);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -977,7 +999,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       constexpr uint32_t idV = tc::idesc_bf16_f32_bmn(kTcAttnRows, D);
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (ok && !tc::mbar_wait(bar, par, abort)) {
+        if (ok && !tc::mbar_wait(bar, par, abort, lim)) {
           raise_status(status, ST_TIMEOUT);
           *abort = 1;
           ok = false;
@@ -1060,7 +1082,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       const int nk = blk ? min(rows, CH) : min(CH, sk.n_ctx - c * CH);
       const bool causal = mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
       const int lim = causal ? P + row_tok - slot0 : CH;
-      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort)) {
+      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort, lim)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;
@@ -1103,7 +1125,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       xs[piece * 64 + qr] = sum;
       // P has one buffer: the P V products of the chunk before must have
       // finished reading it (S of this chunk was issued ahead of them).
-      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort)) {
+      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;
@@ -1158,7 +1180,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     }
     // ---- this CTA's partial of its 64 rows (lanes 0..63, OC columns per thread)
     if (o_owner && nmine > 0) {
-      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort)) {
+      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort, lim)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;

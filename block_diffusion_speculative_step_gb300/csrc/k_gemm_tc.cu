@@ -56,7 +56,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int G;          // CTAs (runs)
   int M;          // token rows
   int defer;      // GEMM, BN >= 128: split tiles are finished by tc_fixup_kernel, not by their last piece
-  float* part;    // partial slots [n_tiles + G][BN][128]
+  float* part;    // partial slots [2 G][BN][128] (piece_slot)
   Top2* tops;     // LM head: per-CTA triples [G][M]
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
   uint32_t* counters;
@@ -87,6 +87,14 @@ __device__ __forceinline__ int run_of(long long p, long long T, int G) {
   while (c + 1 <= G && run_start(T, G, c + 1) <= p) ++c;
   while (c > 0 && run_start(T, G, c) > p) --c;
   return c;
+}
+
+// Partial slot of run c's piece of the tile that starts at tbeg.  A run is
+// contiguous, so only its first piece (slot 2c) and its last piece (slot
+// 2c + 1, when the run began in an earlier tile) can be parts of split
+// tiles: 2 slots per run, whatever the tile count.
+__device__ __forceinline__ size_t piece_slot(long long T, int G, int c, long long tbeg) {
+  return 2 * (size_t)c + (run_start(T, G, c) < tbeg ? 1u : 0u);
 }
 
 __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort) {
@@ -443,6 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   const int nkb = L.nkb;
   const long long p0 = run_start(L.T, L.G, blockIdx.x), p1 = run_start(L.T, L.G, blockIdx.x + 1);
   const int n_my = (int)(p1 - p0);
+  const uint64_t lim = wait_limit_ns(L.status);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -514,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       int issued = pre;
       for (int i = pre; i < n_my; ++i) {
         const int s = i % ST;
-        if (!tc::mbar_wait(&empty[s], ((uint32_t)(i / ST) & 1u) ^ 1u, abort)) {
+        if (!tc::mbar_wait(&empty[s], ((uint32_t)(i / ST) & 1u) ^ 1u, abort, lim)) {
           tc_timeout(L.status, abort);
           break;
         }
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       }
       // every issued copy has landed before this CTA's shared memory goes away
       for (int i = (issued > ST ? issued - ST : 0); i < issued; ++i)
-        tc::mbar_wait(&full[i % ST], (uint32_t)(i / ST) & 1u, nullptr);
+        tc::mbar_wait(&full[i % ST], (uint32_t)(i / ST) & 1u, nullptr, lim);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -539,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         const int t = (int)(pos / nkb);
         const long long end = p1 < (long long)(t + 1) * nkb ? p1 : (long long)(t + 1) * nkb;
         const int b = k & 1;
-        if (!tc::mbar_wait(&acce[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort)) {
+        if (!tc::mbar_wait(&acce[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort, lim)) {
           tc_timeout(L.status, abort);
           break;
         }
@@ -547,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         const uint32_t d = tmem + (uint32_t)(b * Cfg::ACC);
         for (long long q = pos; q < end; ++q, ++i) {
           const int s = i % ST;
-          if (!tc::mbar_wait(&full[s], (uint32_t)(i / ST) & 1u, abort)) {
+          if (!tc::mbar_wait(&full[s], (uint32_t)(i / ST) & 1u, abort, lim)) {
             tc_timeout(L.status, abort);
             stop = true;
             break;
@@ -611,7 +620,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         seg_built = t / L.tps;
         e = make_epi(p.g, seg_built);
       }
-      if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort)) tc_timeout(L.status, abort);
+      if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort, lim)) tc_timeout(L.status, abort);
       tc::named_bar(1, 128);
       if (*abort) break;  // uniform: read after the barrier
       tc::tc_fence_after();
@@ -645,8 +654,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         tc::named_bar(1, 128);
         if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
       } else {
-        const long long slot = blockIdx.x + (long long)t;  // global piece index
-        float* dst0 = L.part + (size_t)slot * BN * 128 + r;
+        const size_t slot = 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);  // piece_slot of this piece
+        float* dst0 = L.part + slot * BN * 128 + r;
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
@@ -676,8 +685,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         }
         tc::named_bar(1, 128);
         if (*s_flag) {
-          const int first = run_of(tbeg, L.T, L.G) + t;
-          const int last = run_of(tend - 1, L.T, L.G) + t;
+          const int first = run_of(tbeg, L.T, L.G);
+          const int last = run_of(tend - 1, L.T, L.G);
           for (int c0 = 0; c0 < ncol; c0 += 16) {
             float v[16];
             float pre[32];
@@ -688,12 +697,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            // partial slots in k order; each batch of up to 4 slots is loaded at once
+            // the pieces' partial slots in k order (runs first..last); each
+            // batch of up to 4 slots is loaded at once
             for (int sb = first; sb <= last; sb += 4) {
               float pv[4][16];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const float* src = L.part + (size_t)(sb + q) * BN * 128 + (size_t)c0 * 128 + r;
+                const int c = sb + q <= last ? sb + q : last;
+                const float* src = L.part + piece_slot(L.T, L.G, c, tbeg) * BN * 128 + (size_t)c0 * 128 + r;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
               }
@@ -746,7 +757,7 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
   const int nch = min(BN, ((L.M + 15) / 16) * 16) / 16;
   const int t = (int)(blockIdx.x / nch), c0 = (int)(blockIdx.x % nch) * 16;
   const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
-  const int first = run_of(tbeg, L.T, L.G) + t, last = run_of(tend - 1, L.T, L.G) + t;
+  const int first = run_of(tbeg, L.T, L.G), last = run_of(tend - 1, L.T, L.G);
   if (first == last) return;  // one run covers the tile: finished inline (uniform over the CTA)
   const int r = threadIdx.x, lane = r & 31;
   // the partial slots first: they depend on nothing below
@@ -782,7 +793,8 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
     float pv[4][16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float* src = L.part + (size_t)(sb + q) * BN * 128 + (size_t)c0 * 128 + r;
+      const int c = sb + q <= last ? sb + q : last;
+      const float* src = L.part + piece_slot(L.T, L.G, c, tbeg) * BN * 128 + (size_t)c0 * 128 + r;
 #pragma unroll
       for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
     }
@@ -815,7 +827,8 @@ int gemm_tiles_per_seg(const GemmDesc& g) { return g.kind == EPI_SWIGLU ? g.inte
 
 int runs_for(long long T, int num_sms) { return (int)(T < num_sms ? T : num_sms); }
 
-size_t part_bytes(int n_tiles, int G, int bn) { return (size_t)(n_tiles + G) * bn * 128 * sizeof(float); }
+// Split-K partial slots: two per run (piece_slot).
+size_t part_bytes(int G, int bn) { return (size_t)2 * G * bn * 128 * sizeof(float); }
 
 template <int BN>
 cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
@@ -862,7 +875,7 @@ bool gemm_tc_supported(const GemmDesc& g) {
 size_t gemm_tc_workspace(const GemmDesc& g, int num_sms) {
   const int n_tiles = g.nseg * gemm_tiles_per_seg(g);
   const long long T = (long long)n_tiles * (g.K / 64);
-  return part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(g.M));
+  return part_bytes(runs_for(T, num_sms), pick_bn(g.M));
 }
 
 cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
@@ -911,7 +924,7 @@ cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, ui
   p.T = (long long)p.n_tiles * p.nkb;
   p.G = runs_for(p.T, num_sms);
   if (p.n_tiles > 8192) return cudaErrorInvalidValue;
-  if (ws_bytes < part_bytes(p.n_tiles, p.G, pick_bn(g.M))) return cudaErrorInvalidValue;
+  if (ws_bytes < part_bytes(p.G, pick_bn(g.M))) return cudaErrorInvalidValue;
   p.part = static_cast<float*>(ws);
   p.counters = counters;
   p.status = status;
@@ -943,14 +956,14 @@ size_t head_sel_bytes(const HeadDesc& h, int n_tiles, int G) {
 size_t head_tc_workspace(const HeadDesc& h, int num_sms) {
   const int n_tiles = (h.V + 127) / 128;
   const long long T = (long long)n_tiles * (h.H / 64);
-  return ((part_bytes(n_tiles, runs_for(T, num_sms), pick_bn(h.M)) + 255) & ~size_t(255)) +
+  return ((part_bytes(runs_for(T, num_sms), pick_bn(h.M)) + 255) & ~size_t(255)) +
          head_sel_bytes(h, n_tiles, runs_for(T, num_sms)) + 256;
 }
 
 const void* head_tc_tlist(const HeadDesc& h, int num_sms, int* n_tiles) {
   const int nt = (h.V + 127) / 128;
   const long long T = (long long)nt * (h.H / 64);
-  const size_t pb = part_bytes(nt, runs_for(T, num_sms), pick_bn(h.M));
+  const size_t pb = part_bytes(runs_for(T, num_sms), pick_bn(h.M));
   *n_tiles = nt;
   return reinterpret_cast<const char*>(h.partials) + ((pb + 255) & ~size_t(255));
 }
@@ -966,7 +979,7 @@ cudaError_t launch_head_tc(const HeadDesc& h, int num_sms, cudaStream_t st) {
   p.nkb = h.H / 64;
   p.T = (long long)p.n_tiles * p.nkb;
   p.G = runs_for(p.T, num_sms);
-  const size_t pb = part_bytes(p.n_tiles, p.G, pick_bn(h.M));
+  const size_t pb = part_bytes(p.G, pick_bn(h.M));
   p.part = h.partials;
   p.tops = reinterpret_cast<Top2*>(reinterpret_cast<char*>(h.partials) + ((pb + 255) & ~size_t(255)));
   p.tlist = reinterpret_cast<Cand*>(p.tops);

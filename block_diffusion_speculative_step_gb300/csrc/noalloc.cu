@@ -10,6 +10,7 @@
 
 namespace dfl {
 int abi_fail(int code, const char* msg);
+int verify_check(const dflash_verify_args* a, const char* who);
 }
 
 namespace {
@@ -49,9 +50,11 @@ int scratch_address(void** out) {
 
 extern "C" int dflash_verify_accept_noalloc(const dflash_verify_args* a, int32_t* status_out,
                                             dflash_stream_t stream) {
-  if (!a) return dfl::abi_fail(DFLASH_ERR_INVALID_ARG, "dflash_verify_accept_noalloc: NULL args");
+  // the checks of dflash_verify_accept first, so that bad arguments report
+  // DFLASH_ERR_INVALID_ARG as they do there, never a scratch size
+  int rc = dfl::verify_check(a, "dflash_verify_accept_noalloc");
+  if (rc) return rc;
   const size_t need = dflash_workspace_bytes(DFLASH_OP_VERIFY, a);
-  if (need == 0) return dfl::abi_fail(DFLASH_ERR_INVALID_ARG, "dflash_verify_accept_noalloc: invalid arguments");
   if (need > kStaticScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg),
@@ -61,7 +64,7 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_verify_args* a, int32_t
     return dfl::abi_fail(DFLASH_ERR_WORKSPACE, msg);
   }
   void* ws = nullptr;
-  int rc = scratch_address(&ws);
+  rc = scratch_address(&ws);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   // status word and arrival counters must start at zero

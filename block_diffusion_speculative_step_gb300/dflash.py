@@ -31,7 +31,7 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
            "dflash_verify_accept_noalloc", "dflash_trace_launches", "dflash_sample_drafts",
-           "dflash_sample_accept")
+           "dflash_sample_accept", "dflash_workspace_control")
 DFLASH_TRACE_FAMILIES = 13
 
 
@@ -71,7 +71,8 @@ class dflash_layer_args(C.Structure):
     _fields_ = [("dims", dflash_dims), ("w", dflash_layer_weights), ("n_seqs", i32), ("rows", i32),
                 ("base_pos", vp), ("h", vp), ("kv", dflash_kv), ("attn_mode", i32), ("max_pos", i32),
                 ("rope_cs", vp), ("rope_max_pos", i32), ("tap", vp), ("tap_stride", i32),
-                ("tap_offset", i32)]
+                ("tap_offset", i32), ("out_x_attn", vp), ("out_q", vp), ("out_kb", vp), ("out_vb", vp),
+                ("out_attn", vp), ("out_x_mlp", vp), ("out_act", vp)]
 
 
 class dflash_fuse_args(C.Structure):
@@ -146,6 +147,8 @@ def lib(path: str | None = None):
         L.dflash_workspace_bytes.restype = C.c_size_t
         L.dflash_workspace_init.argtypes = [vp, C.c_size_t, vp]
         L.dflash_workspace_init.restype = C.c_int
+        L.dflash_workspace_control.argtypes = [vp, C.c_size_t, C.c_uint64, i32, vp]
+        L.dflash_workspace_control.restype = C.c_int
         L.dflash_read_status.argtypes = [vp, vp, P_i32]
         L.dflash_read_status.restype = C.c_int
         L.dflash_last_error.restype = C.c_char_p
@@ -190,6 +193,12 @@ def dflash_workspace_bytes(op: int, args) -> int:
 
 def dflash_workspace_init(ws_ptr: int, ws_bytes: int, stream=None):
     _check(lib().dflash_workspace_init(ws_ptr, ws_bytes, _stream(stream)))
+
+
+def dflash_workspace_control(ws_ptr: int, ws_bytes: int, wait_limit_ns: int = 0, stall_kv_loads: bool = False,
+                             stream=None):
+    _check(lib().dflash_workspace_control(ws_ptr, ws_bytes, wait_limit_ns, 1 if stall_kv_loads else 0,
+                                          _stream(stream)))
 
 
 def dflash_read_status(ws_ptr: int, stream=None) -> int:

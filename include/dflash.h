@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 6
+#define DFLASH_ABI_VERSION 7
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -179,6 +179,19 @@ int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_s
  *   to tap[row * tap_stride + tap_offset + j] (feature taps for fusion).
  * max_pos: host-side bound with base_pos[s] + rows <= max_pos for every s
  *   (sizes the attention grid; also must not exceed the RoPE table).
+ * Stage outputs (each optional, NULL = not wanted; for parity checks that
+ *   compare every stage with an oracle fed the GPU's own inputs): when a
+ *   pointer is given the layer writes that intermediate there instead of
+ *   into its workspace, so asking for it adds no work.  Every pointer must
+ *   be 16-byte aligned; elements are dims.dtype.
+ *     x_attn [M][H]        RMSNorm(h; ln1), the QKV projection's input
+ *     q      [M][n_q*d]    rotated queries
+ *     kb, vb [n_seqs][n_kv][rows][d]  the block's rotated keys and values
+ *                          (DFLASH_ATTN_BLOCK_BIDIR only; causal layers
+ *                          write them into kv)
+ *     attn   [M][n_q*d]    attention output, the O projection's input
+ *     x_mlp  [M][H]        RMSNorm(h; ln2) after the attention residual
+ *     act    [M][I]        SiLU(gate) * up, the down projection's input
  */
 typedef struct {
   dflash_dims dims;
@@ -193,6 +206,13 @@ typedef struct {
   int32_t rope_max_pos;
   void* tap;               /* optional */
   int32_t tap_stride, tap_offset;
+  void* out_x_attn;        /* optional stage outputs (see above) */
+  void* out_q;
+  void* out_kb;
+  void* out_vb;
+  void* out_attn;
+  void* out_x_mlp;
+  void* out_act;
 } dflash_layer_args;
 int dflash_decoder_layer_forward(const dflash_layer_args* a, void* ws, size_t ws_bytes,
                                  dflash_stream_t stream);
@@ -450,6 +470,25 @@ size_t dflash_workspace_bytes(int32_t op, const void* args);
 /* Zero a workspace (status word and the library's arrival counters). */
 int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * Failure-detection controls kept in a workspace's header, next to its
+ * status word (all zero after dflash_workspace_init, which restores the
+ * defaults; dflash_read_status leaves them):
+ *  - wait_limit_ns: how long a bounded device wait (a TMA copy, an MMA, a
+ *    pipeline stage of another warp) spins before the kernel gives up,
+ *    raises DFLASH_ERR_TIMEOUT in the status word and unwinds, keeping the
+ *    GPU context usable.  0 selects the default, 1 s.
+ *  - stall_kv_loads: nonzero makes the attention kernels issue none of their
+ *    K/V copies, so that their waits expire with nothing in flight -- the
+ *    way to test the timeout path without a GPU fault.  Its outputs are then
+ *    meaningless.  Keep it 0 in use.
+ * The controls are copied with cudaMemcpyAsync on `stream` from host memory
+ * (not inside a stream capture).  A workspace used by
+ * dflash_verify_accept_noalloc has its controls reset by every such call.
+ */
+int dflash_workspace_control(void* ws, size_t ws_bytes, uint64_t wait_limit_ns, int32_t stall_kv_loads,
+                             dflash_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's device status word.
  * *host_status receives DFLASH_OK or the first error raised on the device. */
 int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status);
@@ -494,8 +533,17 @@ int dflash_trace_end(void);
  * only input and output buffers, or code that must not allocate on its hot
  * path.  Every GPU that loads the library holds the 8 MiB array until the
  * process exits.
- *  - Rejects, with DFLASH_ERR_WORKSPACE and a message, any call whose scratch
- *    (dflash_workspace_bytes(DFLASH_OP_VERIFY, a)) exceeds 8 MiB.
+ *  - Runs every argument check of dflash_verify_accept first (bad arguments
+ *    return DFLASH_ERR_INVALID_ARG), then rejects, with DFLASH_ERR_WORKSPACE
+ *    and a message, any call whose scratch (dflash_workspace_bytes(
+ *    DFLASH_OP_VERIFY, a)) exceeds 8 MiB.  That scratch is, for M =
+ *    n_seqs * block token rows, G = min(SM count, ceil(V / 128) * H / 64)
+ *    and BN the smallest of 16, 32, 64, 128, 256 not below min(M, 256):
+ *      131328 + M*H*e + 2*G*BN*512 + G*M*12 bytes (+ up to 1 KB of
+ *    alignment; e = 2 for bf16, 4 for fp32).  On a 152-SM GPU at H = 4096
+ *    that admits M <= 32 token rows at any vocabulary size -- one sequence
+ *    of a 16- or 17-row verification block, or two 16-row blocks -- and
+ *    rejects M >= 33 (BN = 64 alone needs 9.5 MiB).
  *  - Calls no cudaMalloc/cudaFree.  The first call on a device looks up the
  *    array's device address once for that device (with it current); make
  *    that first call before any stream capture.

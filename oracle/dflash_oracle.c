@@ -239,8 +239,46 @@ static long slot_of(long t, long window) { return window > 0 ? t % window : t; }
  * else 0); row i attends all of those and all M rows of the block, with no
  * mask inside the block.  The block K/V are not stored.
  */
+/*
+ * Stage values of one layer, each [M][width] row-major: x1 = the attention
+ * input (rounded RMSNorm), q = rotated queries, k / v = the rows' rotated
+ * keys and values ([M][nkv*d]), o = the attention output, x2 = the MLP input,
+ * act = SiLU(gate)*up.  Any field may be NULL.
+ */
+typedef struct {
+  double *x1, *q, *k, *v, *o, *x2, *act;
+} or_stages;
+
+static void stage_io(const double* given, double* out, double* cur, size_t n) {
+  if (out) memcpy(out, cur, sizeof(double) * n);
+  if (given) memcpy(cur, given, sizeof(double) * n);
+}
+
+/*
+ * The layer with every stage open to inspection (teacher forcing).  When
+ * out->F is non-NULL it receives this layer's own value of stage F, computed
+ * from the stages before it; when given->F is non-NULL, that value then
+ * replaces stage F for everything after it -- so each stage can be checked
+ * against an implementation fed that implementation's own inputs.  With both
+ * NULL this is exactly the plain layer.  In causal mode the cache receives
+ * the (possibly given) k, v.
+ */
+int or_decoder_layer_tf(const or_cfg* c, const or_layer* L, const or_conv* cv, int M, long p0, int mode,
+                        double* kc, double* vc, long cap, long window, double* h, const or_stages* given,
+                        or_stages* out);
+
 int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv, int M, long p0,
                           int mode, double* kc, double* vc, long cap, long window, double* h) {
+  return or_decoder_layer_tf(c, L, cv, M, p0, mode, kc, vc, cap, window, h, NULL, NULL);
+}
+
+int or_decoder_layer_tf(const or_cfg* c, const or_layer* L, const or_conv* cv, int M, long p0, int mode,
+                        double* kc, double* vc, long cap, long window, double* h, const or_stages* given,
+                        or_stages* out) {
+  const or_stages none = {0, 0, 0, 0, 0, 0, 0};
+  if (!given) given = &none;
+  or_stages discard = none;
+  if (!out) out = &discard;
   const int H = c->H, d = c->d, nq = c->nq, nkv = c->nkv, I = c->I;
   const int QD = nq * d, KD = nkv * d, grp = nq / nkv;
   if (M <= 0) return 0;
@@ -263,6 +301,7 @@ int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv,
     for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
   }
   if (cv) conv_rows(c, cv, OR_CONV_PRE_ATTN, M, x, 1); /* a projection input: rounded */
+  stage_io(given->x1, out->x1, x, (size_t)M * H);
   or_linear(c, L->wq, QD, H, M, x, q);
   or_linear(c, L->wk, KD, H, M, x, k);
   or_linear(c, L->wv, KD, H, M, x, v);
@@ -276,6 +315,9 @@ int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv,
       v[(size_t)m * KD + i] = rnd(c, v[(size_t)m * KD + i]);
     }
   }
+  stage_io(given->q, out->q, q, (size_t)M * QD);
+  stage_io(given->k, out->k, k, (size_t)M * KD);
+  stage_io(given->v, out->v, v, (size_t)M * KD);
   if (mode == OR_CAUSAL) {
     for (int m = 0; m < M; ++m)
       for (int g = 0; g < nkv; ++g) {
@@ -323,6 +365,7 @@ int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv,
     free(sc);
   }
   for (size_t i = 0; i < (size_t)M * QD; ++i) o[i] = rnd(c, o[i]);
+  stage_io(given->o, out->o, o, (size_t)M * QD);
 
   or_linear(c, L->wo, H, QD, M, o, y);
   if (cv) conv_rows(c, cv, OR_CONV_POST_ATTN, M, y, 0); /* added to the residual: not rounded */
@@ -333,9 +376,11 @@ int or_decoder_layer_conv(const or_cfg* c, const or_layer* L, const or_conv* cv,
     for (int i = 0; i < H; ++i) x[(size_t)m * H + i] = rnd(c, x[(size_t)m * H + i]);
   }
   if (cv) conv_rows(c, cv, OR_CONV_PRE_MLP, M, x, 1);
+  stage_io(given->x2, out->x2, x, (size_t)M * H);
   or_linear(c, L->wg, I, H, M, x, gt);
   or_linear(c, L->wu, I, H, M, x, up);
   for (size_t i = 0; i < (size_t)M * I; ++i) gt[i] = rnd(c, silu(gt[i]) * up[i]);
+  stage_io(given->act, out->act, gt, (size_t)M * I);
   or_linear(c, L->wd, H, I, M, gt, y);
   if (cv) conv_rows(c, cv, OR_CONV_POST_MLP, M, y, 0);
   for (size_t i = 0; i < (size_t)M * H; ++i) h[i] += y[i];

@@ -64,6 +64,13 @@ class _Layer(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g1", "g2")]
 
 
+class _Stages(C.Structure):
+    _fields_ = [(n, C.POINTER(C.c_double)) for n in ("x1", "q", "k", "v", "o", "x2", "act")]
+
+
+STAGES = ("x1", "q", "k", "v", "o", "x2", "act")
+
+
 class _Conv(C.Structure):
     _fields_ = [("w1", C.c_void_p * 4), ("w2", C.c_void_p * 4), ("r", C.c_int)]
 
@@ -83,6 +90,9 @@ def lib():
                                            C.c_int, dp, dp, C.c_long, C.c_long, dp]
             L.or_decoder_layer_conv.argtypes = [C.POINTER(_Cfg), C.POINTER(_Layer), C.POINTER(_Conv), C.c_int,
                                                 C.c_long, C.c_int, dp, dp, C.c_long, C.c_long, dp]
+            L.or_decoder_layer_tf.argtypes = [C.POINTER(_Cfg), C.POINTER(_Layer), C.POINTER(_Conv), C.c_int,
+                                              C.c_long, C.c_int, dp, dp, C.c_long, C.c_long, dp,
+                                              C.POINTER(_Stages), C.POINTER(_Stages)]
             L.or_dyn_conv.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, C.c_void_p, C.c_void_p, dp, dp]
             L.or_final_norm.argtypes = [C.POINTER(_Cfg), C.c_int, dp, C.c_void_p, dp]
             L.or_lm_head_argmax.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_int, C.c_int, dp,
@@ -277,6 +287,35 @@ def decoder_layer(cfg: Cfg, L: Layer, h: np.ndarray, p0: int, mode: int, kc: np.
                                     _dp(kc), _dp(vc), cap, int(window), _dp(h))
     if rc != 0:
         raise ValueError(f"or_decoder_layer failed ({rc})")
+
+
+def decoder_layer_tf(cfg: Cfg, L: Layer, h: np.ndarray, p0: int, mode: int, kc: np.ndarray, vc: np.ndarray,
+                     window: int = 0, given: dict | None = None) -> dict:
+    """The layer of decoder_layer with its stages open (teacher forcing):
+    returns this oracle's own value of every stage (x1, q, k, v, o, x2, act;
+    [M][width], k / v as [M][nkv*d]) computed from the stages before it, where
+    each stage given in `given` (same shapes, float64) replaces the oracle's
+    own value for everything after it.  h (in place) ends as the layer's
+    output; in causal mode the cache receives the rows' (given) k, v."""
+    assert h.dtype == np.float64 and h.flags.c_contiguous
+    M = h.shape[0]
+    width = dict(x1=cfg.H, q=cfg.nq * cfg.d, k=cfg.nkv * cfg.d, v=cfg.nkv * cfg.d, o=cfg.nq * cfg.d, x2=cfg.H,
+                 act=cfg.I)
+    out = {n: np.zeros((M, width[n])) for n in STAGES}
+    keep = {}
+    gv = _Stages()
+    for n in STAGES:
+        if given is not None and given.get(n) is not None:
+            a = np.ascontiguousarray(given[n], dtype=np.float64).reshape(M, width[n])
+            keep[n] = a
+            setattr(gv, n, _dp(a))
+    ov = _Stages(*[_dp(out[n]) for n in STAGES])
+    conv = C.byref(L.conv.c()) if L.conv is not None else None
+    rc = lib().or_decoder_layer_tf(C.byref(cfg.c()), C.byref(L.c()), conv, M, int(p0), int(mode), _dp(kc), _dp(vc),
+                                   kc.shape[1], int(window), _dp(h), C.byref(gv), C.byref(ov))
+    if rc != 0:
+        raise ValueError(f"or_decoder_layer_tf failed ({rc})")
+    return out
 
 
 def dyn_conv(cfg: Cfg, W1: np.ndarray, W2: np.ndarray, u: np.ndarray) -> np.ndarray:

@@ -82,7 +82,7 @@ def tconv(c: O.Cfg, cv: O.Conv, i: int, u: torch.Tensor) -> torch.Tensor:
 
 
 def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=None, ctx_v=None,
-                causal=True, past_k=None, past_v=None):
+                causal=True, past_k=None, past_v=None, stages=None):
     """One decoder layer with F.rms_norm / F.scaled_dot_product_attention /
     F.silu.  Causal: keys = past (already rotated) ++ the rows'; bidirectional:
     keys = ctx ++ the rows', no mask.  Returns (h_out, k_rows, v_rows)."""
@@ -92,6 +92,7 @@ def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=
     x = tround(F.rms_norm(h, (c.H,), t64(L.g1), c.eps), bf)
     if cv is not None:
         x = tround(tconv(c, cv, 0, x), bf)
+    x1 = x
     q = (x @ t64(L.wq).T).view(M, c.nq, c.d)
     k = (x @ t64(L.wk).T).view(M, c.nkv, c.d)
     v = (x @ t64(L.wv).T).view(M, c.nkv, c.d)
@@ -122,4 +123,6 @@ def torch_layer(c: O.Cfg, L: O.Layer, h: torch.Tensor, pos: torch.Tensor, ctx_k=
     a = tround(F.silu(x @ t64(L.wg).T) * (x @ t64(L.wu).T), bf)
     y = a @ t64(L.wd).T
     h = h + (y if cv is None else tconv(c, cv, 3, y))
+    if stages is not None:  # the intermediates, [M][width]
+        stages.update(x1=x1, q=q.reshape(M, -1), k=k.reshape(M, -1), v=v.reshape(M, -1), o=o, x2=x, act=a)
     return h, k, v

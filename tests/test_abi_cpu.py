@@ -101,3 +101,58 @@ def test_binding_raises(D):
     with pytest.raises(D.DFlashError) as e:
         D.dflash_embed(D.dflash_embed_args(), 0, 0, stream=0)
     assert e.value.code == D.DFLASH_ERR_INVALID_ARG
+
+
+def _qwen_verify(D, S, B):
+    v = D.dflash_verify_args()
+    v.dims = D.dflash_dims(4096, 32, 8, 128, 12288, 151936, 1e6, 1e-6, D.DFLASH_BF16)
+    v.h = v.final_norm = v.lm_head = v.argmax = v.accept_len = v.out_tokens = v.drafts = 256
+    v.n_seqs, v.block = S, B
+    return v
+
+
+def test_noalloc_scratch_limit_at_full_shapes(D):
+    """Where the allocation-free verification's 8 MiB scratch ends, at the
+    Qwen3-8B shapes (H 4096, V 151936): up to 32 token rows per call fit (a
+    16- or 17-row block of one sequence, two 16-row blocks), 33 and more do
+    not.  Without a GPU the library sizes for its fallback SM count (148),
+    a few percent below GB300's 152, where the same rows fit."""
+    limit = 8 << 20
+    for S, B, fits in ((1, 16, True), (1, 17, True), (2, 16, True), (1, 32, True), (1, 33, False),
+                       (4, 16, False), (32, 17, False)):
+        need = D.dflash_workspace_bytes(D.DFLASH_OP_VERIFY, _qwen_verify(D, S, B))
+        assert need > 0
+        assert (need <= limit) == fits, (S, B, need)
+        # the documented formula, at 152 SMs (a GB300), keeps the same verdict
+        M = S * B
+        bn = next(b for b in (16, 32, 64, 128, 256) if b >= min(M, 256))
+        G = 152
+        formula = 131328 + M * 4096 * 2 + 2 * G * bn * 512 + G * M * 12
+        assert (formula + 1024 <= limit) == fits, (S, B, formula)
+    # beyond the limit: rejected before any device work, with the size in the message
+    rc = D.lib().dflash_verify_accept_noalloc(C.byref(_qwen_verify(D, 4, 16)), None, None)
+    assert rc == D.DFLASH_ERR_WORKSPACE
+    assert "8 MiB" in D.dflash_last_error()
+
+
+def test_noalloc_checks_arguments_first(D):
+    """Bad arguments give DFLASH_ERR_INVALID_ARG, as dflash_verify_accept
+    does, never a scratch-size error; dflash_workspace_bytes gives 0."""
+    L = D.lib()
+    for field, val, word in (("n_seqs", -3, "n_seqs"), ("block", 0, "block")):
+        v = _qwen_verify(D, 1, 16)
+        setattr(v, field, val)
+        assert L.dflash_verify_accept_noalloc(C.byref(v), None, None) == D.DFLASH_ERR_INVALID_ARG
+        assert word in D.dflash_last_error()
+        assert D.dflash_workspace_bytes(D.DFLASH_OP_VERIFY, v) == 0
+    v = _qwen_verify(D, 1, 16)
+    v.dims.dtype = 7
+    assert L.dflash_verify_accept_noalloc(C.byref(v), None, None) == D.DFLASH_ERR_INVALID_ARG
+    assert "dtype" in D.dflash_last_error()
+    v = _qwen_verify(D, 1, 16)
+    v.dims.hidden = 4100 - 2  # not a multiple of 8
+    assert D.dflash_workspace_bytes(D.DFLASH_OP_VERIFY, v) == 0
+    v = _qwen_verify(D, 1, 16)
+    v.drafts = 0
+    assert L.dflash_verify_accept_noalloc(C.byref(v), None, None) == D.DFLASH_ERR_INVALID_ARG
+    assert "drafts" in D.dflash_last_error()

@@ -1,10 +1,11 @@
 """Parity at the full Qwen3-8B-shaped sizes of the benchmark workload, in the
 launch configuration the benchmark times (batch 1, 16-row block, context
 4096, the tcgen05 stream-K GEMMs, the cluster attention, the fused LM-head
-argmax): one causal target layer, one bidirectional draft layer, the
-context fusion into five draft layers, and verification over the full
-151936-entry vocabulary.  The oracle (OpenMP over output rows) computes
-every output at these sizes in seconds, so all of them are compared."""
+argmax): one causal target layer, the five-layer draft block with its LM
+head, the context fusion into five draft layers, and verification over the
+full 151936-entry vocabulary.  The oracle (OpenMP over output rows) computes
+every output at these sizes in seconds, so all of them are compared; layers
+are compared stage by stage against the oracle fed the GPU's own inputs."""
 import dataclasses
 
 import numpy as np
@@ -13,7 +14,7 @@ import torch
 
 from block_diffusion_speculative_step_gb300 import dflash as D
 from block_diffusion_speculative_step_gb300 import synth
-from block_diffusion_speculative_step_gb300.engine import Engine, layer_weights
+from block_diffusion_speculative_step_gb300.engine import Engine
 from oracle import oracle as O
 from tests import gpu_common as G
 from tests import helpers as Hh
@@ -48,6 +49,8 @@ def olayer(w, s, L):
 
 
 def test_fullsize_causal_layer(big):
+    """One Qwen3-8B-shaped target layer over a 16-row block at position 4096,
+    every stage checked against the oracle fed the GPU's inputs to it."""
     w, m, eng = big
     B = w.block
     eng.base_pos.fill_(CTX)
@@ -55,39 +58,41 @@ def test_fullsize_causal_layer(big):
     eng.h[:B].copy_(h0.cuda())
     kc = G.f64(eng.caches.tk[0][0])
     vc = G.f64(eng.caches.tv[0][0])
-    D.dflash_decoder_layer_forward(eng.target_layer_args(0, B, eng.h), eng.ws_ptr, eng.ws_bytes)
-    got = G.f64(eng.h[:B])
+    bufs = G.stage_buffers(w.target, 1, B, bidir=False)
+    a = G.attach_stages(eng.target_layer_args(0, B, eng.h), bufs)
+    D.dflash_decoder_layer_forward(a, eng.ws_ptr, eng.ws_bytes)
     assert eng.status() == D.DFLASH_OK
-    h = h0.double().numpy().copy()
-    O.decoder_layer(ocfg(w, w.target), olayer(w, w.target, m["target"]["layers"][0]), h, CTX, O.CAUSAL, kc, vc)
-    G.assert_hidden_close(got, h)
+    got = G.f64(eng.h[:B])
     # the block's K/V went into the cache at positions CTX .. CTX+B-1
-    G.assert_bf16_close(G.f64(eng.caches.tk[0][0, :, CTX:CTX + B]), kc[:, CTX:CTX + B])
+    kr = G.f64(eng.caches.tk[0][0, :, CTX:CTX + B])
+    vr = G.f64(eng.caches.tv[0][0, :, CTX:CTX + B])
+    rep = G.check_layer_tf(O, ocfg(w, w.target), olayer(w, w.target, m["target"]["layers"][0]),
+                           h0.double().numpy(), CTX, O.CAUSAL, kc, vc, G.gpu_stages(bufs, 0, B, kr, vr), got)
+    print("PARITY causal layer (teacher-forced):", rep)
 
 
-def test_fullsize_draft_layer(big):
+def test_fullsize_draft_block(big):
+    """The benchmark's draft block at full size: five Qwen3-8B-shaped draft
+    layers over a 4096-position injected context, block 16, the 151936-entry
+    LM head with its fused argmax.  Every layer teacher-forced, the LM head
+    at the stated logit bound, drafts bit for bit up to reported near-ties;
+    the end-to-end logit difference against the oracle's whole draft
+    forward is reported."""
     w, m, eng = big
     B = w.block
     eng.base_pos.fill_(CTX)
-    h0 = torch.randn(B, w.draft.hidden, generator=torch.Generator().manual_seed(2))
-    eng.h[:B].copy_(h0.cuda())
-    a = D.dflash_layer_args()
-    a.dims = eng.ddims
-    a.w = layer_weights(m["draft"]["layers"][2])
-    a.n_seqs, a.rows = 1, B
-    a.base_pos = eng.base_pos.data_ptr()
-    a.h = eng.h.data_ptr()
-    a.kv = D.dflash_kv(eng.caches.dk[2].data_ptr(), eng.caches.dv[2].data_ptr(), eng.dcap, 0)
-    a.attn_mode = D.DFLASH_ATTN_BLOCK_BIDIR
-    a.max_pos = eng.cap
-    a.rope_cs = eng.rope_d.data_ptr()
-    a.rope_max_pos = eng.rope_max
-    D.dflash_decoder_layer_forward(a, eng.ws_ptr, eng.ws_bytes)
-    got = G.f64(eng.h[:B])
-    h = h0.double().numpy().copy()
-    O.decoder_layer(ocfg(w, w.draft), olayer(w, w.draft, m["draft"]["layers"][2]), h, CTX, O.BIDIR,
-                    G.f64(eng.caches.dk[2][0]), G.f64(eng.caches.dv[2][0]))
-    G.assert_hidden_close(got, h)
+    eng.anchor.fill_(4321)
+    logits = torch.zeros(B - 1, w.vocab, device="cuda")
+    eng.draft(logits)
+    torch.cuda.synchronize()
+    assert eng.status() == D.DFLASH_OK
+    gd = eng.drafts[0].cpu().numpy()
+    gl = logits.cpu().numpy()
+    np.testing.assert_array_equal(gd, gl.argmax(-1))  # the fused argmax is the argmax of the logits
+    om = Hh.omodel(w, m)
+    rep = G.draft_parity(O, om, eng, 0, gl, gd)
+    print("PARITY qwen3-8b draft block:", {k: v for k, v in rep.items() if k != "layers"},
+          "layer h err", [round(L["h"], 7) for L in rep["layers"]])
 
 
 def test_fullsize_fusion(big):
@@ -139,3 +144,12 @@ def test_fullsize_verify_accept(big):
     if excluded == 0:
         assert k == 9
     np.testing.assert_allclose(eng.margin[0].cpu().numpy(), mg, rtol=0, atol=1e-3)
+    # the verification logits themselves, at the stated bound
+    logits = torch.zeros(B, w.vocab, device="cuda")
+    eng.base_pos.fill_(CTX)
+    eng.verify(B, eng.drafts, logits)
+    torch.cuda.synchronize()
+    _, _, lg = O.lm_head_argmax(tc, synth.to_numpy(m["lm_head"]), x, want_logits=True)
+    err = float(np.abs(logits.cpu().numpy() - lg).max())
+    assert err <= G.LOGIT_TOL["bf16"], f"verification logits differ by {err}"
+    print("PARITY qwen3-8b verify logits max err", err)

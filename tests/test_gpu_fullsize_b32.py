@@ -53,7 +53,9 @@ def test_b32_causal_layer(b32):
     eng.h[:S * B].copy_(h0.cuda())
     kc = {s: G.f64(eng.caches.tk[0][s]) for s in SAMPLED}
     vc = {s: G.f64(eng.caches.tv[0][s]) for s in SAMPLED}
-    D.dflash_decoder_layer_forward(eng.target_layer_args(0, B, eng.h), eng.ws_ptr, eng.ws_bytes)
+    bufs = G.stage_buffers(w.target, S, B, bidir=False)
+    D.dflash_decoder_layer_forward(G.attach_stages(eng.target_layer_args(0, B, eng.h), bufs), eng.ws_ptr,
+                                   eng.ws_bytes)
     torch.cuda.synchronize()
     assert eng.status() == D.DFLASH_OK
     got = eng.h[:S * B].clone()
@@ -63,9 +65,12 @@ def test_b32_causal_layer(b32):
                               n(L["ln1"]), n(L["ln2"]))
     kt, vt = eng.caches.tk[0], eng.caches.tv[0]
     for s in SAMPLED:
-        h = h0[s * B:(s + 1) * B].double().numpy().copy()
-        O.decoder_layer(ocfg(w, w.target), ol, h, ctx[s], O.CAUSAL, kc[s], vc[s])
-        G.assert_hidden_close(G.f64(got[s * B:(s + 1) * B]), h)
+        # every stage against the oracle fed the GPU's inputs to it
+        kr = G.f64(kt[s, :, ctx[s]:ctx[s] + B])
+        vr = G.f64(vt[s, :, ctx[s]:ctx[s] + B])
+        rep = G.check_layer_tf(O, ocfg(w, w.target), ol, h0[s * B:(s + 1) * B].double().numpy(), ctx[s], O.CAUSAL,
+                               kc[s], vc[s], G.gpu_stages(bufs, s, B, kr, vr), G.f64(got[s * B:(s + 1) * B]))
+        print(f"PARITY b32 causal layer, sequence {s} (context {ctx[s]}):", rep)
         # alone: the same rows from a one-sequence launch
         eng.h[:B].copy_(h0[s * B:(s + 1) * B].cuda())
         a = eng.target_layer_args(0, B, eng.h)

@@ -424,3 +424,60 @@ def test_cost_model_example(orc):
         assert abs(v - case["ms_per_token"]) <= case["abs_tol"]
     sp = g["baseline_ms_per_token"] / orc.per_token_cost_ms(g["t_draft_ms"], g["t_verify_ms"], 6)
     assert abs(sp - g["speedup_at_6"]) <= g["speedup_tol"]
+
+
+# ------------------------------------------------------ teacher-forced stages
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["causal", "bidir"])
+def test_layer_stages_open_for_teacher_forcing(orc, dtype, mode):
+    """decoder_layer_tf is decoder_layer with its stages open: with nothing
+    given it is the plain layer bit for bit, its stage outputs are the torch
+    restatement's intermediates (each named stage is the tensor its name
+    says), and feeding every stage its own value back changes nothing; a
+    given stage replaces the oracle's value (a perturbed attention output
+    moves the output by exactly the O projection of the perturbation)."""
+    w, om = _layer_setup(dtype)
+    causal = mode == "causal"
+    c = om.target.cfg if causal else om.draft.cfg
+    L = om.target.layers[0] if causal else om.draft.layers[0]
+    rng = np.random.default_rng(12)
+    P, M, cap = 7, 4, 16
+    kc = np.zeros((c.nkv, cap, c.d)); vc = np.zeros((c.nkv, cap, c.d))
+    ctx_k = orc.rnd(c, rng.standard_normal((P, c.nkv, c.d)))
+    ctx_v = orc.rnd(c, rng.standard_normal((P, c.nkv, c.d)))
+    for t in range(P):
+        kc[:, t] = ctx_k[t]; vc[:, t] = ctx_v[t]
+    h0 = rng.standard_normal((M, c.H))
+    mo = orc.CAUSAL if causal else orc.BIDIR
+    h_plain = h0.copy(); kp, vp = kc.copy(), vc.copy()
+    orc.decoder_layer(c, L, h_plain, P, mo, kp, vp)
+    h_tf = h0.copy(); kt, vt = kc.copy(), vc.copy()
+    st = orc.decoder_layer_tf(c, L, h_tf, P, mo, kt, vt)
+    np.testing.assert_array_equal(h_tf, h_plain)
+    np.testing.assert_array_equal(kt, kp)
+    ref = {}
+    if causal:
+        Hh.torch_layer(c, L, torch.from_numpy(h0), torch.arange(P, P + M), causal=True,
+                       past_k=torch.from_numpy(ctx_k), past_v=torch.from_numpy(ctx_v), stages=ref)
+    else:
+        Hh.torch_layer(c, L, torch.from_numpy(h0), torch.arange(P, P + M), ctx_k=torch.from_numpy(ctx_k),
+                       ctx_v=torch.from_numpy(ctx_v), causal=False, stages=ref)
+    tol = 1e-10 if dtype == "f32" else 2e-2
+    for n in orc.STAGES:
+        np.testing.assert_allclose(st[n], ref[n].numpy(), rtol=0, atol=tol, err_msg=n)
+    h_again = h0.copy()
+    st2 = orc.decoder_layer_tf(c, L, h_again, P, mo, kc.copy(), vc.copy(), given=st)
+    np.testing.assert_array_equal(h_again, h_plain)
+    for n in orc.STAGES:
+        np.testing.assert_array_equal(st2[n], st[n], err_msg=n)
+    # a given attention output replaces the oracle's: the output moves by the
+    # O projection of the change, and the stages before it do not move
+    delta = np.zeros_like(st["o"]); delta[1, 3] = 0.5
+    h_pert = h0.copy()
+    st3 = orc.decoder_layer_tf(c, L, h_pert, P, mo, kc.copy(), vc.copy(),
+                               given={"o": st["o"] + delta, "x2": st["x2"], "act": st["act"]})
+    np.testing.assert_array_equal(st3["q"], st["q"])
+    wo = orc.wfloat(c, L.wo)
+    np.testing.assert_allclose(h_pert - h_plain, delta @ wo.T, rtol=0, atol=1e-12)
