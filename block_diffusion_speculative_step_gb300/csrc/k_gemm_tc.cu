@@ -89,12 +89,15 @@ __device__ __forceinline__ int run_of(long long p, long long T, int G) {
   return c;
 }
 
-// Partial slot of run c's piece of the tile that starts at tbeg.  A run is
-// contiguous, so only its first piece (slot 2c) and its last piece (slot
-// 2c + 1, when the run began in an earlier tile) can be parts of split
-// tiles: 2 slots per run, whatever the tile count.
-__device__ __forceinline__ size_t piece_slot(long long T, int G, int c, long long tbeg) {
-  return 2 * (size_t)c + (run_start(T, G, c) < tbeg ? 1u : 0u);
+// Partial slot of run c's piece of a tile.  A run is contiguous, so only its
+// first piece (slot 2c) and its last piece (slot 2c + 1, when the run began
+// in an earlier tile) can be parts of split tiles: 2 slots per run, whatever
+// the tile count.  Of the runs first..last covering a tile, only `first` can
+// have begun in an earlier tile (first_tail: run_start(first) < the tile's
+// first k-block), so the slots need one 64-bit division per tile, not one
+// per piece.
+__device__ __forceinline__ size_t piece_slot(int c, int first, bool first_tail) {
+  return 2 * (size_t)c + ((c == first && first_tail) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort) {
@@ -687,6 +690,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         if (*s_flag) {
           const int first = run_of(tbeg, L.T, L.G);
           const int last = run_of(tend - 1, L.T, L.G);
+          const bool first_tail = run_start(L.T, L.G, first) < tbeg;
           for (int c0 = 0; c0 < ncol; c0 += 16) {
             float v[16];
             float pre[32];
@@ -704,7 +708,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const int c = sb + q <= last ? sb + q : last;
-                const float* src = L.part + piece_slot(L.T, L.G, c, tbeg) * BN * 128 + (size_t)c0 * 128 + r;
+                const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128 + (size_t)c0 * 128 + r;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
               }
@@ -758,7 +762,8 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
   const int t = (int)(blockIdx.x / nch), c0 = (int)(blockIdx.x % nch) * 16;
   const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
   const int first = run_of(tbeg, L.T, L.G), last = run_of(tend - 1, L.T, L.G);
-  if (first == last) return;  // one run covers the tile: finished inline (uniform over the CTA)
+  if (first == last) return;
+  const bool first_tail = run_start(L.T, L.G, first) < tbeg;  // one run covers the tile: finished inline (uniform over the CTA)
   const int r = threadIdx.x, lane = r & 31;
   // the partial slots first: they depend on nothing below
   float v[16];
@@ -794,7 +799,7 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int c = sb + q <= last ? sb + q : last;
-      const float* src = L.part + piece_slot(L.T, L.G, c, tbeg) * BN * 128 + (size_t)c0 * 128 + r;
+      const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128 + (size_t)c0 * 128 + r;
 #pragma unroll
       for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
     }

@@ -44,12 +44,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // caller then raises ST_TIMEOUT and unwinds; see wait_limit_ns).  `abort`
 // (shared) lets one role release the others early.  try_wait suspends the
 // thread in hardware until the phase completes or a short time slice passes,
-// so the clock and the abort flag are only consulted every 64 polls.
+// so the clock and the abort flag are only consulted every 256 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 255u) == 0) {
       if (abort && *abort) return false;
       const uint64_t now = global_ns();
       if (t0 == 0) t0 = now;

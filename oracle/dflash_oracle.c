@@ -952,6 +952,17 @@ int or_spec_sample_accept_sparse(int B, int V, const float* tl, const unsigned c
   return k;
 }
 
+/* Threads the OpenMP loops use from now on (the CPU baseline is timed at one
+ * thread and at all cores); the loops are parallel over independent output
+ * rows with every reduction serial, so results do not depend on it. */
+void or_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 int or_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

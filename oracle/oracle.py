@@ -107,6 +107,7 @@ def lib():
                                          C.POINTER(C.c_float), C.c_void_p, C.c_void_p, C.c_void_p,
                                          C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int), dp]
             L.or_num_threads.restype = C.c_int
+            L.or_set_threads.argtypes = [C.c_int]
             u32p = C.POINTER(C.c_uint32)
             L.or_philox4x32_10.argtypes = [u32p, u32p, u32p]
             L.or_uniform.restype = C.c_double
@@ -586,6 +587,12 @@ def speculative_generate(m: Model, prompt, n_new: int, cap: int, drafter=None):
         P += k + 1
         anchor = int(emitted[-1])
     return np.array(out[:n_new], dtype=np.int32), accepts
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (results do not
+    depend on it)."""
+    lib().or_set_threads(int(n))
 
 
 def threads() -> int:
