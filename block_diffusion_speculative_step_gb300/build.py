@@ -12,6 +12,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdflash.so")
+# The checked variant: device bounds assertions (DFLASH_CHECKED) that report
+# through the status word instead of trapping.
+LIB_CHECKED = os.path.join(OUT_DIR, "libdflash_checked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 NVCC = os.environ.get("NVCC", "nvcc")
@@ -29,16 +32,16 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
-    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool, checked: bool = False) -> str:
+    obj = os.path.join(OUT_DIR, os.path.basename(src) + (".checked.o" if checked else ".o"))
+    cmd = [NVCC, *ARCH, *FLAGS, *(["-DDFLASH_CHECKED"] if checked else []), "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -49,21 +52,29 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ and link libdflash.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
-    srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+def _link(objs, lib: str) -> None:
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
            "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every .cu under csrc/ twice (the normal and the checked
+    variant, all in parallel) and link libdflash.so and
+    libdflash_checked.so; returns the normal library's path."""
+    if not force and up_to_date(LIB) and up_to_date(LIB_CHECKED):
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    srcs = _sources()
+    jobs = [(src, False) for src in srcs] + [(src, True) for src in srcs]
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], verbose, j[1]), jobs))
+    _link(objs[:len(srcs)], LIB)
+    _link(objs[len(srcs):], LIB_CHECKED)
     return LIB
 
 

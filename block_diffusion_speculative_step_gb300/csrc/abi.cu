@@ -575,6 +575,14 @@ extern "C" {
 
 int32_t dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
 
+int32_t dflash_build_flags(void) {
+#ifdef DFLASH_CHECKED
+  return DFLASH_BUILD_CHECKED;
+#else
+  return 0;
+#endif
+}
+
 const char* dflash_last_error(void) { return g_err; }
 
 int dflash_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin, dflash_stream_t stream) {
@@ -617,6 +625,7 @@ int dflash_read_status(void* ws, dflash_stream_t stream, int32_t* host_status) {
   *host_status = (v & ST_NUMERIC)   ? DFLASH_ERR_NUMERIC
                  : (v & ST_TIMEOUT) ? DFLASH_ERR_TIMEOUT
                  : (v & ST_RANGE)   ? DFLASH_ERR_INVALID_ARG
+                 : (v & ST_CHECK)   ? DFLASH_ERR_CHECK
                                     : DFLASH_OK;
   if (*host_status != DFLASH_OK) fail(*host_status, "device status word 0x%x", v);
   return DFLASH_OK;
@@ -641,8 +650,8 @@ int dflash_embed(const dflash_embed_args* a, void* ws, size_t ws_bytes, dflash_s
   rc = check_ws(ws, ws_bytes, kReservedBytes, "dflash_embed");
   if (rc) return rc;
   DF_LAUNCH((cudaStream_t)stream, TF_EMBED, 0,
-            launch_embed(a->dims.dtype, a->embed, a->dims.hidden, a->n_seqs, a->rows, a->first, a->rest,
-                         a->fill_token, a->h, (cudaStream_t)stream));
+            launch_embed(a->dims.dtype, a->embed, a->dims.hidden, a->dims.vocab, a->n_seqs, a->rows, a->first,
+                         a->rest, a->fill_token, a->h, header(ws).status, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
@@ -965,8 +974,8 @@ int dflash_draft_block(const dflash_draft_args* a, void* ws, size_t ws_bytes, df
   const int rounds = a->denoise_rounds > 1 ? a->denoise_rounds : 1;
   for (int r = 0; r < rounds; ++r) {
     DF_LAUNCH(st, TF_EMBED, 0,
-              launch_embed(d.dtype, a->embed, d.hidden, a->n_seqs, a->block, a->anchor, r == 0 ? nullptr : a->drafts,
-                           a->mask_token, s.h, st));
+              launch_embed(d.dtype, a->embed, d.hidden, d.vocab, a->n_seqs, a->block, a->anchor,
+                           r == 0 ? nullptr : a->drafts, a->mask_token, s.h, c.status, st));
     rc = draft_round(a, s, c, sms, st);
     if (rc) return rc;
   }

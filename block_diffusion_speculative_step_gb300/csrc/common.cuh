@@ -13,6 +13,7 @@ enum : uint32_t {
   ST_NUMERIC = 1u,  // NaN reached an argmax
   ST_TIMEOUT = 2u,  // a bounded wait gave up
   ST_RANGE = 4u,    // a token id (vocabulary) or KV page id (pool) read on the device was out of range
+  ST_CHECK = 8u,    // a device bounds assertion of the checked build failed (the access was skipped)
 };
 
 // Workspace header: status word + arrival counters of the last-CTA reductions.
@@ -31,6 +32,20 @@ constexpr int kCtrSample = 25600;  // sampling-mode slice arrivals, one per row 
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
+
+// Device bounds assertions of the checked build (compiled with
+// DFLASH_CHECKED): a failed one raises ST_CHECK in the status word and the
+// guarded access is skipped instead of trapping, so the context stays
+// usable.  In the normal build the condition is not evaluated.
+__device__ __forceinline__ bool check_bound(bool ok, uint32_t* status) {
+  if (!ok) raise_status(status, ST_CHECK);
+  return ok;
+}
+#ifdef DFLASH_CHECKED
+#define DFL_CHECK(cond, status) (::dfl::check_bound((cond), (status)))
+#else
+#define DFL_CHECK(cond, status) (true)
+#endif
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v);

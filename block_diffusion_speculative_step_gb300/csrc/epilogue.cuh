@@ -34,6 +34,9 @@ __host__ __device__ __forceinline__ void epi_unit_rows(const GemmDesc& g, int u,
 // so the per-element code never re-reads the (large) launch descriptor.
 struct Epi {
   int kind, seg_row0, d, half, QD, KD, nkv, kv_cap, kv_window, kv_slot_mode, rope_max_pos, inter, ldo, rows;
+  int M;             // token rows of the launch
+  long long kv_rows; // head-dim vectors the K/V destinations hold: (M / rows) * nkv * kv_cap
+  uint32_t* status;  // the checked build's bounds assertions report here (may be null)
   const int32_t* base_pos;
   const int32_t* valid;
   float* out_f32;
@@ -60,6 +63,9 @@ __device__ __forceinline__ Epi make_epi(const GemmDesc& g, int seg) {
   e.inter = g.inter;
   e.ldo = g.ldo;
   e.rows = g.rows;
+  e.M = g.M;
+  e.kv_rows = g.rows > 0 ? (long long)(g.M / g.rows) * g.nkv * g.kv_cap : 0;
+  e.status = nullptr;
   e.base_pos = g.base_pos;
   e.valid = g.valid;
   e.out_f32 = g.out_f32;
@@ -133,6 +139,7 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int u, int m, float va, f
   else
     slot = idx;
   if (slot >= e.kv_cap) return;
+  if (!DFL_CHECK(((long long)s_idx * e.nkv + head) * e.kv_cap + slot < e.kv_rows, e.status)) return;
   T* dst = reinterpret_cast<T*>(is_k ? e.k_dst : e.v_dst) + (((size_t)s_idx * e.nkv + head) * e.kv_cap + slot) * d + col;
   dst[0] = from_f<T>(va);
   dst[half] = from_f<T>(vb);
@@ -254,7 +261,7 @@ __device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, const fl
   if (ra < e.QD) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if ((rw.inpos >> j) & 1u) {
+      if (((rw.inpos >> j) & 1u) && DFL_CHECK(c0 + j < e.M, e.status)) {
         T* q = reinterpret_cast<T*>(e.q_out) + (size_t)(c0 + j) * e.QD + ra;
         q[0] = from_f<T>(lo[j]);
         q[half] = from_f<T>(hi[j]);
@@ -267,6 +274,7 @@ __device__ __forceinline__ void epi_pair16(const Epi& e, int u, int c0, const fl
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (rw.kvr[j] == ~0u) continue;
+    if (!DFL_CHECK((long long)rw.kvr[j] + (long long)(r / d) * e.kv_cap < e.kv_rows, e.status)) continue;
     T* dst = base + (size_t)rw.kvr[j] * d;
     dst[0] = from_f<T>(lo[j]);
     dst[half] = from_f<T>(hi[j]);

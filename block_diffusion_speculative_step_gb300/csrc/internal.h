@@ -203,8 +203,8 @@ inline size_t path_proj_floats(int S, int block, int topk, int rank) {
 
 // elementwise
 cudaError_t launch_rope_table(float theta, int d, int max_pos, float* cs, cudaStream_t st);
-cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, const int32_t* first,
-                         const int32_t* rest, int fill, float* h, cudaStream_t st);
+cudaError_t launch_embed(int dtype, const void* E, int H, int V, int n_seqs, int rows, const int32_t* first,
+                         const int32_t* rest, int fill, float* h, uint32_t* status, cudaStream_t st);
 cudaError_t launch_rmsnorm(int dtype, const float* h, const void* g, int M, int H, float eps,
                            void* x_out, cudaStream_t st);
 cudaError_t launch_to_f32(int dtype, const void* src, size_t n, float* dst, cudaStream_t st);

@@ -323,7 +323,7 @@ __device__ __forceinline__ uint32_t kv_off(int j, int ch) {
 template <int D>
 __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, float* scratch, int NC, int rank,
                                            int nq_tile, int qv0, int grp, int g, int s, int rows, int QD,
-                                           void* out) {
+                                           void* out, uint32_t* status) {
   constexpr int PST = D + 4;
   const int RP = (nq_tile + NC - 1) / NC;
   const int q_lo = rank * RP;
@@ -371,6 +371,7 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
     const float L = Ls[i];
     const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
+    if (!DFL_CHECK(row < rows && head * D + e4 + 4 <= QD, status)) continue;
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
     dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
     dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
@@ -389,7 +390,7 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
 template <int D>
 __device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* psm, float* recv, int NC, int E,
                                            int rank, int nq_tile, int qv0, int grp, int g, int s, int rows, int QD,
-                                           void* out) {
+                                           void* out, uint32_t* status) {
   constexpr int PST = D + 4;
   const int NL = NC * E;
   const int RP = (nq_tile + NL - 1) / NL;
@@ -428,6 +429,7 @@ __device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* p
     }
     const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
+    if (!DFL_CHECK(row < rows && head * D + e4 + 4 <= QD, status)) continue;
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
     dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
     dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
@@ -751,7 +753,7 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
   }
   cl.sync();
 
-  rank_merge<D>(cl, psm, qsm, NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
+  rank_merge<D>(cl, psm, qsm, NC, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out, status);
   cl.sync();  // peers keep their shared memory until every rank has read it
 }
 
@@ -1230,7 +1232,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   }
   cl.sync();  // every rank's chunks are done: its K/V buffers may receive
   // recv follows the E partials (E = 2: 67.6 KB + 76 KB, inside the K/V, Q and P space)
-  push_merge<D>(cl, psm, psm + (size_t)E * kClQT * PST, NC, E, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out);
+  push_merge<D>(cl, psm, psm + (size_t)E * kClQT * PST, NC, E, rank, nq_tile, qv0, grp, g, s, rows, QD, a.out,
+                 status);
 }
 
 // ------------------------------------------------------------------- host

@@ -52,31 +52,37 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
 constexpr int kRowThreads = 256;
 constexpr int kRowVec = 8;  // 4-element groups per thread: rows up to 8192 elements stay in registers
 
-// h[m][:] = E[token(m)][:] as fp32 (4 elements per access).
+// h[m][:] = E[token(m)][:] as fp32 (4 elements per access).  A token id
+// outside [0, V) raises the range status and reads row 0 instead, so no
+// access leaves the table.
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) embed_kernel(const T* __restrict__ E, int H, int rows,
+__global__ void __launch_bounds__(kRowThreads) embed_kernel(const T* __restrict__ E, int H, int V, int rows,
                                                             const int32_t* __restrict__ first,
                                                             const int32_t* __restrict__ rest, int fill,
-                                                            float* __restrict__ h) {
+                                                            float* __restrict__ h, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   const int m = blockIdx.x;
   const int s = m / rows, i = m % rows;
-  const int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
+  int tok = (i == 0) ? first[s] : (rest ? rest[s * (rows - 1) + i - 1] : fill);
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) raise_status(status, ST_RANGE);
+    tok = 0;
+  }
   const T* e = E + (size_t)tok * H;
   float* o = h + (size_t)m * H;
   for (int k = 4 * threadIdx.x; k < H; k += 4 * kRowThreads) st4(o + k, ld4(e + k));
 }
 
-cudaError_t launch_embed(int dtype, const void* E, int H, int n_seqs, int rows, const int32_t* first,
-                         const int32_t* rest, int fill, float* h, cudaStream_t st) {
+cudaError_t launch_embed(int dtype, const void* E, int H, int V, int n_seqs, int rows, const int32_t* first,
+                         const int32_t* rest, int fill, float* h, uint32_t* status, cudaStream_t st) {
   int M = n_seqs * rows;
   if (M == 0) return cudaSuccess;
   if (dtype == DFLASH_BF16)
     return launch_pdl(embed_kernel<__nv_bfloat16>, dim3(M), dim3(kRowThreads), 0, st, (const __nv_bfloat16*)E,
-                      H, rows, first, rest, fill, h);
-  return launch_pdl(embed_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, (const float*)E, H, rows, first, rest,
-                    fill, h);
+                      H, V, rows, first, rest, fill, h, status);
+  return launch_pdl(embed_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, (const float*)E, H, V, rows, first,
+                    rest, fill, h, status);
 }
 
 // x[m] = round(h[m] * rsqrt(mean(h[m]^2) + eps) * g), one block per row, the

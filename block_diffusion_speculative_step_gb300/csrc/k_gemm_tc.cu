@@ -408,7 +408,7 @@ __device__ __forceinline__ void final_wide(const TcLocal& L, const Epi& e, const
   if (ra < e.QD) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (tb->pos[c0 + j] >= 0) {
+      if (tb->pos[c0 + j] >= 0 && DFL_CHECK(c0 + j < e.M, e.status)) {
         __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(e.q_out) + (size_t)(c0 + j) * e.QD + ra;
         q[0] = from_f<__nv_bfloat16>(lo[j]);
         q[half] = from_f<__nv_bfloat16>(hi[j]);
@@ -423,6 +423,7 @@ __device__ __forceinline__ void final_wide(const TcLocal& L, const Epi& e, const
   for (int j = 0; j < 16; ++j) {
     const uint32_t kv = tb->kvr[c0 + j];
     if (kv == ~0u) continue;
+    if (!DFL_CHECK((long long)kv + (long long)(rr / d) * e.kv_cap < e.kv_rows, e.status)) continue;
     __nv_bfloat16* dst = base + (size_t)kv * d;
     dst[0] = from_f<__nv_bfloat16>(lo[j]);
     dst[half] = from_f<__nv_bfloat16>(hi[j]);
@@ -603,6 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       const int t = (int)(p0 / nkb);
       seg_built = t / L.tps;
       e = make_epi(p.g, seg_built);
+      e.status = L.status;
       if constexpr (Cfg::WIDE) {
         row_tab_build(e, L.M, et, tab);
       } else {
@@ -622,6 +624,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       if (L.mode == TC_GEMM && t / L.tps != seg_built) {
         seg_built = t / L.tps;
         e = make_epi(p.g, seg_built);
+        e.status = L.status;
+      e.status = L.status;
       }
       if (!tc::mbar_wait(&accf[b], (uint32_t)(k >> 1) & 1u, abort, lim)) tc_timeout(L.status, abort);
       tc::named_bar(1, 128);
@@ -633,7 +637,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
       for (int j = 0; j < 16; ++j) old_next[j] = 0.f;
       if (!Cfg::WIDE && L.mode == TC_GEMM && end < p1) {
         const int t2 = (int)(end / nkb);
-        const Epi e2 = (t2 / L.tps != seg_built) ? make_epi(p.g, t2 / L.tps) : e;
+        Epi e2 = (t2 / L.tps != seg_built) ? make_epi(p.g, t2 / L.tps) : e;
+        e2.status = L.status;
         int unit2 = 0;
         if (tc_unit(L, t2, r, unit2)) epi_preload_tile(e2, unit2, 0, rows, old_next);
       }
@@ -769,7 +774,8 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
   float v[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = 0.f;
-  const Epi e = make_epi(p.g, t / L.tps);
+  Epi e = make_epi(p.g, t / L.tps);
+  e.status = L.status;
   // row operands of the 32-row word holding the chunk (warp 0)
   if (r < 32) {
     const int m = (c0 & ~31) + lane;

@@ -16,6 +16,7 @@ DFLASH_ERR_WORKSPACE = -3
 DFLASH_ERR_CUDA = -4
 DFLASH_ERR_TIMEOUT = -5
 DFLASH_ERR_NUMERIC = -6
+DFLASH_ERR_CHECK = -7
 
 DFLASH_F32 = 0
 DFLASH_BF16 = 1
@@ -31,7 +32,7 @@ EXPORTS = ("dflash_rope_table", "dflash_embed", "dflash_decoder_layer_forward", 
            "dflash_workspace_init", "dflash_read_status", "dflash_last_error", "dflash_abi_version",
            "dflash_trace_begin", "dflash_trace_pause", "dflash_trace_read", "dflash_trace_end",
            "dflash_verify_accept_noalloc", "dflash_trace_launches", "dflash_sample_drafts",
-           "dflash_sample_accept", "dflash_workspace_control")
+           "dflash_sample_accept", "dflash_workspace_control", "dflash_build_flags")
 DFLASH_TRACE_FAMILIES = 13
 
 
@@ -130,10 +131,11 @@ _lib = None
 
 
 def lib(path: str | None = None):
-    """Load libdflash.so (built in-tree by __graft_entry__.build())."""
+    """Load libdflash.so (built in-tree by __graft_entry__.build()), or the
+    checked variant libdflash_checked.so when DFLASH_LIB=checked is set."""
     global _lib
     if _lib is None:
-        path = path or _build.LIB
+        path = path or (_build.LIB_CHECKED if os.environ.get("DFLASH_LIB") == "checked" else _build.LIB)
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: build the CUDA library first (__graft_entry__.build())")
         L = C.CDLL(path)
@@ -153,6 +155,7 @@ def lib(path: str | None = None):
         L.dflash_read_status.restype = C.c_int
         L.dflash_last_error.restype = C.c_char_p
         L.dflash_abi_version.restype = i32
+        L.dflash_build_flags.restype = i32
         L.dflash_trace_begin.argtypes = [i32]
         L.dflash_verify_accept_noalloc.argtypes = [vp, vp, vp]
         L.dflash_verify_accept_noalloc.restype = C.c_int
@@ -173,6 +176,13 @@ def _stream(stream) -> int:
         import torch
         return torch.cuda.current_stream().cuda_stream
     return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+DFLASH_BUILD_CHECKED = 1
+
+
+def dflash_build_flags() -> int:
+    return int(lib().dflash_build_flags())
 
 
 def dflash_abi_version() -> int:

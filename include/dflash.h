@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_ABI_VERSION 7
+#define DFLASH_ABI_VERSION 8
 #define DFLASH_MAX_LAYERS 16 /* draft layers handled by one fuse / draft call */
 
 typedef struct CUstream_st* dflash_stream_t; /* == cudaStream_t */
@@ -64,7 +64,8 @@ typedef enum {
   DFLASH_ERR_WORKSPACE = -3,   /* ws_bytes below dflash_workspace_bytes */
   DFLASH_ERR_CUDA = -4,        /* a CUDA runtime call failed */
   DFLASH_ERR_TIMEOUT = -5,     /* a bounded device wait gave up (status word) */
-  DFLASH_ERR_NUMERIC = -6      /* NaN reached an argmax (status word) */
+  DFLASH_ERR_NUMERIC = -6,     /* NaN reached an argmax (status word) */
+  DFLASH_ERR_CHECK = -7        /* a device bounds assertion of the checked build failed (status word) */
 } dflash_status;
 
 typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
@@ -150,7 +151,8 @@ int dflash_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos
  * draft reuses the target's embedding and LM head).  Row i of sequence s
  * takes token first[s] for i == 0 and rest[s*(rows-1) + i-1] for i >= 1,
  * or fill_token when rest == NULL (the draft's mask tokens).
- * h[M][H] (fp32) receives the embedding rows.
+ * h[M][H] (fp32) receives the embedding rows.  A token id outside [0, V)
+ * raises DFLASH_ERR_INVALID_ARG in the status word (its row reads token 0).
  */
 typedef struct {
   dflash_dims dims;
@@ -560,6 +562,18 @@ int dflash_verify_accept_noalloc(const dflash_verify_args* a, int32_t* status_ou
 const char* dflash_last_error(void);
 
 int32_t dflash_abi_version(void);
+
+/*
+ * Build variant.  The library is also built as libdflash_checked.so, with
+ * device bounds assertions on the addresses its kernels compute (K/V cache
+ * and query destinations of the projection epilogues, the attention's output
+ * rows): a failed assertion raises DFLASH_ERR_CHECK in the status word and
+ * skips the access instead of trapping.  Results are otherwise identical.
+ * Independent of the variant, token ids and KV page ids read on the device
+ * are always checked (DFLASH_ERR_INVALID_ARG).
+ */
+#define DFLASH_BUILD_CHECKED 1
+int32_t dflash_build_flags(void);
 
 #ifdef __cplusplus
 }

@@ -156,3 +156,18 @@ def test_noalloc_checks_arguments_first(D):
     v.drafts = 0
     assert L.dflash_verify_accept_noalloc(C.byref(v), None, None) == D.DFLASH_ERR_INVALID_ARG
     assert "drafts" in D.dflash_last_error()
+
+
+def test_checked_variant_builds_and_exports(D):
+    """libdflash_checked.so is built next to the normal library, exports the
+    same functions and reports itself as the checked variant."""
+    from block_diffusion_speculative_step_gb300 import build
+    assert os.path.exists(build.LIB_CHECKED)
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_CHECKED], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for name in header_functions():
+        assert name in exported, name
+    chk = C.CDLL(build.LIB_CHECKED)
+    chk.dflash_build_flags.restype = C.c_int32
+    assert chk.dflash_build_flags() == D.DFLASH_BUILD_CHECKED
+    assert D.dflash_build_flags() == 0
