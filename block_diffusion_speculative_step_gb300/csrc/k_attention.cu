@@ -879,7 +879,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   auto chunk_of = [&](int i) { return i < nA ? rank + i * NL : rB + (i - nA) * NL; };
 
   const KvMap km{a.pages, cap, a.ps, a.max_pages, a.pool, nkv};
-  const uint64_t lim = wait_limit_ns(status);
+  const uint64_t lim_ns = wait_limit_ns(status);  // (lim is the causal key limit below)
   const bool stall = stall_kv_loads(status);  // test switch: issue no K/V copy
   auto chunk_row = [&](int c, bool& blk) -> int {
     blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == sk.n_ctx_ch);
@@ -980,7 +980,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // ---------------- K/V producer: chunk i into buffer i & 1 once P V of chunk i-2 is done
       int issued = stall ? 0 : (nmine < 2 ? nmine : 2);  // this thread issued chunks 0 and 1 above
       for (int i = 2; i < nmine; ++i) {
-        if (!tc::mbar_wait(&empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, lim)) {
+        if (!tc::mbar_wait(&empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, lim_ns)) {
           raise_status(status, ST_TIMEOUT);
           *abort = 1;
           break;
@@ -991,8 +991,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // Every copy this CTA issued has landed before its shared memory goes
       // away, also when a wait gave up (the last copy into each buffer).
       for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-        tc::mbar_wait(&full[i & 1], (uint32_t)(i >> 1) & 1u, nullptr, lim);
-      if (p.q_tma) tc::mbar_wait(qfull, 0u, nullptr, lim);
+        tc::mbar_wait(&full[i & 1], (uint32_t)(i >> 1) & 1u, nullptr, lim_ns);
+      if (p.q_tma) tc::mbar_wait(qfull, 0u, nullptr, lim_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -1001,7 +1001,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       constexpr uint32_t idV = tc::idesc_bf16_f32_bmn(kTcAttnRows, D);
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
-        if (ok && !tc::mbar_wait(bar, par, abort, lim)) {
+        if (ok && !tc::mbar_wait(bar, par, abort, lim_ns)) {
           raise_status(status, ST_TIMEOUT);
           *abort = 1;
           ok = false;
@@ -1084,7 +1084,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       const int nk = blk ? min(rows, CH) : min(CH, sk.n_ctx - c * CH);
       const bool causal = mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
       const int lim = causal ? P + row_tok - slot0 : CH;
-      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort, lim)) {
+      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort, lim_ns)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;
@@ -1127,7 +1127,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       xs[piece * 64 + qr] = sum;
       // P has one buffer: the P V products of the chunk before must have
       // finished reading it (S of this chunk was issued ahead of them).
-      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim)) {
+      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim_ns)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;
@@ -1182,7 +1182,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
     }
     // ---- this CTA's partial of its 64 rows (lanes 0..63, OC columns per thread)
     if (o_owner && nmine > 0) {
-      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort, lim)) {
+      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort, lim_ns)) {
         raise_status(status, ST_TIMEOUT);
         *abort = 1;
         ok = false;

@@ -94,13 +94,16 @@ STAGE_ULP_FRAC = 0.02  # share of a bf16 stage's elements that may sit one bf16 
 def check_stage(name, got, ref, frac=STAGE_ULP_FRAC):
     """A bf16 stage output against the oracle's value computed from the same
     inputs.  Each element is within one bf16 step of max(|got|, |ref|) plus
-    1e-5 of the stage's RMS (the fp32-vs-fp64 error of the sum behind a value
-    that cancels to near zero), and at most `frac` of the elements differ at
-    all (an fp32 sum on the other side of a rounding boundary)."""
+    5e-5 of the stage's RMS, and at most `frac` of the elements differ at all
+    (an fp32 sum on the other side of a rounding boundary).  The absolute
+    term is the fp32 error of the sum behind a value that cancels to near
+    zero: the tensor cores' fp32 sums of K = 4096 .. 14336 products carry
+    errors of up to ~1e-5 of the products' scale (measured 1.3e-5 on a
+    SwiGLU product of size 3e-4), which no relative bound covers."""
     got, ref = np.asarray(got, dtype=np.float64), np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     rms = float(np.sqrt((ref ** 2).mean())) if ref.size else 0.0
-    tol = bf16_ulp(np.maximum(np.abs(got), np.abs(ref))) + 1e-5 * rms
+    tol = bf16_ulp(np.maximum(np.abs(got), np.abs(ref))) + 5e-5 * rms
     d = np.abs(got - ref)
     bad = d > tol
     if bad.any():
