@@ -27,6 +27,7 @@ constexpr int kCtrGemm = 0;        // 8192 tiles
 constexpr int kCtrAttn = 8192;     // 16384 (seq, head, query-tile) groups
 constexpr int kCtrHead = 24576;    // LM-head reduction (1)
 constexpr int kCtrHeadEnd = 24577;
+constexpr int kCtrAttnGrid = 24592;  // streaming attention's grid barrier: count, generation
 constexpr int kCtrSample = 25600;  // sampling-mode slice arrivals, one per row (<= 1024)
 
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) {

@@ -100,6 +100,22 @@ __device__ __forceinline__ SeqKeys seq_keys(const AttnDesc& a, int P, int grid_c
   return k;
 }
 
+// The key chunks of a sequence whose block starts at position P (the tensor-core
+// kernels read the cache up to its capacity; 128-key chunks).
+__device__ __forceinline__ SeqKeys tc_seq_keys(const AttnDesc& a, int P) {
+  SeqKeys k;
+  if (a.mode == DFLASH_ATTN_CAUSAL) {
+    k.n_ctx = min(max(P + a.rows, 0), a.cap);
+    k.n_ctx_ch = (k.n_ctx + kMmaCH - 1) / kMmaCH;
+    k.n_ch = k.n_ctx_ch;
+  } else {
+    k.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), a.cap);
+    k.n_ctx_ch = (k.n_ctx + kMmaCH - 1) / kMmaCH;
+    k.n_ch = k.n_ctx_ch + 1;
+  }
+  return k;
+}
+
 // Keys of chunk c: base pointers, count, first slot.
 template <typename T>
 __device__ __forceinline__ void chunk_keys(const AttnDesc& a, const SeqKeys& sk, int s, int g, int c, int CH,
@@ -378,6 +394,73 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
   }
 }
 
+// One output quad (columns e4 .. e4+3) of a query row: the NL logical-rank
+// partials merged in rank order, o the weighted sum, L the weighted
+// denominator.  part(r) gives rank r's partial row (O[D], then m and l, log2
+// units), or null for a rank that had no chunks, which counts as m = -inf,
+// l = 0 and O = 0 -- the values such a rank's partial holds.  CG: the
+// partials are in global memory, written by other SMs (loads bypass L1).
+template <bool CG>
+__device__ __forceinline__ float ld_part(const float* p) {
+  if constexpr (CG) return __ldcg(p);
+  else return *p;
+}
+template <bool CG>
+__device__ __forceinline__ float4 ld_part4(const float* p) {
+  if constexpr (CG) return __ldcg(reinterpret_cast<const float4*>(p));
+  else return *reinterpret_cast<const float4*>(p);
+}
+template <int D, bool CG, class Part>
+__device__ __forceinline__ void merge_quad(int NL, Part part, int e4, float (&o)[4], float& L) {
+  // Loads are issued in batches (every rank's m, then l and O of eight ranks
+  // at a time) so that loads of global partials are in flight together; the
+  // arithmetic runs in rank order.
+  constexpr int G = 8;
+  float mr[kMaxNC];
+#pragma unroll
+  for (int r = 0; r < kMaxNC; ++r) {
+    const float* pr = r < NL ? part(r) : nullptr;
+    mr[r] = pr ? ld_part<CG>(pr + D) : -INFINITY;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < kMaxNC; ++r)
+    if (r < NL) M = fmaxf(M, mr[r]);
+  L = 0.f;
+  o[0] = o[1] = o[2] = o[3] = 0.f;
+#pragma unroll
+  for (int r0 = 0; r0 < kMaxNC; r0 += G) {
+    if (r0 >= NL) break;
+    float lr[G];
+    float4 v[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float* pr = r0 + j < NL ? part(r0 + j) : nullptr;
+      lr[j] = pr ? ld_part<CG>(pr + D + 1) : 0.f;
+      v[j] = pr ? ld_part4<CG>(pr + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      if (r0 + j < NL) {
+        const float mj = mr[r0 + j];
+        const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+        L = fmaf(lr[j], w, L);
+        o[0] = fmaf(v[j].x, w, o[0]);
+        o[1] = fmaf(v[j].y, w, o[1]);
+        o[2] = fmaf(v[j].z, w, o[2]);
+        o[3] = fmaf(v[j].w, w, o[3]);
+      }
+    }
+  }
+}
+
+// The normalised quad, rounded to bf16 (a row that saw no key gives zeros).
+__device__ __forceinline__ void store_quad(__nv_bfloat16* dst, const float (&o)[4], float L) {
+  __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(dst);
+  d2[0] = __floats2bfloat162_rn(L > 0.f ? o[0] / L : 0.f, L > 0.f ? o[1] / L : 0.f);
+  d2[1] = __floats2bfloat162_rn(L > 0.f ? o[2] / L : 0.f, L > 0.f ? o[3] / L : 0.f);
+}
+
 // The same merge with the partials pushed instead of pulled: after a
 // cluster barrier (every rank's chunks done, its K/V buffers free), each
 // rank stores its partial rows into their owner's shared memory (recv, on
@@ -413,26 +496,12 @@ __device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* p
   __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(out);
   for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
     const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
-    float M = -INFINITY;
-    for (int r = 0; r < NL; ++r) M = fmaxf(M, rv[((size_t)r * RP + i) * PST + D]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int r = 0; r < NL; ++r) {
-      const float* pr = rv + ((size_t)r * RP + i) * PST;
-      const float mr = pr[D];
-      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
-      L = fmaf(pr[D + 1], w, L);
-      const float4 v = *reinterpret_cast<const float4*>(pr + e4);
-      o0 = fmaf(v.x, w, o0);
-      o1 = fmaf(v.y, w, o1);
-      o2 = fmaf(v.z, w, o2);
-      o3 = fmaf(v.w, w, o3);
-    }
+    float o[4], L;
+    merge_quad<D, false>(NL, [&](int r) { return rv + ((size_t)r * RP + i) * PST; }, e4, o, L);
     const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
     if (!DFL_CHECK(row < rows && head * D + e4 + 4 <= QD, status)) continue;
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4);
-    dst[0] = __floats2bfloat162_rn(L > 0.f ? o0 / L : 0.f, L > 0.f ? o1 / L : 0.f);
-    dst[1] = __floats2bfloat162_rn(L > 0.f ? o2 / L : 0.f, L > 0.f ? o3 / L : 0.f);
+    store_quad(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + e4, o, L);
   }
   }
 }
@@ -859,16 +928,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
   // base_pos is written only by the acceptance step, never by the kernel that
   // precedes attention inside a call, so it may be read before the PDL wait.
   const int P = a.base_pos[s];
-  SeqKeys sk;
-  if (mode == DFLASH_ATTN_CAUSAL) {
-    sk.n_ctx = min(max(P + rows, 0), cap);
-    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
-    sk.n_ch = sk.n_ctx_ch;
-  } else {
-    sk.n_ctx = min(max(a.window > 0 ? min(P, a.window) : P, 0), cap);
-    sk.n_ctx_ch = (sk.n_ctx + CH - 1) / CH;
-    sk.n_ch = sk.n_ctx_ch + 1;
-  }
+  const SeqKeys sk = tc_seq_keys(a, P);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qv0 = qt * kClQT;
   const int nq_tile = min(kClQT, nqv - qv0);
@@ -1236,6 +1296,708 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
                  status);
 }
 
+// ------------------------------------------------ tcgen05 streaming variant
+//
+// With more (sequence, KV head, query tile) items than clusters fit at once,
+// the same function runs as a grid of one CTA per SM without clusters.  The
+// work is cut into units, one per (item, logical rank): a unit is that
+// rank's chunks of the item under the split of the cluster kernels (NL
+// logical ranks, rank r owning chunks r, r + NL, ...), and the units are
+// ordered by item, then rank.  CTA b takes the units whose first chunk falls
+// in the b-th equal share of all the launch's chunks, so every CTA streams
+// about the same number of K/V chunks whatever the context lengths.  A unit
+// runs the online softmax of its logical rank from scratch; its partial
+// (O, m, l) goes from TMEM to the workspace, and the CTA that completes the
+// last unit of an item merges the item's NL partials in rank order with the
+// arithmetic of push_merge.  The outputs are therefore bit for bit those of
+// the cluster kernels.  The K/V pipeline runs on across unit and item
+// boundaries; the query tile is reloaded when the item changes (one buffer:
+// the load waits until the item's last S = Q K^T has completed).
+
+// A CTA's units walked chunk by chunk: every role keeps its own copy.
+struct UnitCursor {
+  const AttnDesc* a;
+  int ips, NL;          // items per sequence, logical ranks
+  int s, it, r, k;      // sequence, item of the sequence, logical rank, chunk of the rank
+  int P, nle, q, rem;   // block position; ranks with chunks; chunks per rank = q + (r < rem)
+  SeqKeys sk;
+  __device__ __forceinline__ void load() {
+    P = a->base_pos[s];
+    sk = tc_seq_keys(*a, P);
+    nle = min(NL, sk.n_ch);
+    q = sk.n_ch / NL;
+    rem = sk.n_ch - q * NL;
+  }
+  __device__ __forceinline__ int cnt() const { return q + (r < rem ? 1 : 0); }
+  __device__ __forceinline__ int chunk() const { return r + k * NL; }
+  __device__ __forceinline__ bool item_first() const { return k == 0 && r == 0; }
+  __device__ __forceinline__ bool item_last() const { return k + 1 == cnt() && r + 1 == nle; }
+  __device__ __forceinline__ int item() const { return s * ips + it; }
+  __device__ __forceinline__ void next() {
+    if (++k < cnt()) return;
+    k = 0;
+    if (++r < nle) return;
+    r = 0;
+    if (++it < ips) return;
+    it = 0;
+    if (++s < a->n_seqs) load();
+  }
+};
+
+// Chunks of sequence s over all its items.
+__device__ __forceinline__ long long seq_units_chunks(const AttnDesc& a, int s, int ips) {
+  return (long long)tc_seq_keys(a, a.base_pos[s]).n_ch * ips;
+}
+
+// The first unit whose first chunk is at or after chunk x of the launch's
+// chunk order: (s, it, r) and its first chunk t; s = n_seqs when there is
+// none (t is then the total).  Run by a whole warp, the same result in every
+// lane.
+__device__ void find_unit(const AttnDesc& a, int ips, int NL, long long x, int lane, int& s_out, int& it_out,
+                          int& r_out, long long& t_out) {
+  long long cum = 0;  // chunks of the sequences before s0
+  for (int s0 = 0; s0 < a.n_seqs; s0 += 32) {
+    const int sl = s0 + lane;
+    const long long v = sl < a.n_seqs ? seq_units_chunks(a, sl, ips) : 0;
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, sl < a.n_seqs && cum + incl > x);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const long long base = cum + __shfl_sync(0xffffffffu, incl - v, l);  // first chunk of sequence s
+      const int s = s0 + l;
+      const int n_ch = tc_seq_keys(a, a.base_pos[s]).n_ch;
+      const long long off = x - base;  // 0 <= off < n_ch * ips
+      int it = (int)(off / n_ch);
+      const int o2 = (int)(off - (long long)it * n_ch);
+      const int q = n_ch / NL, rem = n_ch - q * NL, nle = min(NL, n_ch);
+      int r = 0;
+      while (r < nle && r * q + min(r, rem) < o2) ++r;
+      if (r < nle) {
+        s_out = s;
+        it_out = it;
+        r_out = r;
+        t_out = base + (long long)it * n_ch + r * q + min(r, rem);
+      } else if (it + 1 < ips) {  // the next item's first unit
+        s_out = s;
+        it_out = it + 1;
+        r_out = 0;
+        t_out = base + (long long)(it + 1) * n_ch;
+      } else {  // the next sequence's first unit (or none)
+        s_out = s + 1;
+        it_out = 0;
+        r_out = 0;
+        t_out = base + (long long)ips * n_ch;
+      }
+      return;
+    }
+    cum += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  s_out = a.n_seqs;
+  it_out = 0;
+  r_out = 0;
+  t_out = cum;
+}
+
+// Threads of the streaming kernel: warp 0 loads K (and the query tiles),
+// warp 1 issues the MMAs, warps 2 .. 9 run the softmax, warp 10 loads V.
+constexpr int kTcStreamThreads = kTcAttnThreads + 32;
+#ifndef DFLASH_STREAM_PF
+#define DFLASH_STREAM_PF 4
+#endif
+constexpr int kStreamPF = DFLASH_STREAM_PF;  // chunks prefetched into L2 ahead of the shared-memory ring
+// One unit's partial (head dim 128): four blocks of 16 query rows, each
+// O [32 column quads][16 rows][4] then m[16], l[16] -- 8320 contiguous bytes,
+// one bulk copy in the merge.
+constexpr int kRbRows = 16;
+constexpr int kRbFloats = (128 + 2) * kRbRows;
+constexpr int kRbBytes = kRbFloats * 4;
+constexpr int kPartFloats = kRbFloats * (kClQT / kRbRows);
+constexpr int kTcStreamVWarp = kTcAttnThreads / 32;
+
+template <int D>
+__global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(const __grid_constant__ AttnTma p,
+                                                                             int n_qt, int NL) {
+  static_assert(D == 128, "two 64-dim boxes per row");
+  constexpr int CH = kMmaCH;
+  constexpr int TILE = CH * D * 2;
+  constexpr int KP = kTcAttnKP;
+  constexpr int OC = D / kTcAttnGroups;  // output columns per owner thread
+  static_assert(CH == 128 && OC % 64 == 0, "whole 64-column TMEM loads");
+  static_assert((D + 2) * kClQT == kPartFloats, "partial size");
+  static_assert(kRbBytes % 16 == 0, "bulk copies of whole 16-byte units");
+  extern __shared__ __align__(1024) uint8_t smem_att[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_att) + 1023) & ~uintptr_t(1023));
+  uint8_t* KV = sm;  // slot b: K at KV + 2*b*TILE, V at KV + (2*b+1)*TILE
+  uint8_t* Qs = KV + 4 * TILE;
+  uint8_t* Ph = Qs + kTcAttnRows * D * 2;
+  uint8_t* Pl = Ph + kTcAttnPloOff;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(Ph + kTcAttnPBytes);  // [2] K of a chunk landed
+  uint64_t* vfull = kfull + 2;                            // [2] V of a chunk landed
+  uint64_t* kempty = vfull + 2;                           // [2] S = Q K^T done: the K slot is free
+  uint64_t* vempty = kempty + 2;                          // [2] P V done: the V slot is free
+  uint64_t* sfull = vempty + 2;                           // [2] S in TMEM
+  uint64_t* pdone = sfull + 2;                            // [2] P written, O rescaled
+  uint64_t* ofull = pdone + 2;                            // P V done
+  uint64_t* qfull = ofull + 1;                            // query tile landed
+  uint64_t* qempty = qfull + 1;                           // the item's last S done: Q may be replaced
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(qempty + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+  int* sched = const_cast<int*>(abort) + 1;  // [4] first unit (s, it, r), chunk count; [4] last-arriver flag
+  // [2 chunk parities][pieces][64 rows] each
+  float* xmax = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(kfull) + 160);
+  float* xsum = xmax + 2 * kTcAttnPieces * 64;
+
+  const AttnDesc& a = p.a;
+  const int ips = a.nkv * n_qt;
+  const int mode = a.mode, rows = a.rows;
+  const int grp = a.nq / a.nkv;
+  const int nqv = rows * grp;
+  const int QD = a.nq * D;
+  uint32_t* status = a.status;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint64_t lim_ns = wait_limit_ns(status);
+  const bool stall = stall_kv_loads(status);  // test switch: issue no K/V copy
+  const KvMap km{a.pages, a.cap, a.ps, a.max_pages, a.pool, a.nkv};
+  float* part = a.partials;  // [items][NL][kPartFloats]
+
+  // ---- this CTA's units (base_pos is not written by the kernel before this
+  // one inside a call, so it may be read before the PDL wait)
+  if (warp == 0) {
+    long long T = 0;
+    for (int s0 = 0; s0 < a.n_seqs; s0 += 32) {
+      long long v = s0 + lane < a.n_seqs ? seq_units_chunks(a, s0 + lane, ips) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      T += v;
+    }
+    const long long lo = (long long)blockIdx.x * T / gridDim.x, hi = (long long)(blockIdx.x + 1) * T / gridDim.x;
+    int s0, it0, r0, s1, it1, r1;
+    long long t0, t1;
+    find_unit(a, ips, NL, lo, lane, s0, it0, r0, t0);
+    find_unit(a, ips, NL, hi, lane, s1, it1, r1, t1);
+    if (lane == 0) {
+      sched[0] = s0;
+      sched[1] = it0;
+      sched[2] = r0;
+      sched[3] = (int)(t1 - t0);
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&kfull[b], 1);
+      tc::mbar_init(&vfull[b], 1);
+      tc::mbar_init(&kempty[b], 1);
+      tc::mbar_init(&vempty[b], 1);
+      tc::mbar_init(&sfull[b], 1);
+      tc::mbar_init(&pdone[b], kTcAttnSoft);
+    }
+    tc::mbar_init(ofull, 1);
+    tc::mbar_init(qfull, 1);
+    tc::mbar_init(qempty, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&p.kc);
+    tc::tma_prefetch_desc(&p.vc);
+    tc::tma_prefetch_desc(&p.q3);
+  }
+  if (warp == 1) tc::tmem_alloc(tslot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const int nmine = sched[3];
+  UnitCursor start;
+  start.a = &a;
+  start.ips = ips;
+  start.NL = NL;
+  start.s = sched[0];
+  start.it = sched[1];
+  start.r = sched[2];
+  start.k = 0;
+  if (nmine > 0) start.load();
+
+  auto chunk_row = [&](const UnitCursor& u, bool& blk) -> int {
+    const int c = u.chunk(), g = u.it / n_qt;
+    blk = (mode == DFLASH_ATTN_BLOCK_BIDIR && c == u.sk.n_ctx_ch);
+    if (blk) return (u.s * a.nkv + g) * rows;
+    bool bad = false;
+    const int r = (int)(km.row0(u.s, c * CH, &bad) + (uint32_t)g * (uint32_t)km.head_rows());
+    if (bad) raise_status(status, ST_RANGE);  // read from page 0 instead
+    return r;
+  };
+  // One operand tile (K: v = 0, V: v = 1) of chunk u into slot buf; one thread.
+  auto issue = [&](const UnitCursor& u, int buf, int v) -> bool {
+    if (stall) return false;
+    bool blk;
+    const int row = chunk_row(u, blk);
+    const CUtensorMap* map = v ? (blk ? &p.vb : &p.vc) : (blk ? &p.kb : &p.kc);
+    uint64_t* bar = v ? &vfull[buf] : &kfull[buf];
+    uint8_t* dst = KV + (2 * buf + v) * TILE;
+    tc::mbar_arrive_expect_tx(bar, TILE);
+    const uint64_t pol = tc::policy_evict_first();
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(dst + h * (CH * 128), map, 64 * h, row, bar, pol);
+    return true;
+  };
+  // L2 prefetch of one operand tile of chunk u: the shared-memory ring is
+  // two chunks deep, so the loaders keep kStreamPF chunks ahead in L2, and
+  // the tiled loads then wait for L2 rather than HBM.  (L2 is the point of
+  // coherence: a prefetch before the PDL wait may be overwritten later by
+  // the kernel before this one, and the load still reads the new data.)
+  auto prefetch = [&](const UnitCursor& u, int v) {
+    bool blk;
+    const int row = chunk_row(u, blk);
+    const CUtensorMap* map = v ? (blk ? &p.vb : &p.vc) : (blk ? &p.kb : &p.kc);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) tc::tma_prefetch_l2_2d(map, 64 * h, row);
+  };
+  auto early_ok = [&](const UnitCursor& u) {
+    const int c = u.chunk();
+    return c < u.sk.n_ctx_ch && (mode == DFLASH_ATTN_BLOCK_BIDIR || (c + 1) * CH <= u.P);
+  };
+  // Context chunks that the kernel before this one does not write may load
+  // before the PDL wait: K by thread 0, V by the V loader.
+  const bool loader = (warp == 0 || warp == kTcStreamVWarp) && lane == 0;
+  const int vsel = warp == kTcStreamVWarp ? 1 : 0;
+  bool pre0 = false, pre1 = false;
+  UnitCursor ahead = start;  // the loaders' prefetch cursor: chunk ipf
+  int ipf = 0;
+  if (loader && nmine > 0) {
+    if (early_ok(start)) pre0 = issue(start, 0, vsel);
+    if (nmine > 1) {
+      UnitCursor u1 = start;
+      u1.next();
+      if (early_ok(u1)) pre1 = issue(u1, 1, vsel);
+    }
+    for (ahead.next(), ipf = 1; ipf < nmine && ipf < 2 + kStreamPF; ahead.next(), ++ipf)
+      if (ipf >= 2) prefetch(ahead, vsel);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const uint32_t kvb = __cvta_generic_to_shared(KV);
+  const uint32_t qb = __cvta_generic_to_shared(Qs);
+  const uint32_t phb = __cvta_generic_to_shared(Ph), plb = __cvta_generic_to_shared(Pl);
+  if (loader) {
+    // ---------------- loaders: chunk i's K (V) into slot i & 1 once S (P V)
+    // of chunk i-2 is done; the K loader also loads each new item's query tile
+    uint64_t* fullb = vsel ? vfull : kfull;
+    uint64_t* emptyb = vsel ? vempty : kempty;
+    UnitCursor u = start;
+    int issued = 0, nq = 0;
+    bool ok = true;
+    for (int i = 0; i < nmine && ok; ++i, u.next()) {
+      if (!vsel && (i == 0 || u.item_first())) {
+        if (nq > 0 && !tc::mbar_wait(qempty, (uint32_t)(nq - 1) & 1u, abort, lim_ns)) {
+          ok = false;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(qfull, 4 * kClQT * 128);
+        const int g = u.it / n_qt, qt = u.it % n_qt;
+        const int z = u.s * rows + (qt * kClQT) / grp, y = g * grp;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+          for (int dup = 0; dup < 2; ++dup)
+            tc::tma_load_3d(Qs + h * (kTcAttnRows * 128) + dup * (kClQT * 128), &p.q3, 64 * h, y, z, qfull);
+        ++nq;
+      }
+      if (i < 2 && (i == 0 ? pre0 : pre1)) {
+        ++issued;
+        continue;
+      }
+      if (i >= 2 && !tc::mbar_wait(&emptyb[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, lim_ns)) {
+        ok = false;
+        break;
+      }
+      if (issue(u, i & 1, vsel)) ++issued;
+      if (ipf < nmine && !stall) {  // keep the prefetch kStreamPF chunks ahead of the ring
+        prefetch(ahead, vsel);
+        ahead.next();
+        ++ipf;
+      }
+    }
+    if (!ok) {
+      raise_status(status, ST_TIMEOUT);
+      *abort = 1;
+    }
+    // Every copy this thread issued has landed before the CTA's shared memory
+    // goes away, also when a wait gave up (the last copy into each slot).
+    for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+      tc::mbar_wait(&fullb[i & 1], (uint32_t)(i >> 1) & 1u, nullptr, lim_ns);
+    if (nq > 0) tc::mbar_wait(qfull, (uint32_t)(nq - 1) & 1u, nullptr, lim_ns);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idS = tc::idesc_bf16_f32(kTcAttnRows, CH);
+      constexpr uint32_t idV = tc::idesc_bf16_f32_bmn(kTcAttnRows, D);
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (ok && !tc::mbar_wait(bar, par, abort, lim_ns)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          ok = false;
+        }
+        return ok;
+      };
+      UnitCursor us = start;  // next chunk whose S is issued
+      int nqs = 0;
+      auto issue_s = [&](int i) {
+        const int b = i & 1;
+        if ((i == 0 || us.item_first()) && !wait(qfull, (uint32_t)(nqs++) & 1u)) return;
+        if (!wait(&kfull[b], (uint32_t)(i >> 1) & 1u)) return;
+        tc::tc_fence_after();
+        const uint32_t kb = kvb + 2 * b * TILE;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t off = (uint32_t)((j >> 2) * (kTcAttnRows * 128) + (j & 3) * 32);
+          const uint32_t koff = (uint32_t)((j >> 2) * (CH * 128) + (j & 3) * 32);
+          tc::mma_bf16(tmem + (uint32_t)(b * CH), tc::sdesc_sw128(qb + off), tc::sdesc_sw128(kb + koff), idS,
+                       j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull[b]);
+        tc::mma_commit(&kempty[b]);
+        if (i + 1 < nmine && us.item_last()) tc::mma_commit(qempty);  // the next chunk starts another item
+        us.next();
+      };
+      UnitCursor uv = start;  // chunk whose P V is issued
+      int unit = 0;           // this CTA's unit of that chunk: output accumulator 2 + (unit & 1)
+      if (nmine > 0) issue_s(0);
+      if (nmine > 1) issue_s(1);
+      for (int i = 0; i < nmine && ok; ++i, uv.next()) {
+        if (i > 0 && uv.k == 0) ++unit;
+        if (!wait(&pdone[i & 1], (uint32_t)(i >> 1) & 1u)) break;
+        if (!wait(&vfull[i & 1], (uint32_t)(i >> 1) & 1u)) break;
+        tc::tc_fence_after();
+        const uint32_t vb = kvb + (2 * (i & 1) + 1) * TILE;
+        const uint32_t od = tmem + (uint32_t)((2 + (unit & 1)) * CH);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t pb = half ? plb : phb;
+#pragma unroll
+          for (int j = 0; j < CH / 16; ++j) {
+            const uint32_t poff = (uint32_t)((j >> 2) * (kTcAttnRows * 128) + (j & 3) * 32);
+            tc::mma_bf16(od, tc::sdesc_sw128(pb + poff),
+                         tc::sdesc_sw128_mn(vb + (uint32_t)j * 2048u, CH * 128, 1024), idV,
+                         (uv.k > 0 || half > 0 || j > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&vempty[i & 1]);
+        tc::mma_commit(ofull);
+        if (i + 2 < nmine) issue_s(i + 2);
+      }
+    }
+  } else if (warp >= 2 && warp < kTcStreamVWarp) {
+    // ---------------- softmax, warps 2 .. 9: the thread roles of attn_tc_kernel
+    const int sw = warp - 2;
+    const int L = (warp & 3) * 32 + lane;
+    const int qr = L & (kClQT - 1), h = L >> 6;
+    const int kg = sw >> 2, piece = 2 * kg + h;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const bool o_owner = h == 0;  // lanes 0..63 hold the output rows; this thread takes columns OC kg ..
+    const float scale = rsqrtf((float)D) * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    // Unit u is complete (its last P V has finished; its output accumulator
+    // is ob): O from TMEM, m and l to its partial (a warp's 32 rows store
+    // two 256-byte runs per instruction).
+    auto flush = [&](const UnitCursor& u, int ob, float m_fin, float l_fin) {
+      if (o_owner) {
+        float* pb = part + (size_t)(u.item() * NL + u.r) * kPartFloats + (qr / kRbRows) * kRbFloats;
+        const int ri = qr % kRbRows;
+        const uint64_t keep = tc::policy_evict_last();  // read back by the merge: keep in L2
+        __syncwarp();
+        tc::tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < OC / 64; ++q) {
+          float o64[64];
+          tc::tmem_ld64(lane_base + (uint32_t)(ob * CH + OC * kg + 64 * q), o64);
+#pragma unroll
+          for (int t = 0; t < 64; t += 4) {
+            const int quad = (OC * kg + 64 * q + t) / 4;
+            tc::st_global_hint(pb + (quad * kRbRows + ri) * 4, make_float4(o64[t], o64[t + 1], o64[t + 2], o64[t + 3]),
+                               keep);
+          }
+        }
+        if (kg == 0) {
+          tc::st_global_hint(pb + D * kRbRows + ri, m_fin, keep);
+          tc::st_global_hint(pb + D * kRbRows + kRbRows + ri, l_fin, keep);
+        }
+      }
+    };
+    UnitCursor u = start, prev = start;
+    int unit = 0;
+    float m_fin = -INFINITY, l_fin = 0.f;
+    for (int i = 0; i < nmine; ++i) {
+      const int c = u.chunk(), b = i & 1;
+      const int li = u.k;
+      if (li == 0 && i > 0) {  // a new logical rank starts from scratch
+        m_fin = m_run;
+        l_fin = l_run;
+        m_run = -INFINITY;
+        l_run = 0.f;
+        ++unit;
+      }
+      const uint32_t ocol = (uint32_t)((2 + (unit & 1)) * CH);  // this unit's output accumulator
+      const int qv0 = (u.it % n_qt) * kClQT;
+      const int row_tok = (qv0 + qr) / grp;
+      float* xm = xmax + b * (kTcAttnPieces * 64);
+      float* xs = xsum + b * (kTcAttnPieces * 64);
+      bool blk;
+      chunk_row(u, blk);
+      const int slot0 = blk ? -1 : c * CH;
+      const int nk = blk ? min(rows, CH) : min(CH, u.sk.n_ctx - c * CH);
+      const bool causal = mode == DFLASH_ATTN_CAUSAL && slot0 >= 0;
+      const int lim = causal ? u.P + row_tok - slot0 : CH;
+      if (ok && !tc::mbar_wait(&sfull[b], (uint32_t)(i >> 1) & 1u, abort, lim_ns)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
+      }
+      __syncwarp();  // the TMEM load below is warp-collective
+      tc::tc_fence_after();
+      float sc[KP];
+#pragma unroll
+      for (int q = 0; q < KP / 16; ++q) {
+        float t16[16];
+        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + KP * piece + 16 * q), t16);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) sc[16 * q + t] = t16[t];
+      }
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < KP; ++t) {
+        const int j = KP * piece + t;  // key index in the chunk
+        sc[t] = (j < nk && j <= lim) ? sc[t] * scale : -INFINITY;
+        cmax = fmaxf(cmax, sc[t]);
+      }
+      xm[piece * 64 + qr] = cmax;
+      tc::named_bar(2, kTcAttnSoft);
+      float m_cand = m_run;
+#pragma unroll
+      for (int pc = 0; pc < kTcAttnPieces; ++pc) m_cand = fmaxf(m_cand, xm[pc * 64 + qr]);
+      // the reference maximum moves only by more than 8 (attn_tc_kernel)
+      const float m_new = (m_run == -INFINITY || m_cand > m_run + 8.f) ? m_cand : m_run;
+      const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+      float sum = 0.f;
+#pragma unroll
+      for (int t = 0; t < KP; ++t) {
+        const float pj = (sc[t] == -INFINITY) ? 0.f : exp2f(sc[t] - m_new);
+        sc[t] = pj;
+        sum += pj;
+      }
+      xs[piece * 64 + qr] = sum;
+      // P has one buffer: the P V products of the chunk before must have
+      // finished reading it (and, for the unit before, writing its output).
+      if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim_ns)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
+      }
+#pragma unroll
+      for (int cc = 0; cc < KP / 8; ++cc) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16(sc[8 * cc + 2 * e], sc[8 * cc + 2 * e + 1], hi[e], lo[e]);
+        const int ch = (KP / 8) * piece + cc;
+        *reinterpret_cast<uint4*>(Ph + op_off(qr, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(Pl + op_off(qr, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      if (nk < CH) {
+        // rows past the last key: zero V (once it has landed) so that P = 0
+        // contributes 0
+        if (ok && !stall && !tc::mbar_wait(&vfull[b], (uint32_t)(i >> 1) & 1u, abort, lim_ns)) {
+          raise_status(status, ST_TIMEOUT);
+          *abort = 1;
+          ok = false;
+        }
+        uint8_t* Vt = KV + (2 * b + 1) * TILE;
+        for (int t = sw * 32 + lane; t < (CH - nk) * (D / 8); t += kTcAttnSoft) {
+          const int j = nk + t / (D / 8), ch = t % (D / 8);
+          *reinterpret_cast<uint4*>(Vt + kv_off(j, ch)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc::named_bar(2, kTcAttnSoft);
+      float lsum = 0.f;
+#pragma unroll
+      for (int pc = 0; pc < kTcAttnPieces; ++pc) lsum += xs[pc * 64 + qr];
+      l_run = fmaf(l_run, alpha, lsum);
+      if (o_owner && li > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        __syncwarp();
+        tc::tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < OC / 16; ++q) {
+          float o16[16];
+          const uint32_t col = ocol + (uint32_t)(OC * kg + 16 * q);
+          tc::tmem_ld16(lane_base + col, o16);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) o16[t] *= alpha;
+          tc::tmem_st16(lane_base + col, o16);
+        }
+      }
+      m_run = m_new;
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&pdone[b]);
+      // The unit before this one finished with chunk i-1 (its P V completed:
+      // waited above) in the other accumulator, which the MMAs of this unit
+      // do not touch: write it out while P V of chunk i runs.
+      if (i > 0 && li == 0) flush(prev, 2 + ((unit - 1) & 1), m_fin, l_fin);
+      prev = u;
+      u.next();
+    }
+    if (nmine > 0) {
+      if (ok && !tc::mbar_wait(ofull, (uint32_t)(nmine - 1) & 1u, abort, lim_ns)) {
+        raise_status(status, ST_TIMEOUT);
+        *abort = 1;
+        ok = false;
+      }
+      flush(prev, 2 + (unit & 1), m_run, l_run);
+      if (o_owner) __threadfence();  // this thread's partial rows, before the grid barrier
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+
+  // ---- every CTA's partials are written (grid barrier: the grid is one CTA
+  // per SM, all resident); then the merges, split evenly over the CTAs in
+  // tasks of (item, 16-row block): the NL partial blocks of a task arrive by
+  // bulk copy, double-buffered when two tasks' blocks fit.
+  if (threadIdx.x == 0) {
+    uint32_t* ctr = a.counters + kCtrAttnGrid;
+    volatile uint32_t* gen = ctr + 1;
+    const uint32_t g0 = *gen;
+    __threadfence();
+    if (atomicAdd(ctr, 1u) == gridDim.x - 1) {
+      *ctr = 0u;  // every CTA has arrived: ready for the next launch
+      __threadfence();
+      atomicAdd(ctr + 1, 1u);
+    } else {
+      const uint64_t t0 = global_ns();
+      while (*gen == g0) {
+        if (global_ns() - t0 > lim_ns) {
+          raise_status(status, ST_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    // the K barriers are idle (every K copy has landed): they now count the merge copies
+    tc::mbar_init(&kfull[0], 1);
+    tc::mbar_init(&kfull[1], 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  constexpr int kMergeSmem = 4 * TILE + kTcAttnRows * D * 2 + kTcAttnPBytes;  // K/V, Q and P space
+  static_assert((kRbRows * kMaxNC + kRbRows) * 4 <= 2 * 2 * kTcAttnPieces * 64 * 4, "weights fit the exchange space");
+  const int NB = 2 * NL * kRbBytes + kRbRows * D * 2 <= kMergeSmem ? 2 : 1;
+  __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(sm + (size_t)NB * NL * kRbBytes);  // [16][D] output rows
+  float* W = xmax;                   // [16][kMaxNC] rank weights (the softmax exchange space)
+  float* Ls = W + kRbRows * kMaxNC;  // [16] denominators
+  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out);
+  const int n_tasks = a.n_seqs * ips * (kClQT / kRbRows);
+  auto task_geom = [&](int task, int& item, int& rb, int& nle, int& nrow) {
+    item = task / (kClQT / kRbRows);
+    rb = task % (kClQT / kRbRows);
+    const int s = item / ips, it = item % ips;
+    nle = min(NL, tc_seq_keys(a, a.base_pos[s]).n_ch);
+    nrow = min(kRbRows, nqv - (it % n_qt) * kClQT - rb * kRbRows);
+  };
+  auto issue_task = [&](int task, int buf) {  // one thread
+    int item, rb, nle, nrow;
+    task_geom(task, item, rb, nle, nrow);
+    if (nrow <= 0) {
+      tc::mbar_arrive(&kfull[buf]);
+      return;
+    }
+    tc::mbar_arrive_expect_tx(&kfull[buf], (uint32_t)(nle * kRbBytes));
+    const uint64_t drop = tc::policy_evict_first();  // read once
+    for (int r = 0; r < nle; ++r)
+      tc::bulk_load_hint(sm + (size_t)(buf * NL + r) * kRbBytes,
+                         part + ((size_t)item * NL + r) * kPartFloats + (size_t)rb * kRbFloats, kRbBytes, &kfull[buf],
+                         drop);
+  };
+  if (threadIdx.x == 0 && (int)blockIdx.x < n_tasks) issue_task(blockIdx.x, 0);
+  int k = 0;
+  for (int task = blockIdx.x; task < n_tasks; task += gridDim.x, ++k) {
+    const int buf = NB == 2 ? (k & 1) : 0;
+    const uint32_t par = (uint32_t)(NB == 2 ? (k >> 1) : k) & 1u;
+    if (NB == 2 && threadIdx.x == 0 && task + (int)gridDim.x < n_tasks) issue_task(task + gridDim.x, buf ^ 1);
+    int item, rb, nle, nrow;
+    task_geom(task, item, rb, nle, nrow);
+    if (!tc::mbar_wait(&kfull[buf], par, nullptr, lim_ns)) raise_status(status, ST_TIMEOUT);
+    const float* B = reinterpret_cast<const float*>(sm + (size_t)buf * NL * kRbBytes);
+    // the rank weights of each query row (the arithmetic of merge_quad)
+    if ((int)threadIdx.x < nrow) {
+      const int i = threadIdx.x;
+      float mr[kMaxNC], lr[kMaxNC];
+#pragma unroll
+      for (int r = 0; r < kMaxNC; ++r) {
+        mr[r] = r < nle ? B[(size_t)r * kRbFloats + D * kRbRows + i] : -INFINITY;
+        lr[r] = r < nle ? B[(size_t)r * kRbFloats + D * kRbRows + kRbRows + i] : 0.f;
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxNC; ++r)
+        if (r < NL) M = fmaxf(M, mr[r]);
+      float Lr = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxNC; ++r) {
+        if (r < NL) {
+          const float w = (mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M);
+          W[i * kMaxNC + r] = w;
+          Lr = fmaf(lr[r], w, Lr);
+        }
+      }
+      Ls[i] = Lr;
+    }
+    __syncthreads();
+    // the weighted sums: consecutive threads take consecutive rows of a quad
+    for (int t = threadIdx.x; t < kRbRows * (D / 4); t += blockDim.x) {
+      const int i = t % kRbRows, quad = t / kRbRows;
+      if (i >= nrow) continue;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < kMaxNC; ++r) {
+        if (r < NL) {
+          const float4 v = r < nle ? *reinterpret_cast<const float4*>(B + (size_t)r * kRbFloats + (quad * kRbRows + i) * 4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float w = W[i * kMaxNC + r];
+          o[0] = fmaf(v.x, w, o[0]);
+          o[1] = fmaf(v.y, w, o[1]);
+          o[2] = fmaf(v.z, w, o[2]);
+          o[3] = fmaf(v.w, w, o[3]);
+        }
+      }
+      store_quad(Ob + i * D + 4 * quad, o, Ls[i]);
+    }
+    __syncthreads();
+    // the block's rows to the output, 16 bytes per thread
+    const int s = item / ips, it = item % ips;
+    const int g = it / n_qt, qv_b = (it % n_qt) * kClQT + rb * kRbRows;
+    for (int t = threadIdx.x; t < nrow * (D / 8); t += blockDim.x) {
+      const int i = t / (D / 8), c8 = 8 * (t % (D / 8));
+      const int qv = qv_b + i;
+      const int row = qv / grp, head = g * grp + qv % grp;
+      if (!DFL_CHECK(row < rows && head * D + c8 + 8 <= QD, status)) continue;
+      *reinterpret_cast<uint4*>(outp + ((size_t)s * rows + row) * QD + (size_t)head * D + c8) =
+          *reinterpret_cast<const uint4*>(Ob + i * D + c8);
+    }
+    __syncthreads();
+    if (NB == 1 && threadIdx.x == 0 && task + (int)gridDim.x < n_tasks) issue_task(task + gridDim.x, 0);
+  }
+}
+
 // ------------------------------------------------------------------- host
 
 namespace {
@@ -1364,12 +2126,53 @@ cudaError_t launch_tc_e(const AttnTma& p, int nc, int n_qt, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k, p, n_qt);
 }
 
+// The streaming variant: one CTA per SM, the NL logical ranks of the
+// cluster kernels as units (NL from the same residency query).
+template <int D>
+cudaError_t launch_tc_stream(const AttnTma& p, int nl, int n_qt, cudaStream_t st) {
+  auto k = attn_tc_stream_kernel<D>;
+  const size_t smem = tc_attn_smem(D) + 64;  // 32 more bytes of barriers and schedule than attn_tc_kernel
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms, 1, 1);
+  cfg.blockDim = dim3(kTcStreamThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  trace_kernel();
+  return cudaLaunchKernelEx(&cfg, k, p, n_qt, nl);
+}
+
+// DFLASH_ATTN_STREAM in the environment (read at every launch): "0" never
+// runs the streaming variant, "1" runs it whenever it applies; unset, it runs
+// when there are more items than clusters of the logical width fit at once.
+// All choices compute the same outputs bit for bit.
+static int stream_override() {
+  const char* v = getenv("DFLASH_ATTN_STREAM");
+  if (v == nullptr || v[0] == 0) return -1;
+  return v[0] == '1' ? 1 : 0;
+}
+
 template <int D>
 cudaError_t launch_tc(const AttnDesc& a, int n_qt, cudaStream_t st) {
   AttnTma p;
   if (!attn_maps<D>(a, p)) return cudaErrorInvalidValue;
   const int nl = pick_nc<D>((long)a.nkv);
   const long items = (long)a.nkv * n_qt * a.n_seqs;
+  const int force = stream_override();
+  if (p.q_tma && a.partials && a.counters && nl <= kMaxNC && force != 0 &&
+      (force == 1 || items > clusters_resident<D>(nl)))
+    return launch_tc_stream<D>(p, nl, n_qt, st);
   if (nl % 2 == 0 && items > clusters_resident<D>(nl) && clusters_resident<D>(nl / 2) > clusters_resident<D>(nl))
     return launch_tc_e<D, 2>(p, nl / 2, n_qt, st);
   return launch_tc_e<D, 1>(p, nl, n_qt, st);
@@ -1378,8 +2181,13 @@ cudaError_t launch_tc(const AttnDesc& a, int n_qt, cudaStream_t st) {
 }  // namespace
 
 size_t attn_workspace(const AttnDesc& a) {
-  if (a.dtype == DFLASH_BF16) return 0;  // merged on chip
   AttnGeom g = attn_geom(a);
+  if (a.dtype == DFLASH_BF16) {
+    // the streaming variant's partials, [items][NL <= kMaxNC][64][d + 4]
+    // (the cluster kernels merge on chip)
+    if (a.d != 128) return 0;
+    return (size_t)a.n_seqs * a.nkv * g.n_qt * kMaxNC * kClQT * (a.d + 4) * sizeof(float);
+  }
   return (size_t)a.n_seqs * a.nkv * g.n_qt * g.nch * kAttnQT * (a.d + 2) * sizeof(float);
 }
 
