@@ -394,66 +394,6 @@ __device__ __forceinline__ void rank_merge(cg::cluster_group& cl, float* psm, fl
   }
 }
 
-// One output quad (columns e4 .. e4+3) of a query row: the NL logical-rank
-// partials merged in rank order, o the weighted sum, L the weighted
-// denominator.  part(r) gives rank r's partial row (O[D], then m and l, log2
-// units), or null for a rank that had no chunks, which counts as m = -inf,
-// l = 0 and O = 0 -- the values such a rank's partial holds.  CG: the
-// partials are in global memory, written by other SMs (loads bypass L1).
-template <bool CG>
-__device__ __forceinline__ float ld_part(const float* p) {
-  if constexpr (CG) return __ldcg(p);
-  else return *p;
-}
-template <bool CG>
-__device__ __forceinline__ float4 ld_part4(const float* p) {
-  if constexpr (CG) return __ldcg(reinterpret_cast<const float4*>(p));
-  else return *reinterpret_cast<const float4*>(p);
-}
-template <int D, bool CG, class Part>
-__device__ __forceinline__ void merge_quad(int NL, Part part, int e4, float (&o)[4], float& L) {
-  // Loads are issued in batches (every rank's m, then l and O of eight ranks
-  // at a time) so that loads of global partials are in flight together; the
-  // arithmetic runs in rank order.
-  constexpr int G = 8;
-  float mr[kMaxNC];
-#pragma unroll
-  for (int r = 0; r < kMaxNC; ++r) {
-    const float* pr = r < NL ? part(r) : nullptr;
-    mr[r] = pr ? ld_part<CG>(pr + D) : -INFINITY;
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int r = 0; r < kMaxNC; ++r)
-    if (r < NL) M = fmaxf(M, mr[r]);
-  L = 0.f;
-  o[0] = o[1] = o[2] = o[3] = 0.f;
-#pragma unroll
-  for (int r0 = 0; r0 < kMaxNC; r0 += G) {
-    if (r0 >= NL) break;
-    float lr[G];
-    float4 v[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const float* pr = r0 + j < NL ? part(r0 + j) : nullptr;
-      lr[j] = pr ? ld_part<CG>(pr + D + 1) : 0.f;
-      v[j] = pr ? ld_part4<CG>(pr + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      if (r0 + j < NL) {
-        const float mj = mr[r0 + j];
-        const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-        L = fmaf(lr[j], w, L);
-        o[0] = fmaf(v[j].x, w, o[0]);
-        o[1] = fmaf(v[j].y, w, o[1]);
-        o[2] = fmaf(v[j].z, w, o[2]);
-        o[3] = fmaf(v[j].w, w, o[3]);
-      }
-    }
-  }
-}
-
 // The normalised quad, rounded to bf16 (a row that saw no key gives zeros).
 __device__ __forceinline__ void store_quad(__nv_bfloat16* dst, const float (&o)[4], float L) {
   __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(dst);
@@ -496,8 +436,21 @@ __device__ __forceinline__ void push_merge(cg::cluster_group& cl, const float* p
   __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(out);
   for (int t = threadIdx.x; t < nrow * (D / 4); t += blockDim.x) {
     const int i = t / (D / 4), e4 = 4 * (t % (D / 4));
-    float o[4], L;
-    merge_quad<D, false>(NL, [&](int r) { return rv + ((size_t)r * RP + i) * PST; }, e4, o, L);
+    // the arithmetic and order of the streaming kernel's merge phase
+    float M = -INFINITY;
+    for (int r = 0; r < NL; ++r) M = fmaxf(M, rv[((size_t)r * RP + i) * PST + D]);
+    float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < NL; ++r) {
+      const float* pr = rv + ((size_t)r * RP + i) * PST;
+      const float mr = pr[D];
+      const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+      L = fmaf(pr[D + 1], w, L);
+      const float4 v = *reinterpret_cast<const float4*>(pr + e4);
+      o[0] = fmaf(v.x, w, o[0]);
+      o[1] = fmaf(v.y, w, o[1]);
+      o[2] = fmaf(v.z, w, o[2]);
+      o[3] = fmaf(v.w, w, o[3]);
+    }
     const int qv = qv0 + q_lo + i;
     const int row = qv / grp, head = g * grp + qv % grp;
     if (!DFL_CHECK(row < rows && head * D + e4 + 4 <= QD, status)) continue;
@@ -1937,7 +1890,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
     task_geom(task, item, rb, nle, nrow);
     if (!tc::mbar_wait(&kfull[buf], par, nullptr, lim_ns)) raise_status(status, ST_TIMEOUT);
     const float* B = reinterpret_cast<const float*>(sm + (size_t)buf * NL * kRbBytes);
-    // the rank weights of each query row (the arithmetic of merge_quad)
+    // the rank weights of each query row (the arithmetic of push_merge)
     if ((int)threadIdx.x < nrow) {
       const int i = threadIdx.x;
       float mr[kMaxNC], lr[kMaxNC];
