@@ -1105,13 +1105,8 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       __syncwarp();  // the TMEM load below is warp-collective
       tc::tc_fence_after();
       float sc[KP];
-#pragma unroll
-      for (int q = 0; q < KP / 16; ++q) {
-        float t16[16];
-        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + KP * piece + 16 * q), t16);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) sc[16 * q + t] = t16[t];
-      }
+      static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
+      tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
       float cmax = -INFINITY;
 #pragma unroll
       for (int t = 0; t < KP; ++t) {
@@ -1217,18 +1212,19 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       for (int e = 0; e < E; ++e) {
         float* pr = psm + ((size_t)e * kClQT + qr) * PST;
         const bool any = (e == 0 ? nA : nB) > 0;  // uniform over the CTA
+        static_assert(OC % 64 == 0, "whole 64-column TMEM loads");
 #pragma unroll
-        for (int q = 0; q < OC / 16; ++q) {
-          float o16[16];
+        for (int q = 0; q < OC / 64; ++q) {
+          float o64[64];
           if (any) {
-            tc::tmem_ld16(lane_base + (uint32_t)((2 + e) * CH + OC * kg + 16 * q), o16);
+            tc::tmem_ld64(lane_base + (uint32_t)((2 + e) * CH + OC * kg + 64 * q), o64);
           } else {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) o16[t] = 0.f;
+            for (int t = 0; t < 64; ++t) o64[t] = 0.f;
           }
 #pragma unroll
-          for (int t = 0; t < 16; t += 4)
-            *reinterpret_cast<float4*>(pr + OC * kg + 16 * q + t) = make_float4(o16[t], o16[t + 1], o16[t + 2], o16[t + 3]);
+          for (int t = 0; t < 64; t += 4)
+            *reinterpret_cast<float4*>(pr + OC * kg + 64 * q + t) = make_float4(o64[t], o64[t + 1], o64[t + 2], o64[t + 3]);
         }
         if (kg == 0) {
           pr[D] = e == 0 ? mA : mB;
@@ -1715,13 +1711,8 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       __syncwarp();  // the TMEM load below is warp-collective
       tc::tc_fence_after();
       float sc[KP];
-#pragma unroll
-      for (int q = 0; q < KP / 16; ++q) {
-        float t16[16];
-        tc::tmem_ld16(lane_base + (uint32_t)(b * CH + KP * piece + 16 * q), t16);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) sc[16 * q + t] = t16[t];
-      }
+      static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
+      tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
       float cmax = -INFINITY;
 #pragma unroll
       for (int t = 0; t < KP; ++t) {
