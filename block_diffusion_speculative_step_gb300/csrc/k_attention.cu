@@ -826,6 +826,45 @@ __host__ __device__ constexpr size_t tc_attn_smem(int d) {
          + 1024;                                // alignment
 }
 
+// The softmax steps of one thread's KP keys, shared by the tcgen05 kernels so
+// that they compute the same values.  Scores: scaled to log2 units, keys past
+// the chunk's last key or the causal limit masked to -inf; the maximum is
+// taken over four interleaved partial maxima (exact in any order).
+template <int KP>
+__device__ __forceinline__ float soft_scores(float (&sc)[KP], int j0, int nk, int lim, float scale) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int t = 0; t < KP; ++t) {
+    const int j = j0 + t;  // key index in the chunk
+    sc[t] = (j < nk && j <= lim) ? sc[t] * scale : -INFINITY;
+    m4[t & 3] = fmaxf(m4[t & 3], sc[t]);
+  }
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// 2^x by the hardware approximation (PTX ex2.approx.ftz; results below the
+// normal range flush to 0): the arguments are at most 8, and P is carried as
+// a bf16 pair (about 16 bits) anyway.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// P = 2^(s - m_new) in place, and its sum: four interleaved partial sums,
+// added pairwise.
+template <int KP>
+__device__ __forceinline__ float soft_exp(float (&sc)[KP], float m_new) {
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int t = 0; t < KP; ++t) {
+    const float pj = (sc[t] == -INFINITY) ? 0.f : ex2_fast(sc[t] - m_new);
+    sc[t] = pj;
+    s4[t & 3] += pj;
+  }
+  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 // Byte offset of (row, 16-byte chunk) in a [128 rows][64 x nbox] bf16 operand
 // stored as nbox 128-byte swizzled boxes of 128 rows (the TMA layout).
 __device__ __forceinline__ uint32_t op_off(int row, int ch) {
@@ -1107,13 +1146,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       float sc[KP];
       static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
       tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
-      float cmax = -INFINITY;
-#pragma unroll
-      for (int t = 0; t < KP; ++t) {
-        const int j = KP * piece + t;  // key index in the chunk
-        sc[t] = (j < nk && j <= lim) ? sc[t] * scale : -INFINITY;
-        cmax = fmaxf(cmax, sc[t]);
-      }
+      const float cmax = soft_scores(sc, KP * piece, nk, lim, scale);
       xm[piece * 64 + qr] = cmax;
       tc::named_bar(2, kTcAttnSoft);
       float m_cand = m_run;
@@ -1125,14 +1158,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // are kept against the same reference, so the result is unchanged.
       const float m_new = (m_run == -INFINITY || m_cand > m_run + 8.f) ? m_cand : m_run;
       const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-      float sum = 0.f;
-#pragma unroll
-      for (int t = 0; t < KP; ++t) {
-        const float pj = (sc[t] == -INFINITY) ? 0.f : exp2f(sc[t] - m_new);
-        sc[t] = pj;
-        sum += pj;
-      }
-      xs[piece * 64 + qr] = sum;
+      xs[piece * 64 + qr] = soft_exp(sc, m_new);
       // P has one buffer: the P V products of the chunk before must have
       // finished reading it (S of this chunk was issued ahead of them).
       if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim_ns)) {
@@ -1713,13 +1739,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       float sc[KP];
       static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
       tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
-      float cmax = -INFINITY;
-#pragma unroll
-      for (int t = 0; t < KP; ++t) {
-        const int j = KP * piece + t;  // key index in the chunk
-        sc[t] = (j < nk && j <= lim) ? sc[t] * scale : -INFINITY;
-        cmax = fmaxf(cmax, sc[t]);
-      }
+      const float cmax = soft_scores(sc, KP * piece, nk, lim, scale);
       xm[piece * 64 + qr] = cmax;
       tc::named_bar(2, kTcAttnSoft);
       float m_cand = m_run;
@@ -1728,14 +1748,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       // the reference maximum moves only by more than 8 (attn_tc_kernel)
       const float m_new = (m_run == -INFINITY || m_cand > m_run + 8.f) ? m_cand : m_run;
       const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-      float sum = 0.f;
-#pragma unroll
-      for (int t = 0; t < KP; ++t) {
-        const float pj = (sc[t] == -INFINITY) ? 0.f : exp2f(sc[t] - m_new);
-        sc[t] = pj;
-        sum += pj;
-      }
-      xs[piece * 64 + qr] = sum;
+      xs[piece * 64 + qr] = soft_exp(sc, m_new);
       // P has one buffer: the P V products of the chunk before must have
       // finished reading it (and, for the unit before, writing its output).
       if (i > 0 && ok && !tc::mbar_wait(ofull, (uint32_t)(i - 1) & 1u, abort, lim_ns)) {
