@@ -786,21 +786,22 @@ __global__ void __launch_bounds__(kClusterWarps * 32, 1) attn_cluster_kernel(con
 // both products on the 5th-generation tensor cores: per 128-key chunk
 // S = Q K^T (M = 128 MMA rows: the 64 query rows of the tile, then the same
 // 64 again; N = 128 keys; K = 128 dims) into one of two TMEM accumulators.
-// The softmax warps (eight: 2..9), four per key group and one of each group
-// on every TMEM lane quadrant, read S: the thread on TMEM lane l of key group
-// k takes query row l mod 64 and the KP = 32 keys of piece 2k + l / 64, so
-// every row is shared by 4 threads, which exchange their maxima and sums
+// The softmax warps (sixteen: 2..17), four per key group and one of each
+// group on every TMEM lane quadrant, read S: the thread on TMEM lane l of key
+// group k takes query row l mod 64 and the KP = 16 keys of piece 2k + l / 64,
+// so every row is shared by 8 threads, which exchange their maxima and sums
 // through shared memory in piece order.  P
 // goes to shared memory as a bf16 pair (P_hi, P_lo), the running output O is
 // rescaled in TMEM, then O += P_hi V + P_lo V (V as an MN-major operand).
 // Roles: warp 0 issues the K/V TMA copies, one lane of warp 1 the MMAs; S of
 // chunk i+1 is computed while the softmax of chunk i runs.  Every wait is
 // bounded.
-// Eight softmax warps (KP = 32 keys per thread) measured faster than sixteen
-// (which need more than a quarter of the register file per sub-partition and
-// spill) and than four (latency-bound).
+// Sixteen softmax warps (KP = 16 keys per thread, 96 registers) measured
+// faster than eight (KP = 32: each chunk's softmax is a chain of dependent
+// instructions, which four warps per sub-partition hide better than two) and
+// than four.
 #ifndef DFLASH_TC_ATTN_SOFT_WARPS
-#define DFLASH_TC_ATTN_SOFT_WARPS 8
+#define DFLASH_TC_ATTN_SOFT_WARPS 16
 #endif
 constexpr int kTcAttnSoftWarps = DFLASH_TC_ATTN_SOFT_WARPS;  // 4 per TMEM lane quadrant x key groups
 constexpr int kTcAttnSoft = kTcAttnSoftWarps * 32;
@@ -840,6 +841,23 @@ __device__ __forceinline__ float soft_scores(float (&sc)[KP], int j0, int nk, in
     m4[t & 3] = fmaxf(m4[t & 3], sc[t]);
   }
   return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// One thread's KP scores of a chunk from TMEM (one load, one wait).
+template <int KP>
+__device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, float (&sc)[KP]) {
+  static_assert(KP == 16 || KP == 32, "16 or 32 keys per softmax thread");
+  if constexpr (KP == 32) tc::tmem_ld32(taddr, sc);
+  else tc::tmem_ld16(taddr, sc);
+}
+
+// N consecutive fp32 columns of this thread's TMEM lane (one load, one wait).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+  static_assert(N == 16 || N == 32 || N == 64, "16, 32 or 64 columns");
+  if constexpr (N == 64) tc::tmem_ld64(taddr, v);
+  else if constexpr (N == 32) tc::tmem_ld32(taddr, v);
+  else tc::tmem_ld16(taddr, v);
 }
 
 // 2^x by the hardware approximation (PTX ex2.approx.ftz; results below the
@@ -1144,8 +1162,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       __syncwarp();  // the TMEM load below is warp-collective
       tc::tc_fence_after();
       float sc[KP];
-      static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
-      tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
+      tmem_ld_scores(lane_base + (uint32_t)(b * CH + KP * piece), sc);
       const float cmax = soft_scores(sc, KP * piece, nk, lim, scale);
       xm[piece * 64 + qr] = cmax;
       tc::named_bar(2, kTcAttnSoft);
@@ -1238,19 +1255,19 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       for (int e = 0; e < E; ++e) {
         float* pr = psm + ((size_t)e * kClQT + qr) * PST;
         const bool any = (e == 0 ? nA : nB) > 0;  // uniform over the CTA
-        static_assert(OC % 64 == 0, "whole 64-column TMEM loads");
+        constexpr int NC_ = OC < 64 ? OC : 64;  // columns per TMEM load
 #pragma unroll
-        for (int q = 0; q < OC / 64; ++q) {
-          float o64[64];
+        for (int q = 0; q < OC / NC_; ++q) {
+          float o64[NC_];
           if (any) {
-            tc::tmem_ld64(lane_base + (uint32_t)((2 + e) * CH + OC * kg + 64 * q), o64);
+            tmem_ld_cols(lane_base + (uint32_t)((2 + e) * CH + OC * kg + NC_ * q), o64);
           } else {
 #pragma unroll
-            for (int t = 0; t < 64; ++t) o64[t] = 0.f;
+            for (int t = 0; t < NC_; ++t) o64[t] = 0.f;
           }
 #pragma unroll
-          for (int t = 0; t < 64; t += 4)
-            *reinterpret_cast<float4*>(pr + OC * kg + 64 * q + t) = make_float4(o64[t], o64[t + 1], o64[t + 2], o64[t + 3]);
+          for (int t = 0; t < NC_; t += 4)
+            *reinterpret_cast<float4*>(pr + OC * kg + NC_ * q + t) = make_float4(o64[t], o64[t + 1], o64[t + 2], o64[t + 3]);
         }
         if (kg == 0) {
           pr[D] = e == 0 ? mA : mB;
@@ -1379,7 +1396,7 @@ __device__ void find_unit(const AttnDesc& a, int ips, int NL, long long x, int l
 }
 
 // Threads of the streaming kernel: warp 0 loads K (and the query tiles),
-// warp 1 issues the MMAs, warps 2 .. 9 run the softmax, warp 10 loads V.
+// warp 1 issues the MMAs, the softmax warps follow, and the last warp loads V.
 constexpr int kTcStreamThreads = kTcAttnThreads + 32;
 #ifndef DFLASH_STREAM_PF
 #define DFLASH_STREAM_PF 4
@@ -1402,7 +1419,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
   constexpr int TILE = CH * D * 2;
   constexpr int KP = kTcAttnKP;
   constexpr int OC = D / kTcAttnGroups;  // output columns per owner thread
-  static_assert(CH == 128 && OC % 64 == 0, "whole 64-column TMEM loads");
+  static_assert(CH == 128 && OC % 16 == 0, "whole 16-column TMEM loads");
   static_assert((D + 2) * kClQT == kPartFloats, "partial size");
   static_assert(kRbBytes % 16 == 0, "bulk copies of whole 16-byte units");
   extern __shared__ __align__(1024) uint8_t smem_att[];
@@ -1668,7 +1685,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       }
     }
   } else if (warp >= 2 && warp < kTcStreamVWarp) {
-    // ---------------- softmax, warps 2 .. 9: the thread roles of attn_tc_kernel
+    // ---------------- softmax warps: the thread roles of attn_tc_kernel
     const int sw = warp - 2;
     const int L = (warp & 3) * 32 + lane;
     const int qr = L & (kClQT - 1), h = L >> 6;
@@ -1689,12 +1706,13 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
         __syncwarp();
         tc::tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < OC / 64; ++q) {
-          float o64[64];
-          tc::tmem_ld64(lane_base + (uint32_t)(ob * CH + OC * kg + 64 * q), o64);
+        constexpr int NC_ = OC < 64 ? OC : 64;  // columns per TMEM load
+        for (int q = 0; q < OC / NC_; ++q) {
+          float o64[NC_];
+          tmem_ld_cols(lane_base + (uint32_t)(ob * CH + OC * kg + NC_ * q), o64);
 #pragma unroll
-          for (int t = 0; t < 64; t += 4) {
-            const int quad = (OC * kg + 64 * q + t) / 4;
+          for (int t = 0; t < NC_; t += 4) {
+            const int quad = (OC * kg + NC_ * q + t) / 4;
             tc::st_global_hint(pb + (quad * kRbRows + ri) * 4, make_float4(o64[t], o64[t + 1], o64[t + 2], o64[t + 3]),
                                keep);
           }
@@ -1737,8 +1755,7 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       __syncwarp();  // the TMEM load below is warp-collective
       tc::tc_fence_after();
       float sc[KP];
-      static_assert(KP == 32, "one 32-column TMEM load per thread and chunk");
-      tc::tmem_ld32(lane_base + (uint32_t)(b * CH + KP * piece), sc);
+      tmem_ld_scores(lane_base + (uint32_t)(b * CH + KP * piece), sc);
       const float cmax = soft_scores(sc, KP * piece, nk, lim, scale);
       xm[piece * 64 + qr] = cmax;
       tc::named_bar(2, kTcAttnSoft);
