@@ -1097,9 +1097,13 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
       // P is written, and S of chunk i+2 after it (its K/V buffer and S
       // accumulator are the ones chunk i used), so that a chunk's load
       // latency hides behind the softmax of the chunk before it.
-      if (nmine > 0) issue_s(0);
-      if (nmine > 1) issue_s(1);
+      // S of chunk ns is issued once its K/V has landed, and at the latest
+      // before the wait for the softmax of that chunk; an S whose K is still
+      // on its way never holds up the P V of the chunk before it.
+      int ns = 0;
+      for (; ns < nmine && ns < 2; ++ns) issue_s(ns);
       for (int i = 0; i < nmine && ok; ++i) {
+        for (; ns <= i && ok; ++ns) issue_s(ns);
         if (!wait(&pdone[i & 1], (uint32_t)(i >> 1) & 1u)) break;
         tc::tc_fence_after();
         const uint32_t vb = kvb + (2 * (i & 1) + 1) * TILE;
@@ -1118,7 +1122,7 @@ __global__ void __launch_bounds__(kTcAttnThreads, 1) attn_tc_kernel(const __grid
         }
         tc::mma_commit(&empty[i & 1]);
         tc::mma_commit(ofull);
-        if (i + 2 < nmine) issue_s(i + 2);
+        if (ns == i + 2 && ns < nmine && tc::mbar_test(&full[ns & 1], (uint32_t)(ns >> 1) & 1u)) issue_s(ns++);
       }
     }
   } else {
@@ -1659,6 +1663,8 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       };
       UnitCursor uv = start;  // chunk whose P V is issued
       int unit = 0;           // this CTA's unit of that chunk: output accumulator 2 + (unit & 1)
+      // S of chunk i+2 right after P V of chunk i: its K slot frees only when
+      // it completes, so deferring it would slow the K ring.
       if (nmine > 0) issue_s(0);
       if (nmine > 1) issue_s(1);
       for (int i = 0; i < nmine && ok; ++i, uv.next()) {
@@ -1705,8 +1711,8 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
         const uint64_t keep = tc::policy_evict_last();  // read back by the merge: keep in L2
         __syncwarp();
         tc::tc_fence_after();
-#pragma unroll
         constexpr int NC_ = OC < 64 ? OC : 64;  // columns per TMEM load
+#pragma unroll
         for (int q = 0; q < OC / NC_; ++q) {
           float o64[NC_];
           tmem_ld_cols(lane_base + (uint32_t)(ob * CH + OC * kg + NC_ * q), o64);
