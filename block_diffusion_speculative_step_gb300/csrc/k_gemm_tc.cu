@@ -89,6 +89,14 @@ __device__ __forceinline__ int run_of(long long p, long long T, int G) {
   return c;
 }
 
+// Offset (floats) within a partial slot [BN][128] of accumulator row r's
+// columns c0 + 4 j4 .. c0 + 4 j4 + 3 (c0 a multiple of 16): per 16-column
+// chunk, four [128 rows][4] blocks, so a warp's 16-byte stores and loads of
+// one block cover 512 contiguous bytes.
+__host__ __device__ __forceinline__ size_t part_off(int c0, int j4, int r) {
+  return (size_t)c0 * 128 + (size_t)j4 * 512 + (size_t)r * 4;
+}
+
 // Partial slot of run c's piece of a tile.  A run is contiguous, so only its
 // first piece (slot 2c) and its last piece (slot 2c + 1, when the run began
 // in an earlier tile) can be parts of split tiles: 2 slots per run, whatever
@@ -663,12 +671,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
       } else {
         const size_t slot = 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);  // piece_slot of this piece
-        float* dst0 = L.part + slot * BN * 128 + r;
+        float* dst0 = L.part + slot * BN * 128;
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst0[(size_t)(c0 + j) * 128] = v[j];
+          for (int j4 = 0; j4 < 4; ++j4)
+            *reinterpret_cast<float4*>(dst0 + part_off(c0, j4, r)) =
+                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
         }
         tc::tc_fence_before();
         // bar.sync orders every epilogue thread's partial stores before the
@@ -713,9 +723,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const int c = sb + q <= last ? sb + q : last;
-                const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128 + (size_t)c0 * 128 + r;
+                const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
+                for (int j4 = 0; j4 < 4; ++j4) {
+                  const float4 x = (sb + q <= last) ? __ldcg(reinterpret_cast<const float4*>(src + part_off(c0, j4, r)))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                  pv[q][4 * j4] = x.x;
+                  pv[q][4 * j4 + 1] = x.y;
+                  pv[q][4 * j4 + 2] = x.z;
+                  pv[q][4 * j4 + 3] = x.w;
+                }
               }
 #pragma unroll
               for (int q = 0; q < 4; ++q)
@@ -805,9 +822,16 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int c = sb + q <= last ? sb + q : last;
-      const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128 + (size_t)c0 * 128 + r;
+      const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pv[q][j] = (sb + q <= last) ? __ldcg(src + (size_t)j * 128) : 0.f;
+      for (int j4 = 0; j4 < 4; ++j4) {
+        const float4 x = (sb + q <= last) ? __ldcg(reinterpret_cast<const float4*>(src + part_off(c0, j4, r)))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        pv[q][4 * j4] = x.x;
+        pv[q][4 * j4 + 1] = x.y;
+        pv[q][4 * j4 + 2] = x.z;
+        pv[q][4 * j4 + 3] = x.w;
+      }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q)

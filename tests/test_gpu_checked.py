@@ -2,9 +2,9 @@
 
 - libdflash_checked.so (DFLASH_CHECKED) carries device bounds assertions on
   the addresses the kernels compute; a failed one reports DFLASH_ERR_CHECK
-  through the status word instead of trapping.  The small parity tests run
-  against it in a child process: every result must still match the oracle
-  and every status word must stay clean.
+  through the status word instead of trapping.  The small parity tests (and
+  the streaming-attention comparisons) run against it in a child process:
+  every result must still match and every status word must stay clean.
 - Token ids read on the device are checked in every build: an out-of-range
   anchor comes back as DFLASH_ERR_INVALID_ARG (its row reads token 0, no
   access leaves the table), and the next clean call as DFLASH_OK.
@@ -36,7 +36,8 @@ def test_parity_suite_on_the_checked_build():
             "import pytest\n"
             f"sys.exit(pytest.main(['-q', '-p', 'no:cacheprovider', '-m', 'gpu', "
             f"{os.path.join(ROOT, 'tests', 'test_gpu_parity.py')!r}, '-k', {sel!r}, "
-            f"{os.path.join(ROOT, 'tests', 'test_gpu_paged.py')!r}]))\n")
+            f"{os.path.join(ROOT, 'tests', 'test_gpu_paged.py')!r}, "
+            f"{os.path.join(ROOT, 'tests', 'test_gpu_attn_stream.py')!r}]))\n")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
