@@ -1402,10 +1402,6 @@ __device__ void find_unit(const AttnDesc& a, int ips, int NL, long long x, int l
 // Threads of the streaming kernel: warp 0 loads K (and the query tiles),
 // warp 1 issues the MMAs, the softmax warps follow, and the last warp loads V.
 constexpr int kTcStreamThreads = kTcAttnThreads + 32;
-#ifndef DFLASH_STREAM_PF
-#define DFLASH_STREAM_PF 4
-#endif
-constexpr int kStreamPF = DFLASH_STREAM_PF;  // chunks prefetched into L2 ahead of the shared-memory ring
 // One unit's partial (head dim 128): four blocks of 16 query rows, each
 // O [32 column quads][16 rows][4] then m[16], l[16] -- 8320 contiguous bytes,
 // one bulk copy in the merge.
@@ -1540,18 +1536,6 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
     for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(dst + h * (CH * 128), map, 64 * h, row, bar, pol);
     return true;
   };
-  // L2 prefetch of one operand tile of chunk u: the shared-memory ring is
-  // two chunks deep, so the loaders keep kStreamPF chunks ahead in L2, and
-  // the tiled loads then wait for L2 rather than HBM.  (L2 is the point of
-  // coherence: a prefetch before the PDL wait may be overwritten later by
-  // the kernel before this one, and the load still reads the new data.)
-  auto prefetch = [&](const UnitCursor& u, int v) {
-    bool blk;
-    const int row = chunk_row(u, blk);
-    const CUtensorMap* map = v ? (blk ? &p.vb : &p.vc) : (blk ? &p.kb : &p.kc);
-#pragma unroll
-    for (int h = 0; h < D / 64; ++h) tc::tma_prefetch_l2_2d(map, 64 * h, row);
-  };
   auto early_ok = [&](const UnitCursor& u) {
     const int c = u.chunk();
     return c < u.sk.n_ctx_ch && (mode == DFLASH_ATTN_BLOCK_BIDIR || (c + 1) * CH <= u.P);
@@ -1561,8 +1545,6 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
   const bool loader = (warp == 0 || warp == kTcStreamVWarp) && lane == 0;
   const int vsel = warp == kTcStreamVWarp ? 1 : 0;
   bool pre0 = false, pre1 = false;
-  UnitCursor ahead = start;  // the loaders' prefetch cursor: chunk ipf
-  int ipf = 0;
   if (loader && nmine > 0) {
     if (early_ok(start)) pre0 = issue(start, 0, vsel);
     if (nmine > 1) {
@@ -1570,8 +1552,6 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
       u1.next();
       if (early_ok(u1)) pre1 = issue(u1, 1, vsel);
     }
-    for (ahead.next(), ipf = 1; ipf < nmine && ipf < 2 + kStreamPF; ahead.next(), ++ipf)
-      if (ipf >= 2) prefetch(ahead, vsel);
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -1612,11 +1592,6 @@ __global__ void __launch_bounds__(kTcStreamThreads, 1) attn_tc_stream_kernel(con
         break;
       }
       if (issue(u, i & 1, vsel)) ++issued;
-      if (ipf < nmine && !stall) {  // keep the prefetch kStreamPF chunks ahead of the ring
-        prefetch(ahead, vsel);
-        ahead.next();
-        ++ipf;
-      }
     }
     if (!ok) {
       raise_status(status, ST_TIMEOUT);

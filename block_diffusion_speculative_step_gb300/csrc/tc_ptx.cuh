@@ -94,14 +94,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Prefetch of the 2-D box at (x, y) into L2 (no shared memory, no barrier):
-// a later tiled load of the same box then reads L2 instead of waiting for HBM.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // 16-byte global store with an L2 cache policy (e.g. evict_last, for data
 // that another SM reads back shortly).
 __device__ __forceinline__ void st_global_hint(float* dst, float4 v, uint64_t policy) {
