@@ -22,9 +22,10 @@
 // Tiles of more than 16 token rows finish in 16-column chunks; their
 // column-independent row operands are staged once per CTA in shared memory
 // (RowTab), so a chunk costs one global round trip.  From 128 token rows on,
-// the pieces of a split tile only store their partials and tc_fixup_kernel,
-// launched behind the GEMM, finishes every split tile with one CTA per
-// 16-column chunk (same k-order sum, same epilogue).  The LM head keeps, per
+// every piece only stores its accumulator (a tile that one run covers, into
+// a slot of its own) and tc_fixup_kernel, launched behind the GEMM, finishes
+// every tile with one CTA per 16-column chunk (same k-order sum, same
+// epilogue), so no CTA holds a whole tile's epilogue past its last MMA.  The LM head keeps, per
 // CTA, each token row's best (logit, index) and runner-up over the tiles the
 // CTA finishes; the last CTA merges one triple per CTA.
 #include <cudaTypedefs.h>
@@ -56,7 +57,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int G;          // CTAs (runs)
   int M;          // token rows
   int defer;      // GEMM, BN >= 128: split tiles are finished by tc_fixup_kernel, not by their last piece
-  float* part;    // partial slots [2 G][BN][128] (piece_slot)
+  float* part;    // partial slots [2 G (+ n_tiles when deferred)][BN][128] (piece_slot, tile_slot)
   Top2* tops;     // LM head: per-CTA triples [G][M]
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
   uint32_t* counters;
@@ -107,6 +108,10 @@ __host__ __device__ __forceinline__ size_t part_off(int c0, int j4, int r) {
 __device__ __forceinline__ size_t piece_slot(int c, int first, bool first_tail) {
   return 2 * (size_t)c + ((c == first && first_tail) ? 1u : 0u);
 }
+
+// Slot of tile t's accumulator when one run covers the tile in a deferred
+// launch: after the 2 G piece slots.
+__host__ __device__ __forceinline__ size_t tile_slot(int G, int t) { return 2 * (size_t)G + (size_t)t; }
 
 __device__ __forceinline__ void tc_timeout(uint32_t* status, volatile int* abort) {
   raise_status(status, ST_TIMEOUT);
@@ -651,7 +656,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         if (tc_unit(L, t2, r, unit2)) epi_preload_tile(e2, unit2, 0, rows, old_next);
       }
       const uint32_t trow = tmem + (uint32_t)(b * Cfg::ACC) + ((uint32_t)(q4 * 32) << 16);
-      if (whole) {
+      const bool deferred = Cfg::WIDE && L.defer;
+      if (whole && !deferred) {
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
           if (Cfg::WIDE && L.mode == TC_GEMM) {
@@ -670,7 +676,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         tc::named_bar(1, 128);
         if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
       } else {
-        const size_t slot = 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);  // piece_slot of this piece
+        // piece_slot of this piece; a deferred whole tile has a slot of its own
+        const size_t slot = whole ? tile_slot(L.G, t) : 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);
         float* dst0 = L.part + slot * BN * 128;
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           float v[16];
@@ -686,7 +693,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
         // (and the barrier after it) orders the fixup's loads after the
         // other pieces' stores.
         tc::named_bar(1, 128);
-        if (Cfg::WIDE && L.defer) {  // finished by tc_fixup_kernel once the grid has completed
+        if (deferred) {  // finished by tc_fixup_kernel once the grid has completed
           if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8u * b) : "memory");
           pos = end;
           ++k;
@@ -767,30 +774,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, gridDim.x, L.tops, &s_last_head);
 }
 
-// Split tiles of a deferred launch (BN >= 128), once the GEMM grid has
-// completed: one CTA of 128 threads per (tile, 16-column chunk); thread r
-// sums accumulator row r's partial slots in k order and runs the chunk's
+// Tiles of a deferred launch (BN >= 128), once the GEMM grid has completed:
+// one CTA of 128 threads per (tile, 16-column chunk); thread r sums
+// accumulator row r's partial slots in k order and runs the chunk's
 // epilogue -- the arithmetic and order of a last piece finishing its tile
-// inline, spread over every SM instead of one CTA per tile.
+// inline (a tile that one run covers: its accumulator as it is), spread over
+// every SM instead of one CTA per tile.  Each thread copies its own 16-byte
+// blocks of the slots into shared memory (cp.async) before the row table is
+// built, so the two latencies overlap and the slots cost no registers.
+constexpr int kFixBatch = 8;  // slots per cp.async batch
+
+__device__ __forceinline__ void part_copy16(void* sdst, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(sdst)), "l"(g) : "memory");
+}
+
 template <int BN>
-__global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ TcParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
+__global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ float4 s_part[];  // [kFixBatch][4][128]: slot q's block j4 of row r at (q * 4 + j4) * 128 + r
   __shared__ RowTab s_tab;
   __shared__ float s_xch[16 * 128];
+  pdl_wait();
+  pdl_launch_dependents();
   const TcLocal L = tc_local(p);
   const int nkb = L.nkb;
   const int nch = min(BN, ((L.M + 15) / 16) * 16) / 16;
   const int t = (int)(blockIdx.x / nch), c0 = (int)(blockIdx.x % nch) * 16;
   const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
   const int first = run_of(tbeg, L.T, L.G), last = run_of(tend - 1, L.T, L.G);
-  if (first == last) return;
-  const bool first_tail = run_start(L.T, L.G, first) < tbeg;  // one run covers the tile: finished inline (uniform over the CTA)
+  const bool first_tail = run_start(L.T, L.G, first) < tbeg;
   const int r = threadIdx.x, lane = r & 31;
-  // the partial slots first: they depend on nothing below
-  float v[16];
+  const int np = last - first + 1;  // pieces, in k order
+  uint32_t dyn;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+  if (min(np, kFixBatch) * 4 * 128 * 16 > (int)dyn) {  // more slots than the launch sized for (uniform)
+    if (r == 0) raise_status(L.status, ST_RANGE);
+    return;
+  }
+  auto copy_batch = [&](int q0) {
+    for (int q = q0; q < np && q < q0 + kFixBatch; ++q) {
+      const size_t slot = np == 1 ? tile_slot(L.G, t) : piece_slot(first + q, first, first_tail);
+      const float* src = L.part + slot * BN * 128;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+      for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((q - q0) * 4 + j4) * 128 + r], src + part_off(c0, j4, r));
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  copy_batch(0);  // depends on nothing below
   Epi e = make_epi(p.g, t / L.tps);
   e.status = L.status;
   // row operands of the 32-row word holding the chunk (warp 0)
@@ -817,27 +846,29 @@ __global__ void __launch_bounds__(128) tc_fixup_kernel(const __grid_constant__ T
   int unit = 0;
   const bool works = tc_unit(L, t, r, unit);
   wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
-  for (int sb = first; sb <= last; sb += 4) {
-    float pv[4][16];
+  float v[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = sb + q <= last ? sb + q : last;
-      const float* src = L.part + piece_slot(c, first, first_tail) * BN * 128;
+  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+  for (int q0 = 0; q0 < np; q0 += kFixBatch) {
+    if (q0 > 0) copy_batch(q0);
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's own copies: no barrier needed
+    for (int q = q0; q < np && q < q0 + kFixBatch; ++q) {
 #pragma unroll
       for (int j4 = 0; j4 < 4; ++j4) {
-        const float4 x = (sb + q <= last) ? __ldcg(reinterpret_cast<const float4*>(src + part_off(c0, j4, r)))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        pv[q][4 * j4] = x.x;
-        pv[q][4 * j4 + 1] = x.y;
-        pv[q][4 * j4 + 2] = x.z;
-        pv[q][4 * j4 + 3] = x.w;
+        const float4 x = s_part[((q - q0) * 4 + j4) * 128 + r];
+        if (np == 1) {  // the tile's accumulator as it is (no 0 + x)
+          v[4 * j4] = x.x;
+          v[4 * j4 + 1] = x.y;
+          v[4 * j4 + 2] = x.z;
+          v[4 * j4 + 3] = x.w;
+        } else {
+          v[4 * j4] += x.x;
+          v[4 * j4 + 1] += x.y;
+          v[4 * j4 + 2] += x.z;
+          v[4 * j4 + 3] += x.w;
+        }
       }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (sb + q <= last) v[j] += pv[q][j];
   }
   final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
 }
@@ -862,8 +893,17 @@ int gemm_tiles_per_seg(const GemmDesc& g) { return g.kind == EPI_SWIGLU ? g.inte
 
 int runs_for(long long T, int num_sms) { return (int)(T < num_sms ? T : num_sms); }
 
-// Split-K partial slots: two per run (piece_slot).
-size_t part_bytes(int G, int bn) { return (size_t)2 * G * bn * 128 * sizeof(float); }
+// Split-K partial slots: two per run (piece_slot), and in a deferred launch
+// (BN >= 128) one per tile as well (tile_slot).
+size_t part_bytes(int G, int bn, int n_tiles = 0) {
+  return ((size_t)2 * G + (bn >= 128 ? (size_t)n_tiles : 0)) * bn * 128 * sizeof(float);
+}
+
+// Most pieces any tile has: runs are at least floor(T / G) k-blocks long.
+int max_pieces(long long T, int G, int nkb) {
+  const long long lmin = T / G;
+  return (int)((nkb - 1 + lmin - 1) / lmin) + 1;
+}
 
 template <int BN>
 cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
@@ -874,7 +914,11 @@ cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
   if (e != cudaSuccess || !p.defer) return e;
   if constexpr (BN >= 128) {
     const int nch = (p.M < BN ? (p.M + 15) / 16 * 16 : BN) / 16;
-    return launch_pdl(tc_fixup_kernel<BN>, dim3(p.n_tiles * nch), dim3(128), 0, st, p);
+    const int pb = std::min(max_pieces(p.T, p.G, p.nkb), kFixBatch);
+    const int fsm = pb * 4 * 128 * 16;
+    e = cudaFuncSetAttribute(tc_fixup_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFixBatch * 4 * 128 * 16);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc_fixup_kernel<BN>, dim3(p.n_tiles * nch), dim3(128), fsm, st, p);
   }
   return cudaErrorInvalidValue;
 }
@@ -910,7 +954,7 @@ bool gemm_tc_supported(const GemmDesc& g) {
 size_t gemm_tc_workspace(const GemmDesc& g, int num_sms) {
   const int n_tiles = g.nseg * gemm_tiles_per_seg(g);
   const long long T = (long long)n_tiles * (g.K / 64);
-  return part_bytes(runs_for(T, num_sms), pick_bn(g.M));
+  return part_bytes(runs_for(T, num_sms), pick_bn(g.M), n_tiles);
 }
 
 cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
@@ -959,7 +1003,7 @@ cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, ui
   p.T = (long long)p.n_tiles * p.nkb;
   p.G = runs_for(p.T, num_sms);
   if (p.n_tiles > 8192) return cudaErrorInvalidValue;
-  if (ws_bytes < part_bytes(p.G, pick_bn(g.M))) return cudaErrorInvalidValue;
+  if (ws_bytes < part_bytes(p.G, pick_bn(g.M), p.n_tiles)) return cudaErrorInvalidValue;
   p.part = static_cast<float*>(ws);
   p.counters = counters;
   p.status = status;
