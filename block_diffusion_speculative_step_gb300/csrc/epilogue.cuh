@@ -91,7 +91,12 @@ __device__ __forceinline__ void epi_single(const Epi& e, int n, int m, float v) 
     *o = v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+// SiLU z * sigmoid(z) with the fast exponential and division intrinsics (a
+// few fp32 ulp, far below the bf16 output rounding): the IEEE division's
+// slow-path branch kept the 16 quotients of an epilogue chunk from
+// overlapping (about 1 us per chunk).  For z below about -88 the
+// denominator is +inf and the quotient 0.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // Rotation of one RoPE pair by (c, s) = (cos, sin): every product and sum
 // rounded on its own (no fused multiply-add), so every epilogue that applies

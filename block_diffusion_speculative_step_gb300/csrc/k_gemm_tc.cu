@@ -775,63 +775,121 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 }
 
 // Tiles of a deferred launch (BN >= 128), once the GEMM grid has completed:
-// one CTA of 128 threads per (tile, 16-column chunk); thread r sums
-// accumulator row r's partial slots in k order and runs the chunk's
+// one CTA of 128 threads per (tile, group of `ch` 16-column chunks); thread
+// r sums accumulator row r's partial slots in k order and runs each chunk's
 // epilogue -- the arithmetic and order of a last piece finishing its tile
 // inline (a tile that one run covers: its accumulator as it is), spread over
-// every SM instead of one CTA per tile.  Each thread copies its own 16-byte
-// blocks of the slots into shared memory (cp.async) before the row table is
-// built, so the two latencies overlap and the slots cost no registers.
-constexpr int kFixBatch = 8;  // slots per cp.async batch
+// every SM instead of one CTA per tile.  Each thread first copies its own
+// 16-byte blocks of every slot of every chunk into shared memory (cp.async,
+// one group per chunk), so the copies, the row table and the epilogues of the
+// earlier chunks overlap, and the slots cost no registers.
+constexpr int kFixBatch = 8;   // most slots held per chunk
+constexpr int kFixChunks = 4;  // most chunks per CTA
+
+// The deferred launches finished by one fixup launch: a projection of more
+// than 256 token rows runs as several GEMM launches (whole sequences each)
+// and one fixup behind the last of them.
+constexpr int kMaxFixParts = 4;
+struct FixPart {
+  GemmDesc g;
+  float* part;
+  long long T;
+  int M, tps, n_tiles, nkb, G;
+  int blocks;  // fixup CTAs of this part: n_tiles x chunk groups
+};
+struct FixParams {
+  FixPart q[kMaxFixParts];
+  int nparts;
+  int ch;  // chunks per CTA
+  int pb;  // slots per chunk held in shared memory ([ch][pb][4][128] float4)
+  uint32_t* status;
+};
+static_assert(sizeof(FixParams) <= 4000, "fixup parameters fit the classic 4 KB parameter space");
 
 __device__ __forceinline__ void part_copy16(void* sdst, const void* g) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(sdst)), "l"(g) : "memory");
 }
 
+// Waits until at most n of this thread's cp.async groups are pending (n < 4).
+__device__ __forceinline__ void part_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+  }
+}
+
 template <int BN>
-__global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant__ TcParams p) {
-  extern __shared__ float4 s_part[];  // [kFixBatch][4][128]: slot q's block j4 of row r at (q * 4 + j4) * 128 + r
+__global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant__ FixParams fp) {
+  extern __shared__ float4 s_part[];  // [ch][pb][4][128]: chunk i, slot q, block j4 of row r
   __shared__ RowTab s_tab;
   __shared__ float s_xch[16 * 128];
   pdl_wait();
   pdl_launch_dependents();
-  const TcLocal L = tc_local(p);
-  const int nkb = L.nkb;
+  int bid = (int)blockIdx.x, pi = 0;
+  while (pi + 1 < fp.nparts && bid >= fp.q[pi].blocks) bid -= fp.q[pi++].blocks;
+  const FixPart& P = fp.q[pi];
+  TcLocal L;
+  memset(&L, 0, sizeof(L));
+  L.mode = TC_GEMM;
+  L.M = P.M;
+  L.defer = 1;
+  L.tps = P.tps;
+  L.nkb = P.nkb;
+  L.G = P.G;
+  L.n_tiles = P.n_tiles;
+  L.T = P.T;
+  L.kind = P.g.kind;
+  L.d = P.g.d;
+  L.inter = P.g.inter;
+  L.row0 = P.g.seg_row0;
+  L.part = P.part;
+  L.status = fp.status;
+  const int nkb = L.nkb, CH = fp.ch, PB = fp.pb;
   const int nch = min(BN, ((L.M + 15) / 16) * 16) / 16;
-  const int t = (int)(blockIdx.x / nch), c0 = (int)(blockIdx.x % nch) * 16;
+  const int ngrp = (nch + CH - 1) / CH;
+  const int t = bid / ngrp, cg = (bid % ngrp) * CH;  // the tile and its first chunk
+  const int nc = min(CH, nch - cg);
   const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
   const int first = run_of(tbeg, L.T, L.G), last = run_of(tend - 1, L.T, L.G);
   const bool first_tail = run_start(L.T, L.G, first) < tbeg;
-  const int r = threadIdx.x, lane = r & 31;
+  const int r = threadIdx.x, lane = r & 31, w = r >> 5;
   const int np = last - first + 1;  // pieces, in k order
   uint32_t dyn;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-  if (min(np, kFixBatch) * 4 * 128 * 16 > (int)dyn) {  // more slots than the launch sized for (uniform)
+  const bool batched = np > PB;  // more pieces than a chunk holds: one chunk, in batches of PB
+  if ((batched && CH != 1) || CH > kFixChunks || (size_t)CH * PB * 4 * 128 * 16 > dyn) {  // uniform
     if (r == 0) raise_status(L.status, ST_RANGE);
     return;
   }
-  auto copy_batch = [&](int q0) {
-    for (int q = q0; q < np && q < q0 + kFixBatch; ++q) {
-      const size_t slot = np == 1 ? tile_slot(L.G, t) : piece_slot(first + q, first, first_tail);
-      const float* src = L.part + slot * BN * 128;
-#pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((q - q0) * 4 + j4) * 128 + r], src + part_off(c0, j4, r));
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+  auto slot_src = [&](int q, int c0, int j4) {
+    const size_t slot = np == 1 ? tile_slot(L.G, t) : piece_slot(first + q, first, first_tail);
+    return L.part + slot * BN * 128 + part_off(c0, j4, r);
   };
-  copy_batch(0);  // depends on nothing below
-  Epi e = make_epi(p.g, t / L.tps);
+  // every chunk's slots first: they depend on nothing below
+  for (int i = 0; i < nc; ++i) {
+    for (int q = 0; q < np && q < PB; ++q)
+#pragma unroll
+      for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((i * PB + q) * 4 + j4) * 128 + r], slot_src(q, (cg + i) * 16, j4));
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  Epi e = make_epi(P.g, t / L.tps);
   e.status = L.status;
-  // row operands of the 32-row word holding the chunk (warp 0)
-  if (r < 32) {
-    const int m = (c0 & ~31) + lane;
-    const bool lv = m < L.M && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + m / e.rows));
+  // row operands of the 32-row words holding the chunks (warp w: word w)
+  const int w0 = (cg * 16) >> 5, nw = (((cg + nc) * 16 + 31) >> 5) - w0;
+  if (w < nw) {
+    const int m = ((w0 + w) << 5) + lane;
+    const bool in = m < L.M;
+    const int sq = in ? m / e.rows : 0;
+    const int bp = (in && e.kind == EPI_QKV) ? __ldg(e.base_pos + sq) : 0;  // issued with the valid load
+    const bool lv = in && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + sq));
     const uint32_t bits = __ballot_sync(0xffffffffu, lv);
-    if (lane == 0) s_tab.live[c0 >> 5] = bits;
+    if (lane == 0) s_tab.live[w0 + w] = bits;
     int pos = -1;
     uint32_t kvr = ~0u;
     if (e.kind == EPI_QKV && lv) {
-      const int q = __ldg(e.base_pos + m / e.rows) + m % e.rows;
+      const int q = bp + m % e.rows;
       if (q >= 0 && q < e.rope_max_pos) {
         pos = q;
         const int slot = e.kv_slot_mode == 1 ? (e.kv_window > 0 ? q % e.kv_window : q) : m % e.rows;
@@ -842,35 +900,43 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
     s_tab.kvr[m] = kvr;
   }
   __syncthreads();
-  float pre[32];
   int unit = 0;
   const bool works = tc_unit(L, t, r, unit);
-  wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
-  float v[16];
+  for (int i = 0; i < nc; ++i) {
+    const int c0 = (cg + i) * 16;
+    float pre[32];
+    wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
+    float v[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = 0.f;
-  for (int q0 = 0; q0 < np; q0 += kFixBatch) {
-    if (q0 > 0) copy_batch(q0);
-    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's own copies: no barrier needed
-    for (int q = q0; q < np && q < q0 + kFixBatch; ++q) {
+    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    for (int q0 = 0; q0 < np; q0 += PB) {
+      if (q0 > 0) {  // batched (one chunk): the next PB slots
+        for (int q = q0; q < np && q < q0 + PB; ++q)
 #pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4) {
-        const float4 x = s_part[((q - q0) * 4 + j4) * 128 + r];
-        if (np == 1) {  // the tile's accumulator as it is (no 0 + x)
-          v[4 * j4] = x.x;
-          v[4 * j4 + 1] = x.y;
-          v[4 * j4 + 2] = x.z;
-          v[4 * j4 + 3] = x.w;
-        } else {
-          v[4 * j4] += x.x;
-          v[4 * j4 + 1] += x.y;
-          v[4 * j4 + 2] += x.z;
-          v[4 * j4 + 3] += x.w;
+          for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((q - q0) * 4 + j4) * 128 + r], slot_src(q, c0, j4));
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      part_wait(q0 > 0 ? 0 : nc - 1 - i);  // this thread's own copies: no barrier needed
+      for (int q = q0; q < np && q < q0 + PB; ++q) {
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 x = s_part[((i * PB + q - q0) * 4 + j4) * 128 + r];
+          if (np == 1) {  // the tile's accumulator as it is (no 0 + x)
+            v[4 * j4] = x.x;
+            v[4 * j4 + 1] = x.y;
+            v[4 * j4 + 2] = x.z;
+            v[4 * j4 + 3] = x.w;
+          } else {
+            v[4 * j4] += x.x;
+            v[4 * j4 + 1] += x.y;
+            v[4 * j4 + 2] += x.z;
+            v[4 * j4 + 3] += x.w;
+          }
         }
       }
     }
+    final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
   }
-  final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
 }
 
 // ------------------------------------------------------------------- host
@@ -910,17 +976,7 @@ cudaError_t launch_bn(const TcParams& p, cudaStream_t st) {
   auto k = tc_stream_kernel<BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k, dim3(p.G), dim3(kTcThreads), TcCfg<BN>::SMEM, st, p);
-  if (e != cudaSuccess || !p.defer) return e;
-  if constexpr (BN >= 128) {
-    const int nch = (p.M < BN ? (p.M + 15) / 16 * 16 : BN) / 16;
-    const int pb = std::min(max_pieces(p.T, p.G, p.nkb), kFixBatch);
-    const int fsm = pb * 4 * 128 * 16;
-    e = cudaFuncSetAttribute(tc_fixup_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFixBatch * 4 * 128 * 16);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(tc_fixup_kernel<BN>, dim3(p.n_tiles * nch), dim3(128), fsm, st, p);
-  }
-  return cudaErrorInvalidValue;
+  return launch_pdl(k, dim3(p.G), dim3(kTcThreads), TcCfg<BN>::SMEM, st, p);
 }
 
 cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
@@ -931,6 +987,29 @@ cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
     case 128: return launch_bn<128>(p, st);
     default: return launch_bn<256>(p, st);
   }
+}
+
+// Slots a fixup CTA holds in shared memory (chunks x slots per chunk): 8
+// (64 KB) keeps three CTAs on an SM.
+constexpr int kFixSlots = 1;
+
+template <int BN>
+cudaError_t launch_fixup(FixParams& f, int pb, cudaStream_t st) {
+  f.pb = pb;
+  f.ch = std::max(1, std::min(kFixChunks, kFixSlots / pb));
+  int blocks = 0;
+  for (int i = 0; i < f.nparts; ++i) {
+    FixPart& q = f.q[i];
+    const int nch = (q.M < BN ? (q.M + 15) / 16 * 16 : BN) / 16;
+    q.blocks = q.n_tiles * ((nch + f.ch - 1) / f.ch);
+    blocks += q.blocks;
+  }
+  const size_t smem = (size_t)f.ch * f.pb * 4 * 128 * 16;
+  static_assert(kFixSlots <= kFixBatch * kFixChunks, "slots");
+  cudaError_t e = cudaFuncSetAttribute(tc_fixup_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(std::max(kFixSlots, kFixBatch) * 4 * 128 * 16));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tc_fixup_kernel<BN>, dim3(blocks), dim3(128), smem, st, f);
 }
 
 }  // namespace
@@ -951,48 +1030,29 @@ bool gemm_tc_supported(const GemmDesc& g) {
   return false;
 }
 
+// Token rows of each launch: more than 256 rows run as launches of whole
+// sequences (<= 256 rows each).
+int launch_rows(const GemmDesc& g) {
+  if (g.M <= 256) return g.M;
+  const int per = g.rows > 0 ? g.rows : 1;
+  return (256 / per) * per;
+}
+
 size_t gemm_tc_workspace(const GemmDesc& g, int num_sms) {
   const int n_tiles = g.nseg * gemm_tiles_per_seg(g);
   const long long T = (long long)n_tiles * (g.K / 64);
-  return part_bytes(runs_for(T, num_sms), pick_bn(g.M), n_tiles);
+  const int G = runs_for(T, num_sms), mc = launch_rows(g);
+  if (mc < 1) return 0;
+  size_t b = 0;  // every launch has its own slots: one fixup reads them all
+  for (int m0 = 0; m0 < g.M; m0 += mc) b += part_bytes(G, pick_bn(std::min(mc, g.M - m0)), n_tiles);
+  return b;
 }
 
-cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
-                                uint32_t* status, int num_sms, cudaStream_t st);
+namespace {
 
-// More than 256 token rows run as launches of whole sequences (<= 256 rows
-// each).  A row's result does not depend on the launch it is in: the
-// k-partition is a function of the tiles and K only.
-cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters, uint32_t* status,
-                           int num_sms, cudaStream_t st) {
-  if (g.M <= 256) return launch_gemm_tc_rows(g, ws, ws_bytes, counters, status, num_sms, st);
-  const int per = g.rows > 0 ? g.rows : 1;
-  const int mc = (256 / per) * per;
-  for (int m0 = 0; m0 < g.M; m0 += mc) {
-    GemmDesc c = g;
-    const int sq = m0 / per;  // first sequence of the launch
-    c.M = g.M - m0 < mc ? g.M - m0 : mc;
-    c.X = static_cast<const char*>(g.X) + (size_t)m0 * g.K * 2;
-    if (g.base_pos) c.base_pos = g.base_pos + sq;
-    if (g.valid) c.valid = g.valid + sq;
-    if (g.out_f32) c.out_f32 = g.out_f32 + (size_t)m0 * g.ldo;
-    if (g.q_out) c.q_out = static_cast<char*>(g.q_out) + (size_t)m0 * g.nq * g.d * 2;
-    if (g.act_out) c.act_out = static_cast<char*>(g.act_out) + (size_t)m0 * g.inter * 2;
-    for (int q = 0; q < g.nseg; ++q) {
-      const size_t kv = (size_t)sq * g.nkv * g.kv_cap * g.d * 2;
-      if (g.k_dst[q]) c.k_dst[q] = static_cast<char*>(g.k_dst[q]) + kv;
-      if (g.v_dst[q]) c.v_dst[q] = static_cast<char*>(g.v_dst[q]) + kv;
-    }
-    const cudaError_t e = launch_gemm_tc_rows(c, ws, ws_bytes, counters, status, num_sms, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters,
-                                uint32_t* status, int num_sms, cudaStream_t st) {
-  if (g.M == 0) return cudaSuccess;
-  TcParams p;
+// The launch parameters of one part of <= 256 token rows, its slots at ws.
+cudaError_t part_params(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters, uint32_t* status,
+                        int num_sms, TcParams& p) {
   memset(&p, 0, sizeof(p));
   p.mode = TC_GEMM;
   p.g = g;
@@ -1013,7 +1073,76 @@ cudaError_t launch_gemm_tc_rows(const GemmDesc& g, void* ws, size_t ws_bytes, ui
   for (int s = 0; s < g.nseg; ++s)
     if (!make_map(&p.wmap[s], g.seg_w[s], g.K, wrows, box_rows)) return cudaErrorInvalidValue;
   if (!make_map(&p.xmap, g.X, g.K, g.M, pick_bn(g.M))) return cudaErrorInvalidValue;
-  return launch_params(p, st);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+// The GEMM launches of every part first, then one fixup for the deferred
+// parts (BN >= 128), so a part's GEMM does not wait for the previous part's
+// fixup.  A row's result does not depend on the launch it is in: the
+// k-partition is a function of the tiles and K only.
+cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_t* counters, uint32_t* status,
+                           int num_sms, cudaStream_t st) {
+  if (g.M == 0) return cudaSuccess;
+  const int per = g.rows > 0 ? g.rows : 1;
+  const int mc = launch_rows(g);
+  if (mc < 1) return cudaErrorInvalidValue;
+  FixParams f;
+  memset(&f, 0, sizeof(f));
+  f.status = status;
+  int f_bn = 0, f_pb = 1;
+  auto flush = [&]() -> cudaError_t {
+    if (f.nparts == 0) return cudaSuccess;
+    const cudaError_t e = f_bn == 256 ? launch_fixup<256>(f, f_pb, st) : launch_fixup<128>(f, f_pb, st);
+    f.nparts = 0;
+    f_pb = 1;
+    return e;
+  };
+  size_t off = 0;
+  for (int m0 = 0; m0 < g.M; m0 += mc) {
+    GemmDesc c = g;
+    const int sq = m0 / per;  // first sequence of the launch
+    c.M = g.M - m0 < mc ? g.M - m0 : mc;
+    if (m0 > 0) {
+      c.X = static_cast<const char*>(g.X) + (size_t)m0 * g.K * 2;
+      if (g.base_pos) c.base_pos = g.base_pos + sq;
+      if (g.valid) c.valid = g.valid + sq;
+      if (g.out_f32) c.out_f32 = g.out_f32 + (size_t)m0 * g.ldo;
+      if (g.q_out) c.q_out = static_cast<char*>(g.q_out) + (size_t)m0 * g.nq * g.d * 2;
+      if (g.act_out) c.act_out = static_cast<char*>(g.act_out) + (size_t)m0 * g.inter * 2;
+      for (int q = 0; q < g.nseg; ++q) {
+        const size_t kv = (size_t)sq * g.nkv * g.kv_cap * g.d * 2;
+        if (g.k_dst[q]) c.k_dst[q] = static_cast<char*>(g.k_dst[q]) + kv;
+        if (g.v_dst[q]) c.v_dst[q] = static_cast<char*>(g.v_dst[q]) + kv;
+      }
+    }
+    TcParams p;
+    if (off > ws_bytes) return cudaErrorInvalidValue;
+    cudaError_t e = part_params(c, static_cast<char*>(ws) + off, ws_bytes - off, counters, status, num_sms, p);
+    if (e != cudaSuccess) return e;
+    const int bn = pick_bn(c.M);
+    off += part_bytes(p.G, bn, p.n_tiles);
+    e = launch_params(p, st);
+    if (e != cudaSuccess) return e;
+    if (!p.defer) continue;
+    if (f.nparts == kMaxFixParts || (f.nparts > 0 && f_bn != bn)) {
+      e = flush();
+      if (e != cudaSuccess) return e;
+    }
+    FixPart& fp = f.q[f.nparts++];
+    fp.g = c;
+    fp.part = p.part;
+    fp.T = p.T;
+    fp.M = p.M;
+    fp.tps = p.tiles_per_seg;
+    fp.n_tiles = p.n_tiles;
+    fp.nkb = p.nkb;
+    fp.G = p.G;
+    f_bn = bn;
+    f_pb = std::max(f_pb, std::min(max_pieces(p.T, p.G, p.nkb), kFixBatch));
+  }
+  return flush();
 }
 
 // ------------------------------------------------------------- LM head
