@@ -75,7 +75,8 @@ __device__ __forceinline__ Top2 ldcg_top2(const Top2* p) {
 }
 
 // Called by every CTA (all its threads) once its per-token triples are stored
-// in part[0 .. n_parts)[M].  The last of n_arrivals CTAs to arrive merges them and writes
+// in part[M][n_parts] (CTA b's triple of row m at m * n_parts + b).  The last
+// of n_arrivals CTAs to arrive merges them and writes
 // the mode's outputs.  The merge (greater value wins, lower index on equal
 // values; second = the largest other value) is associative and commutative,
 // so the warp-parallel reduction below gives the same result in any order.
@@ -96,37 +97,54 @@ __device__ __forceinline__ void head_finish(const HeadDesc& h, int n_arrivals, i
   __threadfence();
   const int M = h.M, B = h.block;
   const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int m = threadIdx.x >> 5; m < M; m += nwarps) {
-    if (!head_row_used(h, m)) continue;
-    Top2 t = top2_empty();
-    for (int b0 = 0; b0 < n_parts; b0 += 32 * 8) {  // eight loads in flight per lane
-      Top2 x[8];
+  // part is [M][n_parts]: a warp reads a row's triples as contiguous bytes.
+  // RG rows per warp at a time, QB parts per lane per row in flight: the
+  // loads of RG rows overlap instead of one row's round trip after another.
+  constexpr int RG = 8, QB = 5;
+  for (int m0 = (threadIdx.x >> 5) * RG; m0 < M; m0 += nwarps * RG) {
+    Top2 t[RG];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int b = b0 + 32 * q + lane;
-        x[q] = b < n_parts ? ldcg_top2(part + (size_t)b * M + m) : top2_empty();
+    for (int g = 0; g < RG; ++g) t[g] = top2_empty();
+    for (int b0 = 0; b0 < n_parts; b0 += 32 * QB) {
+      Top2 x[RG][QB];
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+          const int b = b0 + 32 * q + lane, m = m0 + g;
+          x[g][q] = (b < n_parts && m < M) ? ldcg_top2(part + (size_t)m * n_parts + b) : top2_empty();
+        }
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int q = 0; q < QB; ++q) t[g] = top2_merge(t[g], x[g][q]);
+    }
+#pragma unroll
+    for (int g = 0; g < RG; ++g)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        Top2 u;
+        u.v1 = __shfl_xor_sync(0xffffffffu, t[g].v1, o);
+        u.i1 = __shfl_xor_sync(0xffffffffu, t[g].i1, o);
+        u.v2 = __shfl_xor_sync(0xffffffffu, t[g].v2, o);
+        t[g] = top2_merge(t[g], u);
       }
+    // lane g writes row m0 + g
+    Top2 tl = t[0];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) t = top2_merge(t, x[q]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      Top2 u;
-      u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
-      u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
-      u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
-      t = top2_merge(t, u);
-    }
-    if (lane != 0) continue;
-    int idx = (t.i1 == INT_MAX) ? 0 : t.i1;
+    for (int g = 1; g < RG; ++g)
+      if (lane == g) tl = t[g];
+    const int m = m0 + lane;
+    if (lane >= RG || m >= M || !head_row_used(h, m)) continue;
+    int idx = (tl.i1 == INT_MAX) ? 0 : tl.i1;
     s_arg[m] = idx;
     if (h.mode == 1) {
       h.argmax[m] = idx;
-      if (h.margin) h.margin[m] = t.v1 - t.v2;
+      if (h.margin) h.margin[m] = tl.v1 - tl.v2;
     } else {
       const int s = m / B, j = m % B;
       h.drafts_out[(size_t)s * (B - 1) + j - 1] = idx;
-      if (h.margin) h.margin[(size_t)s * (B - 1) + j - 1] = t.v1 - t.v2;
+      if (h.margin) h.margin[(size_t)s * (B - 1) + j - 1] = tl.v1 - tl.v2;
     }
   }
   __syncthreads();

@@ -58,7 +58,7 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int M;          // token rows
   int defer;      // GEMM, BN >= 128: split tiles are finished by tc_fixup_kernel, not by their last piece
   float* part;    // partial slots [2 G (+ n_tiles when deferred)][BN][128] (piece_slot, tile_slot)
-  Top2* tops;     // LM head: per-CTA triples [G][M]
+  Top2* tops;     // LM head: per-CTA triples [M][G] (a row's G triples contiguous for the final merge)
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
   uint32_t* counters;
   uint32_t* status;
@@ -78,6 +78,7 @@ struct TcCfg {
   static constexpr int TAB = WIDE ? 2304 : 0;     // RowTab, 256-byte multiple
   static constexpr int SMEM = STAGES * STAGE + XCH + 256 + TAB + 1024;
   static_assert(SMEM > 117 * 1024, "a second CTA must not fit on the SM");
+  static_assert(SMEM + 17 * 1024 <= 232448, "with the kernel's ~16.5 KB of static shared memory, one SM");
 };
 
 // Run c of the G equal contiguous runs of the (tile, k-block) line [0, T).
@@ -207,13 +208,63 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
         }
       }
     }
+    if (L.topk == 0) {
+      // Greedy: each warp reduces its 32 rows' (logit, index) pairs of the
+      // 16 columns by a butterfly that halves the columns a lane holds at
+      // every step (48 shuffles in all), then merges the column's best into
+      // its own running selection s_top[warp][m]: no barrier, no shared
+      // memory exchange.  top2_merge is associative and commutative, so the
+      // grouping does not change the result.
+      const bool vr = vrow < L.V;
+      bool nan = false;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) nan |= vr && v[j] != v[j];
+      if (nan) raise_status(L.status, ST_NUMERIC);  // NaN never wins; flag it
+      float a1[16], a2[16];
+      int i1[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool ok = vr && v[j] == v[j];
+        a1[j] = ok ? v[j] : -INFINITY;
+        i1[j] = ok ? vrow : INT_MAX;
+        a2[j] = -INFINITY;
+      }
+      const int lane = r & 31;
+#pragma unroll
+      for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
+        const bool hi = (lane & o) != 0;  // keeps the upper half of its n columns
+#pragma unroll
+        for (int q = 0; q < n / 2; ++q) {
+          const float sv = hi ? a1[q] : a1[q + n / 2], sv2 = hi ? a2[q] : a2[q + n / 2];
+          const int si = hi ? i1[q] : i1[q + n / 2];
+          const Top2 mine = hi ? Top2{a1[q + n / 2], i1[q + n / 2], a2[q + n / 2]} : Top2{a1[q], i1[q], a2[q]};
+          const Top2 got{__shfl_xor_sync(0xffffffffu, sv, o), __shfl_xor_sync(0xffffffffu, si, o),
+                         __shfl_xor_sync(0xffffffffu, sv2, o)};
+          const Top2 mm = top2_merge(mine, got);
+          a1[q] = mm.v1;
+          i1[q] = mm.i1;
+          a2[q] = mm.v2;
+        }
+      }
+      Top2 tp{a1[0], i1[0], a2[0]};  // column c0 + lane / 2, over this lane pair
+      const Top2 u{__shfl_xor_sync(0xffffffffu, tp.v1, 1), __shfl_xor_sync(0xffffffffu, tp.i1, 1),
+                   __shfl_xor_sync(0xffffffffu, tp.v2, 1)};
+      tp = top2_merge(tp, u);
+      const int m = c0 + (lane >> 1);
+      if ((lane & 1) == 0 && m < M && row_used(L, m)) {
+        Top2* st = s_top + (r >> 5) * 256 + m;
+        *st = top2_merge(*st, tp);
+      }
+      return;
+    }
+    // top-k mode: k rounds over the column's 8 threads, through shared memory
     tc::named_bar(1, 128);
 #pragma unroll
     for (int j = 0; j < 16; ++j) xch[j * 128 + r] = v[j];
     tc::named_bar(1, 128);
     const int jc = et >> 3, g8 = et & 7;  // column jc, rows 16*g8 .. 16*g8+15
     const int m = c0 + jc;
-    if (L.topk > 0) {
+    {
       // k rounds: each of the column's 8 threads offers its best unselected
       // row; the winner over the 8 (greater logit, then lower index) is taken.
       const bool used = m < M && row_used(L, m);
@@ -255,25 +306,6 @@ __device__ __forceinline__ void final_chunk(const TcLocal& L, const Epi& e, int 
       }
       return;
     }
-    Top2 tp = top2_empty();
-    if (m < M && row_used(L, m)) {
-      for (int rr = 16 * g8; rr < 16 * g8 + 16; ++rr) {
-        const int vi = t * 128 + rr;
-        if (vi < L.V) top2_push(tp, xch[jc * 128 + rr], vi, L.status);
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      Top2 u;
-      u.v1 = __shfl_xor_sync(0xffffffffu, tp.v1, o);
-      u.i1 = __shfl_xor_sync(0xffffffffu, tp.i1, o);
-      u.v2 = __shfl_xor_sync(0xffffffffu, tp.v2, o);
-      tp = top2_merge(tp, u);
-    }
-    // the CTA's running selection of token row m over the tiles it finished
-    // (one writer per row: thread 8 * (m % 16))
-    if (g8 == 0 && m < M) s_top[m] = top2_merge(s_top[m], tp);
-    return;
   }
   int unit = 0;
   const bool works = tc_unit(L, t, r, unit);
@@ -449,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_last_head;
-  __shared__ Top2 s_top[256];  // LM head: best (logit, index) and runner-up of each token row so far
+  __shared__ Top2 s_top[4 * 256];  // LM head: per epilogue warp, best (logit, index) and runner-up of each token row so far
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xch = reinterpret_cast<float*>(smem + ST * Cfg::STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * Cfg::STAGE + Cfg::XCH);
@@ -610,7 +642,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     for (int j = 0; j < 16; ++j) old[j] = 0.f;
     rows.live = 0u;
     if (L.mode == TC_HEAD)
-      for (int m = et; m < 256; m += 128) s_top[m] = top2_empty();  // ordered by the barrier after accf
+      for (int m = et; m < 4 * 256; m += 128) s_top[m] = top2_empty();  // ordered by the barrier after accf
     if (L.mode == TC_GEMM && p0 < p1) {
       // Nothing loaded here is written before this run's pieces are added:
       // a tile's outputs are written once, by the piece completing its k range.
@@ -762,7 +794,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
     }
     if (L.mode == TC_HEAD && L.topk == 0) {
       tc::named_bar(1, 128);
-      for (int m = et; m < L.M; m += 128) L.tops[(size_t)blockIdx.x * L.M + m] = s_top[m];
+      for (int m = et; m < L.M; m += 128)
+        L.tops[(size_t)m * gridDim.x + blockIdx.x] =
+            top2_merge(top2_merge(s_top[m], s_top[256 + m]), top2_merge(s_top[512 + m], s_top[768 + m]));
     }
   }
   tc::tc_fence_before();

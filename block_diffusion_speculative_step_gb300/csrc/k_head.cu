@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kHeadWarps * 32) head_simt_kernel(const __grid
   for (int m = threadIdx.x; m < M; m += blockDim.x) {
     Top2 t = tsm[m];
     for (int w = 1; w < kHeadWarps; ++w) t = top2_merge(t, tsm[(size_t)w * M + m]);
-    part[(size_t)blockIdx.x * M + m] = t;
+    part[(size_t)m * gridDim.x + blockIdx.x] = t;  // [M][G]: a row's triples contiguous
   }
   head_finish(h, gridDim.x, gridDim.x, part, &s_last);
 }
