@@ -299,6 +299,44 @@ def test_rows_independent_of_batch(kind):
         assert torch.equal(a_, b_)
 
 
+@pytest.mark.parametrize("kind", ["causal", "bidir"])
+def test_rows_independent_of_batch_three_launches(kind):
+    """40 sequences of 16 rows (640 token rows) run every projection as three
+    GEMM launches (256 + 256 + 128 rows: two tile widths) whose split tiles
+    are finished by a fixup behind the launches of the same width; sequences
+    from each launch give bit-identical hidden states and K/V when run alone
+    (16 rows: partial tiles finished inline by their last piece)."""
+    w = small("bf16", d=64, block=16)
+    S, rows = 40, 16
+    g = torch.Generator().manual_seed(5)
+    h0 = torch.randn(S * rows, w.target.hidden, generator=g)
+    eng, _, _ = G.setup(w, S=S, cap=128)
+    kc = torch.randn(S, *eng.caches.tk[1].shape[1:], generator=g).to(eng.caches.tk[1].dtype)
+    vc = torch.randn(S, *eng.caches.tv[1].shape[1:], generator=g).to(eng.caches.tv[1].dtype)
+    base = [(7 * s + 3) % 100 for s in range(S)]
+
+    def run(e, seqs):
+        n = len(seqs)
+        e.caches.tk[1].copy_(kc[seqs].cuda())
+        e.caches.tv[1].copy_(vc[seqs].cuda())
+        e.base_pos.copy_(torch.tensor([base[s] for s in seqs], dtype=torch.int32))
+        e.h[:n * rows].copy_(torch.cat([h0[s * rows:(s + 1) * rows] for s in seqs]).cuda())
+        a = e.target_layer_args(1, rows, e.h)
+        if kind == "bidir":
+            a.attn_mode = D.DFLASH_ATTN_BLOCK_BIDIR
+        D.dflash_decoder_layer_forward(a, e.ws_ptr, e.ws_bytes)
+        torch.cuda.synchronize()
+        assert e.status() == D.DFLASH_OK
+        return e.h[:n * rows].clone().cpu(), e.caches.tk[1][:n].clone().cpu(), e.caches.tv[1][:n].clone().cpu()
+
+    hb, kb, vb = run(eng, list(range(S)))
+    one, _, _ = G.setup(w, S=1, cap=128)
+    for s in (0, 17, 39):  # one sequence from each launch
+        ha, ka, va = run(one, [s])
+        assert torch.equal(ha, hb[s * rows:(s + 1) * rows]), s
+        assert torch.equal(ka[0], kb[s]) and torch.equal(va[0], vb[s]), s
+
+
 def _path_factors(eng, w, seed, dtype):
     """O(1)-scale selector factors, so scores are O(1) and a fixed near-tie
     threshold is meaningful; installed on the device, returned for the oracle."""
