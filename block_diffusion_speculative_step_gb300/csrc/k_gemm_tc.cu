@@ -809,16 +809,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
 }
 
 // Tiles of a deferred launch (BN >= 128), once the GEMM grid has completed:
-// one CTA of 128 threads per (tile, group of `ch` 16-column chunks); thread
-// r sums accumulator row r's partial slots in k order and runs each chunk's
-// epilogue -- the arithmetic and order of a last piece finishing its tile
-// inline (a tile that one run covers: its accumulator as it is), spread over
-// every SM instead of one CTA per tile.  Each thread first copies its own
-// 16-byte blocks of every slot of every chunk into shared memory (cp.async,
-// one group per chunk), so the copies, the row table and the epilogues of the
-// earlier chunks overlap, and the slots cost no registers.
-constexpr int kFixBatch = 8;   // most slots held per chunk
-constexpr int kFixChunks = 4;  // most chunks per CTA
+// one CTA of 128 threads per (part, tile, 16-column chunk); thread r sums
+// accumulator row r's partial slots in k order and runs the chunk's epilogue
+// -- the arithmetic and order of a last piece finishing its tile inline (a
+// tile that one run covers: its accumulator as it is), spread over every SM
+// instead of one CTA per tile.  Each thread first copies its own 16-byte
+// blocks of the slots into shared memory (cp.async), then the row table is
+// built, so the two latencies overlap and the slots cost no registers.
+constexpr int kFixBatch = 8;  // most slots held in shared memory (more: in batches)
 
 // The deferred launches finished by one fixup launch: a projection of more
 // than 256 token rows runs as several GEMM launches (whole sequences each)
@@ -829,13 +827,12 @@ struct FixPart {
   float* part;
   long long T;
   int M, tps, n_tiles, nkb, G;
-  int blocks;  // fixup CTAs of this part: n_tiles x chunk groups
+  int blocks;  // fixup CTAs of this part: n_tiles x 16-column chunks
 };
 struct FixParams {
   FixPart q[kMaxFixParts];
   int nparts;
-  int ch;  // chunks per CTA
-  int pb;  // slots per chunk held in shared memory ([ch][pb][4][128] float4)
+  int pb;  // slots held in shared memory ([pb][4][128] float4)
   uint32_t* status;
 };
 static_assert(sizeof(FixParams) <= 4000, "fixup parameters fit the classic 4 KB parameter space");
@@ -844,19 +841,9 @@ __device__ __forceinline__ void part_copy16(void* sdst, const void* g) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(sdst)), "l"(g) : "memory");
 }
 
-// Waits until at most n of this thread's cp.async groups are pending (n < 4).
-__device__ __forceinline__ void part_wait(int n) {
-  switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-  }
-}
-
 template <int BN>
 __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant__ FixParams fp) {
-  extern __shared__ float4 s_part[];  // [ch][pb][4][128]: chunk i, slot q, block j4 of row r
+  extern __shared__ float4 s_part[];  // [pb][4][128]: slot q's block j4 of row r at (q * 4 + j4) * 128 + r
   __shared__ RowTab s_tab;
   __shared__ float s_xch[16 * 128];
   pdl_wait();
@@ -880,46 +867,41 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
   L.row0 = P.g.seg_row0;
   L.part = P.part;
   L.status = fp.status;
-  const int nkb = L.nkb, CH = fp.ch, PB = fp.pb;
+  const int nkb = L.nkb, PB = fp.pb;
   const int nch = min(BN, ((L.M + 15) / 16) * 16) / 16;
-  const int ngrp = (nch + CH - 1) / CH;
-  const int t = bid / ngrp, cg = (bid % ngrp) * CH;  // the tile and its first chunk
-  const int nc = min(CH, nch - cg);
+  const int t = bid / nch, c0 = (bid % nch) * 16;
   const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
   const int first = run_of(tbeg, L.T, L.G), last = run_of(tend - 1, L.T, L.G);
   const bool first_tail = run_start(L.T, L.G, first) < tbeg;
-  const int r = threadIdx.x, lane = r & 31, w = r >> 5;
+  const int r = threadIdx.x, lane = r & 31;
   const int np = last - first + 1;  // pieces, in k order
   uint32_t dyn;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-  const bool batched = np > PB;  // more pieces than a chunk holds: one chunk, in batches of PB
-  if ((batched && CH != 1) || CH > kFixChunks || (size_t)CH * PB * 4 * 128 * 16 > dyn) {  // uniform
+  if (PB < 1 || (size_t)PB * 4 * 128 * 16 > dyn) {  // uniform
     if (r == 0) raise_status(L.status, ST_RANGE);
     return;
   }
-  auto slot_src = [&](int q, int c0, int j4) {
-    const size_t slot = np == 1 ? tile_slot(L.G, t) : piece_slot(first + q, first, first_tail);
-    return L.part + slot * BN * 128 + part_off(c0, j4, r);
-  };
-  // every chunk's slots first: they depend on nothing below
-  for (int i = 0; i < nc; ++i) {
-    for (int q = 0; q < np && q < PB; ++q)
+  auto copy_batch = [&](int q0) {  // slots q0 .. q0 + PB - 1, one cp.async group
+    for (int q = q0; q < np && q < q0 + PB; ++q) {
+      const size_t slot = np == 1 ? tile_slot(L.G, t) : piece_slot(first + q, first, first_tail);
+      const float* src = L.part + slot * BN * 128;
 #pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((i * PB + q) * 4 + j4) * 128 + r], slot_src(q, (cg + i) * 16, j4));
+      for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((q - q0) * 4 + j4) * 128 + r], src + part_off(c0, j4, r));
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
-  }
+  };
+  copy_batch(0);  // depends on nothing below
   Epi e = make_epi(P.g, t / L.tps);
   e.status = L.status;
-  // row operands of the 32-row words holding the chunks (warp w: word w)
-  const int w0 = (cg * 16) >> 5, nw = (((cg + nc) * 16 + 31) >> 5) - w0;
-  if (w < nw) {
-    const int m = ((w0 + w) << 5) + lane;
+  // row operands of the 32-row word holding the chunk (warp 0)
+  if (r < 32) {
+    const int m = (c0 & ~31) + lane;
     const bool in = m < L.M;
     const int sq = in ? m / e.rows : 0;
     const int bp = (in && e.kind == EPI_QKV) ? __ldg(e.base_pos + sq) : 0;  // issued with the valid load
     const bool lv = in && (e.valid == nullptr || (m % e.rows) < __ldg(e.valid + sq));
     const uint32_t bits = __ballot_sync(0xffffffffu, lv);
-    if (lane == 0) s_tab.live[w0 + w] = bits;
+    if (lane == 0) s_tab.live[c0 >> 5] = bits;
     int pos = -1;
     uint32_t kvr = ~0u;
     if (e.kind == EPI_QKV && lv) {
@@ -934,43 +916,35 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
     s_tab.kvr[m] = kvr;
   }
   __syncthreads();
+  float pre[32];
   int unit = 0;
   const bool works = tc_unit(L, t, r, unit);
-  for (int i = 0; i < nc; ++i) {
-    const int c0 = (cg + i) * 16;
-    float pre[32];
-    wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
-    float v[16];
+  wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
+  float v[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-    for (int q0 = 0; q0 < np; q0 += PB) {
-      if (q0 > 0) {  // batched (one chunk): the next PB slots
-        for (int q = q0; q < np && q < q0 + PB; ++q)
+  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+  for (int q0 = 0; q0 < np; q0 += PB) {
+    if (q0 > 0) copy_batch(q0);
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's own copies: no barrier needed
+    for (int q = q0; q < np && q < q0 + PB; ++q) {
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) part_copy16(&s_part[((q - q0) * 4 + j4) * 128 + r], slot_src(q, c0, j4));
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      }
-      part_wait(q0 > 0 ? 0 : nc - 1 - i);  // this thread's own copies: no barrier needed
-      for (int q = q0; q < np && q < q0 + PB; ++q) {
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const float4 x = s_part[((i * PB + q - q0) * 4 + j4) * 128 + r];
-          if (np == 1) {  // the tile's accumulator as it is (no 0 + x)
-            v[4 * j4] = x.x;
-            v[4 * j4 + 1] = x.y;
-            v[4 * j4 + 2] = x.z;
-            v[4 * j4 + 3] = x.w;
-          } else {
-            v[4 * j4] += x.x;
-            v[4 * j4 + 1] += x.y;
-            v[4 * j4 + 2] += x.z;
-            v[4 * j4 + 3] += x.w;
-          }
+      for (int j4 = 0; j4 < 4; ++j4) {
+        const float4 x = s_part[((q - q0) * 4 + j4) * 128 + r];
+        if (np == 1) {  // the tile's accumulator as it is (no 0 + x)
+          v[4 * j4] = x.x;
+          v[4 * j4 + 1] = x.y;
+          v[4 * j4 + 2] = x.z;
+          v[4 * j4 + 3] = x.w;
+        } else {
+          v[4 * j4] += x.x;
+          v[4 * j4 + 1] += x.y;
+          v[4 * j4 + 2] += x.z;
+          v[4 * j4 + 3] += x.w;
         }
       }
     }
-    final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
   }
+  final_wide(L, e, &s_tab, t, c0, r, v, s_xch, pre);
 }
 
 // ------------------------------------------------------------------- host
@@ -1023,25 +997,18 @@ cudaError_t launch_params(const TcParams& p, cudaStream_t st) {
   }
 }
 
-// Slots a fixup CTA holds in shared memory (chunks x slots per chunk): 8
-// (64 KB) keeps three CTAs on an SM.
-constexpr int kFixSlots = 1;
-
 template <int BN>
 cudaError_t launch_fixup(FixParams& f, int pb, cudaStream_t st) {
   f.pb = pb;
-  f.ch = std::max(1, std::min(kFixChunks, kFixSlots / pb));
   int blocks = 0;
   for (int i = 0; i < f.nparts; ++i) {
     FixPart& q = f.q[i];
-    const int nch = (q.M < BN ? (q.M + 15) / 16 * 16 : BN) / 16;
-    q.blocks = q.n_tiles * ((nch + f.ch - 1) / f.ch);
+    q.blocks = q.n_tiles * ((q.M < BN ? (q.M + 15) / 16 * 16 : BN) / 16);
     blocks += q.blocks;
   }
-  const size_t smem = (size_t)f.ch * f.pb * 4 * 128 * 16;
-  static_assert(kFixSlots <= kFixBatch * kFixChunks, "slots");
+  const size_t smem = (size_t)f.pb * 4 * 128 * 16;
   cudaError_t e = cudaFuncSetAttribute(tc_fixup_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(std::max(kFixSlots, kFixBatch) * 4 * 128 * 16));
+                                       kFixBatch * 4 * 128 * 16);
   if (e != cudaSuccess) return e;
   return launch_pdl(tc_fixup_kernel<BN>, dim3(blocks), dim3(128), smem, st, f);
 }
