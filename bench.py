@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft-block steps/s & verified tok/s at batch 1/32; HBM GB/s as % of roofline"
 UNIT = "draft-block steps/s"  # one step: a whole draft-and-verify cycle of one sequence
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1700.0  # sustained bf16, the fallback for a kernel timed inside a long step
 
 
 def parse():
@@ -193,6 +194,35 @@ def layer_weight_bytes(s, es: int = 2) -> float:
     """Weight bytes of one decoder layer: QKV, O, gate+up, down (each read once)."""
     qkv = (s.n_q + 2 * s.n_kv) * s.head_dim * s.hidden
     return float(es * (qkv + s.hidden * s.n_q * s.head_dim + 3 * s.hidden * s.inter))
+
+
+def layer_gemm_params(s) -> float:
+    """Weights of one decoder layer's four projections (QKV, O, gate+up, down)."""
+    qkv = (s.n_q + 2 * s.n_kv) * s.head_dim * s.hidden
+    return float(qkv + s.hidden * s.n_q * s.head_dim + 3 * s.hidden * s.inter)
+
+
+def gemm_flops_per_cycle(w, rows_committed: float) -> float:
+    """Algorithmic flops (2 per multiply-add) of the GEMM family in one cycle:
+    every draft and target layer over all S*B block rows, and the fusion's
+    FC and K/V-injection projections over the committed rows."""
+    M = w.batch * w.block
+    H = w.draft.hidden
+    fuse = H * len(w.taps) * H + w.draft.layers * 2 * w.draft.n_kv * w.draft.head_dim * H
+    return 2.0 * (M * (w.draft.layers * layer_gemm_params(w.draft) + w.target.layers * layer_gemm_params(w.target))
+                  + rows_committed * fuse)
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a family timed inside a long step:
+    the measured sustained cuBLAS figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        if "bf16_tflops_sustained" in pk:
+            return float(pk["bf16_tflops_sustained"]), "measured bf16_tflops_sustained (of measured)"
+    return FALLBACK_BF16_TFLOPS, "fallback bf16 TFLOP/s"
 
 
 def kv_bytes(s, keys: int, es: int = 2) -> float:
@@ -565,6 +595,14 @@ def run_b32(args, model, world: int, hbm: float, src: str) -> dict:
         ab = attention_bytes_per_cycle(w, lens, True)
         rec["rooflines"]["attention"] = roof(ab / (attn[1] / 1000.0) / 1e9, hbm, src, bytes_per_cycle=ab,
                                              launches_per_cycle=attn[0], avg_launch_us=1000.0 * attn[1] / attn[0])
+    gm = fam.get("gemm_tc")
+    if gm:  # at 512 block rows the projections are dense contractions: tensor-bound
+        fl = gemm_flops_per_cycle(w, tokens)
+        tp, tsrc = tensor_peak()
+        ach = fl / (gm[1] / 1000.0) / 1e12
+        rec["rooflines"]["gemm_tc"] = {"bound": "tensor", "achieved": ach, "peak": tp, "unit": "TFLOP/s",
+                                       "frac": ach / tp, "peak_source": tsrc, "flops_per_cycle": fl,
+                                       "launches_per_cycle": gm[0], "ms_per_cycle": gm[1]}
     del graph, dgraph, eng
     torch.cuda.empty_cache()
     return rec

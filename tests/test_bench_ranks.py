@@ -84,3 +84,22 @@ def test_cost_model_matches_the_worked_example():
         assert c["verify_and_fusion_ms"] == g["t_verify_ms"]
     sp = g["baseline_ms_per_token"] / bench.cost_model(g["t_draft_ms"], cycle, 6)["per_token_ms"]
     assert abs(sp - g["speedup_at_6"]) <= g["speedup_tol"]
+
+
+def test_gemm_flops_of_the_32_sequence_cycle():
+    """The tensor roofline's algorithmic flops: 2 per multiply-add of every
+    projection weight with every row it multiplies (41 layers of 512 block
+    rows; the fusion projections over the committed rows), written out from
+    the Qwen3-8B layer shape (32 query heads, 8 KV heads, head dim 128,
+    hidden 4096, MLP 12288)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_diffusion_speculative_step_gb300 import synth
+
+    w = synth.WORKLOADS["qwen3-8b-b32"]
+    layer = (32 + 2 * 8) * 128 * 4096 + 4096 * 32 * 128 + 3 * 4096 * 12288  # 192,937,984 weights
+    assert layer == 192_937_984
+    rows = 32 * 16
+    fuse = 4096 * 5 * 4096 + 5 * 2 * 8 * 128 * 4096  # FC over 5 taps + K/V injection of 5 draft layers
+    assert bench.gemm_flops_per_cycle(w, 0) == 2.0 * rows * 41 * layer
+    assert bench.gemm_flops_per_cycle(w, 183) == 2.0 * (rows * 41 * layer + 183 * fuse)
