@@ -57,6 +57,8 @@ struct TcParams {  // the CUtensorMap members keep it 64-byte aligned
   int G;          // CTAs (runs)
   int M;          // token rows
   int defer;      // GEMM, BN >= 128: split tiles are finished by tc_fixup_kernel, not by their last piece
+  int M_b;        // tc_pair_kernel: token rows of the second 256-row part (its X box starts at row 256)
+  float* part_b;  // tc_pair_kernel: the second part's slots (same layout as `part`)
   float* part;    // partial slots [2 G (+ n_tiles when deferred)][BN][128] (piece_slot, tile_slot)
   Top2* tops;     // LM head: per-CTA triples [M][G] (a row's G triples contiguous for the final merge)
   Cand* tlist;    // LM head, top-k mode: per-tile lists [n_tiles][M][topk]
@@ -808,6 +810,234 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_stream_kernel(const __grid_c
   if (L.mode == TC_HEAD) head_finish(p.h, gridDim.x, gridDim.x, L.tops, &s_last_head);
 }
 
+// Two 256-row parts of a deferred projection in one launch: each weight
+// k-block lands in shared memory once and feeds the MMAs of both parts (two
+// accumulators of 256 columns: all 512 TMEM columns), so the weights cross
+// HBM once for up to 512 token rows.  The run partition, every piece's k
+// range and the partial slots are those of two separate launches, so the
+// fixup and every row's bits are unchanged; with both accumulators in use,
+// a piece's MMAs wait until the epilogue has stored the previous piece's
+// partials.  Rings: kPairW weight k-blocks and kPairX token-row half blocks
+// (a k-block takes two), each slot freed by the MMAs that read it.
+constexpr int kPairW = 4, kPairX = 4;
+struct PairCfg {
+  static constexpr int WB = kTcA;       // one 128 x 64 weight box pair, bytes
+  static constexpr int XB = 256 * 128;  // 256 token rows x 64, bytes
+  static constexpr int RING = kPairW * WB + kPairX * XB;
+  static constexpr int SMEM = RING + 256 + 1024;
+  static_assert(SMEM > 117 * 1024 && SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert((2 * kPairW + 2 * kPairX + 2) * 8 + 8 <= 256, "barriers fit their 256 bytes");
+  static_assert(kPairX % 2 == 0, "a k-block's two halves take consecutive slots");
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* xring = smem + kPairW * PairCfg::WB;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + PairCfg::RING);
+  uint64_t* wempty = wfull + kPairW;
+  uint64_t* xfull = wempty + kPairW;
+  uint64_t* xempty = xfull + kPairX;
+  uint64_t* accf = xempty + kPairX;  // both accumulators hold a finished piece (MMA -> epilogue)
+  uint64_t* acce = accf + 1;         // both drained (epilogue -> MMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const TcLocal L = tc_local(p);
+  const CUtensorMap* wmaps = p.wmap;
+  const CUtensorMap* xmap = &p.xmap;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = L.nkb;
+  const long long p0 = run_start(L.T, L.G, blockIdx.x), p1 = run_start(L.T, L.G, blockIdx.x + 1);
+  const int n_my = (int)(p1 - p0);
+  const uint64_t lim = wait_limit_ns(L.status);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairW; ++s) {
+      tc::mbar_init(&wfull[s], 1);
+      tc::mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < kPairX; ++s) {
+      tc::mbar_init(&xfull[s], 1);
+      tc::mbar_init(&xempty[s], 1);
+    }
+    tc::mbar_init(accf, 1);
+    tc::mbar_init(acce, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.g.nseg; ++s) tc::tma_prefetch_desc(wmaps + s);
+    tc::tma_prefetch_desc(xmap);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint64_t pol_w = tc::policy_evict_first();
+      const uint64_t pol_x = tc::policy_evict_last();
+      const bool swiglu = L.kind == EPI_SWIGLU;
+      const int tps = L.tps, inter = L.inter, row0 = L.row0;
+      int t = (int)(p0 / nkb), kb = (int)(p0 - (long long)t * nkb);  // position of the next W load
+      int kb_x = kb;                                                   // k-block of the next X load
+      auto load_w = [&](int i) {
+        uint8_t* a = smem + (i % kPairW) * PairCfg::WB;
+        uint64_t* bar = &wfull[i % kPairW];
+        const int kx = kb * 64, seg = t / tps, tile = t - seg * tps;
+        tc::mbar_arrive_expect_tx(bar, PairCfg::WB);
+        if (swiglu) {
+          tc::tma_load_2d(a, wmaps + seg, kx, tile * 64, bar, pol_w);
+          tc::tma_load_2d(a + kTcA / 2, wmaps + seg, kx, inter + tile * 64, bar, pol_w);
+        } else {
+          tc::tma_load_2d(a, wmaps + seg, kx, row0 + tile * 128, bar, pol_w);
+        }
+        if (++kb == nkb) {
+          kb = 0;
+          ++t;
+        }
+      };
+      auto load_x = [&](int i) {  // both 256-row halves of k-block i
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int sl = (2 * i + h) % kPairX;
+          tc::mbar_arrive_expect_tx(&xfull[sl], PairCfg::XB);
+          tc::tma_load_2d(xring + sl * PairCfg::XB, xmap, kb_x * 64, 256 * h, &xfull[sl], pol_x);
+        }
+        if (++kb_x == nkb) kb_x = 0;
+      };
+      // weights depend on nothing upstream: fill their ring before the wait
+      const int prw = n_my < kPairW ? n_my : kPairW, prx = n_my < kPairX / 2 ? n_my : kPairX / 2;
+      for (int i = 0; i < prw; ++i) load_w(i);
+      pdl_wait();
+      for (int i = 0; i < prx; ++i) load_x(i);
+      // the MMAs of k-block j free its two X slots (for k-block j + kPairX / 2)
+      // and its W slot (for k-block j + kPairW); the X halves are needed first
+      int iw = prw, ix = prx;
+      bool ok = true;
+      while (ok && (ix < n_my || iw < n_my)) {
+        if (ix < n_my) {
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int u = 2 * ix + h;
+            if (!tc::mbar_wait(&xempty[u % kPairX], ((uint32_t)(u / kPairX) & 1u) ^ 1u, abort, lim)) {
+              tc_timeout(L.status, abort);
+              ok = false;
+            }
+          }
+          if (!ok) break;
+          load_x(ix++);
+        }
+        if (iw < n_my) {
+          if (!tc::mbar_wait(&wempty[iw % kPairW], ((uint32_t)(iw / kPairW) & 1u) ^ 1u, abort, lim)) {
+            tc_timeout(L.status, abort);
+            break;
+          }
+          load_w(iw++);
+        }
+      }
+      // every issued copy has landed before this CTA's shared memory goes away
+      for (int i = (iw > kPairW ? iw - kPairW : 0); i < iw; ++i)
+        tc::mbar_wait(&wfull[i % kPairW], (uint32_t)(i / kPairW) & 1u, nullptr, lim);
+      for (int u = (2 * ix > kPairX ? 2 * ix - kPairX : 0); u < 2 * ix; ++u)
+        tc::mbar_wait(&xfull[u % kPairX], (uint32_t)(u / kPairX) & 1u, nullptr, lim);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: both parts of every k-block of a piece
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
+      const uint32_t wbase = tc::smem_u32(smem), xbase = tc::smem_u32(xring);
+      long long pos = p0;
+      int i = 0, k = 0;
+      bool stop = false;
+      while (pos < p1 && !stop) {
+        const int t = (int)(pos / nkb);
+        const long long end = p1 < (long long)(t + 1) * nkb ? p1 : (long long)(t + 1) * nkb;
+        if (!tc::mbar_wait(acce, ((uint32_t)k & 1u) ^ 1u, abort, lim)) {
+          tc_timeout(L.status, abort);
+          break;
+        }
+        tc::tc_fence_after();
+        for (long long q = pos; q < end; ++q, ++i) {
+          const int sw = i % kPairW, sx0 = (2 * i) % kPairX, sx1 = (2 * i + 1) % kPairX;
+          if (!tc::mbar_wait(&wfull[sw], (uint32_t)(i / kPairW) & 1u, abort, lim) ||
+              !tc::mbar_wait(&xfull[sx0], (uint32_t)((2 * i) / kPairX) & 1u, abort, lim) ||
+              !tc::mbar_wait(&xfull[sx1], (uint32_t)((2 * i + 1) / kPairX) & 1u, abort, lim)) {
+            tc_timeout(L.status, abort);
+            stop = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t a = wbase + (uint32_t)(sw * PairCfg::WB);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t bb = xbase + (uint32_t)((h ? sx1 : sx0) * PairCfg::XB);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc::mma_bf16(tmem + (uint32_t)(h * 256), tc::sdesc_sw128(a + 32 * j), tc::sdesc_sw128(bb + 32 * j),
+                           idesc, (q > pos || j > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&wempty[sw]);
+          tc::mma_commit(&xempty[sx0]);
+          tc::mma_commit(&xempty[sx1]);
+        }
+        tc::mma_commit(accf);  // arrives when this piece's MMAs completed
+        pos = end;
+        ++k;
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 store both accumulators of each piece
+    pdl_wait();  // the slots may still be read by the fixup of the launch before
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // accumulator row = weight row within the tile
+    const int et = threadIdx.x - 64;
+    const int ncol[2] = {min(256, ((p.M + 15) / 16) * 16), min(256, ((p.M_b + 15) / 16) * 16)};
+    long long pos = p0;
+    int k = 0;
+    while (pos < p1) {
+      const int t = (int)(pos / nkb);
+      const long long tbeg = (long long)t * nkb, tend = tbeg + nkb;
+      const long long end = p1 < tend ? p1 : tend;
+      const bool whole = (pos == tbeg && end == tend);
+      if (!tc::mbar_wait(accf, (uint32_t)k & 1u, abort, lim)) tc_timeout(L.status, abort);
+      tc::named_bar(1, 128);
+      if (*abort) break;  // uniform: read after the barrier
+      tc::tc_fence_after();
+      // piece_slot of this piece; a whole tile has a slot of its own
+      const size_t slot = whole ? tile_slot(L.G, t) : 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float* dst0 = (h ? p.part_b : L.part) + slot * 256 * 128;
+        const uint32_t trow = tmem + (uint32_t)(h * 256) + ((uint32_t)(q4 * 32) << 16);
+        for (int c0 = 0; c0 < ncol[h]; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(trow + c0, v);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4)
+            *reinterpret_cast<float4*>(dst0 + part_off(c0, j4, r)) =
+                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::named_bar(1, 128);
+      if (et == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(acce)) : "memory");
+      pos = end;
+      ++k;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
 // Tiles of a deferred launch (BN >= 128), once the GEMM grid has completed:
 // one CTA of 128 threads per (part, tile, 16-column chunk); thread r sums
 // accumulator row r's partial slots in k order and runs the chunk's epilogue
@@ -973,6 +1203,12 @@ size_t part_bytes(int G, int bn, int n_tiles = 0) {
   return ((size_t)2 * G + (bn >= 128 ? (size_t)n_tiles : 0)) * bn * 128 * sizeof(float);
 }
 
+// Two 256-row parts of a projection as one paired launch (tc_pair_kernel).
+#ifndef DFLASH_GEMM_PAIR
+#define DFLASH_GEMM_PAIR 1
+#endif
+constexpr bool kGemmPair = DFLASH_GEMM_PAIR != 0;
+
 // Most pieces any tile has: runs are at least floor(T / G) k-blocks long.
 int max_pieces(long long T, int G, int nkb) {
   const long long lmin = T / G;
@@ -1092,6 +1328,17 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_
   FixParams f;
   memset(&f, 0, sizeof(f));
   f.status = status;
+  auto add_part = [&](const GemmDesc& c, const TcParams& p, float* part) {
+    FixPart& fp = f.q[f.nparts++];
+    fp.g = c;
+    fp.part = part;
+    fp.T = p.T;
+    fp.M = c.M;
+    fp.tps = p.tiles_per_seg;
+    fp.n_tiles = p.n_tiles;
+    fp.nkb = p.nkb;
+    fp.G = p.G;
+  };
   int f_bn = 0, f_pb = 1;
   auto flush = [&]() -> cudaError_t {
     if (f.nparts == 0) return cudaSuccess;
@@ -1100,6 +1347,40 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_
     f_pb = 1;
     return e;
   };
+  // Two 256-row parts (more than 384 and at most 512 rows, whole sequences
+  // of a 256-row boundary): one paired launch, the weights read once.
+  if (kGemmPair && mc == 256 && g.M > 384 && g.M <= 512) {
+    GemmDesc c0 = g, c1 = g;
+    c0.M = 256;
+    c1.M = g.M - 256;
+    const int sq = 256 / per;
+    c1.X = static_cast<const char*>(g.X) + (size_t)256 * g.K * 2;
+    if (g.base_pos) c1.base_pos = g.base_pos + sq;
+    if (g.valid) c1.valid = g.valid + sq;
+    if (g.out_f32) c1.out_f32 = g.out_f32 + (size_t)256 * g.ldo;
+    if (g.q_out) c1.q_out = static_cast<char*>(g.q_out) + (size_t)256 * g.nq * g.d * 2;
+    if (g.act_out) c1.act_out = static_cast<char*>(g.act_out) + (size_t)256 * g.inter * 2;
+    for (int q = 0; q < g.nseg; ++q) {
+      const size_t kv = (size_t)sq * g.nkv * g.kv_cap * g.d * 2;
+      if (g.k_dst[q]) c1.k_dst[q] = static_cast<char*>(g.k_dst[q]) + kv;
+      if (g.v_dst[q]) c1.v_dst[q] = static_cast<char*>(g.v_dst[q]) + kv;
+    }
+    TcParams p;
+    cudaError_t e = part_params(c0, ws, ws_bytes, counters, status, num_sms, p);
+    if (e != cudaSuccess) return e;
+    const size_t b0 = part_bytes(p.G, 256, p.n_tiles);
+    if (ws_bytes < 2 * b0) return cudaErrorInvalidValue;
+    p.M_b = c1.M;
+    p.part_b = reinterpret_cast<float*>(static_cast<char*>(ws) + b0);
+    if (!make_map(&p.xmap, g.X, g.K, g.M, 256)) return cudaErrorInvalidValue;  // both halves
+    e = cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(tc_pair_kernel, dim3(p.G), dim3(kTcThreads), PairCfg::SMEM, st, p);
+    if (e != cudaSuccess) return e;
+    add_part(c0, p, p.part);
+    add_part(c1, p, p.part_b);
+    return launch_fixup<256>(f, std::min(max_pieces(p.T, p.G, p.nkb), kFixBatch), st);
+  }
   size_t off = 0;
   for (int m0 = 0; m0 < g.M; m0 += mc) {
     GemmDesc c = g;
@@ -1131,15 +1412,7 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, void* ws, size_t ws_bytes, uint32_
       e = flush();
       if (e != cudaSuccess) return e;
     }
-    FixPart& fp = f.q[f.nparts++];
-    fp.g = c;
-    fp.part = p.part;
-    fp.T = p.T;
-    fp.M = p.M;
-    fp.tps = p.tiles_per_seg;
-    fp.n_tiles = p.n_tiles;
-    fp.nkb = p.nkb;
-    fp.G = p.G;
+    add_part(c, p, p.part);
     f_bn = bn;
     f_pb = std::max(f_pb, std::min(max_pieces(p.T, p.G, p.nkb), kFixBatch));
   }
