@@ -93,12 +93,20 @@ cudaError_t launch_embed(int dtype, const void* E, int H, int V, int n_seqs, int
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __restrict__ h, const T* __restrict__ g,
                                                               int H, float eps, T* __restrict__ x) {
+  const bool fits = H <= 4 * kRowThreads * kRowVec;
+  float4 gg[kRowVec];  // the gain is no kernel's output: loaded before the wait
+  if (fits) {
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+      const int k = 4 * (threadIdx.x + i * kRowThreads);
+      gg[i] = k < H ? ld4(g + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[32];
   const float* r = h + (size_t)blockIdx.x * H;
   T* o = x + (size_t)blockIdx.x * H;
-  const bool fits = H <= 4 * kRowThreads * kRowVec;
   float4 v[kRowVec];
   float ss = 0.f;
   if (fits) {
@@ -127,10 +135,9 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __res
 #pragma unroll
     for (int i = 0; i < kRowVec; ++i) {
       const int k = 4 * (threadIdx.x + i * kRowThreads);
-      if (k < H) {
-        const float4 gg = ld4(g + k);
-        st4(o + k, make_float4(v[i].x * inv * gg.x, v[i].y * inv * gg.y, v[i].z * inv * gg.z, v[i].w * inv * gg.w));
-      }
+      if (k < H)
+        st4(o + k, make_float4(v[i].x * inv * gg[i].x, v[i].y * inv * gg[i].y, v[i].z * inv * gg[i].z,
+                               v[i].w * inv * gg[i].w));
     }
   } else {
     for (int k = threadIdx.x; k < H; k += kRowThreads) o[k] = from_f<T>(r[k] * inv * to_f<T>(g[k]));

@@ -1011,6 +1011,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
       // piece_slot of this piece; a whole tile has a slot of its own
       const size_t slot = whole ? tile_slot(L.G, t) : 2 * (size_t)blockIdx.x + (p0 < tbeg ? 1u : 0u);
 #pragma unroll
+      const uint64_t keep = tc::policy_evict_last();
       for (int h = 0; h < 2; ++h) {
         float* dst0 = (h ? p.part_b : L.part) + slot * 256 * 128;
         const uint32_t trow = tmem + (uint32_t)(h * 256) + ((uint32_t)(q4 * 32) << 16);
@@ -1019,8 +1020,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
           tc::tmem_ld16(trow + c0, v);
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4)
-            *reinterpret_cast<float4*>(dst0 + part_off(c0, j4, r)) =
-                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+            tc::st_global_hint(dst0 + part_off(c0, j4, r), make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]), keep);
         }
       }
       tc::tc_fence_before();
