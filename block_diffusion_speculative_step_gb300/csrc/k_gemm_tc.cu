@@ -1015,7 +1015,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
       for (int h = 0; h < 2; ++h) {
         float* dst0 = (h ? p.part_b : L.part) + slot * 256 * 128;
         const uint32_t trow = tmem + (uint32_t)(h * 256) + ((uint32_t)(q4 * 32) << 16);
-        for (int c0 = 0; c0 < ncol[h]; c0 += 16) {
+        int c0 = 0;
+        for (; c0 + 64 <= ncol[h]; c0 += 64) {  // four chunks per TMEM load: one wait instead of four
+          float v[64];
+          tc::tmem_ld64(trow + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            tc::st_global_hint(dst0 + part_off(c0 + 16 * (j >> 2), j & 3, r),
+                               make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), keep);
+        }
+        for (; c0 < ncol[h]; c0 += 16) {
           float v[16];
           tc::tmem_ld16(trow + c0, v);
 #pragma unroll
@@ -1076,8 +1085,6 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
   extern __shared__ float4 s_part[];  // [pb][4][128]: slot q's block j4 of row r at (q * 4 + j4) * 128 + r
   __shared__ RowTab s_tab;
   __shared__ float s_xch[16 * 128];
-  pdl_wait();
-  pdl_launch_dependents();
   int bid = (int)blockIdx.x, pi = 0;
   while (pi + 1 < fp.nparts && bid >= fp.q[pi].blocks) bid -= fp.q[pi++].blocks;
   const FixPart& P = fp.q[pi];
@@ -1120,7 +1127,9 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  copy_batch(0);  // depends on nothing below
+  // The row table and the RoPE operands come from inputs (positions, valid
+  // lengths, the RoPE table) that no kernel of the call writes: resolved
+  // before the wait, while the GEMM still runs.
   Epi e = make_epi(P.g, t / L.tps);
   e.status = L.status;
   // row operands of the 32-row word holding the chunk (warp 0)
@@ -1149,7 +1158,11 @@ __global__ void __launch_bounds__(128, 6) tc_fixup_kernel(const __grid_constant_
   float pre[32];
   int unit = 0;
   const bool works = tc_unit(L, t, r, unit);
-  wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
+  if (e.kind == EPI_QKV) wide_loads(e, &s_tab, unit, works, c0, L.M, pre);
+  pdl_wait();
+  pdl_launch_dependents();
+  copy_batch(0);
+  if (e.kind != EPI_QKV) wide_loads(e, &s_tab, unit, works, c0, L.M, pre);  // the residual: the GEMM's predecessors' output
   float v[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = 0.f;
