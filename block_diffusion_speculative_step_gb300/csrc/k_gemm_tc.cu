@@ -25,7 +25,9 @@
 // every piece only stores its accumulator (a tile that one run covers, into
 // a slot of its own) and tc_fixup_kernel, launched behind the GEMM, finishes
 // every tile with one CTA per 16-column chunk (same k-order sum, same
-// epilogue), so no CTA holds a whole tile's epilogue past its last MMA.  The LM head keeps, per
+// epilogue), so no CTA holds a whole tile's epilogue past its last MMA; two
+// 256-row parts of a projection run as one launch of tc_pair_kernel, which
+// feeds each weight k-block to the MMAs of both.  The LM head keeps, per
 // CTA, each token row's best (logit, index) and runner-up over the tiles the
 // CTA finishes; the last CTA merges one triple per CTA.
 #include <cudaTypedefs.h>
