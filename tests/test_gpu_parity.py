@@ -299,6 +299,40 @@ def test_rows_independent_of_batch(kind):
         assert torch.equal(a_, b_)
 
 
+@pytest.mark.parametrize("S", [25, 32])
+def test_rows_independent_of_batch_paired_launch(S):
+    """25 or 32 sequences of 16 rows (400 or 512 token rows) run every
+    projection as one paired launch of two 256-row parts (the second part
+    partly beyond the last row at 400) and one fixup; sequences from both
+    parts give bit-identical hidden states and K/V when run alone."""
+    w = small("bf16", d=64, block=16)
+    rows = 16
+    g = torch.Generator().manual_seed(11)
+    h0 = torch.randn(S * rows, w.target.hidden, generator=g)
+    eng, _, _ = G.setup(w, S=S, cap=128)
+    kc = torch.randn(S, *eng.caches.tk[1].shape[1:], generator=g).to(eng.caches.tk[1].dtype)
+    vc = torch.randn(S, *eng.caches.tv[1].shape[1:], generator=g).to(eng.caches.tv[1].dtype)
+    base = [(11 * s + 5) % 100 for s in range(S)]
+
+    def run(e, seqs):
+        n = len(seqs)
+        e.caches.tk[1].copy_(kc[seqs].cuda())
+        e.caches.tv[1].copy_(vc[seqs].cuda())
+        e.base_pos.copy_(torch.tensor([base[s] for s in seqs], dtype=torch.int32))
+        e.h[:n * rows].copy_(torch.cat([h0[s * rows:(s + 1) * rows] for s in seqs]).cuda())
+        D.dflash_decoder_layer_forward(e.target_layer_args(1, rows, e.h), e.ws_ptr, e.ws_bytes)
+        torch.cuda.synchronize()
+        assert e.status() == D.DFLASH_OK
+        return e.h[:n * rows].clone().cpu(), e.caches.tk[1][:n].clone().cpu(), e.caches.tv[1][:n].clone().cpu()
+
+    hb, kb, vb = run(eng, list(range(S)))
+    one, _, _ = G.setup(w, S=1, cap=128)
+    for s in (0, 15, 16, S - 1):  # both ends of both parts
+        ha, ka, va = run(one, [s])
+        assert torch.equal(ha, hb[s * rows:(s + 1) * rows]), s
+        assert torch.equal(ka[0], kb[s]) and torch.equal(va[0], vb[s]), s
+
+
 @pytest.mark.parametrize("kind", ["causal", "bidir"])
 def test_rows_independent_of_batch_three_launches(kind):
     """40 sequences of 16 rows (640 token rows) run every projection as three
