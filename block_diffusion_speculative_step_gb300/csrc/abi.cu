@@ -606,9 +606,10 @@ int dflash_workspace_control(void* ws, size_t ws_bytes, uint64_t wait_limit_ns, 
   DF_CHECK(ws != nullptr && ws_bytes >= kReservedBytes, "dflash_workspace_control: workspace below %zu bytes",
            kReservedBytes);
   DF_CHECK((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "dflash_workspace_control: workspace must be 256-byte aligned");
-  // bytes 8..15: the wait limit, 16..19: the stall switch (see wait_limit_ns)
+  DF_CHECK(stall_kv_loads >= 0 && stall_kv_loads <= 3, "dflash_workspace_control: stall switches are bits 0 and 1");
+  // bytes 8..15: the wait limit, 16..19: the stall switches (see wait_limit_ns)
   uint32_t ctl[4] = {(uint32_t)(wait_limit_ns & 0xffffffffu), (uint32_t)(wait_limit_ns >> 32),
-                     stall_kv_loads ? 1u : 0u, 0u};
+                     (uint32_t)stall_kv_loads, 0u};
   DF_CUDA(cudaMemcpyAsync(static_cast<char*>(ws) + 8, ctl, sizeof(ctl), cudaMemcpyHostToDevice,
                           (cudaStream_t)stream));
   return DFLASH_OK;

@@ -159,8 +159,13 @@ __device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* status) {
   return v != 0 ? v : kDefaultWaitNs;
 }
 
+// Test switches (bits of the workspace's stall word): bit 0, the attention
+// kernels issue no K/V copy; bit 1, the paired GEMM issues no weight copy.
 __device__ __forceinline__ bool stall_kv_loads(const uint32_t* status) {
-  return status != nullptr && *reinterpret_cast<const volatile uint32_t*>(status + 4) != 0u;
+  return status != nullptr && (*reinterpret_cast<const volatile uint32_t*>(status + 4) & 1u) != 0u;
+}
+__device__ __forceinline__ bool stall_weight_loads(const uint32_t* status) {
+  return status != nullptr && (*reinterpret_cast<const volatile uint32_t*>(status + 4) & 2u) != 0u;
 }
 
 }  // namespace dfl

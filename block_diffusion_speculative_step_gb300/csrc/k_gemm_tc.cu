@@ -885,6 +885,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
       const uint64_t pol_w = tc::policy_evict_first();
       const uint64_t pol_x = tc::policy_evict_last();
       const bool swiglu = L.kind == EPI_SWIGLU;
+      const bool stall = stall_weight_loads(L.status);  // test switch: issue no weight copy
       const int tps = L.tps, inter = L.inter, row0 = L.row0;
       int t = (int)(p0 / nkb), kb = (int)(p0 - (long long)t * nkb);  // position of the next W load
       int kb_x = kb;                                                   // k-block of the next X load
@@ -892,16 +893,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
         uint8_t* a = smem + (i % kPairW) * PairCfg::WB;
         uint64_t* bar = &wfull[i % kPairW];
         const int kx = kb * 64, seg = t / tps, tile = t - seg * tps;
+        if (++kb == nkb) {
+          kb = 0;
+          ++t;
+        }
+        if (stall) return;
         tc::mbar_arrive_expect_tx(bar, PairCfg::WB);
         if (swiglu) {
           tc::tma_load_2d(a, wmaps + seg, kx, tile * 64, bar, pol_w);
           tc::tma_load_2d(a + kTcA / 2, wmaps + seg, kx, inter + tile * 64, bar, pol_w);
         } else {
           tc::tma_load_2d(a, wmaps + seg, kx, row0 + tile * 128, bar, pol_w);
-        }
-        if (++kb == nkb) {
-          kb = 0;
-          ++t;
         }
       };
       auto load_x = [&](int i) {  // both 256-row halves of k-block i
@@ -943,7 +945,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_pair_kernel(const __grid_con
         }
       }
       // every issued copy has landed before this CTA's shared memory goes away
-      for (int i = (iw > kPairW ? iw - kPairW : 0); i < iw; ++i)
+      for (int i = (iw > kPairW ? iw - kPairW : 0); i < iw && !stall; ++i)
         tc::mbar_wait(&wfull[i % kPairW], (uint32_t)(i / kPairW) & 1u, nullptr, lim);
       for (int u = (2 * ix > kPairX ? 2 * ix - kPairX : 0); u < 2 * ix; ++u)
         tc::mbar_wait(&xfull[u % kPairX], (uint32_t)(u / kPairX) & 1u, nullptr, lim);

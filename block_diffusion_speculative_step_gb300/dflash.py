@@ -207,7 +207,8 @@ def dflash_workspace_init(ws_ptr: int, ws_bytes: int, stream=None):
 
 def dflash_workspace_control(ws_ptr: int, ws_bytes: int, wait_limit_ns: int = 0, stall_kv_loads: bool = False,
                              stream=None):
-    _check(lib().dflash_workspace_control(ws_ptr, ws_bytes, wait_limit_ns, 1 if stall_kv_loads else 0,
+    # stall_kv_loads: True / 1 stalls the attention's K/V copies, 2 the paired GEMM's weight copies
+    _check(lib().dflash_workspace_control(ws_ptr, ws_bytes, wait_limit_ns, int(stall_kv_loads),
                                           _stream(stream)))
 
 

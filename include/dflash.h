@@ -480,10 +480,12 @@ int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
  *    pipeline stage of another warp) spins before the kernel gives up,
  *    raises DFLASH_ERR_TIMEOUT in the status word and unwinds, keeping the
  *    GPU context usable.  0 selects the default, 1 s.
- *  - stall_kv_loads: nonzero makes the attention kernels issue none of their
- *    K/V copies, so that their waits expire with nothing in flight -- the
- *    way to test the timeout path without a GPU fault.  Its outputs are then
- *    meaningless.  Keep it 0 in use.
+ *  - stall_kv_loads: test switches, bits: 1 makes the attention kernels issue
+ *    none of their K/V copies, 2 makes the paired GEMM launch (two 256-row
+ *    parts of a projection) issue none of its weight copies, so that their
+ *    waits expire with nothing in flight -- the way to test the timeout path
+ *    without a GPU fault.  Outputs are then meaningless.  Other bits are
+ *    DFLASH_ERR_INVALID_ARG.  Keep it 0 in use.
  * The controls are copied with cudaMemcpyAsync on `stream` from host memory
  * (not inside a stream capture).  A workspace used by
  * dflash_verify_accept_noalloc has its controls reset by every such call.

@@ -92,3 +92,37 @@ def test_nan_hidden_state_raises_numeric():
     x = O.final_norm(om.target.cfg, h.double().numpy(), om.target.g_final)
     am, mg, _ = O.lm_head_argmax(om.target.cfg, om.Wlm, x)
     G.check_argmax(eng.argmax.cpu().numpy().ravel(), am, mg)
+
+
+def test_paired_gemm_weight_stall_times_out_and_recovers():
+    """512 token rows run each projection as one paired launch; with its
+    weight copies switched off (stall bit 2) the MMAs' waits expire, the call
+    reports DFLASH_ERR_TIMEOUT, and the same workspace then gives the bits of
+    a clean run."""
+    w = Hh.small_workload("bf16", H=256, nq=4, nkv=2, d=64, I=384, V=1000, t_layers=1, d_layers=1,
+                          taps=(0, 0), block=16)
+    S, rows = 32, 16
+    eng, _, _ = G.setup(w, S=S, cap=128)
+    g = torch.Generator().manual_seed(9)
+    kc = torch.randn(eng.caches.tk[0].shape, generator=g).to(eng.caches.tk[0].dtype)
+    vc = torch.randn(eng.caches.tv[0].shape, generator=g).to(eng.caches.tv[0].dtype)
+    base = [(13 * s + 7) % 100 for s in range(S)]
+    h0 = torch.randn(S * rows, w.target.hidden, generator=g)
+
+    def run():
+        eng.caches.tk[0].copy_(kc.cuda())
+        eng.caches.tv[0].copy_(vc.cuda())
+        st = _run_layer(eng, S, rows, base, h0)
+        return st, eng.h[:S * rows].clone().cpu()
+
+    st, ref = run()
+    assert st == D.DFLASH_OK
+    D.dflash_workspace_control(eng.ws_ptr, eng.ws_bytes, wait_limit_ns=2_000_000, stall_kv_loads=2)
+    t0 = time.perf_counter()
+    st, _ = run()
+    assert st == D.DFLASH_ERR_TIMEOUT, st
+    assert time.perf_counter() - t0 < 5.0
+    D.dflash_workspace_control(eng.ws_ptr, eng.ws_bytes)
+    st, again = run()
+    assert st == D.DFLASH_OK
+    assert torch.equal(again, ref)
